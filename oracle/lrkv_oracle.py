@@ -1,0 +1,278 @@
+"""Plain fp64 CPU oracle for Low-Rank Key-Value attention (LRKV).
+
+TEST INFRASTRUCTURE.  Only the tests, the package smoke check and the bench's
+CPU-baseline leg may import this module.  It shares no code with the CUDA
+library: it never imports the package, its binding or its kernels.
+
+Sources, cited by page title and section:
+  * "Low-Rank Key Value Attention：中文研读笔记" (reading notes, below "notes"):
+    §2.1 Eqs. (2)-(5) factorisation; §2.3 decode-time cache rows; §2.4 Eqs.
+    (6)-(7) associative logits/values; §2.5 Eqs. (8)-(9) cache accounting;
+    §2.6 Eq. (10) K/V parameter count.
+  * "Low-Rank Key Value Attention | What a shared cache can preserve"
+    (technical review, below "review"): §2 attention definition with the
+    causal mask; §3 Algorithm 1 (construct the factored cache), Algorithm 2
+    (decode against the factored history) and the hand calculation; §4 cache
+    ceiling, 2.5B byte example, TP replication.
+
+What it computes is the plain definition: each head's full K_h and V_h are
+rebuilt explicitly as K_h = S_K + R_h^K (B_h^K)^T (notes §2.1; review §3), and
+then textbook masked softmax attention runs on them (review §2).  The method is
+exact in real arithmetic (notes §2.4 closing remark; review §3 Algorithm 2
+preamble), so the result of the factored computation must equal this one up to
+rounding order.  Inputs are promoted exactly to float64 (bf16 and fp32 are
+exactly representable).
+
+Readings where the pages leave a step open:
+  * scale: one 1/sqrt(d_h) for the summed logit (review §3, "Associative
+    decode"); never sqrt(r).
+  * one softmax over the summed logits, never two normalised branches (review
+    §2 example with logits (2,0) and (0,2)).
+  * decode visibility: the new token is appended before attending, so the
+    visible history of sequence b is rows [0, seq_lens[b]) (notes §2.4
+    pseudocode appends first).
+  * prefill: query i of q_len sits at absolute position seq_lens[b]-q_len+i
+    and sees keys j <= that position (bottom-right causal alignment; the pages
+    only say "causal").
+  * an empty history (seq_lens[b] == 0) gives out = 0 and lse = -inf.
+  * no RoPE and no post-projection RMSNorm (notes §2.7; review §8).
+  * lse is the natural-log log-sum-exp of the scaled, masked logits.
+"""
+from __future__ import annotations
+
+import math
+from typing import Iterable, Optional, Sequence, Tuple
+
+import numpy as np
+
+
+def _f64(a) -> np.ndarray:
+    """Exact promotion of a torch tensor or array (fp32 / bf16) to float64."""
+    if hasattr(a, "detach"):
+        a = a.detach().cpu()
+        import torch  # local: only for dtype promotion of torch inputs
+        a = a.to(torch.float64).numpy()
+    return np.asarray(a, dtype=np.float64)
+
+
+def default_scale(head_dim: int) -> float:
+    """1/sqrt(d_h): the summed score stands for the full-width dot product
+    (review §3, "Associative decode")."""
+    return 1.0 / math.sqrt(head_dim)
+
+
+# --------------------------------------------------------------------------
+# Factorisation and cache construction
+# --------------------------------------------------------------------------
+
+def reconstruct_head(shared: np.ndarray, latent_h: np.ndarray, basis_h: np.ndarray) -> np.ndarray:
+    """Materialise one head's keys (or values): K_h = S + R_h B_h^T.
+
+    notes §2.1 Eqs. (2)-(5); review §3 "From a weight factorization to token
+    coordinates".  shared [L, d_h], latent_h [L, r], basis_h [d_h, r].
+    """
+    return shared + latent_h @ basis_h.T
+
+
+def append_reference(x, w_sk, w_sv, u_k, u_v, heads: int) -> Tuple[np.ndarray, ...]:
+    """Factored cache rows for new token activations (review §3 Algorithm 1;
+    notes §2.3): S_K = X W_sK, S_V = X W_sV once, and per head
+    R_K[h] = X U_K[h], R_V[h] = X U_V[h], all at the tokens' own indices.
+
+    x [B, T, d]; w_sk, w_sv [d, d_h]; u_k, u_v [d, H*r] with head h in
+    columns [h*r, (h+1)*r).  Returns k_s, v_s [B, T, d_h], z_k, z_v [B, T, H, r].
+    """
+    x = _f64(x)
+    B, T, d = x.shape
+    w_sk, w_sv, u_k, u_v = (_f64(a) for a in (w_sk, w_sv, u_k, u_v))
+    r = u_k.shape[1] // heads
+    k_s = x @ w_sk
+    v_s = x @ w_sv
+    z_k = (x @ u_k).reshape(B, T, heads, r)
+    z_v = (x @ u_v).reshape(B, T, heads, r)
+    return k_s, v_s, z_k, z_v
+
+
+def effective_projection(w_s, u, basis, h: int) -> np.ndarray:
+    """W_h = W_shared + U_h B_h^T (notes §2.1 Eq. (2)); used only to pin the
+    append path against the un-factored projection."""
+    w_s, u, basis = _f64(w_s), _f64(u), _f64(basis)
+    r = basis.shape[2]
+    return w_s + u[:, h * r:(h + 1) * r] @ basis[h].T
+
+
+# --------------------------------------------------------------------------
+# Attention on the reconstructed heads (the definition)
+# --------------------------------------------------------------------------
+
+def _softmax_attend(s: np.ndarray, V: np.ndarray) -> Tuple[np.ndarray, float]:
+    """Textbook softmax over the visible logits s [L] and weighted sum of V
+    rows (review §2).  Returns (o [d_h], lse)."""
+    m = np.max(s)
+    w = np.exp(s - m)
+    l = np.sum(w)
+    return (w @ V) / l, float(m + math.log(l))
+
+
+def decode_reference(q, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens, scale: Optional[float] = None,
+                     pairs: Optional[Iterable[Tuple[int, int]]] = None):
+    """One decode step for every (sequence b, head h), or only for `pairs`.
+
+    For each pair: rebuild K_h, V_h over rows [0, seq_lens[b]), form
+    s_j = scale * q_h . K_h[j], softmax, o = sum_j a_j V_h[j] (review §3
+    Algorithm 2 semantics, computed by the explicit expansion).
+    Returns out [B, H, d_h] and lse [B, H] (float64); pairs not computed are NaN.
+    """
+    q, k_s, v_s, z_k, z_v, b_k, b_v = (_f64(a) for a in (q, k_s, v_s, z_k, z_v, b_k, b_v))
+    lens = np.asarray(_f64(seq_lens), dtype=np.int64)
+    B, H, dh = q.shape
+    if scale is None:
+        scale = default_scale(dh)
+    out = np.full((B, H, dh), np.nan)
+    lse = np.full((B, H), np.nan)
+    todo = pairs if pairs is not None else [(b, h) for b in range(B) for h in range(H)]
+    for b, h in todo:
+        L = int(lens[b])
+        if L == 0:
+            out[b, h] = 0.0
+            lse[b, h] = -np.inf
+            continue
+        K = reconstruct_head(k_s[b, :L], z_k[b, :L, h, :], b_k[h])
+        V = reconstruct_head(v_s[b, :L], z_v[b, :L, h, :], b_v[h])
+        s = scale * (K @ q[b, h])
+        out[b, h], lse[b, h] = _softmax_attend(s, V)
+    return out, lse
+
+
+def prefill_reference(q, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens, scale: Optional[float] = None,
+                      pairs: Optional[Iterable[Tuple[int, int]]] = None,
+                      rows: Optional[Sequence[int]] = None):
+    """Causal attention of q_len queries per sequence against the factored cache.
+
+    q [B, q_len, H, d_h].  Query i of sequence b sits at absolute position
+    p_i = seq_lens[b] - q_len + i and sees keys j <= p_i (causal mask of
+    review §2; bottom-right alignment).  `rows` restricts the query indices
+    computed.  Returns out [B, q_len, H, d_h] and lse [B, H, q_len]; entries
+    not computed are NaN.
+    """
+    q, k_s, v_s, z_k, z_v, b_k, b_v = (_f64(a) for a in (q, k_s, v_s, z_k, z_v, b_k, b_v))
+    lens = np.asarray(_f64(seq_lens), dtype=np.int64)
+    B, Tq, H, dh = q.shape
+    if scale is None:
+        scale = default_scale(dh)
+    out = np.full((B, Tq, H, dh), np.nan)
+    lse = np.full((B, H, Tq), np.nan)
+    todo = pairs if pairs is not None else [(b, h) for b in range(B) for h in range(H)]
+    qi = list(range(Tq)) if rows is None else list(rows)
+    for b, h in todo:
+        L = int(lens[b])
+        if L < Tq:
+            raise ValueError("prefill needs seq_lens[b] >= q_len (queries are part of the history)")
+        K = reconstruct_head(k_s[b, :L], z_k[b, :L, h, :], b_k[h])
+        V = reconstruct_head(v_s[b, :L], z_v[b, :L, h, :], b_v[h])
+        for i in qi:
+            p = L - Tq + i
+            s = scale * (K[: p + 1] @ q[b, i, h])
+            out[b, i, h], lse[b, h, i] = _softmax_attend(s, V[: p + 1])
+    return out, lse
+
+
+# --------------------------------------------------------------------------
+# Second CPU path, used only to pin the definition above: the associative
+# (factored) form of notes §2.4 Eqs. (6)-(7) / review §3 Algorithm 2.
+# --------------------------------------------------------------------------
+
+def decode_factored(q, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens, scale: Optional[float] = None):
+    """Algorithm 2 of the review in its own order, in fp64, never rebuilding
+    K_h or V_h: p = q B_K[h]; score_j = q.S_K[j] + p.R_K[h,j]; scale; one
+    softmax; reduce S_V and R_V[h] with the same weights; map the private
+    reduction through B_V[h]^T; add."""
+    q, k_s, v_s, z_k, z_v, b_k, b_v = (_f64(a) for a in (q, k_s, v_s, z_k, z_v, b_k, b_v))
+    lens = np.asarray(_f64(seq_lens), dtype=np.int64)
+    B, H, dh = q.shape
+    if scale is None:
+        scale = default_scale(dh)
+    out = np.zeros((B, H, dh))
+    lse = np.full((B, H), -np.inf)
+    for b in range(B):
+        L = int(lens[b])
+        if L == 0:
+            continue
+        for h in range(H):
+            p = q[b, h] @ b_k[h]                                   # step 02
+            score = k_s[b, :L] @ q[b, h] + z_k[b, :L, h, :] @ p    # steps 03-04
+            score = score * scale                                  # step 05
+            m = np.max(score)
+            w = np.exp(score - m)
+            l = np.sum(w)
+            a = w / l                                              # step 06
+            shared = a @ v_s[b, :L]                                # step 07
+            private = a @ z_v[b, :L, h, :]
+            out[b, h] = shared + private @ b_v[h].T                # steps 08-09
+            lse[b, h] = m + math.log(l)
+    return out, lse
+
+
+# --------------------------------------------------------------------------
+# Cache and parameter accounting (notes §2.5-2.6; review §4)
+# --------------------------------------------------------------------------
+
+def cache_elems_per_token(heads: int, head_dim: int, rank: int) -> int:
+    """Elements one token adds per layer: 2(d_h + H r) (notes §2.5 Eq. (8))."""
+    return 2 * (head_dim + heads * rank)
+
+
+def mha_elems_per_token(heads: int, head_dim: int) -> int:
+    """Dense MHA: 2 H d_h per token per layer (notes §1 table)."""
+    return 2 * heads * head_dim
+
+
+def cache_fraction(heads: int, head_dim: int, rank: int) -> float:
+    """rho = 1/H + r/d_h, the remaining fraction of the MHA cache
+    (notes §2.5 Eq. (9))."""
+    return 1.0 / heads + rank / head_dim
+
+
+def cache_bytes(elem_bytes: int, layers: int, batch: int, length: int, heads: int,
+                head_dim: int, rank: int) -> int:
+    """2 s N b L (d_h + H r) bytes (notes §2.5; review §4 M_LRKV)."""
+    return 2 * elem_bytes * layers * batch * length * (head_dim + heads * rank)
+
+
+def mha_cache_bytes(elem_bytes: int, layers: int, batch: int, length: int, heads: int,
+                    head_dim: int) -> int:
+    """2 b N B T H d_h (review §2 "Where the bytes go")."""
+    return 2 * elem_bytes * layers * batch * length * heads * head_dim
+
+
+def rank_ceiling(head_dim: int, heads: int, target_fraction: float) -> int:
+    """Largest rank within a cache budget c: floor(d_h (c - 1/H)) (review §4)."""
+    return int(math.floor(head_dim * (target_fraction - 1.0 / heads) + 1e-12))
+
+
+def saves_cache(heads: int, head_dim: int, rank: int) -> bool:
+    """LRKV is smaller than MHA only if r < d_h (1 - 1/H) (notes §2.5)."""
+    return rank < head_dim * (1.0 - 1.0 / heads)
+
+
+def tp_replicated_fraction(shards: int, heads: int, head_dim: int, rank: int) -> float:
+    """P/H + r/d_h when every tensor-parallel shard keeps its own copy of the
+    shared block (review §4 "Tensor parallelism can replicate the shared
+    block")."""
+    return shards / heads + rank / head_dim
+
+
+def kv_param_count(d_model: int, heads: int, head_dim: int, rank: int) -> int:
+    """2 d d_h + 2 H r (d + d_h) K/V projection weights (notes §2.6 Eq. (10))."""
+    return 2 * d_model * head_dim + 2 * heads * rank * (d_model + head_dim)
+
+
+def kv_param_fraction(d_model: int, heads: int, head_dim: int, rank: int) -> float:
+    """Ratio to MHA's 2 H d d_h K/V weights (notes §2.6; review §4)."""
+    return kv_param_count(d_model, heads, head_dim, rank) / (2 * heads * d_model * head_dim)
+
+
+def decode_flop_ratio(head_dim: int, rank: int, history: int) -> float:
+    """C_LRKV / C_MHA ~= 1 + r/d_h + r/T (review §4 "Weight count and the two
+    decode regimes")."""
+    return 1.0 + rank / head_dim + rank / history
