@@ -1,0 +1,110 @@
+// lrkv_api.cu — the extern "C" entry points declared in include/lrkv.h:
+// argument checks (host only, before anything touches the GPU), workspace
+// sizing, and dispatch to the kernels.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/lrkv.h"
+#include "decode_plan.h"
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Checks that need no GPU.  Returns LRKV_OK when `d` describes a shape the
+// decode kernels implement.
+lrkv_status check_decode_dims(const lrkv_dims* d) {
+  if (!d) return LRKV_ERR_INVALID_ARG;
+  if (d->batch < 1 || d->heads < 1 || d->head_dim < 1 || d->rank < 0 || d->max_len < 1)
+    return LRKV_ERR_INVALID_ARG;
+  if (d->dtype != LRKV_F32 && d->dtype != LRKV_BF16) return LRKV_ERR_INVALID_ARG;
+  if (!(d->scale == d->scale)) return LRKV_ERR_INVALID_ARG;  // NaN scale
+  const int esz = d->dtype == LRKV_BF16 ? 2 : 4;
+  if ((static_cast<long long>(d->head_dim) * esz) % 16 != 0) return LRKV_ERR_UNSUPPORTED;
+  if ((static_cast<long long>(d->heads) * d->rank * esz) % 16 != 0) return LRKV_ERR_UNSUPPORTED;
+  if (d->batch > lrkv::kMaxBatch || d->rank > lrkv::kMaxRank || d->head_dim > 256 || d->heads > 256)
+    return LRKV_ERR_UNSUPPORTED;
+  if (d->dtype == LRKV_BF16 && d->head_dim % 16 != 0) return LRKV_ERR_UNSUPPORTED;
+  if (static_cast<long long>(d->batch) * d->max_len > (1LL << 31) - 1) return LRKV_ERR_UNSUPPORTED;
+  return LRKV_OK;
+}
+
+lrkv_status current_sm_count(int* n) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return LRKV_ERR_CUDA;
+  if (cudaDeviceGetAttribute(n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return LRKV_ERR_CUDA;
+  return LRKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int lrkv_abi_version(void) { return LRKV_ABI_VERSION; }
+
+const char* lrkv_status_string(lrkv_status s) {
+  switch (s) {
+    case LRKV_OK: return "LRKV_OK";
+    case LRKV_ERR_INVALID_ARG: return "LRKV_ERR_INVALID_ARG";
+    case LRKV_ERR_UNSUPPORTED: return "LRKV_ERR_UNSUPPORTED";
+    case LRKV_ERR_WORKSPACE: return "LRKV_ERR_WORKSPACE";
+    case LRKV_ERR_CUDA: return "LRKV_ERR_CUDA";
+    case LRKV_ERR_TIMEOUT: return "LRKV_ERR_TIMEOUT";
+    case LRKV_ERR_DEVICE_BOUNDS: return "LRKV_ERR_DEVICE_BOUNDS";
+  }
+  return "LRKV_ERR_UNKNOWN";
+}
+
+size_t lrkv_cache_elems_per_token(int heads, int head_dim, int rank) {
+  if (heads < 0 || head_dim < 0 || rank < 0) return 0;
+  return 2 * (static_cast<size_t>(head_dim) + static_cast<size_t>(heads) * static_cast<size_t>(rank));
+}
+
+lrkv_status lrkv_decode_workspace_size(const lrkv_dims* dims, size_t* bytes) {
+  if (!bytes) return LRKV_ERR_INVALID_ARG;
+  lrkv_status st = check_decode_dims(dims);
+  if (st != LRKV_OK) return st;
+  int sms = 0;
+  if ((st = current_sm_count(&sms)) != LRKV_OK) return st;
+  lrkv::DecodePlan P;
+  return lrkv::decode_make_plan(*dims, sms, P, bytes);
+}
+
+lrkv_status lrkv_decode(const lrkv_dims* dims, const void* q, const void* k_s, const void* v_s,
+                        const void* z_k, const void* z_v, const void* b_k, const void* b_v,
+                        const int32_t* seq_lens, float* out, float* lse, void* ws, size_t ws_bytes,
+                        lrkv_stream_t stream) {
+  lrkv_status st = check_decode_dims(dims);
+  if (st != LRKV_OK) return st;
+  if (!q || !k_s || !v_s || !seq_lens || !out) return LRKV_ERR_INVALID_ARG;
+  if (dims->rank > 0 && (!z_k || !z_v || !b_k || !b_v)) return LRKV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_s) || !aligned16(v_s)) return LRKV_ERR_INVALID_ARG;
+  if (dims->rank > 0 && (!aligned16(z_k) || !aligned16(z_v))) return LRKV_ERR_INVALID_ARG;
+  if (!ws) return LRKV_ERR_WORKSPACE;
+  if (!aligned16(ws)) return LRKV_ERR_INVALID_ARG;
+  int sms = 0;
+  if ((st = current_sm_count(&sms)) != LRKV_OK) return st;
+  lrkv::DecodePlan P;
+  size_t need = 0;
+  if ((st = lrkv::decode_make_plan(*dims, sms, P, &need)) != LRKV_OK) return st;
+  if (ws_bytes < need) return LRKV_ERR_WORKSPACE;
+  lrkv::decode_bind_workspace(P, ws);
+  P.q = q; P.k_s = k_s; P.v_s = v_s; P.z_k = z_k; P.z_v = z_v; P.b_k = b_k; P.b_v = b_v;
+  P.seq_lens = seq_lens; P.out = out; P.lse = lse;
+  return lrkv::decode_launch(P, stream);
+}
+
+lrkv_status lrkv_read_device_status(const void* ws, lrkv_stream_t stream, lrkv_status* out_status) {
+  if (!ws || !out_status) return LRKV_ERR_INVALID_ARG;
+  uint32_t word = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&word, ws, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess) return LRKV_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return LRKV_ERR_CUDA;
+  *out_status = (word & lrkv::kDevTimeout) ? LRKV_ERR_TIMEOUT
+                : (word & lrkv::kDevBounds) ? LRKV_ERR_DEVICE_BOUNDS
+                                               : LRKV_OK;
+  return LRKV_OK;
+}
+
+}  // extern "C"

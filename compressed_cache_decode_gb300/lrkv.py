@@ -1,0 +1,181 @@
+"""ctypes binding of the LRKV C ABI (include/lrkv.h).
+
+Argument marshalling only: every step of the attention path runs in the CUDA
+kernels of `liblrkv.so`.  PyTorch is used for device memory and streams.  The
+library is loaded on first use; if it has not been built, loading raises
+(there is no CPU fallback).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "liblrkv.so")
+
+LRKV_OK = 0
+LRKV_ERR_INVALID_ARG = 1
+LRKV_ERR_UNSUPPORTED = 2
+LRKV_ERR_WORKSPACE = 3
+LRKV_ERR_CUDA = 4
+LRKV_ERR_TIMEOUT = 5
+LRKV_ERR_DEVICE_BOUNDS = 6
+
+LRKV_F32 = 0
+LRKV_BF16 = 1
+
+# Every symbol include/lrkv.h declares (checked by the ABI test).
+EXPORTED = (
+    "lrkv_abi_version",
+    "lrkv_status_string",
+    "lrkv_cache_elems_per_token",
+    "lrkv_decode_workspace_size",
+    "lrkv_decode",
+    "lrkv_read_device_status",
+)
+
+
+class lrkv_dims(ctypes.Structure):
+    _fields_ = [
+        ("batch", ctypes.c_int),
+        ("heads", ctypes.c_int),
+        ("head_dim", ctypes.c_int),
+        ("rank", ctypes.c_int),
+        ("max_len", ctypes.c_int),
+        ("dtype", ctypes.c_int),
+        ("scale", ctypes.c_float),
+    ]
+
+
+class LRKVError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+
+
+_lib = None
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load liblrkv.so (once).  Raises FileNotFoundError if it is missing."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise FileNotFoundError(
+            f"{p} is missing: build it with `python -m compressed_cache_decode_gb300.build` "
+            "(the LRKV path has no CPU fallback)")
+    lib = ctypes.CDLL(p)
+    vp, sz, i32p = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p
+    dims_p = ctypes.POINTER(lrkv_dims)
+    lib.lrkv_abi_version.restype = ctypes.c_int
+    lib.lrkv_abi_version.argtypes = []
+    lib.lrkv_status_string.restype = ctypes.c_char_p
+    lib.lrkv_status_string.argtypes = [ctypes.c_int]
+    lib.lrkv_cache_elems_per_token.restype = sz
+    lib.lrkv_cache_elems_per_token.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    lib.lrkv_decode_workspace_size.restype = ctypes.c_int
+    lib.lrkv_decode_workspace_size.argtypes = [dims_p, ctypes.POINTER(sz)]
+    lib.lrkv_decode.restype = ctypes.c_int
+    lib.lrkv_decode.argtypes = [dims_p, vp, vp, vp, vp, vp, vp, vp, i32p, vp, vp, vp, sz, vp]
+    lib.lrkv_read_device_status.restype = ctypes.c_int
+    lib.lrkv_read_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().lrkv_status_string(int(status)).decode()
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream_handle(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def make_dims(batch: int, heads: int, head_dim: int, rank: int, max_len: int, dtype,
+              scale: float = 0.0) -> lrkv_dims:
+    if dtype in (torch.bfloat16, "bf16", LRKV_BF16):
+        dt = LRKV_BF16
+    elif dtype in (torch.float32, "f32", LRKV_F32):
+        dt = LRKV_F32
+    else:
+        dt = int(dtype) if isinstance(dtype, int) else -1
+    return lrkv_dims(batch, heads, head_dim, rank, max_len, dt, float(scale))
+
+
+# ------------------------------------------------------- raw ABI wrappers --
+
+def lrkv_cache_elems_per_token(heads: int, head_dim: int, rank: int) -> int:
+    return int(load().lrkv_cache_elems_per_token(heads, head_dim, rank))
+
+
+def lrkv_decode_workspace_size(dims: lrkv_dims) -> int:
+    n = ctypes.c_size_t(0)
+    st = load().lrkv_decode_workspace_size(ctypes.byref(dims), ctypes.byref(n))
+    if st != LRKV_OK:
+        raise LRKVError(st, "lrkv_decode_workspace_size")
+    return int(n.value)
+
+
+def lrkv_decode(dims: lrkv_dims, q, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens, out, lse, ws,
+                ws_bytes: int, stream=None) -> int:
+    """Direct call of the C entry point; returns its status code."""
+    return int(load().lrkv_decode(ctypes.byref(dims), _ptr(q), _ptr(k_s), _ptr(v_s), _ptr(z_k),
+                                  _ptr(z_v), _ptr(b_k), _ptr(b_v), _ptr(seq_lens), _ptr(out),
+                                  _ptr(lse), _ptr(ws), ws_bytes, _stream_handle(stream)))
+
+
+def lrkv_read_device_status(ws: torch.Tensor, stream=None) -> int:
+    out = ctypes.c_int(0)
+    st = load().lrkv_read_device_status(_ptr(ws), _stream_handle(stream), ctypes.byref(out))
+    if st != LRKV_OK:
+        raise LRKVError(st, "lrkv_read_device_status")
+    return int(out.value)
+
+
+# ------------------------------------------------------- tensor front end --
+
+def decode_workspace(dims: lrkv_dims, device) -> torch.Tensor:
+    n = lrkv_decode_workspace_size(dims)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def decode(q: torch.Tensor, k_s: torch.Tensor, v_s: torch.Tensor, z_k: torch.Tensor,
+           z_v: torch.Tensor, b_k: torch.Tensor, b_v: torch.Tensor, seq_lens: torch.Tensor,
+           scale: float = 0.0, out: Optional[torch.Tensor] = None,
+           lse: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
+           stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """One decode step on device tensors in the layouts of include/lrkv.h.
+    Allocates out/lse/workspace with torch when not given."""
+    B, H, dh = q.shape
+    max_len = k_s.shape[1]
+    r = z_k.shape[-1] if z_k is not None else 0
+    dims = make_dims(B, H, dh, r, max_len, q.dtype, scale)
+    if out is None:
+        out = torch.empty((B, H, dh), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = decode_workspace(dims, q.device)
+    for t in (q, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens):
+        if t is not None and not t.is_contiguous():
+            raise ValueError("LRKV tensors must be contiguous")
+    if seq_lens.dtype != torch.int32:
+        raise ValueError("seq_lens must be int32")
+    st = lrkv_decode(dims, q, k_s, v_s, z_k if r > 0 else None, z_v if r > 0 else None,
+                     b_k if r > 0 else None, b_v if r > 0 else None, seq_lens, out, lse, ws,
+                     ws.numel(), stream)
+    if st != LRKV_OK:
+        raise LRKVError(st, "lrkv_decode")
+    return out, lse

@@ -1,0 +1,141 @@
+/*
+ * lrkv.h — C ABI of the GB300 (sm_103a) LRKV factored-cache attention library.
+ *
+ * Low-Rank Key-Value attention writes each head's key/value projection as a
+ * shared dense matrix plus a per-head rank-r residual, W_h = W_s + U_h B_h^T
+ * ("Low-Rank Key Value Attention：中文研读笔记", §2.1, Eqs. (2)-(5)).  A token
+ * therefore caches one shared row k_s, v_s (d_h each) plus per-head latents
+ * z_k,h = x U_h^K and z_v,h = x U_h^V (r each) (same page, §2.3), and attention
+ * runs directly on that factored cache by associativity (same page, §2.4,
+ * Eqs. (6)-(7); "Low-Rank Key Value Attention | What a shared cache can
+ * preserve", §3, Algorithm 2):
+ *
+ *   score_{h,j} = (q_h . k_s,j + (q_h B_h^K) . z_k,h,j) / sqrt(d_h)
+ *   a_h        = softmax over the visible j of the summed scores (ONE softmax)
+ *   o_h        = sum_j a_{h,j} v_s,j + (sum_j a_{h,j} z_v,h,j) (B_h^V)^T
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  * Memory.  Every pointer argument except `dims`, `bytes` and `out_status`
+ *    is a DEVICE pointer on the current CUDA device.  The caller owns and
+ *    allocates every buffer, including the workspace; the library allocates
+ *    nothing and keeps no state between calls.  All work is enqueued on
+ *    `stream` (a cudaStream_t passed as void*; NULL is the legacy default
+ *    stream) and the calls return without synchronising.
+ *  * Element types.  `dims->dtype` fixes the storage type of q, the cache
+ *    (k_s, v_s, z_k, z_v), the bases (b_k, b_v) and the append inputs:
+ *    LRKV_F32 (IEEE binary32) or LRKV_BF16 (bfloat16).  Accumulation is fp32.
+ *    Outputs `out` and `lse` are always fp32.
+ *  * Layouts (row-major, C order):
+ *      k_s, v_s   [batch][max_len][head_dim]
+ *      z_k, z_v   [batch][max_len][heads][rank]
+ *      b_k, b_v   [heads][head_dim][rank]       (B_h is d_h x r; K_h = S + R_h B_h^T)
+ *      seq_lens   [batch] int32, visible history length of each sequence
+ *  * Alignment.  Cache pointers, q, x and the append weights must be 16-byte
+ *    aligned, and head_dim*sizeof(elem) and heads*rank*sizeof(elem) must be
+ *    multiples of 16 bytes (every row is moved by the Tensor Memory
+ *    Accelerator, which copies 16-byte-aligned spans).
+ *  * Errors.  Arguments are checked on the host before anything is enqueued;
+ *    a failed check returns a status and enqueues nothing.  A CUDA launch
+ *    failure returns LRKV_ERR_CUDA.  Problems only the device can see (a
+ *    seq_lens entry outside [0, max_len], a bounded wait that ran out) never
+ *    trap: the kernels clamp, finish, and record the status in the workspace,
+ *    readable with lrkv_read_device_status().
+ *  * Scale.  dims->scale <= 0 selects 1/sqrt(head_dim), the scale of the
+ *    summed score (technical review, §3 "Associative decode").
+ */
+#ifndef LRKV_H_
+#define LRKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LRKV_ABI_VERSION 1
+
+typedef enum {
+  LRKV_OK = 0,
+  LRKV_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, bad dtype          */
+  LRKV_ERR_UNSUPPORTED = 2,   /* valid but outside the shapes the kernels implement */
+  LRKV_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required          */
+  LRKV_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed         */
+  LRKV_ERR_TIMEOUT = 5,       /* device: a bounded wait ran out (reported, not trapped) */
+  LRKV_ERR_DEVICE_BOUNDS = 6  /* device: seq_lens/start_pos outside [0, max_len]; clamped */
+} lrkv_status;
+
+typedef enum { LRKV_F32 = 0, LRKV_BF16 = 1 } lrkv_dtype;
+
+typedef struct {
+  int batch;       /* B >= 1                                                  */
+  int heads;       /* H >= 1                                                  */
+  int head_dim;    /* d_h >= 1                                                */
+  int rank;        /* r >= 0; r = 0 is MQA-style sharing (notes §2.1)         */
+  int max_len;     /* token capacity of each sequence's cache rows            */
+  lrkv_dtype dtype;
+  float scale;     /* <= 0 selects 1/sqrt(head_dim)                           */
+} lrkv_dims;
+
+typedef void* lrkv_stream_t; /* a cudaStream_t */
+
+/* ABI version of the loaded library (LRKV_ABI_VERSION). */
+int lrkv_abi_version(void);
+
+/* Human-readable name of a status code; never NULL. */
+const char* lrkv_status_string(lrkv_status status);
+
+/* Cache elements one token adds per layer: 2 (d_h + H r)
+ * ("Low-Rank Key Value Attention：中文研读笔记", §2.5, Eq. (8)).
+ * Returns 0 if any argument is negative. */
+size_t lrkv_cache_elems_per_token(int heads, int head_dim, int rank);
+
+/* Bytes of device workspace lrkv_decode needs for `dims` on the current
+ * device (the split-KV partials depend on its SM count).  The workspace may
+ * hold anything on entry; only its first 16 bytes (the device status word)
+ * keep meaning after a call. */
+lrkv_status lrkv_decode_workspace_size(const lrkv_dims* dims, size_t* bytes);
+
+/*
+ * One decode step of every head of every sequence against its factored
+ * history ("Low-Rank Key Value Attention | What a shared cache can preserve",
+ * §3, Algorithm 2, and the fused online-softmax paragraph after it;
+ * "Low-Rank Key Value Attention：中文研读笔记", §2.4, Eqs. (6)-(7)).
+ *
+ *   q        [batch][heads][head_dim]  query of the new token (dtype)
+ *   k_s, v_s, z_k, z_v                 the factored cache (layouts above); the
+ *                                       new token's rows must already be in it
+ *   b_k, b_v [heads][head_dim][rank]   reconstruction bases (dtype)
+ *   seq_lens [batch] int32             sequence b attends rows [0, seq_lens[b]);
+ *                                       0 gives out = 0 and lse = -inf
+ *   out      [batch][heads][head_dim]  fp32 result o_h (heads not concatenated,
+ *                                       no output projection)
+ *   lse      [batch][heads] fp32 or NULL: natural-log log-sum-exp of the scaled
+ *                                       scores
+ *   ws, ws_bytes                        workspace of at least
+ *                                       lrkv_decode_workspace_size() bytes
+ * z_k, z_v, b_k, b_v may be NULL when rank == 0.
+ * Supported: dtype BF16 with head_dim a multiple of 16 (<= 256) and rank <= 64,
+ * ceil(heads/16) * head_dim / 8 <= 32; dtype F32 with rank <= 64,
+ * head_dim <= 8 * (lanes per head); batch <= 4096.  Others return
+ * LRKV_ERR_UNSUPPORTED.
+ */
+lrkv_status lrkv_decode(const lrkv_dims* dims, const void* q, const void* k_s, const void* v_s,
+                        const void* z_k, const void* z_v, const void* b_k, const void* b_v,
+                        const int32_t* seq_lens, float* out, float* lse, void* ws, size_t ws_bytes,
+                        lrkv_stream_t stream);
+
+/*
+ * Read the device status word that the kernels of the last call(s) using
+ * `ws` recorded (LRKV_OK, LRKV_ERR_TIMEOUT or LRKV_ERR_DEVICE_BOUNDS).
+ * Synchronises `stream`.  Each lrkv_decode/lrkv_prefill call resets the word
+ * when it starts.
+ */
+lrkv_status lrkv_read_device_status(const void* ws, lrkv_stream_t stream, lrkv_status* out_status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LRKV_H_ */

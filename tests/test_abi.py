@@ -1,0 +1,107 @@
+"""The C-ABI library loads and exports every symbol include/lrkv.h declares,
+and its host-side checks reject bad arguments before touching a GPU.  No
+compute call is made here (these run without a GPU)."""
+import ctypes
+
+import pytest
+
+from _lib_util import ensure_built, header_symbols
+from compressed_cache_decode_gb300 import lrkv
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ensure_built()
+    return lrkv.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = header_symbols()
+    assert declared, "no declarations parsed"
+    for name in declared:
+        assert hasattr(lib, name), f"{name} declared in include/lrkv.h but not exported"
+    assert set(declared) == set(lrkv.EXPORTED), "binding and header disagree"
+
+
+def test_version_and_status_strings(lib):
+    assert lib.lrkv_abi_version() == 1
+    for code, name in [(0, "LRKV_OK"), (1, "LRKV_ERR_INVALID_ARG"), (2, "LRKV_ERR_UNSUPPORTED"),
+                       (3, "LRKV_ERR_WORKSPACE"), (4, "LRKV_ERR_CUDA"), (5, "LRKV_ERR_TIMEOUT"),
+                       (6, "LRKV_ERR_DEVICE_BOUNDS")]:
+        assert lrkv.status_string(code) == name
+    assert lrkv.status_string(99) == "LRKV_ERR_UNKNOWN"
+
+
+def test_cache_elems_per_token(lib):
+    # 2 (d_h + H r): 4608 -> 2236 at H=18, d_h=128, r=55 (reading notes §2.5)
+    assert lrkv.lrkv_cache_elems_per_token(18, 128, 55) == 2236
+    assert lrkv.lrkv_cache_elems_per_token(16, 64, 28) == 1024
+    assert lrkv.lrkv_cache_elems_per_token(4, 16, 0) == 32
+    assert lrkv.lrkv_cache_elems_per_token(-1, 16, 0) == 0
+
+
+def _call(dims, **kw):
+    args = dict(q=None, k_s=None, v_s=None, z_k=None, z_v=None, b_k=None, b_v=None,
+                seq_lens=None, out=None, lse=None, ws=None, ws_bytes=0)
+    args.update(kw)
+    lib = lrkv.load()
+    return lib.lrkv_decode(None if dims is None else ctypes.byref(dims), args["q"], args["k_s"],
+                           args["v_s"], args["z_k"], args["z_v"], args["b_k"], args["b_v"],
+                           args["seq_lens"], args["out"], args["lse"], args["ws"],
+                           args["ws_bytes"], None)
+
+
+FAKE = 1 << 20  # a 16-byte-aligned non-null address; never dereferenced on these paths
+
+
+def test_rejects_bad_dims_without_gpu(lib):
+    good = dict(q=FAKE, k_s=FAKE, v_s=FAKE, z_k=FAKE, z_v=FAKE, b_k=FAKE, b_v=FAKE,
+                seq_lens=FAKE, out=FAKE, ws=FAKE, ws_bytes=1 << 30)
+    assert _call(None, **good) == lrkv.LRKV_ERR_INVALID_ARG
+    for bad in [lrkv.make_dims(0, 16, 64, 28, 64, "bf16"), lrkv.make_dims(1, 0, 64, 28, 64, "bf16"),
+                lrkv.make_dims(1, 16, 0, 28, 64, "bf16"), lrkv.make_dims(1, 16, 64, -1, 64, "bf16"),
+                lrkv.make_dims(1, 16, 64, 28, 0, "bf16"), lrkv.make_dims(1, 16, 64, 28, 64, 7)]:
+        assert _call(bad, **good) == lrkv.LRKV_ERR_INVALID_ARG
+    nan_scale = lrkv.make_dims(1, 16, 64, 28, 64, "bf16", scale=float("nan"))
+    assert _call(nan_scale, **good) == lrkv.LRKV_ERR_INVALID_ARG
+
+
+def test_rejects_unsupported_shapes_without_gpu(lib):
+    good = dict(q=FAKE, k_s=FAKE, v_s=FAKE, z_k=FAKE, z_v=FAKE, b_k=FAKE, b_v=FAKE,
+                seq_lens=FAKE, out=FAKE, ws=FAKE, ws_bytes=1 << 30)
+    for dims in [lrkv.make_dims(1, 16, 60, 28, 64, "bf16"),     # row not a multiple of 16 B
+                 lrkv.make_dims(1, 6, 128, 46, 64, "bf16"),     # H*r*2 = 552 B
+                 lrkv.make_dims(1, 16, 64, 72, 64, "bf16"),     # rank above 64
+                 lrkv.make_dims(5000, 16, 64, 28, 64, "bf16"),  # batch above 4096
+                 lrkv.make_dims(1, 16, 24, 28, 64, "bf16")]:    # bf16 head_dim % 16
+        assert _call(dims, **good) == lrkv.LRKV_ERR_UNSUPPORTED
+
+
+def test_rejects_null_and_misaligned_pointers_without_gpu(lib):
+    dims = lrkv.make_dims(2, 16, 64, 28, 128, "bf16")
+    base = dict(q=FAKE, k_s=FAKE, v_s=FAKE, z_k=FAKE, z_v=FAKE, b_k=FAKE, b_v=FAKE,
+                seq_lens=FAKE, out=FAKE, ws=FAKE, ws_bytes=1 << 30)
+    for key in ["q", "k_s", "v_s", "z_k", "z_v", "b_k", "b_v", "seq_lens", "out"]:
+        args = dict(base)
+        args[key] = None
+        assert _call(dims, **args) == lrkv.LRKV_ERR_INVALID_ARG, key
+    for key in ["q", "k_s", "v_s", "z_k", "z_v"]:
+        args = dict(base)
+        args[key] = FAKE + 8
+        assert _call(dims, **args) == lrkv.LRKV_ERR_INVALID_ARG, key
+    args = dict(base)
+    args["ws"] = None
+    assert _call(dims, **args) == lrkv.LRKV_ERR_WORKSPACE
+    # rank 0 (MQA) needs no latents or bases
+    dims0 = lrkv.make_dims(2, 16, 64, 0, 128, "bf16")
+    args = dict(base, z_k=None, z_v=None, b_k=None, b_v=None, ws=None)
+    assert _call(dims0, **args) == lrkv.LRKV_ERR_WORKSPACE
+
+
+def test_workspace_size_checks_arguments(lib):
+    n = ctypes.c_size_t(0)
+    assert lib.lrkv_decode_workspace_size(None, ctypes.byref(n)) == lrkv.LRKV_ERR_INVALID_ARG
+    d = lrkv.make_dims(1, 16, 64, 28, 64, "bf16")
+    assert lib.lrkv_decode_workspace_size(ctypes.byref(d), None) == lrkv.LRKV_ERR_INVALID_ARG
+    bad = lrkv.make_dims(1, 16, 60, 28, 64, "bf16")
+    assert lib.lrkv_decode_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == lrkv.LRKV_ERR_UNSUPPORTED
