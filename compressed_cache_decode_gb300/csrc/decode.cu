@@ -448,8 +448,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) lrkv_decode_split_kernel(const
 
     // ---- scores: shared part (MMA warps) and private part (head lanes) ------
     if constexpr (BF16) {
-      if (warp < ltiles * P.ksplit) {
-        const int tile = warp % ltiles, kg = warp / ltiles;
+      for (int item = warp; item < ltiles * P.ksplit; item += nwarps) {
+        const int tile = item % ltiles, kg = item / ltiles;
         const int mi = tile / (T / 8), nj = tile % (T / 8);
         float d[4] = {0.f, 0.f, 0.f, 0.f};
         for (int kk = kg * kps; kk < (kg + 1) * kps; ++kk) {
@@ -466,6 +466,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) lrkv_decode_split_kernel(const
         sk[(row + 8) * T + col + 1] = d[3];
       }
     }
+    // this lane's tokens lt, lt + lph, ... ; only the first `nvi` hold rows
+    const int nvi = (nvalid > lt) ? min(ppt, (nvalid - lt + P.lph - 1) / P.lph) : 0;
     float sc[kMaxPPT];
     {
       float pr[kMaxPPT] = {0.f, 0.f, 0.f, 0.f};
@@ -474,10 +476,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) lrkv_decode_split_kernel(const
         const float* ph = p_sh + h * P.p_stride;
         const int tstride = P.lph * P.z_stride;
         switch (P.vec) {
-          case 8: if constexpr (BF16) private_logits<BF16, 8, RMAX>(z0, tstride, ppt, ph, r, pr); break;
-          case 4: private_logits<BF16, 4, RMAX>(z0, tstride, ppt, ph, r, pr); break;
-          case 2: private_logits<BF16, 2, RMAX>(z0, tstride, ppt, ph, r, pr); break;
-          default: private_logits<BF16, 1, RMAX>(z0, tstride, ppt, ph, r, pr); break;
+          case 8: if constexpr (BF16) private_logits<BF16, 8, RMAX>(z0, tstride, nvi, ph, r, pr); break;
+          case 4: private_logits<BF16, 4, RMAX>(z0, tstride, nvi, ph, r, pr); break;
+          case 2: private_logits<BF16, 2, RMAX>(z0, tstride, nvi, ph, r, pr); break;
+          default: private_logits<BF16, 1, RMAX>(z0, tstride, nvi, ph, r, pr); break;
         }
       }
       if constexpr (!BF16) {
@@ -485,7 +487,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) lrkv_decode_split_kernel(const
           const float* qh = reinterpret_cast<const float*>(q_sh) + h * P.q_stride;
 #pragma unroll
           for (int i = 0; i < kMaxPPT; ++i)
-            if (i < ppt)
+            if (i < nvi)
               pr[i] += dot_f32(qh, reinterpret_cast<const float*>(ks + (lt + i * P.lph) * P.ks_stride), dh);
         }
       }
@@ -541,10 +543,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) lrkv_decode_split_kernel(const
         const unsigned char* z0 = zv + lt * P.z_stride + h * r * ESZ;
         const int tstride = P.lph * P.z_stride;
         switch (P.vec) {
-          case 8: if constexpr (BF16) private_values<BF16, 8, RMAX>(z0, tstride, ppt, w, alpha, r, acc_z); break;
-          case 4: private_values<BF16, 4, RMAX>(z0, tstride, ppt, w, alpha, r, acc_z); break;
-          case 2: private_values<BF16, 2, RMAX>(z0, tstride, ppt, w, alpha, r, acc_z); break;
-          default: private_values<BF16, 1, RMAX>(z0, tstride, ppt, w, alpha, r, acc_z); break;
+          case 8: if constexpr (BF16) private_values<BF16, 8, RMAX>(z0, tstride, nvi, w, alpha, r, acc_z); break;
+          case 4: private_values<BF16, 4, RMAX>(z0, tstride, nvi, w, alpha, r, acc_z); break;
+          case 2: private_values<BF16, 2, RMAX>(z0, tstride, nvi, w, alpha, r, acc_z); break;
+          default: private_values<BF16, 1, RMAX>(z0, tstride, nvi, w, alpha, r, acc_z); break;
         }
       }
     }
@@ -862,7 +864,6 @@ lrkv_status decode_make_plan(const lrkv_dims& d, int num_sms, DecodePlan& P, siz
     P.ksplit = 1;
     for (int k = ksteps; k >= 1; --k)
       if (ksteps % k == 0 && ltiles * k <= nwarps) { P.ksplit = k; break; }
-    if (ltiles > nwarps) return LRKV_ERR_UNSUPPORTED;
     if (mt * (dh / 8) > kMaxValueTiles * nwarps) return LRKV_ERR_UNSUPPORTED;
     P.q_stride = dh + 8;
     P.w_stride = ((P.T / 8) & 1) ? P.T : P.T + 8;

@@ -63,7 +63,7 @@ def test_random_shapes(dtype, shape):
         pytest.skip("bf16 needs head_dim % 16 == 0")
     if dtype == "f32" and dh > 64 and H >= 32:
         pytest.skip("f32 path keeps d_h/lanes columns per lane")
-    case = inputs.random_decode_case(seed=hash(shape) % 1000, batch=B, heads=H, head_dim=dh,
+    case = inputs.random_decode_case(seed=B * 1000 + H * 10 + r + L, batch=B, heads=H, head_dim=dh,
                                      rank=r, max_len=L, dtype=dtype, lens=lens)
     out, lse, _ = _run(case)
     ref_o, ref_l = _oracle(case)
