@@ -1,0 +1,456 @@
+#!/usr/bin/env python
+"""Benchmark of one LRKV decode step on the factored cache (GB300).
+
+A step is one lrkv_decode call over a batch of 8 sequences x 16 heads,
+d_h = 64, rank 28, 4096 visible rows each (bf16 cache, fp32 accumulation):
+absorb q_h B_h^K, scan the factored history with one online softmax per head,
+combine the split pieces and lift the private sum through (B_h^V)^T.  The
+metric is the cache bytes an ideal kernel must read per second (the shared
+rows counted once per sequence, never per head) and its fraction of the
+measured HBM bandwidth; decode tokens/s = batch / step time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+N > 1 runs one independent replica per GPU under torchrun (weak scaling, no
+data-path collective).  `--impl reference` times the fp64 CPU oracle on the
+host cores instead (rank 0 only).  Prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "LRKV decode cache GB/s (% of HBM peak) & tokens/s; prefill TFLOP/s (% peak)"
+PROFILE_JSON = os.path.join(ROOT, "profiles", "decode_split_b8_h16_d64_r28_L4096.json")
+L2_BYTES = 129 * 1000 * 1000
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=None)
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- accounting
+
+def decode_bytes(w, seq_lens):
+    """Algorithmic bytes of one decode call: every visible cache row once
+    (2 (d_h + H r) elements per token), the bases, q, and the fp32 outputs."""
+    s = w.elem_bytes
+    tokens = int(sum(int(x) for x in seq_lens))
+    cache = tokens * 2 * (w.head_dim + w.heads * w.rank) * s
+    bases = 2 * w.heads * w.head_dim * w.rank * s
+    q = w.batch * w.heads * w.head_dim * s
+    out = w.batch * w.heads * (w.head_dim + 1) * 4
+    split = cache + q  # what the split-KV kernel itself must move
+    return cache + bases + q + out, split, cache
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _profile_traffic(split_kernel_src_sha):
+    """DRAM bytes per split launch from the committed ncu summary, if it was
+    taken on the current kernel source."""
+    try:
+        with open(PROFILE_JSON) as f:
+            d = json.load(f)
+        if d.get("source_sha256") == split_kernel_src_sha:
+            return float(d["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+def _src_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "compressed_cache_decode_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.startswith("decode") or name == "ptx.cuh":
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()
+
+
+# -------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"lrkv_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+        except Exception:
+            return None
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        loaded = [x for x in sm if mx and x > 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------- CPU baseline
+
+_POOL_DATA = None
+
+
+def _pool_init(data):
+    global _POOL_DATA
+    _POOL_DATA = data
+
+
+def _oracle_task(task):
+    """One piece of the CPU baseline: the fp64 oracle on one sequence's heads."""
+    from oracle import lrkv_oracle as O
+    b, heads = task
+    d = _POOL_DATA
+    sl = slice(b, b + 1)
+    O.decode_reference(d["q"][sl], d["k_s"][sl], d["v_s"][sl], d["z_k"][sl], d["z_v"][sl],
+                       d["b_k"], d["b_v"], d["seq_lens"][sl], pairs=[(0, h) for h in heads])
+    return len(heads)
+
+
+class OraclePool:
+    """Spawned worker processes, one BLAS thread each, holding the inputs."""
+
+    def __init__(self, case, cores):
+        import multiprocessing as mp
+        self.cores = cores
+        saved = {k: os.environ.get(k) for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")}
+        for k in saved:
+            os.environ[k] = "1"
+        try:
+            ctx = mp.get_context("spawn")
+            self.pool = ctx.Pool(cores, initializer=_pool_init, initargs=(case,))
+        finally:
+            for k, v in saved.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+        self.pool.map(_oracle_task, [(0, [0])] * cores)  # import oracle in every worker
+
+    def run(self, tasks):
+        return sum(self.pool.map(_oracle_task, tasks, chunksize=1))
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+def _tasks(w, split):
+    heads = list(range(w.heads))
+    per = max(1, math.ceil(w.heads / split))
+    return [(b, heads[i:i + per]) for b in range(w.batch) for i in range(0, w.heads, per)]
+
+
+def cpu_baseline(w, case, seconds, cores):
+    """Oracle timed on a bounded sample: whole decode steps (all sequences and
+    heads) repeated until `seconds` of wall time have passed."""
+    pool = OraclePool(case, cores)
+    tasks = _tasks(w, max(1, (2 * cores) // w.batch))
+    total_bytes, _, _ = decode_bytes(w, case["seq_lens"])
+    n, t0 = 0, time.perf_counter()
+    while True:
+        pool.run(tasks)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or n >= 20:
+            break
+    pool.close()
+    return {"value": total_bytes * n / el / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} full decode step(s) of {w.name} (all {w.batch}x{w.heads} sequence-head "
+                      f"pairs, fp64 explicit K_h/V_h reconstruction), {el:.1f} s wall"}
+
+
+def reference_arm(a, w):
+    """--impl reference: the fp64 oracle on the host cores, one bounded sample
+    (one sequence, all heads) per step."""
+    from compressed_cache_decode_gb300 import inputs
+    case = inputs.make_decode_inputs(w, seed=0)
+    cores = min(os.cpu_count() or 1, 16)
+    pool = OraclePool(case, cores)
+    per_b = _tasks(w, cores)
+    B = w.batch
+    _, _, cache_all = decode_bytes(w, case["seq_lens"])
+    seq_bytes = cache_all / B + 2 * w.heads * w.head_dim * w.rank * w.elem_bytes \
+        + w.heads * w.head_dim * (w.elem_bytes + 4)
+    for i in range(a.warmup):
+        b = i % B
+        pool.run([t for t in per_b if t[0] == b])
+    t0 = time.perf_counter()
+    for i in range(a.steps):
+        b = i % B
+        pool.run([t for t in per_b if t[0] == b])
+    el = time.perf_counter() - t0
+    pool.close()
+    value = seq_bytes * a.steps / el / 1e9
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 0,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": el / a.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": w.name, "batch_per_step": 1, "heads": w.heads,
+                       "head_dim": w.head_dim, "rank": w.rank, "seq_len": w.max_len},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": f"one sequence (all {w.heads} heads) of {w.name} per step"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# -------------------------------------------------------------------- GPU arm
+
+def main():
+    a = _args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    from compressed_cache_decode_gb300 import inputs
+    w = inputs.WORKLOADS[a.workload or inputs.DECODE_BENCH_WORKLOAD]
+    if w.kind != "decode":
+        raise SystemExit("bench.py times the decode workloads")
+
+    if a.impl == "reference":
+        if rank == 0:
+            print(json.dumps(reference_arm(a, w)), flush=True)
+        return
+
+    import torch
+    import torch.distributed as dist
+    from compressed_cache_decode_gb300 import build as _build
+    from compressed_cache_decode_gb300 import lrkv
+
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or world == 1:
+        _build.build()
+    if world > 1:
+        dist.barrier()
+    lrkv.load()
+
+    case = inputs.make_decode_inputs(w, seed=rank)
+    d = {k: v.to(dev) for k, v in case.items()}
+    dims = lrkv.make_dims(w.batch, w.heads, w.head_dim, w.rank, w.max_len, w.torch_dtype)
+    ws = lrkv.decode_workspace(dims, dev)
+    out = torch.empty((w.batch, w.heads, w.head_dim), dtype=torch.float32, device=dev)
+    lse = torch.empty((w.batch, w.heads), dtype=torch.float32, device=dev)
+
+    # rotate cache replicas so that consecutive steps never hit in L2
+    cache_bytes = sum(d[k].numel() * d[k].element_size() for k in ("k_s", "v_s", "z_k", "z_v"))
+    n_rep = max(2, math.ceil(4 * L2_BYTES / cache_bytes)) if cache_bytes < 4 * L2_BYTES else 1
+    reps = [d] + [{k: (v.clone() if k in ("k_s", "v_s", "z_k", "z_v") else v) for k, v in d.items()}
+                  for _ in range(n_rep - 1)]
+    total_bytes, split_bytes, _ = decode_bytes(w, case["seq_lens"])
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(i, s=None):
+        x = reps[i % n_rep]
+        st = lrkv.lrkv_decode(dims, x["q"], x["k_s"], x["v_s"], x["z_k"], x["z_v"], x["b_k"],
+                              x["b_v"], x["seq_lens"], out, lse, ws, ws.numel(), s or stream)
+        if st != lrkv.LRKV_OK:
+            raise lrkv.LRKVError(st, "lrkv_decode")
+
+    K, W = a.steps, a.warmup
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            step(i)
+    torch.cuda.synchronize()
+
+    graph = None
+    if not a.no_graph:
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
+                for i in range(K):
+                    step(i, torch.cuda.current_stream())
+            torch.cuda.synchronize()
+            graph.replay()  # warm the graph once (untimed)
+            torch.cuda.synchronize()
+        except Exception as e:  # fall back to eager launches
+            print(f"graph capture failed ({e}); timing eager launches", file=sys.stderr)
+            graph = None
+            torch.cuda.synchronize()
+
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            if graph is not None:
+                graph.replay()
+            else:
+                for i in range(K):
+                    step(i)
+            ev1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms = ev0.elapsed_time(ev1)
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    ms_step = ms_max / K
+
+    # dominant kernel (split-KV scan) timed alone with events around it
+    n_prof = min(K, 50)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_prof)]
+    with torch.cuda.stream(stream):
+        for i in range(n_prof):
+            x = reps[i % n_rep]
+            st = lrkv.lrkv_decode_profiled(dims, x["q"], x["k_s"], x["v_s"], x["z_k"], x["z_v"],
+                                           x["b_k"], x["b_v"], x["seq_lens"], out, lse, ws,
+                                           ws.numel(), evs[i][0], evs[i][1], stream)
+            if st != lrkv.LRKV_OK:
+                raise lrkv.LRKVError(st, "lrkv_decode_profiled")
+    torch.cuda.synchronize()
+    split_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
+
+    # end to end through the public API: each step copies the new token's
+    # query and cache rows from pinned host memory, appends the rows into the
+    # resident cache, decodes, and reads the outputs back.
+    host_q = case["q"].pin_memory()
+    new_rows = {k: case[k][:, -1:].contiguous().pin_memory() for k in ("k_s", "v_s", "z_k", "z_v")}
+    host_lens = case["seq_lens"].pin_memory()
+    host_out = torch.empty_like(out, device="cpu").pin_memory()
+    host_lse = torch.empty_like(lse, device="cpu").pin_memory()
+    h2d = host_q.numel() * host_q.element_size() + host_lens.numel() * 4 + \
+        sum(v.numel() * v.element_size() for v in new_rows.values())
+    d2h = host_out.numel() * 4 + host_lse.numel() * 4
+    K_e2e = min(K, 100)
+
+    def e2e_step(i):
+        x = reps[i % n_rep]
+        x["q"].copy_(host_q, non_blocking=True)
+        x["seq_lens"].copy_(host_lens, non_blocking=True)
+        for k, v in new_rows.items():
+            x[k][:, -1:].copy_(v, non_blocking=True)
+        step(i)
+        host_out.copy_(out, non_blocking=True)
+        host_lse.copy_(lse, non_blocking=True)
+        stream.synchronize()
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(K_e2e):
+            e2e_step(i)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / K_e2e
+    te = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(te, op=dist.ReduceOp.MAX)
+    e2e_ms = float(te.item())
+
+    cpu = None
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        cpu = cpu_baseline(w, case, a.cpu_seconds, min(os.cpu_count() or 1, 16))
+
+    if rank == 0:
+        peak, peak_kind = _peaks()
+        gbs = total_bytes * world / (ms_step * 1e-3) / 1e9
+        achieved = split_bytes / (split_ms * 1e-3) / 1e9
+        traffic = _profile_traffic(_src_sha())
+        res = {
+            "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
+            "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "accumulate": "f32", "data": "synthetic",
+            "tokens_per_s": w.batch * world / (ms_step * 1e-3),
+            "hbm_frac": gbs / world / peak,
+            "config": {"workload": w.name, "batch": w.batch, "heads": w.heads, "head_dim": w.head_dim,
+                       "rank": w.rank, "seq_len": w.max_len,
+                       "cache_fraction_of_mha": 1 / w.heads + w.rank / w.head_dim,
+                       "bytes_per_step": total_bytes,
+                       "l2": f"{n_rep} rotating cache replicas ({n_rep * cache_bytes / 1e6:.0f} MB > L2 "
+                             f"{L2_BYTES / 1e6:.0f} MB)",
+                       "graph": graph is not None, "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "hbm", "kernel": "lrkv_decode_split_kernel", "achieved": achieved,
+                         "peak": peak, "peak_kind": f"{peak_kind} HBM copy", "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "algorithmic_bytes_per_launch": split_bytes, "launch_ms": split_ms},
+            "cpu_baseline": cpu,
+            "e2e": {"value": total_bytes * world / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                    "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 3 * K,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -11,285 +11,151 @@
 //  split    the HBM-bound scan.  The concatenated histories of all sequences
 //           are cut into `grid` equal token ranges, one per CTA, so any mix of
 //           lengths keeps every SM busy.  A CTA streams its rows through a
-//           ring of shared-memory stages filled by 1-D TMA bulk copies: each
-//           shared row k_s/v_s is read from HBM once and serves all H heads
-//           (the reuse the review's roofline paragraph asks for), each latent
-//           row once for its head.  Per tile it forms the summed score
-//           (shared part on the tensor cores with bf16 mma.sync, private part
-//           as fp32 dot products), runs ONE online softmax per head, and
-//           updates two accumulators per head: d_h-wide shared and r-wide
-//           private.  At the end of each (sequence, range) piece it writes
-//           the unnormalised partial (m, l, acc_s, acc_z).
+//           ring of shared-memory stages filled by TMA: the shared rows k_s,
+//           v_s as swizzled tensor tiles (read from HBM once for all H heads,
+//           the reuse the review's roofline paragraph asks for) and the
+//           latent rows as one bulk copy per tile.  Per tile:
+//             A  shared scores on the tensor cores (bf16 mma.sync, heads are
+//                the M dimension) and private scores p_h . z_k (fp32 FMA, one
+//                thread per head and token group);
+//             B  ONE online-softmax update per head over the summed scores,
+//                and the private value sum, each value column owned by one
+//                thread (no cross-thread merge);
+//             C  shared values on the tensor cores, the accumulators rescaled
+//                by the same factor as the private ones.
+//           At the end of each (sequence, range) piece it writes the
+//           unnormalised partial (m, l, acc_s, acc_z).
 //  combine  merges the pieces of a sequence with the log-sum-exp rule, divides
 //           by the denominator and maps the private sum through (B_h^V)^T
 //           once (Algorithm 2 steps 06-09).
 //
-// The three launches are chained with programmatic dependent launch, so the
-// split kernel starts streaming the cache while absorb still runs.
+// The launches are chained with programmatic dependent launch, so the split
+// kernel starts streaming the cache while absorb still runs.
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
 
+#include "decode_common.cuh"
 #include "decode_plan.h"
 #include "ptx.cuh"
+#include "tmap.h"
 
 namespace lrkv {
 
+using namespace dec;
+
+lrkv_status stream_plan(DecodePlan& P);
+lrkv_status stream_launch(const DecodePlan& P, cudaStream_t stream, bool pdl, const CUtensorMap& tm_k,
+                          const CUtensorMap& tm_v);
+
 namespace {
 
-constexpr float kLn2 = 0.69314718055994530942f;
-constexpr float kLog2e = 1.44269504088896340736f;
-
-__host__ __device__ inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
-
-// Padded shared-memory row stride: a multiple of 16 bytes holding an odd
-// number of 16-byte chunks, so consecutive rows start in different bank
-// groups (conflict-free ldmatrix and per-row vector loads).
-inline int odd_chunk_stride(int bytes) {
-  int s = round_up(bytes > 0 ? bytes : 16, 16);
-  if (((s / 16) & 1) == 0) s += 16;
-  return s;
-}
-
-// CTA that owns global token g when N tokens are cut into G ranges
-// [floor(c N / G), floor((c+1) N / G)).
-__device__ __forceinline__ int cta_of_token(long long g, long long N, long long G) {
-  return static_cast<int>(((g + 1) * G - 1) / N);
-}
-
-// ---------------------------------------------------------- element loads --
-template <bool BF16, int NE>
-__device__ __forceinline__ void load_vec(const unsigned char* p, float* f) {
-  if constexpr (BF16) {
-    if constexpr (NE == 8) {
-      const uint4 u = *reinterpret_cast<const uint4*>(p);
-      f[0] = bf_lo(u.x); f[1] = bf_hi(u.x); f[2] = bf_lo(u.y); f[3] = bf_hi(u.y);
-      f[4] = bf_lo(u.z); f[5] = bf_hi(u.z); f[6] = bf_lo(u.w); f[7] = bf_hi(u.w);
-    } else if constexpr (NE == 4) {
-      const uint2 u = *reinterpret_cast<const uint2*>(p);
-      f[0] = bf_lo(u.x); f[1] = bf_hi(u.x); f[2] = bf_lo(u.y); f[3] = bf_hi(u.y);
-    } else if constexpr (NE == 2) {
-      const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
-      f[0] = bf_lo(u); f[1] = bf_hi(u);
-    } else {
-      const uint32_t u = *reinterpret_cast<const unsigned short*>(p);
-      f[0] = __uint_as_float(u << 16);
-    }
-  } else {
-    if constexpr (NE == 4) {
-      const float4 v = *reinterpret_cast<const float4*>(p);
-      f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
-    } else if constexpr (NE == 2) {
-      const float2 v = *reinterpret_cast<const float2*>(p);
-      f[0] = v.x; f[1] = v.y;
-    } else {
-      f[0] = *reinterpret_cast<const float*>(p);
-    }
-  }
-}
-
-template <int NE>
-__device__ __forceinline__ void load_f32(const float* p, float* f) {
-  if constexpr (NE % 4 == 0) {
-#pragma unroll
-    for (int e = 0; e < NE; e += 4) {
-      const float4 v = *reinterpret_cast<const float4*>(p + e);
-      f[e] = v.x; f[e + 1] = v.y; f[e + 2] = v.z; f[e + 3] = v.w;
-    }
-  } else if constexpr (NE == 2) {
-    const float2 v = *reinterpret_cast<const float2*>(p);
-    f[0] = v.x; f[1] = v.y;
-  } else {
-    f[0] = p[0];
-  }
-}
-
-__device__ __forceinline__ float load_elem(const void* base, size_t i, bool bf16) {
-  if (bf16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[i]);
-  return reinterpret_cast<const float*>(base)[i];
-}
-
-// --------------------------------------------------- private-branch pieces --
-// Private logits p_h . z_k,h,t for this lane's tokens (four partial sums per
-// token to shorten the dependent FMA chain).
-template <bool BF16, int NE, int RMAX>
-__device__ __forceinline__ void private_logits(const unsigned char* zrow0, int tok_stride_bytes,
-                                               int ppt, const float* ph, int r,
-                                               float (&res)[kMaxPPT]) {
-  constexpr int ESZ = BF16 ? 2 : 4;
-  float part[kMaxPPT][4];
-#pragma unroll
-  for (int i = 0; i < kMaxPPT; ++i)
-#pragma unroll
-    for (int k = 0; k < 4; ++k) part[i][k] = 0.f;
-#pragma unroll
-  for (int c = 0; c < RMAX; c += NE) {
-    if (c < r) {
-      float pv[NE];
-      load_f32<NE>(ph + c, pv);
-#pragma unroll
-      for (int i = 0; i < kMaxPPT; ++i) {
-        if (i < ppt) {
-          float zv[NE];
-          load_vec<BF16, NE>(zrow0 + static_cast<size_t>(i) * tok_stride_bytes + c * ESZ, zv);
-#pragma unroll
-          for (int e = 0; e < NE; ++e) part[i][e & 3] = fmaf(zv[e], pv[e], part[i][e & 3]);
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < kMaxPPT; ++i) res[i] = (part[i][0] + part[i][1]) + (part[i][2] + part[i][3]);
-}
-
-// acc_z = alpha * acc_z + sum_i w_i z_v,h,t_i
-template <bool BF16, int NE, int RMAX>
-__device__ __forceinline__ void private_values(const unsigned char* zrow0, int tok_stride_bytes,
-                                               int ppt, const float (&w)[kMaxPPT], float alpha,
-                                               int r, float (&acc)[RMAX]) {
-  constexpr int ESZ = BF16 ? 2 : 4;
-#pragma unroll
-  for (int c = 0; c < RMAX; ++c) acc[c] *= alpha;
-#pragma unroll
-  for (int i = 0; i < kMaxPPT; ++i) {
-    if (i < ppt) {
-#pragma unroll
-      for (int c = 0; c < RMAX; c += NE) {
-        if (c < r) {
-          float zv[NE];
-          load_vec<BF16, NE>(zrow0 + static_cast<size_t>(i) * tok_stride_bytes + c * ESZ, zv);
-#pragma unroll
-          for (int e = 0; e < NE; ++e) acc[c + e] = fmaf(w[i], zv[e], acc[c + e]);
-        }
-      }
-    }
-  }
-}
-
-// Dot product of two staged rows of length n (fp32 path, shared logits).
-__device__ __forceinline__ float dot_f32(const float* a, const float* b, int n) {
-  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-  for (int k = 0; k < n; k += 4) {
-    const float4 x = *reinterpret_cast<const float4*>(a + k);
-    const float4 y = *reinterpret_cast<const float4*>(b + k);
-    s0 = fmaf(x.x, y.x, s0); s1 = fmaf(x.y, y.y, s1); s2 = fmaf(x.z, y.z, s2); s3 = fmaf(x.w, y.w, s3);
-  }
-  return (s0 + s1) + (s2 + s3);
-}
-
-// ------------------------------------------------------ token-range walk --
-// A CTA's token range [g0, g1) of the concatenated histories, visited tile by
-// tile; tiles never straddle two sequences.
-struct TileWalk {
-  int b;       // sequence
-  int t0;      // first row of the tile within the sequence
-  int t_beg;   // first row of this CTA's piece of the sequence
-  int t_end;   // one past its last row
-};
-
-__device__ __forceinline__ bool walk_first(TileWalk& w, const int* pre, int B, int g0, int g1) {
-  if (g0 >= g1) return false;
-  int lo = 0, hi = B - 1;  // last b with pre[b] <= g0
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (pre[mid] <= g0) lo = mid; else hi = mid - 1;
-  }
-  int b = lo;
-  while (b < B && pre[b + 1] <= g0) ++b;  // skip empty sequences at g0
-  if (b >= B) return false;
-  w.b = b;
-  w.t_beg = g0 - pre[b];
-  w.t0 = w.t_beg;
-  w.t_end = min(pre[b + 1], g1) - pre[b];
-  return true;
-}
-
-__device__ __forceinline__ bool walk_next(TileWalk& w, const int* pre, int B, int g1, int T) {
-  w.t0 += T;
-  if (w.t0 < w.t_end) return true;
-  int b = w.b + 1;
-  while (b < B && pre[b] < g1 && pre[b + 1] == pre[b]) ++b;
-  if (b >= B || pre[b] >= g1) return false;
-  w.b = b;
-  w.t_beg = 0;
-  w.t0 = 0;
-  w.t_end = min(pre[b + 1], g1) - pre[b];
-  return true;
-}
-
-// Producer: warp 0 issues the row copies of one tile into stage `s`.
-__device__ __forceinline__ void issue_tile(const DecodePlan& P, unsigned char* stage, uint64_t* bar,
-                                           const TileWalk& w, int lane) {
+// Producer (one thread): the copies of one tile into stage `st`.
+template <bool BF16>
+__device__ __forceinline__ void issue_tile(const DecodePlan& P, const CUtensorMap* tm_k,
+                                           const CUtensorMap* tm_v, unsigned char* st, uint64_t* bar,
+                                           const TileWalk& w) {
   const int nvalid = min(P.T, w.t_end - w.t0);
-  const uint32_t bytes =
-      static_cast<uint32_t>(nvalid) * static_cast<uint32_t>(2 * P.ks_row + (P.r > 0 ? 2 * P.z_row : 0));
-  if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
-  __syncwarp();
-  unsigned char* ks = stage;
-  unsigned char* vs = ks + P.T * P.ks_stride;
-  unsigned char* zk = vs + P.T * P.ks_stride;
-  unsigned char* zv = zk + P.T * P.z_stride;
+  unsigned char* ks = st;
+  unsigned char* vs = ks + P.kv_bytes;
+  unsigned char* zk = vs + P.kv_bytes;
+  unsigned char* zv = zk + P.z_bytes;
   const size_t row0 = static_cast<size_t>(w.b) * P.max_len + w.t0;
-  const unsigned char* gks = static_cast<const unsigned char*>(P.k_s) + row0 * P.ks_row;
-  const unsigned char* gvs = static_cast<const unsigned char*>(P.v_s) + row0 * P.ks_row;
-  for (int i = lane; i < nvalid; i += 32) {
-    tma_load_1d(ks + i * P.ks_stride, gks + static_cast<size_t>(i) * P.ks_row, P.ks_row, bar);
-    tma_load_1d(vs + i * P.ks_stride, gvs + static_cast<size_t>(i) * P.ks_row, P.ks_row, bar);
-  }
-  if (P.r > 0) {
-    const unsigned char* gzk = static_cast<const unsigned char*>(P.z_k) + row0 * P.z_row;
-    const unsigned char* gzv = static_cast<const unsigned char*>(P.z_v) + row0 * P.z_row;
-    for (int i = lane; i < nvalid; i += 32) {
-      tma_load_1d(zk + i * P.z_stride, gzk + static_cast<size_t>(i) * P.z_row, P.z_row, bar);
-      tma_load_1d(zv + i * P.z_stride, gzv + static_cast<size_t>(i) * P.z_row, P.z_row, bar);
+  const uint32_t zbytes = P.r > 0 ? static_cast<uint32_t>(nvalid) * P.z_row : 0u;
+  fence_proxy_async_smem();
+  if constexpr (BF16) {
+    // full boxes (rows past the tensor end arrive as zeros)
+    mbar_arrive_expect_tx(bar, 2u * P.T * P.dh * 2u + 2u * zbytes);
+    for (int bx = 0; bx < P.nbox; ++bx) {
+      tma_load_3d(ks + bx * P.T * P.span, tm_k, bx * P.box_cols, w.t0, w.b, bar);
+      tma_load_3d(vs + bx * P.T * P.span, tm_v, bx * P.box_cols, w.t0, w.b, bar);
     }
+  } else {
+    const uint32_t kvb = static_cast<uint32_t>(nvalid) * P.dh * 4u;
+    mbar_arrive_expect_tx(bar, 2u * kvb + 2u * zbytes);
+    tma_load_1d(ks, static_cast<const unsigned char*>(P.k_s) + row0 * P.dh * 4, kvb, bar);
+    tma_load_1d(vs, static_cast<const unsigned char*>(P.v_s) + row0 * P.dh * 4, kvb, bar);
+  }
+  if (zbytes) {
+    tma_load_1d(zk, static_cast<const unsigned char*>(P.z_k) + row0 * P.z_row, zbytes, bar);
+    tma_load_1d(zv, static_cast<const unsigned char*>(P.z_v) + row0 * P.z_row, zbytes, bar);
   }
 }
 
 }  // namespace
 
 // ===================================================================== absorb
+// grid = H, block = 256: B_h^K staged in shared memory once, then p for every
+// sequence of this head.
 template <bool BF16>
-__global__ void __launch_bounds__(128) lrkv_decode_absorb_kernel(const DecodePlan P) {
+__global__ void __launch_bounds__(256) lrkv_decode_absorb_kernel(const DecodePlan P) {
+  extern __shared__ __align__(16) float bks[];  // [dh][r]
   pdl_trigger();
-  const int h = blockIdx.x, b = blockIdx.y;
-  if (h == 0 && b == 0 && threadIdx.x == 0) *P.status = 0u;
-  if (P.r == 0) return;
-  __shared__ float qs[256];
-  for (int k = threadIdx.x; k < P.dh; k += blockDim.x)
-    qs[k] = load_elem(P.q, (static_cast<size_t>(b) * P.H + h) * P.dh + k, BF16);
+  const int h = blockIdx.x, tid = threadIdx.x;
+  if (h == 0 && tid == 0) *P.status = 0u;
+  const int dh = P.dh, r = P.r, H = P.H;
+  if (r == 0) return;
+  const size_t base = static_cast<size_t>(h) * dh * r;
+  for (int i = tid; i < dh * r; i += blockDim.x) bks[i] = load_elem(P.b_k, base + i, BF16);
   __syncthreads();
-  for (int c = threadIdx.x; c < P.r; c += blockDim.x) {
-    float acc = 0.f;
-    const size_t base = static_cast<size_t>(h) * P.dh * P.r + c;
-    for (int k = 0; k < P.dh; ++k) acc = fmaf(qs[k], load_elem(P.b_k, base + static_cast<size_t>(k) * P.r, BF16), acc);
-    P.p_abs[(static_cast<size_t>(b) * P.H + h) * P.r + c] = acc;
+  for (int idx = tid; idx < P.B * r; idx += blockDim.x) {
+    const int b = idx / r, c = idx % r;
+    const size_t qb = (static_cast<size_t>(b) * H + h) * dh;
+    float a0 = 0.f, a1 = 0.f;
+    int k = 0;
+    for (; k + 1 < dh; k += 2) {
+      a0 = fmaf(load_elem(P.q, qb + k, BF16), bks[k * r + c], a0);
+      a1 = fmaf(load_elem(P.q, qb + k + 1, BF16), bks[(k + 1) * r + c], a1);
+    }
+    if (k < dh) a0 = fmaf(load_elem(P.q, qb + k, BF16), bks[k * r + c], a0);
+    P.p_abs[(static_cast<size_t>(b) * H + h) * r + c] = a0 + a1;
   }
 }
 
 // ====================================================================== split
-template <bool BF16, int RMAX>
-__global__ void __launch_bounds__(kMaxThreads, 1) lrkv_decode_split_kernel(const DecodePlan P) {
-  extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ int s_ok;
+// Thread roles (H heads, 256 threads):
+//   score role   (ha, tg) = (tid % H, tid / H), tg < ntg: the private score
+//                p_h . z_k of tokens tg, tg + ntg, ... and (fp32) the shared
+//                score, the softmax weights of those tokens, and a partial
+//                denominator;
+//   value role   (hb, rg) = (tid % H, tid / H), rg < nrg: value columns
+//                [rg*cw, rg*cw + cw) of the private sum (fp32: of [shared |
+//                private]) over every token of the tile;
+//   MMA role     warps: shared scores and shared values on the tensor cores.
+// Weights are taken against a per-head reference max m_ref.  A tile whose
+// scores all stay below m_ref + 8 (log2 domain, weights <= 256) needs no
+// rescale; otherwise (always on a piece's first tile) the tile max is reduced
+// across the head's threads and every accumulator is rescaled once.  This is
+// the online softmax of the review's fused variant with the rescale taken
+// only when it is needed.
+template <bool BF16, int RMAX, int NE>
+__global__ void __launch_bounds__(kThreads, 1)
+    lrkv_decode_split_kernel(const DecodePlan P, const __grid_constant__ CUtensorMap tm_k,
+                             const __grid_constant__ CUtensorMap tm_v) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ int s_bad;
+  __shared__ int s_timeout;
+  // the swizzled TMA boxes need 1024-byte-aligned destinations
+  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nwarps = blockDim.x >> 5;
   const int B = P.B, H = P.H, dh = P.dh, r = P.r, T = P.T;
   constexpr int ESZ = BF16 ? 2 : 4;
+  constexpr float kHeadroom = 8.f;  // log2 units
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   int* pre = reinterpret_cast<int*>(smem + P.off_prefix);
   unsigned char* q_sh = smem + P.off_q;
-  float* p_sh = reinterpret_cast<float*>(smem + P.off_p);
-  float* s_sh = reinterpret_cast<float*>(smem + P.off_s);
-  unsigned char* w_sh = smem + P.off_w;
-  float* alpha_sh = reinterpret_cast<float*>(smem + P.off_alpha);
+  float* s_sh = reinterpret_cast<float*>(smem + P.off_ssh);   // shared scores [T][s_stride]
+  float* wf_sh = reinterpret_cast<float*>(smem + P.off_sp);   // fp32 weights [T][s_stride]
+  __nv_bfloat16* w_sh = reinterpret_cast<__nv_bfloat16*>(smem + P.off_w);  // bf16 weights [Hp][w_stride]
+  float* alpha_sh = reinterpret_cast<float*>(smem + P.off_alpha);  // [Hp]
+  float* red_sh = reinterpret_cast<float*>(smem + P.off_red);      // [ntg][H]
   unsigned char* stages = smem + P.off_stage;
 
   // ---- 1. sequence starts (clamped lengths) --------------------------------
-  if (tid == 0) s_bad = 0;
+  if (tid == 0) { s_bad = 0; s_timeout = 0; }
   __syncthreads();
   for (int b = tid; b < B; b += blockDim.x) {
     int L = P.seq_lens[b];
@@ -330,57 +196,57 @@ __global__ void __launch_bounds__(kMaxThreads, 1) lrkv_decode_split_kernel(const
   const int g0 = static_cast<int>(static_cast<long long>(c) * N / G);
   const int g1 = static_cast<int>(static_cast<long long>(c + 1) * N / G);
 
-  // ---- 2. barriers and the first tiles -------------------------------------
+  // ---- 2. barriers, constant tiles, first copies ---------------------------
   if (tid == 0) {
     for (int s = 0; s < P.stages; ++s) mbar_init(&bars[s], 1);
     fence_barrier_init();
   }
-  // constant parts of the MMA operand tiles
   if constexpr (BF16) {
     for (int i = tid; i < P.Hp; i += blockDim.x) alpha_sh[i] = 1.f;
-    __nv_bfloat16* wt = reinterpret_cast<__nv_bfloat16*>(w_sh);
-    for (int i = tid; i < P.Hp * P.w_stride; i += blockDim.x) wt[i] = __float2bfloat16(0.f);
+    for (int i = tid; i < P.Hp * P.w_stride; i += blockDim.x) w_sh[i] = __float2bfloat16(0.f);
   }
   __syncthreads();
 
-  TileWalk pw;  // producer walk (warp 0)
+  TileWalk pw;  // producer walk (thread 0)
   bool p_more = walk_first(pw, pre, B, g0, g1);
   int issued = 0;
-  if (warp == 0) {
+  if (tid == 0) {
     for (int s = 0; s < P.stages && p_more; ++s) {
-      issue_tile(P, stages + static_cast<size_t>(s) * P.stage_bytes, &bars[s], pw, lane);
+      issue_tile<BF16>(P, &tm_k, &tm_v, stages + static_cast<size_t>(s) * P.stage_bytes, &bars[s], pw);
       ++issued;
       p_more = walk_next(pw, pre, B, g1, T);
     }
   }
 
-  // operands produced by the absorb kernel are read only after this point
+  // the absorb kernel's output (p) is read only after this point
   pdl_wait();
   if (s_bad && tid == 0) record_status(P.status, kDevBounds);
 
-  // ---- 3. per-thread roles -------------------------------------------------
-  const int h = tid / P.lph;          // head of this lane (private branch, softmax)
-  const int lt = tid % P.lph;         // lane within the head group
-  const bool active = h < H;
-  const int ppt = P.ppt;
+  // ---- 3. thread roles -----------------------------------------------------
+  const int ha = tid % H, tg = tid / H;
+  const bool a_active = tg < P.ntg;
+  const int hb = ha, rg = tg;
+  const bool b_active = rg < P.nrg;
   const int g = lane >> 2, q4 = lane & 3;  // MMA fragment coordinates
+  const int mt = P.Hp / 16;
+  const int n_vtiles = BF16 ? mt * (dh / 8) : 0;
+  const int ltiles = BF16 ? mt * (T / 8) : 0;
+  const int vw = BF16 ? r : dh + r;  // width of the per-thread value space
+  const int col0 = rg * P.cw;
 
-  // online-softmax state of head h (identical across the group's lanes)
-  float m_run = -INFINITY;
-  float l_part = 0.f;
-  float acc_z[RMAX];
+  float p_reg[RMAX];     // q_h B_h^K of head ha (this piece's sequence)
+  float acc_c[kMaxCW];   // value columns owned by (hb, rg)
+  float acc_v[kMaxValueTiles][4];  // shared-value MMA fragments (bf16)
+  float m_ref = -INFINITY;  // reference max of head ha (identical in all its threads)
+  float l_part = 0.f;       // denominator over this thread's tokens
 #pragma unroll
-  for (int i = 0; i < RMAX; ++i) acc_z[i] = 0.f;
-  // shared-value accumulators: bf16 -> MMA fragments; f32 -> per-lane columns
-  float acc_v[kMaxValueTiles][4];
+  for (int i = 0; i < RMAX; ++i) p_reg[i] = 0.f;
+#pragma unroll
+  for (int i = 0; i < kMaxCW; ++i) acc_c[i] = 0.f;
 #pragma unroll
   for (int j = 0; j < kMaxValueTiles; ++j)
 #pragma unroll
     for (int k = 0; k < 4; ++k) acc_v[j][k] = 0.f;
-  const int mt = P.Hp / 16;
-  const int n_vtiles = BF16 ? mt * (dh / 8) : 0;
-  const int ltiles = BF16 ? mt * (T / 8) : 0;
-  const int kps = BF16 ? (dh / 16) / P.ksplit : 0;
 
   TileWalk cw;
   walk_first(cw, pre, B, g0, g1);
@@ -391,32 +257,21 @@ __global__ void __launch_bounds__(kMaxThreads, 1) lrkv_decode_split_kernel(const
   while (true) {
     const int s = it % P.stages;
     const uint32_t parity = static_cast<uint32_t>(it / P.stages) & 1u;
-    unsigned char* st = stages + static_cast<size_t>(s) * P.stage_bytes;
-    unsigned char* ks = st;
-    unsigned char* vs = ks + T * P.ks_stride;
-    unsigned char* zk = vs + T * P.ks_stride;
-    unsigned char* zv = zk + T * P.z_stride;
+    unsigned char* ks = stages + static_cast<size_t>(s) * P.stage_bytes;
+    unsigned char* vs = ks + P.kv_bytes;
+    unsigned char* zk = vs + P.kv_bytes;
+    unsigned char* zv = zk + P.z_bytes;
     const int nvalid = min(T, cw.t_end - cw.t0);
+    // this thread's tokens in the score role: tg, tg + ntg, ... (< nvalid)
+    const int nmine = (a_active && nvalid > tg) ? (nvalid - tg + P.ntg - 1) / P.ntg : 0;
 
-    // ---- wait for the tile (bounded), refill the stage freed last round ----
-    if (tid == 0) s_ok = mbar_wait_bounded(&bars[s], parity) ? 1 : 0;
-    __syncthreads();  // (#1) also: every thread finished the previous tile
-    if (!s_ok) { ok = false; break; }
-    mbar_try_wait(&bars[s], parity);  // acquire the TMA writes in every thread
-    if (warp == 0 && it > 0 && p_more) {
-      const int sp = (it - 1) % P.stages;
-      issue_tile(P, stages + static_cast<size_t>(sp) * P.stage_bytes, &bars[sp], pw, lane);
-      ++issued;
-      p_more = walk_next(pw, pre, B, g1, T);
-    }
-
-    // ---- segment set-up: q and p of sequence cw.b --------------------------
+    // ---- piece set-up: q (shared scores) and p (private scores) -----------
     if (seg_start) {
       const int b = cw.b;
       if constexpr (BF16) {
         const uint4* gq = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(P.q) +
                                                          static_cast<size_t>(b) * H * dh);
-        const int cpr = dh / 8;  // 16-byte chunks per row
+        const int cpr = dh / 8;
         for (int i = tid; i < P.Hp * cpr; i += blockDim.x) {
           const int hh = i / cpr, k8 = i % cpr;
           uint4 v = make_uint4(0, 0, 0, 0);
@@ -428,167 +283,231 @@ __global__ void __launch_bounds__(kMaxThreads, 1) lrkv_decode_split_kernel(const
         float* qf = reinterpret_cast<float*>(q_sh);
         for (int i = tid; i < H * dh; i += blockDim.x) qf[(i / dh) * P.q_stride + (i % dh)] = gq[i];
       }
-      const float* gp = P.p_abs + static_cast<size_t>(b) * H * r;
-      for (int i = tid; i < H * r; i += blockDim.x) p_sh[(i / r) * P.p_stride + (i % r)] = gp[i];
+      if (a_active && r > 0) {
+        const float* gp = P.p_abs + (static_cast<size_t>(b) * H + ha) * r;
+#pragma unroll
+        for (int c4 = 0; c4 < RMAX; c4 += 4) {
+          if (c4 < r) {
+            const float4 v = *reinterpret_cast<const float4*>(gp + c4);
+            p_reg[c4] = v.x; p_reg[c4 + 1] = v.y; p_reg[c4 + 2] = v.z; p_reg[c4 + 3] = v.w;
+          }
+        }
+      }
       __syncthreads();
       seg_start = false;
     }
 
-    // ---- zero the rows past the piece's end (values must not carry NaN) ---
-    if constexpr (BF16) {
-      if (nvalid < T) {
-        const int cpr = P.ks_stride / 16;
-        for (int i = tid; i < (T - nvalid) * cpr; i += blockDim.x) {
-          const int row = nvalid + i / cpr;
-          *reinterpret_cast<uint4*>(vs + row * P.ks_stride + (i % cpr) * 16) = make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
-      }
-    }
+    // ---- wait for the tile (bounded; every thread observes the barrier) ----
+    const bool got = mbar_wait_bounded(&bars[s], parity);
+    if (!got) s_timeout = 1;
 
-    // ---- scores: shared part (MMA warps) and private part (head lanes) ------
-    if constexpr (BF16) {
-      for (int item = warp; item < ltiles * P.ksplit; item += nwarps) {
-        const int tile = item % ltiles, kg = item / ltiles;
-        const int mi = tile / (T / 8), nj = tile % (T / 8);
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int kk = kg * kps; kk < (kg + 1) * kps; ++kk) {
-          uint32_t a0, a1, a2, a3, b0, b1;
-          ldsm_x4(a0, a1, a2, a3, q_sh + ((mi * 16 + (lane & 15)) * P.q_stride + kk * 16 + (lane >> 4) * 8) * 2);
-          ldsm_x2(b0, b1, ks + (nj * 8 + (lane & 7)) * P.ks_stride + (kk * 16 + ((lane >> 3) & 1) * 8) * 2);
-          mma_bf16_16816(d, a0, a1, a2, a3, b0, b1);
-        }
-        float* sk = s_sh + (kg * P.Hp) * T;
-        const int row = mi * 16 + g, col = nj * 8 + 2 * q4;
-        sk[row * T + col] = d[0];
-        sk[row * T + col + 1] = d[1];
-        sk[(row + 8) * T + col] = d[2];
-        sk[(row + 8) * T + col + 1] = d[3];
-      }
-    }
-    // this lane's tokens lt, lt + lph, ... ; only the first `nvi` hold rows
-    const int nvi = (nvalid > lt) ? min(ppt, (nvalid - lt + P.lph - 1) / P.lph) : 0;
-    float sc[kMaxPPT];
-    {
-      float pr[kMaxPPT] = {0.f, 0.f, 0.f, 0.f};
-      if (active && r > 0) {
-        const unsigned char* z0 = zk + lt * P.z_stride + h * r * ESZ;
-        const float* ph = p_sh + h * P.p_stride;
-        const int tstride = P.lph * P.z_stride;
-        switch (P.vec) {
-          case 8: if constexpr (BF16) private_logits<BF16, 8, RMAX>(z0, tstride, nvi, ph, r, pr); break;
-          case 4: private_logits<BF16, 4, RMAX>(z0, tstride, nvi, ph, r, pr); break;
-          case 2: private_logits<BF16, 2, RMAX>(z0, tstride, nvi, ph, r, pr); break;
-          default: private_logits<BF16, 1, RMAX>(z0, tstride, nvi, ph, r, pr); break;
-        }
-      }
-      if constexpr (!BF16) {
-        if (active) {
-          const float* qh = reinterpret_cast<const float*>(q_sh) + h * P.q_stride;
+    // ---- phase A: scores ----------------------------------------------------
+    float sc[kMaxPPT];  // this thread's summed, scaled scores (log2 domain)
 #pragma unroll
-          for (int i = 0; i < kMaxPPT; ++i)
-            if (i < nvi)
-              pr[i] += dot_f32(qh, reinterpret_cast<const float*>(ks + (lt + i * P.lph) * P.ks_stride), dh);
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < kMaxPPT; ++i) sc[i] = pr[i];
-    }
-    if constexpr (BF16) __syncthreads();  // (#2) shared-part scores are in s_sh
-
-    // ---- one online softmax per head over the summed scores ---------------
-    float w[kMaxPPT];
-    float alpha = 1.f;
-    {
-      float mloc = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < kMaxPPT; ++i) {
-        float v = -INFINITY;
-        const int t = lt + i * P.lph;
-        if (i < ppt && active && t < nvalid) {
-          float sum = sc[i];
-          if constexpr (BF16) {
-            for (int kg = 0; kg < P.ksplit; ++kg) sum += s_sh[(kg * P.Hp + h) * T + t];
+    for (int i = 0; i < kMaxPPT; ++i) sc[i] = 0.f;
+    if (got) {
+      if constexpr (BF16) {
+        // rows past the piece's end must hold zeros before the value MMA
+        if (nvalid < T) {
+          const int cpr = P.span / 16;  // 16-byte chunks per box row
+          const int per = (T - nvalid) * cpr;
+          for (int i = tid; i < P.nbox * per; i += blockDim.x) {
+            const int bx = i / per, rem = i % per;
+            const int row = nvalid + rem / cpr, ch = rem % cpr;
+            *reinterpret_cast<uint4*>(vs + bx * T * P.span + row * P.span + ch * 16) = make_uint4(0, 0, 0, 0);
           }
-          v = sum * P.scale_log2;
+          fence_proxy_async_smem();
         }
+        for (int item = warp; item < ltiles; item += nwarps) {
+          const int mi = item / (T / 8), nj = item % (T / 8);
+          float d[4] = {0.f, 0.f, 0.f, 0.f};
+          const int trow = nj * 8 + (lane & 7);
+          for (int kk = 0; kk < dh / 16; ++kk) {
+            uint32_t a0, a1, a2, a3, b0, b1;
+            ldsm_x4(a0, a1, a2, a3, q_sh + ((mi * 16 + (lane & 15)) * P.q_stride + kk * 16 + (lane >> 4) * 8) * 2);
+            const int k0 = kk * 16 + ((lane >> 3) & 1) * 8;
+            const int bx = k0 / P.box_cols, ch = (k0 % P.box_cols) / 8;
+            ldsm_x2(b0, b1, ks + bx * T * P.span + swz_off(trow, ch, P.span));
+            mma_bf16_16816(d, a0, a1, a2, a3, b0, b1);
+          }
+          const int h0 = mi * 16 + g, t0 = nj * 8 + 2 * q4;
+          s_sh[t0 * P.s_stride + h0] = d[0];
+          s_sh[(t0 + 1) * P.s_stride + h0] = d[1];
+          s_sh[t0 * P.s_stride + h0 + 8] = d[2];
+          s_sh[(t0 + 1) * P.s_stride + h0 + 8] = d[3];
+        }
+      }
+      if (nmine > 0) {
+        const unsigned char* zrow = zk + ha * r * ESZ;
+#pragma unroll
+        for (int i = 0; i < kMaxPPT; ++i) {
+          if (i < nmine) {
+            const int t = tg + i * P.ntg;
+            float part[4] = {0.f, 0.f, 0.f, 0.f};
+            if (r > 0) {
+              const unsigned char* zt = zrow + static_cast<size_t>(t) * P.z_row;
+#pragma unroll
+              for (int c0 = 0; c0 < RMAX; c0 += NE) {
+                if (c0 < r) {
+                  float zv4[NE];
+                  load_vec<BF16, NE>(zt + c0 * ESZ, zv4);
+#pragma unroll
+                  for (int e = 0; e < NE; ++e) part[e & 3] = fmaf(zv4[e], p_reg[c0 + e], part[e & 3]);
+                }
+              }
+            }
+            if constexpr (!BF16) {
+              const float* qh = reinterpret_cast<const float*>(q_sh) + ha * P.q_stride;
+              const float* kt = reinterpret_cast<const float*>(ks) + t * dh;
+              for (int k = 0; k < dh; k += 4) {
+                const float4 x = *reinterpret_cast<const float4*>(qh + k);
+                const float4 y = *reinterpret_cast<const float4*>(kt + k);
+                part[0] = fmaf(x.x, y.x, part[0]); part[1] = fmaf(x.y, y.y, part[1]);
+                part[2] = fmaf(x.z, y.z, part[2]); part[3] = fmaf(x.w, y.w, part[3]);
+              }
+            }
+            sc[i] = (part[0] + part[1]) + (part[2] + part[3]);
+          }
+        }
+      }
+    }
+    __syncthreads();  // (#1) shared scores in shared memory; everyone left the previous tile
+    if (s_timeout) { ok = false; break; }
+    if (tid == 0 && it > 0 && p_more) {  // refill the stage the previous tile used
+      const int sp = (it - 1) % P.stages;
+      issue_tile<BF16>(P, &tm_k, &tm_v, stages + static_cast<size_t>(sp) * P.stage_bytes, &bars[sp], pw);
+      ++issued;
+      p_more = walk_next(pw, pre, B, g1, T);
+    }
+
+    // ---- phase B: weights against the reference max --------------------------
+    bool need = false;
+    float mloc = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kMaxPPT; ++i) {
+      if (i < nmine) {
+        const int t = tg + i * P.ntg;
+        float v = sc[i];
+        if constexpr (BF16) v += s_sh[t * P.s_stride + ha];
+        v *= P.scale_log2;
         sc[i] = v;
         mloc = fmaxf(mloc, v);
       }
-      for (int o = P.lph >> 1; o > 0; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
-      const float m_new = fmaxf(m_run, mloc);
-      alpha = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);
+    }
+    need = mloc > m_ref + kHeadroom;
+    auto write_weights = [&](float mref) {
       float lsum = 0.f;
 #pragma unroll
       for (int i = 0; i < kMaxPPT; ++i) {
-        w[i] = (sc[i] == -INFINITY) ? 0.f : exp2f(sc[i] - m_new);
-        lsum += w[i];
-      }
-      l_part = l_part * alpha + lsum;
-      m_run = m_new;
-      if (active) {
-#pragma unroll
-        for (int i = 0; i < kMaxPPT; ++i) {
-          if (i < ppt) {
-            const int t = lt + i * P.lph;
-            if constexpr (BF16)
-              reinterpret_cast<__nv_bfloat16*>(w_sh)[h * P.w_stride + t] = __float2bfloat16(w[i]);
-            else
-              reinterpret_cast<float*>(w_sh)[h * P.w_stride + t] = w[i];
-          }
+        if (i < nmine) {
+          const int t = tg + i * P.ntg;
+          const float w = exp2f(sc[i] - mref);
+          lsum += w;
+          wf_sh[t * P.s_stride + ha] = w;
+          if constexpr (BF16) w_sh[ha * P.w_stride + t] = __float2bfloat16(w);
         }
-        if (BF16 && lt == 0) alpha_sh[h] = alpha;
       }
-      if (active && r > 0) {
-        const unsigned char* z0 = zv + lt * P.z_stride + h * r * ESZ;
-        const int tstride = P.lph * P.z_stride;
-        switch (P.vec) {
-          case 8: if constexpr (BF16) private_values<BF16, 8, RMAX>(z0, tstride, nvi, w, alpha, r, acc_z); break;
-          case 4: private_values<BF16, 4, RMAX>(z0, tstride, nvi, w, alpha, r, acc_z); break;
-          case 2: private_values<BF16, 2, RMAX>(z0, tstride, nvi, w, alpha, r, acc_z); break;
-          default: private_values<BF16, 1, RMAX>(z0, tstride, nvi, w, alpha, r, acc_z); break;
+      return lsum;
+    };
+    float lsum = 0.f;
+    if (!need) lsum = write_weights(m_ref);
+    // rows past the piece's end carry zero weight
+    if (a_active) {
+      for (int t = nvalid + tg; t < T; t += P.ntg) {
+        wf_sh[t * P.s_stride + ha] = 0.f;
+        if constexpr (BF16) w_sh[ha * P.w_stride + t] = __float2bfloat16(0.f);
+      }
+    }
+    if (__syncthreads_or(need)) {  // (#2) rare: some head's max moved up
+      if (a_active) red_sh[tg * H + ha] = mloc;
+      __syncthreads();
+      float alpha = 1.f;
+      if (a_active || b_active) {
+        float mt_ = -INFINITY;
+        for (int k = 0; k < P.ntg; ++k) mt_ = fmaxf(mt_, red_sh[k * H + ha]);
+        const float m_new = fmaxf(m_ref, mt_);
+        alpha = exp2f(m_ref - m_new);  // 0 on a piece's first tile
+        m_ref = m_new;
+      }
+      if (a_active) {
+        l_part *= alpha;
+        lsum = write_weights(m_ref);
+        if (BF16 && tg == 0) alpha_sh[ha] = alpha;
+      }
+      if (b_active) {
+#pragma unroll
+        for (int i = 0; i < kMaxCW; ++i) acc_c[i] *= alpha;
+      }
+      __syncthreads();
+      if constexpr (BF16) {
+#pragma unroll
+        for (int j = 0; j < kMaxValueTiles; ++j) {
+          const int vt = warp + j * nwarps;
+          if (vt < n_vtiles) {
+            const int mi = vt / (dh / 8);
+            const float a_lo = alpha_sh[mi * 16 + g], a_hi = alpha_sh[mi * 16 + g + 8];
+            acc_v[j][0] *= a_lo; acc_v[j][1] *= a_lo; acc_v[j][2] *= a_hi; acc_v[j][3] *= a_hi;
+          }
         }
       }
     }
+    l_part += lsum;
 
-    // ---- shared values ------------------------------------------------------
+    // ---- phase C: values ----------------------------------------------------
     if constexpr (BF16) {
-      __syncthreads();  // (#3) W and alpha of every head are in shared memory
 #pragma unroll
       for (int j = 0; j < kMaxValueTiles; ++j) {
         const int vt = warp + j * nwarps;
         if (vt < n_vtiles) {
           const int mi = vt / (dh / 8), nt = vt % (dh / 8);
-          const float a_lo = alpha_sh[mi * 16 + g], a_hi = alpha_sh[mi * 16 + g + 8];
-          acc_v[j][0] *= a_lo; acc_v[j][1] *= a_lo; acc_v[j][2] *= a_hi; acc_v[j][3] *= a_hi;
-          const unsigned char* wrow = w_sh + ((mi * 16 + (lane & 15)) * P.w_stride) * 2;
+          const unsigned char* wrow = reinterpret_cast<const unsigned char*>(w_sh) +
+                                      (mi * 16 + (lane & 15)) * P.w_stride * 2;
+          const int n0 = nt * 8;
+          const unsigned char* vbox = vs + (n0 / P.box_cols) * T * P.span;
+          const int ch = (n0 % P.box_cols) / 8;
           if ((T & 15) == 0) {
             for (int kk = 0; kk < T / 16; ++kk) {
               uint32_t a0, a1, a2, a3, b0, b1;
               ldsm_x4(a0, a1, a2, a3, wrow + (kk * 16 + (lane >> 4) * 8) * 2);
-              ldsm_x2_trans(b0, b1, vs + (kk * 16 + (lane & 15)) * P.ks_stride + nt * 16);
+              ldsm_x2_trans(b0, b1, vbox + swz_off(kk * 16 + (lane & 15), ch, P.span));
               mma_bf16_16816(acc_v[j], a0, a1, a2, a3, b0, b1);
             }
           } else {
             uint32_t a0, a1, b0;
             ldsm_x2(a0, a1, wrow);
-            ldsm_x1_trans(b0, vs + (lane & 7) * P.ks_stride + nt * 16);
+            ldsm_x1_trans(b0, vbox + swz_off(lane & 7, ch, P.span));
             mma_bf16_1688(acc_v[j], a0, a1, b0);
           }
         }
       }
-    } else {
-      __syncwarp();  // the head group's W are in shared memory
-      if (active) {
-        const float* wrow = reinterpret_cast<const float*>(w_sh) + h * P.w_stride;
+    }
+    if (b_active && vw > 0) {
+      for (int t = 0; t < nvalid; ++t) {
+        const float w = wf_sh[t * P.s_stride + hb];
+        if constexpr (BF16) {
+          const unsigned char* zt = zv + static_cast<size_t>(t) * P.z_row + (hb * r + col0) * ESZ;
 #pragma unroll
-        for (int j = 0; j < kMaxValueTiles * 4; ++j) {
-          const int k = lt + j * P.lph;
-          if (k < dh) {
-            float a = acc_v[j >> 2][j & 3] * alpha;
-            for (int t = 0; t < nvalid; ++t)
-              a = fmaf(wrow[t], reinterpret_cast<const float*>(vs + t * P.ks_stride)[k], a);
-            acc_v[j >> 2][j & 3] = a;
+          for (int c0 = 0; c0 < kMaxCW; c0 += NE) {
+            if (c0 < P.cw && col0 + c0 < r) {
+              float zv4[NE];
+              load_vec<BF16, NE>(zt + c0 * ESZ, zv4);
+#pragma unroll
+              for (int e = 0; e < NE; ++e) acc_c[c0 + e] = fmaf(w, zv4[e], acc_c[c0 + e]);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int c0 = 0; c0 < kMaxCW; c0 += 4) {
+            const int col = col0 + c0;
+            if (c0 < P.cw && col < vw) {
+              const unsigned char* src = col < dh
+                  ? vs + (static_cast<size_t>(t) * dh + col) * 4
+                  : zv + static_cast<size_t>(t) * P.z_row + (hb * r + col - dh) * 4;
+              float x4[4];
+              load_vec<false, 4>(src, x4);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) acc_c[c0 + e] = fmaf(w, x4[e], acc_c[c0 + e]);
+            }
           }
         }
       }
@@ -598,20 +517,21 @@ __global__ void __launch_bounds__(kMaxThreads, 1) lrkv_decode_split_kernel(const
     const bool last_of_piece = cw.t0 + T >= cw.t_end;
     if (last_of_piece) {
       const int slot = cw.b + c;
-      float l_tot = l_part;
-      for (int o = P.lph >> 1; o > 0; o >>= 1) l_tot += __shfl_xor_sync(0xffffffffu, l_tot, o);
-#pragma unroll
-      for (int i = 0; i < RMAX; ++i)
-        for (int o = P.lph >> 1; o > 0; o >>= 1) acc_z[i] += __shfl_xor_sync(0xffffffffu, acc_z[i], o);
       float* pacc = P.part_acc + static_cast<size_t>(slot) * H * (dh + r);
-      if (active) {
-        if (lt == 0) {
-          P.part_ml[(static_cast<size_t>(slot) * H + h) * 2 + 0] = m_run;
-          P.part_ml[(static_cast<size_t>(slot) * H + h) * 2 + 1] = l_tot;
-        }
+      __syncthreads();  // red_sh may still be read by the rescale above
+      if (a_active) red_sh[tg * H + ha] = l_part;
+      __syncthreads();
+      if (a_active && tg == 0) {
+        float l_tot = 0.f;
+        for (int k = 0; k < P.ntg; ++k) l_tot += red_sh[k * H + ha];
+        P.part_ml[(static_cast<size_t>(slot) * H + ha) * 2 + 0] = m_ref;
+        P.part_ml[(static_cast<size_t>(slot) * H + ha) * 2 + 1] = l_tot;
+      }
+      if (b_active) {
+        const int off = BF16 ? dh : 0;  // bf16: the columns are private ones
 #pragma unroll
-        for (int i = 0; i < RMAX; ++i)
-          if (i < r && (i % P.lph) == lt) pacc[h * (dh + r) + dh + i] = acc_z[i];
+        for (int i = 0; i < kMaxCW; ++i)
+          if (i < P.cw && col0 + i < vw) pacc[hb * (dh + r) + off + col0 + i] = acc_c[i];
       }
       if constexpr (BF16) {
 #pragma unroll
@@ -624,20 +544,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) lrkv_decode_split_kernel(const
             if (h0 + 8 < H) { pacc[(h0 + 8) * (dh + r) + col] = acc_v[j][2]; pacc[(h0 + 8) * (dh + r) + col + 1] = acc_v[j][3]; }
           }
         }
-      } else {
-        if (active) {
-#pragma unroll
-          for (int j = 0; j < kMaxValueTiles * 4; ++j) {
-            const int k = lt + j * P.lph;
-            if (k < dh) pacc[h * (dh + r) + k] = acc_v[j >> 2][j & 3];
-          }
-        }
       }
-      // fresh state for the next piece
-      m_run = -INFINITY;
+      m_ref = -INFINITY;
       l_part = 0.f;
 #pragma unroll
-      for (int i = 0; i < RMAX; ++i) acc_z[i] = 0.f;
+      for (int i = 0; i < kMaxCW; ++i) acc_c[i] = 0.f;
 #pragma unroll
       for (int j = 0; j < kMaxValueTiles; ++j)
 #pragma unroll
@@ -678,7 +589,8 @@ __global__ void __launch_bounds__(128) lrkv_decode_combine_kernel(const DecodePl
   }
   const long long N = P.meta[0], G = P.meta[1];
   const int c0 = cta_of_token(start, N, G), c1 = cta_of_token(end - 1, N, G);
-  const int n = c1 - c0 + 1;
+  const int n = (c1 - c0 + 1) * P.ngw;       // partials of this sequence
+  const size_t s0 = static_cast<size_t>(b + c0) * P.ngw;  // first of them
   float* wsl = reinterpret_cast<float*>(csmem);   // [n] per-piece weights
   float* zbar = wsl + n;                          // [r]
   __shared__ float red[32];
@@ -686,7 +598,7 @@ __global__ void __launch_bounds__(128) lrkv_decode_combine_kernel(const DecodePl
 
   float mloc = -INFINITY;
   for (int i = tid; i < n; i += blockDim.x)
-    mloc = fmaxf(mloc, P.part_ml[(static_cast<size_t>(b + c0 + i) * H + h) * 2]);
+    mloc = fmaxf(mloc, P.part_ml[((s0 + i) * H + h) * 2]);
   for (int off = 16; off > 0; off >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, off));
   if ((tid & 31) == 0) red[tid >> 5] = mloc;
   __syncthreads();
@@ -699,8 +611,8 @@ __global__ void __launch_bounds__(128) lrkv_decode_combine_kernel(const DecodePl
   const float M = s_M;
   float lloc = 0.f;
   for (int i = tid; i < n; i += blockDim.x) {
-    const size_t sl = (static_cast<size_t>(b + c0 + i) * H + h) * 2;
-    const float wgt = exp2f(P.part_ml[sl] - M);
+    const size_t sl = ((s0 + i) * H + h) * 2;
+    const float wgt = P.part_ml[sl] == -INFINITY ? 0.f : exp2f(P.part_ml[sl] - M);
     wsl[i] = wgt;
     lloc += wgt * P.part_ml[sl + 1];
   }
@@ -718,10 +630,14 @@ __global__ void __launch_bounds__(128) lrkv_decode_combine_kernel(const DecodePl
   const int width = dh + r;
   float oshared[2] = {0.f, 0.f};
   for (int j = tid; j < width; j += blockDim.x) {
-    float a = 0.f;
-    for (int i = 0; i < n; ++i)
-      a = fmaf(wsl[i], P.part_acc[(static_cast<size_t>(b + c0 + i) * H + h) * width + j], a);
-    a *= inv_l;
+    float a0 = 0.f, a1 = 0.f;
+    int i = 0;
+    for (; i + 1 < n; i += 2) {
+      a0 = fmaf(wsl[i], P.part_acc[((s0 + i) * H + h) * width + j], a0);
+      a1 = fmaf(wsl[i + 1], P.part_acc[((s0 + i + 1) * H + h) * width + j], a1);
+    }
+    if (i < n) a0 = fmaf(wsl[i], P.part_acc[((s0 + i) * H + h) * width + j], a0);
+    const float a = (a0 + a1) * inv_l;
     if (j < dh) oshared[j / blockDim.x] = a; else zbar[j - dh] = a;
   }
   __syncthreads();
@@ -742,70 +658,82 @@ int env_int(const char* name, int dflt) {
   return (v && *v) ? std::atoi(v) : dflt;
 }
 
-template <bool BF16, int RMAX>
-lrkv_status launch_split(const DecodePlan& P, cudaStream_t stream) {
-  auto kern = lrkv_decode_split_kernel<BF16, RMAX>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P.smem_bytes) != cudaSuccess)
-    return LRKV_ERR_CUDA;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(P.grid);
-  cfg.blockDim = dim3(P.nthreads);
-  cfg.dynamicSmemBytes = P.smem_bytes;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, P) == cudaSuccess ? LRKV_OK : LRKV_ERR_CUDA;
+using SplitFn = void (*)(const DecodePlan, const CUtensorMap, const CUtensorMap);
+
+SplitFn split_fn(const DecodePlan& P) {
+  const int rmax = P.r <= 16 ? 16 : P.r <= 32 ? 32 : 64;
+  if (P.bf16) {
+    if (P.vec == 8) {
+      if (rmax == 16) return lrkv_decode_split_kernel<true, 16, 8>;
+      if (rmax == 32) return lrkv_decode_split_kernel<true, 32, 8>;
+      return lrkv_decode_split_kernel<true, 64, 8>;
+    }
+    if (rmax == 16) return lrkv_decode_split_kernel<true, 16, 4>;
+    if (rmax == 32) return lrkv_decode_split_kernel<true, 32, 4>;
+    return lrkv_decode_split_kernel<true, 64, 4>;
+  }
+  if (rmax == 16) return lrkv_decode_split_kernel<false, 16, 4>;
+  if (rmax == 32) return lrkv_decode_split_kernel<false, 32, 4>;
+  return lrkv_decode_split_kernel<false, 64, 4>;
 }
 
 template <bool BF16>
-lrkv_status launch_all(const DecodePlan& P, cudaStream_t stream) {
-  lrkv_decode_absorb_kernel<BF16><<<dim3(P.H, P.B), 128, 0, stream>>>(P);
+lrkv_status launch_all(const DecodePlan& P, cudaStream_t stream, cudaEvent_t ev_begin, cudaEvent_t ev_end) {
+  const bool pdl = ev_begin == nullptr && ev_end == nullptr;
+  CUtensorMap tm_k, tm_v;
+  std::memset(&tm_k, 0, sizeof(tm_k));
+  std::memset(&tm_v, 0, sizeof(tm_v));
+  if (BF16) {
+    const CUtensorMapSwizzle sw = P.span == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : P.span == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                 : CU_TENSOR_MAP_SWIZZLE_32B;
+    if (!make_tmap_3d_bf16(&tm_k, P.k_s, P.dh, P.max_len, P.B, P.box_cols, P.T, sw) ||
+        !make_tmap_3d_bf16(&tm_v, P.v_s, P.dh, P.max_len, P.B, P.box_cols, P.T, sw))
+      return LRKV_ERR_CUDA;
+  }
+  const int absorb_smem = std::max(P.dh * P.r * 4, 16);
+  if (absorb_smem > 48 * 1024 &&
+      cudaFuncSetAttribute(lrkv_decode_absorb_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           absorb_smem) != cudaSuccess)
+    return LRKV_ERR_CUDA;
+  lrkv_decode_absorb_kernel<BF16><<<P.H, 256, absorb_smem, stream>>>(P);
   if (cudaGetLastError() != cudaSuccess) return LRKV_ERR_CUDA;
-  lrkv_status st;
-  if (P.r <= 16) st = launch_split<BF16, 16>(P, stream);
-  else if (P.r <= 32) st = launch_split<BF16, 32>(P, stream);
-  else st = launch_split<BF16, 64>(P, stream);
-  if (st != LRKV_OK) return st;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(P.H, P.B);
-  cfg.blockDim = dim3(128);
-  cfg.dynamicSmemBytes = P.combine_smem;
-  cfg.stream = stream;
+  if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return LRKV_ERR_CUDA;
+
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  if (P.stream) {
+    const lrkv_status st = stream_launch(P, stream, pdl, tm_k, tm_v);
+    if (st != LRKV_OK) return st;
+  } else {
+    const SplitFn kern = split_fn(P);
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P.smem_bytes) != cudaSuccess)
+      return LRKV_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(P.grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = P.smem_bytes;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    if (cudaLaunchKernelEx(&cfg, kern, P, tm_k, tm_v) != cudaSuccess) return LRKV_ERR_CUDA;
+  }
+  if (ev_end && cudaEventRecord(ev_end, stream) != cudaSuccess) return LRKV_ERR_CUDA;
+
+  cudaLaunchConfig_t ccfg = {};
+  ccfg.gridDim = dim3(P.H, P.B);
+  ccfg.blockDim = dim3(128);
+  ccfg.dynamicSmemBytes = P.combine_smem;
+  ccfg.stream = stream;
+  ccfg.attrs = attr;
+  ccfg.numAttrs = pdl ? 1 : 0;
   if (P.combine_smem > 48 * 1024 &&
       cudaFuncSetAttribute(lrkv_decode_combine_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            P.combine_smem) != cudaSuccess)
     return LRKV_ERR_CUDA;
-  if (cudaLaunchKernelEx(&cfg, lrkv_decode_combine_kernel<BF16>, P) != cudaSuccess) return LRKV_ERR_CUDA;
+  if (cudaLaunchKernelEx(&ccfg, lrkv_decode_combine_kernel<BF16>, P) != cudaSuccess) return LRKV_ERR_CUDA;
   return LRKV_OK;
-}
-
-template <bool BF16, int RMAX>
-lrkv_status occupancy_of(const DecodePlan& P, int* occ) {
-  auto kern = lrkv_decode_split_kernel<BF16, RMAX>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P.smem_bytes) != cudaSuccess)
-    return LRKV_ERR_CUDA;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, kern, P.nthreads, P.smem_bytes) == cudaSuccess
-             ? LRKV_OK
-             : LRKV_ERR_CUDA;
-}
-
-lrkv_status split_occupancy(const DecodePlan& P, int* occ) {
-  if (P.bf16) {
-    if (P.r <= 16) return occupancy_of<true, 16>(P, occ);
-    if (P.r <= 32) return occupancy_of<true, 32>(P, occ);
-    return occupancy_of<true, 64>(P, occ);
-  }
-  if (P.r <= 16) return occupancy_of<false, 16>(P, occ);
-  if (P.r <= 32) return occupancy_of<false, 32>(P, occ);
-  return occupancy_of<false, 64>(P, occ);
 }
 
 }  // namespace
@@ -818,99 +746,83 @@ lrkv_status decode_make_plan(const lrkv_dims& d, int num_sms, DecodePlan& P, siz
   P.bf16 = d.dtype == LRKV_BF16;
   P.esz = P.bf16 ? 2 : 4;
   const int H = P.H, dh = P.dh, r = P.r;
+  if (r % 4 != 0) return LRKV_ERR_UNSUPPORTED;
+  if (H > kThreads) return LRKV_ERR_UNSUPPORTED;
 
-  // lanes per head: as many as fit 256 threads, at most a warp
-  int lph = 32;
-  while (lph > 1 && H * lph > kMaxThreads) lph >>= 1;
-  if (H * lph > kMaxThreads) return LRKV_ERR_UNSUPPORTED;
-  P.lph = lph;
-  P.nthreads = std::max(128, round_up(H * lph, 32));
-  if (P.nthreads > kMaxThreads) return LRKV_ERR_UNSUPPORTED;
-  const int nwarps = P.nthreads / 32;
-
-  P.ks_row = dh * P.esz;
-  P.z_row = H * r * P.esz;
-  P.ks_stride = odd_chunk_stride(P.ks_row);
-  P.z_stride = r > 0 ? odd_chunk_stride(P.z_row) : 0;
-  const int per_token = 2 * (P.ks_stride + P.z_stride);
-
-  if (P.bf16) {
-    P.vec = (r % 8 == 0) ? 8 : (r % 4 == 0) ? 4 : (r % 2 == 0) ? 2 : 1;
-    P.Hp = round_up(H, 16);
+  // value columns per thread: every (head, column group) pair owns cw columns
+  const int vw = P.bf16 ? r : dh + r;
+  P.vec = P.bf16 ? ((r % 8 == 0) ? 8 : 4) : 4;
+  const int max_groups = kThreads / H;
+  P.ntg = max_groups;
+  if (vw == 0) {
+    P.cw = P.vec;
+    P.nrg = 1;
   } else {
-    P.vec = (r % 4 == 0) ? 4 : (r % 2 == 0) ? 2 : 1;
-    P.Hp = H;
+    int cw = P.vec;
+    while (cw <= kMaxCW && (vw + cw - 1) / cw > max_groups) cw += P.vec;
+    if (cw > kMaxCW) return LRKV_ERR_UNSUPPORTED;
+    P.cw = cw;
+    P.nrg = (vw + cw - 1) / cw;
   }
-  if (r == 0) P.vec = 1;
 
-  // tile: T = ppt * lph tokens, a multiple of 8, about 48 KB of rows per stage
-  const int stage_target = env_int("LRKV_DECODE_STAGE_KB", 48) * 1024;
-  int best = 0;
-  for (int ppt = 1; ppt <= kMaxPPT; ppt *= 2) {
-    const int T = ppt * lph;
-    if (T % 8 != 0 || T > 64) continue;
-    if (best == 0 || T * per_token <= stage_target) best = T;
-  }
+  // tile: T tokens, a multiple of 8, at most kMaxTile, about `target` bytes
+  const int z_row = H * r * P.esz;
+  P.z_row = z_row;
+  const int per_token = 2 * dh * P.esz + 2 * z_row;
+  const int target = env_int("LRKV_DECODE_STAGE_KB", 56) * 1024;
+  int T = 8;
+  while (T * 2 <= kMaxTile && T * 2 * per_token <= target && T * 2 <= kMaxPPT * P.ntg) T *= 2;
   const int forced_T = env_int("LRKV_DECODE_TILE", 0);
-  if (forced_T > 0 && forced_T % lph == 0 && forced_T % 8 == 0 && forced_T / lph <= kMaxPPT) best = forced_T;
-  if (best == 0) return LRKV_ERR_UNSUPPORTED;
-  P.T = best;
-  P.ppt = P.T / lph;
+  if (forced_T >= 8 && forced_T <= kMaxTile && forced_T % 8 == 0) T = forced_T;
+  if (T > kMaxPPT * P.ntg) return LRKV_ERR_UNSUPPORTED;
+  P.T = T;
 
   if (P.bf16) {
+    if (dh % 16 != 0) return LRKV_ERR_UNSUPPORTED;
+    P.Hp = round_up(H, 16);
     const int mt = P.Hp / 16;
-    const int ltiles = mt * (P.T / 8);
-    const int ksteps = dh / 16;
-    P.ksplit = 1;
-    for (int k = ksteps; k >= 1; --k)
-      if (ksteps % k == 0 && ltiles * k <= nwarps) { P.ksplit = k; break; }
-    if (mt * (dh / 8) > kMaxValueTiles * nwarps) return LRKV_ERR_UNSUPPORTED;
+    if (mt * (dh / 8) > kMaxValueTiles * (kThreads / 32)) return LRKV_ERR_UNSUPPORTED;
+    const int row_bytes = dh * 2;
+    P.span = row_bytes >= 128 ? 128 : row_bytes >= 64 ? 64 : 32;
+    if (row_bytes % P.span != 0) return LRKV_ERR_UNSUPPORTED;
+    P.box_cols = P.span / 2;
+    P.nbox = dh / P.box_cols;
+    P.kv_bytes = round_up(T * dh * 2, 1024);
     P.q_stride = dh + 8;
-    P.w_stride = ((P.T / 8) & 1) ? P.T : P.T + 8;
+    P.w_stride = ((T / 8) & 1) ? T : T + 8;
   } else {
-    if (dh > kMaxValueTiles * 4 * lph) return LRKV_ERR_UNSUPPORTED;
-    P.ksplit = 0;
+    P.Hp = H;
+    P.kv_bytes = round_up(T * dh * 4, 1024);
     P.q_stride = ((dh / 4) & 1) ? dh : dh + 4;
-    P.w_stride = P.T;
+    P.w_stride = T;
   }
-  {
-    const int r4 = round_up(std::max(r, 1), 4);
-    P.p_stride = ((r4 / 4) & 1) ? r4 : r4 + 4;
-  }
+  P.z_bytes = round_up(std::max(T * z_row, 16), 1024);
+  P.s_stride = P.Hp + 1;
 
   // shared-memory carve-up
   int off = 64;  // mbarriers
   P.off_prefix = off; off = round_up(off + (P.B + 1) * 4, 16);
   P.off_q = off; off = round_up(off + P.Hp * P.q_stride * P.esz, 16);
-  P.off_p = off; off = round_up(off + H * P.p_stride * 4, 16);
-  P.off_s = off; off = round_up(off + (P.bf16 ? P.ksplit * P.Hp * P.T * 4 : 0), 16);
-  P.off_w = off; off = round_up(off + P.Hp * P.w_stride * P.esz, 16);
-  P.off_alpha = off; off = round_up(off + P.Hp * 4, 128);
+  P.off_ssh = off; off = round_up(off + (P.bf16 ? T * P.s_stride * 4 : 0), 16);
+  P.off_sp = off; off = round_up(off + T * P.s_stride * 4, 16);  // fp32 weights
+  P.off_w = off; off = round_up(off + (P.bf16 ? P.Hp * P.w_stride * 2 : 0), 16);
+  P.off_alpha = off; off = round_up(off + P.Hp * 4, 16);
+  P.off_red = off; off = round_up(off + P.ntg * H * 4, 1024);
   P.off_stage = off;
-  P.stage_bytes = round_up(P.T * per_token, 128);
-  // Two CTAs per SM when at least two stages fit in half the SM's shared
-  // memory (independent CTAs overlap one another's barriers); else one CTA
-  // with a deeper ring.
-  const int max_stages = env_int("LRKV_DECODE_STAGES", 4);
-  const int want_cps = env_int("LRKV_DECODE_CTAS_PER_SM", 0);
-  int cps = 0, stages = 0;
-  for (int try_cps = 2; try_cps >= 1; --try_cps) {
-    if (want_cps > 0 && try_cps != want_cps) continue;
-    const int budget = (try_cps == 2 ? 113 : 227) * 1024 - off;
-    const int st = std::min(max_stages, budget / P.stage_bytes);
-    if (st >= 2) { cps = try_cps; stages = st; break; }
-  }
+  P.stage_bytes = 2 * P.kv_bytes + 2 * P.z_bytes;
+  const int max_stages = std::min(8, env_int("LRKV_DECODE_STAGES", 6));
+  const int stages = std::min(max_stages, (227 * 1024 - 1024 - off) / P.stage_bytes);
   if (stages < 2) return LRKV_ERR_UNSUPPORTED;
   P.stages = stages;
-  P.smem_bytes = off + stages * P.stage_bytes;
-  // resident CTAs per SM as the hardware will actually schedule them
-  // (registers may allow fewer than shared memory does)
-  int occ = cps;
-  if (split_occupancy(P, &occ) != LRKV_OK) return LRKV_ERR_CUDA;
-  P.grid = env_int("LRKV_DECODE_GRID", num_sms * std::max(1, std::min(occ, cps)));
-  P.min_tokens = env_int("LRKV_DECODE_MIN_TOKENS", 2 * P.T);
-  const int slots = P.B + P.grid;
-  P.combine_smem = (P.grid + 1 + r) * 4;
+  P.smem_bytes = off + stages * P.stage_bytes + 1024;  // + alignment slack
+  P.ngw = 1;
+  // bf16 shapes the streaming kernel covers use it; the rest (and fp32) run
+  // the tile-synchronous kernel planned above
+  if (P.bf16 && env_int("LRKV_DECODE_TILE_SYNC", 0) == 0) stream_plan(P);
+  P.grid = env_int("LRKV_DECODE_GRID", num_sms);
+  P.min_tokens = env_int("LRKV_DECODE_MIN_TOKENS", P.stream ? 8 * P.T : 2 * P.T);
+  const int slots = (P.B + P.grid) * P.ngw;
+  P.combine_smem = ((P.grid + 1) * P.ngw + r) * 4;
 
   // workspace: status | meta | prefix | p | part_ml | part_acc
   size_t w = 256;
@@ -935,14 +847,15 @@ void decode_bind_workspace(DecodePlan& P, void* ws) {
   off += static_cast<size_t>(P.B) * P.H * std::max(P.r, 1) * 4;
   off = (off + 255) / 256 * 256;
   P.part_ml = reinterpret_cast<float*>(base + off);
-  off += static_cast<size_t>(P.B + P.grid) * P.H * 2 * 4;
+  off += static_cast<size_t>(P.B + P.grid) * P.ngw * P.H * 2 * 4;
   off = (off + 255) / 256 * 256;
   P.part_acc = reinterpret_cast<float*>(base + off);
 }
 
-lrkv_status decode_launch(const DecodePlan& P, void* stream) {
+lrkv_status decode_launch(const DecodePlan& P, void* stream, void* ev_begin, void* ev_end) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return P.bf16 ? launch_all<true>(P, s) : launch_all<false>(P, s);
+  cudaEvent_t e0 = static_cast<cudaEvent_t>(ev_begin), e1 = static_cast<cudaEvent_t>(ev_end);
+  return P.bf16 ? launch_all<true>(P, s, e0, e1) : launch_all<false>(P, s, e0, e1);
 }
 
 }  // namespace lrkv

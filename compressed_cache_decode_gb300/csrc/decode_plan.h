@@ -5,15 +5,18 @@
 #include <stddef.h>
 #include <stdint.h>
 
-#include "../../include/lrkv.h"
+#include "lrkv.h"
 
 namespace lrkv {
 
-constexpr int kMaxBatch = 4096;   // sequence-start prefix lives in shared memory
-constexpr int kMaxRank = 64;      // private accumulators live in registers
-constexpr int kMaxPPT = 4;        // tokens per lane per tile
-constexpr int kMaxValueTiles = 4; // value-MMA accumulator tiles per warp (bf16)
-constexpr int kMaxThreads = 256;
+constexpr int kMaxBatch = 4096;  // sequence-start prefix lives in shared memory
+constexpr int kMaxRank = 64;     // q_h B_h^K of a head lives in registers
+constexpr int kMaxTile = 32;     // a tile's scores of one head live in registers
+constexpr int kMaxPPT = 4;       // tokens per thread in the private-score phase
+constexpr int kMaxCW = 16;       // value columns per thread
+constexpr int kMaxValueTiles = 4;  // value-MMA accumulator tiles per warp (bf16)
+constexpr int kThreads = 256;
+constexpr int kStreamConsumers = 8;  // consumer warps of the streaming kernel
 
 // Bits of the device status word (first 4 bytes of a workspace).
 constexpr uint32_t kDevTimeout = 1u;  // a bounded wait ran out
@@ -25,26 +28,39 @@ struct DecodePlan {
   float scale_log2;  // scale * log2(e): scores live in the base-2 domain
   int bf16;          // storage dtype
   int esz;           // bytes per stored element
-  // tiling
+  // tiling and thread roles
   int T;             // tokens per tile
-  int lph;           // lanes per head (power of two <= 32)
-  int ppt;           // tokens per lane per tile (T / lph)
-  int nthreads;      // split-kernel block size
+  int ntg;           // token groups in the private-score phase (thread = head x group)
+  int nrg;           // column groups in the value phase (thread = head x group)
+  int cw;            // value columns per thread
+  int vec;           // elements per latent vector load
   int stages;        // TMA ring depth
   int grid;          // split CTAs launched (upper bound of the CTAs used)
   int min_tokens;    // a split CTA gets at least this many tokens
   int Hp;            // heads padded to 16 (bf16 MMA rows)
-  int ksplit;        // K-split of the logits MMA over warps
-  int vec;           // elements per private-latent load
-  // bytes copied per token row, and padded shared-memory row strides
-  int ks_row, z_row, ks_stride, z_stride;
-  int q_stride;      // elements
-  int p_stride;      // floats
-  int w_stride;      // elements of the W (attention weight) tile
+  int span;          // bf16: swizzle span (bytes) of one k_s/v_s box row
+  int box_cols;      // bf16: elements per box row
+  int nbox;          // bf16: boxes per token row
+  int kv_bytes;      // shared bytes of one k_s (or v_s) tile
+  int z_row;         // bytes of one token's latents (H r esz)
+  int z_bytes;       // shared bytes of one latent tile
+  int q_stride;      // elements per q row in shared memory
+  int s_stride;      // floats per token row of the score tiles
+  int w_stride;      // bf16 elements per head row of the weight tile
   // shared-memory carve-up (bytes from the dynamic base)
-  int off_prefix, off_q, off_p, off_s, off_w, off_alpha, off_stage;
+  int off_prefix, off_q, off_ssh, off_sp, off_w, off_alpha, off_red, off_stage;
   int stage_bytes, smem_bytes;
   int combine_smem;
+  // bf16 streaming kernel (warp-independent): consumer warps form `ng` groups
+  // of `mt` warps (one warp per 16-head MMA tile); tile i goes to stage
+  // i % stages and to group i % ng.  `ngw` partials per piece are written
+  // (1 when the groups merge on chip, else ng).
+  int stream;        // 1: bf16 streaming kernel, 0: fp32 tile-synchronous kernel
+  int nthreads;      // block size of the scan kernel
+  int ng, mt, ngw, merge_smem;
+  int zs_stride;     // padded shared stride of one token's latents (bytes)
+  int p_stride;      // floats per row of q_h B_h^K in shared memory
+  int off_p, off_scr, off_merge, off_kv, off_z;
   // workspace carve-up
   uint32_t* status;
   int* meta;         // [0] = total tokens N, [1] = CTAs used
@@ -68,6 +84,6 @@ struct DecodePlan {
 // Fills everything but the operand pointers; returns the workspace size.
 lrkv_status decode_make_plan(const lrkv_dims& d, int num_sms, DecodePlan& P, size_t* ws_bytes);
 void decode_bind_workspace(DecodePlan& P, void* ws);
-lrkv_status decode_launch(const DecodePlan& P, void* stream);
+lrkv_status decode_launch(const DecodePlan& P, void* stream, void* ev_begin = nullptr, void* ev_end = nullptr);
 
 }  // namespace lrkv

@@ -5,7 +5,7 @@
 
 #include <cstdint>
 
-#include "../../include/lrkv.h"
+#include "lrkv.h"
 #include "decode_plan.h"
 
 namespace {
@@ -71,10 +71,14 @@ lrkv_status lrkv_decode_workspace_size(const lrkv_dims* dims, size_t* bytes) {
   return lrkv::decode_make_plan(*dims, sms, P, bytes);
 }
 
-lrkv_status lrkv_decode(const lrkv_dims* dims, const void* q, const void* k_s, const void* v_s,
-                        const void* z_k, const void* z_v, const void* b_k, const void* b_v,
-                        const int32_t* seq_lens, float* out, float* lse, void* ws, size_t ws_bytes,
-                        lrkv_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+lrkv_status decode_common(const lrkv_dims* dims, const void* q, const void* k_s, const void* v_s,
+                          const void* z_k, const void* z_v, const void* b_k, const void* b_v,
+                          const int32_t* seq_lens, float* out, float* lse, void* ws, size_t ws_bytes,
+                          lrkv_stream_t stream, void* ev_begin, void* ev_end) {
   lrkv_status st = check_decode_dims(dims);
   if (st != LRKV_OK) return st;
   if (!q || !k_s || !v_s || !seq_lens || !out) return LRKV_ERR_INVALID_ARG;
@@ -92,7 +96,29 @@ lrkv_status lrkv_decode(const lrkv_dims* dims, const void* q, const void* k_s, c
   lrkv::decode_bind_workspace(P, ws);
   P.q = q; P.k_s = k_s; P.v_s = v_s; P.z_k = z_k; P.z_v = z_v; P.b_k = b_k; P.b_v = b_v;
   P.seq_lens = seq_lens; P.out = out; P.lse = lse;
-  return lrkv::decode_launch(P, stream);
+  return lrkv::decode_launch(P, stream, ev_begin, ev_end);
+}
+
+}  // namespace
+
+extern "C" {
+
+lrkv_status lrkv_decode(const lrkv_dims* dims, const void* q, const void* k_s, const void* v_s,
+                        const void* z_k, const void* z_v, const void* b_k, const void* b_v,
+                        const int32_t* seq_lens, float* out, float* lse, void* ws, size_t ws_bytes,
+                        lrkv_stream_t stream) {
+  return decode_common(dims, q, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens, out, lse, ws, ws_bytes, stream,
+                       nullptr, nullptr);
+}
+
+lrkv_status lrkv_decode_profiled(const lrkv_dims* dims, const void* q, const void* k_s, const void* v_s,
+                                 const void* z_k, const void* z_v, const void* b_k, const void* b_v,
+                                 const int32_t* seq_lens, float* out, float* lse, void* ws,
+                                 size_t ws_bytes, lrkv_stream_t stream, void* ev_split_begin,
+                                 void* ev_split_end) {
+  if (!ev_split_begin || !ev_split_end) return LRKV_ERR_INVALID_ARG;
+  return decode_common(dims, q, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens, out, lse, ws, ws_bytes, stream,
+                       ev_split_begin, ev_split_end);
 }
 
 lrkv_status lrkv_read_device_status(const void* ws, lrkv_stream_t stream, lrkv_status* out_status) {

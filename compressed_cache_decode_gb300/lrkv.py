@@ -34,6 +34,7 @@ EXPORTED = (
     "lrkv_cache_elems_per_token",
     "lrkv_decode_workspace_size",
     "lrkv_decode",
+    "lrkv_decode_profiled",
     "lrkv_read_device_status",
 )
 
@@ -82,6 +83,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.lrkv_decode_workspace_size.argtypes = [dims_p, ctypes.POINTER(sz)]
     lib.lrkv_decode.restype = ctypes.c_int
     lib.lrkv_decode.argtypes = [dims_p, vp, vp, vp, vp, vp, vp, vp, i32p, vp, vp, vp, sz, vp]
+    lib.lrkv_decode_profiled.restype = ctypes.c_int
+    lib.lrkv_decode_profiled.argtypes = [dims_p, vp, vp, vp, vp, vp, vp, vp, i32p, vp, vp, vp, sz, vp,
+                                         vp, vp]
     lib.lrkv_read_device_status.restype = ctypes.c_int
     lib.lrkv_read_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
     if path is None:
@@ -134,6 +138,19 @@ def lrkv_decode(dims: lrkv_dims, q, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens, out,
     return int(load().lrkv_decode(ctypes.byref(dims), _ptr(q), _ptr(k_s), _ptr(v_s), _ptr(z_k),
                                   _ptr(z_v), _ptr(b_k), _ptr(b_v), _ptr(seq_lens), _ptr(out),
                                   _ptr(lse), _ptr(ws), ws_bytes, _stream_handle(stream)))
+
+
+def lrkv_decode_profiled(dims: lrkv_dims, q, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens, out, lse, ws,
+                         ws_bytes: int, ev_begin: "torch.cuda.Event", ev_end: "torch.cuda.Event",
+                         stream=None) -> int:
+    """lrkv_decode with CUDA events recorded around the split-KV kernel."""
+    for ev in (ev_begin, ev_end):
+        if not ev.cuda_event:  # torch creates the CUDA event on its first record
+            ev.record(torch.cuda.current_stream() if stream is None else stream)
+    return int(load().lrkv_decode_profiled(
+        ctypes.byref(dims), _ptr(q), _ptr(k_s), _ptr(v_s), _ptr(z_k), _ptr(z_v), _ptr(b_k),
+        _ptr(b_v), _ptr(seq_lens), _ptr(out), _ptr(lse), _ptr(ws), ws_bytes,
+        _stream_handle(stream), ev_begin.cuda_event, ev_end.cuda_event))
 
 
 def lrkv_read_device_status(ws: torch.Tensor, stream=None) -> int:

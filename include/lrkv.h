@@ -127,6 +127,20 @@ lrkv_status lrkv_decode(const lrkv_dims* dims, const void* q, const void* k_s, c
                         lrkv_stream_t stream);
 
 /*
+ * lrkv_decode, plus two CUDA events (cudaEvent_t passed as void*, created by
+ * the caller) recorded on `stream` immediately before and after the split-KV
+ * kernel, the HBM-bound scan that dominates a decode step.  Used to time that
+ * kernel alone; with the events in place the three kernels of the step run
+ * strictly one after another instead of overlapping their launch.  Both
+ * events are required (LRKV_ERR_INVALID_ARG otherwise).
+ */
+lrkv_status lrkv_decode_profiled(const lrkv_dims* dims, const void* q, const void* k_s,
+                                 const void* v_s, const void* z_k, const void* z_v, const void* b_k,
+                                 const void* b_v, const int32_t* seq_lens, float* out, float* lse,
+                                 void* ws, size_t ws_bytes, lrkv_stream_t stream,
+                                 void* ev_split_begin, void* ev_split_end);
+
+/*
  * Read the device status word that the kernels of the last call(s) using
  * `ws` recorded (LRKV_OK, LRKV_ERR_TIMEOUT or LRKV_ERR_DEVICE_BOUNDS).
  * Synchronises `stream`.  Each lrkv_decode/lrkv_prefill call resets the word
