@@ -196,14 +196,17 @@ __global__ void __launch_bounds__(32 * kStreamConsumers, 1)
   }
   __syncthreads();
 
-  // ---- first `stages` tiles, issued by warp 0 ------------------------------
-  if (warp == 0) {
-    TileCursor cur;
-    cur.more = piece_first(cur.pc, pre, B, g0, g1);
-    cur.ibase = 0;
-    for (int j = 0; j < P.stages && cur.seek(j, pre, B, g1); ++j) {
-      const int t0 = cur.pc.t_beg + (j - cur.ibase) * kT;
-      stream_issue(P, &tm_k, &tm_v, smem, full, j, cur.pc.b, t0, min(kT, cur.pc.t_end - t0), lane);
+  // ---- first `stages` tiles: each group issues the ones it will consume ----
+  {
+    const int gi0 = warp / P.mt;
+    if (warp % P.mt == 0) {
+      TileCursor cur;
+      cur.more = piece_first(cur.pc, pre, B, g0, g1);
+      cur.ibase = 0;
+      for (int j = gi0; j < P.stages && cur.seek(j, pre, B, g1); j += P.ng) {
+        const int t0 = cur.pc.t_beg + (j - cur.ibase) * kT;
+        stream_issue(P, &tm_k, &tm_v, smem, full, j, cur.pc.b, t0, min(kT, cur.pc.t_end - t0), lane);
+      }
     }
   }
 
