@@ -35,6 +35,7 @@ EXPORTED = (
     "lrkv_decode_workspace_size",
     "lrkv_decode",
     "lrkv_decode_profiled",
+    "lrkv_decode_static_scratch",
     "lrkv_read_device_status",
 )
 
@@ -86,6 +87,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.lrkv_decode_profiled.restype = ctypes.c_int
     lib.lrkv_decode_profiled.argtypes = [dims_p, vp, vp, vp, vp, vp, vp, vp, i32p, vp, vp, vp, sz, vp,
                                          vp, vp]
+    lib.lrkv_decode_static_scratch.restype = ctypes.c_int
+    lib.lrkv_decode_static_scratch.argtypes = [dims_p, vp, vp, vp, vp, vp, vp, vp, i32p, vp, vp, vp]
     lib.lrkv_read_device_status.restype = ctypes.c_int
     lib.lrkv_read_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
     if path is None:
@@ -151,6 +154,16 @@ def lrkv_decode_profiled(dims: lrkv_dims, q, k_s, v_s, z_k, z_v, b_k, b_v, seq_l
         ctypes.byref(dims), _ptr(q), _ptr(k_s), _ptr(v_s), _ptr(z_k), _ptr(z_v), _ptr(b_k),
         _ptr(b_v), _ptr(seq_lens), _ptr(out), _ptr(lse), _ptr(ws), ws_bytes,
         _stream_handle(stream), ev_begin.cuda_event, ev_end.cuda_event))
+
+
+def lrkv_decode_static_scratch(dims: lrkv_dims, q, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens, out,
+                               lse, stream=None) -> int:
+    """lrkv_decode with the workspace taken from the array built into the
+    library (for callers that cannot allocate device memory); returns the
+    status code."""
+    return int(load().lrkv_decode_static_scratch(
+        ctypes.byref(dims), _ptr(q), _ptr(k_s), _ptr(v_s), _ptr(z_k), _ptr(z_v), _ptr(b_k),
+        _ptr(b_v), _ptr(seq_lens), _ptr(out), _ptr(lse), _stream_handle(stream)))
 
 
 def lrkv_read_device_status(ws: torch.Tensor, stream=None) -> int:

@@ -141,6 +141,40 @@ lrkv_status lrkv_decode_profiled(const lrkv_dims* dims, const void* q, const voi
                                  void* ev_split_begin, void* ev_split_end);
 
 /*
+ * Size of the workspace array built into the library for
+ * lrkv_decode_static_scratch: 16 MiB of device memory on every GPU that loads
+ * the library, held until the process exits.
+ */
+#define LRKV_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/*
+ * lrkv_decode for callers that cannot allocate device memory.  The LRKV pages
+ * have no counterpart of this entry point: it only changes where the decode
+ * workspace comes from.
+ *
+ * Some callers cannot hand lrkv_decode a workspace: a plugin inside a host
+ * runtime that owns all device memory through its own pool, or a serving path
+ * that must not allocate (and so possibly synchronise or fail) in the middle
+ * of a request.  This call takes the workspace from a fixed array of
+ * LRKV_STATIC_SCRATCH_BYTES compiled into the library and allocates nothing
+ * (no cudaMalloc, cudaFree or allocating library routine).  Arguments and
+ * results are those of lrkv_decode, without ws/ws_bytes.
+ *
+ *  * Shapes whose workspace (lrkv_decode_workspace_size) exceeds
+ *    LRKV_STATIC_SCRATCH_BYTES return LRKV_ERR_WORKSPACE and enqueue nothing.
+ *  * The first call on a device looks up the array's device address with the
+ *    device current; make that first call before any stream capture.
+ *  * All calls on a device share the array and it keeps the last call's
+ *    contents; nothing in it has to start at zero.  Calls whose kernels
+ *    overlap on the GPU (unordered streams) race on it.
+ *  * The device status word lives in that array and cannot be read back.
+ */
+lrkv_status lrkv_decode_static_scratch(const lrkv_dims* dims, const void* q, const void* k_s,
+                                       const void* v_s, const void* z_k, const void* z_v,
+                                       const void* b_k, const void* b_v, const int32_t* seq_lens,
+                                       float* out, float* lse, lrkv_stream_t stream);
+
+/*
  * Read the device status word that the kernels of the last call(s) using
  * `ws` recorded (LRKV_OK, LRKV_ERR_TIMEOUT or LRKV_ERR_DEVICE_BOUNDS).
  * Synchronises `stream`.  Each lrkv_decode/lrkv_prefill call resets the word
