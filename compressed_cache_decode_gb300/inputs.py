@@ -12,7 +12,7 @@ Layouts (row-major, tokens contiguous per sequence):
   b_k, b_v [H, d_h, r]            per-head reconstruction bases B_h
   seq_lens [B] int32              visible history length per sequence
   x        [B, T, d]              layer input (append workload)
-  w_sk, w_sv [d, d_h]; u_k, u_v [d, H*r] (head-major columns)
+  w_sk, w_sv [d_h, d]; u_k, u_v [H*r, d] (output-major; row h*r+c = column c of U_h)
 
 Workloads mirror the shapes the LRKV pages discuss: head width 128, 16-32
 heads, ranks that keep the cache near half of MHA, and contexts from 4K to
@@ -124,7 +124,9 @@ def make_prefill_inputs(w: Workload, seed: int = 0, batch: Optional[int] = None,
 
     x ~ N(0,1); W_sK, W_sV, U^K, U^V ~ N(0, 1/d); B^K, B^V ~ N(0, 1/r); q ~ N(0,1)
     drawn directly (the workload gives no W^Q).  Draw order: x, W_sK, W_sV,
-    U^K, U^V, q, B^K, B^V.
+    U^K, U^V, q, B^K, B^V.  The projection weights are stored output-major
+    (w_sk [d_h, d], u_k [H*r, d], row h*r + c = column c of U_h), the layout
+    the append entry point reads.
     """
     B = batch if batch is not None else w.batch
     T = q_len if q_len is not None else w.q_len
@@ -133,10 +135,10 @@ def make_prefill_inputs(w: Workload, seed: int = 0, batch: Optional[int] = None,
     gen = torch.Generator().manual_seed(seed)
     wstd = 1.0 / math.sqrt(d)
     x = _normal(gen, (B, T, d))
-    w_sk = _normal(gen, (d, dh), wstd)
-    w_sv = _normal(gen, (d, dh), wstd)
-    u_k = _normal(gen, (d, H * r), wstd)
-    u_v = _normal(gen, (d, H * r), wstd)
+    w_sk = _normal(gen, (dh, d), wstd)
+    w_sv = _normal(gen, (dh, d), wstd)
+    u_k = _normal(gen, (H * r, d), wstd)
+    u_v = _normal(gen, (H * r, d), wstd)
     q = _normal(gen, (B, T, H, dh))
     bstd = 1.0 / math.sqrt(r) if r > 0 else 1.0
     b_k = _normal(gen, (H, dh, r), bstd)

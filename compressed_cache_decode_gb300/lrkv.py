@@ -36,6 +36,7 @@ EXPORTED = (
     "lrkv_decode",
     "lrkv_decode_profiled",
     "lrkv_decode_static_scratch",
+    "lrkv_append",
     "lrkv_read_device_status",
 )
 
@@ -89,6 +90,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                                          vp, vp]
     lib.lrkv_decode_static_scratch.restype = ctypes.c_int
     lib.lrkv_decode_static_scratch.argtypes = [dims_p, vp, vp, vp, vp, vp, vp, vp, i32p, vp, vp, vp]
+    lib.lrkv_append.restype = ctypes.c_int
+    lib.lrkv_append.argtypes = [dims_p, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, vp, i32p, vp, vp, vp,
+                                vp, vp, sz, vp]
     lib.lrkv_read_device_status.restype = ctypes.c_int
     lib.lrkv_read_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
     if path is None:
@@ -209,3 +213,29 @@ def decode(q: torch.Tensor, k_s: torch.Tensor, v_s: torch.Tensor, z_k: torch.Ten
     if st != LRKV_OK:
         raise LRKVError(st, "lrkv_decode")
     return out, lse
+
+
+def lrkv_append(dims: lrkv_dims, d_model: int, n_new: int, x, w_sk, w_sv, u_k, u_v, start_pos,
+                k_s, v_s, z_k, z_v, ws, ws_bytes: int, stream=None) -> int:
+    """Direct call of the append entry point; returns its status code."""
+    return int(load().lrkv_append(ctypes.byref(dims), d_model, n_new, _ptr(x), _ptr(w_sk),
+                                  _ptr(w_sv), _ptr(u_k), _ptr(u_v), _ptr(start_pos), _ptr(k_s),
+                                  _ptr(v_s), _ptr(z_k), _ptr(z_v), _ptr(ws), ws_bytes,
+                                  _stream_handle(stream)))
+
+
+def append(x: torch.Tensor, w_sk: torch.Tensor, w_sv: torch.Tensor, u_k: torch.Tensor,
+           u_v: torch.Tensor, start_pos: torch.Tensor, k_s: torch.Tensor, v_s: torch.Tensor,
+           z_k: torch.Tensor, z_v: torch.Tensor, stream=None) -> int:
+    """Append x [B, n_new, d] to the cache in place (weights output-major:
+    w_sk [d_h, d], u_k [H*r, d]).  Returns the device status word after a
+    synchronising read."""
+    B, n_new, d = x.shape
+    H, r = z_k.shape[2], z_k.shape[3]
+    dims = make_dims(B, H, k_s.shape[2], r, k_s.shape[1], x.dtype)
+    ws = torch.zeros(16, dtype=torch.uint8, device=x.device)
+    st = lrkv_append(dims, d, n_new, x, w_sk, w_sv, u_k, u_v, start_pos, k_s, v_s, z_k, z_v, ws,
+                     ws.numel(), stream)
+    if st != LRKV_OK:
+        raise LRKVError(st, "lrkv_append")
+    return lrkv_read_device_status(ws, stream)

@@ -175,6 +175,34 @@ lrkv_status lrkv_decode_static_scratch(const lrkv_dims* dims, const void* q, con
                                        float* out, float* lse, lrkv_stream_t stream);
 
 /*
+ * Append new tokens to the factored cache ("Low-Rank Key Value Attention |
+ * What a shared cache can preserve", §3, Algorithm 1; "Low-Rank Key Value
+ * Attention：中文研读笔记", §2.3): for every new token row x of sequence b,
+ *   k_s = x W_sK^T, v_s = x W_sV^T (d_h each), and for every head h
+ *   z_k,h = x U_h^K, z_v,h = x U_h^V (r each),
+ * stored at cache row start_pos[b] + t.  One GEMM on the tensor cores with
+ * fp32 accumulation; results rounded to bf16.
+ *
+ *   x          [batch][n_new][d_model]            layer input (bf16)
+ *   w_sk, w_sv [head_dim][d_model]                shared projections, stored
+ *                                                  output-major (row = output
+ *                                                  column, like a Linear weight)
+ *   u_k, u_v   [heads * rank][d_model]            per-head residual factors,
+ *                                                  output-major; row h*r + c is
+ *                                                  column c of U_h
+ *   start_pos  [batch] int32 (device)             first cache row written
+ *   k_s, v_s, z_k, z_v                            the cache (layouts above)
+ *   ws, ws_bytes >= 16                            device status word
+ * Supported: dtype BF16; d_model, head_dim and heads*rank multiples of 64.
+ * Rows with start_pos[b] + t outside [0, max_len) are not written and set
+ * LRKV_ERR_DEVICE_BOUNDS in the status word.
+ */
+lrkv_status lrkv_append(const lrkv_dims* dims, int d_model, int n_new, const void* x, const void* w_sk,
+                        const void* w_sv, const void* u_k, const void* u_v, const int32_t* start_pos,
+                        void* k_s, void* v_s, void* z_k, void* z_v, void* ws, size_t ws_bytes,
+                        lrkv_stream_t stream);
+
+/*
  * Read the device status word that the kernels of the last call(s) using
  * `ws` recorded (LRKV_OK, LRKV_ERR_TIMEOUT or LRKV_ERR_DEVICE_BOUNDS).
  * Synchronises `stream`.  Each lrkv_decode/lrkv_prefill call resets the word
