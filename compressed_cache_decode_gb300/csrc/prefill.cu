@@ -1,0 +1,494 @@
+// prefill.cu — causal attention of a block of queries against the factored
+// LRKV cache on the tensor cores (tcgen05 + TMEM + TMA, sm_103a).
+//
+// For a query row i of head h the logits are a dense contraction over the
+// concatenated [q_h | q_h B_h^K] . [k_s | z_k,h] (K = d_h + r), one causal
+// softmax, and the values [v_s | z_v,h] (N = d_h + r), finally lifted
+//   o_h = O_s / l + (O_z / l) (B_h^V)^T
+// ("Low-Rank Key Value Attention：中文研读笔记", §2.4, Eqs. (6)-(7); "Low-Rank
+// Key Value Attention | What a shared cache can preserve", §3).
+//
+// One CTA = (sequence b, head h, 128 query rows).  Warps 0-3 (one query row
+// per thread) run the softmax and the epilogue, warp 4 issues TMA, warp 5 one
+// thread issues every MMA:
+//   Pq   = Q B_h^K          (TMEM, then split into two bf16 parts, high and
+//                           low, in shared memory, so the latent scores keep
+//                           about 16 significant bits)
+//   S_j  = Q K_s,j^T + Pq Z_k,j^T        two TMEM buffers, S_{j+1} runs while
+//                                        the softmax of tile j does
+//   O_s += P_j V_s,j ; O_z += P_j Z_v,j  P_j read straight from TMEM (the
+//                                        softmax overwrites S_j with bf16 P_j)
+//   O_s += bf16(O_z) (B_h^V)^T           the lift, once
+// Scores are taken against a per-row reference max; the accumulators are
+// rescaled only when a row's max grows by more than 2^8 (then the row's own
+// TMEM lane is read, scaled and written back).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+
+#include "lrkv.h"
+#include "ptx.cuh"
+#include "tmap.h"
+
+namespace lrkv {
+
+namespace {
+
+constexpr int kBQ = 128, kBK = 128, kDH = 128, kR = 64;
+constexpr float kPfLog2e = 1.44269504088896340736f;
+constexpr float kPfLn2 = 0.69314718055994530942f;
+// shared-memory carve-up (bytes, 1024-aligned)
+constexpr int kOffQ = 0;                       // Q: 2 boxes [128][64]      32 KB
+constexpr int kOffB = kOffQ + 32768;           // B^K then B^V: [128][64]   16 KB
+constexpr int kOffP = kOffB + 16384;           // bf16(Pq) high part, then bf16(O_z)  16 KB
+constexpr int kOffP2 = kOffP + 16384;          // bf16(Pq - high part)             16 KB
+constexpr int kOffK = kOffP2 + 16384;          // 2 x (K_s 32 KB + Z_k 16 KB)
+constexpr int kKStage = 49152;
+constexpr int kOffV = kOffK + 2 * kKStage;     // 1 x (V_s 32 KB + Z_v 16 KB)
+constexpr int kSmem = kOffV + 49152 + 1024;    // + alignment slack
+// TMEM columns
+constexpr uint32_t kColS = 0;      // S_0 [0,128), S_1 [128,256)
+constexpr uint32_t kColOs = 256;   // O_s [256,384)
+constexpr uint32_t kColOz = 384;   // O_z [384,448)
+constexpr uint32_t kColPq = 448;   // Q B^K [448,512)
+
+struct PrefillParams {
+  int B, H, Tq, max_len;
+  float scale_log2;
+  const int32_t* seq_lens;
+  float* out;
+  float* lse;
+  uint32_t* status;
+};
+
+struct PrefillMaps {
+  CUtensorMap q;    // {dh, H, Tq, B}
+  CUtensorMap ks;   // {dh, max_len, B}
+  CUtensorMap vs;   // {dh, max_len, B}
+  CUtensorMap zk;   // {r, H, max_len, B}
+  CUtensorMap zv;   // {r, H, max_len, B}
+  CUtensorMap bk;   // {r, dh, H}
+  CUtensorMap bv;   // {r, dh, H}
+};
+
+__device__ __forceinline__ void mbar_arrive_cta(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// byte offset of element (row, col) in a [rows][64] bf16 tile written with
+// the 128-byte swizzle
+__device__ __forceinline__ uint32_t sw128(int row, int col) {
+  const uint32_t chunk = static_cast<uint32_t>(col >> 3) ^ static_cast<uint32_t>(row & 7);
+  return static_cast<uint32_t>(row) * 128u + chunk * 16u + static_cast<uint32_t>(col & 7) * 2u;
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(192, 1)
+    lrkv_prefill_kernel(const PrefillParams p, const __grid_constant__ PrefillMaps maps) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  __shared__ uint64_t bar_q, bar_pq, bar_pqs, bar_bv, bar_pv, bar_all, bar_lift;
+  __shared__ uint64_t bar_kf[2], bar_ke[2], bar_vf, bar_ve, bar_sf[2], bar_pf[2];
+  __shared__ uint32_t tmem_base;
+  __shared__ int s_fail;
+  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qt = gridDim.x - 1 - blockIdx.x;  // heaviest (longest causal range) first
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int q0 = qt * kBQ;
+  int L = p.seq_lens[b];
+  if (L < p.Tq || L > p.max_len) {
+    if (threadIdx.x == 0) atomicOr(p.status, 2u);
+    L = min(max(L, p.Tq), p.max_len);
+  }
+  const int off = L - p.Tq;                         // absolute position of query 0
+  const int last_key = min(L - 1, off + q0 + kBQ - 1);
+  const int nkt = last_key / kBK + 1;               // key tiles this query tile sees
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar_q, 1); mbar_init(&bar_pq, 1); mbar_init(&bar_pqs, 128); mbar_init(&bar_bv, 1);
+    mbar_init(&bar_pv, 1); mbar_init(&bar_all, 1); mbar_init(&bar_lift, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_kf[i], 1); mbar_init(&bar_ke[i], 1);
+      mbar_init(&bar_sf[i], 1); mbar_init(&bar_pf[i], 128);
+    }
+    mbar_init(&bar_vf, 1); mbar_init(&bar_ve, 1);
+    s_fail = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) tmem_alloc(&tmem_base, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
+  const uint32_t sQ = smem_u32(smem + kOffQ), sB = smem_u32(smem + kOffB), sP = smem_u32(smem + kOffP);
+  const uint32_t sP2 = smem_u32(smem + kOffP2);
+  const uint32_t sK = smem_u32(smem + kOffK), sV = smem_u32(smem + kOffV);
+
+  if (warp == 4) {
+    // =============================================================== TMA ====
+    if (lane == 0) {
+      bool ok = true;
+      mbar_arrive_expect_tx(&bar_q, 32768 + 16384);
+      tma_load_4d(smem + kOffQ, &maps.q, 0, h, q0, b, &bar_q);
+      tma_load_4d(smem + kOffQ + 16384, &maps.q, 64, h, q0, b, &bar_q);
+      tma_load_3d(smem + kOffB, &maps.bk, 0, 0, h, &bar_q);
+      auto load_k = [&](int j) {
+        const int s = j & 1;
+        unsigned char* dst = smem + kOffK + s * kKStage;
+        mbar_arrive_expect_tx(&bar_kf[s], kKStage);
+        tma_load_3d(dst, &maps.ks, 0, j * kBK, b, &bar_kf[s]);
+        tma_load_3d(dst + 16384, &maps.ks, 64, j * kBK, b, &bar_kf[s]);
+        tma_load_4d(dst + 32768, &maps.zk, 0, h, j * kBK, b, &bar_kf[s]);
+      };
+      auto load_v = [&](int j) {
+        unsigned char* dst = smem + kOffV;
+        mbar_arrive_expect_tx(&bar_vf, kKStage);
+        tma_load_3d(dst, &maps.vs, 0, j * kBK, b, &bar_vf);
+        tma_load_3d(dst + 16384, &maps.vs, 64, j * kBK, b, &bar_vf);
+        tma_load_4d(dst + 32768, &maps.zv, 0, h, j * kBK, b, &bar_vf);
+      };
+      load_k(0);
+      if (nkt > 1) load_k(1);
+      load_v(0);
+      // B^V replaces B^K once Q B^K is computed
+      if (mbar_wait_bounded(&bar_pq, 0)) {
+        mbar_arrive_expect_tx(&bar_bv, 16384);
+        tma_load_3d(smem + kOffB, &maps.bv, 0, 0, h, &bar_bv);
+      } else {
+        ok = false;
+      }
+      for (int j = 0; ok && j < nkt; ++j) {
+        if (j + 2 < nkt) {  // K ring: stage of tile j frees when S_j is done
+          if (!mbar_wait_bounded(&bar_ke[j & 1], static_cast<uint32_t>(j >> 1) & 1u)) { ok = false; break; }
+          load_k(j + 2);
+        }
+        if (j + 1 < nkt) {  // V stage frees when P_j V_j is done
+          if (!mbar_wait_bounded(&bar_ve, static_cast<uint32_t>(j) & 1u)) { ok = false; break; }
+          load_v(j + 1);
+        }
+      }
+      if (!ok) s_fail = 1;
+    }
+  } else if (warp == 5) {
+    // =============================================================== MMA ====
+    if (lane == 0) {
+      bool ok = mbar_wait_bounded(&bar_q, 0);
+      tc_fence_after();
+      if (ok) {
+        // Pq = Q B^K : M=128, N=64, K=128; B^K tile is [dh][r], r contiguous (MN-major)
+        const uint32_t id = idesc_bf16(kBQ, kR, 0, 1);
+        for (int kk = 0; kk < kDH / 16; ++kk) {
+          const uint64_t ad = smem_desc(sQ + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, 2);
+          const uint64_t bd = smem_desc(sB + kk * 2048, 16384, 1024, 2);
+          tc_mma_ss(tmem + kColPq, ad, bd, id, kk > 0);
+        }
+        tc_commit(&bar_pq);
+      }
+      ok = ok && mbar_wait_bounded(&bar_pqs, 0);  // bf16 Pq is in shared memory
+      tc_fence_after();
+      const uint32_t id_s = idesc_bf16(kBQ, kBK, 0, 0);
+      auto issue_s = [&](int j) {
+        const int s = j & 1;
+        const uint32_t kbase = sK + s * kKStage;
+        const uint32_t d = tmem + kColS + s * 128;
+        for (int kk = 0; kk < kDH / 16; ++kk) {
+          const uint32_t o = (kk >> 2) * 16384 + (kk & 3) * 32;
+          tc_mma_ss(d, smem_desc(sQ + o, 16, 1024, 2), smem_desc(kbase + o, 16, 1024, 2), id_s, kk > 0);
+        }
+        for (int kk = 0; kk < kR / 16; ++kk) {
+          const uint64_t zd = smem_desc(kbase + 32768 + kk * 32, 16, 1024, 2);
+          tc_mma_ss(d, smem_desc(sP + kk * 32, 16, 1024, 2), zd, id_s, 1);
+          tc_mma_ss(d, smem_desc(sP2 + kk * 32, 16, 1024, 2), zd, id_s, 1);
+        }
+        tc_commit(&bar_sf[s]);
+        tc_commit(&bar_ke[s]);
+      };
+      if (ok) {
+        if (!mbar_wait_bounded(&bar_kf[0], 0)) ok = false;
+        tc_fence_after();
+        if (ok) issue_s(0);
+      }
+      const uint32_t id_vs = idesc_bf16(kBQ, kDH, 0, 1), id_vz = idesc_bf16(kBQ, kR, 0, 1);
+      for (int j = 0; ok && j < nkt; ++j) {
+        if (j + 1 < nkt) {
+          if (!mbar_wait_bounded(&bar_kf[(j + 1) & 1], static_cast<uint32_t>((j + 1) >> 1) & 1u)) { ok = false; break; }
+          tc_fence_after();
+          issue_s(j + 1);
+        }
+        if (!mbar_wait_bounded(&bar_pf[j & 1], static_cast<uint32_t>(j >> 1) & 1u) ||
+            !mbar_wait_bounded(&bar_vf, static_cast<uint32_t>(j) & 1u)) { ok = false; break; }
+        tc_fence_after();
+        const int nv = L - j * kBK;  // rows of this value tile inside the history
+        if (nv < kBK) {
+          // rows past the history may hold anything; P is 0 there, so make them 0
+          for (int row = max(nv, 0); row < kBK; ++row)
+            for (int box = 0; box < 3; ++box)
+              for (int ch = 0; ch < 8; ++ch)
+                *reinterpret_cast<uint4*>(smem + kOffV + box * 16384 + row * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+          fence_proxy_async_smem();
+        }
+        const uint32_t pa = tmem + kColS + (j & 1) * 128;  // bf16 P_j, 2 per column
+        for (int kk = 0; kk < kBK / 16; ++kk) {
+          const uint32_t vo = sV + kk * 2048;
+          tc_mma_ts(tmem + kColOs, pa + kk * 8, smem_desc(vo, 16384, 1024, 2), id_vs, (j > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_ts(tmem + kColOz, pa + kk * 8, smem_desc(vo + 32768, 16384, 1024, 2), id_vz,
+                    (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(&bar_ve);
+        tc_commit(&bar_pv);
+      }
+      tc_commit(&bar_all);
+      // lift: O_s += bf16(O_z) (B^V)^T : M=128, N=128 (dh), K=64 (r)
+      ok = ok && mbar_wait_bounded(&bar_bv, 0) && mbar_wait_bounded(&bar_pqs, 1);
+      tc_fence_after();
+      if (ok) {
+        const uint32_t id = idesc_bf16(kBQ, kDH, 0, 0);
+        for (int kk = 0; kk < kR / 16; ++kk)
+          tc_mma_ss(tmem + kColOs, smem_desc(sP + kk * 32, 16, 1024, 2), smem_desc(sB + kk * 32, 16, 1024, 2),
+                    id, 1);
+      } else {
+        s_fail = 1;
+      }
+      tc_commit(&bar_lift);
+    }
+  } else {
+    // ========================================================= softmax ====
+    const int row = threadIdx.x;                     // query row in the tile
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int qpos = off + q0 + row;                 // absolute position of this query
+    bool ok = mbar_wait_bounded(&bar_pq, 0);
+    tc_fence_after();
+    {
+      // Pq row -> high and low bf16 parts -> shared (A operands of S += Pq Z_k^T)
+      uint32_t v[32];
+      unsigned char* pbase = smem + kOffP;
+      unsigned char* pbase2 = smem + kOffP2;
+      for (int c = 0; c < kR / 32; ++c) {
+        tmem_ld32(tmem + lane_off + kColPq + c * 32, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float f0 = __uint_as_float(v[e]), f1 = __uint_as_float(v[e + 1]);
+          const __nv_bfloat162 hi = __floats2bfloat162_rn(f0, f1);
+          const __nv_bfloat162 lo = __floats2bfloat162_rn(f0 - __low2float(hi), f1 - __high2float(hi));
+          *reinterpret_cast<__nv_bfloat162*>(pbase + sw128(row, c * 32 + e)) = hi;
+          *reinterpret_cast<__nv_bfloat162*>(pbase2 + sw128(row, c * 32 + e)) = lo;
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive_cta(&bar_pqs);
+    }
+    float m_ref = -INFINITY, l_sum = 0.f;
+    for (int j = 0; j < nkt; ++j) {
+      const uint32_t sb = tmem + lane_off + kColS + (j & 1) * 128;
+      ok = ok && mbar_wait_bounded(&bar_sf[j & 1], static_cast<uint32_t>(j >> 1) & 1u);
+      tc_fence_after();
+      const int k0 = j * kBK;
+      // keys k0 + c visible iff k0 + c <= qpos and k0 + c < L
+      const int lim = min(qpos, L - 1) - k0;        // last visible column (may be < 0 or >= 127)
+      float mloc = -INFINITY;
+      uint32_t v[32];
+      for (int c = 0; c < 4; ++c) {
+        tmem_ld32(sb + c * 32, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          if (c * 32 + e <= lim) mloc = fmaxf(mloc, __uint_as_float(v[e]) * p.scale_log2);
+      }
+      const bool need = j > 0 && mloc > m_ref + 8.f;
+      if (j == 0) m_ref = mloc;
+      if (__any_sync(0xffffffffu, need)) {
+        // rare: rescale the accumulators of the rows whose max moved, once
+        // P_{j-1} V_{j-1} is done (TMEM loads/stores are warp-wide)
+        const float alpha = need ? exp2f(m_ref - mloc) : 1.f;
+        ok = ok && mbar_wait_bounded(&bar_pv, static_cast<uint32_t>(j - 1) & 1u);
+        tc_fence_after();
+        for (int c = 0; c < 6; ++c) {
+          const uint32_t col = c < 4 ? kColOs + c * 32 : kColOz + (c - 4) * 32;
+          tmem_ld32(tmem + lane_off + col, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+          tmem_st32(tmem + lane_off + col, v);
+        }
+        tmem_wait_st();
+        l_sum *= alpha;
+        if (need) m_ref = mloc;
+      }
+      // probabilities against m_ref, packed bf16 into the S buffer's first 64 columns
+      uint32_t pk[64];
+      float lsum = 0.f;
+      for (int c = 0; c < 4; ++c) {
+        tmem_ld32(sb + c * 32, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const int col = c * 32 + e;
+          const float p0 = col <= lim ? exp2f(__uint_as_float(v[e]) * p.scale_log2 - m_ref) : 0.f;
+          const float p1 = col + 1 <= lim ? exp2f(__uint_as_float(v[e + 1]) * p.scale_log2 - m_ref) : 0.f;
+          const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+          lsum += __low2float(h2) + __high2float(h2);
+          pk[c * 16 + e / 2] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+      }
+      l_sum += lsum;
+      uint32_t half[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) half[e] = pk[e];
+      tmem_st32(sb, half);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) half[e] = pk[32 + e];
+      tmem_st32(sb + 32, half);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive_cta(&bar_pf[j & 1]);
+    }
+    // ---- O_z -> bf16 in shared memory for the lift ---------------------------
+    ok = ok && mbar_wait_bounded(&bar_all, 0);
+    tc_fence_after();
+    {
+      uint32_t v[32];
+      unsigned char* pbase = smem + kOffP;
+      for (int c = 0; c < kR / 32; ++c) {
+        tmem_ld32(tmem + lane_off + kColOz + c * 32, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const __nv_bfloat162 v2 = __floats2bfloat162_rn(__uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+          *reinterpret_cast<__nv_bfloat162*>(pbase + sw128(row, c * 32 + e)) = v2;
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive_cta(&bar_pqs);  // second phase: bf16(O_z) ready
+    }
+    ok = ok && mbar_wait_bounded(&bar_lift, 0);
+    tc_fence_after();
+    const int t = q0 + row;
+    const bool store = t < p.Tq && ok && !s_fail;
+    if (!ok || s_fail) {
+      if (row == 0) atomicOr(p.status, 1u);
+    }
+    const float inv_l = 1.f / l_sum;
+    float* dst = p.out + ((static_cast<size_t>(b) * p.Tq + t) * p.H + h) * kDH;
+    uint32_t v[32];
+    for (int c = 0; c < 4; ++c) {  // warp-wide TMEM reads; only real rows store
+      tmem_ld32(tmem + lane_off + kColOs + c * 32, v);
+      tmem_wait_ld();
+      if (store) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 4)
+          *reinterpret_cast<float4*>(dst + c * 32 + e) =
+              make_float4(__uint_as_float(v[e]) * inv_l, __uint_as_float(v[e + 1]) * inv_l,
+                          __uint_as_float(v[e + 2]) * inv_l, __uint_as_float(v[e + 3]) * inv_l);
+      }
+    }
+    if (store && p.lse) p.lse[(static_cast<size_t>(b) * p.H + h) * p.Tq + t] = (m_ref + log2f(l_sum)) * kPfLn2;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace lrkv
+
+namespace {
+
+bool a16p(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// bf16 tensor map of rank n (dims innermost first; strides in bytes of dims
+// 1..n-1), 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, int n, const uint64_t* dims, const uint64_t* strides,
+              const uint32_t* box) {
+  auto fn = encoder();
+  if (!fn) return false;
+  cuuint64_t d[5], s[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < n; ++i) { d[i] = dims[i]; bx[i] = box[i]; es[i] = 1; }
+  for (int i = 0; i < n - 1; ++i) s[i] = strides[i];
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, n, const_cast<void*>(base), d, s, bx, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" lrkv_status lrkv_prefill(const lrkv_dims* dims, int q_len, const void* q, const void* k_s,
+                                    const void* v_s, const void* z_k, const void* z_v, const void* b_k,
+                                    const void* b_v, const int32_t* seq_lens, float* out, float* lse, void* ws,
+                                    size_t ws_bytes, lrkv_stream_t stream) {
+  if (!dims) return LRKV_ERR_INVALID_ARG;
+  const lrkv_dims& d = *dims;
+  if (d.batch < 1 || d.heads < 1 || d.head_dim < 1 || d.rank < 0 || d.max_len < 1 || q_len < 1)
+    return LRKV_ERR_INVALID_ARG;
+  if (d.dtype != LRKV_BF16 && d.dtype != LRKV_F32) return LRKV_ERR_INVALID_ARG;
+  if (!(d.scale == d.scale)) return LRKV_ERR_INVALID_ARG;
+  if (d.dtype != LRKV_BF16 || d.head_dim != 128 || d.rank != 64) return LRKV_ERR_UNSUPPORTED;
+  if (q_len > d.max_len || d.heads > 65535 || d.batch > 65535) return LRKV_ERR_UNSUPPORTED;
+  if (!q || !k_s || !v_s || !z_k || !z_v || !b_k || !b_v || !seq_lens || !out) return LRKV_ERR_INVALID_ARG;
+  if (!a16p(q) || !a16p(k_s) || !a16p(v_s) || !a16p(z_k) || !a16p(z_v) || !a16p(b_k) || !a16p(b_v) || !a16p(out))
+    return LRKV_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < 16) return LRKV_ERR_WORKSPACE;
+
+  const int B = d.batch, H = d.heads, Lm = d.max_len;
+  const uint64_t dh = 128, r = 64;
+  lrkv::PrefillMaps maps;
+  std::memset(&maps, 0, sizeof(maps));
+  {
+    const uint64_t dm[4] = {dh, static_cast<uint64_t>(H), static_cast<uint64_t>(q_len), static_cast<uint64_t>(B)};
+    const uint64_t st[3] = {dh * 2, H * dh * 2, static_cast<uint64_t>(q_len) * H * dh * 2};
+    const uint32_t bx[4] = {64, 1, 128, 1};
+    if (!make_map(&maps.q, q, 4, dm, st, bx)) return LRKV_ERR_CUDA;
+  }
+  {
+    const uint64_t dm[3] = {dh, static_cast<uint64_t>(Lm), static_cast<uint64_t>(B)};
+    const uint64_t st[2] = {dh * 2, static_cast<uint64_t>(Lm) * dh * 2};
+    const uint32_t bx[3] = {64, 128, 1};
+    if (!make_map(&maps.ks, k_s, 3, dm, st, bx) || !make_map(&maps.vs, v_s, 3, dm, st, bx)) return LRKV_ERR_CUDA;
+  }
+  {
+    const uint64_t dm[4] = {r, static_cast<uint64_t>(H), static_cast<uint64_t>(Lm), static_cast<uint64_t>(B)};
+    const uint64_t st[3] = {r * 2, H * r * 2, static_cast<uint64_t>(Lm) * H * r * 2};
+    const uint32_t bx[4] = {64, 1, 128, 1};
+    if (!make_map(&maps.zk, z_k, 4, dm, st, bx) || !make_map(&maps.zv, z_v, 4, dm, st, bx)) return LRKV_ERR_CUDA;
+  }
+  {
+    const uint64_t dm[3] = {r, dh, static_cast<uint64_t>(H)};
+    const uint64_t st[2] = {r * 2, dh * r * 2};
+    const uint32_t bx[3] = {64, 128, 1};
+    if (!make_map(&maps.bk, b_k, 3, dm, st, bx) || !make_map(&maps.bv, b_v, 3, dm, st, bx)) return LRKV_ERR_CUDA;
+  }
+  lrkv::PrefillParams p;
+  p.B = B; p.H = H; p.Tq = q_len; p.max_len = Lm;
+  const float scale = d.scale > 0.f ? d.scale : 1.f / std::sqrt(static_cast<float>(d.head_dim));
+  p.scale_log2 = scale * lrkv::kPfLog2e;
+  p.seq_lens = seq_lens; p.out = out; p.lse = lse;
+  p.status = static_cast<uint32_t*>(ws);
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, 4, s) != cudaSuccess) return LRKV_ERR_CUDA;
+  if (cudaFuncSetAttribute(lrkv::lrkv_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, lrkv::kSmem) !=
+      cudaSuccess)
+    return LRKV_ERR_CUDA;
+  const dim3 grid((q_len + lrkv::kBQ - 1) / lrkv::kBQ, H, B);
+  lrkv::lrkv_prefill_kernel<<<grid, 192, lrkv::kSmem, s>>>(p, maps);
+  return cudaGetLastError() == cudaSuccess ? LRKV_OK : LRKV_ERR_CUDA;
+}

@@ -172,3 +172,22 @@ def random_decode_case(seed: int, batch: int, heads: int, head_dim: int, rank: i
     dt = torch.float32 if dtype == "f32" else torch.bfloat16
     return dict(q=q.to(dt), k_s=k_s.to(dt), v_s=v_s.to(dt), z_k=z_k.to(dt), z_v=z_v.to(dt),
                 b_k=b_k.to(dt), b_v=b_v.to(dt), seq_lens=seq_lens.to(torch.int32))
+
+
+def random_prefill_case(seed: int, batch: int, q_len: int, heads: int, head_dim: int, rank: int,
+                        max_len: int, lens, dtype: str = "bf16") -> Dict[str, torch.Tensor]:
+    """Small randomised prefill case: a cache of `max_len` rows per sequence
+    (rows past each history are filled too, as garbage the kernels must
+    ignore) and q [B, q_len, H, d_h]."""
+    gen = torch.Generator().manual_seed(seed)
+    k_s = _normal(gen, (batch, max_len, head_dim))
+    v_s = _normal(gen, (batch, max_len, head_dim))
+    z_k = _normal(gen, (batch, max_len, heads, rank))
+    z_v = _normal(gen, (batch, max_len, heads, rank))
+    q = _normal(gen, (batch, q_len, heads, head_dim))
+    bstd = 1.0 / math.sqrt(rank) if rank > 0 else 1.0
+    b_k = _normal(gen, (heads, head_dim, rank), bstd)
+    b_v = _normal(gen, (heads, head_dim, rank), bstd)
+    dt = torch.float32 if dtype == "f32" else torch.bfloat16
+    return dict(q=q.to(dt), k_s=k_s.to(dt), v_s=v_s.to(dt), z_k=z_k.to(dt), z_v=z_v.to(dt),
+                b_k=b_k.to(dt), b_v=b_v.to(dt), seq_lens=torch.tensor(lens, dtype=torch.int32))

@@ -37,6 +37,7 @@ EXPORTED = (
     "lrkv_decode_profiled",
     "lrkv_decode_static_scratch",
     "lrkv_append",
+    "lrkv_prefill",
     "lrkv_read_device_status",
 )
 
@@ -93,6 +94,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.lrkv_append.restype = ctypes.c_int
     lib.lrkv_append.argtypes = [dims_p, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, vp, i32p, vp, vp, vp,
                                 vp, vp, sz, vp]
+    lib.lrkv_prefill.restype = ctypes.c_int
+    lib.lrkv_prefill.argtypes = [dims_p, ctypes.c_int, vp, vp, vp, vp, vp, vp, vp, i32p, vp, vp, vp, sz,
+                                 vp]
     lib.lrkv_read_device_status.restype = ctypes.c_int
     lib.lrkv_read_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
     if path is None:
@@ -239,3 +243,32 @@ def append(x: torch.Tensor, w_sk: torch.Tensor, w_sv: torch.Tensor, u_k: torch.T
     if st != LRKV_OK:
         raise LRKVError(st, "lrkv_append")
     return lrkv_read_device_status(ws, stream)
+
+
+def lrkv_prefill(dims: lrkv_dims, q_len: int, q, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens, out, lse,
+                 ws, ws_bytes: int, stream=None) -> int:
+    """Direct call of the prefill entry point; returns its status code."""
+    return int(load().lrkv_prefill(ctypes.byref(dims), q_len, _ptr(q), _ptr(k_s), _ptr(v_s),
+                                   _ptr(z_k), _ptr(z_v), _ptr(b_k), _ptr(b_v), _ptr(seq_lens),
+                                   _ptr(out), _ptr(lse), _ptr(ws), ws_bytes, _stream_handle(stream)))
+
+
+def prefill(q: torch.Tensor, k_s: torch.Tensor, v_s: torch.Tensor, z_k: torch.Tensor,
+            z_v: torch.Tensor, b_k: torch.Tensor, b_v: torch.Tensor, seq_lens: torch.Tensor,
+            scale: float = 0.0, out: Optional[torch.Tensor] = None,
+            lse: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None, stream=None):
+    """Causal prefill of q [B, q_len, H, d_h]; returns (out, lse, status)."""
+    B, Tq, H, dh = q.shape
+    r = z_k.shape[-1]
+    dims = make_dims(B, H, dh, r, k_s.shape[1], q.dtype, scale)
+    if out is None:
+        out = torch.empty((B, Tq, H, dh), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, Tq), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = torch.zeros(16, dtype=torch.uint8, device=q.device)
+    st = lrkv_prefill(dims, Tq, q, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens, out, lse, ws, ws.numel(),
+                      stream)
+    if st != LRKV_OK:
+        raise LRKVError(st, "lrkv_prefill")
+    return out, lse, ws

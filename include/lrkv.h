@@ -203,6 +203,30 @@ lrkv_status lrkv_append(const lrkv_dims* dims, int d_model, int n_new, const voi
                         lrkv_stream_t stream);
 
 /*
+ * Causal attention of q_len new queries per sequence against the factored
+ * cache, on the tensor cores ("Low-Rank Key Value Attention：中文研读笔记",
+ * §2.4, Eqs. (6)-(7); "Low-Rank Key Value Attention | What a shared cache can
+ * preserve", §3): logits [q_h | q_h B_h^K] . [k_s | z_k,h] / sqrt(d_h), one
+ * causal softmax, values sum_j a_j v_s,j + (sum_j a_j z_v,h,j) (B_h^V)^T.
+ *
+ *   q        [batch][q_len][heads][head_dim]   queries (dtype)
+ *   cache    rows [0, seq_lens[b]) hold the history including the q_len new
+ *            tokens (append them first); query i sits at position
+ *            seq_lens[b] - q_len + i and sees keys j <= that position
+ *   out      [batch][q_len][heads][head_dim] fp32
+ *   lse      [batch][heads][q_len] fp32 or NULL (natural log)
+ *   ws, ws_bytes >= 16                         device status word
+ * q_h B_h^K enters its tensor-core contraction with the latents as the sum
+ * of two bf16 parts (about 16 significant bits).  Supported: dtype BF16,
+ * head_dim 128, rank 64.  seq_lens[b]
+ * outside [q_len, max_len] is clamped and sets LRKV_ERR_DEVICE_BOUNDS.
+ */
+lrkv_status lrkv_prefill(const lrkv_dims* dims, int q_len, const void* q, const void* k_s, const void* v_s,
+                         const void* z_k, const void* z_v, const void* b_k, const void* b_v,
+                         const int32_t* seq_lens, float* out, float* lse, void* ws, size_t ws_bytes,
+                         lrkv_stream_t stream);
+
+/*
  * Read the device status word that the kernels of the last call(s) using
  * `ws` recorded (LRKV_OK, LRKV_ERR_TIMEOUT or LRKV_ERR_DEVICE_BOUNDS).
  * Synchronises `stream`.  Each lrkv_decode/lrkv_prefill call resets the word
