@@ -47,6 +47,7 @@ def _args():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
     return ap.parse_args()
 
 
@@ -221,7 +222,7 @@ def cpu_baseline(w, case, seconds, cores):
         pool.run(tasks)
         n += 1
         el = time.perf_counter() - t0
-        if el >= seconds or n >= 20:
+        if el >= seconds or n >= 400:
             break
     pool.close()
     return {"value": total_bytes * n / el / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
@@ -260,6 +261,83 @@ def reference_arm(a, w):
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
                              "sample": f"one sequence (all {w.heads} heads) of {w.name} per step"},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ------------------------------------------------------------ prefill leg
+
+def prefill_flops(w):
+    """Algorithmic FLOPs of the prefill workload: causal (query, key) pairs
+    only, 2 (d_h + r) per pair for the scores and 2 (d_h + r) for the values,
+    plus q B^K and the (B^V)^T lift; and the append GEMM 2 M N K."""
+    T, B, H, dh, r, d = w.q_len, w.batch, w.heads, w.head_dim, w.rank, w.d_model
+    pairs = B * H * T * (T + 1) // 2
+    attn = pairs * 4 * (dh + r) + 2 * (2 * B * T * H * dh * r)
+    append = 2 * (B * T) * (2 * dh + 2 * H * r) * d
+    return attn, append
+
+
+def prefill_leg(dev, iters=10):
+    """Times append (x -> factored cache) and causal prefill on the prefill
+    workload with CUDA events, L2 flushed (256 MB write) before each timed
+    launch.  Returns TFLOP/s against the measured bf16 peak."""
+    import torch
+    from compressed_cache_decode_gb300 import inputs, lrkv
+    w = inputs.WORKLOADS[inputs.PREFILL_WORKLOAD]
+    c = inputs.make_prefill_inputs(w, seed=0)
+    d = {k: v.to(dev) for k, v in c.items()}
+    B, T, H, dh, r = w.batch, w.q_len, w.heads, w.head_dim, w.rank
+    k_s = torch.empty((B, T, dh), dtype=torch.bfloat16, device=dev)
+    v_s = torch.empty_like(k_s)
+    z_k = torch.empty((B, T, H, r), dtype=torch.bfloat16, device=dev)
+    z_v = torch.empty_like(z_k)
+    dims = lrkv.make_dims(B, H, dh, r, T, torch.bfloat16)
+    ws = torch.zeros(16, dtype=torch.uint8, device=dev)
+    out = torch.empty((B, T, H, dh), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def app():
+        st = lrkv.lrkv_append(dims, w.d_model, T, d["x"], d["w_sk"], d["w_sv"], d["u_k"], d["u_v"],
+                              d["start_pos"], k_s, v_s, z_k, z_v, ws, 16)
+        assert st == lrkv.LRKV_OK
+
+    def pre():
+        st = lrkv.lrkv_prefill(dims, T, d["q"], k_s, v_s, z_k, z_v, d["b_k"], d["b_v"], d["seq_lens"],
+                               out, lse, ws, 16)
+        assert st == lrkv.LRKV_OK
+
+    res = {}
+    for name, fn in (("append", app), ("prefill", pre)):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(iters):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        res[name] = statistics.median(ts)
+    attn, append = prefill_flops(w)
+    peak = _bf16_peak()
+    return {"workload": w.name,
+            "attention": {"ms": res["prefill"], "tflops": attn / (res["prefill"] * 1e-3) / 1e12,
+                          "algorithmic_flop": attn},
+            "append": {"ms": res["append"], "tflops": append / (res["append"] * 1e-3) / 1e12,
+                       "algorithmic_flop": append},
+            "peak_tflops": peak[0], "peak_kind": peak[1],
+            "attention_frac": attn / (res["prefill"] * 1e-3) / 1e12 / peak[0],
+            "append_frac": append / (res["append"] * 1e-3) / 1e12 / peak[0]}
+
+
+def _bf16_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured bf16 burst (cuBLAS)"
+    except Exception:
+        return 1900.0, "fallback bf16 burst"
 
 
 # -------------------------------------------------------------------- GPU arm
@@ -414,6 +492,10 @@ def main():
         dist.all_reduce(te, op=dist.ReduceOp.MAX)
     e2e_ms = float(te.item())
 
+    prefill = None
+    if not a.no_prefill:
+        prefill = prefill_leg(dev)
+
     cpu = None
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
         cpu = cpu_baseline(w, case, a.cpu_seconds, min(os.cpu_count() or 1, 16))
@@ -445,6 +527,7 @@ def main():
                     "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": 3 * K,
             "clocks": clk.summary(),
+            "prefill": prefill,
         }
         print(json.dumps(res), flush=True)
     if world > 1:
