@@ -32,7 +32,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "LRKV decode cache GB/s (% of HBM peak) & tokens/s; prefill TFLOP/s (% peak)"
-PROFILE_JSON = os.path.join(ROOT, "profiles", "decode_split_b8_h16_d64_r28_L4096.json")
+PROFILE_JSON = os.path.join(ROOT, "profiles", "decode_stream_b8_h16_d64_r28_L4096.json")
 L2_BYTES = 129 * 1000 * 1000
 FALLBACK_HBM_GBS = 6800.0
 
@@ -518,7 +518,7 @@ def main():
                        "l2": f"{n_rep} rotating cache replicas ({n_rep * cache_bytes / 1e6:.0f} MB > L2 "
                              f"{L2_BYTES / 1e6:.0f} MB)",
                        "graph": graph is not None, "parallelism": f"replicas x{world}"},
-            "roofline": {"bound": "hbm", "kernel": "lrkv_decode_split_kernel", "achieved": achieved,
+            "roofline": {"bound": "hbm", "kernel": "lrkv_decode_stream_kernel", "achieved": achieved,
                          "peak": peak, "peak_kind": f"{peak_kind} HBM copy", "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "algorithmic_bytes_per_launch": split_bytes, "launch_ms": split_ms},
