@@ -45,8 +45,9 @@ namespace lrkv {
 using namespace dec;
 
 lrkv_status stream_plan(DecodePlan& P);
+lrkv_status stream_prepare(const DecodePlan& P, CUtensorMap* tm_zk, CUtensorMap* tm_zv);
 lrkv_status stream_launch(const DecodePlan& P, cudaStream_t stream, bool pdl, const CUtensorMap& tm_k,
-                          const CUtensorMap& tm_v);
+                          const CUtensorMap& tm_v, const CUtensorMap& tm_zk, const CUtensorMap& tm_zv);
 
 namespace {
 
@@ -85,30 +86,42 @@ __device__ __forceinline__ void issue_tile(const DecodePlan& P, const CUtensorMa
 }  // namespace
 
 // ===================================================================== absorb
-// grid = H, block = 256: B_h^K staged in shared memory once, then p for every
-// sequence of this head.
+// grid = (H, ceil(B / kAbsorbSeq)), block = 256: B_h^K and the q rows of up
+// to kAbsorbSeq sequences staged in shared memory, then one output
+// p_{b,h,c} = q_{b,h} . B_h^K[:, c] per thread.
+constexpr int kAbsorbSeq = 8;
+
 template <bool BF16>
 __global__ void __launch_bounds__(256) lrkv_decode_absorb_kernel(const DecodePlan P) {
-  extern __shared__ __align__(16) float bks[];  // [dh][r]
+  extern __shared__ __align__(16) float absm[];  // B_h^K [dh][r] | q rows [kAbsorbSeq][dh]
   pdl_trigger();
-  const int h = blockIdx.x, tid = threadIdx.x;
-  if (h == 0 && tid == 0) *P.status = 0u;
+  const int h = blockIdx.x, b0 = blockIdx.y * kAbsorbSeq, tid = threadIdx.x;
+  if (h == 0 && blockIdx.y == 0 && tid == 0) *P.status = 0u;
   const int dh = P.dh, r = P.r, H = P.H;
+  const int nb = min(kAbsorbSeq, P.B - b0);
   if (r == 0) return;
+  float* bks = absm;
+  float* qs = absm + dh * r;
   const size_t base = static_cast<size_t>(h) * dh * r;
   for (int i = tid; i < dh * r; i += blockDim.x) bks[i] = load_elem(P.b_k, base + i, BF16);
+  for (int i = tid; i < nb * dh; i += blockDim.x) {
+    const int bb = i / dh, k = i % dh;
+    qs[i] = load_elem(P.q, (static_cast<size_t>(b0 + bb) * H + h) * dh + k, BF16);
+  }
   __syncthreads();
-  for (int idx = tid; idx < P.B * r; idx += blockDim.x) {
-    const int b = idx / r, c = idx % r;
-    const size_t qb = (static_cast<size_t>(b) * H + h) * dh;
-    float a0 = 0.f, a1 = 0.f;
+  for (int idx = tid; idx < nb * r; idx += blockDim.x) {
+    const int bb = idx / r, c = idx % r;
+    const float* qr = qs + bb * dh;
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
     int k = 0;
-    for (; k + 1 < dh; k += 2) {
-      a0 = fmaf(load_elem(P.q, qb + k, BF16), bks[k * r + c], a0);
-      a1 = fmaf(load_elem(P.q, qb + k + 1, BF16), bks[(k + 1) * r + c], a1);
+    for (; k + 3 < dh; k += 4) {
+      a0 = fmaf(qr[k], bks[k * r + c], a0);
+      a1 = fmaf(qr[k + 1], bks[(k + 1) * r + c], a1);
+      a2 = fmaf(qr[k + 2], bks[(k + 2) * r + c], a2);
+      a3 = fmaf(qr[k + 3], bks[(k + 3) * r + c], a3);
     }
-    if (k < dh) a0 = fmaf(load_elem(P.q, qb + k, BF16), bks[k * r + c], a0);
-    P.p_abs[(static_cast<size_t>(b) * H + h) * r + c] = a0 + a1;
+    for (; k < dh; ++k) a0 = fmaf(qr[k], bks[k * r + c], a0);
+    P.p_abs[(static_cast<size_t>(b0 + bb) * H + h) * r + c] = (a0 + a1) + (a2 + a3);
   }
 }
 
@@ -574,12 +587,33 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ==================================================================== combine
+// grid = (H, B), block = 128: the pieces (m_i, l_i, acc_i) of sequence b,
+// head h, merged with the log-sum-exp rule, then the lift
+// o = acc_s / L + (acc_z / L) (B_h^V)^T and lse = (M + log2 L) ln 2
+// (Algorithm 2 steps 06-09).  Thread j owns column j of [acc_s | acc_z] and
+// merges its column over every piece in one pass (32 pieces of loads in
+// flight, the running maximum raised as it goes; the m_i, l_i loads are
+// shared by the warp).  The B_h^V row of its output column is an input, so
+// it is loaded before the wait on the scan kernel.
+constexpr int kCombinePieces = 32;
+constexpr int kCombineRank = 64;
+
 template <bool BF16>
 __global__ void __launch_bounds__(128) lrkv_decode_combine_kernel(const DecodePlan P) {
   extern __shared__ __align__(16) unsigned char csmem[];
-  pdl_wait();
+  float* zbar = reinterpret_cast<float*>(csmem);  // [r]
+  __shared__ float s_M, s_L;
   const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
-  const int H = P.H, dh = P.dh, r = P.r;
+  const int H = P.H, dh = P.dh, r = P.r, W = dh + r;
+  const bool pre_bv = BF16 && dh <= static_cast<int>(blockDim.x) && r <= kCombineRank;
+  uint32_t bvp[kCombineRank / 2];
+  if (pre_bv && tid < dh) {
+    const uint32_t* row = reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(P.b_v) +
+                                                            (static_cast<size_t>(h) * dh + tid) * r);
+#pragma unroll
+    for (int c2 = 0; c2 < kCombineRank / 2; ++c2) bvp[c2] = 2 * c2 < r ? row[c2] : 0u;
+  }
+  pdl_wait();
   float* o = P.out + (static_cast<size_t>(b) * H + h) * dh;
   const int start = P.prefix[b], end = P.prefix[b + 1];
   if (end <= start) {
@@ -591,63 +625,57 @@ __global__ void __launch_bounds__(128) lrkv_decode_combine_kernel(const DecodePl
   const int c0 = cta_of_token(start, N, G), c1 = cta_of_token(end - 1, N, G);
   const int n = (c1 - c0 + 1) * P.ngw;       // partials of this sequence
   const size_t s0 = static_cast<size_t>(b + c0) * P.ngw;  // first of them
-  float* wsl = reinterpret_cast<float*>(csmem);   // [n] per-piece weights
-  float* zbar = wsl + n;                          // [r]
-  __shared__ float red[32];
-  __shared__ float s_M, s_L;
-
-  float mloc = -INFINITY;
-  for (int i = tid; i < n; i += blockDim.x)
-    mloc = fmaxf(mloc, P.part_ml[((s0 + i) * H + h) * 2]);
-  for (int off = 16; off > 0; off >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, off));
-  if ((tid & 31) == 0) red[tid >> 5] = mloc;
-  __syncthreads();
-  if (tid == 0) {
-    float M = -INFINITY;
-    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) M = fmaxf(M, red[i]);
-    s_M = M;
-  }
-  __syncthreads();
-  const float M = s_M;
-  float lloc = 0.f;
-  for (int i = tid; i < n; i += blockDim.x) {
-    const size_t sl = ((s0 + i) * H + h) * 2;
-    const float wgt = P.part_ml[sl] == -INFINITY ? 0.f : exp2f(P.part_ml[sl] - M);
-    wsl[i] = wgt;
-    lloc += wgt * P.part_ml[sl + 1];
-  }
-  for (int off = 16; off > 0; off >>= 1) lloc += __shfl_xor_sync(0xffffffffu, lloc, off);
-  __syncthreads();
-  if ((tid & 31) == 0) red[tid >> 5] = lloc;
-  __syncthreads();
-  if (tid == 0) {
-    float L = 0.f;
-    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) L += red[i];
-    s_L = L;
-  }
-  __syncthreads();
-  const float inv_l = 1.f / s_L;
-  const int width = dh + r;
+  const float* ml = P.part_ml + (s0 * H + h) * 2;
+  const float* acc0 = P.part_acc + (s0 * H + h) * W;
+  const size_t mstep = static_cast<size_t>(H) * 2, astep = static_cast<size_t>(H) * W;
   float oshared[2] = {0.f, 0.f};
-  for (int j = tid; j < width; j += blockDim.x) {
-    float a0 = 0.f, a1 = 0.f;
-    int i = 0;
-    for (; i + 1 < n; i += 2) {
-      a0 = fmaf(wsl[i], P.part_acc[((s0 + i) * H + h) * width + j], a0);
-      a1 = fmaf(wsl[i + 1], P.part_acc[((s0 + i + 1) * H + h) * width + j], a1);
+  for (int j = tid, jj = 0; j < W; j += blockDim.x, ++jj) {
+    float M = -INFINITY, L = 0.f, a = 0.f;
+    for (int i0 = 0; i0 < n; i0 += kCombinePieces) {
+      float mi[kCombinePieces], li[kCombinePieces], vi[kCombinePieces];
+#pragma unroll
+      for (int u = 0; u < kCombinePieces; ++u) {
+        const bool ok = i0 + u < n;
+        mi[u] = ok ? ml[(i0 + u) * mstep] : -INFINITY;
+        li[u] = ok ? ml[(i0 + u) * mstep + 1] : 0.f;
+        vi[u] = (ok && j < W) ? acc0[(i0 + u) * astep + j] : 0.f;
+      }
+      float Mn = M;
+#pragma unroll
+      for (int u = 0; u < kCombinePieces; ++u) Mn = fmaxf(Mn, mi[u]);
+      const float f = M == -INFINITY ? 0.f : exp2f(M - Mn);
+      L *= f;
+      a *= f;
+#pragma unroll
+      for (int u = 0; u < kCombinePieces; ++u) {
+        const float w = mi[u] == -INFINITY ? 0.f : exp2f(mi[u] - Mn);
+        L = fmaf(w, li[u], L);
+        a = fmaf(w, vi[u], a);
+      }
+      M = Mn;
     }
-    if (i < n) a0 = fmaf(wsl[i], P.part_acc[((s0 + i) * H + h) * width + j], a0);
-    const float a = (a0 + a1) * inv_l;
-    if (j < dh) oshared[j / blockDim.x] = a; else zbar[j - dh] = a;
+    if (j == 0) { s_M = M; s_L = L; }  // the same for every column
+    const float v = a / L;
+    if (j < dh) { if (jj < 2) oshared[jj] = v; }
+    else zbar[j - dh] = v;
   }
   __syncthreads();
   for (int k = tid, jj = 0; k < dh; k += blockDim.x, ++jj) {
     float a = oshared[jj];
-    const size_t base = (static_cast<size_t>(h) * dh + k) * r;
-    for (int cc = 0; cc < r; ++cc) a = fmaf(load_elem(P.b_v, base + cc, BF16), zbar[cc], a);
+    if (pre_bv) {
+#pragma unroll
+      for (int c2 = 0; c2 < kCombineRank / 2; ++c2)
+        if (2 * c2 < r) {
+          a = fmaf(bf_lo(bvp[c2]), zbar[2 * c2], a);
+          a = fmaf(bf_hi(bvp[c2]), zbar[2 * c2 + 1], a);
+        }
+    } else {
+      const size_t base = (static_cast<size_t>(h) * dh + k) * r;
+      for (int cc = 0; cc < r; ++cc) a = fmaf(load_elem(P.b_v, base + cc, BF16), zbar[cc], a);
+    }
     o[k] = a;
   }
-  if (tid == 0 && P.lse) P.lse[static_cast<size_t>(b) * H + h] = (M + log2f(s_L)) * kLn2;
+  if (tid == 0 && P.lse) P.lse[static_cast<size_t>(b) * H + h] = (s_M + log2f(s_L)) * kLn2;
 }
 
 // ======================================================================= host
@@ -678,11 +706,16 @@ SplitFn split_fn(const DecodePlan& P) {
 }
 
 template <bool BF16>
+// Every host step (tensor maps, shared-memory attributes) comes before the
+// first launch, so that the profiled interval [ev_begin, ev_end] holds the
+// scan kernel alone.
 lrkv_status launch_all(const DecodePlan& P, cudaStream_t stream, cudaEvent_t ev_begin, cudaEvent_t ev_end) {
   const bool pdl = ev_begin == nullptr && ev_end == nullptr;
-  CUtensorMap tm_k, tm_v;
+  CUtensorMap tm_k, tm_v, tm_zk, tm_zv;
   std::memset(&tm_k, 0, sizeof(tm_k));
   std::memset(&tm_v, 0, sizeof(tm_v));
+  std::memset(&tm_zk, 0, sizeof(tm_zk));
+  std::memset(&tm_zv, 0, sizeof(tm_zv));
   if (BF16) {
     const CUtensorMapSwizzle sw = P.span == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                                   : P.span == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
@@ -691,12 +724,36 @@ lrkv_status launch_all(const DecodePlan& P, cudaStream_t stream, cudaEvent_t ev_
         !make_tmap_3d_bf16(&tm_v, P.v_s, P.dh, P.max_len, P.B, P.box_cols, P.T, sw))
       return LRKV_ERR_CUDA;
   }
-  const int absorb_smem = std::max(P.dh * P.r * 4, 16);
+  const SplitFn split = P.stream ? nullptr : split_fn(P);
+  if (P.stream) {
+    const lrkv_status st = stream_prepare(P, &tm_zk, &tm_zv);
+    if (st != LRKV_OK) return st;
+  } else if (cudaFuncSetAttribute(split, cudaFuncAttributeMaxDynamicSharedMemorySize, P.smem_bytes) != cudaSuccess) {
+    return LRKV_ERR_CUDA;
+  }
+  const int absorb_smem = std::max((P.dh * P.r + kAbsorbSeq * P.dh) * 4, 16);
+  if (P.stream) {
+    // the small kernels around the scan ask for the same L1/shared split as
+    // the scan, so the SMs need no reconfiguration between the launches
+    static bool carve_set = false;
+    if (!carve_set) {
+      cudaFuncSetAttribute(lrkv_decode_absorb_kernel<BF16>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
+      cudaFuncSetAttribute(lrkv_decode_combine_kernel<BF16>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
+      carve_set = true;
+    }
+  }
   if (absorb_smem > 48 * 1024 &&
       cudaFuncSetAttribute(lrkv_decode_absorb_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            absorb_smem) != cudaSuccess)
     return LRKV_ERR_CUDA;
-  lrkv_decode_absorb_kernel<BF16><<<P.H, 256, absorb_smem, stream>>>(P);
+  if (P.combine_smem > 48 * 1024 &&
+      cudaFuncSetAttribute(lrkv_decode_combine_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           P.combine_smem) != cudaSuccess)
+    return LRKV_ERR_CUDA;
+
+  lrkv_decode_absorb_kernel<BF16><<<dim3(P.H, (P.B + kAbsorbSeq - 1) / kAbsorbSeq), 256, absorb_smem, stream>>>(P);
   if (cudaGetLastError() != cudaSuccess) return LRKV_ERR_CUDA;
   if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return LRKV_ERR_CUDA;
 
@@ -704,12 +761,9 @@ lrkv_status launch_all(const DecodePlan& P, cudaStream_t stream, cudaEvent_t ev_
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   if (P.stream) {
-    const lrkv_status st = stream_launch(P, stream, pdl, tm_k, tm_v);
+    const lrkv_status st = stream_launch(P, stream, pdl, tm_k, tm_v, tm_zk, tm_zv);
     if (st != LRKV_OK) return st;
   } else {
-    const SplitFn kern = split_fn(P);
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P.smem_bytes) != cudaSuccess)
-      return LRKV_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(P.grid);
     cfg.blockDim = dim3(kThreads);
@@ -717,7 +771,7 @@ lrkv_status launch_all(const DecodePlan& P, cudaStream_t stream, cudaEvent_t ev_
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    if (cudaLaunchKernelEx(&cfg, kern, P, tm_k, tm_v) != cudaSuccess) return LRKV_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, split, P, tm_k, tm_v) != cudaSuccess) return LRKV_ERR_CUDA;
   }
   if (ev_end && cudaEventRecord(ev_end, stream) != cudaSuccess) return LRKV_ERR_CUDA;
 
@@ -728,10 +782,6 @@ lrkv_status launch_all(const DecodePlan& P, cudaStream_t stream, cudaEvent_t ev_
   ccfg.stream = stream;
   ccfg.attrs = attr;
   ccfg.numAttrs = pdl ? 1 : 0;
-  if (P.combine_smem > 48 * 1024 &&
-      cudaFuncSetAttribute(lrkv_decode_combine_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           P.combine_smem) != cudaSuccess)
-    return LRKV_ERR_CUDA;
   if (cudaLaunchKernelEx(&ccfg, lrkv_decode_combine_kernel<BF16>, P) != cudaSuccess) return LRKV_ERR_CUDA;
   return LRKV_OK;
 }
@@ -818,11 +868,18 @@ lrkv_status decode_make_plan(const lrkv_dims& d, int num_sms, DecodePlan& P, siz
   P.ngw = 1;
   // bf16 shapes the streaming kernel covers use it; the rest (and fp32) run
   // the tile-synchronous kernel planned above
-  if (P.bf16 && env_int("LRKV_DECODE_TILE_SYNC", 0) == 0) stream_plan(P);
   P.grid = env_int("LRKV_DECODE_GRID", num_sms);
+  // the streaming kernel's grid is (range CTAs, row tiles of 16 heads): it
+  // divides P.grid by the row tiles
+  if (P.bf16 && env_int("LRKV_DECODE_TILE_SYNC", 0) == 0) stream_plan(P);
   P.min_tokens = env_int("LRKV_DECODE_MIN_TOKENS", P.stream ? 8 * P.T : 2 * P.T);
+  if (P.stream) {
+    // L2 prefetch window: about 48 MB in flight over all CTAs (L2 is 126 MB)
+    const long long per_cta = (48ll << 20) / std::max(1, P.grid * P.mt);
+    P.pfw = env_int("LRKV_DECODE_PREFETCH_TILES", static_cast<int>(per_cta / P.stage_bytes));
+  }
   const int slots = (P.B + P.grid) * P.ngw;
-  P.combine_smem = ((P.grid + 1) * P.ngw + r) * 4;
+  P.combine_smem = std::max(r, 1) * 4;
 
   // workspace: status | meta | prefix | p | part_ml | part_acc
   size_t w = 256;

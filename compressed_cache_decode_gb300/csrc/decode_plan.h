@@ -51,16 +51,26 @@ struct DecodePlan {
   int off_prefix, off_q, off_ssh, off_sp, off_w, off_alpha, off_red, off_stage;
   int stage_bytes, smem_bytes;
   int combine_smem;
-  // bf16 streaming kernel (warp-independent): consumer warps form `ng` groups
-  // of `mt` warps (one warp per 16-head MMA tile); tile i goes to stage
-  // i % stages and to group i % ng.  `ngw` partials per piece are written
-  // (1 when the groups merge on chip, else ng).
-  int stream;        // 1: bf16 streaming kernel, 0: fp32 tile-synchronous kernel
+  // bf16 streaming kernel: grid (range CTAs, row tiles of 16 heads); the 8
+  // warps of a CTA form 4 pairs, pair p takes every 4th 16-token tile of the
+  // CTA's range (tile i in stage i % stages) and each warp of the pair 8 of
+  // the 16 heads; the pairs merge on chip at the end of each (sequence,
+  // range) piece.  `ngw` partials per piece (1 here).
+  int stream;        // 1: bf16 streaming kernel, 0: tile-synchronous kernel
   int nthreads;      // block size of the scan kernel
-  int ng, mt, ngw, merge_smem;
-  int zs_stride;     // padded shared stride of one token's latents (bytes)
-  int p_stride;      // floats per row of q_h B_h^K in shared memory
-  int off_p, off_scr, off_merge, off_kv, off_z;
+  int mt;            // 16-head row tiles (grid.y of the streaming kernel)
+  int ngw;
+  int hs;            // heads per latent segment (a power of two dividing H)
+  int segw;          // latent elements per segment (hs r, a multiple of 16)
+  int segp;          // padded elements per segment row in shared memory (segw + 8)
+  int nsb;           // segments per row tile (16 / hs)
+  int zt_bytes;      // shared bytes of one latent tile (z_k or z_v) of a row tile
+  int kst;           // 16-wide steps over the latents of 8 heads (r / 2)
+  int cm_stride;     // floats per head row of the on-chip merge buffer
+  int pfw;           // tiles a CTA keeps prefetched into L2 beyond its ring
+  int zo[2][32];     // shared byte offset of 16-column latent step n of head half h2
+  int pq_bytes;      // one p/q buffer: q rows [16][dh] bf16 then p rows [16][r] fp32
+  int off_pq, off_pf, off_kv;
   // workspace carve-up
   uint32_t* status;
   int* meta;         // [0] = total tokens N, [1] = CTAs used

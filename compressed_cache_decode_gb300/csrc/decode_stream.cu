@@ -1,34 +1,47 @@
-// decode_stream.cu — the bf16 split-KV scan as independent warp streams.
+// decode_stream.cu — the bf16 split-KV scan on the tensor cores.
 //
-// One CTA owns a range of the concatenated histories (see decode.cu).  8-token
-// tiles stream through a ring of shared-memory stages filled by TMA (shared
-// rows k_s, v_s as swizzled tensor boxes, read once for all heads; latent rows
-// as per-token bulk copies into padded rows).  Warps work independently: warp
-// (group, m) takes every ng-th tile and handles the 16 heads of MMA row tile
-// m; the group that finishes a tile refills its stage with the tile `stages`
-// ahead, so there is no separate producer.  Per tile, FlashAttention-2 style:
-//   * shared scores q_h . k_s on the tensor cores (bf16 mma.sync, heads are
-//     the rows, q kept in registers as A fragments for the whole piece);
-//   * private scores p_h . z_k,h in fp32 (p_h = q_h B_h^K from the absorb
-//     kernel), added before the softmax;
-//   * ONE online softmax per head (row max over the quad of lanes holding the
-//     row) over the summed scores ("Low-Rank Key Value Attention | What a
-//     shared cache can preserve", §3, fused online-softmax paragraph);
-//   * shared values on the tensor cores with the probabilities reused from
-//     the score fragments as the A operand; private values sum_j a_j z_v,h,j
-//     in fp32 with the same rescale factor.
-// No CTA-wide barrier is taken per tile.  At the end of each (sequence,
-// range) piece the groups' partial states are merged on chip (tree through
-// shared memory) or written per group for the combine kernel.
+// Grid (range CTAs, row tiles): CTA (c, m) owns a range of the concatenated
+// histories (see decode.cu) and the 16 heads of row tile m.  16-token tiles
+// stream through a ring of shared-memory stages, four tensor copies per tile:
+// the shared rows k_s and v_s as 128-byte-swizzled boxes, and this row tile's
+// latents z_k, z_v as one box of [segment][token][segment row] where a
+// segment holds the latents of `hs` heads and each segment row is padded to
+// an odd number of 16-byte chunks (the box is 8 elements wider than the
+// segment; TMA fills the excess with zeros), so that ldmatrix over 8 token
+// rows is free of bank conflicts.
+//
+// The 8 warps work independently: warp w takes every 8th tile and refills
+// the stage it consumed with the tile `stages` ahead.  Per tile (16 tokens x
+// 16 heads), FlashAttention-2 style, everything on the tensor cores
+// (bf16 mma.sync, fp32 accumulation):
+//   * scores, transposed (tokens are the M dimension):
+//       S^T = K_s q^T + Z_k P_bd, where P_bd is block diagonal: column h
+//       holds p_h = q_h B_h^K on the rows of head h's latents.  p_h is split
+//       into bf16 hi + lo parts, so the private score keeps ~16 bits of p.
+//   * ONE online softmax per head over the summed scores ("Low-Rank Key
+//     Value Attention | What a shared cache can preserve", §3, fused
+//     online-softmax paragraph), with a lazily raised reference maximum.
+//   * the probabilities are transposed in registers (movmatrix) into the A
+//     operand (heads x tokens) of
+//       O_s += P V_s            (shared values)
+//       O_z[h] += P[h] Z_v,h    (private values: one MMA per head and 8
+//                                latent columns with A masked to row h, so
+//                                all 16 heads share one accumulator set).
+// At the end of each (sequence, range) piece the warps' states are merged
+// on chip (a tree through shared memory) and written as the piece's partial.
 #include <cmath>
 #include <algorithm>
 #include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include <cuda.h>
 
 #include "decode_common.cuh"
 #include "decode_plan.h"
 #include "ptx.cuh"
+#include "tmap.h"
 
 namespace lrkv {
 
@@ -36,8 +49,11 @@ using namespace dec;
 
 namespace {
 
-constexpr int kT = 8;                 // tokens per tile (one MMA n-tile)
-constexpr int kScratch = 16 * 8 + 32;  // floats of per-warp scratch
+constexpr int kT = 16;                       // tokens per tile
+constexpr int kWarps = kStreamConsumers;     // token streams per CTA
+constexpr int kThreadsS = 32 * kWarps;
+constexpr int kPairs = kWarps / 2;           // a tile is shared by a pair (8 heads each)
+constexpr float kRescaleLog2 = 8.f;          // raise the reference max only past 2^8
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -46,10 +62,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 __device__ __forceinline__ void named_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 // Pieces of this CTA's token range: (sequence b, rows [t_beg, t_end)).
@@ -74,44 +86,6 @@ __device__ __forceinline__ bool piece_next(Piece& p, const int* pre, int B, int 
   return true;
 }
 
-// Producer warp: the copies of tile (piece p, row t0) into stage s.
-__device__ __forceinline__ void stream_issue(const DecodePlan& P, const CUtensorMap* tm_k,
-                                             const CUtensorMap* tm_v, unsigned char* smem, uint64_t* full,
-                                             int s, int b, int t0, int nvalid, int lane) {
-  unsigned char* ks = smem + P.off_kv + static_cast<size_t>(s) * 2 * P.kv_bytes;
-  unsigned char* vs = ks + P.kv_bytes;
-  unsigned char* zk = smem + P.off_z + static_cast<size_t>(s) * 2 * kT * P.zs_stride;
-  unsigned char* zv = zk + kT * P.zs_stride;
-  fence_proxy_async_smem();  // earlier generic reads of the stage before the async writes
-  if (lane == 0) {
-    mbar_arrive_expect_tx(&full[s], 2u * kT * P.dh * 2u + 2u * static_cast<uint32_t>(nvalid) * P.z_row);
-  }
-  __syncwarp();
-  if (lane < P.nbox) {
-    tma_load_3d(ks + lane * kT * P.span, tm_k, lane * P.box_cols, t0, b, &full[s]);
-    tma_load_3d(vs + lane * kT * P.span, tm_v, lane * P.box_cols, t0, b, &full[s]);
-  }
-  if (P.r > 0 && lane < 2 * nvalid) {
-    const int row = lane >> 1;
-    const size_t g = (static_cast<size_t>(b) * P.max_len + t0 + row) * P.z_row;
-    if (lane & 1)
-      tma_load_1d(zv + row * P.zs_stride, static_cast<const unsigned char*>(P.z_v) + g, P.z_row, &full[s]);
-    else
-      tma_load_1d(zk + row * P.zs_stride, static_cast<const unsigned char*>(P.z_k) + g, P.z_row, &full[s]);
-  }
-}
-
-// Per-warp partial state of 16 heads, moved through shared memory or global.
-// Row layout (width W = dh + r + 2): [m, l, acc_s[dh], acc_z[r]].
-template <int DHT, int RMAX>
-struct WarpState {
-  float m0, m1, l0, l1;           // rows g and g+8 of the MMA tile
-  float acc_v[2 * DHT][4];        // shared-value fragments
-  float acc_z[RMAX];              // private sum of head hh = lane & 15
-};
-
-}  // namespace
-
 // Walks the tile sequence forward (monotone), giving the coordinates of tile j.
 struct TileCursor {
   Piece pc;
@@ -126,38 +100,153 @@ struct TileCursor {
   }
 };
 
-template <int DHT, int RMAX, int NE>
-__global__ void __launch_bounds__(32 * kStreamConsumers, 1)
+// The copies of tile (sequence b, rows t0..t0+15) into stage s (one thread).
+__device__ __forceinline__ void stream_issue(const DecodePlan& P, const CUtensorMap* tk, const CUtensorMap* tv,
+                                             const CUtensorMap* tzk, const CUtensorMap* tzv,
+                                             unsigned char* smem, uint64_t* full, int s, int b, int t0,
+                                             int zseg0) {
+  unsigned char* ks = smem + P.off_kv + static_cast<size_t>(s) * P.stage_bytes;
+  unsigned char* vs = ks + P.kv_bytes;
+  unsigned char* zk = vs + P.kv_bytes;
+  unsigned char* zv = zk + P.zt_bytes;
+  mbar_arrive_expect_tx(&full[s], 2u * P.nbox * kT * 128u + 2u * static_cast<uint32_t>(P.zt_bytes));
+  for (int cb = 0; cb < P.nbox; ++cb) {
+    tma_load_3d(ks + cb * kT * 128, tk, cb * 64, t0, b, &full[s]);
+    tma_load_3d(vs + cb * kT * 128, tv, cb * 64, t0, b, &full[s]);
+  }
+  if (P.r > 0) {
+    tma_load_4d(zk, tzk, 0, t0, zseg0, b, &full[s]);
+    tma_load_4d(zv, tzv, 0, t0, zseg0, b, &full[s]);
+  }
+}
+
+// p = q B^K (fp32) and q (bf16) of the row tile's heads of sequence b into
+// buffer `buf` (one thread).
+__device__ __forceinline__ void pq_issue(const DecodePlan& P, unsigned char* smem, uint64_t* pbar, int buf, int b,
+                                         int m0) {
+  const int nh = min(16, P.H - m0);
+  const uint32_t pbytes = static_cast<uint32_t>(nh * P.r * 4), qbytes = static_cast<uint32_t>(nh * P.dh * 2);
+  unsigned char* dst = smem + P.off_pq + buf * P.pq_bytes;
+  mbar_arrive_expect_tx(&pbar[buf], pbytes + qbytes);
+  tma_load_1d(dst, static_cast<const unsigned char*>(P.q) + (static_cast<size_t>(b) * P.H + m0) * P.dh * 2, qbytes,
+              &pbar[buf]);
+  if (pbytes)
+    tma_load_1d(dst + 16 * P.dh * 2, P.p_abs + (static_cast<size_t>(b) * P.H + m0) * P.r, pbytes, &pbar[buf]);
+}
+
+__device__ __forceinline__ void prefetch_tmap(const void* p) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(p) : "memory");
+}
+
+// Stage s holds tile issued[s]; a consumer waits for its tile to be issued
+// before it waits on the stage's barrier, so the parity it waits for always
+// names the barrier's current phase (a waiter two phases ahead would take
+// the completed phase two back for its own).  Bounded like the barrier wait.
+__device__ __forceinline__ bool wait_issued(const int* issued, int want) {
+  const volatile int* p = issued;
+  if (*p >= want) return true;
+  const long long t0 = clock64();
+  while (*p < want) {
+    if (clock64() - t0 > kWaitLimitCycles) return false;
+  }
+  return true;
+}
+
+// L2 prefetch of the cache rows [r0, r1) of sequence b: the shared rows and
+// the latent rows of all heads (each contiguous in memory), by bulk copies
+// with no destination, so that HBM streams ahead of the shared-memory ring.
+__device__ __forceinline__ void l2_prefetch_rows(const DecodePlan& P, int b, int r0, int r1) {
+  if (r1 <= r0) return;
+  const size_t row0 = static_cast<size_t>(b) * P.max_len + r0;
+  const uint32_t n = static_cast<uint32_t>(r1 - r0);
+  const uint32_t kv = static_cast<uint32_t>(P.dh) * 2u, zr = static_cast<uint32_t>(P.H * P.r) * 2u;
+  l2_prefetch_bulk(static_cast<const unsigned char*>(P.k_s) + row0 * kv, n * kv);
+  l2_prefetch_bulk(static_cast<const unsigned char*>(P.v_s) + row0 * kv, n * kv);
+  if (zr) {
+    l2_prefetch_bulk(static_cast<const unsigned char*>(P.z_k) + row0 * zr, n * zr);
+    l2_prefetch_bulk(static_cast<const unsigned char*>(P.z_v) + row0 * zr, n * zr);
+  }
+}
+
+// L2 prefetch of the tiles [t0, t1) of a CTA's range in tile order, in
+// chunks of up to kPrefetchChunk tiles of one piece (one thread).
+constexpr int kPrefetchChunk = 4;
+__device__ __forceinline__ void l2_prefetch_tiles(const DecodePlan& P, const int* pre, int B, int g0, int g1,
+                                                  int t0, int t1) {
+  TileCursor cur;
+  cur.more = piece_first(cur.pc, pre, B, g0, g1);
+  cur.ibase = 0;
+  int j = t0;
+  while (j < t1 && cur.seek(j, pre, B, g1)) {
+    const int e = min(min(t1, j + kPrefetchChunk), cur.ibase + cur.pc.ntiles);
+    const int r0 = cur.pc.t_beg + (j - cur.ibase) * kT;
+    l2_prefetch_rows(P, cur.pc.b, r0, min(cur.pc.t_end, cur.pc.t_beg + (e - cur.ibase) * kT));
+    j = e;
+  }
+}
+
+}  // namespace
+
+template <int DHT, int MZMAX>
+__global__ void __launch_bounds__(kThreadsS, 1)
     lrkv_decode_stream_kernel(const DecodePlan P, const __grid_constant__ CUtensorMap tm_k,
-                              const __grid_constant__ CUtensorMap tm_v) {
+                              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_zk,
+                              const __grid_constant__ CUtensorMap tm_zv) {
+  constexpr int MZA = MZMAX > 0 ? MZMAX : 1;
+  constexpr int BS = MZA > 16 ? 2 : 4;       // private-score steps per load batch
+  constexpr int BZ = MZA > 16 ? 4 : 8;       // private-value steps per load batch
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  __shared__ int s_bad;
   __shared__ int s_timeout;
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int pair = warp >> 1, hf = warp & 1;     // tile stream, half of the row tile's heads
+  const int g = lane >> 2, q4 = lane & 3;
+  const int arow = lane & 15, ahalf = lane >> 4;            // ldmatrix rows for the score A operand
+  const int trow = (lane & 7) + 8 * (lane >> 4), tcol = (lane >> 3) & 1;  // ... for transposed A
   const int B = P.B, H = P.H, dh = P.dh, r = P.r;
-  const int n_cons = P.ng * P.mt;  // warps
-  const int W = dh + r + 2;
+  const int m0 = blockIdx.y * 16;                 // first head of the row tile
+  const int zseg0 = blockIdx.y * P.nsb;           // its first latent segment
 
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* empty = full + P.stages;
+  int* issued = reinterpret_cast<int*>(smem + 128);   // [16] tile in each stage
+  int* cons = reinterpret_cast<int*>(smem + 192);     // [16] warps done with each stage
+  uint64_t* pbar = reinterpret_cast<uint64_t*>(smem + 256);  // [2] p/q buffers
+  int* zo = reinterpret_cast<int*>(smem + 320);       // [2][32] latent step offsets
   int* pre = reinterpret_cast<int*>(smem + P.off_prefix);
-  float* p_sh = reinterpret_cast<float*>(smem + P.off_p);
+  uint4* pf = reinterpret_cast<uint4*>(smem + P.off_pf);    // private-score B fragments
+  float* mbuf = reinterpret_cast<float*>(smem + P.off_pf);  // merge buffer (same region)
 
-  // ---- 1. sequence starts (clamped lengths) --------------------------------
-  if (tid == 0) { s_bad = 0; s_timeout = 0; }
-  __syncthreads();
+  // ---- 1. barriers, sequence starts (clamped lengths) ----------------------
+  if (tid == 0) {
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+    if (r > 0) {
+      prefetch_tmap(&tm_zk);
+      prefetch_tmap(&tm_zv);
+    }
+    s_timeout = 0;
+    for (int s = 0; s < P.stages; ++s) {
+      mbar_init(&full[s], 1);
+      issued[s] = -1;
+      cons[s] = 0;
+    }
+    mbar_init(&pbar[0], 1);
+    mbar_init(&pbar[1], 1);
+    fence_barrier_init();
+  }
+  if (tid < 64) zo[tid] = P.zo[tid >> 5][tid & 31];
+  int bad = 0;
   for (int b = tid; b < B; b += blockDim.x) {
     int L = P.seq_lens[b];
     if (L < 0 || L > P.max_len) {
-      s_bad = 1;
+      bad = 1;
       L = min(max(L, 0), P.max_len);
     }
     pre[b + 1] = L;
   }
   if (tid == 0) pre[0] = 0;
-  __syncthreads();
+  bad = __syncthreads_or(bad);
   if (warp == 0) {
     int carry = 0;
     for (int base = 1; base <= B; base += 32) {
@@ -175,330 +264,348 @@ __global__ void __launch_bounds__(32 * kStreamConsumers, 1)
   __syncthreads();
   const int N = pre[B];
   const int G = max(1, min(static_cast<int>(gridDim.x), (N + P.min_tokens - 1) / max(P.min_tokens, 1)));
-  if (blockIdx.x == 0) {
+  if (blockIdx.x == 0 && blockIdx.y == 0) {
     for (int b = tid; b <= B; b += blockDim.x) P.prefix[b] = pre[b];
     if (tid == 0) { P.meta[0] = N; P.meta[1] = G; }
   }
   if (N == 0 || static_cast<int>(blockIdx.x) >= G) {
-    if (s_bad && tid == 0) { pdl_wait(); record_status(P.status, kDevBounds); }
+    if (bad && tid == 0) { pdl_wait(); record_status(P.status, kDevBounds); }
     return;
   }
   const int c = blockIdx.x;
   const int g0 = static_cast<int>(static_cast<long long>(c) * N / G);
   const int g1 = static_cast<int>(static_cast<long long>(c + 1) * N / G);
-
-  if (tid == 0) {
-    for (int s = 0; s < P.stages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 32 * P.mt);
-    }
-    fence_barrier_init();
-  }
-  __syncthreads();
-
-  // ---- first `stages` tiles: each group issues the ones it will consume ----
-  {
-    const int gi0 = warp / P.mt;
-    if (warp % P.mt == 0) {
-      TileCursor cur;
-      cur.more = piece_first(cur.pc, pre, B, g0, g1);
-      cur.ibase = 0;
-      for (int j = gi0; j < P.stages && cur.seek(j, pre, B, g1); j += P.ng) {
-        const int t0 = cur.pc.t_beg + (j - cur.ibase) * kT;
-        stream_issue(P, &tm_k, &tm_v, smem, full, j, cur.pc.b, t0, min(kT, cur.pc.t_end - t0), lane);
-      }
-    }
-  }
-
-  // ============================================================ warps ====
   pdl_wait();  // p = q B^K from the absorb kernel
-  if (s_bad && tid == 0) record_status(P.status, kDevBounds);
+  if (bad && tid == 0) record_status(P.status, kDevBounds);
 
-  const int gi = warp / P.mt, mi = warp % P.mt;
-  const int g = lane >> 2, q4 = lane & 3;
-  const int hh = lane & 15, tp = lane >> 4;  // private-value role: head, token parity
-  float* scr = reinterpret_cast<float*>(smem + P.off_scr) + warp * kScratch;
-  float* mbuf = reinterpret_cast<float*>(smem + P.off_merge);
-  const int nct = n_cons * 32;
-
-  WarpState<DHT, RMAX> st;
-  uint32_t qa[DHT][4];
-
+  // ---- 2. p and q of the first piece, then the first `stages` tiles (warp w
+  // issues tiles w, w + 8, ...), so that the small copies land first ---------
   Piece pc;
   bool more = piece_first(pc, pre, B, g0, g1);
-  int ibase = 0;      // global tile index of the piece's first tile
+  if (tid == 0) pq_issue(P, smem, pbar, 0, pc.b, m0);
+  if (lane == 0) {
+    TileCursor cur;
+    cur.pc = pc;
+    cur.more = more;
+    cur.ibase = 0;
+    for (int j = warp; j < P.stages && cur.seek(j, pre, B, g1); j += kWarps) {
+      stream_issue(P, &tm_k, &tm_v, &tm_zk, &tm_zv, smem, full, j, cur.pc.b,
+                   cur.pc.t_beg + (j - cur.ibase) * kT, zseg0);
+      *reinterpret_cast<volatile int*>(&issued[j]) = j;
+    }
+  }
+  // the next pfw tiles start streaming into L2 now
+  if (tid == 32) l2_prefetch_tiles(P, pre, B, g0, g1, P.stages, P.stages + P.pfw);
+
+  uint32_t qb[DHT][2];      // q of head 8 hf + g as the B operand (k = head dim)
+  float acc_v[DHT][4];      // O_s^T: rows d = 16 m + g (+8), columns heads 2 q4 + e
+  float acc_z[MZA][4];      // O_z^T: rows latent column j = 16 m + g (+8) of this half
+  float mc[2], lc[2];       // reference max and denominator of head 8 hf + 2 q4 + e
+  const int zrow = P.segp * 2;  // bytes per segment row
+  const int hb = 8 * hf;        // first head (row-tile local) of this half
+
+  int ibase = 0;      // tile index of the piece's first tile
+  int kp = 0;         // piece counter (p/q buffer kp & 1)
   bool ok = true;
-  TileCursor refill;  // tiles this warp issues (index of its tile + stages)
+  TileCursor refill;  // tiles this pair issues (its tile + stages)
   refill.more = piece_first(refill.pc, pre, B, g0, g1);
   refill.ibase = 0;
+  TileCursor pfcur = refill;  // tiles this pair prefetches into L2
   while (more) {
-    // ---- piece set-up: p_h for the heads, q fragments of this warp's tile --
-    named_sync(1, nct);  // the previous piece's merge is finished
+    // ---- piece set-up: p and q of the row tile --------------------------------
+    named_sync(1, kThreadsS);  // the previous piece's merge is done with the buffer
+    const int buf = kp & 1;
+    if (tid == 0) {
+      Piece nx = pc;
+      if (piece_next(nx, pre, B, g1)) {  // prefetch the next piece's p and q
+        fence_proxy_async_smem();
+        pq_issue(P, smem, pbar, buf ^ 1, nx.b, m0);
+      }
+    }
+    if (ok) {
+      ok = mbar_wait_bounded(&pbar[buf], static_cast<uint32_t>(kp >> 1) & 1u);
+      if (!ok) *reinterpret_cast<volatile int*>(&s_timeout) = 1;
+    }
+    const unsigned char* pqb = smem + P.off_pq + buf * P.pq_bytes;
+    const int nh = min(16, H - m0);
     {
-      const float* gp = P.p_abs + static_cast<size_t>(pc.b) * H * r;
-      for (int i = tid; i < H * r; i += nct) p_sh[(i / r) * P.p_stride + (i % r)] = gp[i];
-      const __nv_bfloat16* gq = static_cast<const __nv_bfloat16*>(P.q) + static_cast<size_t>(pc.b) * H * dh;
-      const int h0 = mi * 16 + g, h1 = h0 + 8;
+      const __nv_bfloat16* qsm = reinterpret_cast<const __nv_bfloat16*>(pqb);
+      const int hl = hb + g;
 #pragma unroll
       for (int kk = 0; kk < DHT; ++kk) {
         const int k = kk * 16 + 2 * q4;
-        qa[kk][0] = h0 < H ? *reinterpret_cast<const uint32_t*>(gq + h0 * dh + k) : 0u;
-        qa[kk][1] = h1 < H ? *reinterpret_cast<const uint32_t*>(gq + h1 * dh + k) : 0u;
-        qa[kk][2] = h0 < H ? *reinterpret_cast<const uint32_t*>(gq + h0 * dh + k + 8) : 0u;
-        qa[kk][3] = h1 < H ? *reinterpret_cast<const uint32_t*>(gq + h1 * dh + k + 8) : 0u;
+        qb[kk][0] = hl < nh ? *reinterpret_cast<const uint32_t*>(qsm + hl * dh + k) : 0u;
+        qb[kk][1] = hl < nh ? *reinterpret_cast<const uint32_t*>(qsm + hl * dh + k + 8) : 0u;
       }
     }
-    st.m0 = st.m1 = -INFINITY;
-    st.l0 = st.l1 = 0.f;
+    mc[0] = mc[1] = -INFINITY;
+    lc[0] = lc[1] = 0.f;
 #pragma unroll
-    for (int n = 0; n < 2 * DHT; ++n)
+    for (int n = 0; n < DHT; ++n)
 #pragma unroll
-      for (int k = 0; k < 4; ++k) st.acc_v[n][k] = 0.f;
+      for (int k = 0; k < 4; ++k) acc_v[n][k] = 0.f;
 #pragma unroll
-    for (int k = 0; k < RMAX; ++k) st.acc_z[k] = 0.f;
-    named_sync(1, nct);  // p_sh ready
+    for (int n = 0; n < MZA; ++n)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc_z[n][k] = 0.f;
+    if (MZMAX > 0) {
+      // B fragment of k step kk of half h2 for lane L: {hi(b0), hi(b1),
+      // lo(b0), lo(b1)}, b0 = rows j, j+1 and b1 = rows j+8, j+9
+      // (j = 16 (h2 kst + kk) + 2 (L & 3)) of head 8 h2 + (L >> 2).
+      const float* ps = reinterpret_cast<const float*>(pqb + 16 * dh * 2);
+      const int nent = 2 * P.kst * 32;
+      for (int e = tid; e < nent; e += kThreadsS) {
+        const int k = e >> 5, L = e & 31;
+        const int hl = 8 * (k >= P.kst ? 1 : 0) + (L >> 2);
+        const int j = 16 * k + 2 * (L & 3);
+        float hi[4], lo[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int cc = j + (u & 1) + 8 * (u >> 1) - hl * r;
+          const float v = (hl < nh && cc >= 0 && cc < r) ? ps[hl * r + cc] : 0.f;
+          hi[u] = __bfloat162float(__float2bfloat16_rn(v));
+          lo[u] = v - hi[u];
+        }
+        pf[e] = make_uint4(pack_bf16(hi[0], hi[1]), pack_bf16(hi[2], hi[3]), pack_bf16(lo[0], lo[1]),
+                           pack_bf16(lo[2], lo[3]));
+      }
+    }
+    named_sync(1, kThreadsS);  // fragments ready
 
-    // ---- this group's tiles of the piece ------------------------------------
-    const int first = ibase + ((gi - ibase) % P.ng + P.ng) % P.ng;
-    for (int i = first; i < ibase + pc.ntiles; i += P.ng) {
+    // ---- this pair's tiles of the piece ----------------------------------------
+    const int first = ibase + ((pair - ibase) % kPairs + kPairs) % kPairs;
+    for (int i = first; i < ibase + pc.ntiles; i += kPairs) {
       const int s = i % P.stages;
       const int t0 = pc.t_beg + (i - ibase) * kT;
       const int nvalid = min(kT, pc.t_end - t0);
       if (ok) {
-        ok = mbar_wait_bounded(&full[s], static_cast<uint32_t>(i / P.stages) & 1u);
+        ok = wait_issued(&issued[s], i) && mbar_wait_bounded(&full[s], static_cast<uint32_t>(i / P.stages) & 1u);
         if (!ok) *reinterpret_cast<volatile int*>(&s_timeout) = 1;
       }
       if (ok && !*reinterpret_cast<volatile int*>(&s_timeout)) {
-        const unsigned char* ks = smem + P.off_kv + static_cast<size_t>(s) * 2 * P.kv_bytes;
-        const unsigned char* vs = ks + P.kv_bytes;
-        const unsigned char* zk = smem + P.off_z + static_cast<size_t>(s) * 2 * kT * P.zs_stride;
-        const unsigned char* zv = zk + kT * P.zs_stride;
+        unsigned char* ks = smem + P.off_kv + static_cast<size_t>(s) * P.stage_bytes;
+        unsigned char* vs = ks + P.kv_bytes;
+        unsigned char* zk = vs + P.kv_bytes;
+        unsigned char* zv = zk + P.zt_bytes;
+        // token masks of the value operands: rows past the history (unwritten
+        // cache rows) must not meet their zero probabilities as 0 x NaN
+        const uint32_t keep0 = (2 * q4 < nvalid ? 0x0000ffffu : 0u) | (2 * q4 + 1 < nvalid ? 0xffff0000u : 0u);
+        const uint32_t keep1 = (2 * q4 + 8 < nvalid ? 0x0000ffffu : 0u) | (2 * q4 + 9 < nvalid ? 0xffff0000u : 0u);
 
-        // shared scores: rows = heads of tile mi, columns = the 8 tokens
-        float sv[4] = {0.f, 0.f, 0.f, 0.f};
+        // scores S^T (rows = tokens g / g+8, columns = heads hb + 2 q4 + e),
+        // four independent accumulation chains
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+        float la[4] = {0.f, 0.f, 0.f, 0.f}, lb[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+          uint32_t a[DHT][4];
 #pragma unroll
-        for (int kk = 0; kk < DHT; ++kk) {
-          const int k0 = kk * 16 + ((lane >> 3) & 1) * 8;
-          uint32_t b0, b1;
-          ldsm_x2(b0, b1, ks + (k0 / P.box_cols) * kT * P.span + swz_off(lane & 7, (k0 % P.box_cols) / 8, P.span));
-          mma_bf16_16816(sv, qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+          for (int kk = 0; kk < DHT; ++kk) {
+            const int ch = 2 * kk + ahalf;
+            ldsm_x4(a[kk][0], a[kk][1], a[kk][2], a[kk][3], ks + (ch >> 3) * (kT * 128) + swz_off(arow, ch & 7, 128));
+          }
+#pragma unroll
+          for (int kk = 0; kk < DHT; ++kk)
+            mma_bf16_16816((kk & 1) ? sb : sa, a[kk][0], a[kk][1], a[kk][2], a[kk][3], qb[kk][0], qb[kk][1]);
         }
-        // private scores of (head g / g+8, token 2q4 / 2q4+1)
-        if (r > 0) {
+        if (MZMAX > 0) {
+          const unsigned char* z0 = zk + arow * zrow + ahalf * 16;
+          const int* zoh = zo + 32 * hf;
+          const uint4* pfl = pf + hf * P.kst * 32 + lane;
+          for (int kk = 0; kk < P.kst; kk += BS) {  // batches of BS steps (kst is even)
+            uint32_t a[BS][4];
+            uint4 f[BS];
 #pragma unroll
-          for (int hs = 0; hs < 2; ++hs) {
-            const int h = mi * 16 + g + 8 * hs;
-            if (h < H) {
-              const float* ph = p_sh + h * P.p_stride;
-              const unsigned char* z0 = zk + (2 * q4) * P.zs_stride + h * r * 2;
-              float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-              for (int c0 = 0; c0 < RMAX; c0 += NE) {
-                if (c0 < r) {
-                  float pv[NE], x0[NE], x1[NE];
-#pragma unroll
-                  for (int e = 0; e < NE; e += 4) {
-                    const float4 v = *reinterpret_cast<const float4*>(ph + c0 + e);
-                    pv[e] = v.x; pv[e + 1] = v.y; pv[e + 2] = v.z; pv[e + 3] = v.w;
-                  }
-                  load_vec<true, NE>(z0 + c0 * 2, x0);
-                  load_vec<true, NE>(z0 + P.zs_stride + c0 * 2, x1);
-#pragma unroll
-                  for (int e = 0; e < NE; ++e) {
-                    a0[e & 3] = fmaf(x0[e], pv[e], a0[e & 3]);
-                    a1[e & 3] = fmaf(x1[e], pv[e], a1[e & 3]);
-                  }
-                }
+            for (int u = 0; u < BS; ++u)
+              if (u < 2 || kk + u < P.kst) {
+                ldsm_x4(a[u][0], a[u][1], a[u][2], a[u][3], z0 + zoh[kk + u]);
+                f[u] = pfl[(kk + u) * 32];
               }
-              sv[2 * hs] += (a0[0] + a0[1]) + (a0[2] + a0[3]);
-              sv[2 * hs + 1] += (a1[0] + a1[1]) + (a1[2] + a1[3]);
-            }
-          }
-        }
-        // scale, mask rows past the piece's end, one online softmax per head
-        const bool v0 = 2 * q4 < nvalid, v1 = 2 * q4 + 1 < nvalid;
-        sv[0] = v0 ? sv[0] * P.scale_log2 : -INFINITY;
-        sv[1] = v1 ? sv[1] * P.scale_log2 : -INFINITY;
-        sv[2] = v0 ? sv[2] * P.scale_log2 : -INFINITY;
-        sv[3] = v1 ? sv[3] * P.scale_log2 : -INFINITY;
-        float mx0 = fmaxf(sv[0], sv[1]), mx1 = fmaxf(sv[2], sv[3]);
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        const float mn0 = fmaxf(st.m0, mx0), mn1 = fmaxf(st.m1, mx1);
-        const float al0 = exp2f(st.m0 - mn0), al1 = exp2f(st.m1 - mn1);  // mn is finite
-        st.m0 = mn0;
-        st.m1 = mn1;
-        const float p0 = exp2f(sv[0] - mn0), p1 = exp2f(sv[1] - mn0);
-        const float p2 = exp2f(sv[2] - mn1), p3 = exp2f(sv[3] - mn1);
-        st.l0 = st.l0 * al0 + (p0 + p1);
-        st.l1 = st.l1 * al1 + (p2 + p3);
-        if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
-          for (int n = 0; n < 2 * DHT; ++n) {
-            st.acc_v[n][0] *= al0; st.acc_v[n][1] *= al0;
-            st.acc_v[n][2] *= al1; st.acc_v[n][3] *= al1;
-          }
-        }
-        // shared values: the probabilities are the A fragment of m16n8k8
-        const uint32_t pa0 = pack_bf16(p0, p1), pa1 = pack_bf16(p2, p3);
-        const uint32_t keep = (v0 ? 0x0000ffffu : 0u) | (v1 ? 0xffff0000u : 0u);
-#pragma unroll
-        for (int n = 0; n < 2 * DHT; ++n) {
-          const int n0 = n * 8;
-          uint32_t b0;
-          ldsm_x1_trans(b0, vs + (n0 / P.box_cols) * kT * P.span + swz_off(lane & 7, (n0 % P.box_cols) / 8, P.span));
-          mma_bf16_1688(st.acc_v[n], pa0, pa1, b0 & keep);
-        }
-        // private values: lane (head hh, token parity tp)
-        if (r > 0) {
-          scr[g * 8 + 2 * q4] = p0;
-          scr[g * 8 + 2 * q4 + 1] = p1;
-          scr[(g + 8) * 8 + 2 * q4] = p2;
-          scr[(g + 8) * 8 + 2 * q4 + 1] = p3;
-          if (q4 == 0) { scr[128 + g] = al0; scr[128 + g + 8] = al1; }
-          __syncwarp();
-          const int h = mi * 16 + hh;
-          if (h < H) {
-            const float a = scr[128 + hh];
-            if (a != 1.f) {
-#pragma unroll
-              for (int k = 0; k < RMAX; ++k) st.acc_z[k] *= a;
-            }
-#pragma unroll
-            for (int k = 0; k < kT / 2; ++k) {
-              const int t = tp + 2 * k;
-              if (t < nvalid) {
-                const float w = scr[hh * 8 + t];
-                const unsigned char* zt = zv + t * P.zs_stride + h * r * 2;
-#pragma unroll
-                for (int c0 = 0; c0 < RMAX; c0 += NE) {
-                  if (c0 < r) {
-                    float x[NE];
-                    load_vec<true, NE>(zt + c0 * 2, x);
-#pragma unroll
-                    for (int e = 0; e < NE; ++e) st.acc_z[c0 + e] = fmaf(w, x[e], st.acc_z[c0 + e]);
-                  }
-                }
+            for (int u = 0; u < BS; ++u)
+              if (u < 2 || kk + u < P.kst) {
+                mma_bf16_16816((u & 1) ? sb : sa, a[u][0], a[u][1], a[u][2], a[u][3], f[u].x, f[u].y);
+                mma_bf16_16816((u & 1) ? lb : la, a[u][0], a[u][1], a[u][2], a[u][3], f[u].z, f[u].w);
               }
-            }
           }
-          __syncwarp();
+        }
+
+        // scale, mask rows past the piece's end, tile max per head
+        const bool v0 = g < nvalid, v1 = g + 8 < nvalid;
+        float sc[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float t = ((sa[u] + sb[u]) + (la[u] + lb[u])) * P.scale_log2;
+          sc[u] = (u < 2 ? v0 : v1) ? t : -INFINITY;
+        }
+        float mx[2] = {fmaxf(sc[0], sc[2]), fmaxf(sc[1], sc[3])};
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+          mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xffffffffu, mx[0], o));
+          mx[1] = fmaxf(mx[1], __shfl_xor_sync(0xffffffffu, mx[1], o));
+        }
+        const bool up = mx[0] > mc[0] + kRescaleLog2 || mx[1] > mc[1] + kRescaleLog2;
+        if (__any_sync(0xffffffffu, up)) {
+          // raise the reference max of the heads that outgrew it; rescale the
+          // accumulator columns of those heads (held by this lane)
+          float al[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float mn = mx[e] > mc[e] + kRescaleLog2 ? mx[e] : mc[e];
+            al[e] = mc[e] == -INFINITY ? 0.f : exp2f(mc[e] - mn);
+            mc[e] = mn;
+            lc[e] *= al[e];
+          }
+#pragma unroll
+          for (int n = 0; n < DHT; ++n) {
+            acc_v[n][0] *= al[0]; acc_v[n][1] *= al[1]; acc_v[n][2] *= al[0]; acc_v[n][3] *= al[1];
+          }
+#pragma unroll
+          for (int n = 0; n < MZA; ++n) {
+            acc_z[n][0] *= al[0]; acc_z[n][1] *= al[1]; acc_z[n][2] *= al[0]; acc_z[n][3] *= al[1];
+          }
+        }
+        const float p0 = exp2f(sc[0] - mc[0]), p1 = exp2f(sc[1] - mc[1]);
+        const float p2 = exp2f(sc[2] - mc[0]), p3 = exp2f(sc[3] - mc[1]);
+        lc[0] += p0 + p2;
+        lc[1] += p1 + p3;
+        // P^T (tokens x heads) as the B operand: transpose the 8x8 blocks so
+        // that lane (g, q4) holds head g at tokens 2 q4, 2 q4 + 1 (and + 8)
+        const uint32_t pb0 = movmatrix_trans(pack_bf16(p0, p1));  // tokens 0-7
+        const uint32_t pb1 = movmatrix_trans(pack_bf16(p2, p3));  // tokens 8-15
+
+        // shared values: O_s^T += V_s^T P^T (rows = head dim)
+        {
+          uint32_t a[DHT][4];
+#pragma unroll
+          for (int n = 0; n < DHT; ++n) {
+            const int ch = 2 * n + tcol;
+            ldsm_x4_trans(a[n][0], a[n][1], a[n][2], a[n][3], vs + (ch >> 3) * (kT * 128) + swz_off(trow, ch & 7, 128));
+          }
+#pragma unroll
+          for (int n = 0; n < DHT; ++n)
+            mma_bf16_16816(acc_v[n], a[n][0] & keep0, a[n][1] & keep0, a[n][2] & keep1, a[n][3] & keep1, pb0, pb1);
+        }
+        // private values: O_z^T += Z_v^T P^T over this half's latent columns
+        if (MZMAX > 0) {
+          const unsigned char* z0 = zv + trow * zrow + tcol * 16;
+          const int* zoh = zo + 32 * hf;
+#pragma unroll
+          for (int n0 = 0; n0 < MZA; n0 += BZ) {  // batches of BZ steps
+            uint32_t a[BZ][4];
+#pragma unroll
+            for (int u = 0; u < BZ; ++u)
+              if (n0 + u < P.kst) ldsm_x4_trans(a[u][0], a[u][1], a[u][2], a[u][3], z0 + zoh[n0 + u]);
+#pragma unroll
+            for (int u = 0; u < BZ; ++u)
+              if (n0 + u < P.kst)
+                mma_bf16_16816(acc_z[n0 + u], a[u][0] & keep0, a[u][1] & keep0, a[u][2] & keep1, a[u][3] & keep1,
+                               pb0, pb1);
+          }
         }
       }
-      // done with the stage: refill it with tile i + stages
+      // done with the stage: the second warp of the pair refills it with
+      // tile i + stages
       const int j = i + P.stages;
-      if (P.mt > 1) mbar_arrive(&empty[s]);
-      if (mi == 0 && refill.seek(j, pre, B, g1)) {
-        if (P.mt > 1 && ok) {
-          int got = 0;
-          if (lane == 0) got = mbar_wait_bounded(&empty[s], static_cast<uint32_t>(i / P.stages) & 1u) ? 1 : 0;
-          got = __shfl_sync(0xffffffffu, got, 0);
-          if (!got) { ok = false; *reinterpret_cast<volatile int*>(&s_timeout) = 1; }
+      fence_proxy_async_smem();  // this warp's generic accesses before the async writes
+      __syncwarp();
+      int second = 0;
+      if (lane == 0) second = (atomicAdd(&cons[s], 1) & 1);
+      second = __shfl_sync(0xffffffffu, second, 0);
+      if (second && refill.seek(j, pre, B, g1)) {
+        fence_proxy_async_smem();
+        if (ok && lane == 0) {
+          stream_issue(P, &tm_k, &tm_v, &tm_zk, &tm_zv, smem, full, s, refill.pc.b,
+                       refill.pc.t_beg + (j - refill.ibase) * kT, zseg0);
+          *reinterpret_cast<volatile int*>(&issued[s]) = j;
         }
-        __syncwarp();
-        if (ok) {
-          const int jt0 = refill.pc.t_beg + (j - refill.ibase) * kT;
-          stream_issue(P, &tm_k, &tm_v, smem, full, s, refill.pc.b, jt0, min(kT, refill.pc.t_end - jt0), lane);
+        // keep the L2 prefetch window pfw tiles ahead of the ring
+        const int jp = j + P.pfw;
+        if (ok && lane == 0 && P.pfw > 0 && pfcur.seek(jp, pre, B, g1)) {
+          const int rr = pfcur.pc.t_beg + (jp - pfcur.ibase) * kT;
+          l2_prefetch_rows(P, pfcur.pc.b, rr, min(pfcur.pc.t_end, rr + kT));
         }
       }
     }
 
-    // ---- end of the piece: reduce within the warp ------------------------------
-    st.l0 += __shfl_xor_sync(0xffffffffu, st.l0, 1);
-    st.l0 += __shfl_xor_sync(0xffffffffu, st.l0, 2);
-    st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, 1);
-    st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, 2);
+    // ---- end of the piece: full denominators ------------------------------------
 #pragma unroll
-    for (int k = 0; k < RMAX; ++k) st.acc_z[k] += __shfl_xor_sync(0xffffffffu, st.acc_z[k], 16);
-
-    // write this warp's state into a row block of width W (16 head rows)
-    auto put = [&](float* dst) {
-      if (q4 == 0) {
-        dst[g * W] = st.m0; dst[g * W + 1] = st.l0;
-        dst[(g + 8) * W] = st.m1; dst[(g + 8) * W + 1] = st.l1;
-      }
-#pragma unroll
-      for (int n = 0; n < 2 * DHT; ++n) {
-        const int col = 2 + n * 8 + 2 * q4;
-        dst[g * W + col] = st.acc_v[n][0]; dst[g * W + col + 1] = st.acc_v[n][1];
-        dst[(g + 8) * W + col] = st.acc_v[n][2]; dst[(g + 8) * W + col + 1] = st.acc_v[n][3];
-      }
-      if (tp == 0) {
-#pragma unroll
-        for (int k = 0; k < RMAX; ++k)
-          if (k < r) dst[hh * W + 2 + dh + k] = st.acc_z[k];
-      }
-    };
-
-    if (P.merge_smem) {
-      // tree merge of the groups' states of the same row tile: at step s,
-      // group gi = 2sk + s hands its state to group 2sk
-      for (int step = 1; step < P.ng; step <<= 1) {
-        const int k = gi / (2 * step), rem = gi % (2 * step);
-        float* slot = mbuf + static_cast<size_t>((k * P.mt + mi)) * 16 * W;
-        if (rem == step) put(slot);
-        named_sync(1, nct);
-        if (rem == 0 && gi + step < P.ng) {
-          const float* src = slot;
-          const float mb0 = src[g * W], lb0 = src[g * W + 1];
-          const float mb1 = src[(g + 8) * W], lb1 = src[(g + 8) * W + 1];
-          const float M0 = fmaxf(st.m0, mb0), M1 = fmaxf(st.m1, mb1);
-          const float fa0 = M0 == -INFINITY ? 0.f : exp2f(st.m0 - M0);
-          const float fb0 = M0 == -INFINITY ? 0.f : exp2f(mb0 - M0);
-          const float fa1 = M1 == -INFINITY ? 0.f : exp2f(st.m1 - M1);
-          const float fb1 = M1 == -INFINITY ? 0.f : exp2f(mb1 - M1);
-          st.m0 = M0; st.m1 = M1;
-          st.l0 = st.l0 * fa0 + lb0 * fb0;
-          st.l1 = st.l1 * fa1 + lb1 * fb1;
-#pragma unroll
-          for (int n = 0; n < 2 * DHT; ++n) {
-            const int col = 2 + n * 8 + 2 * q4;
-            st.acc_v[n][0] = st.acc_v[n][0] * fa0 + src[g * W + col] * fb0;
-            st.acc_v[n][1] = st.acc_v[n][1] * fa0 + src[g * W + col + 1] * fb0;
-            st.acc_v[n][2] = st.acc_v[n][2] * fa1 + src[(g + 8) * W + col] * fb1;
-            st.acc_v[n][3] = st.acc_v[n][3] * fa1 + src[(g + 8) * W + col + 1] * fb1;
-          }
-          // factors of head hh for the private sums
-          if (q4 == 0) {
-            scr[128 + g] = fa0; scr[128 + g + 8] = fa1;
-            scr[144 + g] = fb0; scr[144 + g + 8] = fb1;
-          }
-          __syncwarp();
-          const float fa = scr[128 + hh], fb = scr[144 + hh];
-#pragma unroll
-          for (int k = 0; k < RMAX; ++k)
-            if (k < r) st.acc_z[k] = st.acc_z[k] * fa + src[hh * W + 2 + dh + k] * fb;
-          __syncwarp();
-        }
-        named_sync(1, nct);
-      }
+    for (int o = 4; o < 32; o <<= 1) {
+      lc[0] += __shfl_xor_sync(0xffffffffu, lc[0], o);
+      lc[1] += __shfl_xor_sync(0xffffffffu, lc[1], o);
     }
-    if (!P.merge_smem || gi == 0) {
-      // write the (merged) state as this piece's partial
-      const int slot = (pc.b + c) * P.ngw + (P.merge_smem ? 0 : gi);
-      float* pacc = P.part_acc + static_cast<size_t>(slot) * H * (dh + r);
-      float* pml = P.part_ml + static_cast<size_t>(slot) * H * 2;
-      const int h0 = mi * 16 + g, h1 = h0 + 8;
-      if (q4 == 0) {
-        if (h0 < H) { pml[h0 * 2] = st.m0; pml[h0 * 2 + 1] = st.l0; }
-        if (h1 < H) { pml[h1 * 2] = st.m1; pml[h1 * 2 + 1] = st.l1; }
-      }
+
+    // ---- merge the 4 pairs' states, two pairs per round ----------------------
+    // the warps of the round's pairs scatter their useful state into
+    // cm[pair][head][2 + dh + r] = (m, l, O_s, O_z); thread (head tid / 16,
+    // columns tid % 16 + 16 k) folds them into a running (M, l, row) and
+    // finally writes the piece's partial row (coalesced)
+    {
+      constexpr int KC = DHT + (2 * MZA + 15) / 16;  // columns per thread
+      const int hm = tid >> 4, t16 = tid & 15;
+      float Mr = -INFINITY, lr = 0.f, vr[KC];
 #pragma unroll
-      for (int n = 0; n < 2 * DHT; ++n) {
-        const int col = n * 8 + 2 * q4;
-        if (h0 < H) { pacc[h0 * (dh + r) + col] = st.acc_v[n][0]; pacc[h0 * (dh + r) + col + 1] = st.acc_v[n][1]; }
-        if (h1 < H) { pacc[h1 * (dh + r) + col] = st.acc_v[n][2]; pacc[h1 * (dh + r) + col + 1] = st.acc_v[n][3]; }
-      }
-      const int h = mi * 16 + hh;
-      if (tp == 0 && h < H) {
+      for (int k = 0; k < KC; ++k) vr[k] = 0.f;
+      for (int p0 = 0; p0 < kPairs; p0 += 2) {
+        named_sync(1, kThreadsS);  // tiles (first round) or the previous round's reads are done
+        if ((pair >> 1) == (p0 >> 1)) {
+          float* cmw = mbuf + static_cast<size_t>(pair - p0) * 16 * P.cm_stride;
 #pragma unroll
-        for (int k = 0; k < RMAX; ++k)
-          if (k < r) pacc[h * (dh + r) + dh + k] = st.acc_z[k];
+          for (int e = 0; e < 2; ++e) {
+            const int hl = hb + 2 * q4 + e;
+            float* row = cmw + hl * P.cm_stride;
+            if (g == 0) { row[0] = mc[e]; row[1] = lc[e]; }
+#pragma unroll
+            for (int n = 0; n < DHT; ++n) {
+              row[2 + 16 * n + g] = acc_v[n][e];
+              row[2 + 16 * n + g + 8] = acc_v[n][2 + e];
+            }
+            if (MZMAX > 0) {
+              // row j (this half) holds latent column j - (hl - hb) r of head hl
+#pragma unroll
+              for (int n = 0; n < MZA; ++n) {
+                if (n < P.kst) {
+                  const int ca = 16 * n + g - (hl - hb) * r, cb = ca + 8;
+                  if (ca >= 0 && ca < r) row[2 + dh + ca] = acc_z[n][e];
+                  if (cb >= 0 && cb < r) row[2 + dh + cb] = acc_z[n][2 + e];
+                }
+              }
+            }
+          }
+        }
+        named_sync(1, kThreadsS);
+        const float* r0 = mbuf + static_cast<size_t>(hm) * P.cm_stride;
+        const float* r1 = r0 + static_cast<size_t>(16) * P.cm_stride;
+        const float ma = r0[0], mb = r1[0];
+        const float M = fmaxf(Mr, fmaxf(ma, mb));
+        const float f = Mr == -INFINITY ? 0.f : exp2f(Mr - M);
+        const float fa = ma == -INFINITY ? 0.f : exp2f(ma - M);
+        const float fb = mb == -INFINITY ? 0.f : exp2f(mb - M);
+        lr = lr * f + r0[1] * fa + r1[1] * fb;
+        Mr = M;
+#pragma unroll
+        for (int k = 0; k < KC; ++k) {
+          const int col = t16 + 16 * k;
+          if (col < dh + r) vr[k] = vr[k] * f + r0[2 + col] * fa + r1[2 + col] * fb;
+        }
+      }
+      const int h = m0 + hm;
+      if (h < H) {
+        const int slot = pc.b + c;
+        if (t16 == 0) {
+          float* pml = P.part_ml + (static_cast<size_t>(slot) * H + h) * 2;
+          pml[0] = Mr;
+          pml[1] = lr;
+        }
+        float* o = P.part_acc + (static_cast<size_t>(slot) * H + h) * (dh + r);
+#pragma unroll
+        for (int k = 0; k < KC; ++k) {
+          const int col = t16 + 16 * k;
+          if (col < dh + r) o[col] = vr[k];
+        }
       }
     }
     ibase += pc.ntiles;
+    ++kp;
     more = piece_next(pc, pre, B, g1);
   }
   if (!ok && lane == 0) record_status(P.status, kDevTimeout);
@@ -508,19 +615,24 @@ __global__ void __launch_bounds__(32 * kStreamConsumers, 1)
 // ======================================================================= host
 namespace {
 
-using StreamFn = void (*)(const DecodePlan, const CUtensorMap, const CUtensorMap);
+using StreamFn = void (*)(const DecodePlan, const CUtensorMap, const CUtensorMap, const CUtensorMap,
+                          const CUtensorMap);
+
+int mz_max_of(const DecodePlan& P) { return P.r == 0 ? 0 : (P.kst <= 16 ? 16 : 32); }
 
 template <int DHT>
-StreamFn pick_r(const DecodePlan& P) {
-  if (P.r <= 16) return P.vec == 8 ? lrkv_decode_stream_kernel<DHT, 16, 8> : lrkv_decode_stream_kernel<DHT, 16, 4>;
-  if (P.r <= 32) return P.vec == 8 ? lrkv_decode_stream_kernel<DHT, 32, 8> : lrkv_decode_stream_kernel<DHT, 32, 4>;
-  return P.vec == 8 ? lrkv_decode_stream_kernel<DHT, 64, 8> : lrkv_decode_stream_kernel<DHT, 64, 4>;
+StreamFn pick_mz(const DecodePlan& P) {
+  switch (mz_max_of(P)) {
+    case 0: return lrkv_decode_stream_kernel<DHT, 0>;
+    case 16: return lrkv_decode_stream_kernel<DHT, 16>;
+    default: return lrkv_decode_stream_kernel<DHT, 32>;
+  }
 }
 
 StreamFn stream_fn(const DecodePlan& P) {
   switch (P.dh / 16) {
-    case 4: return pick_r<4>(P);
-    case 8: return pick_r<8>(P);
+    case 4: return pick_mz<4>(P);
+    case 8: return pick_mz<8>(P);
     default: return nullptr;
   }
 }
@@ -540,87 +652,120 @@ lrkv_status stream_plan(DecodePlan& P_out) {
 static lrkv_status stream_plan_impl(DecodePlan& P) {
   const int dh = P.dh, r = P.r, H = P.H;
   if (!(dh == 64 || dh == 128)) return LRKV_ERR_UNSUPPORTED;
-  if (r > 0 && r % 4 != 0) return LRKV_ERR_UNSUPPORTED;
+  if (r % 4 != 0 || r > 64) return LRKV_ERR_UNSUPPORTED;
   P.stream = 1;
   P.T = kT;
   P.Hp = round_up(H, 16);
   P.mt = P.Hp / 16;
-  if (P.mt > kStreamConsumers) return LRKV_ERR_UNSUPPORTED;
-  const int row_bytes = dh * 2;
-  P.span = row_bytes >= 128 ? 128 : 64;
-  P.box_cols = P.span / 2;
-  P.nbox = dh / P.box_cols;
+  P.grid = std::max(1, P.grid / P.mt);
+  P.ngw = 1;
+  P.nthreads = kThreadsS;
+  P.span = 128;
+  P.box_cols = 64;
+  P.nbox = dh / 64;
   P.kv_bytes = round_up(kT * dh * 2, 1024);
-  P.vec = (r % 8 == 0) ? 8 : 4;
-  P.z_row = H * r * 2;
-  {
-    int zs = round_up(std::max(P.z_row, 16), 16);
-    if (((zs / 16) & 1) == 0) zs += 16;
-    P.zs_stride = zs;
+  if (r > 0) {
+    // latent segment: hs heads (a power of two dividing H) whose hs r
+    // latents are a multiple of 16 elements and fit a box with 8 spare
+    P.hs = 0;
+    for (int hs = 16; hs >= 1; hs >>= 1)
+      if (H % hs == 0 && (hs * r) % 16 == 0 && hs * r + 8 <= 256) { P.hs = hs; break; }
+    if (P.hs == 0) return LRKV_ERR_UNSUPPORTED;
+    P.segw = P.hs * r;
+    P.segp = P.segw + 8;  // (segw / 8) is even, so segp / 8 is odd
+    P.nsb = 16 / P.hs;
+    P.zt_bytes = P.nsb * kT * P.segp * 2;
+    P.kst = r / 2;  // 16-wide steps over the 8 r latents of 8 heads
+    if (P.kst > 32) return LRKV_ERR_UNSUPPORTED;
+    // shared offset of step n of half h2: latent column j = 8 h2 r + 16 n
+    for (int h2 = 0; h2 < 2; ++h2)
+      for (int n = 0; n < 32; ++n) {
+        const int j = 8 * h2 * r + 16 * std::min(n, P.kst - 1);
+        P.zo[h2][n] = (j / P.segw) * kT * P.segp * 2 + (j % P.segw) * 2;
+      }
+  } else {
+    P.hs = 1; P.segw = 0; P.segp = 0; P.nsb = 0; P.zt_bytes = 0; P.kst = 0;
+    for (int h2 = 0; h2 < 2; ++h2)
+      for (int n = 0; n < 32; ++n) P.zo[h2][n] = 0;
   }
-  {
-    const int r4 = round_up(std::max(r, 1), 4);
-    P.p_stride = ((r4 / 4) & 1) ? r4 : r4 + 4;
-  }
-  const int ng_max = kStreamConsumers / P.mt;
-  const int W = dh + r + 2;
-  const int stage_bytes = 2 * P.kv_bytes + round_up(2 * kT * P.zs_stride, 16);
+  P.pq_bytes = round_up(16 * dh * 2 + 16 * r * 4, 128);
+  P.cm_stride = (dh + r + 2) | 1;  // odd: the scatter rows fall in different banks
+  P.stage_bytes = round_up(2 * P.kv_bytes + 2 * P.zt_bytes, 1024);
+  const int pf_bytes = 2 * P.kst * 32 * 16;
 
-  // shared memory: barriers | prefix | p | scratch | merge buffer | kv ring | z ring
-  auto layout = [&](int stages, int merge, int ng) {
-    int off = 256;
-    P.off_prefix = off; off = round_up(off + (P.B + 1) * 4, 16);
-    P.off_p = off; off = round_up(off + H * P.p_stride * 4, 16);
-    P.off_scr = off; off = round_up(off + (ng * P.mt) * kScratch * 4, 16);
-    P.off_merge = off; off = round_up(off + (merge ? ((ng + 1) / 2) * P.mt * 16 * W * 4 : 0), 1024);
-    P.off_kv = off; off += stages * 2 * P.kv_bytes;
-    P.off_z = off; off += stages * round_up(2 * kT * P.zs_stride, 16);
+  // shared memory: barriers | prefix | p/q buffers | p fragments / merge buffer | ring
+  const int cm_bytes = 2 * 16 * P.cm_stride * 4;
+  auto layout = [&](int stages) {
+    int off = 640;  // barriers, stage records, step offsets
+    P.off_prefix = off; off = round_up(off + (P.B + 1) * 4, 128);
+    P.off_pq = off; off = round_up(off + 2 * P.pq_bytes, 128);
+    P.off_pf = off; off = round_up(off + std::max(pf_bytes, cm_bytes), 1024);
+    P.off_kv = off; off += stages * P.stage_bytes;
     return off + 1024;  // alignment slack
   };
   const int budget = 226 * 1024;  // opt-in limit (227 KB) less static shared memory
-  // most groups whose ring holds a tile for each; merge on chip if it fits
-  int best_stages = 0, best_merge = 0, best_ng = 0;
-  for (int ng = ng_max; ng >= 1 && best_stages == 0; --ng) {
-    for (int merge = 1; merge >= 0; --merge) {
-      int stages = 0;
-      while (stages < 16 && layout(stages + 1, merge, ng) <= budget) ++stages;
-      if (stages >= ng && stages >= 2) {
-        best_stages = std::min(stages, 2 * ng);
-        best_merge = merge;
-        best_ng = ng;
-        break;
-      }
-    }
-  }
-  if (best_stages == 0) return LRKV_ERR_UNSUPPORTED;
-  P.ng = best_ng;
-  P.merge_smem = best_merge;
-  P.ngw = best_merge ? 1 : best_ng;
-  P.stages = best_stages;
-  P.smem_bytes = layout(P.stages, P.merge_smem, P.ng);
-  P.stage_bytes = stage_bytes;
-  P.nthreads = 32 * (P.ng * P.mt);
-  (void)stage_bytes;
+  int stages = 0;
+  while (stages < 16 && layout(stages + 1) <= budget) ++stages;
+  if (stages < 2) return LRKV_ERR_UNSUPPORTED;
+  P.stages = stages;
+  P.smem_bytes = layout(P.stages);
+  P.pfw = 0;  // L2 prefetch window beyond the ring (tiles); set with the grid
   return stream_fn(P) ? LRKV_OK : LRKV_ERR_UNSUPPORTED;
 }
 
-lrkv_status stream_launch(const DecodePlan& P, cudaStream_t stream, bool pdl, const CUtensorMap& tm_k,
-                          const CUtensorMap& tm_v) {
+// Host preparation of a streaming launch: the latent tensor maps and the
+// kernel's shared-memory attribute (set once per kernel and size).
+lrkv_status stream_prepare(const DecodePlan& P, CUtensorMap* tm_zk, CUtensorMap* tm_zv) {
   const StreamFn kern = stream_fn(P);
   if (!kern) return LRKV_ERR_UNSUPPORTED;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P.smem_bytes) != cudaSuccess)
-    return LRKV_ERR_CUDA;
+  std::memset(tm_zk, 0, sizeof(*tm_zk));
+  std::memset(tm_zv, 0, sizeof(*tm_zv));
+  if (P.r > 0) {
+    // z[b][t][h][c] viewed as [b][segment][t][hs r]: dims (inner first)
+    // {hs r, max_len, H / hs, B}, strides t: H r, segment: hs r, b: max_len H r
+    const uint64_t row = static_cast<uint64_t>(P.H) * P.r * 2;
+    const uint64_t dims[4] = {static_cast<uint64_t>(P.segw), static_cast<uint64_t>(P.max_len),
+                              static_cast<uint64_t>(P.H / P.hs), static_cast<uint64_t>(P.B)};
+    const uint64_t strides[3] = {row, static_cast<uint64_t>(P.segw) * 2, row * P.max_len};
+    const uint32_t box[4] = {static_cast<uint32_t>(P.segp), static_cast<uint32_t>(kT),
+                             static_cast<uint32_t>(P.nsb), 1u};
+    if (!make_tmap_4d_bf16_strided(tm_zk, P.z_k, dims, strides, box) ||
+        !make_tmap_4d_bf16_strided(tm_zv, P.z_v, dims, strides, box))
+      return LRKV_ERR_CUDA;
+  }
+  // the largest size set so far per kernel (per device: the attribute is a
+  // property of the function in the current context)
+  static std::mutex mu;
+  static std::map<std::pair<int, const void*>, int> set_bytes;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return LRKV_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  int& have = set_bytes[{dev, reinterpret_cast<const void*>(kern)}];
+  if (have < P.smem_bytes) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P.smem_bytes) != cudaSuccess ||
+        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared) !=
+            cudaSuccess)
+      return LRKV_ERR_CUDA;
+    have = P.smem_bytes;
+  }
+  return LRKV_OK;
+}
+
+lrkv_status stream_launch(const DecodePlan& P, cudaStream_t stream, bool pdl, const CUtensorMap& tm_k,
+                          const CUtensorMap& tm_v, const CUtensorMap& tm_zk, const CUtensorMap& tm_zv) {
+  const StreamFn kern = stream_fn(P);
+  if (!kern) return LRKV_ERR_UNSUPPORTED;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(P.grid);
+  cfg.gridDim = dim3(P.grid, P.mt);
   cfg.blockDim = dim3(P.nthreads);
   cfg.dynamicSmemBytes = P.smem_bytes;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, P, tm_k, tm_v) == cudaSuccess ? LRKV_OK : LRKV_ERR_CUDA;
+  return cudaLaunchKernelEx(&cfg, kern, P, tm_k, tm_v, tm_zk, tm_zv) == cudaSuccess ? LRKV_OK : LRKV_ERR_CUDA;
 }
 
 }  // namespace lrkv

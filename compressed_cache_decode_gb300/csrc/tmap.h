@@ -16,4 +16,11 @@ namespace lrkv {
 bool make_tmap_3d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
                        uint32_t b0, uint32_t b1, CUtensorMapSwizzle swizzle);
 
+// Encode a 4-D tiled tensor map of 2-byte elements with explicit byte
+// strides for dimensions 1..3 (any order; each a multiple of 16), box
+// {b0, b1, b2, b3} and no swizzle.  Box elements outside the extents are
+// filled with zeros.  Returns false on failure.
+bool make_tmap_4d_bf16_strided(CUtensorMap* map, const void* base, const uint64_t dims[4],
+                               const uint64_t strides_bytes[3], const uint32_t box[4]);
+
 }  // namespace lrkv
