@@ -613,7 +613,15 @@ __global__ void __launch_bounds__(128) lrkv_decode_combine_kernel(const DecodePl
 #pragma unroll
     for (int c2 = 0; c2 < kCombineRank / 2; ++c2) bvp[c2] = 2 * c2 < r ? row[c2] : 0u;
   }
+  pdl_trigger();  // the next step's scan may start streaming (it waits before writing)
   pdl_wait();
+  if (P.stream && h == 0 && b == 0 && tid < 32) {
+    // the device status of this call: the bits every scan CTA wrote
+    uint32_t bits = 0u;
+    for (int i = tid; i < P.grid * P.mt; i += 32) bits |= P.cta_status[i];
+    for (int o2 = 16; o2 > 0; o2 >>= 1) bits |= __shfl_xor_sync(0xffffffffu, bits, o2);
+    if (tid == 0) *P.status = bits;
+  }
   float* o = P.out + (static_cast<size_t>(b) * H + h) * dh;
   const int start = P.prefix[b], end = P.prefix[b + 1];
   if (end <= start) {
@@ -753,8 +761,10 @@ lrkv_status launch_all(const DecodePlan& P, cudaStream_t stream, cudaEvent_t ev_
                            P.combine_smem) != cudaSuccess)
     return LRKV_ERR_CUDA;
 
-  lrkv_decode_absorb_kernel<BF16><<<dim3(P.H, (P.B + kAbsorbSeq - 1) / kAbsorbSeq), 256, absorb_smem, stream>>>(P);
-  if (cudaGetLastError() != cudaSuccess) return LRKV_ERR_CUDA;
+  if (!P.stream) {  // the streaming kernel absorbs q itself
+    lrkv_decode_absorb_kernel<BF16><<<dim3(P.H, (P.B + kAbsorbSeq - 1) / kAbsorbSeq), 256, absorb_smem, stream>>>(P);
+    if (cudaGetLastError() != cudaSuccess) return LRKV_ERR_CUDA;
+  }
   if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return LRKV_ERR_CUDA;
 
   cudaLaunchAttribute attr[1];
@@ -881,7 +891,7 @@ lrkv_status decode_make_plan(const lrkv_dims& d, int num_sms, DecodePlan& P, siz
   const int slots = (P.B + P.grid) * P.ngw;
   P.combine_smem = std::max(r, 1) * 4;
 
-  // workspace: status | meta | prefix | p | part_ml | part_acc
+  // workspace: status | meta | prefix | p | part_ml | part_acc | CTA status
   size_t w = 256;
   w += static_cast<size_t>(round_up(P.B + 1, 64)) * 4;
   w += static_cast<size_t>(P.B) * H * std::max(r, 1) * 4;
@@ -889,6 +899,8 @@ lrkv_status decode_make_plan(const lrkv_dims& d, int num_sms, DecodePlan& P, siz
   w += static_cast<size_t>(slots) * H * 2 * 4;
   w = (w + 255) / 256 * 256;
   w += static_cast<size_t>(slots) * H * (dh + r) * 4;
+  w = (w + 255) / 256 * 256;
+  w += static_cast<size_t>(P.grid) * std::max(P.mt, 1) * 4;
   *ws_bytes = w;
   return LRKV_OK;
 }
@@ -907,6 +919,9 @@ void decode_bind_workspace(DecodePlan& P, void* ws) {
   off += static_cast<size_t>(P.B + P.grid) * P.ngw * P.H * 2 * 4;
   off = (off + 255) / 256 * 256;
   P.part_acc = reinterpret_cast<float*>(base + off);
+  off += static_cast<size_t>(P.B + P.grid) * P.ngw * P.H * (P.dh + P.r) * 4;
+  off = (off + 255) / 256 * 256;
+  P.cta_status = reinterpret_cast<uint32_t*>(base + off);
 }
 
 lrkv_status decode_launch(const DecodePlan& P, void* stream, void* ev_begin, void* ev_end) {

@@ -68,6 +68,7 @@ struct DecodePlan {
   int kst;           // 16-wide steps over the latents of 8 heads (r / 2)
   int cm_stride;     // floats per head row of the on-chip merge buffer
   int pfw;           // tiles a CTA keeps prefetched into L2 beyond its ring
+  int bk_dsplit;     // head-dim parts of the in-kernel q B^K (threads per output group)
   int zo[2][32];     // shared byte offset of 16-column latent step n of head half h2
   int pq_bytes;      // one p/q buffer: q rows [16][dh] bf16 then p rows [16][r] fp32
   int off_pq, off_pf, off_kv;
@@ -78,6 +79,7 @@ struct DecodePlan {
   float* p_abs;      // [B][H][r]  q_h B_h^K
   float* part_ml;    // [slots][H][2]  running max (log2 domain), denominator
   float* part_acc;   // [slots][H][dh + r]  unnormalised shared and private sums
+  uint32_t* cta_status;  // [mt][grid] status bits of each streaming CTA, written every launch
   // operands
   const void* q;
   const void* k_s;

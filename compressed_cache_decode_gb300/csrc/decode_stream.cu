@@ -120,18 +120,90 @@ __device__ __forceinline__ void stream_issue(const DecodePlan& P, const CUtensor
   }
 }
 
-// p = q B^K (fp32) and q (bf16) of the row tile's heads of sequence b into
-// buffer `buf` (one thread).
-__device__ __forceinline__ void pq_issue(const DecodePlan& P, unsigned char* smem, uint64_t* pbar, int buf, int b,
-                                         int m0) {
-  const int nh = min(16, P.H - m0);
-  const uint32_t pbytes = static_cast<uint32_t>(nh * P.r * 4), qbytes = static_cast<uint32_t>(nh * P.dh * 2);
+// q (bf16) of the row tile's heads of sequence b into p/q buffer `buf`
+// (one thread).
+__device__ __forceinline__ void q_issue(const DecodePlan& P, unsigned char* smem, uint64_t* pbar, int buf, int b,
+                                        int m0) {
+  const uint32_t qbytes = static_cast<uint32_t>(min(16, P.H - m0) * P.dh * 2);
   unsigned char* dst = smem + P.off_pq + buf * P.pq_bytes;
-  mbar_arrive_expect_tx(&pbar[buf], pbytes + qbytes);
+  mbar_arrive_expect_tx(&pbar[buf], qbytes);
   tma_load_1d(dst, static_cast<const unsigned char*>(P.q) + (static_cast<size_t>(b) * P.H + m0) * P.dh * 2, qbytes,
               &pbar[buf]);
-  if (pbytes)
-    tma_load_1d(dst + 16 * P.dh * 2, P.p_abs + (static_cast<size_t>(b) * P.H + m0) * P.r, pbytes, &pbar[buf]);
+}
+
+// Absorbed query p_h = q_h B_h^K ("Low-Rank Key Value Attention | What a
+// shared cache can preserve", §3, Algorithm 2 step 02) of the row tile's 16
+// heads, for one or two sequences at once (their q rows in shared memory),
+// in fp32.  Thread role: head hl, columns 4 cg .. 4 cg + 3, head-dim part dp
+// of bk_dsplit; B^K is read with 8-byte loads, kBkChunk of them in flight,
+// the first chunk issued early by bk_load (before the tile copies, so that
+// it does not queue behind them).
+constexpr int kBkChunk = 32;
+
+struct BkRole {
+  int hl, cg, dp, nd;
+  bool on;
+};
+
+__device__ __forceinline__ BkRole bk_role(const DecodePlan& P, int m0, int tid) {
+  BkRole R;
+  const int per_head = (P.r / 4) * P.bk_dsplit;
+  R.hl = tid / max(per_head, 1);
+  const int rem = tid - R.hl * per_head;
+  R.cg = rem / P.bk_dsplit;
+  R.dp = rem % P.bk_dsplit;
+  R.nd = P.dh / P.bk_dsplit;
+  R.on = P.r > 0 && R.hl < 16 && m0 + R.hl < P.H;
+  return R;
+}
+
+__device__ __forceinline__ void bk_load(const DecodePlan& P, int m0, const BkRole& R, int d0, uint2 (&v)[kBkChunk]) {
+  const __nv_bfloat16* base = static_cast<const __nv_bfloat16*>(P.b_k) +
+                              (static_cast<size_t>(m0 + R.hl) * P.dh + R.dp * R.nd) * P.r + 4 * R.cg;
+#pragma unroll
+  for (int u = 0; u < kBkChunk; ++u)
+    v[u] = (R.on && d0 + u < R.nd) ? *reinterpret_cast<const uint2*>(base + static_cast<size_t>(d0 + u) * P.r)
+                                   : make_uint2(0u, 0u);
+}
+
+// p rows of up to two sequences (q rows qa, qb: [16][dh] bf16; p rows pa, pb:
+// [16][r] fp32); v holds the first chunk of B^K already.
+__device__ __forceinline__ void absorb_rows(const DecodePlan& P, int m0, const BkRole& R, uint2 (&v)[kBkChunk],
+                                            const __nv_bfloat16* qa, const __nv_bfloat16* qb, float* pa, float* pb) {
+  float aa[4] = {0.f, 0.f, 0.f, 0.f}, ab[4] = {0.f, 0.f, 0.f, 0.f};
+  const int dbase = R.dp * R.nd;
+  for (int d0 = 0; d0 < R.nd; d0 += kBkChunk) {
+    if (d0 > 0) bk_load(P, m0, R, d0, v);
+#pragma unroll
+    for (int u = 0; u < kBkChunk; ++u) {
+      if (d0 + u < R.nd) {
+        const int d = dbase + d0 + u;
+        const float b0 = bf_lo(v[u].x), b1 = bf_hi(v[u].x), b2 = bf_lo(v[u].y), b3 = bf_hi(v[u].y);
+        if (R.on) {
+          const float x = __bfloat162float(qa[R.hl * P.dh + d]);
+          aa[0] = fmaf(x, b0, aa[0]); aa[1] = fmaf(x, b1, aa[1]); aa[2] = fmaf(x, b2, aa[2]); aa[3] = fmaf(x, b3, aa[3]);
+          if (qb) {
+            const float y = __bfloat162float(qb[R.hl * P.dh + d]);
+            ab[0] = fmaf(y, b0, ab[0]); ab[1] = fmaf(y, b1, ab[1]); ab[2] = fmaf(y, b2, ab[2]); ab[3] = fmaf(y, b3, ab[3]);
+          }
+        }
+      }
+    }
+  }
+  // sum the head-dim parts (lanes dp of one (head, column group) are adjacent)
+  for (int o = 1; o < P.bk_dsplit; o <<= 1)
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      aa[u] += __shfl_xor_sync(0xffffffffu, aa[u], o);
+      ab[u] += __shfl_xor_sync(0xffffffffu, ab[u], o);
+    }
+  if (R.on && R.dp == 0) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      pa[R.hl * P.r + 4 * R.cg + u] = aa[u];
+      if (pb) pb[R.hl * P.r + 4 * R.cg + u] = ab[u];
+    }
+  }
 }
 
 __device__ __forceinline__ void prefetch_tmap(const void* p) {
@@ -264,25 +336,30 @@ __global__ void __launch_bounds__(kThreadsS, 1)
   __syncthreads();
   const int N = pre[B];
   const int G = max(1, min(static_cast<int>(gridDim.x), (N + P.min_tokens - 1) / max(P.min_tokens, 1)));
-  if (blockIdx.x == 0 && blockIdx.y == 0) {
-    for (int b = tid; b <= B; b += blockDim.x) P.prefix[b] = pre[b];
-    if (tid == 0) { P.meta[0] = N; P.meta[1] = G; }
-  }
+  uint32_t* cta_status = P.cta_status + blockIdx.y * gridDim.x + blockIdx.x;
   if (N == 0 || static_cast<int>(blockIdx.x) >= G) {
-    if (bad && tid == 0) { pdl_wait(); record_status(P.status, kDevBounds); }
+    // the launch before may still read the workspace: wait before writing it
+    pdl_wait();
+    if (blockIdx.x == 0 && blockIdx.y == 0) {
+      for (int b = tid; b <= B; b += blockDim.x) P.prefix[b] = pre[b];
+      if (tid == 0) { P.meta[0] = N; P.meta[1] = G; }
+    }
+    if (tid == 0) *cta_status = bad ? kDevBounds : 0u;
     return;
   }
   const int c = blockIdx.x;
   const int g0 = static_cast<int>(static_cast<long long>(c) * N / G);
   const int g1 = static_cast<int>(static_cast<long long>(c + 1) * N / G);
-  pdl_wait();  // p = q B^K from the absorb kernel
-  if (bad && tid == 0) record_status(P.status, kDevBounds);
-
-  // ---- 2. p and q of the first piece, then the first `stages` tiles (warp w
+  // ---- 2. q of the first two pieces, then the first `stages` tiles (warp w
   // issues tiles w, w + 8, ...), so that the small copies land first ---------
   Piece pc;
   bool more = piece_first(pc, pre, B, g0, g1);
-  if (tid == 0) pq_issue(P, smem, pbar, 0, pc.b, m0);
+  Piece pc1 = pc;
+  const bool two = piece_next(pc1, pre, B, g1);
+  if (tid == 0) {
+    q_issue(P, smem, pbar, 0, pc.b, m0);
+    if (two) q_issue(P, smem, pbar, 1, pc1.b, m0);
+  }
   if (lane == 0) {
     TileCursor cur;
     cur.pc = pc;
@@ -294,6 +371,11 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       *reinterpret_cast<volatile int*>(&issued[j]) = j;
     }
   }
+  // the first B^K chunk of the in-kernel absorb (after the copies were
+  // issued: the loads hold the issuing warps until they drain)
+  const BkRole bkr = bk_role(P, m0, tid);
+  uint2 bkv[kBkChunk];
+  bk_load(P, m0, bkr, 0, bkv);
   // the next pfw tiles start streaming into L2 now
   if (tid == 32) l2_prefetch_tiles(P, pre, B, g0, g1, P.stages, P.stages + P.pfw);
 
@@ -304,9 +386,19 @@ __global__ void __launch_bounds__(kThreadsS, 1)
   const int zrow = P.segp * 2;  // bytes per segment row
   const int hb = 8 * hf;        // first head (row-tile local) of this half
 
+  bool ok = true;
+  if (MZMAX > 0) {
+    // p of the first two pieces, from the q rows and the early B^K chunk
+    ok = mbar_wait_bounded(&pbar[0], 0u) && (!two || mbar_wait_bounded(&pbar[1], 0u));
+    if (!ok) *reinterpret_cast<volatile int*>(&s_timeout) = 1;
+    unsigned char* pq0 = smem + P.off_pq;
+    unsigned char* pq1 = pq0 + P.pq_bytes;
+    absorb_rows(P, m0, bkr, bkv, reinterpret_cast<const __nv_bfloat16*>(pq0),
+                two ? reinterpret_cast<const __nv_bfloat16*>(pq1) : nullptr, reinterpret_cast<float*>(pq0 + 16 * dh * 2),
+                two ? reinterpret_cast<float*>(pq1 + 16 * dh * 2) : nullptr);
+  }
   int ibase = 0;      // tile index of the piece's first tile
   int kp = 0;         // piece counter (p/q buffer kp & 1)
-  bool ok = true;
   TileCursor refill;  // tiles this pair issues (its tile + stages)
   refill.more = piece_first(refill.pc, pre, B, g0, g1);
   refill.ibase = 0;
@@ -315,19 +407,26 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     // ---- piece set-up: p and q of the row tile --------------------------------
     named_sync(1, kThreadsS);  // the previous piece's merge is done with the buffer
     const int buf = kp & 1;
-    if (tid == 0) {
+    if (tid == 0 && kp >= 1) {
       Piece nx = pc;
-      if (piece_next(nx, pre, B, g1)) {  // prefetch the next piece's p and q
+      if (piece_next(nx, pre, B, g1)) {  // prefetch the next piece's q (pieces 0, 1 came first)
         fence_proxy_async_smem();
-        pq_issue(P, smem, pbar, buf ^ 1, nx.b, m0);
+        q_issue(P, smem, pbar, buf ^ 1, nx.b, m0);
       }
     }
     if (ok) {
       ok = mbar_wait_bounded(&pbar[buf], static_cast<uint32_t>(kp >> 1) & 1u);
       if (!ok) *reinterpret_cast<volatile int*>(&s_timeout) = 1;
     }
-    const unsigned char* pqb = smem + P.off_pq + buf * P.pq_bytes;
+    unsigned char* pqb = smem + P.off_pq + buf * P.pq_bytes;
     const int nh = min(16, H - m0);
+    if (MZMAX > 0 && kp >= 2) {  // p of a third or later piece (the first two came before)
+      uint2 v[kBkChunk];
+      bk_load(P, m0, bkr, 0, v);
+      absorb_rows(P, m0, bkr, v, reinterpret_cast<const __nv_bfloat16*>(pqb), nullptr,
+                  reinterpret_cast<float*>(pqb + 16 * dh * 2), nullptr);
+      named_sync(1, kThreadsS);  // p rows ready
+    }
     {
       const __nv_bfloat16* qsm = reinterpret_cast<const __nv_bfloat16*>(pqb);
       const int hl = hb + g;
@@ -545,6 +644,14 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       float Mr = -INFINITY, lr = 0.f, vr[KC];
 #pragma unroll
       for (int k = 0; k < KC; ++k) vr[k] = 0.f;
+      if (kp == 0) {
+        // first write to the workspace: the launch before may still read it
+        pdl_wait();
+        if (blockIdx.x == 0 && blockIdx.y == 0) {
+          for (int b = tid; b <= B; b += blockDim.x) P.prefix[b] = pre[b];
+          if (tid == 0) { P.meta[0] = N; P.meta[1] = G; }
+        }
+      }
       for (int p0 = 0; p0 < kPairs; p0 += 2) {
         named_sync(1, kThreadsS);  // tiles (first round) or the previous round's reads are done
         if ((pair >> 1) == (p0 >> 1)) {
@@ -608,7 +715,10 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     ++kp;
     more = piece_next(pc, pre, B, g1);
   }
-  if (!ok && lane == 0) record_status(P.status, kDevTimeout);
+  if (!ok) *reinterpret_cast<volatile int*>(&s_timeout) = 1;
+  named_sync(1, kThreadsS);
+  if (tid == 0)
+    *cta_status = (bad ? kDevBounds : 0u) | (*reinterpret_cast<volatile int*>(&s_timeout) ? kDevTimeout : 0u);
   pdl_trigger();
 }
 
@@ -689,6 +799,9 @@ static lrkv_status stream_plan_impl(DecodePlan& P) {
       for (int n = 0; n < 32; ++n) P.zo[h2][n] = 0;
   }
   P.pq_bytes = round_up(16 * dh * 2 + 16 * r * 4, 128);
+  // absorb roles: 16 heads x r/4 column groups x bk_dsplit head-dim parts
+  P.bk_dsplit = 1;
+  while (r > 0 && 16 * (r / 4) * P.bk_dsplit * 2 <= kThreadsS && P.bk_dsplit * 2 <= dh / 4) P.bk_dsplit *= 2;
   P.cm_stride = (dh + r + 2) | 1;  // odd: the scatter rows fall in different banks
   P.stage_bytes = round_up(2 * P.kv_bytes + 2 * P.zt_bytes, 1024);
   const int pf_bytes = 2 * P.kst * 32 * 16;
