@@ -713,6 +713,16 @@ SplitFn split_fn(const DecodePlan& P) {
   return lrkv_decode_split_kernel<false, 64, 4>;
 }
 
+// An event recorded on `stream`; while the stream is being captured into a
+// CUDA graph it becomes an external event-record node (a plain record would
+// only mark a dependency), so that replays can be timed with it.
+cudaError_t record_event(cudaEvent_t ev, cudaStream_t stream) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return cudaErrorInvalidValue;
+  return cs == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(ev, stream, cudaEventRecordExternal)
+                                             : cudaEventRecord(ev, stream);
+}
+
 template <bool BF16>
 // Every host step (tensor maps, shared-memory attributes) comes before the
 // first launch, so that the profiled interval [ev_begin, ev_end] holds the
@@ -765,7 +775,7 @@ lrkv_status launch_all(const DecodePlan& P, cudaStream_t stream, cudaEvent_t ev_
     lrkv_decode_absorb_kernel<BF16><<<dim3(P.H, (P.B + kAbsorbSeq - 1) / kAbsorbSeq), 256, absorb_smem, stream>>>(P);
     if (cudaGetLastError() != cudaSuccess) return LRKV_ERR_CUDA;
   }
-  if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return LRKV_ERR_CUDA;
+  if (ev_begin && record_event(ev_begin, stream) != cudaSuccess) return LRKV_ERR_CUDA;
 
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -783,7 +793,7 @@ lrkv_status launch_all(const DecodePlan& P, cudaStream_t stream, cudaEvent_t ev_
     cfg.numAttrs = pdl ? 1 : 0;
     if (cudaLaunchKernelEx(&cfg, split, P, tm_k, tm_v) != cudaSuccess) return LRKV_ERR_CUDA;
   }
-  if (ev_end && cudaEventRecord(ev_end, stream) != cudaSuccess) return LRKV_ERR_CUDA;
+  if (ev_end && record_event(ev_end, stream) != cudaSuccess) return LRKV_ERR_CUDA;
 
   cudaLaunchConfig_t ccfg = {};
   ccfg.gridDim = dim3(P.H, P.B);

@@ -69,6 +69,9 @@ struct DecodePlan {
   int cm_stride;     // floats per head row of the on-chip merge buffer
   int pfw;           // tiles a CTA keeps prefetched into L2 beyond its ring
   int bk_dsplit;     // head-dim parts of the in-kernel q B^K (threads per output group)
+  int bk_stages;     // ring stages that first hold the row tile's B^K (0: B^K read from global)
+  int bk_warps;      // warps with absorb work (the first ones)
+  int bk_head_bytes; // shared bytes per head of the staged B^K (padded)
   int zo[2][32];     // shared byte offset of 16-column latent step n of head half h2
   int pq_bytes;      // one p/q buffer: q rows [16][dh] bf16 then p rows [16][r] fp32
   int off_pq, off_pf, off_kv;
