@@ -130,9 +130,11 @@ lrkv_status lrkv_decode(const lrkv_dims* dims, const void* q, const void* k_s, c
  * lrkv_decode, plus two CUDA events (cudaEvent_t passed as void*, created by
  * the caller) recorded on `stream` immediately before and after the split-KV
  * kernel, the HBM-bound scan that dominates a decode step.  Used to time that
- * kernel alone; with the events in place the three kernels of the step run
- * strictly one after another instead of overlapping their launch.  Both
- * events are required (LRKV_ERR_INVALID_ARG otherwise).
+ * kernel alone; with the events in place the kernels of the step run
+ * strictly one after another instead of overlapping their launch.  While
+ * `stream` is being captured into a CUDA graph the events are recorded as
+ * external event-record nodes, so that graph replays can be timed with them.
+ * Both events are required (LRKV_ERR_INVALID_ARG otherwise).
  */
 lrkv_status lrkv_decode_profiled(const lrkv_dims* dims, const void* q, const void* k_s,
                                  const void* v_s, const void* z_k, const void* z_v, const void* b_k,
@@ -229,8 +231,9 @@ lrkv_status lrkv_prefill(const lrkv_dims* dims, int q_len, const void* q, const 
 /*
  * Read the device status word that the kernels of the last call(s) using
  * `ws` recorded (LRKV_OK, LRKV_ERR_TIMEOUT or LRKV_ERR_DEVICE_BOUNDS).
- * Synchronises `stream`.  Each lrkv_decode/lrkv_prefill call resets the word
- * when it starts.
+ * Synchronises `stream`.  Each lrkv_decode/lrkv_prefill call sets the word
+ * afresh: a decode writes the bits its kernels recorded (no clearing needed
+ * before a call), a prefill clears it when it starts.
  */
 lrkv_status lrkv_read_device_status(const void* ws, lrkv_stream_t stream, lrkv_status* out_status);
 
