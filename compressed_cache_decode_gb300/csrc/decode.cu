@@ -90,6 +90,7 @@ __device__ __forceinline__ void issue_tile(const DecodePlan& P, const CUtensorMa
 // to kAbsorbSeq sequences staged in shared memory, then one output
 // p_{b,h,c} = q_{b,h} . B_h^K[:, c] per thread.
 constexpr int kAbsorbSeq = 8;
+constexpr int kCombineCtas = 16;  // SMs the streaming scan leaves to the merge
 
 template <bool BF16>
 __global__ void __launch_bounds__(256) lrkv_decode_absorb_kernel(const DecodePlan P) {
@@ -587,103 +588,132 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ==================================================================== combine
-// grid = (H, B), block = 128: the pieces (m_i, l_i, acc_i) of sequence b,
-// head h, merged with the log-sum-exp rule, then the lift
+// One warp per (sequence b, head h), grid-stride over the pairs (the grid
+// is kept small, so that the streaming scan can leave it a few SMs of its
+// own and the next step's scan starts beside it): the pieces
+// (m_i, l_i, acc_i) merged with the log-sum-exp rule, then the lift
 // o = acc_s / L + (acc_z / L) (B_h^V)^T and lse = (M + log2 L) ln 2
-// (Algorithm 2 steps 06-09).  Thread j owns column j of [acc_s | acc_z] and
-// merges its column over every piece in one pass (32 pieces of loads in
-// flight, the running maximum raised as it goes; the m_i, l_i loads are
-// shared by the warp).  The B_h^V row of its output column is an input, so
-// it is loaded before the wait on the scan kernel.
-constexpr int kCombinePieces = 32;
-constexpr int kCombineRank = 64;
+// (Algorithm 2 steps 06-09).  Lane j owns columns j + 32 k of
+// [acc_s | acc_z] and merges them over every piece in one pass (16 pieces of
+// loads in flight, the running maximum raised as it goes; m_i, l_i are read
+// by every lane of the warp at once).  The first pair's B_h^V rows are an
+// input, loaded before the wait on the scan kernel when they fit in
+// registers.
+constexpr int kCombineWarps = 8;
+constexpr int kCombinePieces = 16;
+constexpr int kCombinePre = 32;  // B^V words a lane may hold (2 rows of r <= 32)
 
-template <bool BF16>
-__global__ void __launch_bounds__(128) lrkv_decode_combine_kernel(const DecodePlan P) {
+template <bool BF16, int KC>  // KC: columns per lane, ceil((dh + r) / 32)
+__global__ void __launch_bounds__(32 * kCombineWarps) lrkv_decode_combine_kernel(const DecodePlan P) {
   extern __shared__ __align__(16) unsigned char csmem[];
-  float* zbar = reinterpret_cast<float*>(csmem);  // [r]
-  __shared__ float s_M, s_L;
-  const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = P.H, dh = P.dh, r = P.r, W = dh + r;
-  const bool pre_bv = BF16 && dh <= static_cast<int>(blockDim.x) && r <= kCombineRank;
-  uint32_t bvp[kCombineRank / 2];
-  if (pre_bv && tid < dh) {
-    const uint32_t* row = reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(P.b_v) +
-                                                            (static_cast<size_t>(h) * dh + tid) * r);
+  float* zbar = reinterpret_cast<float*>(csmem) + warp * max(r, 1);  // [r] per warp
+  const long long npairs = static_cast<long long>(P.B) * H;
+  const long long wstride = static_cast<long long>(gridDim.x) * kCombineWarps;
+  long long bh = static_cast<long long>(blockIdx.x) * kCombineWarps + warp;
+  const int nd = (dh + 31) / 32;  // output rows d = lane + 32 k of this lane
+  const bool pre_bv = BF16 && nd <= 2 && r <= 32;
+  uint32_t bvp[kCombinePre];
+  auto load_bv = [&](int h) {
 #pragma unroll
-    for (int c2 = 0; c2 < kCombineRank / 2; ++c2) bvp[c2] = 2 * c2 < r ? row[c2] : 0u;
-  }
-  pdl_trigger();  // the next step's scan may start streaming (it waits before writing)
+    for (int i = 0; i < kCombinePre; ++i) {
+      const int k = i / 16, c2 = i % 16, d = lane + 32 * k;
+      bvp[i] = (k < nd && d < dh && 2 * c2 < r)
+                   ? reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(P.b_v) +
+                                                       (static_cast<size_t>(h) * dh + d) * r)[c2]
+                   : 0u;
+    }
+  };
+  if (pre_bv && bh < npairs) load_bv(static_cast<int>(bh % H));
+  pdl_trigger();  // the next step's scan may launch (it waits before it writes)
   pdl_wait();
-  if (P.stream && h == 0 && b == 0 && tid < 32) {
+  if (P.stream && blockIdx.x == 0 && warp == 0) {
     // the device status of this call: the bits every scan CTA wrote
     uint32_t bits = 0u;
-    for (int i = tid; i < P.grid * P.mt; i += 32) bits |= P.cta_status[i];
+    for (int i = lane; i < P.grid * P.mt; i += 32) bits |= P.cta_status[i];
     for (int o2 = 16; o2 > 0; o2 >>= 1) bits |= __shfl_xor_sync(0xffffffffu, bits, o2);
-    if (tid == 0) *P.status = bits;
-  }
-  float* o = P.out + (static_cast<size_t>(b) * H + h) * dh;
-  const int start = P.prefix[b], end = P.prefix[b + 1];
-  if (end <= start) {
-    for (int k = tid; k < dh; k += blockDim.x) o[k] = 0.f;
-    if (tid == 0 && P.lse) P.lse[static_cast<size_t>(b) * H + h] = -INFINITY;
-    return;
+    if (lane == 0) *P.status = bits;
   }
   const long long N = P.meta[0], G = P.meta[1];
-  const int c0 = cta_of_token(start, N, G), c1 = cta_of_token(end - 1, N, G);
-  const int n = (c1 - c0 + 1) * P.ngw;       // partials of this sequence
-  const size_t s0 = static_cast<size_t>(b + c0) * P.ngw;  // first of them
-  const float* ml = P.part_ml + (s0 * H + h) * 2;
-  const float* acc0 = P.part_acc + (s0 * H + h) * W;
-  const size_t mstep = static_cast<size_t>(H) * 2, astep = static_cast<size_t>(H) * W;
-  float oshared[2] = {0.f, 0.f};
-  for (int j = tid, jj = 0; j < W; j += blockDim.x, ++jj) {
-    float M = -INFINITY, L = 0.f, a = 0.f;
+  for (bool first = true; bh < npairs; bh += wstride, first = false) {
+    const int b = static_cast<int>(bh / H), h = static_cast<int>(bh % H);
+    if (pre_bv && !first) load_bv(h);
+    float* o = P.out + (static_cast<size_t>(b) * H + h) * dh;
+    const int start = P.prefix[b], end = P.prefix[b + 1];
+    if (end <= start) {
+      for (int k = lane; k < dh; k += 32) o[k] = 0.f;
+      if (lane == 0 && P.lse) P.lse[static_cast<size_t>(b) * H + h] = -INFINITY;
+      continue;
+    }
+    const int c0 = cta_of_token(start, N, G), c1 = cta_of_token(end - 1, N, G);
+    const int n = (c1 - c0 + 1) * P.ngw;                    // partials of this sequence
+    const size_t s0 = static_cast<size_t>(b + c0) * P.ngw;  // first of them
+    const float* ml = P.part_ml + (s0 * H + h) * 2;
+    const float* acc0 = P.part_acc + (s0 * H + h) * W;
+    const size_t mstep = static_cast<size_t>(H) * 2, astep = static_cast<size_t>(H) * W;
+    float M = -INFINITY, L = 0.f, a[KC];
+#pragma unroll
+    for (int k = 0; k < KC; ++k) a[k] = 0.f;
     for (int i0 = 0; i0 < n; i0 += kCombinePieces) {
-      float mi[kCombinePieces], li[kCombinePieces], vi[kCombinePieces];
+      float mi[kCombinePieces], li[kCombinePieces], vi[kCombinePieces][KC];
 #pragma unroll
       for (int u = 0; u < kCombinePieces; ++u) {
         const bool ok = i0 + u < n;
         mi[u] = ok ? ml[(i0 + u) * mstep] : -INFINITY;
         li[u] = ok ? ml[(i0 + u) * mstep + 1] : 0.f;
-        vi[u] = (ok && j < W) ? acc0[(i0 + u) * astep + j] : 0.f;
+#pragma unroll
+        for (int k = 0; k < KC; ++k) {
+          const int j = lane + 32 * k;
+          vi[u][k] = (ok && j < W) ? acc0[(i0 + u) * astep + j] : 0.f;
+        }
       }
       float Mn = M;
 #pragma unroll
       for (int u = 0; u < kCombinePieces; ++u) Mn = fmaxf(Mn, mi[u]);
       const float f = M == -INFINITY ? 0.f : exp2f(M - Mn);
       L *= f;
-      a *= f;
+#pragma unroll
+      for (int k = 0; k < KC; ++k) a[k] *= f;
 #pragma unroll
       for (int u = 0; u < kCombinePieces; ++u) {
         const float w = mi[u] == -INFINITY ? 0.f : exp2f(mi[u] - Mn);
         L = fmaf(w, li[u], L);
-        a = fmaf(w, vi[u], a);
+#pragma unroll
+        for (int k = 0; k < KC; ++k) a[k] = fmaf(w, vi[u][k], a[k]);
       }
       M = Mn;
     }
-    if (j == 0) { s_M = M; s_L = L; }  // the same for every column
-    const float v = a / L;
-    if (j < dh) { if (jj < 2) oshared[jj] = v; }
-    else zbar[j - dh] = v;
-  }
-  __syncthreads();
-  for (int k = tid, jj = 0; k < dh; k += blockDim.x, ++jj) {
-    float a = oshared[jj];
-    if (pre_bv) {
+    const float inv_l = 1.f / L;
+    __syncwarp();  // the previous pair's zbar reads are done
 #pragma unroll
-      for (int c2 = 0; c2 < kCombineRank / 2; ++c2)
-        if (2 * c2 < r) {
-          a = fmaf(bf_lo(bvp[c2]), zbar[2 * c2], a);
-          a = fmaf(bf_hi(bvp[c2]), zbar[2 * c2 + 1], a);
-        }
-    } else {
-      const size_t base = (static_cast<size_t>(h) * dh + k) * r;
-      for (int cc = 0; cc < r; ++cc) a = fmaf(load_elem(P.b_v, base + cc, BF16), zbar[cc], a);
+    for (int k = 0; k < KC; ++k) {
+      const int j = lane + 32 * k;
+      if (j >= dh && j < W) zbar[j - dh] = a[k] * inv_l;
     }
-    o[k] = a;
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < KC; ++k) {
+      const int d = lane + 32 * k;
+      if (d >= dh) continue;
+      float v = a[k] * inv_l;
+      if (pre_bv) {
+#pragma unroll
+        for (int c2 = 0; c2 < 16; ++c2) {
+          const int i = k * 16 + c2;
+          if (i < kCombinePre && 2 * c2 < r) {
+            v = fmaf(bf_lo(bvp[i]), zbar[2 * c2], v);
+            v = fmaf(bf_hi(bvp[i]), zbar[2 * c2 + 1], v);
+          }
+        }
+      } else {
+        const size_t base = (static_cast<size_t>(h) * dh + d) * r;
+        for (int cc = 0; cc < r; ++cc) v = fmaf(load_elem(P.b_v, base + cc, BF16), zbar[cc], v);
+      }
+      o[d] = v;
+    }
+    if (lane == 0 && P.lse) P.lse[static_cast<size_t>(b) * H + h] = (M + log2f(L)) * kLn2;
   }
-  if (tid == 0 && P.lse) P.lse[static_cast<size_t>(b) * H + h] = (s_M + log2f(s_L)) * kLn2;
 }
 
 // ======================================================================= host
@@ -695,6 +725,15 @@ int env_int(const char* name, int dflt) {
 }
 
 using SplitFn = void (*)(const DecodePlan, const CUtensorMap, const CUtensorMap);
+using CombineFn = void (*)(const DecodePlan);
+
+template <bool BF16>
+CombineFn combine_fn(const DecodePlan& P) {
+  const int cols = (P.dh + P.r + 31) / 32;
+  if (cols <= 3) return lrkv_decode_combine_kernel<BF16, 3>;
+  if (cols <= 6) return lrkv_decode_combine_kernel<BF16, 6>;
+  return lrkv_decode_combine_kernel<BF16, 10>;
+}
 
 SplitFn split_fn(const DecodePlan& P) {
   const int rmax = P.r <= 16 ? 16 : P.r <= 32 ? 32 : 64;
@@ -757,7 +796,7 @@ lrkv_status launch_all(const DecodePlan& P, cudaStream_t stream, cudaEvent_t ev_
     if (!carve_set) {
       cudaFuncSetAttribute(lrkv_decode_absorb_kernel<BF16>, cudaFuncAttributePreferredSharedMemoryCarveout,
                            cudaSharedmemCarveoutMaxShared);
-      cudaFuncSetAttribute(lrkv_decode_combine_kernel<BF16>, cudaFuncAttributePreferredSharedMemoryCarveout,
+      cudaFuncSetAttribute(combine_fn<BF16>(P), cudaFuncAttributePreferredSharedMemoryCarveout,
                            cudaSharedmemCarveoutMaxShared);
       carve_set = true;
     }
@@ -766,9 +805,9 @@ lrkv_status launch_all(const DecodePlan& P, cudaStream_t stream, cudaEvent_t ev_
       cudaFuncSetAttribute(lrkv_decode_absorb_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            absorb_smem) != cudaSuccess)
     return LRKV_ERR_CUDA;
+  const CombineFn combine = combine_fn<BF16>(P);
   if (P.combine_smem > 48 * 1024 &&
-      cudaFuncSetAttribute(lrkv_decode_combine_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           P.combine_smem) != cudaSuccess)
+      cudaFuncSetAttribute(combine, cudaFuncAttributeMaxDynamicSharedMemorySize, P.combine_smem) != cudaSuccess)
     return LRKV_ERR_CUDA;
 
   if (!P.stream) {  // the streaming kernel absorbs q itself
@@ -796,13 +835,13 @@ lrkv_status launch_all(const DecodePlan& P, cudaStream_t stream, cudaEvent_t ev_
   if (ev_end && record_event(ev_end, stream) != cudaSuccess) return LRKV_ERR_CUDA;
 
   cudaLaunchConfig_t ccfg = {};
-  ccfg.gridDim = dim3(P.H, P.B);
-  ccfg.blockDim = dim3(128);
+  ccfg.gridDim = dim3(P.combine_ctas);
+  ccfg.blockDim = dim3(32 * kCombineWarps);
   ccfg.dynamicSmemBytes = P.combine_smem;
   ccfg.stream = stream;
   ccfg.attrs = attr;
   ccfg.numAttrs = pdl ? 1 : 0;
-  if (cudaLaunchKernelEx(&ccfg, lrkv_decode_combine_kernel<BF16>, P) != cudaSuccess) return LRKV_ERR_CUDA;
+  if (cudaLaunchKernelEx(&ccfg, combine, P) != cudaSuccess) return LRKV_ERR_CUDA;
   return LRKV_OK;
 }
 
@@ -888,10 +927,17 @@ lrkv_status decode_make_plan(const lrkv_dims& d, int num_sms, DecodePlan& P, siz
   P.ngw = 1;
   // bf16 shapes the streaming kernel covers use it; the rest (and fp32) run
   // the tile-synchronous kernel planned above
-  P.grid = env_int("LRKV_DECODE_GRID", num_sms);
+  // the combine kernel: one warp per (sequence, head), at most kCombineCtas
+  // CTAs; the streaming scan leaves it that many SMs, so that consecutive
+  // steps' scans and merges overlap
+  const long long pair_ctas = (static_cast<long long>(P.B) * H + kCombineWarps - 1) / kCombineWarps;
+  const int reserve = static_cast<int>(std::min<long long>(pair_ctas, kCombineCtas));
+  P.grid = env_int("LRKV_DECODE_GRID", std::max(1, num_sms - reserve));
   // the streaming kernel's grid is (range CTAs, row tiles of 16 heads): it
   // divides P.grid by the row tiles
   if (P.bf16 && env_int("LRKV_DECODE_TILE_SYNC", 0) == 0) stream_plan(P);
+  if (!P.stream) P.grid = env_int("LRKV_DECODE_GRID", num_sms);
+  P.combine_ctas = P.stream ? reserve : static_cast<int>(std::min<long long>(pair_ctas, 65535));
   P.min_tokens = env_int("LRKV_DECODE_MIN_TOKENS", P.stream ? 8 * P.T : 2 * P.T);
   if (P.stream) {
     // L2 prefetch window: about 48 MB in flight over all CTAs (L2 is 126 MB)
@@ -899,7 +945,7 @@ lrkv_status decode_make_plan(const lrkv_dims& d, int num_sms, DecodePlan& P, siz
     P.pfw = env_int("LRKV_DECODE_PREFETCH_TILES", static_cast<int>(per_cta / P.stage_bytes));
   }
   const int slots = (P.B + P.grid) * P.ngw;
-  P.combine_smem = std::max(r, 1) * 4;
+  P.combine_smem = kCombineWarps * std::max(r, 1) * 4;
 
   // workspace: status | meta | prefix | p | part_ml | part_acc | CTA status
   size_t w = 256;

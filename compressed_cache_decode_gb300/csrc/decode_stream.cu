@@ -311,6 +311,9 @@ __global__ void __launch_bounds__(kThreadsS, 1)
   __shared__ int s_timeout;
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
 
+  // the merge kernel may launch now: it waits for this grid before it reads
+  // (its few CTAs take the SMs this grid leaves free)
+  pdl_trigger();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int pair = warp >> 1, hf = warp & 1;     // tile stream, half of the row tile's heads
   const int g = lane >> 2, q4 = lane & 3;
@@ -808,7 +811,6 @@ __global__ void __launch_bounds__(kThreadsS, 1)
   named_sync(1, kThreadsS);
   if (tid == 0)
     *cta_status = (bad ? kDevBounds : 0u) | (*reinterpret_cast<volatile int*>(&s_timeout) ? kDevTimeout : 0u);
-  pdl_trigger();
 }
 
 // ======================================================================= host
