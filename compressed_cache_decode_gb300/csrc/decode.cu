@@ -594,18 +594,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 // (m_i, l_i, acc_i) merged with the log-sum-exp rule, then the lift
 // o = acc_s / L + (acc_z / L) (B_h^V)^T and lse = (M + log2 L) ln 2
 // (Algorithm 2 steps 06-09).  Lane j owns columns j + 32 k of
-// [acc_s | acc_z] and merges them over every piece in one pass (16 pieces of
-// loads in flight, the running maximum raised as it goes; m_i, l_i are read
+// [acc_s | acc_z] and merges them over every piece in one pass (8-32 pieces
+// of loads in flight, the running maximum raised as it goes; m_i, l_i are read
 // by every lane of the warp at once).  The first pair's B_h^V rows are an
 // input, loaded before the wait on the scan kernel when they fit in
 // registers.
 constexpr int kCombineWarps = 8;
-constexpr int kCombinePieces = 16;
+constexpr int kCombineLocalB = 256;  // up to this batch, a warp finds its sequence's pieces from seq_lens
 constexpr int kCombinePre = 32;  // B^V words a lane may hold (2 rows of r <= 32)
 
 template <bool BF16, int KC>  // KC: columns per lane, ceil((dh + r) / 32)
 __global__ void __launch_bounds__(32 * kCombineWarps) lrkv_decode_combine_kernel(const DecodePlan P) {
   extern __shared__ __align__(16) unsigned char csmem[];
+  constexpr int kCombinePieces = KC <= 3 ? 32 : KC <= 6 ? 16 : 8;  // pieces of loads in flight
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = P.H, dh = P.dh, r = P.r, W = dh + r;
   float* zbar = reinterpret_cast<float*>(csmem) + warp * max(r, 1);  // [r] per warp
@@ -626,21 +627,40 @@ __global__ void __launch_bounds__(32 * kCombineWarps) lrkv_decode_combine_kernel
     }
   };
   if (pre_bv && bh < npairs) load_bv(static_cast<int>(bh % H));
+  // the first pair's sequence range and the scan's CTA count, from seq_lens
+  // (an input) the way the scan derives them, before the wait
+  const bool local = P.stream && P.B <= kCombineLocalB;
+  int l_start = 0, l_end = 0;
+  long long l_N = 0;
+  auto locate = [&](int b) {
+    int before = 0, mine = 0, total = 0;
+    for (int b0 = 0; b0 < P.B; b0 += 32) {
+      const int bb = b0 + lane;
+      const int L = bb < P.B ? min(max(P.seq_lens[bb], 0), P.max_len) : 0;
+      int x = bb < b ? L : 0, y = bb == b ? L : 0, z = L;
+      for (int o2 = 16; o2 > 0; o2 >>= 1) {
+        x += __shfl_xor_sync(0xffffffffu, x, o2);
+        y += __shfl_xor_sync(0xffffffffu, y, o2);
+        z += __shfl_xor_sync(0xffffffffu, z, o2);
+      }
+      before += x; mine += y; total += z;
+    }
+    l_start = before; l_end = before + mine; l_N = total;
+  };
+  if (local && bh < npairs) locate(static_cast<int>(bh / H));
   pdl_trigger();  // the next step's scan may launch (it waits before it writes)
   pdl_wait();
-  if (P.stream && blockIdx.x == 0 && warp == 0) {
-    // the device status of this call: the bits every scan CTA wrote
-    uint32_t bits = 0u;
-    for (int i = lane; i < P.grid * P.mt; i += 32) bits |= P.cta_status[i];
-    for (int o2 = 16; o2 > 0; o2 >>= 1) bits |= __shfl_xor_sync(0xffffffffu, bits, o2);
-    if (lane == 0) *P.status = bits;
-  }
-  const long long N = P.meta[0], G = P.meta[1];
+  const long long N = local ? l_N : P.meta[0];
+  const long long G = local ? max(1ll, min(static_cast<long long>(P.grid), (N + P.min_tokens - 1) / max(P.min_tokens, 1)))
+                            : P.meta[1];
   for (bool first = true; bh < npairs; bh += wstride, first = false) {
     const int b = static_cast<int>(bh / H), h = static_cast<int>(bh % H);
-    if (pre_bv && !first) load_bv(h);
+    if (!first) {
+      if (pre_bv) load_bv(h);
+      if (local) locate(b);
+    }
     float* o = P.out + (static_cast<size_t>(b) * H + h) * dh;
-    const int start = P.prefix[b], end = P.prefix[b + 1];
+    const int start = local ? l_start : P.prefix[b], end = local ? l_end : P.prefix[b + 1];
     if (end <= start) {
       for (int k = lane; k < dh; k += 32) o[k] = 0.f;
       if (lane == 0 && P.lse) P.lse[static_cast<size_t>(b) * H + h] = -INFINITY;
@@ -713,6 +733,13 @@ __global__ void __launch_bounds__(32 * kCombineWarps) lrkv_decode_combine_kernel
       o[d] = v;
     }
     if (lane == 0 && P.lse) P.lse[static_cast<size_t>(b) * H + h] = (M + log2f(L)) * kLn2;
+  }
+  if (P.stream && blockIdx.x == 0 && warp == 0) {
+    // the device status of this call: the bits every scan CTA wrote
+    uint32_t bits = 0u;
+    for (int i = lane; i < P.grid * P.mt; i += 32) bits |= P.cta_status[i];
+    for (int o2 = 16; o2 > 0; o2 >>= 1) bits |= __shfl_xor_sync(0xffffffffu, bits, o2);
+    if (lane == 0) *P.status = bits;
   }
 }
 
