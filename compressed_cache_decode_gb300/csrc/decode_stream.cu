@@ -401,8 +401,14 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     return;
   }
   const int c = blockIdx.x;
-  const int g0 = static_cast<int>(static_cast<long long>(c) * N / G);
-  const int g1 = static_cast<int>(static_cast<long long>(c + 1) * N / G);
+  int g0, g1;
+  if (static_cast<unsigned long long>(N) * G < (1ull << 32)) {  // 32-bit division when it fits
+    g0 = static_cast<int>(static_cast<unsigned>(c) * static_cast<unsigned>(N) / static_cast<unsigned>(G));
+    g1 = static_cast<int>(static_cast<unsigned>(c + 1) * static_cast<unsigned>(N) / static_cast<unsigned>(G));
+  } else {
+    g0 = static_cast<int>(static_cast<long long>(c) * N / G);
+    g1 = static_cast<int>(static_cast<long long>(c + 1) * N / G);
+  }
   // ---- 2. q of the first two pieces, then the first `stages` tiles (warp w
   // issues tiles w, w + 8, ...), so that the small copies land first ---------
   Piece pc;
@@ -459,7 +465,8 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     float* pa = reinterpret_cast<float*>(pq0 + 16 * dh * 2);
     float* pb = two ? reinterpret_cast<float*>(pq1 + 16 * dh * 2) : nullptr;
     if (P.bk_stages > 0) {
-      ok = ok && mbar_wait_bounded(bkbar, 0u);
+      const bool bk_in = mbar_wait_bounded(bkbar, 0u);  // always: the copy must land before exit
+      ok = ok && bk_in;
       absorb_rows_smem(P, bkr, smem + P.off_kv + static_cast<size_t>(first_burst) * P.stage_bytes, qa, qb2, pa,
                        pb);
     } else {
