@@ -8,9 +8,9 @@
 // ("Low-Rank Key Value Attention：中文研读笔记", §2.4, Eqs. (6)-(7); "Low-Rank
 // Key Value Attention | What a shared cache can preserve", §3).
 //
-// One CTA = (sequence b, head h, 128 query rows).  Warps 0-3 (one query row
-// per thread) run the softmax and the epilogue, warp 4 issues TMA, warp 5 one
-// thread issues every MMA:
+// One CTA = (sequence b, head h, 128 query rows).  Warps 0-7 run the softmax
+// and the epilogue (one query row per lane, each row split over two warps by
+// key columns), warp 8 issues TMA, one thread of warp 9 issues every MMA:
 //   Pq   = Q B_h^K          (TMEM, then split into two bf16 parts, high and
 //                           low, in shared memory, so the latent scores keep
 //                           about 16 significant bits)
@@ -37,11 +37,12 @@ namespace lrkv {
 namespace {
 
 constexpr int kBQ = 128, kBK = 128, kDH = 128, kR = 64;
+constexpr int kThreads = 320;  // warps 0-7 softmax, 8 TMA, 9 MMA
 constexpr float kPfLog2e = 1.44269504088896340736f;
 constexpr float kPfLn2 = 0.69314718055994530942f;
 // shared-memory carve-up (bytes, 1024-aligned)
 constexpr int kOffQ = 0;                       // Q: 2 boxes [128][64]      32 KB
-constexpr int kOffB = kOffQ + 32768;           // B^K then B^V: [128][64]   16 KB
+constexpr int kOffB = kOffQ + 32768;           // B^K, then the softmax max/sum swap  16 KB
 constexpr int kOffP = kOffB + 16384;           // bf16(Pq) high part, then bf16(O_z)  16 KB
 constexpr int kOffP2 = kOffP + 16384;          // bf16(Pq - high part)             16 KB
 constexpr int kOffK = kOffP2 + 16384;          // 2 x (K_s 32 KB + Z_k 16 KB)
@@ -84,9 +85,62 @@ __device__ __forceinline__ uint32_t sw128(int row, int col) {
   return static_cast<uint32_t>(row) * 128u + chunk * 16u + static_cast<uint32_t>(col & 7) * 2u;
 }
 
+__device__ __forceinline__ void named_bar(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// 2^x on the MUFU pipe (flush-to-zero; 2^-inf = +0)
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// max of three (sm_100 three-input max)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float y;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+  return y;
+}
+
+// 32 TMEM columns of this warp's 32 lanes, load and wait in one statement so
+// that no use of the registers can be scheduled before the data arrived
+__device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+        "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+        "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+// 64 TMEM columns (two 32-column loads, one wait)
+__device__ __forceinline__ void tmem_ld64_wait(uint32_t taddr, uint32_t (&v)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+        "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+        "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31]),
+        "=r"(v[32]), "=r"(v[33]), "=r"(v[34]), "=r"(v[35]), "=r"(v[36]), "=r"(v[37]), "=r"(v[38]), "=r"(v[39]),
+        "=r"(v[40]), "=r"(v[41]), "=r"(v[42]), "=r"(v[43]), "=r"(v[44]), "=r"(v[45]), "=r"(v[46]), "=r"(v[47]),
+        "=r"(v[48]), "=r"(v[49]), "=r"(v[50]), "=r"(v[51]), "=r"(v[52]), "=r"(v[53]), "=r"(v[54]), "=r"(v[55]),
+        "=r"(v[56]), "=r"(v[57]), "=r"(v[58]), "=r"(v[59]), "=r"(v[60]), "=r"(v[61]), "=r"(v[62]), "=r"(v[63])
+      : "r"(taddr), "r"(taddr + 32u)
+      : "memory");
+}
+
 }  // namespace
 
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     lrkv_prefill_kernel(const PrefillParams p, const __grid_constant__ PrefillMaps maps) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ uint64_t bar_q, bar_pq, bar_pqs, bar_bv, bar_pv, bar_all, bar_lift;
@@ -109,11 +163,11 @@ __global__ void __launch_bounds__(192, 1)
   const int nkt = last_key / kBK + 1;               // key tiles this query tile sees
 
   if (threadIdx.x == 0) {
-    mbar_init(&bar_q, 1); mbar_init(&bar_pq, 1); mbar_init(&bar_pqs, 128); mbar_init(&bar_bv, 1);
+    mbar_init(&bar_q, 1); mbar_init(&bar_pq, 1); mbar_init(&bar_pqs, 256); mbar_init(&bar_bv, 1);
     mbar_init(&bar_pv, 1); mbar_init(&bar_all, 1); mbar_init(&bar_lift, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar_kf[i], 1); mbar_init(&bar_ke[i], 1);
-      mbar_init(&bar_sf[i], 1); mbar_init(&bar_pf[i], 128);
+      mbar_init(&bar_sf[i], 1); mbar_init(&bar_pf[i], 256);
     }
     mbar_init(&bar_vf, 1); mbar_init(&bar_ve, 1);
     s_fail = 0;
@@ -128,7 +182,7 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t sP2 = smem_u32(smem + kOffP2);
   const uint32_t sK = smem_u32(smem + kOffK), sV = smem_u32(smem + kOffV);
 
-  if (warp == 4) {
+  if (warp == 8) {
     // =============================================================== TMA ====
     if (lane == 0) {
       bool ok = true;
@@ -154,13 +208,6 @@ __global__ void __launch_bounds__(192, 1)
       load_k(0);
       if (nkt > 1) load_k(1);
       load_v(0);
-      // B^V replaces B^K once Q B^K is computed
-      if (mbar_wait_bounded(&bar_pq, 0)) {
-        mbar_arrive_expect_tx(&bar_bv, 16384);
-        tma_load_3d(smem + kOffB, &maps.bv, 0, 0, h, &bar_bv);
-      } else {
-        ok = false;
-      }
       for (int j = 0; ok && j < nkt; ++j) {
         if (j + 2 < nkt) {  // K ring: stage of tile j frees when S_j is done
           if (!mbar_wait_bounded(&bar_ke[j & 1], static_cast<uint32_t>(j >> 1) & 1u)) { ok = false; break; }
@@ -171,9 +218,16 @@ __global__ void __launch_bounds__(192, 1)
           load_v(j + 1);
         }
       }
+      // B^V goes to the K stage of the last tile once its scores are done
+      if (ok && mbar_wait_bounded(&bar_ke[(nkt - 1) & 1], static_cast<uint32_t>((nkt - 1) >> 1) & 1u)) {
+        mbar_arrive_expect_tx(&bar_bv, 16384);
+        tma_load_3d(smem + kOffK + ((nkt - 1) & 1) * kKStage, &maps.bv, 0, 0, h, &bar_bv);
+      } else {
+        ok = false;
+      }
       if (!ok) s_fail = 1;
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // =============================================================== MMA ====
     if (lane == 0) {
       bool ok = mbar_wait_bounded(&bar_q, 0);
@@ -247,8 +301,9 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_after();
       if (ok) {
         const uint32_t id = idesc_bf16(kBQ, kDH, 0, 0);
+        const uint32_t sBv = sK + ((nkt - 1) & 1) * kKStage;
         for (int kk = 0; kk < kR / 16; ++kk)
-          tc_mma_ss(tmem + kColOs, smem_desc(sP + kk * 32, 16, 1024, 2), smem_desc(sB + kk * 32, 16, 1024, 2),
+          tc_mma_ss(tmem + kColOs, smem_desc(sP + kk * 32, 16, 1024, 2), smem_desc(sBv + kk * 32, 16, 1024, 2),
                     id, 1);
       } else {
         s_fail = 1;
@@ -257,111 +312,115 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     // ========================================================= softmax ====
-    const int row = threadIdx.x;                     // query row in the tile
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    // Warps w and w + 4 read the same 32 TMEM lanes (lane quadrant w % 4): one
+    // query row per lane; the first warp takes key columns 0-63 of every tile,
+    // the second columns 64-127.  The two halves of a row swap their maxima
+    // and, at the end, their sums through shared memory (the B^K region, free
+    // once Q B^K is computed) with one 64-thread named barrier per quadrant.
+    const int quad = warp & 3, half = warp >> 2;
+    const int row = quad * 32 + lane;                // query row in the tile
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const int qpos = off + q0 + row;                 // absolute position of this query
+    float* xmax = reinterpret_cast<float*>(smem + kOffB);          // [2 parities][2 halves][128]
+    float* xsum = reinterpret_cast<float*>(smem + kOffB + 2048);   // [2 halves][128]
     bool ok = mbar_wait_bounded(&bar_pq, 0);
     tc_fence_after();
     {
-      // Pq row -> high and low bf16 parts -> shared (A operands of S += Pq Z_k^T)
+      // this half's 32 columns of Pq -> high and low bf16 parts -> shared (A
+      // operands of S += Pq Z_k^T)
       uint32_t v[32];
+      tmem_ld32_wait(tmem + lane_off + kColPq + half * 32, v);
       unsigned char* pbase = smem + kOffP;
       unsigned char* pbase2 = smem + kOffP2;
-      for (int c = 0; c < kR / 32; ++c) {
-        tmem_ld32(tmem + lane_off + kColPq + c * 32, v);
-        tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float f0 = __uint_as_float(v[e]), f1 = __uint_as_float(v[e + 1]);
-          const __nv_bfloat162 hi = __floats2bfloat162_rn(f0, f1);
-          const __nv_bfloat162 lo = __floats2bfloat162_rn(f0 - __low2float(hi), f1 - __high2float(hi));
-          *reinterpret_cast<__nv_bfloat162*>(pbase + sw128(row, c * 32 + e)) = hi;
-          *reinterpret_cast<__nv_bfloat162*>(pbase2 + sw128(row, c * 32 + e)) = lo;
-        }
+      for (int e = 0; e < 32; e += 2) {
+        const float f0 = __uint_as_float(v[e]), f1 = __uint_as_float(v[e + 1]);
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(f0, f1);
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(f0 - __low2float(hi), f1 - __high2float(hi));
+        *reinterpret_cast<__nv_bfloat162*>(pbase + sw128(row, half * 32 + e)) = hi;
+        *reinterpret_cast<__nv_bfloat162*>(pbase2 + sw128(row, half * 32 + e)) = lo;
       }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive_cta(&bar_pqs);
     }
+    const float sc = p.scale_log2;
     float m_ref = -INFINITY, l_sum = 0.f;
     for (int j = 0; j < nkt; ++j) {
       const uint32_t sb = tmem + lane_off + kColS + (j & 1) * 128;
       ok = ok && mbar_wait_bounded(&bar_sf[j & 1], static_cast<uint32_t>(j >> 1) & 1u);
       tc_fence_after();
-      const int k0 = j * kBK;
-      // keys k0 + c visible iff k0 + c <= qpos and k0 + c < L
-      const int lim = min(qpos, L - 1) - k0;        // last visible column (may be < 0 or >= 127)
-      float mloc = -INFINITY;
-      uint32_t v[32];
-      for (int c = 0; c < 4; ++c) {
-        tmem_ld32(sb + c * 32, v);
-        tmem_wait_ld();
+      uint32_t v[64];
+      tmem_ld64_wait(sb + half * 64, v);
+      // keys j*128 + half*64 + c are visible iff c <= lim (causal and length)
+      const int lim = min(qpos, L - 1) - j * kBK - half * 64;
+      if (lim < 63) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-          if (c * 32 + e <= lim) mloc = fmaxf(mloc, __uint_as_float(v[e]) * p.scale_log2);
+        for (int e = 0; e < 64; ++e)
+          if (e > lim) v[e] = __float_as_uint(-INFINITY);
       }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < 64; e += 2) mx = fmax3(mx, __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+      float* xm = xmax + (j & 1) * 256;
+      xm[half * 128 + row] = mx;
+      named_bar(1 + quad, 64);
+      mx = fmaxf(mx, xm[(half ^ 1) * 128 + row]);
+      const float mloc = mx * sc;                    // scale > 0
       const bool need = j > 0 && mloc > m_ref + 8.f;
       if (j == 0) m_ref = mloc;
       if (__any_sync(0xffffffffu, need)) {
-        // rare: rescale the accumulators of the rows whose max moved, once
-        // P_{j-1} V_{j-1} is done (TMEM loads/stores are warp-wide)
-        const float alpha = need ? exp2f(m_ref - mloc) : 1.f;
+        // rare: rescale this half's share of the row's accumulators (O_s and
+        // O_z, 96 of the 192 columns) once P_{j-1} V_{j-1} is done
+        const float alpha = need ? ex2_approx(m_ref - mloc) : 1.f;
         ok = ok && mbar_wait_bounded(&bar_pv, static_cast<uint32_t>(j - 1) & 1u);
         tc_fence_after();
-        for (int c = 0; c < 6; ++c) {
+        for (int c = half * 3; c < half * 3 + 3; ++c) {
           const uint32_t col = c < 4 ? kColOs + c * 32 : kColOz + (c - 4) * 32;
-          tmem_ld32(tmem + lane_off + col, v);
-          tmem_wait_ld();
+          uint32_t o[32];
+          tmem_ld32_wait(tmem + lane_off + col, o);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-          tmem_st32(tmem + lane_off + col, v);
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(tmem + lane_off + col, o);
         }
         tmem_wait_st();
         l_sum *= alpha;
         if (need) m_ref = mloc;
       }
-      // probabilities against m_ref, packed bf16 into the S buffer's first 64 columns
-      uint32_t pk[64];
-      float lsum = 0.f;
-      for (int c = 0; c < 4; ++c) {
-        tmem_ld32(sb + c * 32, v);
-        tmem_wait_ld();
+      // probabilities against m_ref, bf16 pairs written over this half's
+      // share of the S buffer's first 64 columns
+      const float nm = -m_ref;
+      uint32_t pk[32];
+      float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const int col = c * 32 + e;
-          const float p0 = col <= lim ? exp2f(__uint_as_float(v[e]) * p.scale_log2 - m_ref) : 0.f;
-          const float p1 = col + 1 <= lim ? exp2f(__uint_as_float(v[e + 1]) * p.scale_log2 - m_ref) : 0.f;
-          const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-          lsum += __low2float(h2) + __high2float(h2);
-          pk[c * 16 + e / 2] = *reinterpret_cast<const uint32_t*>(&h2);
-        }
+      for (int e = 0; e < 64; e += 2) {
+        const float p0 = ex2_approx(fmaf(__uint_as_float(v[e]), sc, nm));
+        const float p1 = ex2_approx(fmaf(__uint_as_float(v[e + 1]), sc, nm));
+        ls0 += p0;
+        ls1 += p1;
+        const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+        pk[e / 2] = *reinterpret_cast<const uint32_t*>(&h2);
       }
-      l_sum += lsum;
-      uint32_t half[32];
-#pragma unroll
-      for (int e = 0; e < 32; ++e) half[e] = pk[e];
-      tmem_st32(sb, half);
-#pragma unroll
-      for (int e = 0; e < 32; ++e) half[e] = pk[32 + e];
-      tmem_st32(sb + 32, half);
+      l_sum += ls0 + ls1;
+      tmem_st32(sb + half * 32, pk);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive_cta(&bar_pf[j & 1]);
     }
-    // ---- O_z -> bf16 in shared memory for the lift ---------------------------
+    xsum[half * 128 + row] = l_sum;
+    named_bar(1 + quad, 64);
+    l_sum += xsum[(half ^ 1) * 128 + row];
+    // ---- O_z -> bf16 in shared memory for the lift (each half 32 columns) ----
     ok = ok && mbar_wait_bounded(&bar_all, 0);
     tc_fence_after();
     {
       uint32_t v[32];
+      tmem_ld32_wait(tmem + lane_off + kColOz + half * 32, v);
       unsigned char* pbase = smem + kOffP;
-      for (int c = 0; c < kR / 32; ++c) {
-        tmem_ld32(tmem + lane_off + kColOz + c * 32, v);
-        tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const __nv_bfloat162 v2 = __floats2bfloat162_rn(__uint_as_float(v[e]), __uint_as_float(v[e + 1]));
-          *reinterpret_cast<__nv_bfloat162*>(pbase + sw128(row, c * 32 + e)) = v2;
-        }
+      for (int e = 0; e < 32; e += 2) {
+        const __nv_bfloat162 v2 = __floats2bfloat162_rn(__uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+        *reinterpret_cast<__nv_bfloat162*>(pbase + sw128(row, half * 32 + e)) = v2;
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -372,23 +431,21 @@ __global__ void __launch_bounds__(192, 1)
     const int t = q0 + row;
     const bool store = t < p.Tq && ok && !s_fail;
     if (!ok || s_fail) {
-      if (row == 0) atomicOr(p.status, 1u);
+      if (row == 0 && half == 0) atomicOr(p.status, 1u);
     }
     const float inv_l = 1.f / l_sum;
-    float* dst = p.out + ((static_cast<size_t>(b) * p.Tq + t) * p.H + h) * kDH;
-    uint32_t v[32];
-    for (int c = 0; c < 4; ++c) {  // warp-wide TMEM reads; only real rows store
-      tmem_ld32(tmem + lane_off + kColOs + c * 32, v);
-      tmem_wait_ld();
-      if (store) {
+    float* dst = p.out + ((static_cast<size_t>(b) * p.Tq + t) * p.H + h) * kDH + half * 64;
+    uint32_t v[64];
+    tmem_ld64_wait(tmem + lane_off + kColOs + half * 64, v);  // warp-wide; only real rows store
+    if (store) {
 #pragma unroll
-        for (int e = 0; e < 32; e += 4)
-          *reinterpret_cast<float4*>(dst + c * 32 + e) =
-              make_float4(__uint_as_float(v[e]) * inv_l, __uint_as_float(v[e + 1]) * inv_l,
-                          __uint_as_float(v[e + 2]) * inv_l, __uint_as_float(v[e + 3]) * inv_l);
-      }
+      for (int e = 0; e < 64; e += 4)
+        *reinterpret_cast<float4*>(dst + e) =
+            make_float4(__uint_as_float(v[e]) * inv_l, __uint_as_float(v[e + 1]) * inv_l,
+                        __uint_as_float(v[e + 2]) * inv_l, __uint_as_float(v[e + 3]) * inv_l);
     }
-    if (store && p.lse) p.lse[(static_cast<size_t>(b) * p.H + h) * p.Tq + t] = (m_ref + log2f(l_sum)) * kPfLn2;
+    if (store && half == 0 && p.lse)
+      p.lse[(static_cast<size_t>(b) * p.H + h) * p.Tq + t] = (m_ref + log2f(l_sum)) * kPfLn2;
   }
   tc_fence_before();
   __syncthreads();
@@ -489,6 +546,6 @@ extern "C" lrkv_status lrkv_prefill(const lrkv_dims* dims, int q_len, const void
       cudaSuccess)
     return LRKV_ERR_CUDA;
   const dim3 grid((q_len + lrkv::kBQ - 1) / lrkv::kBQ, H, B);
-  lrkv::lrkv_prefill_kernel<<<grid, 192, lrkv::kSmem, s>>>(p, maps);
+  lrkv::lrkv_prefill_kernel<<<grid, lrkv::kThreads, lrkv::kSmem, s>>>(p, maps);
   return cudaGetLastError() == cudaSuccess ? LRKV_OK : LRKV_ERR_CUDA;
 }
