@@ -10,12 +10,14 @@
 //
 // One CTA = (sequence b, head h, 128 query rows).  Warps 0-7 run the softmax
 // and the epilogue (one query row per lane, each row split over two warps by
-// key columns), warp 8 issues TMA, one thread of warp 9 issues every MMA:
-//   Pq   = Q B_h^K          (TMEM, then split into two bf16 parts, high and
-//                           low, in shared memory, so the latent scores keep
-//                           about 16 significant bits)
+// key columns), warps 8 (queries, keys) and 10 (values) issue TMA, one thread
+// of warp 9 issues every MMA:
+//   Pq   = Q B_h^K          (TMEM, then split in place into two bf16 parts,
+//                           high and low, so the latent scores keep about 16
+//                           significant bits; both are TMEM A operands)
 //   S_j  = Q K_s,j^T + Pq Z_k,j^T        two TMEM buffers, S_{j+1} runs while
-//                                        the softmax of tile j does
+//                                        the softmax of tile j does; a ring
+//                                        of three key stages, one value stage
 //   O_s += P_j V_s,j ; O_z += P_j Z_v,j  P_j read straight from TMEM (the
 //                                        softmax overwrites S_j with bf16 P_j)
 //   O_s += bf16(O_z) (B_h^V)^T           the lift, once
@@ -37,23 +39,23 @@ namespace lrkv {
 namespace {
 
 constexpr int kBQ = 128, kBK = 128, kDH = 128, kR = 64;
-constexpr int kThreads = 320;  // warps 0-7 softmax, 8 TMA, 9 MMA
+constexpr int kThreads = 352;  // warps 0-7 softmax, 8 TMA (Q, keys), 9 MMA, 10 TMA (values)
 constexpr float kPfLog2e = 1.44269504088896340736f;
 constexpr float kPfLn2 = 0.69314718055994530942f;
 // shared-memory carve-up (bytes, 1024-aligned)
-constexpr int kOffQ = 0;                       // Q: 2 boxes [128][64]      32 KB
-constexpr int kOffB = kOffQ + 32768;           // B^K, then the softmax max/sum swap  16 KB
-constexpr int kOffP = kOffB + 16384;           // bf16(Pq) high part, then bf16(O_z)  16 KB
-constexpr int kOffP2 = kOffP + 16384;          // bf16(Pq - high part)             16 KB
-constexpr int kOffK = kOffP2 + 16384;          // 2 x (K_s 32 KB + Z_k 16 KB)
-constexpr int kKStage = 49152;
-constexpr int kOffV = kOffK + 2 * kKStage;     // 1 x (V_s 32 KB + Z_v 16 KB)
-constexpr int kSmem = kOffV + 49152 + 1024;    // + alignment slack
+constexpr int kOffQ = 0;                          // Q: [2 halves][128][64]             32 KB
+constexpr int kKStages = 3, kVStages = 1;
+constexpr int kKStage = 49152;                    // K_s [2][128][64] 32 KB + Z_k [128][64] 16 KB
+                                                  // (a value stage: V_s + Z_v, same shape)
+constexpr int kOffK = kOffQ + 32768;              // key ring; after the last scores its stage holds
+                                                  // B^V and then bf16(O_z)
+constexpr int kOffV = kOffK + kKStages * kKStage; // value ring (B^K in its last stage until Pq is done)
+constexpr int kSmem = kOffV + kVStages * kKStage + 1024;  // + alignment slack
 // TMEM columns
 constexpr uint32_t kColS = 0;      // S_0 [0,128), S_1 [128,256)
 constexpr uint32_t kColOs = 256;   // O_s [256,384)
 constexpr uint32_t kColOz = 384;   // O_z [384,448)
-constexpr uint32_t kColPq = 448;   // Q B^K [448,512)
+constexpr uint32_t kColPq = 448;   // fp32 Q B^K [448,512), then bf16 high part [448,480), low [480,512)
 
 struct PrefillParams {
   int B, H, Tq, max_len;
@@ -65,9 +67,9 @@ struct PrefillParams {
 };
 
 struct PrefillMaps {
-  CUtensorMap q;    // {dh, H, Tq, B}
-  CUtensorMap ks;   // {dh, max_len, B}
-  CUtensorMap vs;   // {dh, max_len, B}
+  CUtensorMap q;    // {64, Tq, 2, H, B}
+  CUtensorMap ks;   // {64, max_len, 2, B}
+  CUtensorMap vs;   // {64, max_len, 2, B}
   CUtensorMap zk;   // {r, H, max_len, B}
   CUtensorMap zv;   // {r, H, max_len, B}
   CUtensorMap bk;   // {r, dh, H}
@@ -76,6 +78,15 @@ struct PrefillMaps {
 
 __device__ __forceinline__ void mbar_arrive_cta(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_5d(void* dst_smem, const void* tmap, int x, int y, int z, int w, int v,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(
+          smem_u32(dst_smem)),
+      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(w), "r"(v), "r"(smem_u32(bar))
+      : "memory");
 }
 
 // byte offset of element (row, col) in a [rows][64] bf16 tile written with
@@ -118,6 +129,15 @@ __device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, uint32_t (&v)[32]
       : "memory");
 }
 
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+
 // 64 TMEM columns (two 32-column loads, one wait)
 __device__ __forceinline__ void tmem_ld64_wait(uint32_t taddr, uint32_t (&v)[64]) {
   asm volatile(
@@ -144,9 +164,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     lrkv_prefill_kernel(const PrefillParams p, const __grid_constant__ PrefillMaps maps) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ uint64_t bar_q, bar_pq, bar_pqs, bar_bv, bar_pv, bar_all, bar_lift;
-  __shared__ uint64_t bar_kf[2], bar_ke[2], bar_vf, bar_ve, bar_sf[2], bar_pf[2];
+  __shared__ uint64_t bar_kf[kKStages], bar_ke[kKStages], bar_vf[kVStages], bar_ve[kVStages], bar_sf[2], bar_pf[2];
   __shared__ uint32_t tmem_base;
   __shared__ int s_fail;
+  __shared__ float xchg[2][kBQ];  // the two halves of a row swap their maxima, at the end their sums
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -161,15 +182,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int off = L - p.Tq;                         // absolute position of query 0
   const int last_key = min(L - 1, off + q0 + kBQ - 1);
   const int nkt = last_key / kBK + 1;               // key tiles this query tile sees
+  const int klast = (nkt - 1) % kKStages;           // key stage of the last tile (B^V, bf16(O_z) after it)
 
   if (threadIdx.x == 0) {
     mbar_init(&bar_q, 1); mbar_init(&bar_pq, 1); mbar_init(&bar_pqs, 256); mbar_init(&bar_bv, 1);
     mbar_init(&bar_pv, 1); mbar_init(&bar_all, 1); mbar_init(&bar_lift, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar_kf[i], 1); mbar_init(&bar_ke[i], 1);
-      mbar_init(&bar_sf[i], 1); mbar_init(&bar_pf[i], 256);
-    }
-    mbar_init(&bar_vf, 1); mbar_init(&bar_ve, 1);
+    for (int i = 0; i < kKStages; ++i) { mbar_init(&bar_kf[i], 1); mbar_init(&bar_ke[i], 1); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&bar_sf[i], 1); mbar_init(&bar_pf[i], 256); }
+    for (int i = 0; i < kVStages; ++i) { mbar_init(&bar_vf[i], 1); mbar_init(&bar_ve[i], 1); }
     s_fail = 0;
     fence_barrier_init();
   }
@@ -178,52 +198,56 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base;
-  const uint32_t sQ = smem_u32(smem + kOffQ), sB = smem_u32(smem + kOffB), sP = smem_u32(smem + kOffP);
-  const uint32_t sP2 = smem_u32(smem + kOffP2);
-  const uint32_t sK = smem_u32(smem + kOffK), sV = smem_u32(smem + kOffV);
+  const uint32_t sQ = smem_u32(smem + kOffQ), sK = smem_u32(smem + kOffK), sV = smem_u32(smem + kOffV);
 
   if (warp == 8) {
-    // =============================================================== TMA ====
+    // ========================================================= TMA: Q, K ====
+    // One box per operand tile: the two 64-column halves of a 128-row tile
+    // of Q, k_s or v_s come in one copy (the halves are a tensor-map
+    // dimension), so a key tile costs two copies (k_s, z_k) and a value tile
+    // two more (v_s, z_v, issued by warp 10).
     if (lane == 0) {
       bool ok = true;
       mbar_arrive_expect_tx(&bar_q, 32768 + 16384);
-      tma_load_4d(smem + kOffQ, &maps.q, 0, h, q0, b, &bar_q);
-      tma_load_4d(smem + kOffQ + 16384, &maps.q, 64, h, q0, b, &bar_q);
-      tma_load_3d(smem + kOffB, &maps.bk, 0, 0, h, &bar_q);
+      tma_load_5d(smem + kOffQ, &maps.q, 0, q0, 0, h, b, &bar_q);
+      // B^K sits in the last value stage until Pq is done
+      tma_load_3d(smem + kOffV + (kVStages - 1) * kKStage, &maps.bk, 0, 0, h, &bar_q);
       auto load_k = [&](int j) {
-        const int s = j & 1;
+        const int s = j % kKStages;
         unsigned char* dst = smem + kOffK + s * kKStage;
         mbar_arrive_expect_tx(&bar_kf[s], kKStage);
-        tma_load_3d(dst, &maps.ks, 0, j * kBK, b, &bar_kf[s]);
-        tma_load_3d(dst + 16384, &maps.ks, 64, j * kBK, b, &bar_kf[s]);
+        tma_load_4d(dst, &maps.ks, 0, j * kBK, 0, b, &bar_kf[s]);
         tma_load_4d(dst + 32768, &maps.zk, 0, h, j * kBK, b, &bar_kf[s]);
       };
-      auto load_v = [&](int j) {
-        unsigned char* dst = smem + kOffV;
-        mbar_arrive_expect_tx(&bar_vf, kKStage);
-        tma_load_3d(dst, &maps.vs, 0, j * kBK, b, &bar_vf);
-        tma_load_3d(dst + 16384, &maps.vs, 64, j * kBK, b, &bar_vf);
-        tma_load_4d(dst + 32768, &maps.zv, 0, h, j * kBK, b, &bar_vf);
-      };
-      load_k(0);
-      if (nkt > 1) load_k(1);
-      load_v(0);
-      for (int j = 0; ok && j < nkt; ++j) {
-        if (j + 2 < nkt) {  // K ring: stage of tile j frees when S_j is done
-          if (!mbar_wait_bounded(&bar_ke[j & 1], static_cast<uint32_t>(j >> 1) & 1u)) { ok = false; break; }
-          load_k(j + 2);
-        }
-        if (j + 1 < nkt) {  // V stage frees when P_j V_j is done
-          if (!mbar_wait_bounded(&bar_ve, static_cast<uint32_t>(j) & 1u)) { ok = false; break; }
-          load_v(j + 1);
-        }
+      for (int j = 0; j < kKStages && j < nkt; ++j) load_k(j);
+      for (int j = 0; j + kKStages < nkt; ++j) {  // stage of tile j frees when S_j is done
+        if (!mbar_wait_bounded(&bar_ke[j % kKStages], static_cast<uint32_t>(j / kKStages) & 1u)) { ok = false; break; }
+        load_k(j + kKStages);
       }
-      // B^V goes to the K stage of the last tile once its scores are done
-      if (ok && mbar_wait_bounded(&bar_ke[(nkt - 1) & 1], static_cast<uint32_t>((nkt - 1) >> 1) & 1u)) {
+      // B^V goes to the key stage of the last tile once its scores are done
+      if (ok && mbar_wait_bounded(&bar_ke[klast], static_cast<uint32_t>((nkt - 1) / kKStages) & 1u)) {
         mbar_arrive_expect_tx(&bar_bv, 16384);
-        tma_load_3d(smem + kOffK + ((nkt - 1) & 1) * kKStage, &maps.bv, 0, 0, h, &bar_bv);
+        tma_load_3d(smem + kOffK + klast * kKStage, &maps.bv, 0, 0, h, &bar_bv);
       } else {
         ok = false;
+      }
+      if (!ok) s_fail = 1;
+    }
+  } else if (warp == 10) {
+    // ============================================================ TMA: V ====
+    if (lane == 0) {
+      auto load_v = [&](int j) {
+        const int s = j % kVStages;
+        unsigned char* dst = smem + kOffV + s * kKStage;
+        mbar_arrive_expect_tx(&bar_vf[s], kKStage);
+        tma_load_4d(dst, &maps.vs, 0, j * kBK, 0, b, &bar_vf[s]);
+        tma_load_4d(dst + 32768, &maps.zv, 0, h, j * kBK, b, &bar_vf[s]);
+      };
+      bool ok = mbar_wait_bounded(&bar_pq, 0);  // Q B^K done with B^K
+      for (int j = 0; ok && j < kVStages && j < nkt; ++j) load_v(j);
+      for (int j = 0; ok && j + kVStages < nkt; ++j) {  // stage of tile j frees when P_j V_j is done
+        if (!mbar_wait_bounded(&bar_ve[j % kVStages], static_cast<uint32_t>(j / kVStages) & 1u)) { ok = false; break; }
+        load_v(j + kVStages);
       }
       if (!ok) s_fail = 1;
     }
@@ -237,28 +261,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t id = idesc_bf16(kBQ, kR, 0, 1);
         for (int kk = 0; kk < kDH / 16; ++kk) {
           const uint64_t ad = smem_desc(sQ + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, 2);
-          const uint64_t bd = smem_desc(sB + kk * 2048, 16384, 1024, 2);
+          const uint64_t bd = smem_desc(sV + (kVStages - 1) * kKStage + kk * 2048, 16384, 1024, 2);
           tc_mma_ss(tmem + kColPq, ad, bd, id, kk > 0);
         }
         tc_commit(&bar_pq);
       }
-      ok = ok && mbar_wait_bounded(&bar_pqs, 0);  // bf16 Pq is in shared memory
+      ok = ok && mbar_wait_bounded(&bar_pqs, 0);  // bf16 Pq (high, low) is in TMEM
       tc_fence_after();
       const uint32_t id_s = idesc_bf16(kBQ, kBK, 0, 0);
       auto issue_s = [&](int j) {
-        const int s = j & 1;
+        const int s = j % kKStages;
         const uint32_t kbase = sK + s * kKStage;
-        const uint32_t d = tmem + kColS + s * 128;
+        const uint32_t d = tmem + kColS + (j & 1) * 128;
         for (int kk = 0; kk < kDH / 16; ++kk) {
           const uint32_t o = (kk >> 2) * 16384 + (kk & 3) * 32;
           tc_mma_ss(d, smem_desc(sQ + o, 16, 1024, 2), smem_desc(kbase + o, 16, 1024, 2), id_s, kk > 0);
         }
-        for (int kk = 0; kk < kR / 16; ++kk) {
+        for (int kk = 0; kk < kR / 16; ++kk) {  // A = Pq parts from TMEM, 8 columns per 16 values
           const uint64_t zd = smem_desc(kbase + 32768 + kk * 32, 16, 1024, 2);
-          tc_mma_ss(d, smem_desc(sP + kk * 32, 16, 1024, 2), zd, id_s, 1);
-          tc_mma_ss(d, smem_desc(sP2 + kk * 32, 16, 1024, 2), zd, id_s, 1);
+          tc_mma_ts(d, tmem + kColPq + kk * 8, zd, id_s, 1);
+          tc_mma_ts(d, tmem + kColPq + 32 + kk * 8, zd, id_s, 1);
         }
-        tc_commit(&bar_sf[s]);
+        tc_commit(&bar_sf[j & 1]);
         tc_commit(&bar_ke[s]);
       };
       if (ok) {
@@ -269,12 +293,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t id_vs = idesc_bf16(kBQ, kDH, 0, 1), id_vz = idesc_bf16(kBQ, kR, 0, 1);
       for (int j = 0; ok && j < nkt; ++j) {
         if (j + 1 < nkt) {
-          if (!mbar_wait_bounded(&bar_kf[(j + 1) & 1], static_cast<uint32_t>((j + 1) >> 1) & 1u)) { ok = false; break; }
+          const int s = (j + 1) % kKStages;
+          if (!mbar_wait_bounded(&bar_kf[s], static_cast<uint32_t>((j + 1) / kKStages) & 1u)) { ok = false; break; }
           tc_fence_after();
           issue_s(j + 1);
         }
+        const int vs = j % kVStages;
         if (!mbar_wait_bounded(&bar_pf[j & 1], static_cast<uint32_t>(j >> 1) & 1u) ||
-            !mbar_wait_bounded(&bar_vf, static_cast<uint32_t>(j) & 1u)) { ok = false; break; }
+            !mbar_wait_bounded(&bar_vf[vs], static_cast<uint32_t>(j / kVStages) & 1u)) { ok = false; break; }
         tc_fence_after();
         const int nv = L - j * kBK;  // rows of this value tile inside the history
         if (nv < kBK) {
@@ -282,65 +308,67 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int row = max(nv, 0); row < kBK; ++row)
             for (int box = 0; box < 3; ++box)
               for (int ch = 0; ch < 8; ++ch)
-                *reinterpret_cast<uint4*>(smem + kOffV + box * 16384 + row * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4*>(smem + kOffV + vs * kKStage + box * 16384 + row * 128 + ch * 16) =
+                    make_uint4(0, 0, 0, 0);
           fence_proxy_async_smem();
         }
         const uint32_t pa = tmem + kColS + (j & 1) * 128;  // bf16 P_j, 2 per column
         for (int kk = 0; kk < kBK / 16; ++kk) {
-          const uint32_t vo = sV + kk * 2048;
+          const uint32_t vo = sV + vs * kKStage + kk * 2048;
           tc_mma_ts(tmem + kColOs, pa + kk * 8, smem_desc(vo, 16384, 1024, 2), id_vs, (j > 0 || kk > 0) ? 1u : 0u);
           tc_mma_ts(tmem + kColOz, pa + kk * 8, smem_desc(vo + 32768, 16384, 1024, 2), id_vz,
                     (j > 0 || kk > 0) ? 1u : 0u);
         }
-        tc_commit(&bar_ve);
+        tc_commit(&bar_ve[vs]);
         tc_commit(&bar_pv);
       }
       tc_commit(&bar_all);
-      // lift: O_s += bf16(O_z) (B^V)^T : M=128, N=128 (dh), K=64 (r)
+      // lift: O_s += bf16(O_z) (B^V)^T : M=128, N=128 (dh), K=64 (r); B^V and
+      // bf16(O_z) sit in the key stage of the last tile
       ok = ok && mbar_wait_bounded(&bar_bv, 0) && mbar_wait_bounded(&bar_pqs, 1);
       tc_fence_after();
       if (ok) {
         const uint32_t id = idesc_bf16(kBQ, kDH, 0, 0);
-        const uint32_t sBv = sK + ((nkt - 1) & 1) * kKStage;
+        const uint32_t sBv = sK + klast * kKStage, sOz = sBv + 16384;
         for (int kk = 0; kk < kR / 16; ++kk)
-          tc_mma_ss(tmem + kColOs, smem_desc(sP + kk * 32, 16, 1024, 2), smem_desc(sBv + kk * 32, 16, 1024, 2),
+          tc_mma_ss(tmem + kColOs, smem_desc(sOz + kk * 32, 16, 1024, 2), smem_desc(sBv + kk * 32, 16, 1024, 2),
                     id, 1);
       } else {
         s_fail = 1;
       }
       tc_commit(&bar_lift);
     }
-  } else {
+  } else if (warp < 8) {
     // ========================================================= softmax ====
     // Warps w and w + 4 read the same 32 TMEM lanes (lane quadrant w % 4): one
     // query row per lane; the first warp takes key columns 0-63 of every tile,
     // the second columns 64-127.  The two halves of a row swap their maxima
-    // and, at the end, their sums through shared memory (the B^K region, free
-    // once Q B^K is computed) with one 64-thread named barrier per quadrant.
+    // and, at the end, their sums through shared memory, each swap between two
+    // 64-thread named barriers of the quadrant.
     const int quad = warp & 3, half = warp >> 2;
     const int row = quad * 32 + lane;                // query row in the tile
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const int qpos = off + q0 + row;                 // absolute position of this query
-    float* xmax = reinterpret_cast<float*>(smem + kOffB);          // [2 parities][2 halves][128]
-    float* xsum = reinterpret_cast<float*>(smem + kOffB + 2048);   // [2 halves][128]
     bool ok = mbar_wait_bounded(&bar_pq, 0);
     tc_fence_after();
     {
-      // this half's 32 columns of Pq -> high and low bf16 parts -> shared (A
-      // operands of S += Pq Z_k^T)
-      uint32_t v[32];
+      // Pq -> high and low bf16 parts, written back over the fp32 Pq columns
+      // (high [448,480), low [480,512)) as the A operands of S += Pq Z_k^T;
+      // each half converts its 32 values once both halves have read theirs
+      uint32_t v[32], hi[16], lo[16];
       tmem_ld32_wait(tmem + lane_off + kColPq + half * 32, v);
-      unsigned char* pbase = smem + kOffP;
-      unsigned char* pbase2 = smem + kOffP2;
 #pragma unroll
       for (int e = 0; e < 32; e += 2) {
         const float f0 = __uint_as_float(v[e]), f1 = __uint_as_float(v[e + 1]);
-        const __nv_bfloat162 hi = __floats2bfloat162_rn(f0, f1);
-        const __nv_bfloat162 lo = __floats2bfloat162_rn(f0 - __low2float(hi), f1 - __high2float(hi));
-        *reinterpret_cast<__nv_bfloat162*>(pbase + sw128(row, half * 32 + e)) = hi;
-        *reinterpret_cast<__nv_bfloat162*>(pbase2 + sw128(row, half * 32 + e)) = lo;
+        const __nv_bfloat162 h2 = __floats2bfloat162_rn(f0, f1);
+        const __nv_bfloat162 l2 = __floats2bfloat162_rn(f0 - __low2float(h2), f1 - __high2float(h2));
+        hi[e / 2] = *reinterpret_cast<const uint32_t*>(&h2);
+        lo[e / 2] = *reinterpret_cast<const uint32_t*>(&l2);
       }
-      fence_proxy_async_smem();
+      named_bar(1 + quad, 64);
+      tmem_st16(tmem + lane_off + kColPq + half * 16, hi);
+      tmem_st16(tmem + lane_off + kColPq + 32 + half * 16, lo);
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive_cta(&bar_pqs);
     }
@@ -362,10 +390,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       float mx = -INFINITY;
 #pragma unroll
       for (int e = 0; e < 64; e += 2) mx = fmax3(mx, __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
-      float* xm = xmax + (j & 1) * 256;
-      xm[half * 128 + row] = mx;
+      xchg[half][row] = mx;
       named_bar(1 + quad, 64);
-      mx = fmaxf(mx, xm[(half ^ 1) * 128 + row]);
+      mx = fmaxf(mx, xchg[half ^ 1][row]);
+      named_bar(1 + quad, 64);                       // both read before either writes again
       const float mloc = mx * sc;                    // scale > 0
       const bool need = j > 0 && mloc > m_ref + 8.f;
       if (j == 0) m_ref = mloc;
@@ -407,20 +435,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive_cta(&bar_pf[j & 1]);
     }
-    xsum[half * 128 + row] = l_sum;
+    xchg[half][row] = l_sum;
     named_bar(1 + quad, 64);
-    l_sum += xsum[(half ^ 1) * 128 + row];
+    l_sum += xchg[half ^ 1][row];
     // ---- O_z -> bf16 in shared memory for the lift (each half 32 columns) ----
     ok = ok && mbar_wait_bounded(&bar_all, 0);
     tc_fence_after();
     {
       uint32_t v[32];
       tmem_ld32_wait(tmem + lane_off + kColOz + half * 32, v);
-      unsigned char* pbase = smem + kOffP;
+      unsigned char* obase = smem + kOffK + klast * kKStage + 16384;
 #pragma unroll
       for (int e = 0; e < 32; e += 2) {
         const __nv_bfloat162 v2 = __floats2bfloat162_rn(__uint_as_float(v[e]), __uint_as_float(v[e + 1]));
-        *reinterpret_cast<__nv_bfloat162*>(pbase + sw128(row, half * 32 + e)) = v2;
+        *reinterpret_cast<__nv_bfloat162*>(obase + sw128(row, half * 32 + e)) = v2;
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -510,16 +538,19 @@ extern "C" lrkv_status lrkv_prefill(const lrkv_dims* dims, int q_len, const void
   lrkv::PrefillMaps maps;
   std::memset(&maps, 0, sizeof(maps));
   {
-    const uint64_t dm[4] = {dh, static_cast<uint64_t>(H), static_cast<uint64_t>(q_len), static_cast<uint64_t>(B)};
-    const uint64_t st[3] = {dh * 2, H * dh * 2, static_cast<uint64_t>(q_len) * H * dh * 2};
-    const uint32_t bx[4] = {64, 1, 128, 1};
-    if (!make_map(&maps.q, q, 4, dm, st, bx)) return LRKV_ERR_CUDA;
+    // q [B][Tq][H][128] seen as {64 columns, Tq, 2 halves, H, B}: one box of
+    // 128 rows x both halves lands as [half][row][64]
+    const uint64_t dm[5] = {64, static_cast<uint64_t>(q_len), 2, static_cast<uint64_t>(H), static_cast<uint64_t>(B)};
+    const uint64_t st[4] = {H * dh * 2, 128, dh * 2, static_cast<uint64_t>(q_len) * H * dh * 2};
+    const uint32_t bx[5] = {64, 128, 2, 1, 1};
+    if (!make_map(&maps.q, q, 5, dm, st, bx)) return LRKV_ERR_CUDA;
   }
   {
-    const uint64_t dm[3] = {dh, static_cast<uint64_t>(Lm), static_cast<uint64_t>(B)};
-    const uint64_t st[2] = {dh * 2, static_cast<uint64_t>(Lm) * dh * 2};
-    const uint32_t bx[3] = {64, 128, 1};
-    if (!make_map(&maps.ks, k_s, 3, dm, st, bx) || !make_map(&maps.vs, v_s, 3, dm, st, bx)) return LRKV_ERR_CUDA;
+    // k_s, v_s [B][max_len][128] seen as {64 columns, max_len, 2 halves, B}
+    const uint64_t dm[4] = {64, static_cast<uint64_t>(Lm), 2, static_cast<uint64_t>(B)};
+    const uint64_t st[3] = {dh * 2, 128, static_cast<uint64_t>(Lm) * dh * 2};
+    const uint32_t bx[4] = {64, 128, 2, 1};
+    if (!make_map(&maps.ks, k_s, 4, dm, st, bx) || !make_map(&maps.vs, v_s, 4, dm, st, bx)) return LRKV_ERR_CUDA;
   }
   {
     const uint64_t dm[4] = {r, static_cast<uint64_t>(H), static_cast<uint64_t>(Lm), static_cast<uint64_t>(B)};
