@@ -10,16 +10,16 @@
 //
 // One CTA = (sequence b, head h, 128 query rows).  Warps 0-7 run the softmax
 // and the epilogue (one query row per lane, each row split over two warps by
-// key columns), warps 8 (queries, keys) and 10 (values) issue TMA, one thread
-// of warp 9 issues every MMA:
+// key columns), warp 8 issues TMA, one thread of warp 9 issues every MMA:
 //   Pq   = Q B_h^K          (TMEM, then split in place into two bf16 parts,
 //                           high and low, so the latent scores keep about 16
 //                           significant bits; both are TMEM A operands)
 //   S_j  = Q K_s,j^T + Pq Z_k,j^T        two TMEM buffers, S_{j+1} runs while
-//                                        the softmax of tile j does; a ring
-//                                        of three key stages, one value stage
-//   O_s += P_j V_s,j ; O_z += P_j Z_v,j  P_j read straight from TMEM (the
-//                                        softmax overwrites S_j with bf16 P_j)
+//                                        the softmax of tile j does; two key
+//                                        and two value stages
+//   [O_s | O_z] += P_j [V_s,j | Z_v,j]   one N = 192 MMA per 16 keys, P_j read
+//                                        straight from TMEM (the softmax
+//                                        overwrites S_j with bf16 P_j)
 //   O_s += bf16(O_z) (B_h^V)^T           the lift, once
 // Scores are taken against a per-row reference max; the accumulators are
 // rescaled only when a row's max grows by more than 2^8 (then the row's own
@@ -39,18 +39,17 @@ namespace lrkv {
 namespace {
 
 constexpr int kBQ = 128, kBK = 128, kDH = 128, kR = 64;
-constexpr int kThreads = 352;  // warps 0-7 softmax, 8 TMA (Q, keys), 9 MMA, 10 TMA (values)
+constexpr int kThreads = 320;  // warps 0-7 softmax, 8 TMA, 9 MMA
 constexpr float kPfLog2e = 1.44269504088896340736f;
 constexpr float kPfLn2 = 0.69314718055994530942f;
 // shared-memory carve-up (bytes, 1024-aligned)
 constexpr int kOffQ = 0;                          // Q: [2 halves][128][64]             32 KB
-constexpr int kKStages = 3, kVStages = 1;
 constexpr int kKStage = 49152;                    // K_s [2][128][64] 32 KB + Z_k [128][64] 16 KB
                                                   // (a value stage: V_s + Z_v, same shape)
-constexpr int kOffK = kOffQ + 32768;              // key ring; after the last scores its stage holds
-                                                  // B^V and then bf16(O_z)
-constexpr int kOffV = kOffK + kKStages * kKStage; // value ring (B^K in its last stage until Pq is done)
-constexpr int kSmem = kOffV + kVStages * kKStage + 1024;  // + alignment slack
+constexpr int kOffK = kOffQ + 32768;              // 2 key stages; after the last scores the last
+                                                  // tile's stage holds B^V and then bf16(O_z)
+constexpr int kOffV = kOffK + 2 * kKStage;        // 2 value stages (B^K in stage 1 until Pq is done)
+constexpr int kSmem = kOffV + 2 * kKStage + 1024; // + alignment slack
 // TMEM columns
 constexpr uint32_t kColS = 0;      // S_0 [0,128), S_1 [128,256)
 constexpr uint32_t kColOs = 256;   // O_s [256,384)
@@ -164,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     lrkv_prefill_kernel(const PrefillParams p, const __grid_constant__ PrefillMaps maps) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ uint64_t bar_q, bar_pq, bar_pqs, bar_bv, bar_pv, bar_all, bar_lift;
-  __shared__ uint64_t bar_kf[kKStages], bar_ke[kKStages], bar_vf[kVStages], bar_ve[kVStages], bar_sf[2], bar_pf[2];
+  __shared__ uint64_t bar_k0, bar_g[2], bar_ve[2], bar_sf[2], bar_pf[2];
   __shared__ uint32_t tmem_base;
   __shared__ int s_fail;
   __shared__ float xchg[2][kBQ];  // the two halves of a row swap their maxima, at the end their sums
@@ -182,14 +181,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int off = L - p.Tq;                         // absolute position of query 0
   const int last_key = min(L - 1, off + q0 + kBQ - 1);
   const int nkt = last_key / kBK + 1;               // key tiles this query tile sees
-  const int klast = (nkt - 1) % kKStages;           // key stage of the last tile (B^V, bf16(O_z) after it)
+  const int klast = (nkt - 1) & 1;                  // key stage of the last tile (B^V, bf16(O_z) after it)
 
   if (threadIdx.x == 0) {
     mbar_init(&bar_q, 1); mbar_init(&bar_pq, 1); mbar_init(&bar_pqs, 256); mbar_init(&bar_bv, 1);
     mbar_init(&bar_pv, 1); mbar_init(&bar_all, 1); mbar_init(&bar_lift, 1);
-    for (int i = 0; i < kKStages; ++i) { mbar_init(&bar_kf[i], 1); mbar_init(&bar_ke[i], 1); }
+    mbar_init(&bar_k0, 1);
     for (int i = 0; i < 2; ++i) { mbar_init(&bar_sf[i], 1); mbar_init(&bar_pf[i], 256); }
-    for (int i = 0; i < kVStages; ++i) { mbar_init(&bar_vf[i], 1); mbar_init(&bar_ve[i], 1); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&bar_g[i], 1); mbar_init(&bar_ve[i], 1); }
     s_fail = 0;
     fence_barrier_init();
   }
@@ -201,53 +200,49 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sQ = smem_u32(smem + kOffQ), sK = smem_u32(smem + kOffK), sV = smem_u32(smem + kOffV);
 
   if (warp == 8) {
-    // ========================================================= TMA: Q, K ====
+    // ================================================================ TMA ====
     // One box per operand tile: the two 64-column halves of a 128-row tile
     // of Q, k_s or v_s come in one copy (the halves are a tensor-map
-    // dimension), so a key tile costs two copies (k_s, z_k) and a value tile
-    // two more (v_s, z_v, issued by warp 10).
+    // dimension).  After K_0 the copies go in groups, one barrier each:
+    // group t = {V_t, K_{t+1}} (four copies, 96 KB), issued back to back
+    // once P_{t-2} V_{t-2} is done (that frees value stage t % 2 and, the
+    // MMAs completing in issue order, the key stage of S_{t-1}).  The TMA
+    // unit serves copies that complete on one barrier faster than copies
+    // spread over several.
     if (lane == 0) {
       bool ok = true;
       mbar_arrive_expect_tx(&bar_q, 32768 + 16384);
       tma_load_5d(smem + kOffQ, &maps.q, 0, q0, 0, h, b, &bar_q);
-      // B^K sits in the last value stage until Pq is done
-      tma_load_3d(smem + kOffV + (kVStages - 1) * kKStage, &maps.bk, 0, 0, h, &bar_q);
-      auto load_k = [&](int j) {
-        const int s = j % kKStages;
-        unsigned char* dst = smem + kOffK + s * kKStage;
-        mbar_arrive_expect_tx(&bar_kf[s], kKStage);
-        tma_load_4d(dst, &maps.ks, 0, j * kBK, 0, b, &bar_kf[s]);
-        tma_load_4d(dst + 32768, &maps.zk, 0, h, j * kBK, b, &bar_kf[s]);
+      tma_load_3d(smem + kOffV + kKStage, &maps.bk, 0, 0, h, &bar_q);  // B^K: value stage 1 until Pq is done
+      auto load_k = [&](int j, uint64_t* bar) {
+        unsigned char* dst = smem + kOffK + (j & 1) * kKStage;
+        tma_load_4d(dst, &maps.ks, 0, j * kBK, 0, b, bar);
+        tma_load_4d(dst + 32768, &maps.zk, 0, h, j * kBK, b, bar);
       };
-      for (int j = 0; j < kKStages && j < nkt; ++j) load_k(j);
-      for (int j = 0; j + kKStages < nkt; ++j) {  // stage of tile j frees when S_j is done
-        if (!mbar_wait_bounded(&bar_ke[j % kKStages], static_cast<uint32_t>(j / kKStages) & 1u)) { ok = false; break; }
-        load_k(j + kKStages);
+      auto load_v = [&](int j, uint64_t* bar) {
+        unsigned char* dst = smem + kOffV + (j & 1) * kKStage;
+        tma_load_4d(dst, &maps.vs, 0, j * kBK, 0, b, bar);
+        tma_load_4d(dst + 32768, &maps.zv, 0, h, j * kBK, b, bar);
+      };
+      mbar_arrive_expect_tx(&bar_k0, kKStage);
+      load_k(0, &bar_k0);
+      for (int t = 0; t < nkt; ++t) {
+        if (t == 1)  // value stage 1 held B^K, key stage 0 held K_0
+          ok = mbar_wait_bounded(&bar_pq, 0) && mbar_wait_bounded(&bar_sf[0], 0);
+        else if (t >= 2)
+          ok = mbar_wait_bounded(&bar_ve[t & 1], static_cast<uint32_t>((t - 2) >> 1) & 1u);
+        if (!ok) break;
+        uint64_t* gb = &bar_g[t & 1];
+        mbar_arrive_expect_tx(gb, t + 1 < nkt ? 2 * kKStage : kKStage);
+        load_v(t, gb);
+        if (t + 1 < nkt) load_k(t + 1, gb);
       }
       // B^V goes to the key stage of the last tile once its scores are done
-      if (ok && mbar_wait_bounded(&bar_ke[klast], static_cast<uint32_t>((nkt - 1) / kKStages) & 1u)) {
+      if (ok && mbar_wait_bounded(&bar_sf[klast], static_cast<uint32_t>((nkt - 1) >> 1) & 1u)) {
         mbar_arrive_expect_tx(&bar_bv, 16384);
         tma_load_3d(smem + kOffK + klast * kKStage, &maps.bv, 0, 0, h, &bar_bv);
       } else {
         ok = false;
-      }
-      if (!ok) s_fail = 1;
-    }
-  } else if (warp == 10) {
-    // ============================================================ TMA: V ====
-    if (lane == 0) {
-      auto load_v = [&](int j) {
-        const int s = j % kVStages;
-        unsigned char* dst = smem + kOffV + s * kKStage;
-        mbar_arrive_expect_tx(&bar_vf[s], kKStage);
-        tma_load_4d(dst, &maps.vs, 0, j * kBK, 0, b, &bar_vf[s]);
-        tma_load_4d(dst + 32768, &maps.zv, 0, h, j * kBK, b, &bar_vf[s]);
-      };
-      bool ok = mbar_wait_bounded(&bar_pq, 0);  // Q B^K done with B^K
-      for (int j = 0; ok && j < kVStages && j < nkt; ++j) load_v(j);
-      for (int j = 0; ok && j + kVStages < nkt; ++j) {  // stage of tile j frees when P_j V_j is done
-        if (!mbar_wait_bounded(&bar_ve[j % kVStages], static_cast<uint32_t>(j / kVStages) & 1u)) { ok = false; break; }
-        load_v(j + kVStages);
       }
       if (!ok) s_fail = 1;
     }
@@ -261,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t id = idesc_bf16(kBQ, kR, 0, 1);
         for (int kk = 0; kk < kDH / 16; ++kk) {
           const uint64_t ad = smem_desc(sQ + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, 2);
-          const uint64_t bd = smem_desc(sV + (kVStages - 1) * kKStage + kk * 2048, 16384, 1024, 2);
+          const uint64_t bd = smem_desc(sV + kKStage + kk * 2048, 16384, 1024, 2);
           tc_mma_ss(tmem + kColPq, ad, bd, id, kk > 0);
         }
         tc_commit(&bar_pq);
@@ -270,8 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t id_s = idesc_bf16(kBQ, kBK, 0, 0);
       auto issue_s = [&](int j) {
-        const int s = j % kKStages;
-        const uint32_t kbase = sK + s * kKStage;
+        const uint32_t kbase = sK + (j & 1) * kKStage;
         const uint32_t d = tmem + kColS + (j & 1) * 128;
         for (int kk = 0; kk < kDH / 16; ++kk) {
           const uint32_t o = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -283,24 +277,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_mma_ts(d, tmem + kColPq + 32 + kk * 8, zd, id_s, 1);
         }
         tc_commit(&bar_sf[j & 1]);
-        tc_commit(&bar_ke[s]);
       };
       if (ok) {
-        if (!mbar_wait_bounded(&bar_kf[0], 0)) ok = false;
+        if (!mbar_wait_bounded(&bar_k0, 0)) ok = false;
         tc_fence_after();
         if (ok) issue_s(0);
       }
-      const uint32_t id_vs = idesc_bf16(kBQ, kDH, 0, 1), id_vz = idesc_bf16(kBQ, kR, 0, 1);
+      // values: one N = d_h + r = 192 MMA per 16 keys; the stage's v_s halves and z_v
+      // are three 64-column blocks 16 KB apart, O_s and O_z adjacent TMEM columns
+      const uint32_t id_v = idesc_bf16(kBQ, kDH + kR, 0, 1);
       for (int j = 0; ok && j < nkt; ++j) {
+        // group j = {V_j, K_{j+1}}
+        const uint32_t gpar = static_cast<uint32_t>(j >> 1) & 1u;
         if (j + 1 < nkt) {
-          const int s = (j + 1) % kKStages;
-          if (!mbar_wait_bounded(&bar_kf[s], static_cast<uint32_t>((j + 1) / kKStages) & 1u)) { ok = false; break; }
+          if (!mbar_wait_bounded(&bar_g[j & 1], gpar)) { ok = false; break; }
           tc_fence_after();
           issue_s(j + 1);
         }
-        const int vs = j % kVStages;
+        const int vs = j & 1;
         if (!mbar_wait_bounded(&bar_pf[j & 1], static_cast<uint32_t>(j >> 1) & 1u) ||
-            !mbar_wait_bounded(&bar_vf[vs], static_cast<uint32_t>(j / kVStages) & 1u)) { ok = false; break; }
+            !mbar_wait_bounded(&bar_g[j & 1], gpar)) { ok = false; break; }
         tc_fence_after();
         const int nv = L - j * kBK;  // rows of this value tile inside the history
         if (nv < kBK) {
@@ -315,9 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t pa = tmem + kColS + (j & 1) * 128;  // bf16 P_j, 2 per column
         for (int kk = 0; kk < kBK / 16; ++kk) {
           const uint32_t vo = sV + vs * kKStage + kk * 2048;
-          tc_mma_ts(tmem + kColOs, pa + kk * 8, smem_desc(vo, 16384, 1024, 2), id_vs, (j > 0 || kk > 0) ? 1u : 0u);
-          tc_mma_ts(tmem + kColOz, pa + kk * 8, smem_desc(vo + 32768, 16384, 1024, 2), id_vz,
-                    (j > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_ts(tmem + kColOs, pa + kk * 8, smem_desc(vo, 16384, 1024, 2), id_v, (j > 0 || kk > 0) ? 1u : 0u);
         }
         tc_commit(&bar_ve[vs]);
         tc_commit(&bar_pv);
