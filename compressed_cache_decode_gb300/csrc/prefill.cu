@@ -73,6 +73,7 @@ struct PrefillMaps {
   CUtensorMap zv;   // {r, H, max_len, B}
   CUtensorMap bk;   // {r, dh, H}
   CUtensorMap bv;   // {r, dh, H}
+  CUtensorMap out;  // fp32 {dh, H, Tq, B}, box 32 columns x 128 rows
 };
 
 __device__ __forceinline__ void mbar_arrive_cta(uint64_t* bar) {
@@ -86,6 +87,13 @@ __device__ __forceinline__ void tma_load_5d(void* dst_smem, const void* tmap, in
           smem_u32(dst_smem)),
       "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(w), "r"(v), "r"(smem_u32(bar))
       : "memory");
+}
+
+// 4-D tiled tensor store shared -> global (bulk group of this thread)
+__device__ __forceinline__ void tma_store_4d(const void* tmap, int x, int y, int z, int w, const void* src_smem) {
+  asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(tmap),
+               "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(src_smem))
+               : "memory");
 }
 
 // byte offset of element (row, col) in a [rows][64] bf16 tile written with
@@ -165,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint64_t bar_q, bar_pq, bar_pqs, bar_bv, bar_pv, bar_all, bar_lift;
   __shared__ uint64_t bar_k0, bar_g[2], bar_ve[2], bar_sf[2], bar_pf[2];
   __shared__ uint32_t tmem_base;
-  __shared__ int s_fail;
+  __shared__ int s_fail, s_bad;
   __shared__ float xchg[2][kBQ];  // the two halves of a row swap their maxima, at the end their sums
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
 
@@ -190,7 +198,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) { mbar_init(&bar_sf[i], 1); mbar_init(&bar_pf[i], 256); }
     for (int i = 0; i < 2; ++i) { mbar_init(&bar_g[i], 1); mbar_init(&bar_ve[i], 1); }
     s_fail = 0;
+    s_bad = 0;
     fence_barrier_init();
+    // the first copies go out before anything else: Q and B^K (the first
+    // MMA's operands; B^K sits in value stage 1 until Pq is done) and K_0
+    mbar_arrive_expect_tx(&bar_q, 32768 + 16384);
+    tma_load_5d(smem + kOffQ, &maps.q, 0, q0, 0, h, b, &bar_q);
+    tma_load_3d(smem + kOffV + kKStage, &maps.bk, 0, 0, h, &bar_q);
+    mbar_arrive_expect_tx(&bar_k0, kKStage);
+    tma_load_4d(smem + kOffK, &maps.ks, 0, 0, 0, b, &bar_k0);
+    tma_load_4d(smem + kOffK + 32768, &maps.zk, 0, h, 0, b, &bar_k0);
   }
   if (warp == 0) tmem_alloc(&tmem_base, 512);
   tc_fence_before();
@@ -211,9 +228,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // spread over several.
     if (lane == 0) {
       bool ok = true;
-      mbar_arrive_expect_tx(&bar_q, 32768 + 16384);
-      tma_load_5d(smem + kOffQ, &maps.q, 0, q0, 0, h, b, &bar_q);
-      tma_load_3d(smem + kOffV + kKStage, &maps.bk, 0, 0, h, &bar_q);  // B^K: value stage 1 until Pq is done
       auto load_k = [&](int j, uint64_t* bar) {
         unsigned char* dst = smem + kOffK + (j & 1) * kKStage;
         tma_load_4d(dst, &maps.ks, 0, j * kBK, 0, b, bar);
@@ -224,9 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_4d(dst, &maps.vs, 0, j * kBK, 0, b, bar);
         tma_load_4d(dst + 32768, &maps.zv, 0, h, j * kBK, b, bar);
       };
-      mbar_arrive_expect_tx(&bar_k0, kKStage);
-      load_k(0, &bar_k0);
-      for (int t = 0; t < nkt; ++t) {
+      for (int t = 0; t < nkt; ++t) {  // (Q, B^K and K_0 went out with the barrier set-up)
         if (t == 1)  // value stage 1 held B^K, key stage 0 held K_0
           ok = mbar_wait_bounded(&bar_pq, 0) && mbar_wait_bounded(&bar_sf[0], 0);
         else if (t >= 2)
@@ -450,23 +462,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ok = ok && mbar_wait_bounded(&bar_lift, 0);
     tc_fence_after();
-    const int t = q0 + row;
-    const bool store = t < p.Tq && ok && !s_fail;
-    if (!ok || s_fail) {
-      if (row == 0 && half == 0) atomicOr(p.status, 1u);
-    }
+    // o = O_s / l into shared memory (the value stages are free), four
+    // 32-column blocks of [128 rows][128 bytes] in the 128-byte swizzle, then
+    // four TMA stores (rows past q_len are clipped by the tensor map)
+    if (!ok) s_bad = 1;
     const float inv_l = 1.f / l_sum;
-    float* dst = p.out + ((static_cast<size_t>(b) * p.Tq + t) * p.H + h) * kDH + half * 64;
-    uint32_t v[64];
-    tmem_ld64_wait(tmem + lane_off + kColOs + half * 64, v);  // warp-wide; only real rows store
-    if (store) {
+    {
+      uint32_t v[64];
+      tmem_ld64_wait(tmem + lane_off + kColOs + half * 64, v);
 #pragma unroll
-      for (int e = 0; e < 64; e += 4)
-        *reinterpret_cast<float4*>(dst + e) =
+      for (int e = 0; e < 64; e += 4) {
+        const int col = half * 64 + e;
+        unsigned char* dst = smem + kOffV + (col >> 5) * 16384 + row * 128 +
+                             ((((col & 31) >> 2) ^ (row & 7)) << 4);
+        *reinterpret_cast<float4*>(dst) =
             make_float4(__uint_as_float(v[e]) * inv_l, __uint_as_float(v[e + 1]) * inv_l,
                         __uint_as_float(v[e + 2]) * inv_l, __uint_as_float(v[e + 3]) * inv_l);
+      }
     }
-    if (store && half == 0 && p.lse)
+    fence_proxy_async_smem();
+    named_bar(5, 256);
+    const bool failed = s_bad || s_fail;
+    if (threadIdx.x == 0) {
+      if (failed) {
+        atomicOr(p.status, 1u);
+      } else {
+        for (int k = 0; k < 4; ++k) tma_store_4d(&maps.out, 32 * k, h, q0, b, smem + kOffV + k * 16384);
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // shared memory read before exit
+      }
+    }
+    const int t = q0 + row;
+    if (!failed && t < p.Tq && half == 0 && p.lse)
       p.lse[(static_cast<size_t>(b) * p.H + h) * p.Tq + t] = (m_ref + log2f(l_sum)) * kPfLn2;
   }
   tc_fence_before();
@@ -496,14 +523,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 // bf16 tensor map of rank n (dims innermost first; strides in bytes of dims
 // 1..n-1), 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, int n, const uint64_t* dims, const uint64_t* strides,
-              const uint32_t* box) {
+              const uint32_t* box, CUtensorMapDataType ty = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   auto fn = encoder();
   if (!fn) return false;
   cuuint64_t d[5], s[4];
   cuuint32_t bx[5], es[5];
   for (int i = 0; i < n; ++i) { d[i] = dims[i]; bx[i] = box[i]; es[i] = 1; }
   for (int i = 0; i < n - 1; ++i) s[i] = strides[i];
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, n, const_cast<void*>(base), d, s, bx, es,
+  return fn(m, ty, n, const_cast<void*>(base), d, s, bx, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -557,6 +584,12 @@ extern "C" lrkv_status lrkv_prefill(const lrkv_dims* dims, int q_len, const void
     const uint64_t st[2] = {r * 2, dh * r * 2};
     const uint32_t bx[3] = {64, 128, 1};
     if (!make_map(&maps.bk, b_k, 3, dm, st, bx) || !make_map(&maps.bv, b_v, 3, dm, st, bx)) return LRKV_ERR_CUDA;
+  }
+  {
+    const uint64_t dm[4] = {dh, static_cast<uint64_t>(H), static_cast<uint64_t>(q_len), static_cast<uint64_t>(B)};
+    const uint64_t st[3] = {dh * 4, H * dh * 4, static_cast<uint64_t>(q_len) * H * dh * 4};
+    const uint32_t bx[4] = {32, 1, 128, 1};
+    if (!make_map(&maps.out, out, 4, dm, st, bx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32)) return LRKV_ERR_CUDA;
   }
   lrkv::PrefillParams p;
   p.B = B; p.H = H; p.Tq = q_len; p.max_len = Lm;
