@@ -58,6 +58,7 @@ constexpr uint32_t kColPq = 448;   // fp32 Q B^K [448,512), then bf16 high part 
 
 struct PrefillParams {
   int B, H, Tq, max_len;
+  int nsm;  // SMs: the CTA nsm places later in launch order runs in the next wave
   float scale_log2;
   const int32_t* seq_lens;
   float* out;
@@ -87,6 +88,13 @@ __device__ __forceinline__ void tma_load_5d(void* dst_smem, const void* tmap, in
           smem_u32(dst_smem)),
       "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(w), "r"(v), "r"(smem_u32(bar))
       : "memory");
+}
+
+// L2 prefetch of a 5-D tensor box (no destination, no completion)
+__device__ __forceinline__ void tma_prefetch_5d(const void* tmap, int x, int y, int z, int w, int v) {
+  asm volatile("cp.async.bulk.prefetch.tensor.5d.L2.global.tile [%0, {%1, %2, %3, %4, %5}];" ::"l"(tmap), "r"(x),
+               "r"(y), "r"(z), "r"(w), "r"(v)
+               : "memory");
 }
 
 // 4-D tiled tensor store shared -> global (bulk group of this thread)
@@ -208,6 +216,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_arrive_expect_tx(&bar_k0, kKStage);
     tma_load_4d(smem + kOffK, &maps.ks, 0, 0, 0, b, &bar_k0);
     tma_load_4d(smem + kOffK + 32768, &maps.zk, 0, h, 0, b, &bar_k0);
+    // the queries of the CTA one wave later start moving into L2 (q is read
+    // once, from HBM; the cache tiles are shared and already in L2)
+    const unsigned ncta = gridDim.x * gridDim.y * gridDim.z;
+    const unsigned nxt = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z) + static_cast<unsigned>(p.nsm);
+    if (nxt < ncta) {
+      const int x2 = static_cast<int>(nxt % gridDim.x), r2 = static_cast<int>(nxt / gridDim.x);
+      const int h2 = r2 % static_cast<int>(gridDim.y), b2 = r2 / static_cast<int>(gridDim.y);
+      tma_prefetch_5d(&maps.q, 0, (static_cast<int>(gridDim.x) - 1 - x2) * kBQ, 0, h2, b2);
+    }
   }
   if (warp == 0) tmem_alloc(&tmem_base, 512);
   tc_fence_before();
@@ -593,6 +610,15 @@ extern "C" lrkv_status lrkv_prefill(const lrkv_dims* dims, int q_len, const void
   }
   lrkv::PrefillParams p;
   p.B = B; p.H = H; p.Tq = q_len; p.max_len = Lm;
+  {
+    static int nsm = 0;
+    if (nsm == 0) {
+      int dev = 0;
+      if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return LRKV_ERR_CUDA;
+    }
+    p.nsm = nsm;
+  }
   const float scale = d.scale > 0.f ? d.scale : 1.f / std::sqrt(static_cast<float>(d.head_dim));
   p.scale_log2 = scale * lrkv::kPfLog2e;
   p.seq_lens = seq_lens; p.out = out; p.lse = lse;
