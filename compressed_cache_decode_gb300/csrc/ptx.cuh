@@ -248,6 +248,16 @@ __device__ __forceinline__ void tma_load_4d(void* dst_smem, const void* tmap, in
       : "memory");
 }
 
+// 5-D tiled tensor copy global -> shared.
+__device__ __forceinline__ void tma_load_5d(void* dst_smem, const void* tmap, int x, int y, int z, int w, int v,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(
+          smem_u32(dst_smem)),
+      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(w), "r"(v), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // --------------------------------------------------------- bf16 unpacking --
 // A 32-bit word holds two bf16 values (low half = lower address).  bf16 is the
 // top half of a binary32, so widening is a shift or a mask.
