@@ -8,9 +8,12 @@
 // ("Low-Rank Key Value Attention：中文研读笔记", §2.4, Eqs. (6)-(7); "Low-Rank
 // Key Value Attention | What a shared cache can preserve", §3).
 //
-// One CTA = (sequence b, head h, 128 query rows).  Warps 0-7 run the softmax
-// and the epilogue (one query row per lane, each row split over two warps by
-// key columns), warp 8 issues TMA, one thread of warp 9 issues every MMA:
+// Persistent: one CTA per SM works through items (sequence b, head h, 128
+// query rows), heaviest first, dealt out in a snake; an item's copies, Pq and
+// first scores overlap the previous item's last tiles and output.  Warps 0-7
+// run the softmax and the epilogue (one query row per lane, each row split
+// over two warps by key columns), warp 8 issues TMA, one thread of warp 9
+// issues every MMA:
 //   Pq   = Q B_h^K          (TMEM, then split in place into two bf16 parts,
 //                           high and low, so the latent scores keep about 16
 //                           significant bits; both are TMEM A operands)
@@ -27,6 +30,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 
@@ -58,7 +62,7 @@ constexpr uint32_t kColPq = 448;   // fp32 Q B^K [448,512), then bf16 high part 
 
 struct PrefillParams {
   int B, H, Tq, max_len;
-  int nsm;  // SMs: the CTA nsm places later in launch order runs in the next wave
+  int out_v8;  // out is 32-byte aligned: 256-bit stores
   float scale_log2;
   const int32_t* seq_lens;
   float* out;
@@ -74,7 +78,6 @@ struct PrefillMaps {
   CUtensorMap zv;   // {r, H, max_len, B}
   CUtensorMap bk;   // {r, dh, H}
   CUtensorMap bv;   // {r, dh, H}
-  CUtensorMap out;  // fp32 {dh, H, Tq, B}, box 32 columns x 128 rows
 };
 
 __device__ __forceinline__ void mbar_arrive_cta(uint64_t* bar) {
@@ -85,13 +88,6 @@ __device__ __forceinline__ void mbar_arrive_cta(uint64_t* bar) {
 __device__ __forceinline__ void tma_prefetch_5d(const void* tmap, int x, int y, int z, int w, int v) {
   asm volatile("cp.async.bulk.prefetch.tensor.5d.L2.global.tile [%0, {%1, %2, %3, %4, %5}];" ::"l"(tmap), "r"(x),
                "r"(y), "r"(z), "r"(w), "r"(v)
-               : "memory");
-}
-
-// 4-D tiled tensor store shared -> global (bulk group of this thread)
-__device__ __forceinline__ void tma_store_4d(const void* tmap, int x, int y, int z, int w, const void* src_smem) {
-  asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(tmap),
-               "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(src_smem))
                : "memory");
 }
 
@@ -164,57 +160,98 @@ __device__ __forceinline__ void tmem_ld64_wait(uint32_t taddr, uint32_t (&v)[64]
       : "memory");
 }
 
+// A work item: (sequence b, head h, 128 query rows from q0) and its keys.
+struct Item {
+  int b, h, q0, L, off, nkt;
+  bool valid, bad_len;
+};
+
+// Item k of CTA c among G: items ordered heaviest (latest query tile) first,
+// dealt to the CTAs in a snake (c, then G - 1 - c on the next round), which
+// evens out the CTAs' totals.
+__device__ __forceinline__ Item item_of(const PrefillParams& p, int c, int G, int k) {
+  Item it;
+  const int X = (p.Tq + kBQ - 1) / kBQ, HB = p.H * p.B;
+  const int idx = k * G + ((k & 1) ? G - 1 - c : c);
+  it.valid = idx < X * HB;
+  it.bad_len = false;
+  it.b = it.h = it.q0 = it.L = it.off = 0;
+  it.nkt = 1;
+  if (!it.valid) return it;
+  const int qtr = idx / HB, hb = idx - qtr * HB;
+  it.h = hb % p.H;
+  it.b = hb / p.H;
+  it.q0 = (X - 1 - qtr) * kBQ;
+  int L = p.seq_lens[it.b];
+  if (L < p.Tq || L > p.max_len) {
+    it.bad_len = true;
+    L = min(max(L, p.Tq), p.max_len);
+  }
+  it.L = L;
+  it.off = L - p.Tq;  // absolute position of query 0
+  const int last_key = min(L - 1, it.off + it.q0 + kBQ - 1);
+  it.nkt = last_key / kBK + 1;
+  return it;
+}
+
+// Bounded wait that also gives up as soon as another thread of the CTA
+// recorded a failure (so that a failed CTA leaves its item loop quickly).
+__device__ __forceinline__ bool pwait(uint64_t* bar, uint32_t parity, volatile int* fail) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*fail) return false;
+    if (clock64() - t0 > kWaitLimitCycles) {
+      *fail = 1;
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ void st_global_v8(float* dst, const float (&v)[8]) {
+  asm volatile("st.global.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst), "f"(v[0]), "f"(v[1]), "f"(v[2]),
+               "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7])
+               : "memory");
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(kThreads, 1)
     lrkv_prefill_kernel(const PrefillParams p, const __grid_constant__ PrefillMaps maps) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  __shared__ uint64_t bar_q, bar_pq, bar_pqs, bar_bv, bar_pv, bar_all, bar_lift;
+  __shared__ uint64_t bar_q, bar_pq, bar_pqs, bar_ozs, bar_bv, bar_pv, bar_all, bar_lift, bar_ofree;
   __shared__ uint64_t bar_k0, bar_g[2], bar_ve[2], bar_sf[2], bar_pf[2];
   __shared__ uint32_t tmem_base;
-  __shared__ int s_fail, s_bad;
+  __shared__ int s_fail;
   __shared__ float xchg[2][kBQ];  // the two halves of a row swap their maxima, at the end their sums
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  volatile int* fail = &s_fail;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qt = gridDim.x - 1 - blockIdx.x;  // heaviest (longest causal range) first
-  const int h = blockIdx.y, b = blockIdx.z;
-  const int q0 = qt * kBQ;
-  int L = p.seq_lens[b];
-  if (L < p.Tq || L > p.max_len) {
-    if (threadIdx.x == 0) atomicOr(p.status, 2u);
-    L = min(max(L, p.Tq), p.max_len);
-  }
-  const int off = L - p.Tq;                         // absolute position of query 0
-  const int last_key = min(L - 1, off + q0 + kBQ - 1);
-  const int nkt = last_key / kBK + 1;               // key tiles this query tile sees
-  const int klast = (nkt - 1) & 1;                  // key stage of the last tile (B^V, bf16(O_z) after it)
+  const int cta = blockIdx.x, G = gridDim.x;
 
   if (threadIdx.x == 0) {
     mbar_init(&bar_q, 1); mbar_init(&bar_pq, 1); mbar_init(&bar_pqs, 256); mbar_init(&bar_bv, 1);
-    mbar_init(&bar_pv, 1); mbar_init(&bar_all, 1); mbar_init(&bar_lift, 1);
+    mbar_init(&bar_pv, 1); mbar_init(&bar_all, 1); mbar_init(&bar_lift, 1); mbar_init(&bar_ofree, 256);
+    mbar_init(&bar_ozs, 256);
     mbar_init(&bar_k0, 1);
-    for (int i = 0; i < 2; ++i) { mbar_init(&bar_sf[i], 1); mbar_init(&bar_pf[i], 256); }
-    for (int i = 0; i < 2; ++i) { mbar_init(&bar_g[i], 1); mbar_init(&bar_ve[i], 1); }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_g[i], 1); mbar_init(&bar_ve[i], 1);
+      mbar_init(&bar_sf[i], 1); mbar_init(&bar_pf[i], 256);
+    }
     s_fail = 0;
-    s_bad = 0;
     fence_barrier_init();
-    // the first copies go out before anything else: Q and B^K (the first
-    // MMA's operands; B^K sits in value stage 1 until Pq is done) and K_0
-    mbar_arrive_expect_tx(&bar_q, 32768 + 16384);
-    tma_load_5d(smem + kOffQ, &maps.q, 0, q0, 0, h, b, &bar_q);
-    tma_load_3d(smem + kOffV + kKStage, &maps.bk, 0, 0, h, &bar_q);
-    mbar_arrive_expect_tx(&bar_k0, kKStage);
-    tma_load_4d(smem + kOffK, &maps.ks, 0, 0, 0, b, &bar_k0);
-    tma_load_4d(smem + kOffK + 32768, &maps.zk, 0, h, 0, b, &bar_k0);
-    // the queries of the CTA one wave later start moving into L2 (q is read
-    // once, from HBM; the cache tiles are shared and already in L2)
-    const unsigned ncta = gridDim.x * gridDim.y * gridDim.z;
-    const unsigned nxt = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z) + static_cast<unsigned>(p.nsm);
-    if (nxt < ncta) {
-      const int x2 = static_cast<int>(nxt % gridDim.x), r2 = static_cast<int>(nxt / gridDim.x);
-      const int h2 = r2 % static_cast<int>(gridDim.y), b2 = r2 / static_cast<int>(gridDim.y);
-      tma_prefetch_5d(&maps.q, 0, (static_cast<int>(gridDim.x) - 1 - x2) * kBQ, 0, h2, b2);
+    // the first item's copies go out before anything else: Q and B^K (the
+    // first MMA's operands; B^K sits in value stage 1 until Pq is done) and K_0
+    const Item it = item_of(p, cta, G, 0);
+    if (it.valid) {
+      mbar_arrive_expect_tx(&bar_q, 32768 + 16384);
+      tma_load_5d(smem + kOffQ, &maps.q, 0, it.q0, 0, it.h, it.b, &bar_q);
+      tma_load_3d(smem + kOffV + kKStage, &maps.bk, 0, 0, it.h, &bar_q);
+      mbar_arrive_expect_tx(&bar_k0, kKStage);
+      tma_load_4d(smem + kOffK, &maps.ks, 0, 0, 0, it.b, &bar_k0);
+      tma_load_4d(smem + kOffK + 32768, &maps.zk, 0, it.h, 0, it.b, &bar_k0);
     }
   }
   if (warp == 0) tmem_alloc(&tmem_base, 512);
@@ -228,62 +265,80 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================================ TMA ====
     // One box per operand tile: the two 64-column halves of a 128-row tile
     // of Q, k_s or v_s come in one copy (the halves are a tensor-map
-    // dimension).  After K_0 the copies go in groups, one barrier each:
-    // group t = {V_t, K_{t+1}} (four copies, 96 KB), issued back to back
-    // once P_{t-2} V_{t-2} is done (that frees value stage t % 2 and, the
-    // MMAs completing in issue order, the key stage of S_{t-1}).  The TMA
-    // unit serves copies that complete on one barrier faster than copies
-    // spread over several.
+    // dimension).  Tiles are numbered J over all of this CTA's items; group
+    // J = {V_J, K_{J+1}} (four copies, 96 KB, one barrier; K_{J+1} may be the
+    // next item's first key tile) goes out once P_{J-2} V_{J-2} is done, which
+    // frees value stage J % 2 and, the MMAs completing in issue order, the key
+    // stage of S_{J-1}.  When J - 1 ended an item, that key stage held the
+    // item's lift operands (B^V, bf16(O_z)) and the next item's B^K, so the
+    // group also waits for that lift and for the next Q B^K.  The TMA unit
+    // serves copies that complete on one barrier faster than copies spread
+    // over several.
     if (lane == 0) {
-      bool ok = true;
-      auto load_k = [&](int j, uint64_t* bar) {
+      auto load_k = [&](int j, const Item& w, int kt, uint64_t* bar) {
         unsigned char* dst = smem + kOffK + (j & 1) * kKStage;
-        tma_load_4d(dst, &maps.ks, 0, j * kBK, 0, b, bar);
-        tma_load_4d(dst + 32768, &maps.zk, 0, h, j * kBK, b, bar);
+        tma_load_4d(dst, &maps.ks, 0, kt * kBK, 0, w.b, bar);
+        tma_load_4d(dst + 32768, &maps.zk, 0, w.h, kt * kBK, w.b, bar);
       };
-      auto load_v = [&](int j, uint64_t* bar) {
+      auto load_v = [&](int j, const Item& w, int kt, uint64_t* bar) {
         unsigned char* dst = smem + kOffV + (j & 1) * kKStage;
-        tma_load_4d(dst, &maps.vs, 0, j * kBK, 0, b, bar);
-        tma_load_4d(dst + 32768, &maps.zv, 0, h, j * kBK, b, bar);
+        tma_load_4d(dst, &maps.vs, 0, kt * kBK, 0, w.b, bar);
+        tma_load_4d(dst + 32768, &maps.zv, 0, w.h, kt * kBK, w.b, bar);
       };
-      for (int t = 0; t < nkt; ++t) {  // (Q, B^K and K_0 went out with the barrier set-up)
-        if (t == 1)  // value stage 1 held B^K, key stage 0 held K_0
-          ok = mbar_wait_bounded(&bar_pq, 0) && mbar_wait_bounded(&bar_sf[0], 0);
-        else if (t >= 2)
-          ok = mbar_wait_bounded(&bar_ve[t & 1], static_cast<uint32_t>((t - 2) >> 1) & 1u);
+      bool ok = true;
+      int J = 0;  // this item's first tile
+      Item it = item_of(p, cta, G, 0);
+      for (int k = 0; ok && it.valid; ++k) {
+        const Item nx = item_of(p, cta, G, k + 1);
+        if (nx.valid) tma_prefetch_5d(&maps.q, 0, nx.q0, 0, nx.h, nx.b);  // its queries start moving into L2
+        for (int t = 0; ok && t < it.nkt; ++t) {
+          const int Jt = J + t;
+          if (Jt == 1)  // value stage 1 held the first B^K, key stage 0 held K_0
+            ok = pwait(&bar_pq, 0, fail) && pwait(&bar_sf[0], 0, fail);
+          else if (Jt >= 2)
+            ok = pwait(&bar_ve[Jt & 1], static_cast<uint32_t>((Jt - 2) >> 1) & 1u, fail);
+          // an item's first scores are issued after the previous item's last
+          // P V, so for its second group that P V does not vouch for them
+          if (ok && t == 1 && k > 0) ok = pwait(&bar_sf[J & 1], static_cast<uint32_t>(J >> 1) & 1u, fail);
+          const bool more_k = t + 1 < it.nkt || nx.valid;
+          if (ok && t == 0 && k > 0 && more_k)
+            ok = pwait(&bar_lift, static_cast<uint32_t>(k - 1) & 1u, fail) &&
+                 pwait(&bar_pq, static_cast<uint32_t>(k) & 1u, fail);
+          if (!ok) break;
+          uint64_t* gb = &bar_g[Jt & 1];
+          mbar_arrive_expect_tx(gb, more_k ? 2 * kKStage : kKStage);
+          load_v(Jt, it, t, gb);
+          if (t + 1 < it.nkt)
+            load_k(Jt + 1, it, t + 1, gb);
+          else if (nx.valid)
+            load_k(Jt + 1, nx, 0, gb);
+        }
         if (!ok) break;
-        uint64_t* gb = &bar_g[t & 1];
-        mbar_arrive_expect_tx(gb, t + 1 < nkt ? 2 * kKStage : kKStage);
-        load_v(t, gb);
-        if (t + 1 < nkt) load_k(t + 1, gb);
-      }
-      // B^V goes to the key stage of the last tile once its scores are done
-      if (ok && mbar_wait_bounded(&bar_sf[klast], static_cast<uint32_t>((nkt - 1) >> 1) & 1u)) {
+        // the item's last scores done: its key stage takes B^V (lift) and the
+        // next item's B^K; the next item's Q replaces this one's
+        const int Jl = J + it.nkt - 1;
+        ok = pwait(&bar_sf[Jl & 1], static_cast<uint32_t>(Jl >> 1) & 1u, fail);
+        if (!ok) break;
+        unsigned char* stg = smem + kOffK + (Jl & 1) * kKStage;
         mbar_arrive_expect_tx(&bar_bv, 16384);
-        tma_load_3d(smem + kOffK + klast * kKStage, &maps.bv, 0, 0, h, &bar_bv);
-      } else {
-        ok = false;
+        tma_load_3d(stg, &maps.bv, 0, 0, it.h, &bar_bv);
+        if (nx.valid) {
+          mbar_arrive_expect_tx(&bar_q, 32768 + 16384);
+          tma_load_5d(smem + kOffQ, &maps.q, 0, nx.q0, 0, nx.h, nx.b, &bar_q);
+          tma_load_3d(stg + 32768, &maps.bk, 0, 0, nx.h, &bar_q);
+        }
+        J += it.nkt;
+        it = nx;
       }
-      if (!ok) s_fail = 1;
     }
   } else if (warp == 9) {
     // =============================================================== MMA ====
     if (lane == 0) {
-      bool ok = mbar_wait_bounded(&bar_q, 0);
-      tc_fence_after();
-      if (ok) {
-        // Pq = Q B^K : M=128, N=64, K=128; B^K tile is [dh][r], r contiguous (MN-major)
-        const uint32_t id = idesc_bf16(kBQ, kR, 0, 1);
-        for (int kk = 0; kk < kDH / 16; ++kk) {
-          const uint64_t ad = smem_desc(sQ + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, 2);
-          const uint64_t bd = smem_desc(sV + kKStage + kk * 2048, 16384, 1024, 2);
-          tc_mma_ss(tmem + kColPq, ad, bd, id, kk > 0);
-        }
-        tc_commit(&bar_pq);
-      }
-      ok = ok && mbar_wait_bounded(&bar_pqs, 0);  // bf16 Pq (high, low) is in TMEM
-      tc_fence_after();
-      const uint32_t id_s = idesc_bf16(kBQ, kBK, 0, 0);
+      const uint32_t id_pq = idesc_bf16(kBQ, kR, 0, 1), id_s = idesc_bf16(kBQ, kBK, 0, 0);
+      // values: one N = d_h + r = 192 MMA per 16 keys; a value stage's v_s
+      // halves and z_v are three 64-column blocks 16 KB apart, O_s and O_z
+      // adjacent TMEM columns
+      const uint32_t id_v = idesc_bf16(kBQ, kDH + kR, 0, 1), id_l = idesc_bf16(kBQ, kDH, 0, 0);
       auto issue_s = [&](int j) {
         const uint32_t kbase = sK + (j & 1) * kKStage;
         const uint32_t d = tmem + kColS + (j & 1) * 128;
@@ -298,77 +353,103 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_commit(&bar_sf[j & 1]);
       };
-      if (ok) {
-        if (!mbar_wait_bounded(&bar_k0, 0)) ok = false;
+      // Pq = Q B^K : M=128, N=64, K=128; B^K tile is [dh][r], r contiguous (MN-major)
+      auto issue_pq = [&](int k, uint32_t sBk) {
+        bool good = pwait(&bar_q, static_cast<uint32_t>(k) & 1u, fail);
         tc_fence_after();
-        if (ok) issue_s(0);
-      }
-      // values: one N = d_h + r = 192 MMA per 16 keys; the stage's v_s halves and z_v
-      // are three 64-column blocks 16 KB apart, O_s and O_z adjacent TMEM columns
-      const uint32_t id_v = idesc_bf16(kBQ, kDH + kR, 0, 1);
-      for (int j = 0; ok && j < nkt; ++j) {
-        // group j = {V_j, K_{j+1}}
-        const uint32_t gpar = static_cast<uint32_t>(j >> 1) & 1u;
-        if (j + 1 < nkt) {
-          if (!mbar_wait_bounded(&bar_g[j & 1], gpar)) { ok = false; break; }
+        if (!good) return false;
+        for (int kk = 0; kk < kDH / 16; ++kk) {
+          const uint64_t ad = smem_desc(sQ + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, 2);
+          tc_mma_ss(tmem + kColPq, ad, smem_desc(sBk + kk * 2048, 16384, 1024, 2), id_pq, kk > 0);
+        }
+        tc_commit(&bar_pq);
+        return true;
+      };
+      int J = 0;
+      Item it = item_of(p, cta, G, 0);
+      bool ok = true;
+      for (int k = 0; ok && it.valid; ++k) {
+        if (it.bad_len) atomicOr(p.status, 2u);
+        // the first item's B^K sits in value stage 1, a later one's in the key
+        // stage of the previous item's last tile (after that item's lift)
+        if (!issue_pq(k, k == 0 ? sV + kKStage : sK + ((J - 1) & 1) * kKStage + 32768)) { ok = false; break; }
+        ok = pwait(&bar_pqs, static_cast<uint32_t>(k) & 1u, fail);  // bf16 Pq (high, low) is in TMEM
+        // K_J: the first item's came with the set-up; a later item's came in
+        // the previous item's last group, waited for before its last P V
+        if (ok && k == 0) ok = pwait(&bar_k0, 0u, fail);
+        tc_fence_after();
+        if (!ok) break;
+        issue_s(J);
+        for (int t = 0; t < it.nkt; ++t) {
+          const int Jt = J + t;
+          const uint32_t gpar = static_cast<uint32_t>(Jt >> 1) & 1u;  // group Jt = {V_Jt, K_Jt+1}
+          if (t + 1 < it.nkt) {
+            if (!pwait(&bar_g[Jt & 1], gpar, fail)) { ok = false; break; }
+            tc_fence_after();
+            issue_s(Jt + 1);
+          }
+          if (!pwait(&bar_pf[Jt & 1], static_cast<uint32_t>(Jt >> 1) & 1u, fail) ||
+              !pwait(&bar_g[Jt & 1], gpar, fail)) { ok = false; break; }
+          // the first P V of an item overwrites O: the previous item's O must be read out
+          if (t == 0 && k > 0 && !pwait(&bar_ofree, static_cast<uint32_t>(k - 1) & 1u, fail)) { ok = false; break; }
           tc_fence_after();
-          issue_s(j + 1);
+          const int vs = Jt & 1;
+          const int nv = it.L - t * kBK;  // rows of this value tile inside the history
+          if (nv < kBK) {
+            // rows past the history may hold anything; P is 0 there, so make them 0
+            for (int row = max(nv, 0); row < kBK; ++row)
+              for (int box = 0; box < 3; ++box)
+                for (int ch = 0; ch < 8; ++ch)
+                  *reinterpret_cast<uint4*>(smem + kOffV + vs * kKStage + box * 16384 + row * 128 + ch * 16) =
+                      make_uint4(0, 0, 0, 0);
+            fence_proxy_async_smem();
+          }
+          const uint32_t pa = tmem + kColS + (Jt & 1) * 128;  // bf16 P, 2 per column
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint32_t vo = sV + vs * kKStage + kk * 2048;
+            tc_mma_ts(tmem + kColOs, pa + kk * 8, smem_desc(vo, 16384, 1024, 2), id_v, (t > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(&bar_ve[vs]);
+          tc_commit(&bar_pv);
         }
-        const int vs = j & 1;
-        if (!mbar_wait_bounded(&bar_pf[j & 1], static_cast<uint32_t>(j >> 1) & 1u) ||
-            !mbar_wait_bounded(&bar_g[j & 1], gpar)) { ok = false; break; }
+        if (!ok) break;
+        tc_commit(&bar_all);
+        const int Jl = J + it.nkt - 1;
+        // lift: O_s += bf16(O_z) (B^V)^T : M=128, N=128 (dh), K=64 (r); B^V and
+        // bf16(O_z) sit in the key stage of the item's last tile
+        ok = pwait(&bar_bv, static_cast<uint32_t>(k) & 1u, fail) && pwait(&bar_ozs, static_cast<uint32_t>(k) & 1u, fail);
         tc_fence_after();
-        const int nv = L - j * kBK;  // rows of this value tile inside the history
-        if (nv < kBK) {
-          // rows past the history may hold anything; P is 0 there, so make them 0
-          for (int row = max(nv, 0); row < kBK; ++row)
-            for (int box = 0; box < 3; ++box)
-              for (int ch = 0; ch < 8; ++ch)
-                *reinterpret_cast<uint4*>(smem + kOffV + vs * kKStage + box * 16384 + row * 128 + ch * 16) =
-                    make_uint4(0, 0, 0, 0);
-          fence_proxy_async_smem();
-        }
-        const uint32_t pa = tmem + kColS + (j & 1) * 128;  // bf16 P_j, 2 per column
-        for (int kk = 0; kk < kBK / 16; ++kk) {
-          const uint32_t vo = sV + vs * kKStage + kk * 2048;
-          tc_mma_ts(tmem + kColOs, pa + kk * 8, smem_desc(vo, 16384, 1024, 2), id_v, (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        tc_commit(&bar_ve[vs]);
-        tc_commit(&bar_pv);
-      }
-      tc_commit(&bar_all);
-      // lift: O_s += bf16(O_z) (B^V)^T : M=128, N=128 (dh), K=64 (r); B^V and
-      // bf16(O_z) sit in the key stage of the last tile
-      ok = ok && mbar_wait_bounded(&bar_bv, 0) && mbar_wait_bounded(&bar_pqs, 1);
-      tc_fence_after();
-      if (ok) {
-        const uint32_t id = idesc_bf16(kBQ, kDH, 0, 0);
-        const uint32_t sBv = sK + klast * kKStage, sOz = sBv + 16384;
+        if (!ok) break;
+        const uint32_t sBv = sK + (Jl & 1) * kKStage, sOz = sBv + 16384;
         for (int kk = 0; kk < kR / 16; ++kk)
           tc_mma_ss(tmem + kColOs, smem_desc(sOz + kk * 32, 16, 1024, 2), smem_desc(sBv + kk * 32, 16, 1024, 2),
-                    id, 1);
-      } else {
-        s_fail = 1;
+                    id_l, 1);
+        tc_commit(&bar_lift);
+        J += it.nkt;
+        it = item_of(p, cta, G, k + 1);
       }
-      tc_commit(&bar_lift);
+      if (!ok) *fail = 1;
     }
   } else if (warp < 8) {
     // ========================================================= softmax ====
     // Warps w and w + 4 read the same 32 TMEM lanes (lane quadrant w % 4): one
     // query row per lane; the first warp takes key columns 0-63 of every tile,
     // the second columns 64-127.  The two halves of a row swap their maxima
-    // and, at the end, their sums through shared memory, each swap between two
-    // 64-thread named barriers of the quadrant.
+    // and, at the end of an item, their sums through shared memory, each swap
+    // between two 64-thread named barriers of the quadrant.  These warps never
+    // leave their loops early (a failed wait is skipped, not retried), so the
+    // named barriers always pair up.
     const int quad = warp & 3, half = warp >> 2;
     const int row = quad * 32 + lane;                // query row in the tile
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const int qpos = off + q0 + row;                 // absolute position of this query
-    bool ok = mbar_wait_bounded(&bar_pq, 0);
-    tc_fence_after();
-    {
-      // Pq -> high and low bf16 parts, written back over the fp32 Pq columns
-      // (high [448,480), low [480,512)) as the A operands of S += Pq Z_k^T;
-      // each half converts its 32 values once both halves have read theirs
+    const float sc = p.scale_log2;
+    bool ok = true;
+    // Pq -> high and low bf16 parts, written back over the fp32 Pq columns
+    // (high [448,480), low [480,512)) as the A operands of S += Pq Z_k^T;
+    // each half converts its 32 values once both halves have read theirs
+    auto split_pq = [&](int k) {
+      ok = ok && pwait(&bar_pq, static_cast<uint32_t>(k) & 1u, fail);
+      tc_fence_after();
       uint32_t v[32], hi[16], lo[16];
       tmem_ld32_wait(tmem + lane_off + kColPq + half * 32, v);
 #pragma unroll
@@ -385,127 +466,137 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive_cta(&bar_pqs);
-    }
-    const float sc = p.scale_log2;
-    float m_ref = -INFINITY, l_sum = 0.f;
-    for (int j = 0; j < nkt; ++j) {
-      const uint32_t sb = tmem + lane_off + kColS + (j & 1) * 128;
-      ok = ok && mbar_wait_bounded(&bar_sf[j & 1], static_cast<uint32_t>(j >> 1) & 1u);
-      tc_fence_after();
-      uint32_t v[64];
-      tmem_ld64_wait(sb + half * 64, v);
-      // keys j*128 + half*64 + c are visible iff c <= lim (causal and length)
-      const int lim = min(qpos, L - 1) - j * kBK - half * 64;
-      if (lim < 63) {
-#pragma unroll
-        for (int e = 0; e < 64; ++e)
-          if (e > lim) v[e] = __float_as_uint(-INFINITY);
-      }
-      float mx = -INFINITY;
-#pragma unroll
-      for (int e = 0; e < 64; e += 2) mx = fmax3(mx, __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
-      xchg[half][row] = mx;
-      named_bar(1 + quad, 64);
-      mx = fmaxf(mx, xchg[half ^ 1][row]);
-      named_bar(1 + quad, 64);                       // both read before either writes again
-      const float mloc = mx * sc;                    // scale > 0
-      const bool need = j > 0 && mloc > m_ref + 8.f;
-      if (j == 0) m_ref = mloc;
-      if (__any_sync(0xffffffffu, need)) {
-        // rare: rescale this half's share of the row's accumulators (O_s and
-        // O_z, 96 of the 192 columns) once P_{j-1} V_{j-1} is done
-        const float alpha = need ? ex2_approx(m_ref - mloc) : 1.f;
-        ok = ok && mbar_wait_bounded(&bar_pv, static_cast<uint32_t>(j - 1) & 1u);
+    };
+    int J = 0;
+    Item it = item_of(p, cta, G, 0);
+    if (it.valid) split_pq(0);
+    for (int k = 0; it.valid; ++k) {
+      const Item nx = item_of(p, cta, G, k + 1);
+      const int qpos = it.off + it.q0 + row;         // absolute position of this query
+      float m_ref = -INFINITY, l_sum = 0.f;
+      for (int t = 0; t < it.nkt; ++t) {
+        const int Jt = J + t;
+        const uint32_t sb = tmem + lane_off + kColS + (Jt & 1) * 128;
+        ok = ok && pwait(&bar_sf[Jt & 1], static_cast<uint32_t>(Jt >> 1) & 1u, fail);
         tc_fence_after();
-        for (int c = half * 3; c < half * 3 + 3; ++c) {
-          const uint32_t col = c < 4 ? kColOs + c * 32 : kColOz + (c - 4) * 32;
-          uint32_t o[32];
-          tmem_ld32_wait(tmem + lane_off + col, o);
+        uint32_t v[64];
+        tmem_ld64_wait(sb + half * 64, v);
+        // keys t*128 + half*64 + c are visible iff c <= lim (causal and length)
+        const int lim = min(qpos, it.L - 1) - t * kBK - half * 64;
+        if (lim < 63) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(tmem + lane_off + col, o);
+          for (int e = 0; e < 64; ++e)
+            if (e > lim) v[e] = __float_as_uint(-INFINITY);
         }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < 64; e += 2) mx = fmax3(mx, __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+        xchg[half][row] = mx;
+        named_bar(1 + quad, 64);
+        mx = fmaxf(mx, xchg[half ^ 1][row]);
+        named_bar(1 + quad, 64);                       // both read before either writes again
+        const float mloc = mx * sc;                    // scale > 0
+        const bool need = t > 0 && mloc > m_ref + 8.f;
+        if (t == 0) m_ref = mloc;
+        if (__any_sync(0xffffffffu, need)) {
+          // rare: rescale this half's share of the row's accumulators (O_s and
+          // O_z, 96 of the 192 columns) once the previous P V is done
+          const float alpha = need ? ex2_approx(m_ref - mloc) : 1.f;
+          ok = ok && pwait(&bar_pv, static_cast<uint32_t>(Jt - 1) & 1u, fail);
+          tc_fence_after();
+          for (int c = half * 3; c < half * 3 + 3; ++c) {
+            const uint32_t col = c < 4 ? kColOs + c * 32 : kColOz + (c - 4) * 32;
+            uint32_t o[32];
+            tmem_ld32_wait(tmem + lane_off + col, o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(tmem + lane_off + col, o);
+          }
+          tmem_wait_st();
+          l_sum *= alpha;
+          if (need) m_ref = mloc;
+        }
+        // probabilities against m_ref, bf16 pairs written over this half's
+        // share of the S buffer's first 64 columns
+        const float nm = -m_ref;
+        uint32_t pk[32];
+        float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+        for (int e = 0; e < 64; e += 2) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(v[e]), sc, nm));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(v[e + 1]), sc, nm));
+          ls0 += p0;
+          ls1 += p1;
+          const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+          pk[e / 2] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+        l_sum += ls0 + ls1;
+        tmem_st32(sb + half * 32, pk);
         tmem_wait_st();
-        l_sum *= alpha;
-        if (need) m_ref = mloc;
+        tc_fence_before();
+        mbar_arrive_cta(&bar_pf[Jt & 1]);
       }
-      // probabilities against m_ref, bf16 pairs written over this half's
-      // share of the S buffer's first 64 columns
-      const float nm = -m_ref;
-      uint32_t pk[32];
-      float ls0 = 0.f, ls1 = 0.f;
+      xchg[half][row] = l_sum;
+      named_bar(1 + quad, 64);
+      l_sum += xchg[half ^ 1][row];
+      named_bar(1 + quad, 64);
+      const int Jl = J + it.nkt - 1;
+      // ---- O_z -> bf16 in shared memory for the lift (each half 32 columns) ----
+      ok = ok && pwait(&bar_all, static_cast<uint32_t>(k) & 1u, fail);
+      tc_fence_after();
+      {
+        uint32_t v[32];
+        tmem_ld32_wait(tmem + lane_off + kColOz + half * 32, v);
+        unsigned char* obase = smem + kOffK + (Jl & 1) * kKStage + 16384;
 #pragma unroll
-      for (int e = 0; e < 64; e += 2) {
-        const float p0 = ex2_approx(fmaf(__uint_as_float(v[e]), sc, nm));
-        const float p1 = ex2_approx(fmaf(__uint_as_float(v[e + 1]), sc, nm));
-        ls0 += p0;
-        ls1 += p1;
-        const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-        pk[e / 2] = *reinterpret_cast<const uint32_t*>(&h2);
+        for (int e = 0; e < 32; e += 2) {
+          const __nv_bfloat162 v2 = __floats2bfloat162_rn(__uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+          *reinterpret_cast<__nv_bfloat162*>(obase + sw128(row, half * 32 + e)) = v2;
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive_cta(&bar_ozs);  // bf16(O_z) ready
       }
-      l_sum += ls0 + ls1;
-      tmem_st32(sb + half * 32, pk);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive_cta(&bar_pf[j & 1]);
-    }
-    xchg[half][row] = l_sum;
-    named_bar(1 + quad, 64);
-    l_sum += xchg[half ^ 1][row];
-    // ---- O_z -> bf16 in shared memory for the lift (each half 32 columns) ----
-    ok = ok && mbar_wait_bounded(&bar_all, 0);
-    tc_fence_after();
-    {
-      uint32_t v[32];
-      tmem_ld32_wait(tmem + lane_off + kColOz + half * 32, v);
-      unsigned char* obase = smem + kOffK + klast * kKStage + 16384;
-#pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        const __nv_bfloat162 v2 = __floats2bfloat162_rn(__uint_as_float(v[e]), __uint_as_float(v[e + 1]));
-        *reinterpret_cast<__nv_bfloat162*>(obase + sw128(row, half * 32 + e)) = v2;
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive_cta(&bar_pqs);  // second phase: bf16(O_z) ready
-    }
-    ok = ok && mbar_wait_bounded(&bar_lift, 0);
-    tc_fence_after();
-    // o = O_s / l into shared memory (the value stages are free), four
-    // 32-column blocks of [128 rows][128 bytes] in the 128-byte swizzle, then
-    // four TMA stores (rows past q_len are clipped by the tensor map)
-    if (!ok) s_bad = 1;
-    const float inv_l = 1.f / l_sum;
-    {
+      // the next item's Pq parts while this item's lift runs
+      if (nx.valid) split_pq(k + 1);
+      ok = ok && pwait(&bar_lift, static_cast<uint32_t>(k) & 1u, fail);
+      tc_fence_after();
+      // o = O_s / l: read this half's 64 columns, free O for the next item's
+      // first P V, then store from registers (rows past q_len are skipped)
       uint32_t v[64];
       tmem_ld64_wait(tmem + lane_off + kColOs + half * 64, v);
+      tc_fence_before();
+      mbar_arrive_cta(&bar_ofree);
+      const int tq = it.q0 + row;
+      if (ok && !*fail && tq < p.Tq) {
+        const float inv_l = 1.f / l_sum;
+        float* dst = p.out + ((static_cast<size_t>(it.b) * p.Tq + tq) * p.H + it.h) * kDH + half * 64;
+        if (p.out_v8) {
 #pragma unroll
-      for (int e = 0; e < 64; e += 4) {
-        const int col = half * 64 + e;
-        unsigned char* dst = smem + kOffV + (col >> 5) * 16384 + row * 128 +
-                             ((((col & 31) >> 2) ^ (row & 7)) << 4);
-        *reinterpret_cast<float4*>(dst) =
-            make_float4(__uint_as_float(v[e]) * inv_l, __uint_as_float(v[e + 1]) * inv_l,
-                        __uint_as_float(v[e + 2]) * inv_l, __uint_as_float(v[e + 3]) * inv_l);
+          for (int e = 0; e < 64; e += 8) {
+            float o[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) o[u] = __uint_as_float(v[e + u]) * inv_l;
+            st_global_v8(dst + e, o);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 64; e += 4)
+            *reinterpret_cast<float4*>(dst + e) =
+                make_float4(__uint_as_float(v[e]) * inv_l, __uint_as_float(v[e + 1]) * inv_l,
+                            __uint_as_float(v[e + 2]) * inv_l, __uint_as_float(v[e + 3]) * inv_l);
+        }
+        if (half == 0 && p.lse)
+          p.lse[(static_cast<size_t>(it.b) * p.H + it.h) * p.Tq + tq] = (m_ref + log2f(l_sum)) * kPfLn2;
       }
+      J += it.nkt;
+      it = nx;
     }
-    fence_proxy_async_smem();
-    named_bar(5, 256);
-    const bool failed = s_bad || s_fail;
-    if (threadIdx.x == 0) {
-      if (failed) {
-        atomicOr(p.status, 1u);
-      } else {
-        for (int k = 0; k < 4; ++k) tma_store_4d(&maps.out, 32 * k, h, q0, b, smem + kOffV + k * 16384);
-        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // shared memory read before exit
-      }
-    }
-    const int t = q0 + row;
-    if (!failed && t < p.Tq && half == 0 && p.lse)
-      p.lse[(static_cast<size_t>(b) * p.H + h) * p.Tq + t] = (m_ref + log2f(l_sum)) * kPfLn2;
+    if (!ok) *fail = 1;
   }
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0 && *fail) atomicOr(p.status, 1u);
   if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
@@ -593,26 +684,13 @@ extern "C" lrkv_status lrkv_prefill(const lrkv_dims* dims, int q_len, const void
     const uint32_t bx[3] = {64, 128, 1};
     if (!make_map(&maps.bk, b_k, 3, dm, st, bx) || !make_map(&maps.bv, b_v, 3, dm, st, bx)) return LRKV_ERR_CUDA;
   }
-  {
-    const uint64_t dm[4] = {dh, static_cast<uint64_t>(H), static_cast<uint64_t>(q_len), static_cast<uint64_t>(B)};
-    const uint64_t st[3] = {dh * 4, H * dh * 4, static_cast<uint64_t>(q_len) * H * dh * 4};
-    const uint32_t bx[4] = {32, 1, 128, 1};
-    if (!make_map(&maps.out, out, 4, dm, st, bx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32)) return LRKV_ERR_CUDA;
-  }
   lrkv::PrefillParams p;
   p.B = B; p.H = H; p.Tq = q_len; p.max_len = Lm;
-  {
-    static int nsm = 0;
-    if (nsm == 0) {
-      int dev = 0;
-      if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return LRKV_ERR_CUDA;
-    }
-    p.nsm = nsm;
-  }
+
   const float scale = d.scale > 0.f ? d.scale : 1.f / std::sqrt(static_cast<float>(d.head_dim));
   p.scale_log2 = scale * lrkv::kPfLog2e;
   p.seq_lens = seq_lens; p.out = out; p.lse = lse;
+  p.out_v8 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
   p.status = static_cast<uint32_t*>(ws);
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -620,7 +698,17 @@ extern "C" lrkv_status lrkv_prefill(const lrkv_dims* dims, int q_len, const void
   if (cudaFuncSetAttribute(lrkv::lrkv_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, lrkv::kSmem) !=
       cudaSuccess)
     return LRKV_ERR_CUDA;
-  const dim3 grid((q_len + lrkv::kBQ - 1) / lrkv::kBQ, H, B);
+  // persistent: one CTA per SM (the kernel deals the (sequence, head, query
+  // tile) items out itself)
+  static int nsm = 0;
+  if (nsm == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return LRKV_ERR_CUDA;
+  }
+  const long long items = static_cast<long long>((q_len + lrkv::kBQ - 1) / lrkv::kBQ) * H * B;
+  if (items > (1ll << 30)) return LRKV_ERR_UNSUPPORTED;
+  const int grid = static_cast<int>(std::min<long long>(nsm, items));
   lrkv::lrkv_prefill_kernel<<<grid, lrkv::kThreads, lrkv::kSmem, s>>>(p, maps);
   return cudaGetLastError() == cudaSuccess ? LRKV_OK : LRKV_ERR_CUDA;
 }
