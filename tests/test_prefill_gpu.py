@@ -37,6 +37,9 @@ def _check(out, lse, ref_o, ref_l, what):
     (2, 256, 2, [256, 300], 320),        # extra history before the queries, ragged key tile
     (1, 200, 1, [200], 256),             # partial query tile and key tile
     (2, 64, 3, [64, 500], 512),          # short block after a long history
+    # more (sequence, head, query tile) items than SMs: each persistent CTA
+    # runs several items back to back, of different sequences and lengths
+    (2, 512, 48, [512, 700], 768),
 ])
 def test_prefill_matches_oracle(shape):
     B, Tq, H, lens, Lm = shape
