@@ -342,6 +342,24 @@ def _bf16_peak():
 
 # -------------------------------------------------------------------- GPU arm
 
+def max_over_ranks(value, world, device):
+    """The job's time for a per-rank time: the slowest rank's (all-reduce MAX
+    over the default process group; the value itself when world == 1)."""
+    if world == 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(bytes_per_rank, world, ms_per_step):
+    """Whole-job throughput: all ranks' bytes per step over the slowest rank's
+    step time (every rank decodes its own batch: replicas)."""
+    return bytes_per_rank * world / (ms_per_step * 1e-3) / 1e9
+
+
 def main():
     a = _args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -431,11 +449,7 @@ def main():
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    ms = ev0.elapsed_time(ev1)
-    t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
+    ms_max = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
     ms_step = ms_max / K
 
     # dominant kernel (split-KV scan) timed alone with events around it; the
@@ -507,11 +521,7 @@ def main():
             e2e_step(i)
         e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / K_e2e
-    te = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(te, op=dist.ReduceOp.MAX)
-    e2e_ms = float(te.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / K_e2e, world, dev)
 
     prefill = None
     if not a.no_prefill:
@@ -523,7 +533,7 @@ def main():
 
     if rank == 0:
         peak, peak_kind = _peaks()
-        gbs = total_bytes * world / (ms_step * 1e-3) / 1e9
+        gbs = job_gbs(total_bytes, world, ms_step)
         achieved = split_bytes / (split_ms * 1e-3) / 1e9
         traffic = _profile_traffic(_src_sha())
         res = {
@@ -545,7 +555,7 @@ def main():
                          "algorithmic_bytes_per_launch": split_bytes, "launch_ms": split_ms,
                          "launch_timing": f"CUDA events around each launch, {split_timing} launches"},
             "cpu_baseline": cpu,
-            "e2e": {"value": total_bytes * world / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+            "e2e": {"value": job_gbs(total_bytes, world, e2e_ms), "unit": "GB/s",
                     "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": 3 * K,
             "clocks": clk.summary(),
