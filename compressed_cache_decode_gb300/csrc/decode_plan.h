@@ -69,6 +69,7 @@ struct DecodePlan {
   int kst;           // 16-wide steps over the latents of 8 heads (r / 2)
   int cm_stride;     // floats per head row of the on-chip merge buffer
   int pfw;           // tiles a CTA keeps prefetched into L2 beyond its ring
+  int after_append;  // 1: the launch before writes cache rows: the scan waits for it before its first copy
   int bk_dsplit;     // head-dim parts of the in-kernel q B^K (threads per output group)
   int bk_stages;     // ring stages that first hold the row tile's B^K (0: B^K read from global)
   int bk_warps;      // warps with absorb work (the first ones)
@@ -99,6 +100,9 @@ struct DecodePlan {
 
 // Fills everything but the operand pointers; returns the workspace size.
 lrkv_status decode_make_plan(const lrkv_dims& d, int num_sms, DecodePlan& P, size_t* ws_bytes);
+lrkv_status step_append_launch(const lrkv_dims& dm, int d_model, const void* x, const void* w_sk,
+                               const void* w_sv, const void* u_k, const void* u_v, const int32_t* seq_lens,
+                               void* k_s, void* v_s, void* z_k, void* z_v, int num_sms, void* stream);
 void decode_bind_workspace(DecodePlan& P, void* ws);
 lrkv_status decode_launch(const DecodePlan& P, void* stream, void* ev_begin = nullptr, void* ev_end = nullptr);
 

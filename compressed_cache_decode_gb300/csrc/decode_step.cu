@@ -1,0 +1,152 @@
+// decode_step.cu — one decode step of an attention layer: the new token's
+// cache rows from its layer input x ("Low-Rank Key Value Attention | What a
+// shared cache can preserve", §3, Algorithm 1, for one token; "Low-Rank Key
+// Value Attention：中文研读笔记", §2.3), then attention over the cache that
+// now holds them (Algorithm 2).  Two programmatically dependent launches:
+// this kernel writes the rows, the decode scan waits for it before it reads
+// the cache (its set-up overlaps this kernel).
+//
+// For a batch of one-token steps the projection is a matrix-vector product
+// per sequence, bound by reading the weights once: one warp per output
+// column (grid-stride), the weight row streamed with 16-byte loads, the batch's
+// x rows in shared memory, fp32 accumulation, bf16 (round to nearest even)
+// stores at cache row seq_lens[b] - 1.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+
+#include "lrkv.h"
+#include "ptx.cuh"
+
+namespace lrkv {
+
+namespace {
+
+constexpr int kStepThreads = 256;
+constexpr int kStepMaxB = 16;              // sequences per pass over the weights
+constexpr int kStepSmem = 192 * 1024;      // x rows of one pass
+
+struct StepParams {
+  int B, H, dh, r, d, max_len, bc;
+  const __nv_bfloat16* x;                  // [B][d]
+  const __nv_bfloat16* w_sk;               // [dh][d]
+  const __nv_bfloat16* w_sv;               // [dh][d]
+  const __nv_bfloat16* u_k;                // [H r][d]
+  const __nv_bfloat16* u_v;                // [H r][d]
+  const int32_t* seq_lens;                 // [B], rows [0, seq_lens[b]) incl. the new one
+  __nv_bfloat16 *k_s, *v_s, *z_k, *z_v;
+};
+
+__device__ __forceinline__ float dot8(const uint4 w, const uint4 x, float acc) {
+  acc = fmaf(bf_lo(w.x), bf_lo(x.x), acc); acc = fmaf(bf_hi(w.x), bf_hi(x.x), acc);
+  acc = fmaf(bf_lo(w.y), bf_lo(x.y), acc); acc = fmaf(bf_hi(w.y), bf_hi(x.y), acc);
+  acc = fmaf(bf_lo(w.z), bf_lo(x.z), acc); acc = fmaf(bf_hi(w.z), bf_hi(x.z), acc);
+  acc = fmaf(bf_lo(w.w), bf_lo(x.w), acc); acc = fmaf(bf_hi(w.w), bf_hi(x.w), acc);
+  return acc;
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kStepThreads) lrkv_append_token_kernel(const StepParams p) {
+  extern __shared__ __align__(16) unsigned char sx_raw[];
+  // x may come from the launch before: wait for it; only then may the decode
+  // scan launch (its set-up reads q and the lengths, which the launch before
+  // may also write; it waits for this grid before it reads the cache)
+  pdl_wait();
+  pdl_trigger();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int wpc = blockDim.x >> 5;
+  const int nwarps = gridDim.x * wpc, gw = blockIdx.x * wpc + warp;
+  const int HR = p.H * p.r, N = 2 * p.dh + 2 * HR;
+  const int chunks = p.d / 8;  // 16-byte chunks per row
+  uint4* xs = reinterpret_cast<uint4*>(sx_raw);
+  for (int b0 = 0; b0 < p.B; b0 += p.bc) {
+    const int nb = min(p.bc, p.B - b0);
+    __syncthreads();  // the previous pass is done with xs
+    const uint4* xg = reinterpret_cast<const uint4*>(p.x) + static_cast<size_t>(b0) * chunks;
+    for (int i = tid; i < nb * chunks; i += blockDim.x) xs[i] = xg[i];
+    __syncthreads();
+    for (int n = gw; n < N; n += nwarps) {
+      const __nv_bfloat16* wrow = n < p.dh ? p.w_sk + static_cast<size_t>(n) * p.d
+                                  : n < 2 * p.dh ? p.w_sv + static_cast<size_t>(n - p.dh) * p.d
+                                  : n < 2 * p.dh + HR ? p.u_k + static_cast<size_t>(n - 2 * p.dh) * p.d
+                                                      : p.u_v + static_cast<size_t>(n - 2 * p.dh - HR) * p.d;
+      const uint4* wv = reinterpret_cast<const uint4*>(wrow);
+      float acc[kStepMaxB];
+#pragma unroll
+      for (int b = 0; b < kStepMaxB; ++b) acc[b] = 0.f;
+      for (int c = lane; c < chunks; c += 32) {
+        const uint4 w = __ldg(wv + c);
+#pragma unroll
+        for (int b = 0; b < kStepMaxB; ++b)
+          if (b < nb) acc[b] = dot8(w, xs[b * chunks + c], acc[b]);
+      }
+      float mine = 0.f;  // lane b keeps the total of sequence b0 + b
+#pragma unroll
+      for (int b = 0; b < kStepMaxB; ++b) {
+        float v = acc[b];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == b) mine = v;
+      }
+      if (lane < nb) {
+        const int b = b0 + lane;
+        const int pos = p.seq_lens[b] - 1;  // the new token's row (lengths out of range: no row;
+                                            // the decode flags them)
+        if (pos >= 0 && pos < p.max_len) {
+          const size_t row = static_cast<size_t>(b) * p.max_len + pos;
+          __nv_bfloat16* dst = n < p.dh ? p.k_s + row * p.dh + n
+                               : n < 2 * p.dh ? p.v_s + row * p.dh + (n - p.dh)
+                               : n < 2 * p.dh + HR ? p.z_k + row * HR + (n - 2 * p.dh)
+                                                   : p.z_v + row * HR + (n - 2 * p.dh - HR);
+          *dst = __float2bfloat16_rn(mine);
+        }
+      }
+    }
+  }
+}
+
+// Host launch of the token rows (programmatic dependent launch after the
+// caller's previous work).  Checks were done by the caller.
+lrkv_status step_append_launch(const lrkv_dims& dm, int d_model, const void* x, const void* w_sk,
+                               const void* w_sv, const void* u_k, const void* u_v, const int32_t* seq_lens,
+                               void* k_s, void* v_s, void* z_k, void* z_v, int num_sms, void* stream) {
+  StepParams p;
+  p.B = dm.batch; p.H = dm.heads; p.dh = dm.head_dim; p.r = dm.rank; p.d = d_model; p.max_len = dm.max_len;
+  const long long row_bytes = static_cast<long long>(d_model) * 2;
+  p.bc = static_cast<int>(std::min<long long>(std::min(kStepMaxB, dm.batch), kStepSmem / row_bytes));
+  if (p.bc < 1) return LRKV_ERR_UNSUPPORTED;
+  p.x = static_cast<const __nv_bfloat16*>(x);
+  p.w_sk = static_cast<const __nv_bfloat16*>(w_sk); p.w_sv = static_cast<const __nv_bfloat16*>(w_sv);
+  p.u_k = static_cast<const __nv_bfloat16*>(u_k); p.u_v = static_cast<const __nv_bfloat16*>(u_v);
+  p.seq_lens = seq_lens;
+  p.k_s = static_cast<__nv_bfloat16*>(k_s); p.v_s = static_cast<__nv_bfloat16*>(v_s);
+  p.z_k = static_cast<__nv_bfloat16*>(z_k); p.z_v = static_cast<__nv_bfloat16*>(z_v);
+  const int smem = static_cast<int>(p.bc * row_bytes);
+  static int have = 0;
+  if (smem > 48 * 1024 && smem > have) {
+    if (cudaFuncSetAttribute(lrkv_append_token_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+      return LRKV_ERR_CUDA;
+    have = smem;
+  }
+  // one warp per output column, at most one CTA per SM
+  const long long N = 2ll * dm.head_dim + 2ll * dm.heads * dm.rank;
+  const long long wpc = kStepThreads / 32;
+  const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(num_sms, (N + wpc - 1) / wpc)));
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kStepThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, lrkv_append_token_kernel, p) == cudaSuccess ? LRKV_OK : LRKV_ERR_CUDA;
+}
+
+}  // namespace lrkv

@@ -430,6 +430,9 @@ __global__ void __launch_bounds__(kThreadsS, 1)
                   static_cast<const __nv_bfloat16*>(P.b_k) + static_cast<size_t>(m0) * dh * r, bytes, bkbar);
     }
   }
+  // a decode step's token rows come from the launch before: wait for it
+  // before the first cache copy (the set-up above overlapped it)
+  if (P.after_append) pdl_wait();
   if (lane == 0) {
     TileCursor cur;
     cur.pc = pc;

@@ -121,6 +121,40 @@ lrkv_status lrkv_decode_profiled(const lrkv_dims* dims, const void* q, const voi
                        ev_split_begin, ev_split_end);
 }
 
+lrkv_status lrkv_decode_step(const lrkv_dims* dims, int d_model, const void* x, const void* w_sk,
+                             const void* w_sv, const void* u_k, const void* u_v, const void* q, void* k_s,
+                             void* v_s, void* z_k, void* z_v, const void* b_k, const void* b_v,
+                             const int32_t* seq_lens, float* out, float* lse, void* ws, size_t ws_bytes,
+                             lrkv_stream_t stream) {
+  lrkv_status st = check_decode_dims(dims);
+  if (st != LRKV_OK) return st;
+  if (dims->dtype != LRKV_BF16 || dims->rank < 1) return LRKV_ERR_UNSUPPORTED;
+  if (d_model < 8 || d_model % 8 != 0) return LRKV_ERR_UNSUPPORTED;
+  if (!x || !w_sk || !w_sv || !u_k || !u_v) return LRKV_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_sk) || !aligned16(w_sv) || !aligned16(u_k) || !aligned16(u_v))
+    return LRKV_ERR_INVALID_ARG;
+  if (!q || !k_s || !v_s || !z_k || !z_v || !b_k || !b_v || !seq_lens || !out) return LRKV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_s) || !aligned16(v_s) || !aligned16(z_k) || !aligned16(z_v))
+    return LRKV_ERR_INVALID_ARG;
+  if (!ws) return LRKV_ERR_WORKSPACE;
+  if (!aligned16(ws)) return LRKV_ERR_INVALID_ARG;
+  int sms = 0;
+  if ((st = current_sm_count(&sms)) != LRKV_OK) return st;
+  lrkv::DecodePlan P;
+  size_t need = 0;
+  if ((st = lrkv::decode_make_plan(*dims, sms, P, &need)) != LRKV_OK) return st;
+  if (ws_bytes < need) return LRKV_ERR_WORKSPACE;
+  lrkv::decode_bind_workspace(P, ws);
+  P.q = q; P.k_s = k_s; P.v_s = v_s; P.z_k = z_k; P.z_v = z_v; P.b_k = b_k; P.b_v = b_v;
+  P.seq_lens = seq_lens; P.out = out; P.lse = lse;
+  P.after_append = 1;
+  // the token's rows first (every host check is done: nothing is enqueued on failure)
+  if ((st = lrkv::step_append_launch(*dims, d_model, x, w_sk, w_sv, u_k, u_v, seq_lens, k_s, v_s, z_k, z_v, sms,
+                                     stream)) != LRKV_OK)
+    return st;
+  return lrkv::decode_launch(P, stream, nullptr, nullptr);
+}
+
 lrkv_status lrkv_read_device_status(const void* ws, lrkv_stream_t stream, lrkv_status* out_status) {
   if (!ws || !out_status) return LRKV_ERR_INVALID_ARG;
   uint32_t word = 0;

@@ -38,6 +38,7 @@ EXPORTED = (
     "lrkv_decode_static_scratch",
     "lrkv_append",
     "lrkv_prefill",
+    "lrkv_decode_step",
     "lrkv_read_device_status",
 )
 
@@ -94,6 +95,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.lrkv_append.restype = ctypes.c_int
     lib.lrkv_append.argtypes = [dims_p, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, vp, i32p, vp, vp, vp,
                                 vp, vp, sz, vp]
+    lib.lrkv_decode_step.restype = ctypes.c_int
+    lib.lrkv_decode_step.argtypes = [dims_p, ctypes.c_int, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                     i32p, vp, vp, vp, sz, vp]
     lib.lrkv_prefill.restype = ctypes.c_int
     lib.lrkv_prefill.argtypes = [dims_p, ctypes.c_int, vp, vp, vp, vp, vp, vp, vp, i32p, vp, vp, vp, sz,
                                  vp]
@@ -243,6 +247,44 @@ def append(x: torch.Tensor, w_sk: torch.Tensor, w_sv: torch.Tensor, u_k: torch.T
     if st != LRKV_OK:
         raise LRKVError(st, "lrkv_append")
     return lrkv_read_device_status(ws, stream)
+
+
+def lrkv_decode_step(dims: lrkv_dims, d_model: int, x, w_sk, w_sv, u_k, u_v, q, k_s, v_s, z_k, z_v,
+                     b_k, b_v, seq_lens, out, lse, ws, ws_bytes: int, stream=None) -> int:
+    """Direct call of the decode-step entry point; returns its status code."""
+    return int(load().lrkv_decode_step(ctypes.byref(dims), d_model, _ptr(x), _ptr(w_sk), _ptr(w_sv),
+                                       _ptr(u_k), _ptr(u_v), _ptr(q), _ptr(k_s), _ptr(v_s), _ptr(z_k),
+                                       _ptr(z_v), _ptr(b_k), _ptr(b_v), _ptr(seq_lens), _ptr(out),
+                                       _ptr(lse), _ptr(ws), ws_bytes, _stream_handle(stream)))
+
+
+def decode_step(x: torch.Tensor, w_sk: torch.Tensor, w_sv: torch.Tensor, u_k: torch.Tensor,
+                u_v: torch.Tensor, q: torch.Tensor, k_s: torch.Tensor, v_s: torch.Tensor,
+                z_k: torch.Tensor, z_v: torch.Tensor, b_k: torch.Tensor, b_v: torch.Tensor,
+                seq_lens: torch.Tensor, scale: float = 0.0, out: Optional[torch.Tensor] = None,
+                lse: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
+                stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """One decode step: writes the token's rows (from x [B, d]) at
+    seq_lens[b] - 1, then decodes.  Allocates out/lse/workspace when not given."""
+    B, H, dh = q.shape
+    d = x.shape[-1]
+    dims = make_dims(B, H, dh, z_k.shape[-1], k_s.shape[1], q.dtype, scale)
+    if out is None:
+        out = torch.empty((B, H, dh), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = decode_workspace(dims, q.device)
+    for t in (x, w_sk, w_sv, u_k, u_v, q, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens):
+        if not t.is_contiguous():
+            raise ValueError("LRKV tensors must be contiguous")
+    if seq_lens.dtype != torch.int32:
+        raise ValueError("seq_lens must be int32")
+    st = lrkv_decode_step(dims, d, x, w_sk, w_sv, u_k, u_v, q, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens,
+                          out, lse, ws, ws.numel(), stream)
+    if st != LRKV_OK:
+        raise LRKVError(st, "lrkv_decode_step")
+    return out, lse
 
 
 def lrkv_prefill(dims: lrkv_dims, q_len: int, q, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens, out, lse,

@@ -229,6 +229,34 @@ lrkv_status lrkv_prefill(const lrkv_dims* dims, int q_len, const void* q, const 
                          lrkv_stream_t stream);
 
 /*
+ * One decode step of a layer: the new token's cache rows from its layer
+ * input x, then attention over the cache that now holds them ("Low-Rank Key
+ * Value Attention | What a shared cache can preserve", §3, Algorithm 1 for
+ * one token, then Algorithm 2; "Low-Rank Key Value Attention：中文研读笔记",
+ * §2.3-§2.4).  For every sequence b the token's
+ *   k_s = x W_sK^T, v_s = x W_sV^T, z_k,h = x U_h^K, z_v,h = x U_h^V
+ * (fp32 accumulation, rounded to bf16) are written at cache row
+ * seq_lens[b] - 1, then the call decodes exactly like lrkv_decode over rows
+ * [0, seq_lens[b]).  Two launches chained by programmatic dependent launch
+ * (the decode's set-up overlaps the projection), plus the decode's merge.
+ *
+ *   x          [batch][d_model]               the new token's layer input
+ *   w_sk, w_sv [head_dim][d_model]            as in lrkv_append (output-major)
+ *   u_k, u_v   [heads * rank][d_model]        as in lrkv_append
+ *   q, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens, out, lse, ws, ws_bytes: as in
+ *              lrkv_decode; seq_lens[b] counts the new token (seq_lens[b] = 0:
+ *              no row is written and that sequence decodes as empty)
+ * Supported: dtype BF16, rank >= 1, d_model a multiple of 8 (16-byte rows);
+ * the decode's own limits.  Lengths outside [0, max_len] write no row and
+ * set LRKV_ERR_DEVICE_BOUNDS through the decode.
+ */
+lrkv_status lrkv_decode_step(const lrkv_dims* dims, int d_model, const void* x, const void* w_sk,
+                             const void* w_sv, const void* u_k, const void* u_v, const void* q, void* k_s,
+                             void* v_s, void* z_k, void* z_v, const void* b_k, const void* b_v,
+                             const int32_t* seq_lens, float* out, float* lse, void* ws, size_t ws_bytes,
+                             lrkv_stream_t stream);
+
+/*
  * Read the device status word that the kernels of the last call(s) using
  * `ws` recorded (LRKV_OK, LRKV_ERR_TIMEOUT or LRKV_ERR_DEVICE_BOUNDS).
  * Synchronises `stream`.  Each lrkv_decode/lrkv_prefill call sets the word
