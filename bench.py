@@ -560,6 +560,49 @@ def main():
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / K_e2e, world, dev)
 
+    # decode step: the new token's rows from its layer input (d_model =
+    # heads x head_dim), then the decode, as one call per step, from a graph
+    step_leg = None
+    if not a.no_graph:
+        d_model = w.heads * w.head_dim
+        g = torch.Generator().manual_seed(1234)
+        xs = torch.randn(w.batch, d_model, generator=g).to(torch.bfloat16).to(dev)
+        ws_rows = [(torch.randn(n, d_model, generator=g) / d_model ** 0.5).to(torch.bfloat16).to(dev)
+                   for n in (w.head_dim, w.head_dim, w.heads * w.rank, w.heads * w.rank)]
+
+        def fstep(i, s=None):
+            x = reps[i % n_rep]
+            st = lrkv.lrkv_decode_step(dims, d_model, xs, *ws_rows, x["q"], x["k_s"], x["v_s"], x["z_k"],
+                                       x["z_v"], x["b_k"], x["b_v"], x["seq_lens"], out, lse, ws, ws.numel(),
+                                       s or stream)
+            if st != lrkv.LRKV_OK:
+                raise lrkv.LRKVError(st, "lrkv_decode_step")
+
+        with torch.cuda.stream(stream):
+            for i in range(W):
+                fstep(i)
+        torch.cuda.synchronize()
+        fg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(fg, stream=stream, capture_error_mode="thread_local"):
+            for i in range(K):
+                fstep(i, torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        fg.replay()
+        torch.cuda.synchronize()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            f0.record(stream)
+            fg.replay()
+            f1.record(stream)
+        torch.cuda.synchronize()
+        f_ms = max_over_ranks(f0.elapsed_time(f1) / K, world, dev)
+        w_bytes = sum(t.numel() * 2 for t in ws_rows)
+        rows_bytes = w.batch * 2 * (w.head_dim + w.heads * w.rank) * 2
+        step_leg = {"d_model": d_model, "ms_per_step": f_ms, "decode_ms_per_step": ms_step,
+                    "projection_ms_per_step": f_ms - ms_step,
+                    "algorithmic_bytes": total_bytes + w_bytes + xs.numel() * 2 + rows_bytes,
+                    "gbs": job_gbs(total_bytes + w_bytes + xs.numel() * 2 + rows_bytes, world, f_ms)}
+
     prefill = None
     if not a.no_prefill:
         prefill = prefill_leg(dev)
@@ -598,6 +641,7 @@ def main():
             # a bf16 step on the streaming path is two launches (scan, merge)
             "gpu_launches": 2 * K,
             "clocks": clk.summary(),
+            "decode_step": step_leg,
             "prefill": prefill,
         }
         print(json.dumps(res), flush=True)

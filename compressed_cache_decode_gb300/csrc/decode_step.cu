@@ -51,16 +51,29 @@ __device__ __forceinline__ float dot8(const uint4 w, const uint4 x, float acc) {
 
 __global__ void __launch_bounds__(kStepThreads) lrkv_append_token_kernel(const StepParams p) {
   extern __shared__ __align__(16) unsigned char sx_raw[];
-  // x may come from the launch before: wait for it; only then may the decode
-  // scan launch (its set-up reads q and the lengths, which the launch before
-  // may also write; it waits for this grid before it reads the cache)
-  pdl_wait();
-  pdl_trigger();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int wpc = blockDim.x >> 5;
   const int nwarps = gridDim.x * wpc, gw = blockIdx.x * wpc + warp;
   const int HR = p.H * p.r, N = 2 * p.dh + 2 * HR;
   const int chunks = p.d / 8;  // 16-byte chunks per row
+  auto weight_row = [&](int n) {
+    return n < p.dh ? p.w_sk + static_cast<size_t>(n) * p.d
+           : n < 2 * p.dh ? p.w_sv + static_cast<size_t>(n - p.dh) * p.d
+           : n < 2 * p.dh + HR ? p.u_k + static_cast<size_t>(n - 2 * p.dh) * p.d
+                               : p.u_v + static_cast<size_t>(n - 2 * p.dh - HR) * p.d;
+  };
+  // this warp's weight rows start moving into L2 while the launch before
+  // finishes (a prefetch reads nothing that could be stale: L2 is coherent)
+  for (int n = gw; n < N; n += nwarps) {
+    const char* row = reinterpret_cast<const char*>(weight_row(n));
+    for (int off = lane * 128; off < p.d * 2; off += 32 * 128)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(row + off));
+  }
+  // x may come from the launch before: wait for it; only then may the decode
+  // scan launch (its set-up reads q and the lengths, which the launch before
+  // may also write; it waits for this grid before it reads the cache)
+  pdl_wait();
+  pdl_trigger();
   uint4* xs = reinterpret_cast<uint4*>(sx_raw);
   for (int b0 = 0; b0 < p.B; b0 += p.bc) {
     const int nb = min(p.bc, p.B - b0);
@@ -69,11 +82,7 @@ __global__ void __launch_bounds__(kStepThreads) lrkv_append_token_kernel(const S
     for (int i = tid; i < nb * chunks; i += blockDim.x) xs[i] = xg[i];
     __syncthreads();
     for (int n = gw; n < N; n += nwarps) {
-      const __nv_bfloat16* wrow = n < p.dh ? p.w_sk + static_cast<size_t>(n) * p.d
-                                  : n < 2 * p.dh ? p.w_sv + static_cast<size_t>(n - p.dh) * p.d
-                                  : n < 2 * p.dh + HR ? p.u_k + static_cast<size_t>(n - 2 * p.dh) * p.d
-                                                      : p.u_v + static_cast<size_t>(n - 2 * p.dh - HR) * p.d;
-      const uint4* wv = reinterpret_cast<const uint4*>(wrow);
+      const uint4* wv = reinterpret_cast<const uint4*>(weight_row(n));
       float acc[kStepMaxB];
 #pragma unroll
       for (int b = 0; b < kStepMaxB; ++b) acc[b] = 0.f;

@@ -120,6 +120,9 @@ lrkv_status lrkv_decode_workspace_size(const lrkv_dims* dims, size_t* bytes);
  * ceil(heads/16) * head_dim / 8 <= 32; dtype F32 with rank <= 64,
  * head_dim <= 8 * (lanes per head); batch <= 4096.  Others return
  * LRKV_ERR_UNSUPPORTED.
+ * The call's kernels use programmatic dependent launch: its inputs must be
+ * complete when the launch before it on the stream lets its dependents start
+ * (a kernel that does not do so explicitly lets them start when it ends).
  */
 lrkv_status lrkv_decode(const lrkv_dims* dims, const void* q, const void* k_s, const void* v_s,
                         const void* z_k, const void* z_v, const void* b_k, const void* b_v,
