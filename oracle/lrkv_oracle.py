@@ -35,7 +35,12 @@ Readings where the pages leave a step open:
     and sees keys j <= that position (bottom-right causal alignment; the pages
     only say "causal").
   * an empty history (seq_lens[b] == 0) gives out = 0 and lse = -inf.
-  * no RoPE and no post-projection RMSNorm (notes §2.7; review §8).
+  * no RoPE (notes §2.7; review §8).  Post-projection RMSNorm only in the
+    *_normed functions (review §8, "Post-projection normalization has a cache
+    cost"): the key k_j = s_j + z_j B_h^T is divided by its joint RMS
+    n_{h,j} = sqrt(mean_d k_j[d]^2 + eps) (never the two parts by separate
+    norms); values are not normalised; a per-head gain is the caller's, folded
+    into q (the review's remark on affine gains).
   * lse is the natural-log log-sum-exp of the scaled, masked logits.
 """
 from __future__ import annotations
@@ -138,6 +143,75 @@ def decode_reference(q, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens, scale: Optional[
             lse[b, h] = -np.inf
             continue
         K = reconstruct_head(k_s[b, :L], z_k[b, :L, h, :], b_k[h])
+        V = reconstruct_head(v_s[b, :L], z_v[b, :L, h, :], b_v[h])
+        s = scale * (K @ q[b, h])
+        out[b, h], lse[b, h] = _softmax_attend(s, V)
+    return out, lse
+
+
+def _rms(K: np.ndarray, rms_eps: float) -> np.ndarray:
+    """Root mean square of every row of K [L, d_h] with eps inside the root
+    (the review's d_h n^2 = |k|^2 + d_h eps)."""
+    return np.sqrt(np.mean(K * K, axis=1) + rms_eps)
+
+
+def key_rms_scales(k_s, z_k, b_k, rms_eps: float) -> np.ndarray:
+    """Reciprocal post-projection RMS of every cached key (review §8,
+    "Post-projection normalization has a cache cost"): k_j = s_j + z_j B_h^T
+    rebuilt explicitly, n_{h,j} = sqrt(mean_d k_j[d]^2 + eps).  k_s [B, L, d_h],
+    z_k [B, L, H, r], b_k [H, d_h, r]; returns 1 / n [B, L, H]."""
+    k_s, z_k, b_k = (_f64(a) for a in (k_s, z_k, b_k))
+    B, L, dh = k_s.shape
+    H = z_k.shape[2]
+    out = np.empty((B, L, H))
+    for b in range(B):
+        for h in range(H):
+            K = reconstruct_head(k_s[b], z_k[b, :, h, :], b_k[h])
+            out[b, :, h] = 1.0 / _rms(K, rms_eps)
+    return out
+
+
+def key_rms_scales_expanded(k_s, z_k, b_k, rms_eps: float) -> np.ndarray:
+    """The same scale from the review's expansion of the squared norm,
+    d_h n^2 = |s|^2 + 2 s B z^T + z B^T B z^T + d_h eps (shared, cross and
+    private terms).  Used only to pin key_rms_scales."""
+    k_s, z_k, b_k = (_f64(a) for a in (k_s, z_k, b_k))
+    B, L, dh = k_s.shape
+    H = z_k.shape[2]
+    out = np.empty((B, L, H))
+    for h in range(H):
+        Bh = b_k[h]                                      # [d_h, r]
+        G = Bh.T @ Bh                                    # [r, r]
+        ss = np.einsum("bld,bld->bl", k_s, k_s)
+        cross = 2.0 * np.einsum("bld,dc,blc->bl", k_s, Bh, z_k[:, :, h, :])
+        priv = np.einsum("blc,ce,ble->bl", z_k[:, :, h, :], G, z_k[:, :, h, :])
+        out[:, :, h] = 1.0 / np.sqrt((ss + cross + priv) / dh + rms_eps)
+    return out
+
+
+def decode_reference_normed(q, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens, rms_eps: float,
+                            scale: Optional[float] = None,
+                            pairs: Optional[Iterable[Tuple[int, int]]] = None):
+    """decode_reference with post-projection RMSNorm of the keys (review §8):
+    every rebuilt key row is divided by its RMS sqrt(mean k^2 + eps) before the
+    scaled dot product with q; the softmax and the values are as in the plain
+    decode."""
+    q, k_s, v_s, z_k, z_v, b_k, b_v = (_f64(a) for a in (q, k_s, v_s, z_k, z_v, b_k, b_v))
+    lens = np.asarray(_f64(seq_lens), dtype=np.int64)
+    B, H, dh = q.shape
+    if scale is None:
+        scale = default_scale(dh)
+    out = np.full((B, H, dh), np.nan)
+    lse = np.full((B, H), np.nan)
+    todo = pairs if pairs is not None else [(b, h) for b in range(B) for h in range(H)]
+    for b, h in todo:
+        L = int(lens[b])
+        if L == 0:
+            out[b, h] = 0.0
+            lse[b, h] = -np.inf
+            continue
+        K = reconstruct_head(k_s[b, :L], z_k[b, :L, h, :], b_k[h])
+        K = K / _rms(K, rms_eps)[:, None]
         V = reconstruct_head(v_s[b, :L], z_v[b, :L, h, :], b_v[h])
         s = scale * (K @ q[b, h])
         out[b, h], lse[b, h] = _softmax_attend(s, V)

@@ -426,3 +426,89 @@ def test_planted_mistakes_are_caught(mutant, monkeypatch):
         monkeypatch.setattr(O, "_softmax_attend",
                             lambda s, V: orig(s[:-1], V[:-1]) if len(s) > 1 else orig(s, V))
     assert not all(c() for c in _PINS), mutant
+
+
+# --------------------------------------------------------------------------
+# Post-projection RMSNorm of the keys (review §8, "Post-projection
+# normalization has a cache cost"): the oracle's joint reciprocal scale and
+# the normalised decode.
+
+def _norm_case(seed):
+    rng = np.random.default_rng(seed)
+    B, H, dh, r, L = 2, 3, 8, 4, 7
+    k_s, v_s = _rand(rng, B, L, dh), _rand(rng, B, L, dh)
+    z_k, z_v = _rand(rng, B, L, H, r), _rand(rng, B, L, H, r)
+    b_k, b_v = _rand(rng, H, dh, r), _rand(rng, H, dh, r)
+    # head 0 of sequence 0: shared part nearly cancelling the private one, so
+    # the cross term of the expansion carries the norm
+    k_s[0] = -(z_k[0, :, 0, :] @ b_k[0].T) + 1e-3 * _rand(rng, L, dh)
+    q = _rand(rng, B, H, dh)
+    return q, k_s, v_s, z_k, z_v, b_k, b_v, [L, L - 2]
+
+
+def _check_norm_expansion():
+    """The scale from the rebuilt key equals the review's expansion
+    |s|^2 + 2 s B z^T + z B^T B z^T (with and without eps)."""
+    _, k_s, _, z_k, _, b_k, _, _ = _norm_case(31)
+    ok = True
+    for eps in (0.0, 1e-3):
+        a = O.key_rms_scales(k_s, z_k, b_k, eps)
+        e = O.key_rms_scales_expanded(k_s, z_k, b_k, eps)
+        ok = ok and np.allclose(a, e, rtol=1e-6, atol=0)
+    return ok
+
+
+def _check_norm_unit_rms_is_plain():
+    """Keys whose rows already have RMS 1 (eps 0): the normalised decode equals
+    the plain one."""
+    q, k_s, v_s, z_k, z_v, b_k, b_v, lens = _norm_case(32)
+    H = 1
+    q, z_k, z_v, b_k, b_v = q[:, :H], z_k[:, :, :H], z_v[:, :, :H], b_k[:H], b_v[:H]
+    K = k_s + np.einsum("blc,dc->bld", z_k[:, :, 0, :], b_k[0])
+    c = 1.0 / np.sqrt(np.mean(K * K, axis=2))           # per (b, j): scales s_j and z_j together
+    k_s, z_k = k_s * c[:, :, None], z_k * c[:, :, None, None]
+    plain, _ = O.decode_reference(q, k_s, v_s, z_k, z_v, b_k, b_v, lens)
+    normed, _ = O.decode_reference_normed(q, k_s, v_s, z_k, z_v, b_k, b_v, lens, 0.0)
+    return np.allclose(plain, normed, rtol=1e-10, atol=1e-12)
+
+
+def _check_norm_scale_invariance():
+    """eps 0: scaling every key (shared and private parts) by 3.7 changes
+    nothing after the norm, while the plain decode changes."""
+    q, k_s, v_s, z_k, z_v, b_k, b_v, lens = _norm_case(33)
+    a, la = O.decode_reference_normed(q, k_s, v_s, z_k, z_v, b_k, b_v, lens, 0.0)
+    b, lb = O.decode_reference_normed(q, 3.7 * k_s, v_s, 3.7 * z_k, z_v, b_k, b_v, lens, 0.0)
+    p1, _ = O.decode_reference(q, k_s, v_s, z_k, z_v, b_k, b_v, lens)
+    p2, _ = O.decode_reference(q, 3.7 * k_s, v_s, 3.7 * z_k, z_v, b_k, b_v, lens)
+    return np.allclose(a, b, rtol=1e-10, atol=1e-12) and np.allclose(la, lb) and not np.allclose(p1, p2)
+
+
+def _check_norm_single_row():
+    """One visible row: lse = scale q . k / rms(k) for the rebuilt key."""
+    q, k_s, v_s, z_k, z_v, b_k, b_v, _ = _norm_case(34)
+    eps = 1e-2
+    _, lse = O.decode_reference_normed(q, k_s, v_s, z_k, z_v, b_k, b_v, [1, 1], eps)
+    k = k_s[1, 0] + b_k[2] @ z_k[1, 0, 2]
+    want = q[1, 2] @ k / math.sqrt(np.mean(k * k) + eps) / math.sqrt(k_s.shape[2])
+    return abs(lse[1, 2] - want) < 1e-12
+
+
+_NORM_PINS = [_check_norm_expansion, _check_norm_unit_rms_is_plain, _check_norm_scale_invariance,
+              _check_norm_single_row]
+
+
+def test_norm_pins_pass_on_the_oracle():
+    assert all(c() for c in _NORM_PINS)
+
+
+@pytest.mark.parametrize("mutant", ["no_sqrt", "sum_not_mean", "eps_outside", "dropped_latent"])
+def test_norm_planted_mistakes_are_caught(mutant, monkeypatch):
+    if mutant == "no_sqrt":
+        monkeypatch.setattr(O, "_rms", lambda K, eps: np.mean(K * K, axis=1) + eps)
+    elif mutant == "sum_not_mean":
+        monkeypatch.setattr(O, "_rms", lambda K, eps: np.sqrt(np.sum(K * K, axis=1) + eps))
+    elif mutant == "eps_outside":
+        monkeypatch.setattr(O, "_rms", lambda K, eps: np.sqrt(np.mean(K * K, axis=1)) + eps)
+    elif mutant == "dropped_latent":
+        monkeypatch.setattr(O, "reconstruct_head", lambda s, z, b: s)
+    assert not all(c() for c in _NORM_PINS), mutant
