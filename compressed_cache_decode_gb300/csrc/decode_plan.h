@@ -94,12 +94,15 @@ struct DecodePlan {
   const void* b_k;
   const void* b_v;
   const int32_t* seq_lens;
+  const float* key_scale;  // [B][max_len][H] reciprocal key RMS (post-projection RMSNorm) or NULL
   float* out;
   float* lse;
 };
 
 // Fills everything but the operand pointers; returns the workspace size.
 lrkv_status decode_make_plan(const lrkv_dims& d, int num_sms, DecodePlan& P, size_t* ws_bytes);
+lrkv_status key_scale_launch(const lrkv_dims& dm, float eps, int n_new, const void* k_s, const void* z_k,
+                             const void* b_k, const int32_t* start_pos, float* key_scale, void* stream);
 lrkv_status step_append_launch(const lrkv_dims& dm, int d_model, const void* x, const void* w_sk,
                                const void* w_sv, const void* u_k, const void* u_v, const int32_t* seq_lens,
                                void* k_s, void* v_s, void* z_k, void* z_v, int num_sms, void* stream);

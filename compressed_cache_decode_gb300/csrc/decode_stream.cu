@@ -601,6 +601,22 @@ __global__ void __launch_bounds__(kThreadsS, 1)
         const uint32_t keep0 = (2 * q4 < nvalid ? 0x0000ffffu : 0u) | (2 * q4 + 1 < nvalid ? 0xffff0000u : 0u);
         const uint32_t keep1 = (2 * q4 + 8 < nvalid ? 0x0000ffffu : 0u) | (2 * q4 + 9 < nvalid ? 0xffff0000u : 0u);
 
+        // post-projection RMSNorm: the joint reciprocal scale of each key
+        // (token g / g+8, head hb + 2 q4 + e) multiplies its summed score;
+        // loaded now, used after the score MMAs
+        float ksc[4] = {1.f, 1.f, 1.f, 1.f};
+        if (P.key_scale) {
+          const int hl = m0 + hb + 2 * q4;
+          const float* kp = P.key_scale + (static_cast<size_t>(pc.b) * P.max_len + t0) * H + hl;
+          if (g < nvalid) {
+            if (hl < H) ksc[0] = __ldg(kp + static_cast<size_t>(g) * H);
+            if (hl + 1 < H) ksc[1] = __ldg(kp + static_cast<size_t>(g) * H + 1);
+          }
+          if (g + 8 < nvalid) {
+            if (hl < H) ksc[2] = __ldg(kp + static_cast<size_t>(g + 8) * H);
+            if (hl + 1 < H) ksc[3] = __ldg(kp + static_cast<size_t>(g + 8) * H + 1);
+          }
+        }
         // scores S^T (rows = tokens g / g+8, columns = heads hb + 2 q4 + e),
         // four independent accumulation chains
         float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
@@ -643,7 +659,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
         float sc[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const float t = ((sa[u] + sb[u]) + (la[u] + lb[u])) * P.scale_log2;
+          const float t = ((sa[u] + sb[u]) + (la[u] + lb[u])) * P.scale_log2 * ksc[u];
           sc[u] = (u < 2 ? v0 : v1) ? t : -INFINITY;
         }
         float mx[2] = {fmaxf(sc[0], sc[2]), fmaxf(sc[1], sc[3])};

@@ -78,7 +78,8 @@ namespace {
 lrkv_status decode_common(const lrkv_dims* dims, const void* q, const void* k_s, const void* v_s,
                           const void* z_k, const void* z_v, const void* b_k, const void* b_v,
                           const int32_t* seq_lens, float* out, float* lse, void* ws, size_t ws_bytes,
-                          lrkv_stream_t stream, void* ev_begin, void* ev_end) {
+                          lrkv_stream_t stream, void* ev_begin, void* ev_end,
+                          const float* key_scale = nullptr) {
   lrkv_status st = check_decode_dims(dims);
   if (st != LRKV_OK) return st;
   if (!q || !k_s || !v_s || !seq_lens || !out) return LRKV_ERR_INVALID_ARG;
@@ -93,9 +94,12 @@ lrkv_status decode_common(const lrkv_dims* dims, const void* q, const void* k_s,
   size_t need = 0;
   if ((st = lrkv::decode_make_plan(*dims, sms, P, &need)) != LRKV_OK) return st;
   if (ws_bytes < need) return LRKV_ERR_WORKSPACE;
+  // post-projection RMSNorm: the streaming scan applies the key scales
+  if (key_scale && !P.stream) return LRKV_ERR_UNSUPPORTED;
   lrkv::decode_bind_workspace(P, ws);
   P.q = q; P.k_s = k_s; P.v_s = v_s; P.z_k = z_k; P.z_v = z_v; P.b_k = b_k; P.b_v = b_v;
   P.seq_lens = seq_lens; P.out = out; P.lse = lse;
+  P.key_scale = key_scale;
   return lrkv::decode_launch(P, stream, ev_begin, ev_end);
 }
 
@@ -119,6 +123,28 @@ lrkv_status lrkv_decode_profiled(const lrkv_dims* dims, const void* q, const voi
   if (!ev_split_begin || !ev_split_end) return LRKV_ERR_INVALID_ARG;
   return decode_common(dims, q, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens, out, lse, ws, ws_bytes, stream,
                        ev_split_begin, ev_split_end);
+}
+
+lrkv_status lrkv_key_scales(const lrkv_dims* dims, float eps, int n_new, const void* k_s, const void* z_k,
+                            const void* b_k, const int32_t* start_pos, float* key_scale, lrkv_stream_t stream) {
+  lrkv_status st = check_decode_dims(dims);
+  if (st != LRKV_OK) return st;
+  if (dims->dtype != LRKV_BF16 || dims->rank < 1 || dims->head_dim > 256) return LRKV_ERR_UNSUPPORTED;
+  if (!(eps >= 0.f) || n_new < 1) return LRKV_ERR_INVALID_ARG;
+  if (!k_s || !z_k || !b_k || !start_pos || !key_scale) return LRKV_ERR_INVALID_ARG;
+  if ((static_cast<long long>(dims->head_dim) * dims->rank + 64ll * (dims->rank + dims->head_dim)) * 4 > 200 * 1024)
+    return LRKV_ERR_UNSUPPORTED;
+  return lrkv::key_scale_launch(*dims, eps, n_new, k_s, z_k, b_k, start_pos, key_scale, stream);
+}
+
+lrkv_status lrkv_decode_normed(const lrkv_dims* dims, const void* q, const void* k_s, const void* v_s,
+                               const void* z_k, const void* z_v, const void* b_k, const void* b_v,
+                               const float* key_scale, const int32_t* seq_lens, float* out, float* lse, void* ws,
+                               size_t ws_bytes, lrkv_stream_t stream) {
+  if (!key_scale || !dims) return LRKV_ERR_INVALID_ARG;
+  if (dims->dtype != LRKV_BF16 || dims->rank < 1) return LRKV_ERR_UNSUPPORTED;
+  return decode_common(dims, q, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens, out, lse, ws, ws_bytes, stream, nullptr,
+                       nullptr, key_scale);
 }
 
 lrkv_status lrkv_decode_step(const lrkv_dims* dims, int d_model, const void* x, const void* w_sk,

@@ -39,6 +39,8 @@ EXPORTED = (
     "lrkv_append",
     "lrkv_prefill",
     "lrkv_decode_step",
+    "lrkv_key_scales",
+    "lrkv_decode_normed",
     "lrkv_read_device_status",
 )
 
@@ -95,6 +97,10 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.lrkv_append.restype = ctypes.c_int
     lib.lrkv_append.argtypes = [dims_p, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, vp, i32p, vp, vp, vp,
                                 vp, vp, sz, vp]
+    lib.lrkv_key_scales.restype = ctypes.c_int
+    lib.lrkv_key_scales.argtypes = [dims_p, ctypes.c_float, ctypes.c_int, vp, vp, vp, i32p, vp, vp]
+    lib.lrkv_decode_normed.restype = ctypes.c_int
+    lib.lrkv_decode_normed.argtypes = [dims_p, vp, vp, vp, vp, vp, vp, vp, vp, i32p, vp, vp, vp, sz, vp]
     lib.lrkv_decode_step.restype = ctypes.c_int
     lib.lrkv_decode_step.argtypes = [dims_p, ctypes.c_int, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                      i32p, vp, vp, vp, sz, vp]
@@ -247,6 +253,45 @@ def append(x: torch.Tensor, w_sk: torch.Tensor, w_sv: torch.Tensor, u_k: torch.T
     if st != LRKV_OK:
         raise LRKVError(st, "lrkv_append")
     return lrkv_read_device_status(ws, stream)
+
+
+def key_scales(k_s: torch.Tensor, z_k: torch.Tensor, b_k: torch.Tensor, start_pos: torch.Tensor,
+               n_new: int, key_scale: torch.Tensor, eps: float = 1e-6, stream=None) -> None:
+    """Reciprocal key RMS (post-projection RMSNorm) of the rows
+    [start_pos[b], start_pos[b] + n_new) into key_scale [B, max_len, H] (fp32)."""
+    B, L, dh = k_s.shape
+    H, r = z_k.shape[2], z_k.shape[3]
+    dims = make_dims(B, H, dh, r, L, k_s.dtype)
+    st = int(load().lrkv_key_scales(ctypes.byref(dims), float(eps), int(n_new), _ptr(k_s), _ptr(z_k), _ptr(b_k),
+                                    _ptr(start_pos), _ptr(key_scale), _stream_handle(stream)))
+    if st != LRKV_OK:
+        raise LRKVError(st, "lrkv_key_scales")
+
+
+def lrkv_decode_normed(dims: lrkv_dims, q, k_s, v_s, z_k, z_v, b_k, b_v, key_scale, seq_lens, out, lse,
+                       ws, ws_bytes: int, stream=None) -> int:
+    """Direct call of the normalised-key decode entry point; returns its status."""
+    return int(load().lrkv_decode_normed(ctypes.byref(dims), _ptr(q), _ptr(k_s), _ptr(v_s), _ptr(z_k),
+                                         _ptr(z_v), _ptr(b_k), _ptr(b_v), _ptr(key_scale), _ptr(seq_lens),
+                                         _ptr(out), _ptr(lse), _ptr(ws), ws_bytes, _stream_handle(stream)))
+
+
+def decode_normed(q, k_s, v_s, z_k, z_v, b_k, b_v, key_scale, seq_lens, scale: float = 0.0, out=None,
+                  lse=None, ws=None, stream=None):
+    """decode with the keys' post-projection RMSNorm scales applied to the scores."""
+    B, H, dh = q.shape
+    dims = make_dims(B, H, dh, z_k.shape[-1], k_s.shape[1], q.dtype, scale)
+    if out is None:
+        out = torch.empty((B, H, dh), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = decode_workspace(dims, q.device)
+    st = lrkv_decode_normed(dims, q, k_s, v_s, z_k, z_v, b_k, b_v, key_scale, seq_lens, out, lse, ws,
+                            ws.numel(), stream)
+    if st != LRKV_OK:
+        raise LRKVError(st, "lrkv_decode_normed")
+    return out, lse
 
 
 def lrkv_decode_step(dims: lrkv_dims, d_model: int, x, w_sk, w_sv, u_k, u_v, q, k_s, v_s, z_k, z_v,

@@ -1,0 +1,75 @@
+"""Post-projection RMSNorm of the keys (review §8, "Post-projection
+normalization has a cache cost") against the fp64 oracle: the cached joint
+reciprocal scales (fp32; relative error from the fp32 rebuild of each key) and
+the decode that multiplies each summed score by its key's scale (the bf16
+decode bar)."""
+import numpy as np
+import pytest
+import torch
+
+from _lib_util import assert_decode_close, ensure_built
+from compressed_cache_decode_gb300 import inputs, lrkv
+from oracle import lrkv_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    ensure_built()
+    lrkv.load()
+
+
+@pytest.mark.parametrize("shape", [
+    # B, H, d_h, r, max_len, start positions, n_new, eps
+    (2, 4, 64, 16, 200, [0, 37], 150, 1e-6),
+    (1, 8, 128, 64, 130, [0], 130, 1e-3),     # two 64-token blocks + a ragged one
+    (3, 16, 64, 28, 96, [5, 90, 0], 20, 0.0),  # rows past max_len skipped
+])
+def test_key_scales_match_oracle(shape):
+    B, H, dh, r, Lm, start, n_new, eps = shape
+    case = inputs.random_decode_case(seed=B * 11 + dh, batch=B, heads=H, head_dim=dh, rank=r, max_len=Lm,
+                                     dtype="bf16")
+    dev = {k: v.cuda() for k, v in case.items()}
+    ks = torch.full((B, Lm, H), -1.0, dtype=torch.float32, device="cuda")
+    sp = torch.tensor(start, dtype=torch.int32, device="cuda")
+    lrkv.key_scales(dev["k_s"], dev["z_k"], dev["b_k"], sp, n_new, ks, eps=eps)
+    torch.cuda.synchronize()
+    got = ks.cpu().numpy()
+    ref = O.key_rms_scales(case["k_s"], case["z_k"], case["b_k"], eps)
+    for b in range(B):
+        lo, hi = max(start[b], 0), min(start[b] + n_new, Lm)
+        rel = np.abs(got[b, lo:hi] - ref[b, lo:hi]) / np.abs(ref[b, lo:hi])
+        assert rel.max() <= 2e-5, f"seq {b}: worst relative error {rel.max():.2e}"
+        assert np.all(got[b, :lo] == -1.0) and np.all(got[b, hi:] == -1.0), f"seq {b}: rows outside written"
+
+
+@pytest.mark.parametrize("shape", [
+    # B, H, d_h, r, max_len, lengths
+    (3, 4, 64, 16, 200, [57, 120, 1]),
+    (2, 8, 128, 32, 300, [300, 129]),
+    (4, 16, 64, 28, 4096, [4096, 3000, 17, 0]),
+])
+def test_decode_normed_matches_oracle(shape):
+    B, H, dh, r, Lm, lens = shape
+    eps = 1e-6
+    case = inputs.random_decode_case(seed=B * 13 + Lm, batch=B, heads=H, head_dim=dh, rank=r, max_len=Lm,
+                                     dtype="bf16", lens=lens)
+    dev = {k: v.cuda() for k, v in case.items()}
+    ks = torch.empty((B, Lm, H), dtype=torch.float32, device="cuda")
+    lrkv.key_scales(dev["k_s"], dev["z_k"], dev["b_k"], torch.zeros(B, dtype=torch.int32, device="cuda"), Lm, ks,
+                    eps=eps)
+    out, lse = lrkv.decode_normed(dev["q"], dev["k_s"], dev["v_s"], dev["z_k"], dev["z_v"], dev["b_k"], dev["b_v"],
+                                  ks, dev["seq_lens"])
+    torch.cuda.synchronize()
+    ref_o, ref_l = O.decode_reference_normed(case["q"], case["k_s"], case["v_s"], case["z_k"], case["z_v"],
+                                             case["b_k"], case["b_v"], case["seq_lens"], eps)
+    assert_decode_close(out.cpu().numpy(), lse.cpu().numpy(), ref_o, ref_l, "bf16",
+                        what=f"normed decode {shape}")
+    # the normalisation matters here: the plain decode is far from the normed reference
+    plain, _ = lrkv.decode(dev["q"], dev["k_s"], dev["v_s"], dev["z_k"], dev["z_v"], dev["b_k"], dev["b_v"],
+                           dev["seq_lens"])
+    live = np.asarray(lens) > 1
+    assert np.abs(plain.cpu().numpy()[live] - ref_o[live]).max() > 1e-2
