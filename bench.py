@@ -603,6 +603,49 @@ def main():
                     "algorithmic_bytes": total_bytes + w_bytes + xs.numel() * 2 + rows_bytes,
                     "gbs": job_gbs(total_bytes + w_bytes + xs.numel() * 2 + rows_bytes, world, f_ms)}
 
+    # decode with post-projection RMSNorm of the keys: the cached reciprocal
+    # key scales (one fp32 per head and token) multiply the summed scores
+    normed_leg = None
+    if not a.no_graph:
+        kscales = []
+        for x in reps:
+            t = torch.empty((w.batch, w.max_len, w.heads), dtype=torch.float32, device=dev)
+            lrkv.key_scales(x["k_s"], x["z_k"], x["b_k"], torch.zeros(w.batch, dtype=torch.int32, device=dev),
+                            w.max_len, t, eps=1e-6)
+            kscales.append(t)
+        torch.cuda.synchronize()
+
+        def nstep(i, s=None):
+            x = reps[i % n_rep]
+            st = lrkv.lrkv_decode_normed(dims, x["q"], x["k_s"], x["v_s"], x["z_k"], x["z_v"], x["b_k"], x["b_v"],
+                                         kscales[i % n_rep], x["seq_lens"], out, lse, ws, ws.numel(), s or stream)
+            if st != lrkv.LRKV_OK:
+                raise lrkv.LRKVError(st, "lrkv_decode_normed")
+
+        with torch.cuda.stream(stream):
+            for i in range(W):
+                nstep(i)
+        torch.cuda.synchronize()
+        ng = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(ng, stream=stream, capture_error_mode="thread_local"):
+            for i in range(K):
+                nstep(i, torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        ng.replay()
+        torch.cuda.synchronize()
+        n0, n1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            n0.record(stream)
+            ng.replay()
+            n1.record(stream)
+        torch.cuda.synchronize()
+        n_ms = max_over_ranks(n0.elapsed_time(n1) / K, world, dev)
+        scale_bytes = int(case["seq_lens"].long().sum()) * w.heads * 4
+        normed_leg = {"ms_per_step": n_ms, "decode_ms_per_step": ms_step,
+                      "algorithmic_bytes": total_bytes + scale_bytes,
+                      "gbs": job_gbs(total_bytes + scale_bytes, world, n_ms),
+                      "key_scale_bytes": scale_bytes}
+
     prefill = None
     if not a.no_prefill:
         prefill = prefill_leg(dev)
@@ -642,6 +685,7 @@ def main():
             "gpu_launches": 2 * K,
             "clocks": clk.summary(),
             "decode_step": step_leg,
+            "decode_normed": normed_leg,
             "prefill": prefill,
         }
         print(json.dumps(res), flush=True)
