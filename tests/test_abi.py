@@ -105,3 +105,27 @@ def test_workspace_size_checks_arguments(lib):
     assert lib.lrkv_decode_workspace_size(ctypes.byref(d), None) == lrkv.LRKV_ERR_INVALID_ARG
     bad = lrkv.make_dims(1, 16, 60, 28, 64, "bf16")
     assert lib.lrkv_decode_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == lrkv.LRKV_ERR_UNSUPPORTED
+
+
+def test_new_entries_reject_bad_arguments_without_gpu(lib):
+    """The decode step, the key scales and the normalised decode check dtype,
+    rank and pointers on the host before any launch."""
+    f32 = lrkv.make_dims(2, 4, 64, 16, 128, None)
+    f32.dtype = lrkv.LRKV_F32
+    bf = lrkv.make_dims(2, 4, 64, 16, 128, None)
+    bf.dtype = lrkv.LRKV_BF16
+    fake = ctypes.c_void_p(4096)  # aligned, never dereferenced: the checks fail first
+    args_scales = (0.0, 8, fake, fake, fake, fake, fake, None)
+    assert lib.lrkv_key_scales(ctypes.byref(f32), *args_scales) == lrkv.LRKV_ERR_UNSUPPORTED
+    assert lib.lrkv_key_scales(ctypes.byref(bf), -1.0, 8, fake, fake, fake, fake, fake, None) == \
+        lrkv.LRKV_ERR_INVALID_ARG
+    assert lib.lrkv_key_scales(ctypes.byref(bf), 0.0, 8, None, fake, fake, fake, fake, None) == \
+        lrkv.LRKV_ERR_INVALID_ARG
+    normed = (fake,) * 7 + (fake, fake, fake, fake, fake, 1 << 20, None)
+    assert lib.lrkv_decode_normed(ctypes.byref(f32), *normed) == lrkv.LRKV_ERR_UNSUPPORTED
+    assert lib.lrkv_decode_normed(ctypes.byref(bf), *((fake,) * 7), None, fake, fake, fake, fake, 1 << 20,
+                                  None) == lrkv.LRKV_ERR_INVALID_ARG
+    ptrs = (fake,) * 15   # x, the weights, q, the cache, the bases, seq_lens, out, lse
+    assert lib.lrkv_decode_step(ctypes.byref(f32), 64, *ptrs, fake, 1 << 20, None) == lrkv.LRKV_ERR_UNSUPPORTED
+    assert lib.lrkv_decode_step(ctypes.byref(bf), 60, *ptrs, fake, 1 << 20, None) == \
+        lrkv.LRKV_ERR_UNSUPPORTED       # d_model not a multiple of 8
