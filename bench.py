@@ -306,8 +306,19 @@ def prefill_leg(dev, iters=10):
                                out, lse, ws, 16)
         assert st == lrkv.LRKV_OK
 
+    # post-projection RMSNorm of the keys: the scales of every appended row
+    # (computed once after the append; the timed call multiplies them in)
+    kscale = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+
+    def pre_normed():
+        st = lrkv.lrkv_prefill_normed(dims, T, d["q"], k_s, v_s, z_k, z_v, d["b_k"], d["b_v"], kscale,
+                                      d["seq_lens"], out, lse, ws, 16)
+        assert st == lrkv.LRKV_OK
+
     res = {}
-    for name, fn in (("append", app), ("prefill", pre)):
+    for name, fn in (("append", app), ("prefill", pre), ("prefill_normed", pre_normed)):
+        if name == "prefill_normed":
+            lrkv.key_scales(k_s, z_k, d["b_k"], d["start_pos"], T, kscale, eps=1e-6)
         for _ in range(3):
             fn()
         ts = []
@@ -327,6 +338,8 @@ def prefill_leg(dev, iters=10):
                           "algorithmic_flop": attn},
             "append": {"ms": res["append"], "tflops": append / (res["append"] * 1e-3) / 1e12,
                        "algorithmic_flop": append},
+            "attention_normed": {"ms": res["prefill_normed"],
+                                 "tflops": attn / (res["prefill_normed"] * 1e-3) / 1e12},
             "peak_tflops": peak[0], "peak_kind": peak[1],
             "attention_frac": attn / (res["prefill"] * 1e-3) / 1e12 / peak[0],
             "append_frac": append / (res["append"] * 1e-3) / 1e12 / peak[0]}
@@ -609,7 +622,7 @@ def main():
     if not a.no_graph:
         kscales = []
         for x in reps:
-            t = torch.empty((w.batch, w.max_len, w.heads), dtype=torch.float32, device=dev)
+            t = torch.empty((w.batch, w.heads, w.max_len), dtype=torch.float32, device=dev)
             lrkv.key_scales(x["k_s"], x["z_k"], x["b_k"], torch.zeros(w.batch, dtype=torch.int32, device=dev),
                             w.max_len, t, eps=1e-6)
             kscales.append(t)

@@ -94,7 +94,7 @@ struct DecodePlan {
   const void* b_k;
   const void* b_v;
   const int32_t* seq_lens;
-  const float* key_scale;  // [B][max_len][H] reciprocal key RMS (post-projection RMSNorm) or NULL
+  const float* key_scale;  // [B][H][max_len] reciprocal key RMS (post-projection RMSNorm) or NULL
   float* out;
   float* lse;
 };

@@ -607,14 +607,14 @@ __global__ void __launch_bounds__(kThreadsS, 1)
         float ksc[4] = {1.f, 1.f, 1.f, 1.f};
         if (P.key_scale) {
           const int hl = m0 + hb + 2 * q4;
-          const float* kp = P.key_scale + (static_cast<size_t>(pc.b) * P.max_len + t0) * H + hl;
+          const float* kp = P.key_scale + (static_cast<size_t>(pc.b) * H + hl) * P.max_len + t0;
           if (g < nvalid) {
-            if (hl < H) ksc[0] = __ldg(kp + static_cast<size_t>(g) * H);
-            if (hl + 1 < H) ksc[1] = __ldg(kp + static_cast<size_t>(g) * H + 1);
+            if (hl < H) ksc[0] = __ldg(kp + g);
+            if (hl + 1 < H) ksc[1] = __ldg(kp + P.max_len + g);
           }
           if (g + 8 < nvalid) {
-            if (hl < H) ksc[2] = __ldg(kp + static_cast<size_t>(g + 8) * H);
-            if (hl + 1 < H) ksc[3] = __ldg(kp + static_cast<size_t>(g + 8) * H + 1);
+            if (hl < H) ksc[2] = __ldg(kp + g + 8);
+            if (hl + 1 < H) ksc[3] = __ldg(kp + P.max_len + g + 8);
           }
         }
         // scores S^T (rows = tokens g / g+8, columns = heads hb + 2 q4 + e),

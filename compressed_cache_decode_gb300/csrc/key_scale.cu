@@ -31,7 +31,7 @@ struct KeyScaleParams {
   const __nv_bfloat16* z_k;   // [B][max_len][H][r]
   const __nv_bfloat16* b_k;   // [H][dh][r]
   const int32_t* start_pos;   // [B]
-  float* key_scale;           // [B][max_len][H]
+  float* key_scale;           // [B][H][max_len]
 };
 
 }  // namespace
@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(kKsThreads) lrkv_key_scale_kernel(const KeySca
   ss += __shfl_xor_sync(0xffffffffu, ss, 2);
   const int pos = start + t_first + t;
   if (part == 0 && t_first + t < p.n_new && pos >= 0 && pos < p.max_len)
-    p.key_scale[(static_cast<size_t>(b) * p.max_len + pos) * p.H + h] = 1.f / sqrtf(ss / dh + p.eps);
+    p.key_scale[(static_cast<size_t>(b) * p.H + h) * p.max_len + pos] = 1.f / sqrtf(ss / dh + p.eps);
 }
 
 lrkv_status key_scale_launch(const lrkv_dims& dm, float eps, int n_new, const void* k_s, const void* z_k,

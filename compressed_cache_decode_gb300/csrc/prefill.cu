@@ -65,6 +65,7 @@ struct PrefillParams {
   int out_v8;  // out is 32-byte aligned: 256-bit stores
   float scale_log2;
   const int32_t* seq_lens;
+  const float* key_scale;  // [B][H][max_len] reciprocal key RMS, or NULL
   float* out;
   float* lse;
   uint32_t* status;
@@ -217,6 +218,8 @@ __device__ __forceinline__ void st_global_v8(float* dst, const float (&v)[8]) {
 
 }  // namespace
 
+// KS: the scores are multiplied by the keys' cached RMSNorm scales
+template <bool KS>
 __global__ void __launch_bounds__(kThreads, 1)
     lrkv_prefill_kernel(const PrefillParams p, const __grid_constant__ PrefillMaps maps) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -477,10 +480,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = 0; t < it.nkt; ++t) {
         const int Jt = J + t;
         const uint32_t sb = tmem + lane_off + kColS + (Jt & 1) * 128;
+        // post-projection RMSNorm: this half's 64 key scales (lane l loads keys
+        // 2l, 2l+1; every row of the tile shares them), fetched before the wait
+        float ks0 = 1.f, ks1 = 1.f;
+        if (KS) {
+          const int kb = t * kBK + half * 64 + 2 * lane;
+          const float* kp = p.key_scale + (static_cast<size_t>(it.b) * p.H + it.h) * p.max_len;
+          if (kb < p.max_len) ks0 = __ldg(kp + kb);
+          if (kb + 1 < p.max_len) ks1 = __ldg(kp + kb + 1);
+        }
         ok = ok && pwait(&bar_sf[Jt & 1], static_cast<uint32_t>(Jt >> 1) & 1u, fail);
         tc_fence_after();
         uint32_t v[64];
         tmem_ld64_wait(sb + half * 64, v);
+        if (KS) {
+#pragma unroll
+          for (int e = 0; e < 64; e += 2) {
+            v[e] = __float_as_uint(__uint_as_float(v[e]) * __shfl_sync(0xffffffffu, ks0, e >> 1));
+            v[e + 1] = __float_as_uint(__uint_as_float(v[e + 1]) * __shfl_sync(0xffffffffu, ks1, e >> 1));
+          }
+        }
         // keys t*128 + half*64 + c are visible iff c <= lim (causal and length)
         const int lim = min(qpos, it.L - 1) - t * kBK - half * 64;
         if (lim < 63) {
@@ -636,10 +655,10 @@ bool make_map(CUtensorMap* m, const void* base, int n, const uint64_t* dims, con
 
 }  // namespace
 
-extern "C" lrkv_status lrkv_prefill(const lrkv_dims* dims, int q_len, const void* q, const void* k_s,
-                                    const void* v_s, const void* z_k, const void* z_v, const void* b_k,
-                                    const void* b_v, const int32_t* seq_lens, float* out, float* lse, void* ws,
-                                    size_t ws_bytes, lrkv_stream_t stream) {
+static lrkv_status prefill_impl(const lrkv_dims* dims, int q_len, const void* q, const void* k_s,
+                                const void* v_s, const void* z_k, const void* z_v, const void* b_k,
+                                const void* b_v, const float* key_scale, const int32_t* seq_lens, float* out,
+                                float* lse, void* ws, size_t ws_bytes, lrkv_stream_t stream) {
   if (!dims) return LRKV_ERR_INVALID_ARG;
   const lrkv_dims& d = *dims;
   if (d.batch < 1 || d.heads < 1 || d.head_dim < 1 || d.rank < 0 || d.max_len < 1 || q_len < 1)
@@ -690,12 +709,14 @@ extern "C" lrkv_status lrkv_prefill(const lrkv_dims* dims, int q_len, const void
   const float scale = d.scale > 0.f ? d.scale : 1.f / std::sqrt(static_cast<float>(d.head_dim));
   p.scale_log2 = scale * lrkv::kPfLog2e;
   p.seq_lens = seq_lens; p.out = out; p.lse = lse;
+  p.key_scale = key_scale;
+  auto kern = key_scale ? lrkv::lrkv_prefill_kernel<true> : lrkv::lrkv_prefill_kernel<false>;
   p.out_v8 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
   p.status = static_cast<uint32_t*>(ws);
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(ws, 0, 4, s) != cudaSuccess) return LRKV_ERR_CUDA;
-  if (cudaFuncSetAttribute(lrkv::lrkv_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, lrkv::kSmem) !=
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, lrkv::kSmem) !=
       cudaSuccess)
     return LRKV_ERR_CUDA;
   // persistent: one CTA per SM (the kernel deals the (sequence, head, query
@@ -709,6 +730,24 @@ extern "C" lrkv_status lrkv_prefill(const lrkv_dims* dims, int q_len, const void
   const long long items = static_cast<long long>((q_len + lrkv::kBQ - 1) / lrkv::kBQ) * H * B;
   if (items > (1ll << 30)) return LRKV_ERR_UNSUPPORTED;
   const int grid = static_cast<int>(std::min<long long>(nsm, items));
-  lrkv::lrkv_prefill_kernel<<<grid, lrkv::kThreads, lrkv::kSmem, s>>>(p, maps);
+  kern<<<grid, lrkv::kThreads, lrkv::kSmem, s>>>(p, maps);
   return cudaGetLastError() == cudaSuccess ? LRKV_OK : LRKV_ERR_CUDA;
+}
+
+extern "C" lrkv_status lrkv_prefill(const lrkv_dims* dims, int q_len, const void* q, const void* k_s,
+                                    const void* v_s, const void* z_k, const void* z_v, const void* b_k,
+                                    const void* b_v, const int32_t* seq_lens, float* out, float* lse, void* ws,
+                                    size_t ws_bytes, lrkv_stream_t stream) {
+  return prefill_impl(dims, q_len, q, k_s, v_s, z_k, z_v, b_k, b_v, nullptr, seq_lens, out, lse, ws, ws_bytes,
+                      stream);
+}
+
+extern "C" lrkv_status lrkv_prefill_normed(const lrkv_dims* dims, int q_len, const void* q, const void* k_s,
+                                           const void* v_s, const void* z_k, const void* z_v, const void* b_k,
+                                           const void* b_v, const float* key_scale, const int32_t* seq_lens,
+                                           float* out, float* lse, void* ws, size_t ws_bytes,
+                                           lrkv_stream_t stream) {
+  if (!key_scale) return LRKV_ERR_INVALID_ARG;
+  return prefill_impl(dims, q_len, q, k_s, v_s, z_k, z_v, b_k, b_v, key_scale, seq_lens, out, lse, ws, ws_bytes,
+                      stream);
 }

@@ -41,6 +41,7 @@ EXPORTED = (
     "lrkv_decode_step",
     "lrkv_key_scales",
     "lrkv_decode_normed",
+    "lrkv_prefill_normed",
     "lrkv_read_device_status",
 )
 
@@ -107,6 +108,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.lrkv_prefill.restype = ctypes.c_int
     lib.lrkv_prefill.argtypes = [dims_p, ctypes.c_int, vp, vp, vp, vp, vp, vp, vp, i32p, vp, vp, vp, sz,
                                  vp]
+    lib.lrkv_prefill_normed.restype = ctypes.c_int
+    lib.lrkv_prefill_normed.argtypes = [dims_p, ctypes.c_int, vp, vp, vp, vp, vp, vp, vp, vp, i32p, vp, vp,
+                                        vp, sz, vp]
     lib.lrkv_read_device_status.restype = ctypes.c_int
     lib.lrkv_read_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
     if path is None:
@@ -258,7 +262,7 @@ def append(x: torch.Tensor, w_sk: torch.Tensor, w_sv: torch.Tensor, u_k: torch.T
 def key_scales(k_s: torch.Tensor, z_k: torch.Tensor, b_k: torch.Tensor, start_pos: torch.Tensor,
                n_new: int, key_scale: torch.Tensor, eps: float = 1e-6, stream=None) -> None:
     """Reciprocal key RMS (post-projection RMSNorm) of the rows
-    [start_pos[b], start_pos[b] + n_new) into key_scale [B, max_len, H] (fp32)."""
+    [start_pos[b], start_pos[b] + n_new) into key_scale [B, H, max_len] (fp32)."""
     B, L, dh = k_s.shape
     H, r = z_k.shape[2], z_k.shape[3]
     dims = make_dims(B, H, dh, r, L, k_s.dtype)
@@ -340,6 +344,15 @@ def lrkv_prefill(dims: lrkv_dims, q_len: int, q, k_s, v_s, z_k, z_v, b_k, b_v, s
                                    _ptr(out), _ptr(lse), _ptr(ws), ws_bytes, _stream_handle(stream)))
 
 
+def lrkv_prefill_normed(dims: lrkv_dims, q_len: int, q, k_s, v_s, z_k, z_v, b_k, b_v, key_scale, seq_lens,
+                        out, lse, ws, ws_bytes: int, stream=None) -> int:
+    """Direct call of the normalised-key prefill entry point; returns its status."""
+    return int(load().lrkv_prefill_normed(ctypes.byref(dims), q_len, _ptr(q), _ptr(k_s), _ptr(v_s),
+                                          _ptr(z_k), _ptr(z_v), _ptr(b_k), _ptr(b_v), _ptr(key_scale),
+                                          _ptr(seq_lens), _ptr(out), _ptr(lse), _ptr(ws), ws_bytes,
+                                          _stream_handle(stream)))
+
+
 def prefill(q: torch.Tensor, k_s: torch.Tensor, v_s: torch.Tensor, z_k: torch.Tensor,
             z_v: torch.Tensor, b_k: torch.Tensor, b_v: torch.Tensor, seq_lens: torch.Tensor,
             scale: float = 0.0, out: Optional[torch.Tensor] = None,
@@ -358,4 +371,26 @@ def prefill(q: torch.Tensor, k_s: torch.Tensor, v_s: torch.Tensor, z_k: torch.Te
                       stream)
     if st != LRKV_OK:
         raise LRKVError(st, "lrkv_prefill")
+    return out, lse, ws
+
+
+def prefill_normed(q: torch.Tensor, k_s: torch.Tensor, v_s: torch.Tensor, z_k: torch.Tensor,
+                   z_v: torch.Tensor, b_k: torch.Tensor, b_v: torch.Tensor, key_scale: torch.Tensor,
+                   seq_lens: torch.Tensor, scale: float = 0.0, out: Optional[torch.Tensor] = None,
+                   lse: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None, stream=None):
+    """prefill with the keys' post-projection RMSNorm scales (key_scale
+    [B, H, max_len] fp32) applied to the scores; returns (out, lse, status)."""
+    B, Tq, H, dh = q.shape
+    r = z_k.shape[-1]
+    dims = make_dims(B, H, dh, r, k_s.shape[1], q.dtype, scale)
+    if out is None:
+        out = torch.empty((B, Tq, H, dh), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, Tq), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = torch.zeros(16, dtype=torch.uint8, device=q.device)
+    st = lrkv_prefill_normed(dims, Tq, q, k_s, v_s, z_k, z_v, b_k, b_v, key_scale, seq_lens, out, lse, ws,
+                             ws.numel(), stream)
+    if st != LRKV_OK:
+        raise LRKVError(st, "lrkv_prefill_normed")
     return out, lse, ws

@@ -268,18 +268,23 @@ lrkv_status lrkv_decode_step(const lrkv_dims* dims, int d_model, const void* x, 
  * head and token and multiplies the summed score by it; a per-head gain of
  * the norm is folded into q by the caller.
  *
- * lrkv_key_scales writes key_scale[b][t][h] = 1 / n (fp32) for the rows
+ * lrkv_key_scales writes key_scale[b][h][t] = 1 / n (fp32) for the rows
  * t = start_pos[b] .. start_pos[b] + n_new - 1 of every sequence, from the
  * cached k_s, z_k (bf16, as stored) and B^K; rows outside [0, max_len) are
  * skipped.  Call it after appending the rows.
- *   key_scale  [batch][max_len][heads] fp32 (device), caller-allocated
+ *   key_scale  [batch][heads][max_len] fp32 (device), caller-allocated
  * Supported: dtype BF16, rank >= 1, (head_dim*rank + 64*(head_dim+rank))*4
  * <= 200 KB.
  *
  * lrkv_decode_normed is lrkv_decode with every summed score multiplied by
- * key_scale[b][j][h] before the softmax (values are not normalised).
+ * key_scale[b][h][j] before the softmax (values are not normalised).
  * Supported: the shapes on which lrkv_decode streams bf16 (others return
  * LRKV_ERR_UNSUPPORTED).
+ *
+ * lrkv_prefill_normed is lrkv_prefill with the same per-key multiplication
+ * of the summed scores (before the causal mask and the softmax); key_scale
+ * must hold rows [0, seq_lens[b]) of every sequence.  key_scale NULL returns
+ * LRKV_ERR_INVALID_ARG.  Supported: the shapes of lrkv_prefill.
  */
 lrkv_status lrkv_key_scales(const lrkv_dims* dims, float eps, int n_new, const void* k_s, const void* z_k,
                             const void* b_k, const int32_t* start_pos, float* key_scale, lrkv_stream_t stream);
@@ -287,6 +292,10 @@ lrkv_status lrkv_decode_normed(const lrkv_dims* dims, const void* q, const void*
                                const void* z_k, const void* z_v, const void* b_k, const void* b_v,
                                const float* key_scale, const int32_t* seq_lens, float* out, float* lse, void* ws,
                                size_t ws_bytes, lrkv_stream_t stream);
+lrkv_status lrkv_prefill_normed(const lrkv_dims* dims, int q_len, const void* q, const void* k_s,
+                                const void* v_s, const void* z_k, const void* z_v, const void* b_k,
+                                const void* b_v, const float* key_scale, const int32_t* seq_lens, float* out,
+                                float* lse, void* ws, size_t ws_bytes, lrkv_stream_t stream);
 
 /*
  * Read the device status word that the kernels of the last call(s) using

@@ -220,14 +220,16 @@ def decode_reference_normed(q, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens, rms_eps: 
 
 def prefill_reference(q, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens, scale: Optional[float] = None,
                       pairs: Optional[Iterable[Tuple[int, int]]] = None,
-                      rows: Optional[Sequence[int]] = None):
+                      rows: Optional[Sequence[int]] = None, rms_eps: Optional[float] = None):
     """Causal attention of q_len queries per sequence against the factored cache.
 
     q [B, q_len, H, d_h].  Query i of sequence b sits at absolute position
     p_i = seq_lens[b] - q_len + i and sees keys j <= p_i (causal mask of
     review §2; bottom-right alignment).  `rows` restricts the query indices
-    computed.  Returns out [B, q_len, H, d_h] and lse [B, H, q_len]; entries
-    not computed are NaN.
+    computed.  With `rms_eps` given, every rebuilt key row is first divided by
+    its RMS sqrt(mean k^2 + rms_eps) (post-projection RMSNorm of the keys,
+    review §8, as in decode_reference_normed).  Returns out [B, q_len, H, d_h]
+    and lse [B, H, q_len]; entries not computed are NaN.
     """
     q, k_s, v_s, z_k, z_v, b_k, b_v = (_f64(a) for a in (q, k_s, v_s, z_k, z_v, b_k, b_v))
     lens = np.asarray(_f64(seq_lens), dtype=np.int64)
@@ -243,6 +245,8 @@ def prefill_reference(q, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens, scale: Optional
         if L < Tq:
             raise ValueError("prefill needs seq_lens[b] >= q_len (queries are part of the history)")
         K = reconstruct_head(k_s[b, :L], z_k[b, :L, h, :], b_k[h])
+        if rms_eps is not None:
+            K = K / _rms(K, rms_eps)[:, None]
         V = reconstruct_head(v_s[b, :L], z_v[b, :L, h, :], b_v[h])
         for i in qi:
             p = L - Tq + i

@@ -108,8 +108,8 @@ def test_workspace_size_checks_arguments(lib):
 
 
 def test_new_entries_reject_bad_arguments_without_gpu(lib):
-    """The decode step, the key scales and the normalised decode check dtype,
-    rank and pointers on the host before any launch."""
+    """The decode step, the key scales and the normalised decode and prefill
+    check dtype, rank, sizes and pointers on the host before any launch."""
     f32 = lrkv.make_dims(2, 4, 64, 16, 128, None)
     f32.dtype = lrkv.LRKV_F32
     bf = lrkv.make_dims(2, 4, 64, 16, 128, None)
@@ -125,6 +125,12 @@ def test_new_entries_reject_bad_arguments_without_gpu(lib):
     assert lib.lrkv_decode_normed(ctypes.byref(f32), *normed) == lrkv.LRKV_ERR_UNSUPPORTED
     assert lib.lrkv_decode_normed(ctypes.byref(bf), *((fake,) * 7), None, fake, fake, fake, fake, 1 << 20,
                                   None) == lrkv.LRKV_ERR_INVALID_ARG
+    pre = (fake,) * 7     # q, the cache, the bases
+    assert lib.lrkv_prefill_normed(ctypes.byref(bf), 128, *pre, None, fake, fake, fake, fake, 1 << 20,
+                                   None) == lrkv.LRKV_ERR_INVALID_ARG      # no key scales
+    pbf = lrkv.make_dims(1, 2, 128, 64, 128, "bf16")
+    assert lib.lrkv_prefill_normed(ctypes.byref(pbf), 256, *pre, fake, fake, fake, fake, fake, 1 << 20,
+                                   None) == lrkv.LRKV_ERR_UNSUPPORTED      # q_len > max_len
     ptrs = (fake,) * 15   # x, the weights, q, the cache, the bases, seq_lens, out, lse
     assert lib.lrkv_decode_step(ctypes.byref(f32), 64, *ptrs, fake, 1 << 20, None) == lrkv.LRKV_ERR_UNSUPPORTED
     assert lib.lrkv_decode_step(ctypes.byref(bf), 60, *ptrs, fake, 1 << 20, None) == \

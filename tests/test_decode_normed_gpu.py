@@ -1,8 +1,8 @@
 """Post-projection RMSNorm of the keys (review §8, "Post-projection
 normalization has a cache cost") against the fp64 oracle: the cached joint
-reciprocal scales (fp32; relative error from the fp32 rebuild of each key) and
-the decode that multiplies each summed score by its key's scale (the bf16
-decode bar)."""
+reciprocal scales (fp32; relative error from the fp32 rebuild of each key),
+the decode and the causal prefill that multiply each summed score by its
+key's scale (the bf16 decode bar)."""
 import numpy as np
 import pytest
 import torch
@@ -33,11 +33,11 @@ def test_key_scales_match_oracle(shape):
     case = inputs.random_decode_case(seed=B * 11 + dh, batch=B, heads=H, head_dim=dh, rank=r, max_len=Lm,
                                      dtype="bf16")
     dev = {k: v.cuda() for k, v in case.items()}
-    ks = torch.full((B, Lm, H), -1.0, dtype=torch.float32, device="cuda")
+    ks = torch.full((B, H, Lm), -1.0, dtype=torch.float32, device="cuda")
     sp = torch.tensor(start, dtype=torch.int32, device="cuda")
     lrkv.key_scales(dev["k_s"], dev["z_k"], dev["b_k"], sp, n_new, ks, eps=eps)
     torch.cuda.synchronize()
-    got = ks.cpu().numpy()
+    got = ks.cpu().numpy().transpose(0, 2, 1)           # [B, L, H] like the oracle
     ref = O.key_rms_scales(case["k_s"], case["z_k"], case["b_k"], eps)
     for b in range(B):
         lo, hi = max(start[b], 0), min(start[b] + n_new, Lm)
@@ -58,7 +58,7 @@ def test_decode_normed_matches_oracle(shape):
     case = inputs.random_decode_case(seed=B * 13 + Lm, batch=B, heads=H, head_dim=dh, rank=r, max_len=Lm,
                                      dtype="bf16", lens=lens)
     dev = {k: v.cuda() for k, v in case.items()}
-    ks = torch.empty((B, Lm, H), dtype=torch.float32, device="cuda")
+    ks = torch.empty((B, H, Lm), dtype=torch.float32, device="cuda")
     lrkv.key_scales(dev["k_s"], dev["z_k"], dev["b_k"], torch.zeros(B, dtype=torch.int32, device="cuda"), Lm, ks,
                     eps=eps)
     out, lse = lrkv.decode_normed(dev["q"], dev["k_s"], dev["v_s"], dev["z_k"], dev["z_v"], dev["b_k"], dev["b_v"],
@@ -73,3 +73,48 @@ def test_decode_normed_matches_oracle(shape):
                            dev["seq_lens"])
     live = np.asarray(lens) > 1
     assert np.abs(plain.cpu().numpy()[live] - ref_o[live]).max() > 1e-2
+
+
+@pytest.mark.parametrize("shape", [
+    # B, q_len, H, L per sequence, max_len
+    (1, 128, 2, [128], 128),
+    (2, 200, 3, [200, 450], 512),        # partial query tile, history before the queries
+    (2, 512, 40, [512, 700], 768),       # more items than SMs: several per persistent CTA
+])
+def test_prefill_normed_matches_oracle(shape):
+    B, Tq, H, lens, Lm = shape
+    eps = 1e-6
+    case = inputs.random_prefill_case(seed=B * 7 + Tq, batch=B, q_len=Tq, heads=H, head_dim=128, rank=64,
+                                      max_len=Lm, lens=lens)
+    dev = {k: v.cuda() for k, v in case.items()}
+    ks = torch.empty((B, H, Lm), dtype=torch.float32, device="cuda")
+    lrkv.key_scales(dev["k_s"], dev["z_k"], dev["b_k"], torch.zeros(B, dtype=torch.int32, device="cuda"), Lm, ks,
+                    eps=eps)
+    for b, L in enumerate(lens):
+        ks[b, :, L:] = float("nan")      # scales past the history are never used
+    out, lse, ws = lrkv.prefill_normed(dev["q"], dev["k_s"], dev["v_s"], dev["z_k"], dev["z_v"], dev["b_k"],
+                                       dev["b_v"], ks, dev["seq_lens"])
+    torch.cuda.synchronize()
+    assert lrkv.lrkv_read_device_status(ws) == lrkv.LRKV_OK
+    ref_o, ref_l = O.prefill_reference(case["q"], case["k_s"], case["v_s"], case["z_k"], case["z_v"],
+                                       case["b_k"], case["b_v"], case["seq_lens"], rms_eps=eps)
+    o, l_ = out.cpu().numpy(), lse.cpu().numpy()
+    assert_decode_close(o.reshape(-1, o.shape[-1]), l_.transpose(0, 2, 1).reshape(-1),
+                        ref_o.reshape(-1, ref_o.shape[-1]), ref_l.transpose(0, 2, 1).reshape(-1), "bf16",
+                        what=f"normed prefill {shape}")
+    plain, _, _ = lrkv.prefill(dev["q"], dev["k_s"], dev["v_s"], dev["z_k"], dev["z_v"], dev["b_k"], dev["b_v"],
+                               dev["seq_lens"])
+    assert np.abs(plain.cpu().numpy()[:, 1:] - ref_o[:, 1:]).max() > 1e-2
+
+
+def test_prefill_normed_needs_scales():
+    B, Tq, H, Lm = 1, 128, 1, 128
+    case = inputs.random_prefill_case(seed=3, batch=B, q_len=Tq, heads=H, head_dim=128, rank=64, max_len=Lm,
+                                      lens=[128])
+    dev = {k: v.cuda() for k, v in case.items()}
+    dims = lrkv.make_dims(B, H, 128, 64, Lm, torch.bfloat16)
+    out = torch.empty((B, Tq, H, 128), dtype=torch.float32, device="cuda")
+    ws = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    st = lrkv.lrkv_prefill_normed(dims, Tq, dev["q"], dev["k_s"], dev["v_s"], dev["z_k"], dev["z_v"],
+                                  dev["b_k"], dev["b_v"], None, dev["seq_lens"], out, None, ws, 16)
+    assert st == lrkv.LRKV_ERR_INVALID_ARG

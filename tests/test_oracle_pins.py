@@ -493,8 +493,28 @@ def _check_norm_single_row():
     return abs(lse[1, 2] - want) < 1e-12
 
 
+def _check_norm_prefill_rows_are_decodes():
+    """Normalised causal prefill: query i (absolute position p_i) gives the
+    normalised decode of the same query over the first p_i + 1 rows; the rows
+    at the end of the history are normalised by their own key only."""
+    q, k_s, v_s, z_k, z_v, b_k, b_v, lens = _norm_case(35)
+    rng = np.random.default_rng(36)
+    B, H, dh = q.shape
+    Tq = 4
+    qp = _rand(rng, B, Tq, H, dh)
+    eps = 1e-3
+    out, lse = O.prefill_reference(qp, k_s, v_s, z_k, z_v, b_k, b_v, lens, rms_eps=eps)
+    ok = True
+    for i in range(Tq):
+        pos = [L - Tq + i + 1 for L in lens]
+        o, l = O.decode_reference_normed(qp[:, i], k_s, v_s, z_k, z_v, b_k, b_v, pos, eps)
+        ok = ok and np.allclose(out[:, i], o, rtol=1e-10, atol=1e-12) and np.allclose(lse[:, :, i], l)
+    plain, _ = O.prefill_reference(qp, k_s, v_s, z_k, z_v, b_k, b_v, lens)
+    return ok and not np.allclose(plain, out)
+
+
 _NORM_PINS = [_check_norm_expansion, _check_norm_unit_rms_is_plain, _check_norm_scale_invariance,
-              _check_norm_single_row]
+              _check_norm_single_row, _check_norm_prefill_rows_are_decodes]
 
 
 def test_norm_pins_pass_on_the_oracle():
