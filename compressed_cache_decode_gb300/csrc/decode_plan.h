@@ -55,8 +55,9 @@ struct DecodePlan {
   // bf16 streaming kernel: grid (range CTAs, row tiles of 16 heads); the 8
   // warps of a CTA form 4 pairs, pair p takes every 4th 16-token tile of the
   // CTA's range (tile i in stage i % stages) and each warp of the pair 8 of
-  // the 16 heads; the pairs merge on chip at the end of each (sequence,
-  // range) piece.  `ngw` partials per piece (1 here).
+  // the 16 heads; at the end of each (sequence, range) piece every pair
+  // writes its own partial.  `ngw` partials per piece (4 here, 1 for the
+  // tile-synchronous kernel).
   int stream;        // 1: bf16 streaming kernel, 0: tile-synchronous kernel
   int nthreads;      // block size of the scan kernel
   int mt;            // 16-head row tiles (grid.y of the streaming kernel)
@@ -67,7 +68,6 @@ struct DecodePlan {
   int nsb;           // segments per row tile (16 / hs)
   int zt_bytes;      // shared bytes of one latent tile (z_k or z_v) of a row tile
   int kst;           // 16-wide steps over the latents of 8 heads (r / 2)
-  int cm_stride;     // floats per head row of the on-chip merge buffer
   int pfw;           // tiles a CTA keeps prefetched into L2 beyond its ring
   int after_append;  // 1: the launch before writes cache rows: the scan waits for it before its first copy
   int bk_dsplit;     // head-dim parts of the in-kernel q B^K (threads per output group)

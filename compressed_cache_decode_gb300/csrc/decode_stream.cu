@@ -64,6 +64,11 @@ __device__ __forceinline__ void named_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Arrive at named barrier `id` (of `nthreads` threads) without waiting.
+__device__ __forceinline__ void named_arrive(int id, int nthreads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // Pieces of this CTA's token range: (sequence b, rows [t_beg, t_end)).
 struct Piece {
   int b, t_beg, t_end, ntiles;
@@ -330,7 +335,6 @@ __global__ void __launch_bounds__(kThreadsS, 1)
   int* zo = reinterpret_cast<int*>(smem + 320);       // [2][32] latent step offsets
   int* pre = reinterpret_cast<int*>(smem + P.off_prefix);
   uint4* pf = reinterpret_cast<uint4*>(smem + P.off_pf);    // private-score B fragments
-  float* mbuf = reinterpret_cast<float*>(smem + P.off_pf);  // merge buffer (same region)
 
   // ---- 1. barriers, sequence starts (clamped lengths) ----------------------
   {
@@ -508,7 +512,12 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     const bool dry = kp < 0;
     if (!dry) {
     // ---- piece set-up: p and q of the row tile --------------------------------
-    named_sync(1, kThreadsS);  // the previous piece's merge is done with the buffer
+    // The first piece's set-up is built by the warps other than the warm-up
+    // warp (which may still be in its pass); they signal it on barrier 3.
+    const bool split = kp == 0 && P.bk_warps < kWarps;
+    const int nset = split ? kThreadsS - 32 : kThreadsS;  // threads that build the set-up
+    if (!(split && warm))
+      named_sync(1, nset);  // the p rows are written; the previous piece is done with the buffers
     const int buf = kp & 1;
     if (tid == 0 && kp >= 1) {
       Piece nx = pc;
@@ -556,7 +565,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       // (j = 16 (h2 kst + kk) + 2 (L & 3)) of head 8 h2 + (L >> 2).
       const float* ps = reinterpret_cast<const float*>(pqb + 16 * dh * 2);
       const int nent = 2 * P.kst * 32;
-      for (int e = tid; e < nent; e += kThreadsS) {
+      for (int e = tid; e < (tid < nset ? nent : 0); e += nset) {
         const int k = e >> 5, L = e & 31;
         const int hl = 8 * (k >= P.kst ? 1 : 0) + (L >> 2);
         const int j = 16 * k + 2 * (L & 3);
@@ -572,7 +581,14 @@ __global__ void __launch_bounds__(kThreadsS, 1)
                            pack_bf16(lo[2], lo[3]));
       }
     }
-    named_sync(1, kThreadsS);  // fragments ready
+    if (!split) {
+      named_sync(1, kThreadsS);  // fragments ready
+    } else if (!warm) {
+      named_sync(1, nset);       // fragments ready (the builders)
+      named_arrive(3, kThreadsS);
+    } else {
+      named_sync(3, kThreadsS);  // fragments ready (the warm-up warp)
+    }
     }
 
     // the ring's later tiles start streaming into L2 (issued by the last warp,
@@ -764,81 +780,45 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       lc[1] += __shfl_xor_sync(0xffffffffu, lc[1], o);
     }
 
-    // ---- merge the 4 pairs' states, two pairs per round ----------------------
-    // the warps of the round's pairs scatter their useful state into
-    // cm[pair][head][2 + dh + r] = (m, l, O_s, O_z); thread (head tid / 16,
-    // columns tid % 16 + 16 k) folds them into a running (M, l, row) and
-    // finally writes the piece's partial row (coalesced)
-    {
-      constexpr int KC = DHT + (2 * MZA + 15) / 16;  // columns per thread
-      const int hm = tid >> 4, t16 = tid & 15;
-      float Mr = -INFINITY, lr = 0.f, vr[KC];
-#pragma unroll
-      for (int k = 0; k < KC; ++k) vr[k] = 0.f;
-      if (kp == 0) {
-        // first write to the workspace: the launch before may still read it
-        pdl_wait();
-        if (blockIdx.x == 0 && blockIdx.y == 0) {
-          for (int b = tid; b <= B; b += blockDim.x) P.prefix[b] = pre[b];
-          if (tid == 0) { P.meta[0] = N; P.meta[1] = G; }
-        }
+    // ---- this pair's state is one partial of the piece: (m, l) per head and
+    // the unnormalised O_s and O_z rows, written straight from the
+    // accumulators; the combine kernel merges the pairs' partials
+    if (kp == 0) {
+      // first write to the workspace: the launch before may still read it
+      pdl_wait();
+      if (blockIdx.x == 0 && blockIdx.y == 0) {
+        for (int b = tid; b <= B; b += blockDim.x) P.prefix[b] = pre[b];
+        if (tid == 0) { P.meta[0] = N; P.meta[1] = G; }
       }
-      for (int p0 = 0; p0 < kPairs; p0 += 2) {
-        named_sync(1, kThreadsS);  // tiles (first round) or the previous round's reads are done
-        if ((pair >> 1) == (p0 >> 1)) {
-          float* cmw = mbuf + static_cast<size_t>(pair - p0) * 16 * P.cm_stride;
+    }
+    {
+      const size_t slot = static_cast<size_t>(pc.b + c) * kPairs + pair;
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int hl = hb + 2 * q4 + e;
-            float* row = cmw + hl * P.cm_stride;
-            if (g == 0) { row[0] = mc[e]; row[1] = lc[e]; }
+      for (int e = 0; e < 2; ++e) {
+        const int hl = hb + 2 * q4 + e, h = m0 + hl;
+        if (h < H) {
+          if (g == 0) {
+            float* pml = P.part_ml + (slot * H + h) * 2;
+            pml[0] = mc[e];
+            pml[1] = lc[e];
+          }
+          float* o = P.part_acc + (slot * H + h) * (dh + r);
 #pragma unroll
-            for (int n = 0; n < DHT; ++n) {
-              row[2 + 16 * n + g] = acc_v[n][e];
-              row[2 + 16 * n + g + 8] = acc_v[n][2 + e];
-            }
-            if (MZMAX > 0) {
-              // row j (this half) holds latent column j - (hl - hb) r of head hl
+          for (int n = 0; n < DHT; ++n) {
+            o[16 * n + g] = acc_v[n][e];
+            o[16 * n + g + 8] = acc_v[n][2 + e];
+          }
+          if (MZMAX > 0) {
+            // row j (this half) holds latent column j - (hl - hb) r of head hl
 #pragma unroll
-              for (int n = 0; n < MZA; ++n) {
-                if (n < P.kst) {
-                  const int ca = 16 * n + g - (hl - hb) * r, cb = ca + 8;
-                  if (ca >= 0 && ca < r) row[2 + dh + ca] = acc_z[n][e];
-                  if (cb >= 0 && cb < r) row[2 + dh + cb] = acc_z[n][2 + e];
-                }
+            for (int n = 0; n < MZA; ++n) {
+              if (n < P.kst) {
+                const int ca = 16 * n + g - (hl - hb) * r, cb = ca + 8;
+                if (ca >= 0 && ca < r) o[dh + ca] = acc_z[n][e];
+                if (cb >= 0 && cb < r) o[dh + cb] = acc_z[n][2 + e];
               }
             }
           }
-        }
-        named_sync(1, kThreadsS);
-        const float* r0 = mbuf + static_cast<size_t>(hm) * P.cm_stride;
-        const float* r1 = r0 + static_cast<size_t>(16) * P.cm_stride;
-        const float ma = r0[0], mb = r1[0];
-        const float M = fmaxf(Mr, fmaxf(ma, mb));
-        const float f = Mr == -INFINITY ? 0.f : exp2f(Mr - M);
-        const float fa = ma == -INFINITY ? 0.f : exp2f(ma - M);
-        const float fb = mb == -INFINITY ? 0.f : exp2f(mb - M);
-        lr = lr * f + r0[1] * fa + r1[1] * fb;
-        Mr = M;
-#pragma unroll
-        for (int k = 0; k < KC; ++k) {
-          const int col = t16 + 16 * k;
-          if (col < dh + r) vr[k] = vr[k] * f + r0[2 + col] * fa + r1[2 + col] * fb;
-        }
-      }
-      const int h = m0 + hm;
-      if (h < H) {
-        const int slot = pc.b + c;
-        if (t16 == 0) {
-          float* pml = P.part_ml + (static_cast<size_t>(slot) * H + h) * 2;
-          pml[0] = Mr;
-          pml[1] = lr;
-        }
-        float* o = P.part_acc + (static_cast<size_t>(slot) * H + h) * (dh + r);
-#pragma unroll
-        for (int k = 0; k < KC; ++k) {
-          const int col = t16 + 16 * k;
-          if (col < dh + r) o[col] = vr[k];
         }
       }
     }
@@ -898,7 +878,7 @@ static lrkv_status stream_plan_impl(DecodePlan& P) {
   P.Hp = round_up(H, 16);
   P.mt = P.Hp / 16;
   P.grid = std::max(1, P.grid / P.mt);
-  P.ngw = 1;
+  P.ngw = kPairs;  // one partial per warp pair and piece
   P.nthreads = kThreadsS;
   P.span = 128;
   P.box_cols = 64;
@@ -933,17 +913,15 @@ static lrkv_status stream_plan_impl(DecodePlan& P) {
   P.bk_dsplit = 1;
   while (r > 0 && 16 * (r / 4) * P.bk_dsplit * 2 <= kThreadsS && P.bk_dsplit * 2 <= dh / 4) P.bk_dsplit *= 2;
   P.bk_warps = r > 0 ? (16 * (r / 4) * P.bk_dsplit + 31) / 32 : 1;
-  P.cm_stride = (dh + r + 2) | 1;  // odd: the scatter rows fall in different banks
   P.stage_bytes = round_up(2 * P.kv_bytes + 2 * P.zt_bytes, 1024);
   const int pf_bytes = 2 * P.kst * 32 * 16;
 
-  // shared memory: barriers | prefix | p/q buffers | p fragments / merge buffer | ring
-  const int cm_bytes = 2 * 16 * P.cm_stride * 4;
+  // shared memory: barriers | prefix | p/q buffers | p fragments | ring
   auto layout = [&](int stages) {
     int off = 640;  // barriers, stage records, step offsets
     P.off_prefix = off; off = round_up(off + (P.B + 1) * 4, 128);
     P.off_pq = off; off = round_up(off + 2 * P.pq_bytes, 128);
-    P.off_pf = off; off = round_up(off + std::max(pf_bytes, cm_bytes), 1024);
+    P.off_pf = off; off = round_up(off + std::max(pf_bytes, 16), 1024);
     P.off_kv = off; off += stages * P.stage_bytes;
     return off + 1024;  // alignment slack
   };
