@@ -185,8 +185,8 @@ __device__ __forceinline__ void absorb_rows_smem(const DecodePlan& P, const BkRo
     const __nv_bfloat16* xa = qa + R.hl * P.dh + R.dp;
     const __nv_bfloat16* xb = qb ? qb + R.hl * P.dh + R.dp : nullptr;
     const int step = P.bk_dsplit * P.r, qstep = P.bk_dsplit;
-#pragma unroll 1
-    for (int i = 0; i < R.nd; ++i) {  // runs once per launch: kept small (cold code)
+#pragma unroll 4
+    for (int i = 0; i < R.nd; ++i) {  // runs once per launch: a short unroll keeps loads in flight
       const uint2 v = *reinterpret_cast<const uint2*>(bk + i * step);
       const float b0 = bf_lo(v.x), b1 = bf_hi(v.x), b2 = bf_lo(v.y), b3 = bf_hi(v.y);
       const float x = __bfloat162float(xa[i * qstep]);
