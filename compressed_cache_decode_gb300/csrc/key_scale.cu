@@ -6,9 +6,13 @@
 // k = s_j + z_j B_h^T (never the two parts normalised apart) and the scale is
 // 1 / sqrt(mean_d k[d]^2 + eps), in fp32.
 //
-// One CTA = (sequence b, head h, 64 new tokens): B_h^K, the tokens' shared rows
-// and their latents of head h staged in shared memory as fp32; four threads
-// per token rebuild a quarter of the key each and sum its squares.
+// The rebuild is a contraction per (sequence, head, block of 64 tokens):
+// K = Z_h B_h^T (64 x d_h, inner dimension r) plus the shared rows, on the
+// tensor cores (mma.sync m16n8k16: bf16 operands, exact products, fp32
+// accumulation); the epilogue adds the shared row, squares and sums over d
+// (thread, then quad), and writes 1 / sqrt(ss / d_h + eps).  B_h^K, the
+// block's latent rows and shared rows are staged in shared memory with padded
+// row strides (conflict-free ldmatrix).  Four warps, 16 tokens each.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -21,11 +25,15 @@ namespace lrkv {
 
 namespace {
 
-constexpr int kKsTokens = 64;
-constexpr int kKsThreads = 256;  // 4 per token
+constexpr int kKsTok = 64;       // tokens per CTA
+constexpr int kKsThreads = 128;  // four warps of 16 tokens
+constexpr int kKsCols = 128;     // key columns per accumulator pass
 
 struct KeyScaleParams {
   int B, H, dh, r, max_len, n_new;
+  int rp;                     // rank padded to a multiple of 16 (zeros)
+  int zs;                     // shared row stride (elements) of the B^K and latent rows: rp + 8
+  int rvec;                   // rows copied in 16-byte pieces (r a multiple of 8, aligned bases)
   float eps;
   const __nv_bfloat16* k_s;   // [B][max_len][dh]
   const __nv_bfloat16* z_k;   // [B][max_len][H][r]
@@ -37,55 +45,121 @@ struct KeyScaleParams {
 }  // namespace
 
 __global__ void __launch_bounds__(kKsThreads) lrkv_key_scale_kernel(const KeyScaleParams p) {
-  extern __shared__ float ks_smem[];
+  extern __shared__ __align__(16) unsigned char ks_raw[];
+  const int dh = p.dh, r = p.r, rp = p.rp, zs = p.zs;
+  __nv_bfloat16* sB = reinterpret_cast<__nv_bfloat16*>(ks_raw);  // [dh][zs]
+  __nv_bfloat16* sZ = sB + dh * zs;                              // [64][zs]
+  __nv_bfloat16* sS = sZ + kKsTok * zs;                          // [64][dh]
   const int h = blockIdx.y, b = blockIdx.z;
-  const int t_first = blockIdx.x * kKsTokens;
-  const int dh = p.dh, r = p.r;
-  float* sB = ks_smem;                       // [dh][r]
-  float* sZ = sB + dh * r;                   // [64][r]
-  float* sS = sZ + kKsTokens * r;            // [64][dh]
-  const int start = p.start_pos[b];
-  const int tid = threadIdx.x;
-  for (int i = tid; i < dh * r; i += blockDim.x)
-    sB[i] = __bfloat162float(p.b_k[static_cast<size_t>(h) * dh * r + i]);
-  for (int i = tid; i < kKsTokens * r; i += blockDim.x) {
-    const int t = i / r, c = i - t * r, pos = start + t_first + t;
-    const bool in = t_first + t < p.n_new && pos >= 0 && pos < p.max_len;
-    sZ[i] = in ? __bfloat162float(p.z_k[((static_cast<size_t>(b) * p.max_len + pos) * p.H + h) * r + c]) : 0.f;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, q4 = lane & 3;
+  const int t0 = blockIdx.x * kKsTok, start = p.start_pos[b];
+  const int nt = min(kKsTok, p.n_new - t0);
+  const __nv_bfloat16* bh = p.b_k + static_cast<size_t>(h) * dh * r;
+  auto zrow = [&](int t) -> const __nv_bfloat16* {  // latent row of block token t, or null
+    const int pos = start + t0 + t;
+    if (t >= nt || pos < 0 || pos >= p.max_len) return nullptr;
+    return p.z_k + ((static_cast<size_t>(b) * p.max_len + pos) * p.H + h) * r;
+  };
+  const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
+  if (p.rvec) {
+    const int pr = rp / 8;  // 16-byte pieces per padded row
+    for (int i = tid; i < dh * pr; i += kKsThreads) {
+      const int d = i / pr, c8 = i - d * pr;
+      *reinterpret_cast<uint4*>(sB + d * zs + 8 * c8) =
+          8 * c8 < r ? reinterpret_cast<const uint4*>(bh + static_cast<size_t>(d) * r)[c8] : zero4;
+    }
+    for (int i = tid; i < kKsTok * pr; i += kKsThreads) {
+      const int t = i / pr, c8 = i - t * pr;
+      const __nv_bfloat16* zr = zrow(t);
+      *reinterpret_cast<uint4*>(sZ + t * zs + 8 * c8) =
+          (zr && 8 * c8 < r) ? reinterpret_cast<const uint4*>(zr)[c8] : zero4;
+    }
+  } else {
+    const __nv_bfloat16 zb = __float2bfloat16_rn(0.f);
+    for (int i = tid; i < dh * rp; i += kKsThreads) {
+      const int d = i / rp, c = i - d * rp;
+      sB[d * zs + c] = c < r ? bh[static_cast<size_t>(d) * r + c] : zb;
+    }
+    for (int i = tid; i < kKsTok * rp; i += kKsThreads) {
+      const int t = i / rp, c = i - t * rp;
+      const __nv_bfloat16* zr = zrow(t);
+      sZ[t * zs + c] = (zr && c < r) ? zr[c] : zb;
+    }
   }
-  for (int i = tid; i < kKsTokens * dh; i += blockDim.x) {
-    const int t = i / dh, d = i - t * dh, pos = start + t_first + t;
-    const bool in = t_first + t < p.n_new && pos >= 0 && pos < p.max_len;
-    sS[i] = in ? __bfloat162float(p.k_s[(static_cast<size_t>(b) * p.max_len + pos) * dh + d]) : 0.f;
+  const int pieces = dh / 8;
+  for (int i = tid; i < kKsTok * pieces; i += kKsThreads) {
+    const int t = i / pieces, c8 = i - t * pieces, pos = start + t0 + t;
+    uint4 u = zero4;
+    if (t < nt && pos >= 0 && pos < p.max_len)
+      u = reinterpret_cast<const uint4*>(p.k_s + (static_cast<size_t>(b) * p.max_len + pos) * dh)[c8];
+    *reinterpret_cast<uint4*>(sS + t * dh + 8 * c8) = u;
   }
   __syncthreads();
-  const int t = tid >> 2, part = tid & 3;    // token, quarter of the key
-  const float* z = sZ + t * r;
-  float ss = 0.f;
-  for (int d = part; d < dh; d += 4) {
-    const float* bd = sB + d * r;
-    float k = sS[t * dh + d];
-    for (int c = 0; c < r; ++c) k = fmaf(z[c], bd[c], k);
-    ss = fmaf(k, k, ss);
+
+  const int trow = 16 * warp;  // this warp's first token
+  float ss0 = 0.f, ss1 = 0.f;  // sums of squares of tokens trow + g and trow + g + 8
+  for (int dc = 0; dc < dh; dc += kKsCols) {
+    const int nn = min(kKsCols, dh - dc) / 8;  // n tiles of 8 columns (a multiple of 4)
+    float acc[kKsCols / 8][4];
+#pragma unroll
+    for (int j = 0; j < kKsCols / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+    for (int kk = 0; kk < rp / 16; ++kk) {
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4(a0, a1, a2, a3, sZ + (trow + (lane & 15)) * zs + 16 * kk + 8 * (lane >> 4));
+      const int m = lane >> 3;
+#pragma unroll
+      for (int j = 0; j < kKsCols / 8; j += 2) {
+        if (j < nn) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(b0, b1, b2, b3, sB + (dc + 8 * (j + (m >> 1)) + (lane & 7)) * zs + 16 * kk + 8 * (m & 1));
+          mma_bf16_16816(acc[j], a0, a1, a2, a3, b0, b1);
+          mma_bf16_16816(acc[j + 1], a0, a1, a2, a3, b2, b3);
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kKsCols / 8; ++j) {
+      if (j < nn) {
+        const int d = dc + 8 * j + 2 * q4;
+        const uint32_t s0 = *reinterpret_cast<const uint32_t*>(sS + (trow + g) * dh + d);
+        const uint32_t s1 = *reinterpret_cast<const uint32_t*>(sS + (trow + g + 8) * dh + d);
+        const float k00 = acc[j][0] + bf_lo(s0), k01 = acc[j][1] + bf_hi(s0);
+        const float k10 = acc[j][2] + bf_lo(s1), k11 = acc[j][3] + bf_hi(s1);
+        ss0 = fmaf(k00, k00, fmaf(k01, k01, ss0));
+        ss1 = fmaf(k10, k10, fmaf(k11, k11, ss1));
+      }
+    }
   }
-  ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-  ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-  const int pos = start + t_first + t;
-  if (part == 0 && t_first + t < p.n_new && pos >= 0 && pos < p.max_len)
-    p.key_scale[(static_cast<size_t>(b) * p.H + h) * p.max_len + pos] = 1.f / sqrtf(ss / dh + p.eps);
+  ss0 += __shfl_xor_sync(0xffffffffu, ss0, 1);
+  ss0 += __shfl_xor_sync(0xffffffffu, ss0, 2);
+  ss1 += __shfl_xor_sync(0xffffffffu, ss1, 1);
+  ss1 += __shfl_xor_sync(0xffffffffu, ss1, 2);
+  if (q4 == 0) {
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int t = trow + g + 8 * u, pos = start + t0 + t;
+      if (t < nt && pos >= 0 && pos < p.max_len)
+        p.key_scale[(static_cast<size_t>(b) * p.H + h) * p.max_len + pos] =
+            1.f / sqrtf((u ? ss1 : ss0) / dh + p.eps);
+    }
+  }
 }
 
 lrkv_status key_scale_launch(const lrkv_dims& dm, float eps, int n_new, const void* k_s, const void* z_k,
                              const void* b_k, const int32_t* start_pos, float* key_scale, void* stream) {
   KeyScaleParams p;
   p.B = dm.batch; p.H = dm.heads; p.dh = dm.head_dim; p.r = dm.rank; p.max_len = dm.max_len; p.n_new = n_new;
+  p.rp = (dm.rank + 15) / 16 * 16;
+  p.zs = p.rp + 8;
+  p.rvec = dm.rank % 8 == 0 && (reinterpret_cast<uintptr_t>(b_k) & 15u) == 0 &&
+           (reinterpret_cast<uintptr_t>(z_k) & 15u) == 0;
   p.eps = eps;
   p.k_s = static_cast<const __nv_bfloat16*>(k_s);
   p.z_k = static_cast<const __nv_bfloat16*>(z_k);
   p.b_k = static_cast<const __nv_bfloat16*>(b_k);
   p.start_pos = start_pos;
   p.key_scale = key_scale;
-  const int smem = (dm.head_dim * dm.rank + kKsTokens * dm.rank + kKsTokens * dm.head_dim) * 4;
+  const int smem = ((dm.head_dim + kKsTok) * p.zs + kKsTok * dm.head_dim) * 2;
   static int have = 0;
   if (smem > 48 * 1024 && smem > have) {
     if (cudaFuncSetAttribute(lrkv_key_scale_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
@@ -93,7 +167,7 @@ lrkv_status key_scale_launch(const lrkv_dims& dm, float eps, int n_new, const vo
       return LRKV_ERR_CUDA;
     have = smem;
   }
-  const dim3 grid((n_new + kKsTokens - 1) / kKsTokens, dm.heads, dm.batch);
+  const dim3 grid((n_new + kKsTok - 1) / kKsTok, dm.heads, dm.batch);
   lrkv_key_scale_kernel<<<grid, kKsThreads, smem, static_cast<cudaStream_t>(stream)>>>(p);
   return cudaGetLastError() == cudaSuccess ? LRKV_OK : LRKV_ERR_CUDA;
 }

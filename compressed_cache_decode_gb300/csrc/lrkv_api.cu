@@ -132,8 +132,8 @@ lrkv_status lrkv_key_scales(const lrkv_dims* dims, float eps, int n_new, const v
   if (dims->dtype != LRKV_BF16 || dims->rank < 1 || dims->head_dim > 256) return LRKV_ERR_UNSUPPORTED;
   if (!(eps >= 0.f) || n_new < 1) return LRKV_ERR_INVALID_ARG;
   if (!k_s || !z_k || !b_k || !start_pos || !key_scale) return LRKV_ERR_INVALID_ARG;
-  if ((static_cast<long long>(dims->head_dim) * dims->rank + 64ll * (dims->rank + dims->head_dim)) * 4 > 200 * 1024)
-    return LRKV_ERR_UNSUPPORTED;
+  if (dims->rank > 64 || dims->head_dim % 32 != 0) return LRKV_ERR_UNSUPPORTED;
+  if (!aligned16(k_s)) return LRKV_ERR_INVALID_ARG;  // rows read in 16-byte pieces
   return lrkv::key_scale_launch(*dims, eps, n_new, k_s, z_k, b_k, start_pos, key_scale, stream);
 }
 

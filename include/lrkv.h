@@ -273,8 +273,8 @@ lrkv_status lrkv_decode_step(const lrkv_dims* dims, int d_model, const void* x, 
  * cached k_s, z_k (bf16, as stored) and B^K; rows outside [0, max_len) are
  * skipped.  Call it after appending the rows.
  *   key_scale  [batch][heads][max_len] fp32 (device), caller-allocated
- * Supported: dtype BF16, rank >= 1, (head_dim*rank + 64*(head_dim+rank))*4
- * <= 200 KB.
+ * Supported: dtype BF16, 1 <= rank <= 64, head_dim a multiple of 32 (at most
+ * 256); k_s 16-byte aligned (else LRKV_ERR_INVALID_ARG).
  *
  * lrkv_decode_normed is lrkv_decode with every summed score multiplied by
  * key_scale[b][h][j] before the softmax (values are not normalised).

@@ -78,7 +78,9 @@ def test_decode_normed_matches_oracle(shape):
 @pytest.mark.parametrize("shape", [
     # B, q_len, H, L per sequence, max_len
     (1, 128, 2, [128], 128),
-    (2, 200, 3, [200, 450], 512),        # partial query tile, history before the queries
+    (2, 200, 3, [200, 450], 452),        # partial query tile, history before the queries, a key
+                                         # tile past max_len (vector and shuffled scale reads)
+    (1, 130, 2, [301], 301),             # max_len not a multiple of 4: shuffled scale reads only
     (2, 512, 40, [512, 700], 768),       # more items than SMs: several per persistent CTA
 ])
 def test_prefill_normed_matches_oracle(shape):
