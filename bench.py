@@ -19,6 +19,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import os
@@ -90,12 +91,17 @@ def _profile_traffic(split_kernel_src_sha):
 
 
 def _src_sha():
+    """sha256 of the decode kernel sources with comments and blank lines
+    removed (a comment edit leaves the profiled code, and its hash, as is)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "compressed_cache_decode_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.startswith("decode") or name == "ptx.cuh":
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(f.read())
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
+                text = f.read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines())
+            h.update("\n".join(ln for ln in lines if ln).encode())
     return h.hexdigest()
 
 

@@ -10,10 +10,11 @@
 // segment; TMA fills the excess with zeros), so that ldmatrix over 8 token
 // rows is free of bank conflicts.
 //
-// The 8 warps work independently: warp w takes every 8th tile and refills
-// the stage it consumed with the tile `stages` ahead.  Per tile (16 tokens x
-// 16 heads), FlashAttention-2 style, everything on the tensor cores
-// (bf16 mma.sync, fp32 accumulation):
+// The 8 warps form 4 pairs: pair p takes every 4th tile of the CTA's range
+// (tile i in stage i % stages), each warp of the pair 8 of the 16 heads, and
+// the second warp of the pair to finish a stage refills it with the tile
+// `stages` ahead.  Per tile and warp, FlashAttention-2 style, the products on
+// the tensor cores (bf16 mma.sync, fp32 accumulation):
 //   * scores, transposed (tokens are the M dimension):
 //       S^T = K_s q^T + Z_k P_bd, where P_bd is block diagonal: column h
 //       holds p_h = q_h B_h^K on the rows of head h's latents.  p_h is split
@@ -21,14 +22,17 @@
 //   * ONE online softmax per head over the summed scores ("Low-Rank Key
 //     Value Attention | What a shared cache can preserve", §3, fused
 //     online-softmax paragraph), with a lazily raised reference maximum.
-//   * the probabilities are transposed in registers (movmatrix) into the A
-//     operand (heads x tokens) of
-//       O_s += P V_s            (shared values)
-//       O_z[h] += P[h] Z_v,h    (private values: one MMA per head and 8
-//                                latent columns with A masked to row h, so
-//                                all 16 heads share one accumulator set).
-// At the end of each (sequence, range) piece the warps' states are merged
-// on chip (a tree through shared memory) and written as the piece's partial.
+//   * the probabilities are transposed in registers (movmatrix) into the B
+//     operand of the transposed value products
+//       O_s^T += V_s^T P^T      (shared values: rows of the head dim)
+//       O_z^T += Z_v^T P^T      (private values: the half's latent rows; only
+//                                the entries on a head's own rows are kept).
+// At the end of each (sequence, range) piece every pair writes its state
+// (m, l, O_s, O_z of its heads) as one partial; the combine kernel merges
+// the pairs' and the pieces' partials.  The first launch phase (lengths,
+// first copies, absorb of p, set-up) runs code the SM has not fetched yet;
+// the last warp runs the tile code once on no tokens meanwhile, so that the
+// tiles find it in the instruction cache.
 #include <cmath>
 #include <algorithm>
 #include <cstring>
