@@ -804,8 +804,8 @@ lrkv_status launch_all(const DecodePlan& P, cudaStream_t stream, cudaEvent_t ev_
     const CUtensorMapSwizzle sw = P.span == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                                   : P.span == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
                                                  : CU_TENSOR_MAP_SWIZZLE_32B;
-    if (!make_tmap_3d_bf16(&tm_k, P.k_s, P.dh, P.max_len, P.B, P.box_cols, P.T, sw) ||
-        !make_tmap_3d_bf16(&tm_v, P.v_s, P.dh, P.max_len, P.B, P.box_cols, P.T, sw))
+    if (!make_tmap_3d_bf16(&tm_k, P.k_s, P.dh, P.map_len, P.map_seqs, P.box_cols, P.T, sw) ||
+        !make_tmap_3d_bf16(&tm_v, P.v_s, P.dh, P.map_len, P.map_seqs, P.box_cols, P.T, sw))
       return LRKV_ERR_CUDA;
   }
   const SplitFn split = P.stream ? nullptr : split_fn(P);
@@ -877,6 +877,7 @@ lrkv_status launch_all(const DecodePlan& P, cudaStream_t stream, cudaEvent_t ev_
 lrkv_status decode_make_plan(const lrkv_dims& d, int num_sms, DecodePlan& P, size_t* ws_bytes) {
   std::memset(&P, 0, sizeof(P));
   P.B = d.batch; P.H = d.heads; P.dh = d.head_dim; P.r = d.rank; P.max_len = d.max_len;
+  P.map_len = d.max_len; P.map_seqs = d.batch;  // contiguous cache (a paged call overrides)
   const float scale = d.scale > 0.f ? d.scale : 1.f / std::sqrt(static_cast<float>(d.head_dim));
   P.scale_log2 = scale * kLog2e;
   P.bf16 = d.dtype == LRKV_BF16;

@@ -95,6 +95,13 @@ struct DecodePlan {
   const void* b_v;
   const int32_t* seq_lens;
   const float* key_scale;  // [B][H][max_len] reciprocal key RMS (post-projection RMSNorm) or NULL
+  // cache layout: contiguous ([B][max_len] rows), or paged: logical row t of
+  // sequence b is row t & (2^page_shift - 1) of page block_table[b][t >> page_shift]
+  // of a pool [num_pages][2^page_shift]; the tensor maps span (map_len rows,
+  // map_seqs sequences or pages)
+  const int32_t* block_table;  // [B][max_blocks] or NULL (contiguous)
+  int max_blocks, page_shift, num_pages;
+  int map_len, map_seqs;
   float* out;
   float* lse;
 };

@@ -73,15 +73,20 @@ __device__ __forceinline__ void named_arrive(int id, int nthreads) {
   asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-// Pieces of this CTA's token range: (sequence b, rows [t_beg, t_end)).
+// Pieces of this CTA's token range: (sequence b, rows [t_lo, t_end)), in
+// tiles of kT rows from row t_beg.  For a paged cache the first piece's tiles
+// start on the 16-row grid of the sequence (t_beg = t_lo rounded down; the
+// rows before t_lo, the previous CTA's, are masked), so that no tile spans
+// two pages; otherwise t_beg = t_lo.  Later pieces start at row 0.
 struct Piece {
-  int b, t_beg, t_end, ntiles;
+  int b, t_beg, t_end, ntiles, t_lo;
 };
 
-__device__ __forceinline__ bool piece_first(Piece& p, const int* pre, int B, int g0, int g1) {
+__device__ __forceinline__ bool piece_first(Piece& p, const int* pre, int B, int g0, int g1, bool align) {
   TileWalk w;
   if (!walk_first(w, pre, B, g0, g1)) return false;
-  p.b = w.b; p.t_beg = w.t0; p.t_end = w.t_end;
+  p.b = w.b; p.t_lo = w.t0; p.t_end = w.t_end;
+  p.t_beg = align ? (w.t0 & ~(kT - 1)) : w.t0;
   p.ntiles = (p.t_end - p.t_beg + kT - 1) / kT;
   return true;
 }
@@ -90,7 +95,7 @@ __device__ __forceinline__ bool piece_next(Piece& p, const int* pre, int B, int 
   int b = p.b + 1;
   while (b < B && pre[b] < g1 && pre[b + 1] == pre[b]) ++b;
   if (b >= B || pre[b] >= g1) return false;
-  p.b = b; p.t_beg = 0; p.t_end = min(pre[b + 1], g1) - pre[b];
+  p.b = b; p.t_beg = 0; p.t_lo = 0; p.t_end = min(pre[b + 1], g1) - pre[b];
   p.ntiles = (p.t_end + kT - 1) / kT;
   return true;
 }
@@ -110,10 +115,26 @@ struct TileCursor {
 };
 
 // The copies of tile (sequence b, rows t0..t0+15) into stage s (one thread).
-__device__ __forceinline__ void stream_issue(const DecodePlan& P, const CUtensorMap* tk, const CUtensorMap* tv,
+// Tensor-map coordinates (sequence or page, row) of logical row t of
+// sequence b; false when the block table names no page of the pool (the copy
+// then reads the fill value, zeros, and the caller records the bound).
+__device__ __forceinline__ bool cache_coords(const DecodePlan& P, int b, int t, int& seq, int& row) {
+  if (!P.block_table) {
+    seq = b;
+    row = t;
+    return true;
+  }
+  seq = __ldg(P.block_table + static_cast<size_t>(b) * P.max_blocks + (t >> P.page_shift));
+  row = t & ((1 << P.page_shift) - 1);
+  return seq >= 0 && seq < P.num_pages;
+}
+
+__device__ __forceinline__ bool stream_issue(const DecodePlan& P, const CUtensorMap* tk, const CUtensorMap* tv,
                                              const CUtensorMap* tzk, const CUtensorMap* tzv,
-                                             unsigned char* smem, uint64_t* full, int s, int b, int t0,
+                                             unsigned char* smem, uint64_t* full, int s, int b_log, int t_log,
                                              int zseg0) {
+  int b, t0;  // a 16-token tile never spans two pages (page_size is a multiple of 16)
+  const bool in_pool = cache_coords(P, b_log, t_log, b, t0);
   unsigned char* ks = smem + P.off_kv + static_cast<size_t>(s) * P.stage_bytes;
   unsigned char* vs = ks + P.kv_bytes;
   unsigned char* zk = vs + P.kv_bytes;
@@ -127,6 +148,7 @@ __device__ __forceinline__ void stream_issue(const DecodePlan& P, const CUtensor
     tma_load_4d(zk, tzk, 0, t0, zseg0, b, &full[s]);
     tma_load_4d(zv, tzv, 0, t0, zseg0, b, &full[s]);
   }
+  return in_pool;
 }
 
 // q (bf16) of the row tile's heads of sequence b into p/q buffer `buf`
@@ -277,15 +299,22 @@ __device__ __forceinline__ bool wait_issued(const int* issued, int want) {
 // the latent rows of all heads (each contiguous in memory), by bulk copies
 // with no destination, so that HBM streams ahead of the shared-memory ring.
 __device__ __forceinline__ void l2_prefetch_rows(const DecodePlan& P, int b, int r0, int r1) {
-  if (r1 <= r0) return;
-  const size_t row0 = static_cast<size_t>(b) * P.max_len + r0;
-  const uint32_t n = static_cast<uint32_t>(r1 - r0);
   const uint32_t kv = static_cast<uint32_t>(P.dh) * 2u, zr = static_cast<uint32_t>(P.H * P.r) * 2u;
-  l2_prefetch_bulk(static_cast<const unsigned char*>(P.k_s) + row0 * kv, n * kv);
-  l2_prefetch_bulk(static_cast<const unsigned char*>(P.v_s) + row0 * kv, n * kv);
-  if (zr) {
-    l2_prefetch_bulk(static_cast<const unsigned char*>(P.z_k) + row0 * zr, n * zr);
-    l2_prefetch_bulk(static_cast<const unsigned char*>(P.z_v) + row0 * zr, n * zr);
+  while (r0 < r1) {
+    // rows of one page at a time (all rows at once for a contiguous cache)
+    const int r_end = P.block_table ? min(r1, ((r0 >> P.page_shift) + 1) << P.page_shift) : r1;
+    int sq, rw;
+    if (cache_coords(P, b, r0, sq, rw)) {
+      const size_t row0 = static_cast<size_t>(sq) * P.map_len + rw;
+      const uint32_t n = static_cast<uint32_t>(r_end - r0);
+      l2_prefetch_bulk(static_cast<const unsigned char*>(P.k_s) + row0 * kv, n * kv);
+      l2_prefetch_bulk(static_cast<const unsigned char*>(P.v_s) + row0 * kv, n * kv);
+      if (zr) {
+        l2_prefetch_bulk(static_cast<const unsigned char*>(P.z_k) + row0 * zr, n * zr);
+        l2_prefetch_bulk(static_cast<const unsigned char*>(P.z_v) + row0 * zr, n * zr);
+      }
+    }
+    r0 = r_end;
   }
 }
 
@@ -295,7 +324,7 @@ constexpr int kPrefetchChunk = 4;
 __device__ __forceinline__ void l2_prefetch_tiles(const DecodePlan& P, const int* pre, int B, int g0, int g1,
                                                   int t0, int t1) {
   TileCursor cur;
-  cur.more = piece_first(cur.pc, pre, B, g0, g1);
+  cur.more = piece_first(cur.pc, pre, B, g0, g1, P.block_table != nullptr);
   cur.ibase = 0;
   int j = t0;
   while (j < t1 && cur.seek(j, pre, B, g1)) {
@@ -318,6 +347,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
   constexpr int BZ = MZA > 16 ? 4 : 8;       // private-value steps per load batch
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ int s_timeout;
+  __shared__ int s_nopage;  // a block table entry named no page of the pool
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
 
   // the merge kernel may launch now: it waits for this grid before it reads
@@ -358,6 +388,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       prefetch_tmap(&tm_zv);
     }
     s_timeout = 0;
+    s_nopage = 0;
     for (int s = 0; s < P.stages; ++s) {
       mbar_init(&full[s], 1);
       issued[s] = -1;
@@ -420,7 +451,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
   // ---- 2. q of the first two pieces, then the first `stages` tiles (warp w
   // issues tiles w, w + 8, ...), so that the small copies land first ---------
   Piece pc;
-  bool more = piece_first(pc, pre, B, g0, g1);
+  bool more = piece_first(pc, pre, B, g0, g1, P.block_table != nullptr);
   Piece pc1 = pc;
   const bool two = piece_next(pc1, pre, B, g1);
   // with bk_stages > 0 the row tile's B^K lands in the last bk_stages ring
@@ -447,8 +478,9 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     cur.more = more;
     cur.ibase = 0;
     for (int j = warp; j < first_burst && cur.seek(j, pre, B, g1); j += kWarps) {
-      stream_issue(P, &tm_k, &tm_v, &tm_zk, &tm_zv, smem, full, j, cur.pc.b,
-                   cur.pc.t_beg + (j - cur.ibase) * kT, zseg0);
+      if (!stream_issue(P, &tm_k, &tm_v, &tm_zk, &tm_zv, smem, full, j, cur.pc.b,
+                        cur.pc.t_beg + (j - cur.ibase) * kT, zseg0))
+        *reinterpret_cast<volatile int*>(&s_nopage) = 1;
       *reinterpret_cast<volatile int*>(&issued[j]) = j;
     }
   }
@@ -500,8 +532,9 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       cur.more = more;
       cur.ibase = 0;
       for (int j = first_burst + warp; j < P.stages && cur.seek(j, pre, B, g1); j += P.bk_warps) {
-        stream_issue(P, &tm_k, &tm_v, &tm_zk, &tm_zv, smem, full, j, cur.pc.b,
-                     cur.pc.t_beg + (j - cur.ibase) * kT, zseg0);
+        if (!stream_issue(P, &tm_k, &tm_v, &tm_zk, &tm_zv, smem, full, j, cur.pc.b,
+                          cur.pc.t_beg + (j - cur.ibase) * kT, zseg0))
+          *reinterpret_cast<volatile int*>(&s_nopage) = 1;
         *reinterpret_cast<volatile int*>(&issued[j]) = j;
       }
     }
@@ -509,7 +542,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
   int ibase = 0;      // tile index of the piece's first tile
   int kp = warm ? -1 : 0;  // piece counter (p/q buffer kp & 1); -1: the warm-up pass
   TileCursor refill;  // tiles this pair issues (its tile + stages)
-  refill.more = piece_first(refill.pc, pre, B, g0, g1);
+  refill.more = piece_first(refill.pc, pre, B, g0, g1, P.block_table != nullptr);
   refill.ibase = 0;
   TileCursor pfcur = refill;  // tiles this pair prefetches into L2
   while (more) {
@@ -607,6 +640,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       const int s = i % P.stages;
       const int t0 = pc.t_beg + (i - ibase) * kT;
       const int nvalid = dry ? 0 : min(kT, pc.t_end - t0);
+      const int lo = max(0, pc.t_lo - t0);  // rows [lo, nvalid) of the tile are this CTA's
       if (ok && !dry) {
         ok = wait_issued(&issued[s], i) && mbar_wait_bounded(&full[s], static_cast<uint32_t>(i / P.stages) & 1u);
         if (!ok) *reinterpret_cast<volatile int*>(&s_timeout) = 1;
@@ -618,8 +652,9 @@ __global__ void __launch_bounds__(kThreadsS, 1)
         unsigned char* zv = zk + P.zt_bytes;
         // token masks of the value operands: rows past the history (unwritten
         // cache rows) must not meet their zero probabilities as 0 x NaN
-        const uint32_t keep0 = (2 * q4 < nvalid ? 0x0000ffffu : 0u) | (2 * q4 + 1 < nvalid ? 0xffff0000u : 0u);
-        const uint32_t keep1 = (2 * q4 + 8 < nvalid ? 0x0000ffffu : 0u) | (2 * q4 + 9 < nvalid ? 0xffff0000u : 0u);
+        auto mine = [&](int row) { return row >= lo && row < nvalid; };
+        const uint32_t keep0 = (mine(2 * q4) ? 0x0000ffffu : 0u) | (mine(2 * q4 + 1) ? 0xffff0000u : 0u);
+        const uint32_t keep1 = (mine(2 * q4 + 8) ? 0x0000ffffu : 0u) | (mine(2 * q4 + 9) ? 0xffff0000u : 0u);
 
         // post-projection RMSNorm: the joint reciprocal scale of each key
         // (token g / g+8, head hb + 2 q4 + e) multiplies its summed score;
@@ -675,7 +710,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
         }
 
         // scale, mask rows past the piece's end, tile max per head
-        const bool v0 = g < nvalid, v1 = g + 8 < nvalid;
+        const bool v0 = mine(g), v1 = mine(g + 8);
         float sc[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -760,8 +795,9 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       if (second && refill.seek(j, pre, B, g1)) {
         fence_proxy_async_smem();
         if (ok && lane == 0) {
-          stream_issue(P, &tm_k, &tm_v, &tm_zk, &tm_zv, smem, full, s, refill.pc.b,
-                       refill.pc.t_beg + (j - refill.ibase) * kT, zseg0);
+          if (!stream_issue(P, &tm_k, &tm_v, &tm_zk, &tm_zv, smem, full, s, refill.pc.b,
+                            refill.pc.t_beg + (j - refill.ibase) * kT, zseg0))
+            *reinterpret_cast<volatile int*>(&s_nopage) = 1;
           *reinterpret_cast<volatile int*>(&issued[s]) = j;
         }
         // keep the L2 prefetch window pfw tiles ahead of the ring
@@ -833,7 +869,8 @@ __global__ void __launch_bounds__(kThreadsS, 1)
   if (!ok) *reinterpret_cast<volatile int*>(&s_timeout) = 1;
   named_sync(1, kThreadsS);
   if (tid == 0)
-    *cta_status = (bad ? kDevBounds : 0u) | (*reinterpret_cast<volatile int*>(&s_timeout) ? kDevTimeout : 0u);
+    *cta_status = (bad || *reinterpret_cast<volatile int*>(&s_nopage) ? kDevBounds : 0u) |
+                  (*reinterpret_cast<volatile int*>(&s_timeout) ? kDevTimeout : 0u);
 }
 
 // ======================================================================= host
@@ -956,11 +993,12 @@ lrkv_status stream_prepare(const DecodePlan& P, CUtensorMap* tm_zk, CUtensorMap*
   std::memset(tm_zv, 0, sizeof(*tm_zv));
   if (P.r > 0) {
     // z[b][t][h][c] viewed as [b][segment][t][hs r]: dims (inner first)
-    // {hs r, max_len, H / hs, B}, strides t: H r, segment: hs r, b: max_len H r
+    // {hs r, rows, H / hs, sequences}, strides t: H r, segment: hs r, b: rows H r
+    // (rows, sequences) = (max_len, B), or (page_size, pages) for a paged cache
     const uint64_t row = static_cast<uint64_t>(P.H) * P.r * 2;
-    const uint64_t dims[4] = {static_cast<uint64_t>(P.segw), static_cast<uint64_t>(P.max_len),
-                              static_cast<uint64_t>(P.H / P.hs), static_cast<uint64_t>(P.B)};
-    const uint64_t strides[3] = {row, static_cast<uint64_t>(P.segw) * 2, row * P.max_len};
+    const uint64_t dims[4] = {static_cast<uint64_t>(P.segw), static_cast<uint64_t>(P.map_len),
+                              static_cast<uint64_t>(P.H / P.hs), static_cast<uint64_t>(P.map_seqs)};
+    const uint64_t strides[3] = {row, static_cast<uint64_t>(P.segw) * 2, row * P.map_len};
     const uint32_t box[4] = {static_cast<uint32_t>(P.segp), static_cast<uint32_t>(kT),
                              static_cast<uint32_t>(P.nsb), 1u};
     if (!make_tmap_4d_bf16_strided(tm_zk, P.z_k, dims, strides, box) ||

@@ -75,11 +75,17 @@ lrkv_status lrkv_decode_workspace_size(const lrkv_dims* dims, size_t* bytes) {
 
 namespace {
 
+// A paged cache: pools of num_pages pages of page_size rows, block_table [B][max_len / page_size].
+struct PagedCache {
+  const int32_t* block_table;
+  int page_size, num_pages;
+};
+
 lrkv_status decode_common(const lrkv_dims* dims, const void* q, const void* k_s, const void* v_s,
                           const void* z_k, const void* z_v, const void* b_k, const void* b_v,
                           const int32_t* seq_lens, float* out, float* lse, void* ws, size_t ws_bytes,
                           lrkv_stream_t stream, void* ev_begin, void* ev_end,
-                          const float* key_scale = nullptr) {
+                          const float* key_scale = nullptr, const PagedCache* paged = nullptr) {
   lrkv_status st = check_decode_dims(dims);
   if (st != LRKV_OK) return st;
   if (!q || !k_s || !v_s || !seq_lens || !out) return LRKV_ERR_INVALID_ARG;
@@ -94,8 +100,18 @@ lrkv_status decode_common(const lrkv_dims* dims, const void* q, const void* k_s,
   size_t need = 0;
   if ((st = lrkv::decode_make_plan(*dims, sms, P, &need)) != LRKV_OK) return st;
   if (ws_bytes < need) return LRKV_ERR_WORKSPACE;
-  // post-projection RMSNorm: the streaming scan applies the key scales
-  if (key_scale && !P.stream) return LRKV_ERR_UNSUPPORTED;
+  // post-projection RMSNorm and the paged cache: the streaming scan only
+  if ((key_scale || paged) && !P.stream) return LRKV_ERR_UNSUPPORTED;
+  if (paged) {
+    int shift = 0;
+    while ((1 << shift) < paged->page_size) ++shift;
+    P.block_table = paged->block_table;
+    P.max_blocks = dims->max_len / paged->page_size;
+    P.page_shift = shift;
+    P.num_pages = paged->num_pages;
+    P.map_len = paged->page_size;
+    P.map_seqs = paged->num_pages;
+  }
   lrkv::decode_bind_workspace(P, ws);
   P.q = q; P.k_s = k_s; P.v_s = v_s; P.z_k = z_k; P.z_v = z_v; P.b_k = b_k; P.b_v = b_v;
   P.seq_lens = seq_lens; P.out = out; P.lse = lse;
@@ -123,6 +139,20 @@ lrkv_status lrkv_decode_profiled(const lrkv_dims* dims, const void* q, const voi
   if (!ev_split_begin || !ev_split_end) return LRKV_ERR_INVALID_ARG;
   return decode_common(dims, q, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens, out, lse, ws, ws_bytes, stream,
                        ev_split_begin, ev_split_end);
+}
+
+lrkv_status lrkv_decode_paged(const lrkv_dims* dims, int page_size, int num_pages, const int32_t* block_table,
+                              const void* q, const void* k_s, const void* v_s, const void* z_k, const void* z_v,
+                              const void* b_k, const void* b_v, const int32_t* seq_lens, float* out, float* lse,
+                              void* ws, size_t ws_bytes, lrkv_stream_t stream) {
+  if (!dims || !block_table) return LRKV_ERR_INVALID_ARG;
+  if (page_size < 16 || (page_size & (page_size - 1)) != 0 || num_pages < 1) return LRKV_ERR_INVALID_ARG;
+  if (dims->max_len % page_size != 0) return LRKV_ERR_INVALID_ARG;
+  if (static_cast<long long>(num_pages) * page_size > (1LL << 31) - 1) return LRKV_ERR_UNSUPPORTED;
+  if (dims->dtype != LRKV_BF16) return LRKV_ERR_UNSUPPORTED;
+  const PagedCache pc{block_table, page_size, num_pages};
+  return decode_common(dims, q, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens, out, lse, ws, ws_bytes, stream, nullptr,
+                       nullptr, nullptr, &pc);
 }
 
 lrkv_status lrkv_key_scales(const lrkv_dims* dims, float eps, int n_new, const void* k_s, const void* z_k,

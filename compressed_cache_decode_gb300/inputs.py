@@ -174,6 +174,36 @@ def random_decode_case(seed: int, batch: int, heads: int, head_dim: int, rank: i
                 b_k=b_k.to(dt), b_v=b_v.to(dt), seq_lens=seq_lens.to(torch.int32))
 
 
+def paged_from_contiguous(case: Dict[str, torch.Tensor], page_size: int, seed: int,
+                          extra_pages: int = 3) -> Dict[str, torch.Tensor]:
+    """The cache of a contiguous case (max_len a multiple of page_size) laid
+    out in a page pool: block j of sequence b goes to a page drawn by a seeded
+    permutation; `extra_pages` unused pages and every page row never written
+    hold NaN; the block table [B][max_len / page_size] (int32) maps the blocks
+    of each sequence that hold any of its rows and is -1 past them."""
+    k_s = case["k_s"]
+    B, L = k_s.shape[0], k_s.shape[1]
+    assert L % page_size == 0
+    nb = L // page_size
+    lens = case["seq_lens"].tolist()
+    used = [(b, j) for b in range(B) for j in range(nb) if j * page_size < lens[b]]
+    n_pages = len(used) + extra_pages
+    gen = torch.Generator().manual_seed(seed)
+    perm = torch.randperm(n_pages, generator=gen).tolist()
+    table = torch.full((B, nb), -1, dtype=torch.int32)
+    out = dict(case)
+    for name in ("k_s", "v_s", "z_k", "z_v"):
+        t = case[name]
+        pool = torch.full((n_pages, page_size) + tuple(t.shape[2:]), float("nan"), dtype=t.dtype)
+        for k, (b, j) in enumerate(used):
+            pool[perm[k]] = t[b, j * page_size:(j + 1) * page_size]
+        out[name] = pool
+    for k, (b, j) in enumerate(used):
+        table[b, j] = perm[k]
+    out["block_table"] = table
+    return out
+
+
 def random_prefill_case(seed: int, batch: int, q_len: int, heads: int, head_dim: int, rank: int,
                         max_len: int, lens, dtype: str = "bf16") -> Dict[str, torch.Tensor]:
     """Small randomised prefill case: a cache of `max_len` rows per sequence

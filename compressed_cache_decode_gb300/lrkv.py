@@ -42,6 +42,7 @@ EXPORTED = (
     "lrkv_key_scales",
     "lrkv_decode_normed",
     "lrkv_prefill_normed",
+    "lrkv_decode_paged",
     "lrkv_read_device_status",
 )
 
@@ -111,6 +112,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.lrkv_prefill_normed.restype = ctypes.c_int
     lib.lrkv_prefill_normed.argtypes = [dims_p, ctypes.c_int, vp, vp, vp, vp, vp, vp, vp, vp, i32p, vp, vp,
                                         vp, sz, vp]
+    lib.lrkv_decode_paged.restype = ctypes.c_int
+    lib.lrkv_decode_paged.argtypes = [dims_p, ctypes.c_int, ctypes.c_int, i32p, vp, vp, vp, vp, vp, vp, vp, i32p,
+                                      vp, vp, vp, sz, vp]
     lib.lrkv_read_device_status.restype = ctypes.c_int
     lib.lrkv_read_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
     if path is None:
@@ -393,4 +397,34 @@ def prefill_normed(q: torch.Tensor, k_s: torch.Tensor, v_s: torch.Tensor, z_k: t
                              ws.numel(), stream)
     if st != LRKV_OK:
         raise LRKVError(st, "lrkv_prefill_normed")
+    return out, lse, ws
+
+
+def lrkv_decode_paged(dims: lrkv_dims, page_size: int, num_pages: int, block_table, q, k_s, v_s, z_k, z_v, b_k,
+                      b_v, seq_lens, out, lse, ws, ws_bytes: int, stream=None) -> int:
+    """Direct call of the paged-cache decode entry point; returns its status."""
+    return int(load().lrkv_decode_paged(ctypes.byref(dims), page_size, num_pages, _ptr(block_table), _ptr(q),
+                                        _ptr(k_s), _ptr(v_s), _ptr(z_k), _ptr(z_v), _ptr(b_k), _ptr(b_v),
+                                        _ptr(seq_lens), _ptr(out), _ptr(lse), _ptr(ws), ws_bytes,
+                                        _stream_handle(stream)))
+
+
+def decode_paged(q, k_s, v_s, z_k, z_v, b_k, b_v, block_table, seq_lens, scale: float = 0.0, out=None, lse=None,
+                 ws=None, stream=None):
+    """decode over a paged cache: pools k_s, v_s [P, page_size, d_h] and
+    z_k, z_v [P, page_size, H, r]; block_table [B, max_len / page_size] int32."""
+    B, H, dh = q.shape
+    num_pages, page_size = k_s.shape[0], k_s.shape[1]
+    r = z_k.shape[-1]
+    dims = make_dims(B, H, dh, r, block_table.shape[1] * page_size, q.dtype, scale)
+    if out is None:
+        out = torch.empty((B, H, dh), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = decode_workspace(dims, q.device)
+    st = lrkv_decode_paged(dims, page_size, num_pages, block_table, q, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens,
+                           out, lse, ws, ws.numel(), stream)
+    if st != LRKV_OK:
+        raise LRKVError(st, "lrkv_decode_paged")
     return out, lse, ws

@@ -298,6 +298,32 @@ lrkv_status lrkv_prefill_normed(const lrkv_dims* dims, int q_len, const void* q,
                                 float* lse, void* ws, size_t ws_bytes, lrkv_stream_t stream);
 
 /*
+ * Decode over a paged factored cache (page boundaries as a serving concern:
+ * "Low-Rank Key Value Attention | What a shared cache can preserve", §4 and
+ * §9; the pages give no layout).  The rows of every sequence live in pages
+ * of page_size rows drawn from one pool per cache tensor:
+ *   k_s, v_s     [num_pages][page_size][head_dim]
+ *   z_k, z_v     [num_pages][page_size][heads][rank]
+ *   block_table  [batch][max_len / page_size] int32 (device): logical row t
+ *                of sequence b is row t % page_size of page
+ *                block_table[b][t / page_size]; entries of blocks at or past
+ *                seq_lens[b] are not read
+ * dims->max_len is the logical capacity of a sequence (a multiple of
+ * page_size).  Everything else (q, b_k, b_v, seq_lens, out, lse, ws, the
+ * workspace size from lrkv_decode_workspace_size(dims)) is as in lrkv_decode,
+ * and so is the result over the logical rows [0, seq_lens[b]).
+ * page_size: a power of two >= 16 (a 16-token tile never spans two pages);
+ * num_pages * page_size < 2^31.  A block table entry outside [0, num_pages)
+ * reads as zero rows and sets LRKV_ERR_DEVICE_BOUNDS in the status word.
+ * Supported: the shapes on which lrkv_decode streams bf16 (others return
+ * LRKV_ERR_UNSUPPORTED).
+ */
+lrkv_status lrkv_decode_paged(const lrkv_dims* dims, int page_size, int num_pages, const int32_t* block_table,
+                              const void* q, const void* k_s, const void* v_s, const void* z_k, const void* z_v,
+                              const void* b_k, const void* b_v, const int32_t* seq_lens, float* out, float* lse,
+                              void* ws, size_t ws_bytes, lrkv_stream_t stream);
+
+/*
  * Read the device status word that the kernels of the last call(s) using
  * `ws` recorded (LRKV_OK, LRKV_ERR_TIMEOUT or LRKV_ERR_DEVICE_BOUNDS).
  * Synchronises `stream`.  Each lrkv_decode/lrkv_prefill call sets the word

@@ -42,6 +42,11 @@ Readings where the pages leave a step open:
     norms); values are not normalised; a per-head gain is the caller's, folded
     into q (the review's remark on affine gains).
   * lse is the natural-log log-sum-exp of the scaled, masked logits.
+  * paged cache (review §4 and §9, page boundaries as a serving concern; the
+    pages give no layout): the rows of every sequence live in fixed-size pages
+    of a shared pool; logical row t of sequence b is row t mod page_size of
+    page block_table[b][t div page_size].  Attention over a paged cache is
+    attention over the logical rows (gather_paged).
 """
 from __future__ import annotations
 
@@ -354,3 +359,32 @@ def decode_flop_ratio(head_dim: int, rank: int, history: int) -> float:
     """C_LRKV / C_MHA ~= 1 + r/d_h + r/T (review §4 "Weight count and the two
     decode regimes")."""
     return 1.0 + rank / head_dim + rank / history
+
+
+# --------------------------------------------------------------------------
+# Paged cache: the logical rows of each sequence gathered from a page pool.
+
+def gather_paged(pool, block_table, page_size: int, max_len: int) -> np.ndarray:
+    """Logical cache [B, max_len, ...] of a page pool [num_pages, page_size,
+    ...]: row t of sequence b is pool[block_table[b][t // page_size], t %
+    page_size].  Blocks whose table entry is negative are left NaN (never
+    visible when the lengths stay inside the mapped blocks)."""
+    pool = _f64(pool)
+    bt = np.asarray(block_table, dtype=np.int64)
+    B = bt.shape[0]
+    out = np.full((B, max_len) + pool.shape[2:], np.nan)
+    for b in range(B):
+        for t in range(max_len):
+            pg = bt[b, t // page_size]
+            if pg >= 0:
+                out[b, t] = pool[pg, t % page_size]
+    return out
+
+
+def decode_reference_paged(q, k_s, v_s, z_k, z_v, b_k, b_v, block_table, page_size: int, seq_lens,
+                           scale: Optional[float] = None, pairs: Optional[Iterable[Tuple[int, int]]] = None):
+    """decode_reference over the logical rows of a paged cache (pools
+    k_s, v_s [P, page_size, d_h] and z_k, z_v [P, page_size, H, r])."""
+    max_len = np.asarray(block_table).shape[1] * page_size
+    g = [gather_paged(t, block_table, page_size, max_len) for t in (k_s, v_s, z_k, z_v)]
+    return decode_reference(q, g[0], g[1], g[2], g[3], b_k, b_v, seq_lens, scale=scale, pairs=pairs)

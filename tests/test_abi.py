@@ -135,3 +135,19 @@ def test_new_entries_reject_bad_arguments_without_gpu(lib):
     assert lib.lrkv_decode_step(ctypes.byref(f32), 64, *ptrs, fake, 1 << 20, None) == lrkv.LRKV_ERR_UNSUPPORTED
     assert lib.lrkv_decode_step(ctypes.byref(bf), 60, *ptrs, fake, 1 << 20, None) == \
         lrkv.LRKV_ERR_UNSUPPORTED       # d_model not a multiple of 8
+
+
+def test_paged_decode_rejects_bad_paging_without_gpu(lib):
+    """Page size, pool size and table are checked on the host before any launch."""
+    bf = lrkv.make_dims(2, 16, 64, 28, 256, "bf16")
+    fake = ctypes.c_void_p(4096)  # aligned, never dereferenced: the checks fail first
+    rest = (fake,) * 7 + (fake, fake, fake, fake, 1 << 24, None)  # q .. b_v, seq_lens, out, lse, ws, bytes, stream
+    call = lib.lrkv_decode_paged
+    assert call(ctypes.byref(bf), 24, 8, fake, *rest) == lrkv.LRKV_ERR_INVALID_ARG    # not a power of two
+    assert call(ctypes.byref(bf), 8, 8, fake, *rest) == lrkv.LRKV_ERR_INVALID_ARG     # below one 16-token tile
+    assert call(ctypes.byref(bf), 512, 8, fake, *rest) == lrkv.LRKV_ERR_INVALID_ARG   # max_len not a multiple
+    assert call(ctypes.byref(bf), 64, 0, fake, *rest) == lrkv.LRKV_ERR_INVALID_ARG    # empty pool
+    assert call(ctypes.byref(bf), 64, 8, None, *rest) == lrkv.LRKV_ERR_INVALID_ARG    # no block table
+    f32 = lrkv.make_dims(2, 16, 64, 28, 256, None)
+    f32.dtype = lrkv.LRKV_F32
+    assert call(ctypes.byref(f32), 64, 8, fake, *rest) == lrkv.LRKV_ERR_UNSUPPORTED   # bf16 streaming only

@@ -51,6 +51,7 @@ def test_key_scales_match_oracle(shape):
     (3, 4, 64, 16, 200, [57, 120, 1]),
     (2, 8, 128, 32, 300, [300, 129]),
     (4, 16, 64, 28, 4096, [4096, 3000, 17, 0]),
+    (6, 18, 64, 8, 80, [1, 2, 3, 80, 79, 5]),     # several pieces per CTA, a partial row tile
 ])
 def test_decode_normed_matches_oracle(shape):
     B, H, dh, r, Lm, lens = shape

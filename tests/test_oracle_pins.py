@@ -532,3 +532,57 @@ def test_norm_planted_mistakes_are_caught(mutant, monkeypatch):
     elif mutant == "dropped_latent":
         monkeypatch.setattr(O, "reconstruct_head", lambda s, z, b: s)
     assert not all(c() for c in _NORM_PINS), mutant
+
+
+# --------------------------------------------------------------------------
+# Paged cache: the oracle's gather through the block table against the cache
+# the pages were scattered from (by the input generator, written apart from
+# the oracle), and the paged decode against the contiguous one.
+
+def test_paged_gather_round_trip():
+    from compressed_cache_decode_gb300 import inputs
+    case = inputs.random_decode_case(seed=5, batch=3, heads=2, head_dim=8, rank=4, max_len=48, dtype="f32",
+                                     lens=[48, 1, 20])
+    ps = 16
+    paged = inputs.paged_from_contiguous(case, page_size=ps, seed=1)
+    bt = paged["block_table"].numpy()
+    assert len(set(bt[bt >= 0].tolist())) == (bt >= 0).sum()  # distinct pages
+    for name in ("k_s", "v_s", "z_k", "z_v"):
+        g = O.gather_paged(paged[name], bt, ps, 48)
+        ref = case[name].double().numpy()
+        for b, L in enumerate(case["seq_lens"].tolist()):
+            nblk = -(-L // ps)
+            assert np.array_equal(g[b, :nblk * ps], ref[b, :nblk * ps]), (name, b)
+            assert np.isnan(g[b, nblk * ps:]).all()
+    o1, l1 = O.decode_reference_paged(case["q"], paged["k_s"], paged["v_s"], paged["z_k"], paged["z_v"],
+                                      case["b_k"], case["b_v"], bt, ps, case["seq_lens"])
+    o2, l2 = O.decode_reference(case["q"], case["k_s"], case["v_s"], case["z_k"], case["z_v"], case["b_k"],
+                                case["b_v"], case["seq_lens"])
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_paged_gather_catches_a_wrong_row_order(monkeypatch):
+    """A gather that takes the block index and the row in page the wrong way
+    round fails the round trip."""
+    from compressed_cache_decode_gb300 import inputs
+    case = inputs.random_decode_case(seed=6, batch=2, heads=1, head_dim=4, rank=2, max_len=32, dtype="f32",
+                                     lens=[32, 17])
+    paged = inputs.paged_from_contiguous(case, page_size=16, seed=2)
+    bt = paged["block_table"].numpy()
+
+    def bad_gather(pool, block_table, page_size, max_len):
+        pool = np.asarray(pool, dtype=np.float64)
+        out = np.full((block_table.shape[0], max_len) + pool.shape[2:], np.nan)
+        for b in range(block_table.shape[0]):
+            for t in range(max_len):
+                pg = block_table[b, t % block_table.shape[1]]
+                if pg >= 0:
+                    out[b, t] = pool[pg, t // block_table.shape[1] % page_size]
+        return out
+
+    monkeypatch.setattr(O, "gather_paged", bad_gather)
+    o1, _ = O.decode_reference_paged(case["q"], paged["k_s"], paged["v_s"], paged["z_k"], paged["z_v"],
+                                     case["b_k"], case["b_v"], bt, 16, case["seq_lens"])
+    o2, _ = O.decode_reference(case["q"], case["k_s"], case["v_s"], case["z_k"], case["z_v"], case["b_k"],
+                               case["b_v"], case["seq_lens"])
+    assert not np.allclose(np.nan_to_num(o1), o2)
