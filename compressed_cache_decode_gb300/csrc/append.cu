@@ -37,6 +37,10 @@ struct AppendParams {
   int M, N, K;            // rows (B * n_new), columns (2 dh + 2 H r), depth (d_model)
   int n_new, max_len, dh, hr;
   const int32_t* start_pos;
+  // paged cache: row t of sequence b is row t & (2^page_shift - 1) of page
+  // block_table[b][t >> page_shift] of pools [num_pages][2^page_shift]; NULL: [B][max_len]
+  const int32_t* block_table;
+  int max_blocks, page_shift, num_pages;
   __nv_bfloat16* k_s;
   __nv_bfloat16* v_s;
   __nv_bfloat16* z_k;
@@ -146,8 +150,16 @@ __global__ void __launch_bounds__(128, 1)
       if (pos < 0 || pos >= p.max_len) {
         row_ok = false;
         atomicOr(p.status, kStatusBounds);
-      } else {
+      } else if (!p.block_table) {
         crow = static_cast<size_t>(b) * p.max_len + pos;
+      } else {
+        const int pg = p.block_table[static_cast<size_t>(b) * p.max_blocks + (pos >> p.page_shift)];
+        if (pg < 0 || pg >= p.num_pages) {  // no page of the pool: the row is not written
+          row_ok = false;
+          atomicOr(p.status, kStatusBounds);
+        } else {
+          crow = (static_cast<size_t>(pg) << p.page_shift) + (pos & ((1 << p.page_shift) - 1));
+        }
       }
     }
     for (int c = 0; c < kBN / 32; ++c) {
@@ -194,10 +206,10 @@ bool make_map_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t ro
 
 }  // namespace
 
-extern "C" lrkv_status lrkv_append(const lrkv_dims* dims, int d_model, int n_new, const void* x,
-                                   const void* w_sk, const void* w_sv, const void* u_k, const void* u_v,
-                                   const int32_t* start_pos, void* k_s, void* v_s, void* z_k, void* z_v,
-                                   void* ws, size_t ws_bytes, lrkv_stream_t stream) {
+static lrkv_status append_impl(const lrkv_dims* dims, int d_model, int n_new, const void* x, const void* w_sk,
+                               const void* w_sv, const void* u_k, const void* u_v, const int32_t* start_pos,
+                               const int32_t* block_table, int page_size, int num_pages, void* k_s, void* v_s,
+                               void* z_k, void* z_v, void* ws, size_t ws_bytes, lrkv_stream_t stream) {
   if (!dims) return LRKV_ERR_INVALID_ARG;
   const lrkv_dims& d = *dims;
   if (d.batch < 1 || d.heads < 1 || d.head_dim < 1 || d.rank < 0 || d.max_len < 1 || d_model < 1 || n_new < 1)
@@ -222,6 +234,11 @@ extern "C" lrkv_status lrkv_append(const lrkv_dims* dims, int d_model, int n_new
   p.dh = d.head_dim;
   p.hr = hr;
   p.start_pos = start_pos;
+  p.block_table = block_table;
+  p.max_blocks = block_table ? d.max_len / page_size : 0;
+  p.page_shift = 0;
+  while (block_table && (1 << p.page_shift) < page_size) ++p.page_shift;
+  p.num_pages = num_pages;
   p.k_s = static_cast<__nv_bfloat16*>(k_s);
   p.v_s = static_cast<__nv_bfloat16*>(v_s);
   p.z_k = static_cast<__nv_bfloat16*>(z_k);
@@ -247,4 +264,25 @@ extern "C" lrkv_status lrkv_append(const lrkv_dims* dims, int d_model, int n_new
   const dim3 grid((p.N + lrkv::kBN - 1) / lrkv::kBN, (p.M + lrkv::kBM - 1) / lrkv::kBM);
   lrkv::lrkv_append_gemm_kernel<<<grid, 128, smem, s>>>(p, maps);
   return cudaGetLastError() == cudaSuccess ? LRKV_OK : LRKV_ERR_CUDA;
+}
+
+extern "C" lrkv_status lrkv_append(const lrkv_dims* dims, int d_model, int n_new, const void* x,
+                                   const void* w_sk, const void* w_sv, const void* u_k, const void* u_v,
+                                   const int32_t* start_pos, void* k_s, void* v_s, void* z_k, void* z_v,
+                                   void* ws, size_t ws_bytes, lrkv_stream_t stream) {
+  return append_impl(dims, d_model, n_new, x, w_sk, w_sv, u_k, u_v, start_pos, nullptr, 0, 0, k_s, v_s, z_k, z_v,
+                     ws, ws_bytes, stream);
+}
+
+extern "C" lrkv_status lrkv_append_paged(const lrkv_dims* dims, int d_model, int n_new, const void* x,
+                                         const void* w_sk, const void* w_sv, const void* u_k, const void* u_v,
+                                         const int32_t* start_pos, int page_size, int num_pages,
+                                         const int32_t* block_table, void* k_s, void* v_s, void* z_k, void* z_v,
+                                         void* ws, size_t ws_bytes, lrkv_stream_t stream) {
+  if (!dims || !block_table) return LRKV_ERR_INVALID_ARG;
+  if (page_size < 16 || (page_size & (page_size - 1)) != 0 || num_pages < 1) return LRKV_ERR_INVALID_ARG;
+  if (dims->max_len % page_size != 0) return LRKV_ERR_INVALID_ARG;
+  if (static_cast<long long>(num_pages) * page_size > (1LL << 31) - 1) return LRKV_ERR_UNSUPPORTED;
+  return append_impl(dims, d_model, n_new, x, w_sk, w_sv, u_k, u_v, start_pos, block_table, page_size, num_pages,
+                     k_s, v_s, z_k, z_v, ws, ws_bytes, stream);
 }

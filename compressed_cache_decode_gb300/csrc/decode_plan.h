@@ -112,7 +112,8 @@ lrkv_status key_scale_launch(const lrkv_dims& dm, float eps, int n_new, const vo
                              const void* b_k, const int32_t* start_pos, float* key_scale, void* stream);
 lrkv_status step_append_launch(const lrkv_dims& dm, int d_model, const void* x, const void* w_sk,
                                const void* w_sv, const void* u_k, const void* u_v, const int32_t* seq_lens,
-                               void* k_s, void* v_s, void* z_k, void* z_v, int num_sms, void* stream);
+                               void* k_s, void* v_s, void* z_k, void* z_v, int num_sms, void* stream,
+                               const int32_t* block_table = nullptr, int page_size = 0, int num_pages = 0);
 void decode_bind_workspace(DecodePlan& P, void* ws);
 lrkv_status decode_launch(const DecodePlan& P, void* stream, void* ev_begin = nullptr, void* ev_end = nullptr);
 

@@ -37,6 +37,10 @@ struct StepParams {
   const __nv_bfloat16* u_v;                // [H r][d]
   const int32_t* seq_lens;                 // [B], rows [0, seq_lens[b]) incl. the new one
   __nv_bfloat16 *k_s, *v_s, *z_k, *z_v;
+  // paged cache: row t of sequence b is row t & (2^page_shift - 1) of page
+  // block_table[b][t >> page_shift]; NULL: [B][max_len]
+  const int32_t* block_table;
+  int max_blocks, page_shift, num_pages;
 };
 
 __device__ __forceinline__ float dot8(const uint4 w, const uint4 x, float acc) {
@@ -104,8 +108,15 @@ __global__ void __launch_bounds__(kStepThreads) lrkv_append_token_kernel(const S
         const int b = b0 + lane;
         const int pos = p.seq_lens[b] - 1;  // the new token's row (lengths out of range: no row;
                                             // the decode flags them)
-        if (pos >= 0 && pos < p.max_len) {
-          const size_t row = static_cast<size_t>(b) * p.max_len + pos;
+        int pg = b, rw = pos;  // pool page (or sequence) and row of the new token
+        if (p.block_table && pos >= 0 && pos < p.max_len) {
+          pg = p.block_table[static_cast<size_t>(b) * p.max_blocks + (pos >> p.page_shift)];
+          rw = pos & ((1 << p.page_shift) - 1);
+        }
+        // lengths out of range, or a page outside the pool: no row (the decode flags both)
+        if (pos >= 0 && pos < p.max_len && (!p.block_table || (pg >= 0 && pg < p.num_pages))) {
+          const size_t row = p.block_table ? (static_cast<size_t>(pg) << p.page_shift) + rw
+                                           : static_cast<size_t>(b) * p.max_len + pos;
           __nv_bfloat16* dst = n < p.dh ? p.k_s + row * p.dh + n
                                : n < 2 * p.dh ? p.v_s + row * p.dh + (n - p.dh)
                                : n < 2 * p.dh + HR ? p.z_k + row * HR + (n - 2 * p.dh)
@@ -121,8 +132,14 @@ __global__ void __launch_bounds__(kStepThreads) lrkv_append_token_kernel(const S
 // caller's previous work).  Checks were done by the caller.
 lrkv_status step_append_launch(const lrkv_dims& dm, int d_model, const void* x, const void* w_sk,
                                const void* w_sv, const void* u_k, const void* u_v, const int32_t* seq_lens,
-                               void* k_s, void* v_s, void* z_k, void* z_v, int num_sms, void* stream) {
+                               void* k_s, void* v_s, void* z_k, void* z_v, int num_sms, void* stream,
+                               const int32_t* block_table, int page_size, int num_pages) {
   StepParams p;
+  p.block_table = block_table;
+  p.max_blocks = block_table ? dm.max_len / page_size : 0;
+  p.page_shift = 0;
+  while (block_table && (1 << p.page_shift) < page_size) ++p.page_shift;
+  p.num_pages = num_pages;
   p.B = dm.batch; p.H = dm.heads; p.dh = dm.head_dim; p.r = dm.rank; p.d = d_model; p.max_len = dm.max_len;
   const long long row_bytes = static_cast<long long>(d_model) * 2;
   p.bc = static_cast<int>(std::min<long long>(std::min(kStepMaxB, dm.batch), kStepSmem / row_bytes));

@@ -81,6 +81,27 @@ struct PagedCache {
   int page_size, num_pages;
 };
 
+// Sets the paging fields of a plan (checks done by the caller).
+void set_paging(lrkv::DecodePlan& P, const lrkv_dims& d, const PagedCache& pc) {
+  int shift = 0;
+  while ((1 << shift) < pc.page_size) ++shift;
+  P.block_table = pc.block_table;
+  P.max_blocks = d.max_len / pc.page_size;
+  P.page_shift = shift;
+  P.num_pages = pc.num_pages;
+  P.map_len = pc.page_size;
+  P.map_seqs = pc.num_pages;
+}
+
+lrkv_status check_paging(const lrkv_dims* dims, const PagedCache& pc) {
+  if (!dims || !pc.block_table) return LRKV_ERR_INVALID_ARG;
+  if (pc.page_size < 16 || (pc.page_size & (pc.page_size - 1)) != 0 || pc.num_pages < 1) return LRKV_ERR_INVALID_ARG;
+  if (dims->max_len % pc.page_size != 0) return LRKV_ERR_INVALID_ARG;
+  if (static_cast<long long>(pc.num_pages) * pc.page_size > (1LL << 31) - 1) return LRKV_ERR_UNSUPPORTED;
+  return LRKV_OK;
+}
+
+
 lrkv_status decode_common(const lrkv_dims* dims, const void* q, const void* k_s, const void* v_s,
                           const void* z_k, const void* z_v, const void* b_k, const void* b_v,
                           const int32_t* seq_lens, float* out, float* lse, void* ws, size_t ws_bytes,
@@ -102,16 +123,7 @@ lrkv_status decode_common(const lrkv_dims* dims, const void* q, const void* k_s,
   if (ws_bytes < need) return LRKV_ERR_WORKSPACE;
   // post-projection RMSNorm and the paged cache: the streaming scan only
   if ((key_scale || paged) && !P.stream) return LRKV_ERR_UNSUPPORTED;
-  if (paged) {
-    int shift = 0;
-    while ((1 << shift) < paged->page_size) ++shift;
-    P.block_table = paged->block_table;
-    P.max_blocks = dims->max_len / paged->page_size;
-    P.page_shift = shift;
-    P.num_pages = paged->num_pages;
-    P.map_len = paged->page_size;
-    P.map_seqs = paged->num_pages;
-  }
+  if (paged) set_paging(P, *dims, *paged);
   lrkv::decode_bind_workspace(P, ws);
   P.q = q; P.k_s = k_s; P.v_s = v_s; P.z_k = z_k; P.z_v = z_v; P.b_k = b_k; P.b_v = b_v;
   P.seq_lens = seq_lens; P.out = out; P.lse = lse;
@@ -145,12 +157,10 @@ lrkv_status lrkv_decode_paged(const lrkv_dims* dims, int page_size, int num_page
                               const void* q, const void* k_s, const void* v_s, const void* z_k, const void* z_v,
                               const void* b_k, const void* b_v, const int32_t* seq_lens, float* out, float* lse,
                               void* ws, size_t ws_bytes, lrkv_stream_t stream) {
-  if (!dims || !block_table) return LRKV_ERR_INVALID_ARG;
-  if (page_size < 16 || (page_size & (page_size - 1)) != 0 || num_pages < 1) return LRKV_ERR_INVALID_ARG;
-  if (dims->max_len % page_size != 0) return LRKV_ERR_INVALID_ARG;
-  if (static_cast<long long>(num_pages) * page_size > (1LL << 31) - 1) return LRKV_ERR_UNSUPPORTED;
-  if (dims->dtype != LRKV_BF16) return LRKV_ERR_UNSUPPORTED;
   const PagedCache pc{block_table, page_size, num_pages};
+  const lrkv_status st = check_paging(dims, pc);
+  if (st != LRKV_OK) return st;
+  if (dims->dtype != LRKV_BF16) return LRKV_ERR_UNSUPPORTED;
   return decode_common(dims, q, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens, out, lse, ws, ws_bytes, stream, nullptr,
                        nullptr, nullptr, &pc);
 }
@@ -177,11 +187,15 @@ lrkv_status lrkv_decode_normed(const lrkv_dims* dims, const void* q, const void*
                        nullptr, key_scale);
 }
 
-lrkv_status lrkv_decode_step(const lrkv_dims* dims, int d_model, const void* x, const void* w_sk,
-                             const void* w_sv, const void* u_k, const void* u_v, const void* q, void* k_s,
-                             void* v_s, void* z_k, void* z_v, const void* b_k, const void* b_v,
-                             const int32_t* seq_lens, float* out, float* lse, void* ws, size_t ws_bytes,
-                             lrkv_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+lrkv_status decode_step_common(const lrkv_dims* dims, int d_model, const void* x, const void* w_sk,
+                               const void* w_sv, const void* u_k, const void* u_v, const void* q, void* k_s,
+                               void* v_s, void* z_k, void* z_v, const void* b_k, const void* b_v,
+                               const int32_t* seq_lens, float* out, float* lse, void* ws, size_t ws_bytes,
+                               lrkv_stream_t stream, const PagedCache* paged) {
   lrkv_status st = check_decode_dims(dims);
   if (st != LRKV_OK) return st;
   if (dims->dtype != LRKV_BF16 || dims->rank < 1) return LRKV_ERR_UNSUPPORTED;
@@ -200,15 +214,43 @@ lrkv_status lrkv_decode_step(const lrkv_dims* dims, int d_model, const void* x, 
   size_t need = 0;
   if ((st = lrkv::decode_make_plan(*dims, sms, P, &need)) != LRKV_OK) return st;
   if (ws_bytes < need) return LRKV_ERR_WORKSPACE;
+  if (paged && !P.stream) return LRKV_ERR_UNSUPPORTED;
+  if (paged) set_paging(P, *dims, *paged);
   lrkv::decode_bind_workspace(P, ws);
   P.q = q; P.k_s = k_s; P.v_s = v_s; P.z_k = z_k; P.z_v = z_v; P.b_k = b_k; P.b_v = b_v;
   P.seq_lens = seq_lens; P.out = out; P.lse = lse;
   P.after_append = 1;
   // the token's rows first (every host check is done: nothing is enqueued on failure)
   if ((st = lrkv::step_append_launch(*dims, d_model, x, w_sk, w_sv, u_k, u_v, seq_lens, k_s, v_s, z_k, z_v, sms,
-                                     stream)) != LRKV_OK)
+                                     stream, paged ? paged->block_table : nullptr, paged ? paged->page_size : 0,
+                                     paged ? paged->num_pages : 0)) != LRKV_OK)
     return st;
   return lrkv::decode_launch(P, stream, nullptr, nullptr);
+}
+
+}  // namespace
+
+extern "C" {
+
+lrkv_status lrkv_decode_step(const lrkv_dims* dims, int d_model, const void* x, const void* w_sk,
+                             const void* w_sv, const void* u_k, const void* u_v, const void* q, void* k_s,
+                             void* v_s, void* z_k, void* z_v, const void* b_k, const void* b_v,
+                             const int32_t* seq_lens, float* out, float* lse, void* ws, size_t ws_bytes,
+                             lrkv_stream_t stream) {
+  return decode_step_common(dims, d_model, x, w_sk, w_sv, u_k, u_v, q, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens,
+                            out, lse, ws, ws_bytes, stream, nullptr);
+}
+
+lrkv_status lrkv_decode_step_paged(const lrkv_dims* dims, int d_model, const void* x, const void* w_sk,
+                                   const void* w_sv, const void* u_k, const void* u_v, const void* q,
+                                   int page_size, int num_pages, const int32_t* block_table, void* k_s, void* v_s,
+                                   void* z_k, void* z_v, const void* b_k, const void* b_v, const int32_t* seq_lens,
+                                   float* out, float* lse, void* ws, size_t ws_bytes, lrkv_stream_t stream) {
+  const PagedCache pc{block_table, page_size, num_pages};
+  const lrkv_status st = check_paging(dims, pc);
+  if (st != LRKV_OK) return st;
+  return decode_step_common(dims, d_model, x, w_sk, w_sv, u_k, u_v, q, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens,
+                            out, lse, ws, ws_bytes, stream, &pc);
 }
 
 lrkv_status lrkv_read_device_status(const void* ws, lrkv_stream_t stream, lrkv_status* out_status) {

@@ -43,6 +43,8 @@ EXPORTED = (
     "lrkv_decode_normed",
     "lrkv_prefill_normed",
     "lrkv_decode_paged",
+    "lrkv_append_paged",
+    "lrkv_decode_step_paged",
     "lrkv_read_device_status",
 )
 
@@ -115,6 +117,12 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.lrkv_decode_paged.restype = ctypes.c_int
     lib.lrkv_decode_paged.argtypes = [dims_p, ctypes.c_int, ctypes.c_int, i32p, vp, vp, vp, vp, vp, vp, vp, i32p,
                                       vp, vp, vp, sz, vp]
+    lib.lrkv_append_paged.restype = ctypes.c_int
+    lib.lrkv_append_paged.argtypes = [dims_p, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, vp, i32p, ctypes.c_int,
+                                      ctypes.c_int, i32p, vp, vp, vp, vp, vp, sz, vp]
+    lib.lrkv_decode_step_paged.restype = ctypes.c_int
+    lib.lrkv_decode_step_paged.argtypes = [dims_p, ctypes.c_int, vp, vp, vp, vp, vp, vp, ctypes.c_int,
+                                           ctypes.c_int, i32p, vp, vp, vp, vp, vp, vp, i32p, vp, vp, vp, sz, vp]
     lib.lrkv_read_device_status.restype = ctypes.c_int
     lib.lrkv_read_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
     if path is None:
@@ -427,4 +435,47 @@ def decode_paged(q, k_s, v_s, z_k, z_v, b_k, b_v, block_table, seq_lens, scale: 
                            out, lse, ws, ws.numel(), stream)
     if st != LRKV_OK:
         raise LRKVError(st, "lrkv_decode_paged")
+    return out, lse, ws
+
+
+def append_paged(x, w_sk, w_sv, u_k, u_v, start_pos, block_table, k_s, v_s, z_k, z_v, heads: int, ws=None,
+                 stream=None):
+    """The factored rows of x [B, n_new, d_model] into a paged cache (pools
+    k_s, v_s [P, page_size, d_h], z_k, z_v [P, page_size, H, r]) at logical
+    rows start_pos[b] + t; returns the status workspace."""
+    B, n_new, d = x.shape
+    num_pages, page_size, dh = k_s.shape
+    r = z_k.shape[-1]
+    dims = make_dims(B, heads, dh, r, block_table.shape[1] * page_size, x.dtype)
+    if ws is None:
+        ws = torch.zeros(16, dtype=torch.uint8, device=x.device)
+    st = int(load().lrkv_append_paged(ctypes.byref(dims), d, n_new, _ptr(x), _ptr(w_sk), _ptr(w_sv), _ptr(u_k),
+                                      _ptr(u_v), _ptr(start_pos), page_size, num_pages, _ptr(block_table),
+                                      _ptr(k_s), _ptr(v_s), _ptr(z_k), _ptr(z_v), _ptr(ws), ws.numel(),
+                                      _stream_handle(stream)))
+    if st != LRKV_OK:
+        raise LRKVError(st, "lrkv_append_paged")
+    return ws
+
+
+def decode_step_paged(x, w_sk, w_sv, u_k, u_v, q, k_s, v_s, z_k, z_v, b_k, b_v, block_table, seq_lens,
+                      scale: float = 0.0, out=None, lse=None, ws=None, stream=None):
+    """decode_step over a paged cache; returns (out, lse, ws)."""
+    B, H, dh = q.shape
+    num_pages, page_size = k_s.shape[0], k_s.shape[1]
+    r = z_k.shape[-1]
+    dims = make_dims(B, H, dh, r, block_table.shape[1] * page_size, q.dtype, scale)
+    if out is None:
+        out = torch.empty((B, H, dh), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = decode_workspace(dims, q.device)
+    st = int(load().lrkv_decode_step_paged(ctypes.byref(dims), x.shape[-1], _ptr(x), _ptr(w_sk), _ptr(w_sv),
+                                           _ptr(u_k), _ptr(u_v), _ptr(q), page_size, num_pages,
+                                           _ptr(block_table), _ptr(k_s), _ptr(v_s), _ptr(z_k), _ptr(z_v),
+                                           _ptr(b_k), _ptr(b_v), _ptr(seq_lens), _ptr(out), _ptr(lse), _ptr(ws),
+                                           ws.numel(), _stream_handle(stream)))
+    if st != LRKV_OK:
+        raise LRKVError(st, "lrkv_decode_step_paged")
     return out, lse, ws

@@ -324,6 +324,30 @@ lrkv_status lrkv_decode_paged(const lrkv_dims* dims, int page_size, int num_page
                               void* ws, size_t ws_bytes, lrkv_stream_t stream);
 
 /*
+ * Appends into a paged cache (pools, block table and page_size as in
+ * lrkv_decode_paged): after a prefill, at any position, across page
+ * boundaries.
+ *
+ * lrkv_append_paged is lrkv_append writing logical row start_pos[b] + t of
+ * sequence b through the block table; a row whose block names no page of the
+ * pool is not written and sets LRKV_ERR_DEVICE_BOUNDS in the status word
+ * (as a row past max_len does).
+ *
+ * lrkv_decode_step_paged is lrkv_decode_step over a paged cache: the token's
+ * rows go to logical row seq_lens[b] - 1 through the block table (a page
+ * outside the pool: no row; the decode flags it), then lrkv_decode_paged.
+ */
+lrkv_status lrkv_append_paged(const lrkv_dims* dims, int d_model, int n_new, const void* x, const void* w_sk,
+                              const void* w_sv, const void* u_k, const void* u_v, const int32_t* start_pos,
+                              int page_size, int num_pages, const int32_t* block_table, void* k_s, void* v_s,
+                              void* z_k, void* z_v, void* ws, size_t ws_bytes, lrkv_stream_t stream);
+lrkv_status lrkv_decode_step_paged(const lrkv_dims* dims, int d_model, const void* x, const void* w_sk,
+                                   const void* w_sv, const void* u_k, const void* u_v, const void* q,
+                                   int page_size, int num_pages, const int32_t* block_table, void* k_s, void* v_s,
+                                   void* z_k, void* z_v, const void* b_k, const void* b_v, const int32_t* seq_lens,
+                                   float* out, float* lse, void* ws, size_t ws_bytes, lrkv_stream_t stream);
+
+/*
  * Read the device status word that the kernels of the last call(s) using
  * `ws` recorded (LRKV_OK, LRKV_ERR_TIMEOUT or LRKV_ERR_DEVICE_BOUNDS).
  * Synchronises `stream`.  Each lrkv_decode/lrkv_prefill call sets the word
