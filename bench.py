@@ -665,6 +665,47 @@ def main():
                       "gbs": job_gbs(total_bytes + scale_bytes, world, n_ms),
                       "key_scale_bytes": scale_bytes}
 
+    # decode over a paged cache: the same rows in 256-row pages of a pool, in a
+    # seeded random page order, through a block table
+    paged_leg = None
+    if not a.no_graph:
+        page = 256
+        pc = inputs.paged_from_contiguous(case, page_size=page, seed=7)
+        pd = {k: v.to(dev) for k, v in pc.items()}
+        preps = [pd] + [{k: (v.clone() if k in ("k_s", "v_s", "z_k", "z_v") else v) for k, v in pd.items()}
+                        for _ in range(n_rep - 1)]
+        n_pages = pd["k_s"].shape[0]
+
+        def pstep(i, s=None):
+            x = preps[i % n_rep]
+            st = lrkv.lrkv_decode_paged(dims, page, n_pages, x["block_table"], x["q"], x["k_s"], x["v_s"],
+                                        x["z_k"], x["z_v"], x["b_k"], x["b_v"], x["seq_lens"], out, lse, ws,
+                                        ws.numel(), s or stream)
+            if st != lrkv.LRKV_OK:
+                raise lrkv.LRKVError(st, "lrkv_decode_paged")
+
+        with torch.cuda.stream(stream):
+            for i in range(W):
+                pstep(i)
+        torch.cuda.synchronize()
+        pg_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(pg_graph, stream=stream, capture_error_mode="thread_local"):
+            for i in range(K):
+                pstep(i, torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        pg_graph.replay()
+        torch.cuda.synchronize()
+        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            p0.record(stream)
+            pg_graph.replay()
+            p1.record(stream)
+        torch.cuda.synchronize()
+        p_ms = max_over_ranks(p0.elapsed_time(p1) / K, world, dev)
+        paged_leg = {"page_size": page, "pages": n_pages, "ms_per_step": p_ms, "decode_ms_per_step": ms_step,
+                     "gbs": job_gbs(total_bytes, world, p_ms)}
+        del preps, pd
+
     prefill = None
     if not a.no_prefill:
         prefill = prefill_leg(dev)
@@ -714,6 +755,7 @@ def main():
             "clocks": clk.summary(),
             "decode_step": step_leg,
             "decode_normed": normed_leg,
+            "decode_paged": paged_leg,
             "prefill": prefill,
         }
         print(json.dumps(res), flush=True)
