@@ -66,6 +66,11 @@ struct PrefillParams {
   float scale_log2;
   const int32_t* seq_lens;
   const float* key_scale;  // [B][H][max_len] reciprocal key RMS, or NULL
+  // paged cache: row t of sequence b is row t & (2^page_shift - 1) of page
+  // block_table[b][t >> page_shift] (page_size >= 128: a key tile never spans
+  // two pages); NULL: [B][max_len]
+  const int32_t* block_table;
+  int max_blocks, page_shift, num_pages;
   float* out;
   float* lse;
   uint32_t* status;
@@ -73,10 +78,10 @@ struct PrefillParams {
 
 struct PrefillMaps {
   CUtensorMap q;    // {64, Tq, 2, H, B}
-  CUtensorMap ks;   // {64, max_len, 2, B}
-  CUtensorMap vs;   // {64, max_len, 2, B}
-  CUtensorMap zk;   // {r, H, max_len, B}
-  CUtensorMap zv;   // {r, H, max_len, B}
+  CUtensorMap ks;   // {64, rows, 2, seqs}: (rows, seqs) = (max_len, B), or (page_size, pages)
+  CUtensorMap vs;   // {64, rows, 2, seqs}
+  CUtensorMap zk;   // {r, H, rows, seqs}
+  CUtensorMap zv;   // {r, H, rows, seqs}
   CUtensorMap bk;   // {r, dh, H}
   CUtensorMap bv;   // {r, dh, H}
 };
@@ -218,6 +223,19 @@ __device__ __forceinline__ void st_global_v8(float* dst, const float (&v)[8]) {
 
 }  // namespace
 
+// Tensor-map (sequence or page, row) of key tile row `row` of sequence b; a
+// page outside the pool is recorded (its copy reads zeros).
+__device__ __forceinline__ int kv_seq(const PrefillParams& p, int b, int row, int& r_out) {
+  if (!p.block_table) {
+    r_out = row;
+    return b;
+  }
+  const int pg = __ldg(p.block_table + static_cast<size_t>(b) * p.max_blocks + (row >> p.page_shift));
+  r_out = row & ((1 << p.page_shift) - 1);
+  if (pg < 0 || pg >= p.num_pages) atomicOr(p.status, 2u);
+  return pg;
+}
+
 // KS: the scores are multiplied by the keys' cached RMSNorm scales
 template <bool KS>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -253,8 +271,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_5d(smem + kOffQ, &maps.q, 0, it.q0, 0, it.h, it.b, &bar_q);
       tma_load_3d(smem + kOffV + kKStage, &maps.bk, 0, 0, it.h, &bar_q);
       mbar_arrive_expect_tx(&bar_k0, kKStage);
-      tma_load_4d(smem + kOffK, &maps.ks, 0, 0, 0, it.b, &bar_k0);
-      tma_load_4d(smem + kOffK + 32768, &maps.zk, 0, it.h, 0, it.b, &bar_k0);
+      int r0;
+      const int s0 = kv_seq(p, it.b, 0, r0);
+      tma_load_4d(smem + kOffK, &maps.ks, 0, r0, 0, s0, &bar_k0);
+      tma_load_4d(smem + kOffK + 32768, &maps.zk, 0, it.h, r0, s0, &bar_k0);
     }
   }
   if (warp == 0) tmem_alloc(&tmem_base, 512);
@@ -280,13 +300,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       auto load_k = [&](int j, const Item& w, int kt, uint64_t* bar) {
         unsigned char* dst = smem + kOffK + (j & 1) * kKStage;
-        tma_load_4d(dst, &maps.ks, 0, kt * kBK, 0, w.b, bar);
-        tma_load_4d(dst + 32768, &maps.zk, 0, w.h, kt * kBK, w.b, bar);
+        int rw;
+        const int sq = kv_seq(p, w.b, kt * kBK, rw);
+        tma_load_4d(dst, &maps.ks, 0, rw, 0, sq, bar);
+        tma_load_4d(dst + 32768, &maps.zk, 0, w.h, rw, sq, bar);
       };
       auto load_v = [&](int j, const Item& w, int kt, uint64_t* bar) {
         unsigned char* dst = smem + kOffV + (j & 1) * kKStage;
-        tma_load_4d(dst, &maps.vs, 0, kt * kBK, 0, w.b, bar);
-        tma_load_4d(dst + 32768, &maps.zv, 0, w.h, kt * kBK, w.b, bar);
+        int rw;
+        const int sq = kv_seq(p, w.b, kt * kBK, rw);
+        tma_load_4d(dst, &maps.vs, 0, rw, 0, sq, bar);
+        tma_load_4d(dst + 32768, &maps.zv, 0, w.h, rw, sq, bar);
       };
       bool ok = true;
       int J = 0;  // this item's first tile
@@ -658,7 +682,8 @@ bool make_map(CUtensorMap* m, const void* base, int n, const uint64_t* dims, con
 static lrkv_status prefill_impl(const lrkv_dims* dims, int q_len, const void* q, const void* k_s,
                                 const void* v_s, const void* z_k, const void* z_v, const void* b_k,
                                 const void* b_v, const float* key_scale, const int32_t* seq_lens, float* out,
-                                float* lse, void* ws, size_t ws_bytes, lrkv_stream_t stream) {
+                                float* lse, void* ws, size_t ws_bytes, lrkv_stream_t stream,
+                                const int32_t* block_table = nullptr, int page_size = 0, int num_pages = 0) {
   if (!dims) return LRKV_ERR_INVALID_ARG;
   const lrkv_dims& d = *dims;
   if (d.batch < 1 || d.heads < 1 || d.head_dim < 1 || d.rank < 0 || d.max_len < 1 || q_len < 1)
@@ -674,6 +699,9 @@ static lrkv_status prefill_impl(const lrkv_dims* dims, int q_len, const void* q,
 
   const int B = d.batch, H = d.heads, Lm = d.max_len;
   const uint64_t dh = 128, r = 64;
+  // tensor-map extents of the cache: (rows, sequences), or (page_size, pages) for a paged cache
+  const uint64_t rows = static_cast<uint64_t>(block_table ? page_size : Lm);
+  const uint64_t seqs = static_cast<uint64_t>(block_table ? num_pages : B);
   lrkv::PrefillMaps maps;
   std::memset(&maps, 0, sizeof(maps));
   {
@@ -686,14 +714,15 @@ static lrkv_status prefill_impl(const lrkv_dims* dims, int q_len, const void* q,
   }
   {
     // k_s, v_s [B][max_len][128] seen as {64 columns, max_len, 2 halves, B}
-    const uint64_t dm[4] = {64, static_cast<uint64_t>(Lm), 2, static_cast<uint64_t>(B)};
-    const uint64_t st[3] = {dh * 2, 128, static_cast<uint64_t>(Lm) * dh * 2};
+    // (paged: [pages][page_size][128] as {64, page_size, 2, pages})
+    const uint64_t dm[4] = {64, rows, 2, seqs};
+    const uint64_t st[3] = {dh * 2, 128, rows * dh * 2};
     const uint32_t bx[4] = {64, 128, 2, 1};
     if (!make_map(&maps.ks, k_s, 4, dm, st, bx) || !make_map(&maps.vs, v_s, 4, dm, st, bx)) return LRKV_ERR_CUDA;
   }
   {
-    const uint64_t dm[4] = {r, static_cast<uint64_t>(H), static_cast<uint64_t>(Lm), static_cast<uint64_t>(B)};
-    const uint64_t st[3] = {r * 2, H * r * 2, static_cast<uint64_t>(Lm) * H * r * 2};
+    const uint64_t dm[4] = {r, static_cast<uint64_t>(H), rows, seqs};
+    const uint64_t st[3] = {r * 2, H * r * 2, rows * H * r * 2};
     const uint32_t bx[4] = {64, 1, 128, 1};
     if (!make_map(&maps.zk, z_k, 4, dm, st, bx) || !make_map(&maps.zv, z_v, 4, dm, st, bx)) return LRKV_ERR_CUDA;
   }
@@ -710,6 +739,11 @@ static lrkv_status prefill_impl(const lrkv_dims* dims, int q_len, const void* q,
   p.scale_log2 = scale * lrkv::kPfLog2e;
   p.seq_lens = seq_lens; p.out = out; p.lse = lse;
   p.key_scale = key_scale;
+  p.block_table = block_table;
+  p.max_blocks = block_table ? Lm / page_size : 0;
+  p.page_shift = 0;
+  while (block_table && (1 << p.page_shift) < page_size) ++p.page_shift;
+  p.num_pages = num_pages;
   auto kern = key_scale ? lrkv::lrkv_prefill_kernel<true> : lrkv::lrkv_prefill_kernel<false>;
   p.out_v8 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
   p.status = static_cast<uint32_t*>(ws);
@@ -750,4 +784,17 @@ extern "C" lrkv_status lrkv_prefill_normed(const lrkv_dims* dims, int q_len, con
   if (!key_scale) return LRKV_ERR_INVALID_ARG;
   return prefill_impl(dims, q_len, q, k_s, v_s, z_k, z_v, b_k, b_v, key_scale, seq_lens, out, lse, ws, ws_bytes,
                       stream);
+}
+
+extern "C" lrkv_status lrkv_prefill_paged(const lrkv_dims* dims, int q_len, const void* q, int page_size,
+                                          int num_pages, const int32_t* block_table, const void* k_s,
+                                          const void* v_s, const void* z_k, const void* z_v, const void* b_k,
+                                          const void* b_v, const int32_t* seq_lens, float* out, float* lse,
+                                          void* ws, size_t ws_bytes, lrkv_stream_t stream) {
+  if (!dims || !block_table) return LRKV_ERR_INVALID_ARG;
+  if (page_size < 128 || (page_size & (page_size - 1)) != 0 || num_pages < 1) return LRKV_ERR_INVALID_ARG;
+  if (dims->max_len % page_size != 0) return LRKV_ERR_INVALID_ARG;
+  if (static_cast<long long>(num_pages) * page_size > (1LL << 31) - 1) return LRKV_ERR_UNSUPPORTED;
+  return prefill_impl(dims, q_len, q, k_s, v_s, z_k, z_v, b_k, b_v, nullptr, seq_lens, out, lse, ws, ws_bytes,
+                      stream, block_table, page_size, num_pages);
 }

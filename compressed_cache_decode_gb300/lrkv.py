@@ -45,6 +45,7 @@ EXPORTED = (
     "lrkv_decode_paged",
     "lrkv_append_paged",
     "lrkv_decode_step_paged",
+    "lrkv_prefill_paged",
     "lrkv_read_device_status",
 )
 
@@ -123,6 +124,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.lrkv_decode_step_paged.restype = ctypes.c_int
     lib.lrkv_decode_step_paged.argtypes = [dims_p, ctypes.c_int, vp, vp, vp, vp, vp, vp, ctypes.c_int,
                                            ctypes.c_int, i32p, vp, vp, vp, vp, vp, vp, i32p, vp, vp, vp, sz, vp]
+    lib.lrkv_prefill_paged.restype = ctypes.c_int
+    lib.lrkv_prefill_paged.argtypes = [dims_p, ctypes.c_int, vp, ctypes.c_int, ctypes.c_int, i32p, vp, vp, vp, vp,
+                                       vp, vp, i32p, vp, vp, vp, sz, vp]
     lib.lrkv_read_device_status.restype = ctypes.c_int
     lib.lrkv_read_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
     if path is None:
@@ -478,4 +482,28 @@ def decode_step_paged(x, w_sk, w_sv, u_k, u_v, q, k_s, v_s, z_k, z_v, b_k, b_v, 
                                            ws.numel(), _stream_handle(stream)))
     if st != LRKV_OK:
         raise LRKVError(st, "lrkv_decode_step_paged")
+    return out, lse, ws
+
+
+def prefill_paged(q, k_s, v_s, z_k, z_v, b_k, b_v, block_table, seq_lens, scale: float = 0.0, out=None, lse=None,
+                  ws=None, stream=None):
+    """Causal prefill of q [B, q_len, H, d_h] over a paged cache (pools k_s,
+    v_s [P, page_size, d_h], z_k, z_v [P, page_size, H, r]); returns
+    (out, lse, status workspace)."""
+    B, Tq, H, dh = q.shape
+    num_pages, page_size = k_s.shape[0], k_s.shape[1]
+    r = z_k.shape[-1]
+    dims = make_dims(B, H, dh, r, block_table.shape[1] * page_size, q.dtype, scale)
+    if out is None:
+        out = torch.empty((B, Tq, H, dh), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, Tq), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = torch.zeros(16, dtype=torch.uint8, device=q.device)
+    st = int(load().lrkv_prefill_paged(ctypes.byref(dims), Tq, _ptr(q), page_size, num_pages, _ptr(block_table),
+                                       _ptr(k_s), _ptr(v_s), _ptr(z_k), _ptr(z_v), _ptr(b_k), _ptr(b_v),
+                                       _ptr(seq_lens), _ptr(out), _ptr(lse), _ptr(ws), ws.numel(),
+                                       _stream_handle(stream)))
+    if st != LRKV_OK:
+        raise LRKVError(st, "lrkv_prefill_paged")
     return out, lse, ws

@@ -337,6 +337,19 @@ lrkv_status lrkv_decode_paged(const lrkv_dims* dims, int page_size, int num_page
  * rows go to logical row seq_lens[b] - 1 through the block table (a page
  * outside the pool: no row; the decode flags it), then lrkv_decode_paged.
  */
+/*
+ * Causal prefill over a paged cache (pools, block table as in
+ * lrkv_decode_paged): lrkv_prefill over the logical rows [0, seq_lens[b]);
+ * the chunk's own rows are appended first (lrkv_append_paged), the rows
+ * before them are the cached prefix.  page_size: a power of two >= 128 (a
+ * 128-key tile never spans two pages).  A block table entry outside the pool
+ * reads as zero rows and sets LRKV_ERR_DEVICE_BOUNDS.  Supported: the shapes
+ * of lrkv_prefill.
+ */
+lrkv_status lrkv_prefill_paged(const lrkv_dims* dims, int q_len, const void* q, int page_size, int num_pages,
+                               const int32_t* block_table, const void* k_s, const void* v_s, const void* z_k,
+                               const void* z_v, const void* b_k, const void* b_v, const int32_t* seq_lens,
+                               float* out, float* lse, void* ws, size_t ws_bytes, lrkv_stream_t stream);
 lrkv_status lrkv_append_paged(const lrkv_dims* dims, int d_model, int n_new, const void* x, const void* w_sk,
                               const void* w_sv, const void* u_k, const void* u_v, const int32_t* start_pos,
                               int page_size, int num_pages, const int32_t* block_table, void* k_s, void* v_s,

@@ -388,3 +388,12 @@ def decode_reference_paged(q, k_s, v_s, z_k, z_v, b_k, b_v, block_table, page_si
     max_len = np.asarray(block_table).shape[1] * page_size
     g = [gather_paged(t, block_table, page_size, max_len) for t in (k_s, v_s, z_k, z_v)]
     return decode_reference(q, g[0], g[1], g[2], g[3], b_k, b_v, seq_lens, scale=scale, pairs=pairs)
+
+
+def prefill_reference_paged(q, k_s, v_s, z_k, z_v, b_k, b_v, block_table, page_size: int, seq_lens,
+                            scale: Optional[float] = None, pairs: Optional[Iterable[Tuple[int, int]]] = None,
+                            rows: Optional[Sequence[int]] = None):
+    """prefill_reference over the logical rows of a paged cache."""
+    max_len = np.asarray(block_table).shape[1] * page_size
+    g = [gather_paged(t, block_table, page_size, max_len) for t in (k_s, v_s, z_k, z_v)]
+    return prefill_reference(q, g[0], g[1], g[2], g[3], b_k, b_v, seq_lens, scale=scale, pairs=pairs, rows=rows)

@@ -151,3 +151,7 @@ def test_paged_decode_rejects_bad_paging_without_gpu(lib):
     f32 = lrkv.make_dims(2, 16, 64, 28, 256, None)
     f32.dtype = lrkv.LRKV_F32
     assert call(ctypes.byref(f32), 64, 8, fake, *rest) == lrkv.LRKV_ERR_UNSUPPORTED   # bf16 streaming only
+    pre = lrkv.make_dims(1, 2, 128, 64, 512, "bf16")
+    prest = (fake,) * 6 + (fake, fake, fake, fake, 1 << 20, None)  # k_s .. b_v, seq_lens, out, lse, ws, bytes, stream
+    assert lib.lrkv_prefill_paged(ctypes.byref(pre), 128, fake, 64, 8, fake, *prest) == \
+        lrkv.LRKV_ERR_INVALID_ARG                                                     # a key tile spans pages

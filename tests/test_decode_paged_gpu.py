@@ -1,4 +1,4 @@
-"""Decode over a paged factored cache against the fp64 oracle: the cache rows
+"""Decode and causal prefill over a paged factored cache against the fp64 oracle: the cache rows
 of every sequence sit in pages of a shared pool in a seeded random order
 (unused pages and rows hold NaN), a block table maps each sequence's blocks;
 the result must match the decode over the logical rows and the
@@ -69,3 +69,28 @@ def test_paged_decode_flags_a_page_outside_the_pool():
     ref_o, ref_l = O.decode_reference(paged["q"][:1], case["k_s"][:1], case["v_s"][:1], case["z_k"][:1],
                                       case["z_v"][:1], case["b_k"], case["b_v"], case["seq_lens"][:1])
     assert_decode_close(out[:1].cpu().numpy(), lse[:1].cpu().numpy(), ref_o, ref_l, "bf16", what="valid sequence")
+
+
+@pytest.mark.parametrize("shape", [
+    # B, q_len, H, page_size, max_len, lengths
+    (2, 200, 3, 128, 512, [200, 450]),        # a prefix of 250 cached rows before the second chunk
+    (1, 128, 2, 256, 512, [384]),             # the chunk starts on a page boundary
+    (2, 512, 40, 128, 768, [512, 700]),       # more items than SMs
+])
+def test_paged_prefill_matches_oracle(shape):
+    B, Tq, H, ps, Lm, lens = shape
+    case = inputs.random_prefill_case(seed=B * 3 + Tq, batch=B, q_len=Tq, heads=H, head_dim=128, rank=64,
+                                      max_len=Lm, lens=lens)
+    paged = inputs.paged_from_contiguous(case, page_size=ps, seed=Tq + ps)
+    d = {k: v.cuda() for k, v in paged.items()}
+    out, lse, ws = lrkv.prefill_paged(d["q"], d["k_s"], d["v_s"], d["z_k"], d["z_v"], d["b_k"], d["b_v"],
+                                      d["block_table"], d["seq_lens"])
+    torch.cuda.synchronize()
+    assert lrkv.lrkv_read_device_status(ws) == lrkv.LRKV_OK
+    ref_o, ref_l = O.prefill_reference_paged(paged["q"], paged["k_s"], paged["v_s"], paged["z_k"], paged["z_v"],
+                                             paged["b_k"], paged["b_v"], paged["block_table"], ps,
+                                             paged["seq_lens"])
+    o, l_ = out.cpu().numpy(), lse.cpu().numpy()
+    assert_decode_close(o.reshape(-1, o.shape[-1]), l_.transpose(0, 2, 1).reshape(-1),
+                        ref_o.reshape(-1, ref_o.shape[-1]), ref_l.transpose(0, 2, 1).reshape(-1), "bf16",
+                        what=f"paged prefill {shape}")
