@@ -37,6 +37,7 @@
 
 #include "decode_common.cuh"
 #include "decode_plan.h"
+#include "host_cache.h"
 #include "ptx.cuh"
 #include "tmap.h"
 
@@ -819,14 +820,10 @@ lrkv_status launch_all(const DecodePlan& P, cudaStream_t stream, cudaEvent_t ev_
   if (P.stream) {
     // the small kernels around the scan ask for the same L1/shared split as
     // the scan, so the SMs need no reconfiguration between the launches
-    static bool carve_set = false;
-    if (!carve_set) {
-      cudaFuncSetAttribute(lrkv_decode_absorb_kernel<BF16>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                           cudaSharedmemCarveoutMaxShared);
-      cudaFuncSetAttribute(combine_fn<BF16>(P), cudaFuncAttributePreferredSharedMemoryCarveout,
-                           cudaSharedmemCarveoutMaxShared);
-      carve_set = true;
-    }
+    if (ensure_kernel_smem(reinterpret_cast<const void*>(lrkv_decode_absorb_kernel<BF16>), 0, true) !=
+            cudaSuccess ||
+        ensure_kernel_smem(reinterpret_cast<const void*>(combine_fn<BF16>(P)), 0, true) != cudaSuccess)
+      return LRKV_ERR_CUDA;
   }
   if (absorb_smem > 48 * 1024 &&
       cudaFuncSetAttribute(lrkv_decode_absorb_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,

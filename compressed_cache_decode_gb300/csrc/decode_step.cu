@@ -17,6 +17,7 @@
 #include <algorithm>
 #include <cstdint>
 
+#include "host_cache.h"
 #include "lrkv.h"
 #include "ptx.cuh"
 
@@ -151,13 +152,8 @@ lrkv_status step_append_launch(const lrkv_dims& dm, int d_model, const void* x, 
   p.k_s = static_cast<__nv_bfloat16*>(k_s); p.v_s = static_cast<__nv_bfloat16*>(v_s);
   p.z_k = static_cast<__nv_bfloat16*>(z_k); p.z_v = static_cast<__nv_bfloat16*>(z_v);
   const int smem = static_cast<int>(p.bc * row_bytes);
-  static int have = 0;
-  if (smem > 48 * 1024 && smem > have) {
-    if (cudaFuncSetAttribute(lrkv_append_token_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-        cudaSuccess)
-      return LRKV_ERR_CUDA;
-    have = smem;
-  }
+  if (ensure_kernel_smem(reinterpret_cast<const void*>(lrkv_append_token_kernel), smem) != cudaSuccess)
+    return LRKV_ERR_CUDA;
   // one warp per output column, at most one CTA per SM
   const long long N = 2ll * dm.head_dim + 2ll * dm.heads * dm.rank;
   const long long wpc = kStepThreads / 32;

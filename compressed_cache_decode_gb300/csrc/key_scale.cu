@@ -18,6 +18,7 @@
 
 #include <cstdint>
 
+#include "host_cache.h"
 #include "lrkv.h"
 #include "ptx.cuh"
 
@@ -160,13 +161,8 @@ lrkv_status key_scale_launch(const lrkv_dims& dm, float eps, int n_new, const vo
   p.start_pos = start_pos;
   p.key_scale = key_scale;
   const int smem = ((dm.head_dim + kKsTok) * p.zs + kKsTok * dm.head_dim) * 2;
-  static int have = 0;
-  if (smem > 48 * 1024 && smem > have) {
-    if (cudaFuncSetAttribute(lrkv_key_scale_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-        cudaSuccess)
-      return LRKV_ERR_CUDA;
-    have = smem;
-  }
+  if (ensure_kernel_smem(reinterpret_cast<const void*>(lrkv_key_scale_kernel), smem) != cudaSuccess)
+    return LRKV_ERR_CUDA;
   const dim3 grid((n_new + kKsTok - 1) / kKsTok, dm.heads, dm.batch);
   lrkv_key_scale_kernel<<<grid, kKsThreads, smem, static_cast<cudaStream_t>(stream)>>>(p);
   return cudaGetLastError() == cudaSuccess ? LRKV_OK : LRKV_ERR_CUDA;

@@ -34,6 +34,7 @@
 #include <cmath>
 #include <cstring>
 
+#include "host_cache.h"
 #include "lrkv.h"
 #include "ptx.cuh"
 #include "tmap.h"
@@ -750,17 +751,12 @@ static lrkv_status prefill_impl(const lrkv_dims* dims, int q_len, const void* q,
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(ws, 0, 4, s) != cudaSuccess) return LRKV_ERR_CUDA;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, lrkv::kSmem) !=
-      cudaSuccess)
+  if (lrkv::ensure_kernel_smem(reinterpret_cast<const void*>(kern), lrkv::kSmem) != cudaSuccess)
     return LRKV_ERR_CUDA;
   // persistent: one CTA per SM (the kernel deals the (sequence, head, query
   // tile) items out itself)
-  static int nsm = 0;
-  if (nsm == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return LRKV_ERR_CUDA;
-  }
+  const int nsm = lrkv::device_sm_count();
+  if (nsm < 1) return LRKV_ERR_CUDA;
   const long long items = static_cast<long long>((q_len + lrkv::kBQ - 1) / lrkv::kBQ) * H * B;
   if (items > (1ll << 30)) return LRKV_ERR_UNSUPPORTED;
   const int grid = static_cast<int>(std::min<long long>(nsm, items));
