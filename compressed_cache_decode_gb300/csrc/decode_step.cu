@@ -26,11 +26,13 @@ namespace lrkv {
 namespace {
 
 constexpr int kStepThreads = 256;
-constexpr int kStepMaxB = 16;              // sequences per pass over the weights
-constexpr int kStepSmem = 192 * 1024;      // x rows of one pass
+constexpr int kStepWarps = kStepThreads / 32;
+constexpr int kStepSmem = 200 * 1024;      // x rows of one pass + the warps' first weight rows
+constexpr int kStepWRows = 64 * 1024;      // weight rows staged when 8 of them fit here
 
 struct StepParams {
   int B, H, dh, r, d, max_len, bc;
+  int wstage;                              // the warps' first weight rows staged in shared memory
   const __nv_bfloat16* x;                  // [B][d]
   const __nv_bfloat16* w_sk;               // [dh][d]
   const __nv_bfloat16* w_sv;               // [dh][d]
@@ -52,24 +54,65 @@ __device__ __forceinline__ float dot8(const uint4 w, const uint4 x, float acc) {
   return acc;
 }
 
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(src) : "memory");
+}
+
+// Warp sums of M values per lane (M a power of two <= 32) by halving
+// exchanges: after log2(M) steps each lane holds one partially summed value,
+// whose index is given by the lane bits 16, 8, ...; the remaining lane bits
+// are summed by xor shuffles.  Returns the full sum of value `idx` (every
+// lane holds one; the lanes with the same idx hold the same sum).
+template <int M>
+__device__ __forceinline__ float warp_sums(float (&v)[M], int lane, int& idx) {
+  int off = 16;
+  idx = 0;
+#pragma unroll
+  for (int half = M / 2; half >= 1; half /= 2) {
+    const bool up = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = up ? v[i] : v[i + half];
+      const float keep = up ? v[i + half] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+    if (up) idx += half;
+    off >>= 1;
+  }
+  float s = v[0];
+  for (; off >= 1; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  return s;
+}
+
 }  // namespace
 
+// M: sequences per pass over the weights (8 or 16)
+template <int M>
 __global__ void __launch_bounds__(kStepThreads) lrkv_append_token_kernel(const StepParams p) {
   extern __shared__ __align__(16) unsigned char sx_raw[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int wpc = blockDim.x >> 5;
-  const int nwarps = gridDim.x * wpc, gw = blockIdx.x * wpc + warp;
+  const int nwarps = gridDim.x * kStepWarps, gw = blockIdx.x * kStepWarps + warp;
   const int HR = p.H * p.r, N = 2 * p.dh + 2 * HR;
   const int chunks = p.d / 8;  // 16-byte chunks per row
+  uint4* xs = reinterpret_cast<uint4*>(sx_raw);                    // [bc][chunks]
+  uint4* wsm = xs + static_cast<size_t>(p.bc) * chunks + warp * chunks;  // this warp's first row
   auto weight_row = [&](int n) {
     return n < p.dh ? p.w_sk + static_cast<size_t>(n) * p.d
            : n < 2 * p.dh ? p.w_sv + static_cast<size_t>(n - p.dh) * p.d
            : n < 2 * p.dh + HR ? p.u_k + static_cast<size_t>(n - 2 * p.dh) * p.d
                                : p.u_v + static_cast<size_t>(n - 2 * p.dh - HR) * p.d;
   };
-  // this warp's weight rows start moving into L2 while the launch before
-  // finishes (a prefetch reads nothing that could be stale: L2 is coherent)
-  for (int n = gw; n < N; n += nwarps) {
+  // The weights are inputs of the call (no launch before writes them): the
+  // warp's first column's row is copied into shared memory while the launch
+  // before finishes, and its later columns start moving into L2 (a prefetch
+  // reads nothing that could be stale: L2 is coherent).
+  const bool staged = p.wstage && gw < N;
+  if (staged) {
+    const uint4* wv = reinterpret_cast<const uint4*>(weight_row(gw));
+    for (int c = lane; c < chunks; c += 32) cp_async16(wsm + c, wv + c);
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  for (int n = gw + (staged ? nwarps : 0); n < N; n += nwarps) {
     const char* row = reinterpret_cast<const char*>(weight_row(n));
     for (int off = lane * 128; off < p.d * 2; off += 32 * 128)
       asm volatile("prefetch.global.L2 [%0];" ::"l"(row + off));
@@ -79,34 +122,28 @@ __global__ void __launch_bounds__(kStepThreads) lrkv_append_token_kernel(const S
   // may also write; it waits for this grid before it reads the cache)
   pdl_wait();
   pdl_trigger();
-  uint4* xs = reinterpret_cast<uint4*>(sx_raw);
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
   for (int b0 = 0; b0 < p.B; b0 += p.bc) {
     const int nb = min(p.bc, p.B - b0);
-    __syncthreads();  // the previous pass is done with xs
+    __syncthreads();  // the previous pass is done with xs (first pass: the staged rows are in)
     const uint4* xg = reinterpret_cast<const uint4*>(p.x) + static_cast<size_t>(b0) * chunks;
     for (int i = tid; i < nb * chunks; i += blockDim.x) xs[i] = xg[i];
     __syncthreads();
     for (int n = gw; n < N; n += nwarps) {
-      const uint4* wv = reinterpret_cast<const uint4*>(weight_row(n));
-      float acc[kStepMaxB];
+      const uint4* wv = (staged && n == gw) ? wsm : reinterpret_cast<const uint4*>(weight_row(n));
+      float acc[M];
 #pragma unroll
-      for (int b = 0; b < kStepMaxB; ++b) acc[b] = 0.f;
+      for (int b = 0; b < M; ++b) acc[b] = 0.f;
       for (int c = lane; c < chunks; c += 32) {
-        const uint4 w = __ldg(wv + c);
+        const uint4 w = wv[c];
 #pragma unroll
-        for (int b = 0; b < kStepMaxB; ++b)
+        for (int b = 0; b < M; ++b)
           if (b < nb) acc[b] = dot8(w, xs[b * chunks + c], acc[b]);
       }
-      float mine = 0.f;  // lane b keeps the total of sequence b0 + b
-#pragma unroll
-      for (int b = 0; b < kStepMaxB; ++b) {
-        float v = acc[b];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == b) mine = v;
-      }
-      if (lane < nb) {
-        const int b = b0 + lane;
+      int idx;
+      const float tot = warp_sums<M>(acc, lane, idx);  // sequence b0 + idx
+      if ((lane & (32 / M - 1)) == 0 && idx < nb) {
+        const int b = b0 + idx;
         const int pos = p.seq_lens[b] - 1;  // the new token's row (lengths out of range: no row;
                                             // the decode flags them)
         int pg = b, rw = pos;  // pool page (or sequence) and row of the new token
@@ -122,7 +159,7 @@ __global__ void __launch_bounds__(kStepThreads) lrkv_append_token_kernel(const S
                                : n < 2 * p.dh ? p.v_s + row * p.dh + (n - p.dh)
                                : n < 2 * p.dh + HR ? p.z_k + row * HR + (n - 2 * p.dh)
                                                    : p.z_v + row * HR + (n - 2 * p.dh - HR);
-          *dst = __float2bfloat16_rn(mine);
+          *dst = __float2bfloat16_rn(tot);
         }
       }
     }
@@ -143,7 +180,10 @@ lrkv_status step_append_launch(const lrkv_dims& dm, int d_model, const void* x, 
   p.num_pages = num_pages;
   p.B = dm.batch; p.H = dm.heads; p.dh = dm.head_dim; p.r = dm.rank; p.d = d_model; p.max_len = dm.max_len;
   const long long row_bytes = static_cast<long long>(d_model) * 2;
-  p.bc = static_cast<int>(std::min<long long>(std::min(kStepMaxB, dm.batch), kStepSmem / row_bytes));
+  const int M = dm.batch > 8 ? 16 : 8;
+  p.wstage = kStepWarps * row_bytes <= kStepWRows;
+  const long long x_budget = kStepSmem - (p.wstage ? kStepWarps * row_bytes : 0);
+  p.bc = static_cast<int>(std::min<long long>(std::min(M, dm.batch), x_budget / row_bytes));
   if (p.bc < 1) return LRKV_ERR_UNSUPPORTED;
   p.x = static_cast<const __nv_bfloat16*>(x);
   p.w_sk = static_cast<const __nv_bfloat16*>(w_sk); p.w_sv = static_cast<const __nv_bfloat16*>(w_sv);
@@ -151,12 +191,12 @@ lrkv_status step_append_launch(const lrkv_dims& dm, int d_model, const void* x, 
   p.seq_lens = seq_lens;
   p.k_s = static_cast<__nv_bfloat16*>(k_s); p.v_s = static_cast<__nv_bfloat16*>(v_s);
   p.z_k = static_cast<__nv_bfloat16*>(z_k); p.z_v = static_cast<__nv_bfloat16*>(z_v);
-  const int smem = static_cast<int>(p.bc * row_bytes);
-  if (ensure_kernel_smem(reinterpret_cast<const void*>(lrkv_append_token_kernel), smem) != cudaSuccess)
-    return LRKV_ERR_CUDA;
+  const int smem = static_cast<int>((p.bc + (p.wstage ? kStepWarps : 0)) * row_bytes);
+  auto kern = M == 8 ? lrkv_append_token_kernel<8> : lrkv_append_token_kernel<16>;
+  if (ensure_kernel_smem(reinterpret_cast<const void*>(kern), smem) != cudaSuccess) return LRKV_ERR_CUDA;
   // one warp per output column, at most one CTA per SM
   const long long N = 2ll * dm.head_dim + 2ll * dm.heads * dm.rank;
-  const long long wpc = kStepThreads / 32;
+  const long long wpc = kStepWarps;
   const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(num_sms, (N + wpc - 1) / wpc)));
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -168,7 +208,7 @@ lrkv_status step_append_launch(const lrkv_dims& dm, int d_model, const void* x, 
   cfg.stream = static_cast<cudaStream_t>(stream);
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, lrkv_append_token_kernel, p) == cudaSuccess ? LRKV_OK : LRKV_ERR_CUDA;
+  return cudaLaunchKernelEx(&cfg, kern, p) == cudaSuccess ? LRKV_OK : LRKV_ERR_CUDA;
 }
 
 }  // namespace lrkv

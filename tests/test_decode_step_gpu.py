@@ -70,6 +70,8 @@ def _check_rows(cache, case, x, w, lens, H):
     (3, 4, 64, 16, 256, 200, [57, 120, 1]),
     (2, 8, 128, 32, 512, 300, [300, 129]),        # the row at the last cache position
     (4, 16, 64, 28, 1024, 4096, [4096, 3000, 17, 2048]),
+    (12, 4, 64, 16, 256, 96, [5, 96, 1, 40, 77, 12, 64, 65, 3, 90, 33, 18]),   # 16 sequences per pass
+    (20, 4, 64, 16, 128, 64, list(range(1, 21))),                         # two passes over the weights
 ])
 def test_decode_step_matches_oracle(shape):
     B, H, dh, r, d, Lm, lens = shape
