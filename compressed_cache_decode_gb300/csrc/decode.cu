@@ -611,6 +611,9 @@ __global__ void __launch_bounds__(32 * kCombineWarps) lrkv_decode_combine_kernel
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = P.H, dh = P.dh, r = P.r, W = dh + r;
   float* zbar = reinterpret_cast<float*>(csmem) + warp * max(r, 1);  // [r] per warp
+  const int nmax = P.grid * P.ngw;                                     // partials of one sequence, at most
+  float* wts = reinterpret_cast<float*>(csmem) + kCombineWarps * max(r, 1) + warp * 2 * nmax;  // [nmax] per warp
+  float* lsm = wts + nmax;                                                                     // [nmax] per warp
   const long long npairs = static_cast<long long>(P.B) * H;
   const long long wstride = static_cast<long long>(gridDim.x) * kCombineWarps;
   long long bh = static_cast<long long>(blockIdx.x) * kCombineWarps + warp;
@@ -673,37 +676,50 @@ __global__ void __launch_bounds__(32 * kCombineWarps) lrkv_decode_combine_kernel
     const float* ml = P.part_ml + (s0 * H + h) * 2;
     const float* acc0 = P.part_acc + (s0 * H + h) * W;
     const size_t mstep = static_cast<size_t>(H) * 2, astep = static_cast<size_t>(H) * W;
-    float M = -INFINITY, L = 0.f, a[KC];
+    // 1. the partials' weights 2^(m_i - M) against the largest maximum M,
+    //    the lanes taking the partials in turn (kept in shared memory)
+    __syncwarp();  // the previous pair's weight reads are done
+    float M = -INFINITY;
+#pragma unroll 4
+    for (int i = lane; i < n; i += 32) {
+      const float m = ml[i * mstep];
+      wts[i] = m;
+      lsm[i] = ml[i * mstep + 1];
+      M = fmaxf(M, m);
+    }
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
+    float L = 0.f;
+    for (int i = lane; i < n; i += 32) {
+      const float m = wts[i];
+      const float w = m == -INFINITY ? 0.f : exp2f(m - M);
+      wts[i] = w;
+      L = fmaf(w, lsm[i], L);
+    }
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o2);
+    __syncwarp();
+    // 2. the weighted sum of the partials' rows (lanes own columns)
+    float a[KC];
 #pragma unroll
     for (int k = 0; k < KC; ++k) a[k] = 0.f;
     for (int i0 = 0; i0 < n; i0 += kCombinePieces) {
-      float mi[kCombinePieces], li[kCombinePieces], vi[kCombinePieces][KC];
+      float vi[kCombinePieces][KC];
 #pragma unroll
       for (int u = 0; u < kCombinePieces; ++u) {
         const bool ok = i0 + u < n;
-        mi[u] = ok ? ml[(i0 + u) * mstep] : -INFINITY;
-        li[u] = ok ? ml[(i0 + u) * mstep + 1] : 0.f;
 #pragma unroll
         for (int k = 0; k < KC; ++k) {
           const int j = lane + 32 * k;
           vi[u][k] = (ok && j < W) ? acc0[(i0 + u) * astep + j] : 0.f;
         }
       }
-      float Mn = M;
-#pragma unroll
-      for (int u = 0; u < kCombinePieces; ++u) Mn = fmaxf(Mn, mi[u]);
-      const float f = M == -INFINITY ? 0.f : exp2f(M - Mn);
-      L *= f;
-#pragma unroll
-      for (int k = 0; k < KC; ++k) a[k] *= f;
 #pragma unroll
       for (int u = 0; u < kCombinePieces; ++u) {
-        const float w = mi[u] == -INFINITY ? 0.f : exp2f(mi[u] - Mn);
-        L = fmaf(w, li[u], L);
+        const float w = i0 + u < n ? wts[i0 + u] : 0.f;
 #pragma unroll
         for (int k = 0; k < KC; ++k) a[k] = fmaf(w, vi[u][k], a[k]);
       }
-      M = Mn;
     }
     const float inv_l = 1.f / L;
     __syncwarp();  // the previous pair's zbar reads are done
@@ -970,7 +986,8 @@ lrkv_status decode_make_plan(const lrkv_dims& d, int num_sms, DecodePlan& P, siz
     P.pfw = env_int("LRKV_DECODE_PREFETCH_TILES", static_cast<int>(per_cta / P.stage_bytes));
   }
   const int slots = (P.B + P.grid) * P.ngw;
-  P.combine_smem = kCombineWarps * std::max(r, 1) * 4;
+  // per warp: the lift's z row, and the weights and denominators of one sequence's partials
+  P.combine_smem = kCombineWarps * (std::max(r, 1) + 2 * P.grid * P.ngw) * 4;
 
   // workspace: status | meta | prefix | p | part_ml | part_acc | CTA status
   size_t w = 256;
