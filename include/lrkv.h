@@ -63,7 +63,7 @@ typedef enum {
   LRKV_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required          */
   LRKV_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed         */
   LRKV_ERR_TIMEOUT = 5,       /* device: a bounded wait ran out (reported, not trapped) */
-  LRKV_ERR_DEVICE_BOUNDS = 6  /* device: seq_lens/start_pos outside [0, max_len]; clamped */
+  LRKV_ERR_DEVICE_BOUNDS = 6  /* device: a length, position or page out of range; clamped or skipped */
 } lrkv_status;
 
 typedef enum { LRKV_F32 = 0, LRKV_BF16 = 1 } lrkv_dtype;
