@@ -14,6 +14,15 @@ measured HBM bandwidth; decode tokens/s = batch / step time.
 N > 1 runs one independent replica per GPU under torchrun (weak scaling, no
 data-path collective).  `--impl reference` times the fp64 CPU oracle on the
 host cores instead (rank 0 only).  Prints one JSON line.
+
+Besides the headline step, the line carries: `roofline` (the scan kernel's
+average launch duration over the timed region, with the isolated per-launch
+figure beside it), `e2e` (host copies in and out every step), and the legs of
+the rest of the path on the same cache: `decode_step` (the new token's rows
+from its layer input, then the decode, as dependent steps), `decode_normed`
+(post-projection RMSNorm key scales), `decode_paged` (the rows in 256-row pages
+through a block table) and `prefill` (append GEMM, causal prefill and the
+normalised-key prefill of 2 x 4096 tokens, against the bf16 tensor peak).
 """
 from __future__ import annotations
 
