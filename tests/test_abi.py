@@ -155,3 +155,21 @@ def test_paged_decode_rejects_bad_paging_without_gpu(lib):
     prest = (fake,) * 6 + (fake, fake, fake, fake, 1 << 20, None)  # k_s .. b_v, seq_lens, out, lse, ws, bytes, stream
     assert lib.lrkv_prefill_paged(ctypes.byref(pre), 128, fake, 64, 8, fake, *prest) == \
         lrkv.LRKV_ERR_INVALID_ARG                                                     # a key tile spans pages
+
+
+def test_paged_appends_reject_bad_paging_without_gpu(lib):
+    """The paged append and decode step check the paging before any launch."""
+    bf = lrkv.make_dims(2, 4, 64, 16, 256, "bf16")
+    fake = ctypes.c_void_p(4096)
+    w = (fake,) * 5                                     # x and the four weights
+    cache = (fake,) * 4
+    # append: (dims, d_model, n_new, x, w_sk, w_sv, u_k, u_v, start_pos, page_size, num_pages, table, cache.., ws..)
+    assert lib.lrkv_append_paged(ctypes.byref(bf), 256, 8, *w, fake, 24, 8, fake, *cache, fake, 16, None) == \
+        lrkv.LRKV_ERR_INVALID_ARG                       # page size not a power of two
+    assert lib.lrkv_append_paged(ctypes.byref(bf), 256, 8, *w, fake, 64, 8, None, *cache, fake, 16, None) == \
+        lrkv.LRKV_ERR_INVALID_ARG                       # no block table
+    # decode step: (dims, d_model, x, w.., q, page_size, num_pages, table, cache.., b_k, b_v, seq_lens, out, lse, ws..)
+    assert lib.lrkv_decode_step_paged(ctypes.byref(bf), 256, *w, fake, 512, 8, fake, *cache, fake, fake, fake,
+                                      fake, fake, fake, 1 << 20, None) == lrkv.LRKV_ERR_INVALID_ARG  # > max_len
+    assert lib.lrkv_decode_step_paged(ctypes.byref(bf), 256, *w, fake, 64, 0, fake, *cache, fake, fake, fake,
+                                      fake, fake, fake, 1 << 20, None) == lrkv.LRKV_ERR_INVALID_ARG  # no pages
