@@ -1,13 +1,14 @@
 #!/usr/bin/env python
-"""Benchmark of one LRKV decode step on the factored cache (GB300).
+"""Benchmark of the LRKV decode on the factored cache (GB300).
 
-A step is one lrkv_decode call over a batch of 8 sequences x 16 heads,
-d_h = 64, rank 28, 4096 visible rows each (bf16 cache, fp32 accumulation):
-absorb q_h B_h^K, scan the factored history with one online softmax per head,
-combine the split pieces and lift the private sum through (B_h^V)^T.  The
-metric is the cache bytes an ideal kernel must read per second (the shared
-rows counted once per sequence, never per head) and its fraction of the
-measured HBM bandwidth; decode tokens/s = batch / step time.
+The headline step is one lrkv_decode call over the long-context workload:
+4 sequences x 65,536 visible rows, 32 heads, d_h = 128, rank 48, bf16 cache
+with fp32 accumulation, 5% of the shared key rows scaled by 8.  A step
+absorbs q_h B_h^K, scans the factored history with one online softmax per
+head, combines the split pieces and lifts the private sum through (B_h^V)^T.
+The metric is the cache bytes an ideal kernel must read per second (the
+shared rows counted once per sequence, never per head) and its fraction of
+the measured HBM bandwidth; decode tokens/s = batch / step time.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -15,23 +16,29 @@ N > 1 runs one independent replica per GPU under torchrun (weak scaling, no
 data-path collective).  `--impl reference` times the fp64 CPU oracle on the
 host cores instead (rank 0 only).  Prints one JSON line.
 
-Besides the headline step, the line carries: `roofline` (the scan kernel's
-average launch duration over the timed region, with the isolated per-launch
-figure beside it), `e2e` (host copies in and out every step), and the legs of
-the rest of the path on the same cache: `decode_step` (the new token's rows
-from its layer input, then the decode, as dependent steps), `decode_normed`
-(post-projection RMSNorm key scales), `decode_paged` (the rows in 256-row pages
-through a block table) and `prefill` (append GEMM, causal prefill and the
-normalised-key prefill of 2 x 4096 tokens, against the bf16 tensor peak).
+Timing: W eager warm-up steps, then the K steps are captured as a CUDA graph,
+replayed until the GPU has run warm work for a while, and the K-step region is
+timed several times (CUDA events on the launching stream); `ms_per_step` is
+the median region over K, with the min and max beside it.  `roofline` is the
+scan kernel's own: algorithmic bytes per launch over the median duration of
+one isolated launch (events right around the kernel, launches replayed from a
+graph).  Besides the headline, the line carries: `decode_legs` (the same
+measurement on the other decode workloads), `e2e` (host copies in and out
+every step, one public-API call per step), `decode_step` (the new token's
+rows from its layer input, then the decode, as dependent steps),
+`decode_normed` (post-projection RMSNorm key scales), `decode_paged` (the
+rows in 256-row pages through a block table) and `prefill` (append GEMM,
+causal prefill and the normalised-key prefill of 2 x 4096 tokens, against the
+bf16 tensor peak).
 """
 from __future__ import annotations
 
 import argparse
 import hashlib
-import re
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -42,22 +49,27 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "LRKV decode cache GB/s (% of HBM peak) & tokens/s; prefill TFLOP/s (% peak)"
-PROFILE_JSON = os.path.join(ROOT, "profiles", "decode_stream_b8_h16_d64_r28_L4096.json")
+PROFILES = os.path.join(ROOT, "profiles")
 L2_BYTES = 129 * 1000 * 1000
 FALLBACK_HBM_GBS = 6800.0
+WARM_MS = 200.0        # warm work replayed before a timed region
+TIMED_MS = 1000.0      # the timed repeats of the headline span at least this long
 
 
 def _args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=None)
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-legs", action="store_true", help="headline decode only (no e2e, no other legs)")
+    ap.add_argument("--max-len", type=int, default=None,
+                    help="rows per sequence of the headline workload (a smaller copy of its recipe)")
     return ap.parse_args()
 
 
@@ -86,13 +98,21 @@ def _peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def _profile_traffic(split_kernel_src_sha):
-    """DRAM bytes per split launch from the committed ncu summary, if it was
-    taken on the current kernel source."""
+def _bf16_peak():
     try:
-        with open(PROFILE_JSON) as f:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured bf16 burst (cuBLAS)"
+    except Exception:
+        return 1900.0, "fallback bf16 burst"
+
+
+def _profile_traffic(workload, src_sha):
+    """DRAM bytes per scan launch from the committed ncu summary of this
+    workload, if it was taken on the current kernel sources."""
+    try:
+        with open(os.path.join(PROFILES, f"decode_stream_{workload}.json")) as f:
             d = json.load(f)
-        if d.get("source_sha256") == split_kernel_src_sha:
+        if d.get("source_sha256") == src_sha:
             return float(d["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -114,6 +134,11 @@ def _src_sha():
     return h.hexdigest()
 
 
+def _spread(xs):
+    """median, min and max of a list of per-step times (ms)."""
+    return {"median": statistics.median(xs), "min": min(xs), "max": max(xs), "n": len(xs)}
+
+
 # -------------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -122,7 +147,7 @@ class ClockSampler:
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.path = os.path.join("/tmp", f"lrkv_clocks_{os.getpid()}.csv")
+        self.path = os.path.join("/tmp", f"lrkv_clocks_{os.getpid()}_{index}.csv")
 
     def __enter__(self):
         q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -168,114 +193,348 @@ class ClockSampler:
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
         loaded = [x for x in sm if mx and x > 0.5 * max(mx)] or sm
         return {"sm_mhz": statistics.median(loaded) if loaded else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows),
+                "samples_under_load": len(loaded)}
 
 
 # ------------------------------------------------------------- CPU baseline
+#
+# The oracle (fp64, explicit K_h/V_h reconstruction) runs on bounded samples
+# of (sequence, head) pairs.  Each spawned worker (one BLAS thread) receives
+# the rows of its own few pairs once, before any timing; a round then asks
+# every worker for one pair at once.  Throughput is reported in the metric's
+# unit: the workload's algorithmic bytes per decode step times the fraction
+# of its (sequence, head) pairs the oracle finished, per second.
 
-_POOL_DATA = None
-
-
-def _pool_init(data):
-    global _POOL_DATA
-    _POOL_DATA = data
-
-
-def _oracle_task(task):
-    """One piece of the CPU baseline: the fp64 oracle on one sequence's heads."""
+def _pair_worker(conn):
+    import torch
     from oracle import lrkv_oracle as O
-    b, heads = task
-    d = _POOL_DATA
-    sl = slice(b, b + 1)
-    O.decode_reference(d["q"][sl], d["k_s"][sl], d["v_s"][sl], d["z_k"][sl], d["z_v"][sl],
-                       d["b_k"], d["b_v"], d["seq_lens"][sl], pairs=[(0, h) for h in heads])
-    return len(heads)
+    data = conn.recv()
+    conn.send("ready")
+    k = 0
+    while True:
+        msg = conn.recv()
+        if msg is None:
+            break
+        q, k_s, v_s, z_k, z_v, b_k, b_v, L = data[k % len(data)]
+        k += 1
+        O.decode_reference(q, k_s, v_s, z_k, z_v, b_k, b_v, torch.tensor([L], dtype=torch.int32))
+        conn.send(1)
 
 
-class OraclePool:
-    """Spawned worker processes, one BLAS thread each, holding the inputs."""
+def _pair_slices(case, b, h):
+    """The inputs of one (sequence, head) pair as a one-sequence, one-head
+    decode: q [1,1,d_h], k_s/v_s [1,L,d_h], z [1,L,1,r], bases [1,d_h,r]."""
+    L = int(case["seq_lens"][b])
+    sl = lambda t: t.contiguous().clone()  # noqa: E731
+    return (sl(case["q"][b:b + 1, h:h + 1]), sl(case["k_s"][b:b + 1, :L]), sl(case["v_s"][b:b + 1, :L]),
+            sl(case["z_k"][b:b + 1, :L, h:h + 1]), sl(case["z_v"][b:b + 1, :L, h:h + 1]),
+            sl(case["b_k"][h:h + 1]), sl(case["b_v"][h:h + 1]), L)
 
-    def __init__(self, case, cores):
+
+def _sample_pairs(w, n, seed=0):
+    import random
+    rng = random.Random(seed)
+    pairs = [(b, h) for b in range(w.batch) for h in range(w.heads)]
+    rng.shuffle(pairs)
+    return [pairs[i % len(pairs)] for i in range(n)]
+
+
+class PairWorkers:
+    """`cores` spawned processes, each holding `per` (sequence, head) pairs of
+    the case; round() runs one pair on every worker at once."""
+
+    def __init__(self, w, case, cores, per=2, seed=0):
         import multiprocessing as mp
-        self.cores = cores
+        ctx = mp.get_context("spawn")
         saved = {k: os.environ.get(k) for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")}
         for k in saved:
             os.environ[k] = "1"
+        self.procs, self.conns = [], []
         try:
-            ctx = mp.get_context("spawn")
-            self.pool = ctx.Pool(cores, initializer=_pool_init, initargs=(case,))
+            for _ in range(cores):
+                a, b = ctx.Pipe()
+                p = ctx.Process(target=_pair_worker, args=(b,), daemon=True)
+                p.start()
+                self.procs.append(p)
+                self.conns.append(a)
         finally:
             for k, v in saved.items():
                 if v is None:
                     os.environ.pop(k, None)
                 else:
                     os.environ[k] = v
-        self.pool.map(_oracle_task, [(0, [0])] * cores)  # import oracle in every worker
+        order = _sample_pairs(w, cores * per, seed)
+        for i, c in enumerate(self.conns):
+            c.send([_pair_slices(case, *order[i * per + j]) for j in range(per)])
+        for c in self.conns:
+            assert c.recv() == "ready"
+        self.cores = cores
 
-    def run(self, tasks):
-        return sum(self.pool.map(_oracle_task, tasks, chunksize=1))
+    def round(self):
+        for c in self.conns:
+            c.send(1)
+        return sum(c.recv() for c in self.conns)
 
     def close(self):
-        self.pool.close()
-        self.pool.join()
-
-
-def _tasks(w, split):
-    heads = list(range(w.heads))
-    per = max(1, math.ceil(w.heads / split))
-    return [(b, heads[i:i + per]) for b in range(w.batch) for i in range(0, w.heads, per)]
+        for c in self.conns:
+            c.send(None)
+        for p in self.procs:
+            p.join(timeout=30)
 
 
 def cpu_baseline(w, case, seconds, cores):
-    """Oracle timed on a bounded sample: whole decode steps (all sequences and
-    heads) repeated until `seconds` of wall time have passed."""
-    pool = OraclePool(case, cores)
-    tasks = _tasks(w, max(1, (2 * cores) // w.batch))
+    """The oracle timed on a bounded sample: rounds of `cores` (sequence,
+    head) pairs, one per core, until `seconds` of wall time have passed."""
+    workers = PairWorkers(w, case, cores, seed=1)
     total_bytes, _, _ = decode_bytes(w, case["seq_lens"])
+    workers.round()  # untimed: imports and first-touch in every worker
     n, t0 = 0, time.perf_counter()
     while True:
-        pool.run(tasks)
-        n += 1
+        n += workers.round()
         el = time.perf_counter() - t0
-        if el >= seconds or n >= 400:
+        if el >= seconds or n >= 4096:
             break
-    pool.close()
-    return {"value": total_bytes * n / el / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": f"{n} full decode step(s) of {w.name} (all {w.batch}x{w.heads} sequence-head "
-                      f"pairs, fp64 explicit K_h/V_h reconstruction), {el:.1f} s wall"}
+    workers.close()
+    frac = n / (w.batch * w.heads)
+    return {"value": total_bytes * frac / el / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} (sequence, head) pairs of {w.name} ({frac:.3g} of a decode step; each pair "
+                      f"an fp64 explicit K_h/V_h reconstruction over its full history), {el:.1f} s wall; "
+                      f"GB/s = the step's algorithmic bytes x that fraction / wall time"}
 
 
 def reference_arm(a, w):
-    """--impl reference: the fp64 oracle on the host cores, one bounded sample
-    (one sequence, all heads) per step."""
+    """--impl reference: the fp64 oracle on the host cores.  A step is a
+    bounded sample of the workload: one (sequence, head) pair per core."""
     from compressed_cache_decode_gb300 import inputs
     case = inputs.make_decode_inputs(w, seed=0)
     cores = min(os.cpu_count() or 1, 16)
-    pool = OraclePool(case, cores)
-    per_b = _tasks(w, cores)
-    B = w.batch
-    _, _, cache_all = decode_bytes(w, case["seq_lens"])
-    seq_bytes = cache_all / B + 2 * w.heads * w.head_dim * w.rank * w.elem_bytes \
-        + w.heads * w.head_dim * (w.elem_bytes + 4)
-    for i in range(a.warmup):
-        b = i % B
-        pool.run([t for t in per_b if t[0] == b])
+    workers = PairWorkers(w, case, cores, seed=2)
+    total_bytes, _, _ = decode_bytes(w, case["seq_lens"])
+    del case
+    for _ in range(a.warmup):
+        workers.round()
     t0 = time.perf_counter()
-    for i in range(a.steps):
-        b = i % B
-        pool.run([t for t in per_b if t[0] == b])
+    for _ in range(a.steps):
+        workers.round()
     el = time.perf_counter() - t0
-    pool.close()
-    value = seq_bytes * a.steps / el / 1e9
+    workers.close()
+    frac = cores / (w.batch * w.heads)
+    value = total_bytes * frac * a.steps / el / 1e9 if a.steps > 0 else 0.0
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 0,
-            "steps": a.steps, "warmup": a.warmup, "ms_per_step": el / a.steps * 1e3,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": el / max(a.steps, 1) * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": w.name, "batch_per_step": 1, "heads": w.heads,
+            "config": {"workload": w.name, "pairs_per_step": cores, "batch": w.batch, "heads": w.heads,
                        "head_dim": w.head_dim, "rank": w.rank, "seq_len": w.max_len},
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
-                             "sample": f"one sequence (all {w.heads} heads) of {w.name} per step"},
+                             "sample": f"{cores} (sequence, head) pairs of {w.name} per step ({frac:.3g} of "
+                                       f"a decode step); GB/s = the step's algorithmic bytes x that fraction "
+                                       f"/ wall time"},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ------------------------------------------------------------ GPU timing
+
+def max_over_ranks(value, world, device):
+    """The job's time for a per-rank time: the slowest rank's (all-reduce MAX
+    over the default process group; the value itself when world == 1)."""
+    if world == 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(bytes_per_rank, world, ms_per_step):
+    """Whole-job throughput: all ranks' bytes per step over the slowest rank's
+    step time (every rank decodes its own batch: replicas)."""
+    return bytes_per_rank * world / (ms_per_step * 1e-3) / 1e9
+
+
+class StepTimer:
+    """K calls of `fn(i, stream)` captured as one CUDA graph (eager launches
+    when capture is off or fails), replayed warm, then timed."""
+
+    def __init__(self, fn, K, W, stream, use_graph=True):
+        import torch
+        self.fn, self.K, self.stream = fn, K, stream
+        with torch.cuda.stream(stream):
+            for i in range(W):
+                fn(i, stream)
+        torch.cuda.synchronize()
+        self.graph = None
+        if use_graph:
+            try:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+                    for i in range(K):
+                        fn(i, torch.cuda.current_stream())
+                torch.cuda.synchronize()
+                self.graph = g
+            except Exception as e:  # fall back to eager launches
+                print(f"graph capture failed ({e}); timing eager launches", file=sys.stderr)
+                torch.cuda.synchronize()
+
+    def _region(self):
+        if self.graph is not None:
+            self.graph.replay()
+        else:
+            for i in range(self.K):
+                self.fn(i, self.stream)
+
+    def warm(self, ms=WARM_MS):
+        import torch
+        t0 = time.perf_counter()
+        n = 0
+        while n < 2 or (time.perf_counter() - t0) * 1e3 < ms:
+            with torch.cuda.stream(self.stream):
+                self._region()
+            torch.cuda.synchronize()
+            n += 1
+
+    def time(self, repeats=None, min_ms=0.0):
+        """Per-step ms of each timed K-step region."""
+        import torch
+        out = []
+        t0 = time.perf_counter()
+        while True:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            with torch.cuda.stream(self.stream):
+                e0.record(self.stream)
+                self._region()
+                e1.record(self.stream)
+            torch.cuda.synchronize()
+            out.append(e0.elapsed_time(e1) / self.K)
+            if repeats is not None and len(out) >= repeats and (time.perf_counter() - t0) * 1e3 >= min_ms:
+                break
+            if len(out) >= 2000:
+                break
+        return out
+
+
+def scan_launch_ms(profiled, n, stream, use_graph=True):
+    """Median duration of one isolated scan launch: `profiled(i, ev0, ev1, s)`
+    enqueues a decode with CUDA events right around its scan kernel; the n
+    calls are replayed from a graph (so the interval holds the kernel, not the
+    host's launch latency), warm, and the last replay's launches are read."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    with torch.cuda.stream(stream):
+        for i in range(n):
+            profiled(i, evs[i][0], evs[i][1], stream)
+    torch.cuda.synchronize()
+    kind = "eager"
+    g = None
+    if use_graph:
+        try:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+                for i in range(n):
+                    profiled(i, evs[i][0], evs[i][1], torch.cuda.current_stream())
+            torch.cuda.synchronize()
+            kind = "graph"
+        except Exception as e:
+            print(f"profiled graph capture failed ({e}); eager timing", file=sys.stderr)
+            g = None
+            torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    while True:
+        with torch.cuda.stream(stream):
+            if g is not None:
+                g.replay()
+            else:
+                for i in range(n):
+                    profiled(i, evs[i][0], evs[i][1], stream)
+        torch.cuda.synchronize()
+        if (time.perf_counter() - t0) * 1e3 >= 50.0:
+            break
+    ms = [e0.elapsed_time(e1) for e0, e1 in evs]
+    return statistics.median(ms), min(ms), max(ms), kind
+
+
+class DecodeSetup:
+    """One decode workload on the device: inputs, rotating cache replicas
+    when the cache is small enough to stay in L2, outputs and workspace."""
+
+    def __init__(self, w, dev, seed, max_len=None):
+        import torch
+        from compressed_cache_decode_gb300 import inputs, lrkv
+        if max_len is not None and max_len != w.max_len:
+            import dataclasses
+            w = dataclasses.replace(w, name=f"{w.name}@L{max_len}", max_len=max_len)
+        self.w = w
+        self.case = inputs.make_decode_inputs(w, seed=seed)
+        d = {k: v.to(dev) for k, v in self.case.items()}
+        self.dims = lrkv.make_dims(w.batch, w.heads, w.head_dim, w.rank, w.max_len, w.torch_dtype)
+        self.ws = lrkv.decode_workspace(self.dims, dev)
+        n_out = w.batch * w.heads * w.head_dim
+        self.out_lse = torch.empty(n_out + w.batch * w.heads, dtype=torch.float32, device=dev)
+        self.out = self.out_lse[:n_out].view(w.batch, w.heads, w.head_dim)
+        self.lse = self.out_lse[n_out:].view(w.batch, w.heads)
+        self.total_bytes, self.split_bytes, self.cache_alg = decode_bytes(w, self.case["seq_lens"])
+        self.cache_bytes = sum(d[k].numel() * d[k].element_size() for k in ("k_s", "v_s", "z_k", "z_v"))
+        if self.cache_alg >= 4 * L2_BYTES:
+            self.n_rep = 1
+            self.l2 = f"inputs larger than L2 ({self.cache_alg / 1e6:.0f} MB read per step > {L2_BYTES / 1e6:.0f} MB)"
+        elif self.cache_alg >= 4096:
+            self.n_rep = min(16, max(2, math.ceil(4 * L2_BYTES / self.cache_alg)))
+            self.l2 = (f"{self.n_rep} rotating cache replicas ({self.n_rep * self.cache_alg / 1e6:.0f} MB read "
+                       f"per cycle > L2 {L2_BYTES / 1e6:.0f} MB)")
+        else:
+            self.n_rep = 1
+            self.l2 = "L2-resident (launch-latency bound: microseconds only)"
+        self.reps = [d] + [{k: (v.clone() if k in ("k_s", "v_s", "z_k", "z_v") else v) for k, v in d.items()}
+                           for _ in range(self.n_rep - 1)]
+
+    def step(self, i, s):
+        from compressed_cache_decode_gb300 import lrkv
+        x = self.reps[i % self.n_rep]
+        st = lrkv.lrkv_decode(self.dims, x["q"], x["k_s"], x["v_s"], x["z_k"], x["z_v"], x["b_k"], x["b_v"],
+                              x["seq_lens"], self.out, self.lse, self.ws, self.ws.numel(), s)
+        if st != lrkv.LRKV_OK:
+            raise lrkv.LRKVError(st, "lrkv_decode")
+
+    def profiled(self, i, e0, e1, s):
+        from compressed_cache_decode_gb300 import lrkv
+        x = self.reps[i % self.n_rep]
+        st = lrkv.lrkv_decode_profiled(self.dims, x["q"], x["k_s"], x["v_s"], x["z_k"], x["z_v"], x["b_k"],
+                                       x["b_v"], x["seq_lens"], self.out, self.lse, self.ws, self.ws.numel(), e0,
+                                       e1, s)
+        if st != lrkv.LRKV_OK:
+            raise lrkv.LRKVError(st, "lrkv_decode_profiled")
+
+
+def scan_kernel_name(w):
+    return "lrkv_decode_stream_kernel" if w.dtype == "bf16" else "lrkv_decode_split_kernel"
+
+
+def decode_leg(setup, K, W, stream, use_graph, peak, world, dev, repeats=7, min_ms=0.0):
+    """Step rate (median of timed K-step regions) and the isolated scan
+    launch of one decode workload."""
+    w = setup.w
+    timer = StepTimer(setup.step, K, W, stream, use_graph)
+    timer.warm()
+    ms = timer.time(repeats=repeats, min_ms=min_ms)
+    sp = _spread(ms)
+    ms_step = max_over_ranks(sp["median"], world, dev)
+    iso, iso_min, iso_max, kind = scan_launch_ms(setup.profiled, min(K, 20), stream, use_graph)
+    achieved = setup.split_bytes / (iso * 1e-3) / 1e9
+    return {
+        "workload": w.name, "ms_per_step": ms_step, "ms_per_step_spread": sp,
+        "gbs": job_gbs(setup.total_bytes, world, ms_step), "hbm_frac": setup.total_bytes / (ms_step * 1e-3) / 1e9 / peak,
+        "tokens_per_s": w.batch * world / (ms_step * 1e-3), "bytes_per_step": setup.total_bytes,
+        "seq_len_sum": int(setup.case["seq_lens"].long().sum()), "l2": setup.l2,
+        "graph": timer.graph is not None,
+        "roofline": {"bound": "hbm", "kernel": scan_kernel_name(w), "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "algorithmic_bytes_per_launch": setup.split_bytes,
+                     "launch_ms": iso, "launch_ms_min": iso_min, "launch_ms_max": iso_max,
+                     "launch_timing": f"CUDA events right around each isolated scan launch on the launching "
+                                      f"stream ({kind} launches), median of {min(K, 20)}"},
+    }, timer
 
 
 # ------------------------------------------------------------ prefill leg
@@ -306,19 +565,20 @@ def prefill_leg(dev, iters=10):
     z_k = torch.empty((B, T, H, r), dtype=torch.bfloat16, device=dev)
     z_v = torch.empty_like(z_k)
     dims = lrkv.make_dims(B, H, dh, r, T, torch.bfloat16)
-    ws = torch.zeros(16, dtype=torch.uint8, device=dev)
+    nws = lrkv.lrkv_prefill_workspace_size(dims, T)
+    ws = torch.zeros(max(nws, 16), dtype=torch.uint8, device=dev)
     out = torch.empty((B, T, H, dh), dtype=torch.float32, device=dev)
     lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
 
     def app():
         st = lrkv.lrkv_append(dims, w.d_model, T, d["x"], d["w_sk"], d["w_sv"], d["u_k"], d["u_v"],
-                              d["start_pos"], k_s, v_s, z_k, z_v, ws, 16)
+                              d["start_pos"], k_s, v_s, z_k, z_v, ws, ws.numel())
         assert st == lrkv.LRKV_OK
 
     def pre():
         st = lrkv.lrkv_prefill(dims, T, d["q"], k_s, v_s, z_k, z_v, d["b_k"], d["b_v"], d["seq_lens"],
-                               out, lse, ws, 16)
+                               out, lse, ws, ws.numel())
         assert st == lrkv.LRKV_OK
 
     # post-projection RMSNorm of the keys: the scales of every appended row
@@ -327,13 +587,14 @@ def prefill_leg(dev, iters=10):
 
     def pre_normed():
         st = lrkv.lrkv_prefill_normed(dims, T, d["q"], k_s, v_s, z_k, z_v, d["b_k"], d["b_v"], kscale,
-                                      d["seq_lens"], out, lse, ws, 16)
+                                      d["seq_lens"], out, lse, ws, ws.numel())
         assert st == lrkv.LRKV_OK
 
+    def kscales():
+        lrkv.key_scales(k_s, z_k, d["b_k"], d["start_pos"], T, kscale, eps=1e-6)
+
     res = {}
-    for name, fn in (("append", app), ("prefill", pre), ("prefill_normed", pre_normed)):
-        if name == "prefill_normed":
-            lrkv.key_scales(k_s, z_k, d["b_k"], d["start_pos"], T, kscale, eps=1e-6)
+    for name, fn in (("append", app), ("prefill", pre), ("key_scales", kscales), ("prefill_normed", pre_normed)):
         for _ in range(3):
             fn()
         ts = []
@@ -345,48 +606,225 @@ def prefill_leg(dev, iters=10):
             e1.record()
             torch.cuda.synchronize()
             ts.append(e0.elapsed_time(e1))
-        res[name] = statistics.median(ts)
+        res[name] = _spread(ts)
     attn, append = prefill_flops(w)
     peak = _bf16_peak()
+    hbm, _ = _peaks()
+    # key scales read k_s and z_k of every row and B^K, write one fp32 per (head, row)
+    ks_bytes = B * T * (dh + H * r) * 2 + H * dh * r * 2 + B * H * T * 4
+    ms = {k: v["median"] for k, v in res.items()}
     return {"workload": w.name,
-            "attention": {"ms": res["prefill"], "tflops": attn / (res["prefill"] * 1e-3) / 1e12,
-                          "algorithmic_flop": attn},
-            "append": {"ms": res["append"], "tflops": append / (res["append"] * 1e-3) / 1e12,
-                       "algorithmic_flop": append},
-            "attention_normed": {"ms": res["prefill_normed"],
-                                 "tflops": attn / (res["prefill_normed"] * 1e-3) / 1e12},
+            "attention": {"ms": ms["prefill"], "tflops": attn / (ms["prefill"] * 1e-3) / 1e12,
+                          "algorithmic_flop": attn, "spread": res["prefill"]},
+            "append": {"ms": ms["append"], "tflops": append / (ms["append"] * 1e-3) / 1e12,
+                       "algorithmic_flop": append, "spread": res["append"]},
+            "attention_normed": {"ms": ms["prefill_normed"],
+                                 "tflops": attn / (ms["prefill_normed"] * 1e-3) / 1e12},
+            "key_scales": {"ms": ms["key_scales"], "algorithmic_bytes": ks_bytes,
+                           "gbs": ks_bytes / (ms["key_scales"] * 1e-3) / 1e9,
+                           "hbm_frac": ks_bytes / (ms["key_scales"] * 1e-3) / 1e9 / hbm},
             "peak_tflops": peak[0], "peak_kind": peak[1],
-            "attention_frac": attn / (res["prefill"] * 1e-3) / 1e12 / peak[0],
-            "append_frac": append / (res["append"] * 1e-3) / 1e12 / peak[0]}
+            "attention_frac": attn / (ms["prefill"] * 1e-3) / 1e12 / peak[0],
+            "append_frac": append / (ms["append"] * 1e-3) / 1e12 / peak[0],
+            "timing": f"CUDA events around each launch, L2 flushed before it, median of {iters}"}
 
 
-def _bf16_peak():
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            return float(json.load(f)["bf16_tflops"]), "measured bf16 burst (cuBLAS)"
-    except Exception:
-        return 1900.0, "fallback bf16 burst"
+# -------------------------------------------------------------------- legs
 
-
-# -------------------------------------------------------------------- GPU arm
-
-def max_over_ranks(value, world, device):
-    """The job's time for a per-rank time: the slowest rank's (all-reduce MAX
-    over the default process group; the value itself when world == 1)."""
-    if world == 1:
-        return float(value)
+def _token_weights(w, dev, seed=1234):
+    """Projection weights of a layer of width d_model = heads x head_dim (the
+    new token's rows come from them), x of the new token, seeded."""
     import torch
-    import torch.distributed as dist
-    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+    d_model = w.heads * w.head_dim
+    g = torch.Generator().manual_seed(seed)
+    xs = torch.randn(w.batch, d_model, generator=g).to(torch.bfloat16).to(dev)
+    wr = [(torch.randn(n, d_model, generator=g) / d_model ** 0.5).to(torch.bfloat16).to(dev)
+          for n in (w.head_dim, w.head_dim, w.heads * w.rank, w.heads * w.rank)]
+    return d_model, xs, wr
 
 
-def job_gbs(bytes_per_rank, world, ms_per_step):
-    """Whole-job throughput: all ranks' bytes per step over the slowest rank's
-    step time (every rank decodes its own batch: replicas)."""
-    return bytes_per_rank * world / (ms_per_step * 1e-3) / 1e9
+def decode_step_leg(setup, K, W, stream, use_graph, world, dev, base_ms):
+    """The new token's rows from its layer input, then the decode, as a chain
+    of dependent steps (one lrkv_decode_step per step)."""
+    from compressed_cache_decode_gb300 import lrkv
+    w = setup.w
+    d_model, xs, wr = _token_weights(w, dev)
 
+    def fstep(i, s):
+        x = setup.reps[i % setup.n_rep]
+        st = lrkv.lrkv_decode_step(setup.dims, d_model, xs, *wr, x["q"], x["k_s"], x["v_s"], x["z_k"], x["z_v"],
+                                   x["b_k"], x["b_v"], x["seq_lens"], setup.out, setup.lse, setup.ws,
+                                   setup.ws.numel(), s)
+        if st != lrkv.LRKV_OK:
+            raise lrkv.LRKVError(st, "lrkv_decode_step")
+
+    t = StepTimer(fstep, K, W, stream, use_graph)
+    t.warm()
+    sp = _spread(t.time(repeats=7))
+    f_ms = max_over_ranks(sp["median"], world, dev)
+    w_bytes = sum(x.numel() * 2 for x in wr)
+    rows_bytes = w.batch * 2 * (w.head_dim + w.heads * w.rank) * 2
+    alg = setup.total_bytes + w_bytes + xs.numel() * 2 + rows_bytes
+    return {"workload": w.name, "d_model": d_model, "ms_per_step": f_ms, "ms_per_step_spread": sp,
+            "decode_ms_per_step": base_ms, "projection_ms_per_step": f_ms - base_ms,
+            "algorithmic_bytes": alg, "gbs": job_gbs(alg, world, f_ms)}
+
+
+def decode_normed_leg(setup, K, W, stream, use_graph, world, dev, base_ms):
+    """Decode with post-projection RMSNorm of the keys: the cached reciprocal
+    key scales (one fp32 per head and token) multiply the summed scores."""
+    import torch
+    from compressed_cache_decode_gb300 import lrkv
+    w = setup.w
+    kscales = []
+    for x in setup.reps:
+        t = torch.empty((w.batch, w.heads, w.max_len), dtype=torch.float32, device=dev)
+        lrkv.key_scales(x["k_s"], x["z_k"], x["b_k"], torch.zeros(w.batch, dtype=torch.int32, device=dev),
+                        w.max_len, t, eps=1e-6)
+        kscales.append(t)
+    torch.cuda.synchronize()
+
+    def nstep(i, s):
+        x = setup.reps[i % setup.n_rep]
+        st = lrkv.lrkv_decode_normed(setup.dims, x["q"], x["k_s"], x["v_s"], x["z_k"], x["z_v"], x["b_k"], x["b_v"],
+                                     kscales[i % setup.n_rep], x["seq_lens"], setup.out, setup.lse, setup.ws,
+                                     setup.ws.numel(), s)
+        if st != lrkv.LRKV_OK:
+            raise lrkv.LRKVError(st, "lrkv_decode_normed")
+
+    t = StepTimer(nstep, K, W, stream, use_graph)
+    t.warm()
+    sp = _spread(t.time(repeats=7))
+    n_ms = max_over_ranks(sp["median"], world, dev)
+    scale_bytes = int(setup.case["seq_lens"].long().sum()) * w.heads * 4
+    del kscales
+    return {"workload": w.name, "ms_per_step": n_ms, "ms_per_step_spread": sp, "decode_ms_per_step": base_ms,
+            "algorithmic_bytes": setup.total_bytes + scale_bytes,
+            "gbs": job_gbs(setup.total_bytes + scale_bytes, world, n_ms), "key_scale_bytes": scale_bytes}
+
+
+def decode_paged_leg(setup, K, W, stream, use_graph, world, dev, base_ms, page=256):
+    """Decode over a paged cache: the same rows in `page`-row pages of a
+    pool, in a seeded random page order, through a block table."""
+    from compressed_cache_decode_gb300 import inputs, lrkv
+    w = setup.w
+    pc = inputs.paged_from_contiguous(setup.case, page_size=page, seed=7)
+    pd = {k: v.to(dev) for k, v in pc.items()}
+    del pc
+    preps = [pd] + [{k: (v.clone() if k in ("k_s", "v_s", "z_k", "z_v") else v) for k, v in pd.items()}
+                    for _ in range(setup.n_rep - 1)]
+    n_pages = pd["k_s"].shape[0]
+
+    def pstep(i, s):
+        x = preps[i % setup.n_rep]
+        st = lrkv.lrkv_decode_paged(setup.dims, page, n_pages, x["block_table"], x["q"], x["k_s"], x["v_s"],
+                                    x["z_k"], x["z_v"], x["b_k"], x["b_v"], x["seq_lens"], setup.out, setup.lse,
+                                    setup.ws, setup.ws.numel(), s)
+        if st != lrkv.LRKV_OK:
+            raise lrkv.LRKVError(st, "lrkv_decode_paged")
+
+    t = StepTimer(pstep, K, W, stream, use_graph)
+    t.warm()
+    sp = _spread(t.time(repeats=7))
+    p_ms = max_over_ranks(sp["median"], world, dev)
+    return {"workload": w.name, "page_size": page, "pages": n_pages, "ms_per_step": p_ms, "ms_per_step_spread": sp,
+            "decode_ms_per_step": base_ms, "gbs": job_gbs(setup.total_bytes, world, p_ms)}
+
+
+def e2e_leg(setup, K, stream, use_graph, world, dev):
+    """End to end through the public API: every step copies the new token's
+    layer input x, its query q and the lengths from pinned host memory (one
+    packed copy), makes ONE library call (lrkv_decode_step: the token's cache
+    rows from x, then the decode over the cache that now holds them) and
+    reads out and lse back (one copy); the host waits for each step's result
+    before the next.  Timed two ways: eager (the C-ABI call made from Python
+    every step) and with each step's copies and call replayed from a graph.
+    The GB/s counts the decode's algorithmic bytes only (the projection's
+    weight reads are extra work, not credited)."""
+    import torch
+    from compressed_cache_decode_gb300 import lrkv
+    w = setup.w
+    d_model, xs, wr = _token_weights(w, dev, seed=4321)
+    host_parts = [("x", xs.cpu()), ("q", setup.case["q"].contiguous()),
+                  ("seq_lens", setup.case["seq_lens"].contiguous())]
+    offs, n_in = [], 0
+    for _, v in host_parts:
+        offs.append(n_in)
+        n_in += (v.numel() * v.element_size() + 255) // 256 * 256
+    host_in = torch.zeros(n_in, dtype=torch.uint8).pin_memory()
+    dev_in = torch.empty(n_in, dtype=torch.uint8, device=dev)
+    views = {}
+    for (k, v), o in zip(host_parts, offs):
+        nb = v.numel() * v.element_size()
+        host_in[o:o + nb].copy_(v.reshape(-1).view(torch.uint8))
+        views[k] = dev_in[o:o + nb].view(v.dtype).view(v.shape)
+    host_out = torch.empty_like(setup.out_lse, device="cpu").pin_memory()
+    h2d = sum(v.numel() * v.element_size() for _, v in host_parts)
+    d2h = host_out.numel() * 4
+
+    def body(i, s):
+        x = setup.reps[i % setup.n_rep]
+        dev_in.copy_(host_in, non_blocking=True)
+        st = lrkv.lrkv_decode_step(setup.dims, d_model, views["x"], *wr, views["q"], x["k_s"], x["v_s"], x["z_k"],
+                                   x["z_v"], x["b_k"], x["b_v"], views["seq_lens"], setup.out, setup.lse, setup.ws,
+                                   setup.ws.numel(), s)
+        if st != lrkv.LRKV_OK:
+            raise lrkv.LRKVError(st, "lrkv_decode_step")
+        host_out.copy_(setup.out_lse, non_blocking=True)
+
+    graphs = None
+    if use_graph:
+        try:
+            graphs = []
+            for r in range(setup.n_rep):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+                    body(r, torch.cuda.current_stream())
+                graphs.append(g)
+            torch.cuda.synchronize()
+        except Exception as e:
+            print(f"end-to-end graph capture failed ({e})", file=sys.stderr)
+            graphs = None
+            torch.cuda.synchronize()
+
+    def run(n, graphed):
+        with torch.cuda.stream(stream):
+            for i in range(n):
+                if graphed:
+                    graphs[i % setup.n_rep].replay()
+                else:
+                    body(i, stream)
+                stream.synchronize()
+
+    K_e2e = max(K, 10)
+    res = {}
+    for kind in (["eager", "graph"] if graphs is not None else ["eager"]):
+        g = kind == "graph"
+        t0 = time.perf_counter()
+        while (time.perf_counter() - t0) < 0.1:
+            run(3, g)
+        reps = []
+        for _ in range(5):
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            run(K_e2e, g)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            reps.append(e0.elapsed_time(e1) / K_e2e)
+        res[kind] = _spread(reps)
+    e_ms = max_over_ranks(res["eager"]["median"], world, dev)
+    out = {"value": job_gbs(setup.total_bytes, world, e_ms), "unit": "GB/s", "ms_per_step": e_ms,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "call": "lrkv_decode_step",
+           "workload": w.name, "timing": "eager: host copy in, one C-ABI call, copy out, host waits, every step",
+           "eager": res["eager"]}
+    if "graph" in res:
+        g_ms = max_over_ranks(res["graph"]["median"], world, dev)
+        out["graph"] = dict(res["graph"], gbs=job_gbs(setup.total_bytes, world, g_ms))
+    return out
+
+
+# -------------------------------------------------------------------- main
 
 def main():
     a = _args()
@@ -417,303 +855,43 @@ def main():
     if world > 1:
         dist.barrier()
     lrkv.load()
-
-    case = inputs.make_decode_inputs(w, seed=rank)
-    d = {k: v.to(dev) for k, v in case.items()}
-    dims = lrkv.make_dims(w.batch, w.heads, w.head_dim, w.rank, w.max_len, w.torch_dtype)
-    ws = lrkv.decode_workspace(dims, dev)
-    # out and lse in one buffer, so that a step's results come back in one copy
-    n_out = w.batch * w.heads * w.head_dim
-    out_lse = torch.empty(n_out + w.batch * w.heads, dtype=torch.float32, device=dev)
-    out = out_lse[:n_out].view(w.batch, w.heads, w.head_dim)
-    lse = out_lse[n_out:].view(w.batch, w.heads)
-
-    # rotate cache replicas so that consecutive steps never hit in L2
-    cache_bytes = sum(d[k].numel() * d[k].element_size() for k in ("k_s", "v_s", "z_k", "z_v"))
-    n_rep = max(2, math.ceil(4 * L2_BYTES / cache_bytes)) if cache_bytes < 4 * L2_BYTES else 1
-    reps = [d] + [{k: (v.clone() if k in ("k_s", "v_s", "z_k", "z_v") else v) for k, v in d.items()}
-                  for _ in range(n_rep - 1)]
-    total_bytes, split_bytes, _ = decode_bytes(w, case["seq_lens"])
+    peak, peak_kind = _peaks()
+    use_graph = not a.no_graph
+    K, W = a.steps, a.warmup
     stream = torch.cuda.Stream(device=dev)
 
-    def step(i, s=None):
-        x = reps[i % n_rep]
-        st = lrkv.lrkv_decode(dims, x["q"], x["k_s"], x["v_s"], x["z_k"], x["z_v"], x["b_k"],
-                              x["b_v"], x["seq_lens"], out, lse, ws, ws.numel(), s or stream)
-        if st != lrkv.LRKV_OK:
-            raise lrkv.LRKVError(st, "lrkv_decode")
-
-    K, W = a.steps, a.warmup
-    with torch.cuda.stream(stream):
-        for i in range(W):
-            step(i)
-    torch.cuda.synchronize()
-
-    graph = None
-    if not a.no_graph:
-        try:
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
-                for i in range(K):
-                    step(i, torch.cuda.current_stream())
-            torch.cuda.synchronize()
-            graph.replay()  # warm the graph once (untimed)
-            torch.cuda.synchronize()
-        except Exception as e:  # fall back to eager launches
-            print(f"graph capture failed ({e}); timing eager launches", file=sys.stderr)
-            graph = None
-            torch.cuda.synchronize()
-
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # ---- headline: timed repeats of the K-step region, clocks sampled ----
+    head = DecodeSetup(w, dev, seed=rank, max_len=a.max_len)
+    w = head.w
+    timer = StepTimer(head.step, K, W, stream, use_graph)
+    timer.warm()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        with torch.cuda.stream(stream):
-            ev0.record(stream)
-            if graph is not None:
-                graph.replay()
-            else:
-                for i in range(K):
-                    step(i)
-            ev1.record(stream)
-        torch.cuda.synchronize()
+        ms_list = timer.time(repeats=7, min_ms=TIMED_MS)
     if world > 1:
         dist.barrier()
-    ms_max = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
-    ms_step = ms_max / K
+    spread = _spread(ms_list)
+    ms_step = max_over_ranks(spread["median"], world, dev)
+    iso, iso_min, iso_max, iso_kind = scan_launch_ms(head.profiled, min(K, 20), stream, use_graph)
+    del timer
 
-    # dominant kernel (split-KV scan) timed alone with events around it; the
-    # profiled calls are replayed from a CUDA graph (as the step is), so that
-    # the interval holds the kernel rather than the host's launch latency
-    n_prof = min(K, 50)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_prof)]
+    e2e = e2e_leg(head, K, stream, use_graph, world, dev) if not a.no_legs else None
+    normed_leg = decode_normed_leg(head, K, W, stream, use_graph, world, dev, ms_step) if not a.no_legs else None
+    paged_leg = decode_paged_leg(head, K, W, stream, use_graph, world, dev, ms_step) if not a.no_legs else None
 
-    def prof_calls(s):
-        for i in range(n_prof):
-            x = reps[i % n_rep]
-            st = lrkv.lrkv_decode_profiled(dims, x["q"], x["k_s"], x["v_s"], x["z_k"], x["z_v"],
-                                           x["b_k"], x["b_v"], x["seq_lens"], out, lse, ws,
-                                           ws.numel(), evs[i][0], evs[i][1], s)
-            if st != lrkv.LRKV_OK:
-                raise lrkv.LRKVError(st, "lrkv_decode_profiled")
-
-    split_timing = "eager"
-    with torch.cuda.stream(stream):
-        prof_calls(stream)  # warm, and the eager fallback
-    torch.cuda.synchronize()
-    if graph is not None:
-        try:
-            pg = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(pg, stream=stream, capture_error_mode="thread_local"):
-                prof_calls(torch.cuda.current_stream())
-            torch.cuda.synchronize()
-            pg.replay()
-            torch.cuda.synchronize()
-            pg.replay()
-            torch.cuda.synchronize()
-            split_timing = "graph"
-        except Exception as e:
-            print(f"profiled graph capture failed ({e}); using the eager timing", file=sys.stderr)
-            torch.cuda.synchronize()
-    split_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
-
-    # end to end through the public API: each step copies the new token's
-    # query, the lengths and the token's cache rows from pinned host memory
-    # (packed in one buffer: one host->device copy, then device-side placement
-    # into the resident cache), decodes, and reads out and lse back (one copy).
-    host_parts = [("q", case["q"].contiguous()), ("seq_lens", case["seq_lens"].contiguous())] + \
-        [(k, case[k][:, -1:].contiguous()) for k in ("k_s", "v_s", "z_k", "z_v")]
-    offs, n_in = [], 0
-    for k, v in host_parts:
-        offs.append(n_in)
-        n_in += (v.numel() * v.element_size() + 255) // 256 * 256
-    host_in = torch.zeros(n_in, dtype=torch.uint8).pin_memory()
-    dev_in = torch.empty(n_in, dtype=torch.uint8, device=dev)
-    in_views = []
-    for (k, v), o in zip(host_parts, offs):
-        nb = v.numel() * v.element_size()
-        host_in[o:o + nb].copy_(v.reshape(-1).view(torch.uint8))
-        in_views.append((k, dev_in[o:o + nb].view(v.dtype).view(v.shape)))
-    host_out_lse = torch.empty_like(out_lse, device="cpu").pin_memory()
-    h2d = sum(v.numel() * v.element_size() for _, v in host_parts)
-    d2h = host_out_lse.numel() * 4
-    K_e2e = min(K, 100)
-
-    def e2e_body(i, s=None):
-        x = reps[i % n_rep]
-        dev_in.copy_(host_in, non_blocking=True)
-        for k, v in in_views:
-            if k in ("q", "seq_lens"):
-                x[k].copy_(v)
-            else:
-                x[k][:, -1:].copy_(v)
-        step(i, s)
-        host_out_lse.copy_(out_lse, non_blocking=True)
-
-    # one CUDA graph per cache replica holds a step's copies and the decode
-    # call (as a serving loop replays its step); the host still waits for each
-    # step's outputs before the next step starts
-    e2e_graphs = None
-    if not a.no_graph:
-        try:
-            e2e_graphs = []
-            for r in range(n_rep):
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
-                    e2e_body(r, torch.cuda.current_stream())
-                e2e_graphs.append(g)
-            torch.cuda.synchronize()
-        except Exception as e:
-            print(f"end-to-end graph capture failed ({e}); eager steps", file=sys.stderr)
-            e2e_graphs = None
-            torch.cuda.synchronize()
-
-    def e2e_step(i):
-        if e2e_graphs is not None:
-            e2e_graphs[i % n_rep].replay()
-        else:
-            e2e_body(i)
-        stream.synchronize()
-
-    with torch.cuda.stream(stream):
-        for i in range(3):
-            e2e_step(i)
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for i in range(K_e2e):
-            e2e_step(i)
-        e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / K_e2e, world, dev)
-
-    # decode step: the new token's rows from its layer input (d_model =
-    # heads x head_dim), then the decode, as one call per step, from a graph
-    step_leg = None
-    if not a.no_graph:
-        d_model = w.heads * w.head_dim
-        g = torch.Generator().manual_seed(1234)
-        xs = torch.randn(w.batch, d_model, generator=g).to(torch.bfloat16).to(dev)
-        ws_rows = [(torch.randn(n, d_model, generator=g) / d_model ** 0.5).to(torch.bfloat16).to(dev)
-                   for n in (w.head_dim, w.head_dim, w.heads * w.rank, w.heads * w.rank)]
-
-        def fstep(i, s=None):
-            x = reps[i % n_rep]
-            st = lrkv.lrkv_decode_step(dims, d_model, xs, *ws_rows, x["q"], x["k_s"], x["v_s"], x["z_k"],
-                                       x["z_v"], x["b_k"], x["b_v"], x["seq_lens"], out, lse, ws, ws.numel(),
-                                       s or stream)
-            if st != lrkv.LRKV_OK:
-                raise lrkv.LRKVError(st, "lrkv_decode_step")
-
-        with torch.cuda.stream(stream):
-            for i in range(W):
-                fstep(i)
-        torch.cuda.synchronize()
-        fg = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(fg, stream=stream, capture_error_mode="thread_local"):
-            for i in range(K):
-                fstep(i, torch.cuda.current_stream())
-        torch.cuda.synchronize()
-        fg.replay()
-        torch.cuda.synchronize()
-        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            f0.record(stream)
-            fg.replay()
-            f1.record(stream)
-        torch.cuda.synchronize()
-        f_ms = max_over_ranks(f0.elapsed_time(f1) / K, world, dev)
-        w_bytes = sum(t.numel() * 2 for t in ws_rows)
-        rows_bytes = w.batch * 2 * (w.head_dim + w.heads * w.rank) * 2
-        step_leg = {"d_model": d_model, "ms_per_step": f_ms, "decode_ms_per_step": ms_step,
-                    "projection_ms_per_step": f_ms - ms_step,
-                    "algorithmic_bytes": total_bytes + w_bytes + xs.numel() * 2 + rows_bytes,
-                    "gbs": job_gbs(total_bytes + w_bytes + xs.numel() * 2 + rows_bytes, world, f_ms)}
-
-    # decode with post-projection RMSNorm of the keys: the cached reciprocal
-    # key scales (one fp32 per head and token) multiply the summed scores
-    normed_leg = None
-    if not a.no_graph:
-        kscales = []
-        for x in reps:
-            t = torch.empty((w.batch, w.heads, w.max_len), dtype=torch.float32, device=dev)
-            lrkv.key_scales(x["k_s"], x["z_k"], x["b_k"], torch.zeros(w.batch, dtype=torch.int32, device=dev),
-                            w.max_len, t, eps=1e-6)
-            kscales.append(t)
-        torch.cuda.synchronize()
-
-        def nstep(i, s=None):
-            x = reps[i % n_rep]
-            st = lrkv.lrkv_decode_normed(dims, x["q"], x["k_s"], x["v_s"], x["z_k"], x["z_v"], x["b_k"], x["b_v"],
-                                         kscales[i % n_rep], x["seq_lens"], out, lse, ws, ws.numel(), s or stream)
-            if st != lrkv.LRKV_OK:
-                raise lrkv.LRKVError(st, "lrkv_decode_normed")
-
-        with torch.cuda.stream(stream):
-            for i in range(W):
-                nstep(i)
-        torch.cuda.synchronize()
-        ng = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(ng, stream=stream, capture_error_mode="thread_local"):
-            for i in range(K):
-                nstep(i, torch.cuda.current_stream())
-        torch.cuda.synchronize()
-        ng.replay()
-        torch.cuda.synchronize()
-        n0, n1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            n0.record(stream)
-            ng.replay()
-            n1.record(stream)
-        torch.cuda.synchronize()
-        n_ms = max_over_ranks(n0.elapsed_time(n1) / K, world, dev)
-        scale_bytes = int(case["seq_lens"].long().sum()) * w.heads * 4
-        normed_leg = {"ms_per_step": n_ms, "decode_ms_per_step": ms_step,
-                      "algorithmic_bytes": total_bytes + scale_bytes,
-                      "gbs": job_gbs(total_bytes + scale_bytes, world, n_ms),
-                      "key_scale_bytes": scale_bytes}
-
-    # decode over a paged cache: the same rows in 256-row pages of a pool, in a
-    # seeded random page order, through a block table
-    paged_leg = None
-    if not a.no_graph:
-        page = 256
-        pc = inputs.paged_from_contiguous(case, page_size=page, seed=7)
-        pd = {k: v.to(dev) for k, v in pc.items()}
-        preps = [pd] + [{k: (v.clone() if k in ("k_s", "v_s", "z_k", "z_v") else v) for k, v in pd.items()}
-                        for _ in range(n_rep - 1)]
-        n_pages = pd["k_s"].shape[0]
-
-        def pstep(i, s=None):
-            x = preps[i % n_rep]
-            st = lrkv.lrkv_decode_paged(dims, page, n_pages, x["block_table"], x["q"], x["k_s"], x["v_s"],
-                                        x["z_k"], x["z_v"], x["b_k"], x["b_v"], x["seq_lens"], out, lse, ws,
-                                        ws.numel(), s or stream)
-            if st != lrkv.LRKV_OK:
-                raise lrkv.LRKVError(st, "lrkv_decode_paged")
-
-        with torch.cuda.stream(stream):
-            for i in range(W):
-                pstep(i)
-        torch.cuda.synchronize()
-        pg_graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(pg_graph, stream=stream, capture_error_mode="thread_local"):
-            for i in range(K):
-                pstep(i, torch.cuda.current_stream())
-        torch.cuda.synchronize()
-        pg_graph.replay()
-        torch.cuda.synchronize()
-        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            p0.record(stream)
-            pg_graph.replay()
-            p1.record(stream)
-        torch.cuda.synchronize()
-        p_ms = max_over_ranks(p0.elapsed_time(p1) / K, world, dev)
-        paged_leg = {"page_size": page, "pages": n_pages, "ms_per_step": p_ms, "decode_ms_per_step": ms_step,
-                     "gbs": job_gbs(total_bytes, world, p_ms)}
-        del preps, pd
+    # ---- the other decode workloads, and the decode step on the 4K one ----
+    legs, step_leg = {}, None
+    if not a.no_legs:
+        for name in inputs.DECODE_LEG_WORKLOADS:
+            s = DecodeSetup(inputs.WORKLOADS[name], dev, seed=rank)
+            leg, _ = decode_leg(s, K, W, stream, use_graph, peak, world, dev)
+            legs[name] = leg
+            if name == "decode_bf16_b8_h16_d64_r28_L4096":
+                step_leg = decode_step_leg(s, K, W, stream, use_graph, world, dev, leg["ms_per_step"])
+            del s
+            torch.cuda.empty_cache()
 
     prefill = None
     if not a.no_prefill:
@@ -721,47 +899,40 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
-        cpu = cpu_baseline(w, case, a.cpu_seconds, min(os.cpu_count() or 1, 16))
+        cpu = cpu_baseline(w, head.case, a.cpu_seconds, min(os.cpu_count() or 1, 16))
 
     if rank == 0:
-        peak, peak_kind = _peaks()
-        gbs = job_gbs(total_bytes, world, ms_step)
-        # the scan's average launch duration over the timed region: one scan
-        # launch per step, back to back (each launched ahead, programmatic
-        # dependent launch), the combine beside it on SMs the scan leaves free
-        achieved = split_bytes / (ms_step * 1e-3) / 1e9
-        isolated = split_bytes / (split_ms * 1e-3) / 1e9
-        traffic = _profile_traffic(_src_sha())
+        gbs = job_gbs(head.total_bytes, world, ms_step)
+        achieved = head.split_bytes / (iso * 1e-3) / 1e9
+        traffic = _profile_traffic(w.name, _src_sha())
         res = {
             "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
-            "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "ms_per_step": ms_step, "ms_per_step_spread": spread, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "accumulate": "f32", "data": "synthetic",
             "tokens_per_s": w.batch * world / (ms_step * 1e-3),
             "hbm_frac": gbs / world / peak,
             "config": {"workload": w.name, "batch": w.batch, "heads": w.heads, "head_dim": w.head_dim,
-                       "rank": w.rank, "seq_len": w.max_len,
+                       "rank": w.rank, "seq_len": w.max_len, "seq_len_sum": int(head.case["seq_lens"].long().sum()),
                        "cache_fraction_of_mha": 1 / w.heads + w.rank / w.head_dim,
-                       "bytes_per_step": total_bytes,
-                       "l2": f"{n_rep} rotating cache replicas ({n_rep * cache_bytes / 1e6:.0f} MB > L2 "
-                             f"{L2_BYTES / 1e6:.0f} MB)",
-                       "graph": graph is not None, "parallelism": f"replicas x{world}"},
+                       "bytes_per_step": head.total_bytes, "l2": head.l2,
+                       "graph": use_graph, "parallelism": f"replicas x{world}",
+                       "timing": f"median of {spread['n']} timed regions of {K} steps (graph replays, after "
+                                 f">= {WARM_MS:.0f} ms of warm replays)"},
             "roofline": {"bound": "hbm", "kernel": "lrkv_decode_stream_kernel", "achieved": achieved,
                          "peak": peak, "peak_kind": f"{peak_kind} HBM copy", "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
-                         "algorithmic_bytes_per_launch": split_bytes, "launch_ms": ms_step,
-                         "launch_timing": "CUDA events around the timed region of K back-to-back steps "
-                                          "(one scan launch per step) on the launching stream",
-                         "isolated_launch_ms": split_ms, "isolated_achieved": isolated,
-                         "isolated_frac": isolated / peak,
-                         "isolated_timing": f"CUDA events around each launch alone, {split_timing} launches "
-                                            "(includes the launch and drain the chained steps overlap)"},
+                         "algorithmic_bytes_per_launch": head.split_bytes, "launch_ms": iso,
+                         "launch_ms_min": iso_min, "launch_ms_max": iso_max,
+                         "launch_timing": f"CUDA events right around each isolated scan launch on the launching "
+                                          f"stream ({iso_kind} launches), median of {min(K, 20)}",
+                         "step_rate_gbs": head.split_bytes / (ms_step * 1e-3) / 1e9,
+                         "step_rate_frac": head.split_bytes / (ms_step * 1e-3) / 1e9 / peak},
             "cpu_baseline": cpu,
-            "e2e": {"value": job_gbs(total_bytes, world, e2e_ms), "unit": "GB/s",
-                    "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "graph": e2e_graphs is not None},
+            "e2e": e2e,
             # a bf16 step on the streaming path is two launches (scan, merge)
             "gpu_launches": 2 * K,
             "clocks": clk.summary(),
+            "decode_legs": legs or None,
             "decode_step": step_leg,
             "decode_normed": normed_leg,
             "decode_paged": paged_leg,

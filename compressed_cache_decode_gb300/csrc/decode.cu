@@ -92,6 +92,7 @@ __device__ __forceinline__ void issue_tile(const DecodePlan& P, const CUtensorMa
 // p_{b,h,c} = q_{b,h} . B_h^K[:, c] per thread.
 constexpr int kAbsorbSeq = 8;
 constexpr int kCombineCtas = 16;  // SMs the streaming scan leaves to the merge
+constexpr long long kLargeCacheBytes = 512ll << 20;  // see decode_make_plan
 
 template <bool BF16>
 __global__ void __launch_bounds__(256) lrkv_decode_absorb_kernel(const DecodePlan P) {
@@ -972,18 +973,30 @@ lrkv_status decode_make_plan(const lrkv_dims& d, int num_sms, DecodePlan& P, siz
   // CTAs; the streaming scan leaves it that many SMs, so that consecutive
   // steps' scans and merges overlap
   const long long pair_ctas = (static_cast<long long>(P.B) * H + kCombineWarps - 1) / kCombineWarps;
-  const int reserve = static_cast<int>(std::min<long long>(pair_ctas, kCombineCtas));
+  // A large cache (at least kLargeCacheBytes of rows at capacity) keeps every
+  // SM on the scan: a step is long, so the scan's streaming matters more
+  // than overlapping the merge with the next step's scan; the merge then
+  // gets one warp per (sequence, head) on as many SMs as that needs.
+  const long long cap_bytes = static_cast<long long>(P.B) * P.max_len * per_token;
+  const bool large = P.bf16 && cap_bytes >= kLargeCacheBytes;
+  const int reserve = large ? 0 : static_cast<int>(std::min<long long>(pair_ctas, kCombineCtas));
   P.grid = env_int("LRKV_DECODE_GRID", std::max(1, num_sms - reserve));
   // the streaming kernel's grid is (range CTAs, row tiles of 16 heads): it
   // divides P.grid by the row tiles
   if (P.bf16 && env_int("LRKV_DECODE_TILE_SYNC", 0) == 0) stream_plan(P);
   if (!P.stream) P.grid = env_int("LRKV_DECODE_GRID", num_sms);
-  P.combine_ctas = P.stream ? reserve : static_cast<int>(std::min<long long>(pair_ctas, 65535));
+  P.combine_ctas = P.stream && !large ? std::max(reserve, 1)
+                                      : static_cast<int>(std::min<long long>(pair_ctas, large ? num_sms : 65535));
   P.min_tokens = env_int("LRKV_DECODE_MIN_TOKENS", P.stream ? 8 * P.T : 2 * P.T);
   if (P.stream) {
-    // L2 prefetch window: about 48 MB in flight over all CTAs (L2 is 126 MB)
+    // L2 prefetch window: about 48 MB in flight over all CTAs (L2 is 126 MB).
+    // Only for a small cache read by one row tile: with several row tiles
+    // every CTA of a range would prefetch the same rows, and on a large
+    // cache the ring alone keeps HBM busier (measured: 0.51 -> 0.69 of the
+    // HBM peak on 4 x 64K rows of 32 heads without it).
     const long long per_cta = (48ll << 20) / std::max(1, P.grid * P.mt);
-    P.pfw = env_int("LRKV_DECODE_PREFETCH_TILES", static_cast<int>(per_cta / P.stage_bytes));
+    const int pfw = (large || P.mt > 1) ? 0 : static_cast<int>(per_cta / P.stage_bytes);
+    P.pfw = env_int("LRKV_DECODE_PREFETCH_TILES", pfw);
   }
   const int slots = (P.B + P.grid) * P.ngw;
   // per warp: the lift's z row, and the weights and denominators of one sequence's partials

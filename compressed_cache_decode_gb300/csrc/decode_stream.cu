@@ -35,6 +35,7 @@
 // tiles find it in the instruction cache.
 #include <cmath>
 #include <algorithm>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -345,6 +346,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
   constexpr int MZA = MZMAX > 0 ? MZMAX : 1;
   constexpr int BS = MZA > 16 ? 2 : 4;       // private-score steps per load batch
   constexpr int BZ = MZA > 16 ? 4 : 8;       // private-value steps per load batch
+  constexpr int KB = DHT > 4 ? 4 : DHT;      // head-dim steps per load batch of the shared rows
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ int s_timeout;
   __shared__ int s_nopage;  // a block table entry named no page of the pool
@@ -676,16 +678,17 @@ __global__ void __launch_bounds__(kThreadsS, 1)
         // four independent accumulation chains
         float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
         float la[4] = {0.f, 0.f, 0.f, 0.f}, lb[4] = {0.f, 0.f, 0.f, 0.f};
-        {
-          uint32_t a[DHT][4];
 #pragma unroll
-          for (int kk = 0; kk < DHT; ++kk) {
-            const int ch = 2 * kk + ahalf;
-            ldsm_x4(a[kk][0], a[kk][1], a[kk][2], a[kk][3], ks + (ch >> 3) * (kT * 128) + swz_off(arow, ch & 7, 128));
+        for (int k0 = 0; k0 < DHT; k0 += KB) {  // batches of KB head-dim steps (fewer live registers)
+          uint32_t a[KB][4];
+#pragma unroll
+          for (int u = 0; u < KB; ++u) {
+            const int ch = 2 * (k0 + u) + ahalf;
+            ldsm_x4(a[u][0], a[u][1], a[u][2], a[u][3], ks + (ch >> 3) * (kT * 128) + swz_off(arow, ch & 7, 128));
           }
 #pragma unroll
-          for (int kk = 0; kk < DHT; ++kk)
-            mma_bf16_16816((kk & 1) ? sb : sa, a[kk][0], a[kk][1], a[kk][2], a[kk][3], qb[kk][0], qb[kk][1]);
+          for (int u = 0; u < KB; ++u)
+            mma_bf16_16816(((k0 + u) & 1) ? sb : sa, a[u][0], a[u][1], a[u][2], a[u][3], qb[k0 + u][0], qb[k0 + u][1]);
         }
         if (MZMAX > 0) {
           const unsigned char* z0 = zk + arow * zrow + ahalf * 16;
@@ -754,16 +757,18 @@ __global__ void __launch_bounds__(kThreadsS, 1)
         const uint32_t pb1 = movmatrix_trans(pack_bf16(p2, p3));  // tokens 8-15
 
         // shared values: O_s^T += V_s^T P^T (rows = head dim)
-        {
-          uint32_t a[DHT][4];
 #pragma unroll
-          for (int n = 0; n < DHT; ++n) {
-            const int ch = 2 * n + tcol;
-            ldsm_x4_trans(a[n][0], a[n][1], a[n][2], a[n][3], vs + (ch >> 3) * (kT * 128) + swz_off(trow, ch & 7, 128));
+        for (int n0 = 0; n0 < DHT; n0 += KB) {
+          uint32_t a[KB][4];
+#pragma unroll
+          for (int u = 0; u < KB; ++u) {
+            const int ch = 2 * (n0 + u) + tcol;
+            ldsm_x4_trans(a[u][0], a[u][1], a[u][2], a[u][3], vs + (ch >> 3) * (kT * 128) + swz_off(trow, ch & 7, 128));
           }
 #pragma unroll
-          for (int n = 0; n < DHT; ++n)
-            mma_bf16_16816(acc_v[n], a[n][0] & keep0, a[n][1] & keep0, a[n][2] & keep1, a[n][3] & keep1, pb0, pb1);
+          for (int u = 0; u < KB; ++u)
+            mma_bf16_16816(acc_v[n0 + u], a[u][0] & keep0, a[u][1] & keep0, a[u][2] & keep1, a[u][3] & keep1, pb0,
+                           pb1);
         }
         // private values: O_z^T += Z_v^T P^T over this half's latent columns
         if (MZMAX > 0) {
@@ -879,13 +884,21 @@ namespace {
 using StreamFn = void (*)(const DecodePlan, const CUtensorMap, const CUtensorMap, const CUtensorMap,
                           const CUtensorMap);
 
-int mz_max_of(const DecodePlan& P) { return P.r == 0 ? 0 : (P.kst <= 16 ? 16 : 32); }
+// The latent steps a warp keeps accumulators for: the smallest instantiated
+// count >= kst (accumulators sized exactly for the common ranks 48 and 56
+// keep the kernel free of register spills).
+int mz_max_of(const DecodePlan& P) {
+  if (P.r == 0) return 0;
+  return P.kst <= 16 ? 16 : P.kst <= 24 ? 24 : P.kst <= 28 ? 28 : 32;
+}
 
 template <int DHT>
 StreamFn pick_mz(const DecodePlan& P) {
   switch (mz_max_of(P)) {
     case 0: return lrkv_decode_stream_kernel<DHT, 0>;
     case 16: return lrkv_decode_stream_kernel<DHT, 16>;
+    case 24: return lrkv_decode_stream_kernel<DHT, 24>;
+    case 28: return lrkv_decode_stream_kernel<DHT, 28>;
     default: return lrkv_decode_stream_kernel<DHT, 32>;
   }
 }
@@ -967,8 +980,10 @@ static lrkv_status stream_plan_impl(DecodePlan& P) {
     return off + 1024;  // alignment slack
   };
   const int budget = 226 * 1024;  // opt-in limit (227 KB) less static shared memory
+  const char* cap_env = std::getenv("LRKV_DECODE_STREAM_STAGES");  // tuning: at most this many stages
+  const int cap = (cap_env && *cap_env) ? std::max(2, std::atoi(cap_env)) : 16;
   int stages = 0;
-  while (stages < 16 && layout(stages + 1) <= budget) ++stages;
+  while (stages < std::min(16, cap) && layout(stages + 1) <= budget) ++stages;
   if (stages < 2) return LRKV_ERR_UNSUPPORTED;
   P.stages = stages;
   P.smem_bytes = layout(P.stages);

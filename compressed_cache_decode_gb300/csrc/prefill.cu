@@ -680,11 +680,9 @@ bool make_map(CUtensorMap* m, const void* base, int n, const uint64_t* dims, con
 
 }  // namespace
 
-static lrkv_status prefill_impl(const lrkv_dims* dims, int q_len, const void* q, const void* k_s,
-                                const void* v_s, const void* z_k, const void* z_v, const void* b_k,
-                                const void* b_v, const float* key_scale, const int32_t* seq_lens, float* out,
-                                float* lse, void* ws, size_t ws_bytes, lrkv_stream_t stream,
-                                const int32_t* block_table = nullptr, int page_size = 0, int num_pages = 0) {
+// Host checks of the prefill shape (no pointers): LRKV_OK when the kernel
+// implements it.
+static lrkv_status check_prefill_dims(const lrkv_dims* dims, int q_len) {
   if (!dims) return LRKV_ERR_INVALID_ARG;
   const lrkv_dims& d = *dims;
   if (d.batch < 1 || d.heads < 1 || d.head_dim < 1 || d.rank < 0 || d.max_len < 1 || q_len < 1)
@@ -693,10 +691,34 @@ static lrkv_status prefill_impl(const lrkv_dims* dims, int q_len, const void* q,
   if (!(d.scale == d.scale)) return LRKV_ERR_INVALID_ARG;
   if (d.dtype != LRKV_BF16 || d.head_dim != 128 || d.rank != 64) return LRKV_ERR_UNSUPPORTED;
   if (q_len > d.max_len || d.heads > 65535 || d.batch > 65535) return LRKV_ERR_UNSUPPORTED;
+  return LRKV_OK;
+}
+
+// The prefill's workspace: the device status word (the kernel needs no other
+// scratch memory).
+constexpr size_t kPrefillWorkspaceBytes = 16;
+
+extern "C" lrkv_status lrkv_prefill_workspace_size(const lrkv_dims* dims, int q_len, size_t* bytes) {
+  if (!bytes) return LRKV_ERR_INVALID_ARG;
+  const lrkv_status st = check_prefill_dims(dims, q_len);
+  if (st != LRKV_OK) return st;
+  *bytes = kPrefillWorkspaceBytes;
+  return LRKV_OK;
+}
+
+static lrkv_status prefill_impl(const lrkv_dims* dims, int q_len, const void* q, const void* k_s,
+                                const void* v_s, const void* z_k, const void* z_v, const void* b_k,
+                                const void* b_v, const float* key_scale, const int32_t* seq_lens, float* out,
+                                float* lse, void* ws, size_t ws_bytes, lrkv_stream_t stream,
+                                const int32_t* block_table = nullptr, int page_size = 0, int num_pages = 0) {
+  const lrkv_status cst = check_prefill_dims(dims, q_len);
+  if (cst != LRKV_OK) return cst;
+  const lrkv_dims& d = *dims;
   if (!q || !k_s || !v_s || !z_k || !z_v || !b_k || !b_v || !seq_lens || !out) return LRKV_ERR_INVALID_ARG;
   if (!a16p(q) || !a16p(k_s) || !a16p(v_s) || !a16p(z_k) || !a16p(z_v) || !a16p(b_k) || !a16p(b_v) || !a16p(out))
     return LRKV_ERR_INVALID_ARG;
-  if (!ws || ws_bytes < 16) return LRKV_ERR_WORKSPACE;
+  if (!ws || ws_bytes < kPrefillWorkspaceBytes) return LRKV_ERR_WORKSPACE;
+  if (!a16p(ws)) return LRKV_ERR_INVALID_ARG;
 
   const int B = d.batch, H = d.heads, Lm = d.max_len;
   const uint64_t dh = 128, r = 64;

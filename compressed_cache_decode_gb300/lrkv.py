@@ -38,6 +38,7 @@ EXPORTED = (
     "lrkv_decode_static_scratch",
     "lrkv_append",
     "lrkv_prefill",
+    "lrkv_prefill_workspace_size",
     "lrkv_decode_step",
     "lrkv_key_scales",
     "lrkv_decode_normed",
@@ -109,6 +110,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.lrkv_decode_step.restype = ctypes.c_int
     lib.lrkv_decode_step.argtypes = [dims_p, ctypes.c_int, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                      i32p, vp, vp, vp, sz, vp]
+    lib.lrkv_prefill_workspace_size.restype = ctypes.c_int
+    lib.lrkv_prefill_workspace_size.argtypes = [dims_p, ctypes.c_int, ctypes.POINTER(sz)]
     lib.lrkv_prefill.restype = ctypes.c_int
     lib.lrkv_prefill.argtypes = [dims_p, ctypes.c_int, vp, vp, vp, vp, vp, vp, vp, i32p, vp, vp, vp, sz,
                                  vp]
@@ -352,6 +355,14 @@ def decode_step(x: torch.Tensor, w_sk: torch.Tensor, w_sv: torch.Tensor, u_k: to
     return out, lse
 
 
+def lrkv_prefill_workspace_size(dims: lrkv_dims, q_len: int) -> int:
+    n = ctypes.c_size_t(0)
+    st = load().lrkv_prefill_workspace_size(ctypes.byref(dims), int(q_len), ctypes.byref(n))
+    if st != LRKV_OK:
+        raise LRKVError(st, "lrkv_prefill_workspace_size")
+    return int(n.value)
+
+
 def lrkv_prefill(dims: lrkv_dims, q_len: int, q, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens, out, lse,
                  ws, ws_bytes: int, stream=None) -> int:
     """Direct call of the prefill entry point; returns its status code."""
@@ -382,7 +393,7 @@ def prefill(q: torch.Tensor, k_s: torch.Tensor, v_s: torch.Tensor, z_k: torch.Te
     if lse is None:
         lse = torch.empty((B, H, Tq), dtype=torch.float32, device=q.device)
     if ws is None:
-        ws = torch.zeros(16, dtype=torch.uint8, device=q.device)
+        ws = torch.zeros(lrkv_prefill_workspace_size(dims, Tq), dtype=torch.uint8, device=q.device)
     st = lrkv_prefill(dims, Tq, q, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens, out, lse, ws, ws.numel(),
                       stream)
     if st != LRKV_OK:
@@ -404,7 +415,7 @@ def prefill_normed(q: torch.Tensor, k_s: torch.Tensor, v_s: torch.Tensor, z_k: t
     if lse is None:
         lse = torch.empty((B, H, Tq), dtype=torch.float32, device=q.device)
     if ws is None:
-        ws = torch.zeros(16, dtype=torch.uint8, device=q.device)
+        ws = torch.zeros(lrkv_prefill_workspace_size(dims, Tq), dtype=torch.uint8, device=q.device)
     st = lrkv_prefill_normed(dims, Tq, q, k_s, v_s, z_k, z_v, b_k, b_v, key_scale, seq_lens, out, lse, ws,
                              ws.numel(), stream)
     if st != LRKV_OK:
@@ -499,7 +510,7 @@ def prefill_paged(q, k_s, v_s, z_k, z_v, b_k, b_v, block_table, seq_lens, scale:
     if lse is None:
         lse = torch.empty((B, H, Tq), dtype=torch.float32, device=q.device)
     if ws is None:
-        ws = torch.zeros(16, dtype=torch.uint8, device=q.device)
+        ws = torch.zeros(lrkv_prefill_workspace_size(dims, Tq), dtype=torch.uint8, device=q.device)
     st = int(load().lrkv_prefill_paged(ctypes.byref(dims), Tq, _ptr(q), page_size, num_pages, _ptr(block_table),
                                        _ptr(k_s), _ptr(v_s), _ptr(z_k), _ptr(z_v), _ptr(b_k), _ptr(b_v),
                                        _ptr(seq_lens), _ptr(out), _ptr(lse), _ptr(ws), ws.numel(),

@@ -220,7 +220,8 @@ lrkv_status lrkv_append(const lrkv_dims* dims, int d_model, int n_new, const voi
  *            seq_lens[b] - q_len + i and sees keys j <= that position
  *   out      [batch][q_len][heads][head_dim] fp32
  *   lse      [batch][heads][q_len] fp32 or NULL (natural log)
- *   ws, ws_bytes >= 16                         device status word
+ *   ws, ws_bytes >= lrkv_prefill_workspace_size()  device status word (16-byte
+ *                                              aligned)
  * q_h B_h^K enters its tensor-core contraction with the latents as the sum
  * of two bf16 parts (about 16 significant bits).  Supported: dtype BF16,
  * head_dim 128, rank 64.  seq_lens[b]
@@ -230,6 +231,19 @@ lrkv_status lrkv_prefill(const lrkv_dims* dims, int q_len, const void* q, const 
                          const void* z_k, const void* z_v, const void* b_k, const void* b_v,
                          const int32_t* seq_lens, float* out, float* lse, void* ws, size_t ws_bytes,
                          lrkv_stream_t stream);
+
+/*
+ * Bytes of device workspace lrkv_prefill, lrkv_prefill_normed and
+ * lrkv_prefill_paged need for `dims` and `q_len` queries per sequence
+ * ("Low-Rank Key Value Attention | What a shared cache can preserve", §3: the
+ * prefill is Algorithm 2 for a block of causal queries).  The workspace holds
+ * the device status word; the prefill kernel keeps its partial results on
+ * chip and needs no other scratch memory.  Returns LRKV_ERR_INVALID_ARG or
+ * LRKV_ERR_UNSUPPORTED for the shapes lrkv_prefill rejects (the same checks,
+ * without the pointers); a prefill given fewer bytes returns
+ * LRKV_ERR_WORKSPACE and enqueues nothing.
+ */
+lrkv_status lrkv_prefill_workspace_size(const lrkv_dims* dims, int q_len, size_t* bytes);
 
 /*
  * One decode step of a layer: the new token's cache rows from its layer

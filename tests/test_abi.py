@@ -173,3 +173,31 @@ def test_paged_appends_reject_bad_paging_without_gpu(lib):
                                       fake, fake, fake, 1 << 20, None) == lrkv.LRKV_ERR_INVALID_ARG  # > max_len
     assert lib.lrkv_decode_step_paged(ctypes.byref(bf), 256, *w, fake, 64, 0, fake, *cache, fake, fake, fake,
                                       fake, fake, fake, 1 << 20, None) == lrkv.LRKV_ERR_INVALID_ARG  # no pages
+
+
+def test_prefill_workspace_size_and_rejection_without_gpu(lib):
+    """The prefill's workspace query checks the shape like the prefill does,
+    and a prefill given fewer bytes is rejected before any launch."""
+    n = ctypes.c_size_t(0)
+    d = lrkv.make_dims(2, 32, 128, 64, 4096, "bf16")
+    assert lib.lrkv_prefill_workspace_size(ctypes.byref(d), 4096, ctypes.byref(n)) == lrkv.LRKV_OK
+    assert n.value == 16 == lrkv.lrkv_prefill_workspace_size(d, 4096)
+    assert lib.lrkv_prefill_workspace_size(None, 16, ctypes.byref(n)) == lrkv.LRKV_ERR_INVALID_ARG
+    assert lib.lrkv_prefill_workspace_size(ctypes.byref(d), 16, None) == lrkv.LRKV_ERR_INVALID_ARG
+    assert lib.lrkv_prefill_workspace_size(ctypes.byref(d), 0, ctypes.byref(n)) == lrkv.LRKV_ERR_INVALID_ARG
+    assert lib.lrkv_prefill_workspace_size(ctypes.byref(d), 8192, ctypes.byref(n)) == \
+        lrkv.LRKV_ERR_UNSUPPORTED                                          # q_len > max_len
+    other = lrkv.make_dims(2, 32, 64, 64, 4096, "bf16")
+    assert lib.lrkv_prefill_workspace_size(ctypes.byref(other), 16, ctypes.byref(n)) == lrkv.LRKV_ERR_UNSUPPORTED
+    fake = ctypes.c_void_p(4096)  # aligned, never dereferenced: the checks fail first
+    pre = (fake,) * 8             # q, the cache, the bases, seq_lens
+    need = lrkv.lrkv_prefill_workspace_size(d, 128)
+    for call, extra in ((lib.lrkv_prefill, ()), (lib.lrkv_prefill_normed, None)):
+        args = pre if extra is not None else (fake,) * 7 + (fake, fake)   # normed: + key_scale before seq_lens
+        assert call(ctypes.byref(d), 128, *args, fake, fake, fake, need - 1, None) == lrkv.LRKV_ERR_WORKSPACE
+        assert call(ctypes.byref(d), 128, *args, fake, fake, None, need, None) == lrkv.LRKV_ERR_WORKSPACE
+        assert call(ctypes.byref(d), 128, *args, fake, fake, ctypes.c_void_p(4096 + 8), need, None) == \
+            lrkv.LRKV_ERR_INVALID_ARG                                      # misaligned workspace
+    paged = (fake,) * 6 + (fake,)  # k_s .. b_v, seq_lens
+    assert lib.lrkv_prefill_paged(ctypes.byref(d), 128, fake, 128, 64, fake, *paged, fake, fake, fake, need - 1,
+                                  None) == lrkv.LRKV_ERR_WORKSPACE
