@@ -59,6 +59,8 @@ constexpr int kWarps = kStreamConsumers;     // token streams per CTA
 constexpr int kThreadsS = 32 * kWarps;
 constexpr int kPairs = kWarps / 2;           // a tile is shared by a pair (8 heads each)
 constexpr float kRescaleLog2 = 8.f;          // raise the reference max only past 2^8
+constexpr int kCursorOff = 640;              // shared bytes of the pairs' tile cursors (2 per pair)
+constexpr int kHeaderBytes = 1024;           // barriers, stage records, step offsets, cursors
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -370,7 +372,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
   uint64_t* pbar = reinterpret_cast<uint64_t*>(smem + 256);  // [2] p/q buffers
   int* zo = reinterpret_cast<int*>(smem + 320);       // [2][32] latent step offsets
   int* pre = reinterpret_cast<int*>(smem + P.off_prefix);
-  uint4* pf = reinterpret_cast<uint4*>(smem + P.off_pf);    // private-score B fragments
+  uint2* qf = reinterpret_cast<uint2*>(smem + P.off_pf);    // shared-score B fragments (q)
 
   // ---- 1. barriers, sequence starts (clamped lengths) ----------------------
   {
@@ -492,12 +494,21 @@ __global__ void __launch_bounds__(kThreadsS, 1)
   uint2 bkv[kBkChunk];
   if (P.bk_stages == 0) bk_load(P, m0, bkr, 0, bkv);
 
-  uint32_t qb[DHT][2] = {};      // q of head 8 hf + g as the B operand (k = head dim)
   float acc_v[DHT][4] = {};      // O_s^T: rows d = 16 m + g (+8), columns heads 2 q4 + e
   float acc_z[MZA][4] = {};      // O_z^T: rows latent column j = 16 m + g (+8) of this half
   float mc[2] = {-INFINITY, -INFINITY}, lc[2] = {0.f, 0.f};  // reference max, denominator
   const int zrow = P.segp * 2;  // bytes per segment row
   const int hb = 8 * hf;        // first head (row-tile local) of this half
+  const uint2* qfl = qf + hf * DHT * 32 + lane;   // this lane's q fragments
+  const unsigned char* pqcur = smem + P.off_pq;  // the current piece's q / p buffer
+  // steps kk whose latent column 16 kk + 2 q4 (bit of vmask0), or that
+  // column + 8 (vmask1), belongs to this lane's head g within the half
+  uint32_t vmask0 = 0u, vmask1 = 0u;
+  for (int kk = 0; kk < P.kst; ++kk) {
+    const int j = 16 * kk + 2 * q4;
+    vmask0 |= (j / r == g ? 1u : 0u) << kk;
+    vmask1 |= ((j + 8) / r == g ? 1u : 0u) << kk;
+  }
 
   // The last warp, when it has no absorb role, first runs one tile of the
   // scan's code on no tokens (nvalid 0: every score is masked, no value row
@@ -543,10 +554,18 @@ __global__ void __launch_bounds__(kThreadsS, 1)
   }
   int ibase = 0;      // tile index of the piece's first tile
   int kp = warm ? -1 : 0;  // piece counter (p/q buffer kp & 1); -1: the warm-up pass
-  TileCursor refill;  // tiles this pair issues (its tile + stages)
-  refill.more = piece_first(refill.pc, pre, B, g0, g1, P.block_table != nullptr);
-  refill.ibase = 0;
-  TileCursor pfcur = refill;  // tiles this pair prefetches into L2
+  // this pair's cursors over its tiles to issue (tile + stages) and to
+  // prefetch into L2, kept in shared memory (used once per tile, by lane 0
+  // of whichever warp of the pair refills; the stage counters' atomics order
+  // the two warps' turns)
+  TileCursor* pcur = reinterpret_cast<TileCursor*>(smem + kCursorOff) + 2 * pair;
+  if (hf == 0 && lane == 0) {
+    TileCursor c0;
+    c0.more = piece_first(c0.pc, pre, B, g0, g1, P.block_table != nullptr);
+    c0.ibase = 0;
+    pcur[0] = c0;
+    pcur[1] = c0;
+  }
   while (more) {
     const bool dry = kp < 0;
     if (!dry) {
@@ -570,6 +589,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       if (!ok) *reinterpret_cast<volatile int*>(&s_timeout) = 1;
     }
     unsigned char* pqb = smem + P.off_pq + buf * P.pq_bytes;
+    pqcur = pqb;
     const int nh = min(16, H - m0);
     if (MZMAX > 0 && kp >= 2) {  // p of a third or later piece (the first two came before)
       uint2 v[kBkChunk];
@@ -577,16 +597,6 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       absorb_rows(P, m0, bkr, v, reinterpret_cast<const __nv_bfloat16*>(pqb), nullptr,
                   reinterpret_cast<float*>(pqb + 16 * dh * 2), nullptr);
       named_sync(1, kThreadsS);  // p rows ready
-    }
-    {
-      const __nv_bfloat16* qsm = reinterpret_cast<const __nv_bfloat16*>(pqb);
-      const int hl = hb + g;
-#pragma unroll
-      for (int kk = 0; kk < DHT; ++kk) {
-        const int k = kk * 16 + 2 * q4;
-        qb[kk][0] = hl < nh ? *reinterpret_cast<const uint32_t*>(qsm + hl * dh + k) : 0u;
-        qb[kk][1] = hl < nh ? *reinterpret_cast<const uint32_t*>(qsm + hl * dh + k + 8) : 0u;
-      }
     }
     mc[0] = mc[1] = -INFINITY;
     lc[0] = lc[1] = 0.f;
@@ -598,26 +608,36 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     for (int n = 0; n < MZA; ++n)
 #pragma unroll
       for (int k = 0; k < 4; ++k) acc_z[n][k] = 0.f;
-    if (MZMAX > 0) {
-      // B fragment of k step kk of half h2 for lane L: {hi(b0), hi(b1),
-      // lo(b0), lo(b1)}, b0 = rows j, j+1 and b1 = rows j+8, j+9
-      // (j = 16 (h2 kst + kk) + 2 (L & 3)) of head 8 h2 + (L >> 2).
-      const float* ps = reinterpret_cast<const float*>(pqb + 16 * dh * 2);
-      const int nent = 2 * P.kst * 32;
-      for (int e = tid; e < (tid < nset ? nent : 0); e += nset) {
-        const int k = e >> 5, L = e & 31;
-        const int hl = 8 * (k >= P.kst ? 1 : 0) + (L >> 2);
-        const int j = 16 * k + 2 * (L & 3);
-        float hi[4], lo[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int cc = j + (u & 1) + 8 * (u >> 1) - hl * r;
-          const float v = (hl < nh && cc >= 0 && cc < r) ? ps[hl * r + cc] : 0.f;
-          hi[u] = __bfloat162float(__float2bfloat16_rn(v));
-          lo[u] = v - hi[u];
+    {
+      // q as the B operand of the shared scores: entry (h2, kk, L) holds
+      // q[hl][k, k+1] and q[hl][k+8, k+9] of head hl = 8 h2 + (L >> 2),
+      // k = 16 kk + 2 (L & 3), zero past H: one conflict-free 8-byte load
+      // per step and lane in the tile loop
+      const __nv_bfloat16* qsm = reinterpret_cast<const __nv_bfloat16*>(pqb);
+      const int nq = 2 * DHT * 32;
+      for (int e = tid; e < (tid < nset ? nq : 0); e += nset) {
+        const int L = e & 31, kk = (e >> 5) % DHT, h2 = (e >> 5) / DHT;
+        const int hl = 8 * h2 + (L >> 2), k = 16 * kk + 2 * (L & 3);
+        uint2 v = make_uint2(0u, 0u);
+        if (hl < nh) {
+          v.x = *reinterpret_cast<const uint32_t*>(qsm + hl * dh + k);
+          v.y = *reinterpret_cast<const uint32_t*>(qsm + hl * dh + k + 8);
         }
-        pf[e] = make_uint4(pack_bf16(hi[0], hi[1]), pack_bf16(hi[2], hi[3]), pack_bf16(lo[0], lo[1]),
-                           pack_bf16(lo[2], lo[3]));
+        qf[e] = v;
+      }
+    }
+    if (MZMAX > 0) {
+      // p of the row tile's heads as bf16 high and low parts, head-major in
+      // pairs of latent columns: entry e = hl r/2 + c/2 holds
+      // {hi(p[c]), hi(p[c+1])}, {lo(p[c]), lo(p[c+1])} (zero past H), written
+      // over the fp32 p rows in place (the same 8 bytes per entry)
+      float2* pr = reinterpret_cast<float2*>(pqb + 16 * dh * 2);
+      const int np = 16 * (r / 2);
+      for (int e = tid; e < (tid < nset ? np : 0); e += nset) {
+        const float2 v = e / (r / 2) < nh ? pr[e] : make_float2(0.f, 0.f);
+        const float h0 = __bfloat162float(__float2bfloat16_rn(v.x));
+        const float h1 = __bfloat162float(__float2bfloat16_rn(v.y));
+        reinterpret_cast<uint2*>(pr)[e] = make_uint2(pack_bf16(h0, h1), pack_bf16(v.x - h0, v.y - h1));
       }
     }
     if (!split) {
@@ -681,33 +701,43 @@ __global__ void __launch_bounds__(kThreadsS, 1)
 #pragma unroll
         for (int k0 = 0; k0 < DHT; k0 += KB) {  // batches of KB head-dim steps (fewer live registers)
           uint32_t a[KB][4];
+          uint2 qv[KB];
 #pragma unroll
           for (int u = 0; u < KB; ++u) {
             const int ch = 2 * (k0 + u) + ahalf;
             ldsm_x4(a[u][0], a[u][1], a[u][2], a[u][3], ks + (ch >> 3) * (kT * 128) + swz_off(arow, ch & 7, 128));
+            qv[u] = qfl[(k0 + u) * 32];
           }
 #pragma unroll
           for (int u = 0; u < KB; ++u)
-            mma_bf16_16816(((k0 + u) & 1) ? sb : sa, a[u][0], a[u][1], a[u][2], a[u][3], qb[k0 + u][0], qb[k0 + u][1]);
+            mma_bf16_16816(((k0 + u) & 1) ? sb : sa, a[u][0], a[u][1], a[u][2], a[u][3], qv[u].x, qv[u].y);
         }
         if (MZMAX > 0) {
+          // B fragment of step kk (latent columns j = 16 kk + 2 q4 (+1, +8,
+          // +9) of this half; column g = head hb + g): the pairs 8 kk + q4 and
+          // 8 kk + q4 + 4 of the half's p table, kept where their head is g
+          // (bit kk of vmask0 / vmask1) and zero elsewhere (block diagonal)
           const unsigned char* z0 = zk + arow * zrow + ahalf * 16;
           const int* zoh = zo + 32 * hf;
-          const uint4* pfl = pf + hf * P.kst * 32 + lane;
+          const uint2* pt = reinterpret_cast<const uint2*>(pqcur + 16 * dh * 2) + 4 * hf * r + q4;
           for (int kk = 0; kk < P.kst; kk += BS) {  // batches of BS steps (kst is even)
             uint32_t a[BS][4];
-            uint4 f[BS];
+            uint2 f0[BS], f1[BS];
 #pragma unroll
             for (int u = 0; u < BS; ++u)
               if (u < 2 || kk + u < P.kst) {
                 ldsm_x4(a[u][0], a[u][1], a[u][2], a[u][3], z0 + zoh[kk + u]);
-                f[u] = pfl[(kk + u) * 32];
+                f0[u] = pt[8 * (kk + u)];
+                f1[u] = pt[8 * (kk + u) + 4];
               }
 #pragma unroll
             for (int u = 0; u < BS; ++u)
               if (u < 2 || kk + u < P.kst) {
-                mma_bf16_16816((u & 1) ? sb : sa, a[u][0], a[u][1], a[u][2], a[u][3], f[u].x, f[u].y);
-                mma_bf16_16816((u & 1) ? lb : la, a[u][0], a[u][1], a[u][2], a[u][3], f[u].z, f[u].w);
+                const bool k0v = (vmask0 >> (kk + u)) & 1u, k1v = (vmask1 >> (kk + u)) & 1u;
+                const uint32_t h0 = k0v ? f0[u].x : 0u, l0 = k0v ? f0[u].y : 0u;
+                const uint32_t h1 = k1v ? f1[u].x : 0u, l1 = k1v ? f1[u].y : 0u;
+                mma_bf16_16816((u & 1) ? sb : sa, a[u][0], a[u][1], a[u][2], a[u][3], h0, h1);
+                mma_bf16_16816((u & 1) ? lb : la, a[u][0], a[u][1], a[u][2], a[u][3], l0, l1);
               }
           }
         }
@@ -794,24 +824,35 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       const int j = i + P.stages;
       fence_proxy_async_smem();  // this warp's generic accesses before the async writes
       __syncwarp();
-      int second = 0;
-      if (lane == 0) second = (atomicAdd(&cons[s], 1) & 1);
-      second = __shfl_sync(0xffffffffu, second, 0);
-      if (second && refill.seek(j, pre, B, g1)) {
-        fence_proxy_async_smem();
-        if (ok && lane == 0) {
-          if (!stream_issue(P, &tm_k, &tm_v, &tm_zk, &tm_zv, smem, full, s, refill.pc.b,
-                            refill.pc.t_beg + (j - refill.ibase) * kT, zseg0))
-            *reinterpret_cast<volatile int*>(&s_nopage) = 1;
-          *reinterpret_cast<volatile int*>(&issued[s]) = j;
-        }
-        // keep the L2 prefetch window pfw tiles ahead of the ring
-        const int jp = j + P.pfw;
-        if (ok && lane == 0 && P.pfw > 0 && pfcur.seek(jp, pre, B, g1)) {
-          const int rr = pfcur.pc.t_beg + (jp - pfcur.ibase) * kT;
-          l2_prefetch_rows(P, pfcur.pc.b, rr, min(pfcur.pc.t_end, rr + kT));
+      if (lane == 0) {
+        __threadfence_block();  // this warp's cursor writes before its count (release)
+        const bool second = (atomicAdd(&cons[s], 1) & 1) != 0;
+        __threadfence_block();  // the other warp's cursor writes after its count (acquire)
+        if (second) {
+          TileCursor rc = pcur[0];
+          if (rc.seek(j, pre, B, g1)) {
+            fence_proxy_async_smem();
+            if (ok) {
+              if (!stream_issue(P, &tm_k, &tm_v, &tm_zk, &tm_zv, smem, full, s, rc.pc.b,
+                                rc.pc.t_beg + (j - rc.ibase) * kT, zseg0))
+                *reinterpret_cast<volatile int*>(&s_nopage) = 1;
+              *reinterpret_cast<volatile int*>(&issued[s]) = j;
+            }
+            // keep the L2 prefetch window pfw tiles ahead of the ring
+            const int jp = j + P.pfw;
+            if (ok && P.pfw > 0) {
+              TileCursor pfc = pcur[1];
+              if (pfc.seek(jp, pre, B, g1)) {
+                const int rr = pfc.pc.t_beg + (jp - pfc.ibase) * kT;
+                l2_prefetch_rows(P, pfc.pc.b, rr, min(pfc.pc.t_end, rr + kT));
+              }
+              pcur[1] = pfc;
+            }
+          }
+          pcur[0] = rc;
         }
       }
+      __syncwarp();
     }
 
     if (dry) {  // warm-up pass done: the real first piece
@@ -968,11 +1009,11 @@ static lrkv_status stream_plan_impl(DecodePlan& P) {
   while (r > 0 && 16 * (r / 4) * P.bk_dsplit * 2 <= kThreadsS && P.bk_dsplit * 2 <= dh / 4) P.bk_dsplit *= 2;
   P.bk_warps = r > 0 ? (16 * (r / 4) * P.bk_dsplit + 31) / 32 : 1;
   P.stage_bytes = round_up(2 * P.kv_bytes + 2 * P.zt_bytes, 1024);
-  const int pf_bytes = 2 * P.kst * 32 * 16;
+  const int pf_bytes = 2 * (dh / 16) * 32 * 8;  // q fragments of both halves
 
   // shared memory: barriers | prefix | p/q buffers | p fragments | ring
   auto layout = [&](int stages) {
-    int off = 640;  // barriers, stage records, step offsets
+    int off = kHeaderBytes;  // barriers, stage records, step offsets, tile cursors
     P.off_prefix = off; off = round_up(off + (P.B + 1) * 4, 128);
     P.off_pq = off; off = round_up(off + 2 * P.pq_bytes, 128);
     P.off_pf = off; off = round_up(off + std::max(pf_bytes, 16), 1024);
