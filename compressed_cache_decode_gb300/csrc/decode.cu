@@ -761,6 +761,118 @@ __global__ void __launch_bounds__(32 * kCombineWarps) lrkv_decode_combine_kernel
   }
 }
 
+// ================================================================ wide merge
+// The merge of a large cache's decode: one CTA per (sequence b, head h),
+// grid-stride.  The partials of the sequence's pieces are split over the 8
+// warps (warp w takes partials w, w + 8, ...); each warp merges its share
+// against its own largest maximum (lanes own columns of [acc_s | acc_z]),
+// the CTA merges the 8 warp results through shared memory with the same
+// log-sum-exp rule, then lifts the private sum: o = acc_s / L +
+// (acc_z / L) (B_h^V)^T and lse = (M + log2 L) ln 2 (Algorithm 2 steps 06-09).
+// Spread over every SM it reads the partials at once instead of one warp per
+// (sequence, head) walking all of them.
+constexpr int kWideWarps = 8;
+
+template <bool BF16, int KC>  // KC: columns per lane, ceil((dh + r) / 32)
+__global__ void __launch_bounds__(32 * kWideWarps) lrkv_decode_merge_wide_kernel(const DecodePlan P) {
+  __shared__ float s_m[kWideWarps], s_l[kWideWarps];
+  __shared__ float s_acc[kWideWarps][32 * KC];
+  __shared__ float s_z[kMaxRank];
+  __shared__ float s_os[256];  // acc_s / L (head_dim <= 256)
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int H = P.H, dh = P.dh, r = P.r, W = dh + r;
+  pdl_trigger();  // the next step's scan may launch (it waits before it writes)
+  pdl_wait();
+  const long long N = P.meta[0], G = P.meta[1];
+  const long long npairs = static_cast<long long>(P.B) * H;
+  const size_t mstep = static_cast<size_t>(H) * 2, astep = static_cast<size_t>(H) * W;
+  for (long long bh = blockIdx.x; bh < npairs; bh += gridDim.x) {
+    const int b = static_cast<int>(bh / H), h = static_cast<int>(bh % H);
+    float* o = P.out + (static_cast<size_t>(b) * H + h) * dh;
+    const int start = P.prefix[b], end = P.prefix[b + 1];
+    if (end <= start) {
+      for (int k = threadIdx.x; k < dh; k += blockDim.x) o[k] = 0.f;
+      if (threadIdx.x == 0 && P.lse) P.lse[static_cast<size_t>(b) * H + h] = -INFINITY;
+      continue;
+    }
+    const int c0 = cta_of_token(start, N, G), c1 = cta_of_token(end - 1, N, G);
+    const int n = (c1 - c0 + 1) * P.ngw;
+    const size_t s0 = static_cast<size_t>(b + c0) * P.ngw;
+    const float* ml = P.part_ml + (s0 * H + h) * 2;
+    const float* acc0 = P.part_acc + (s0 * H + h) * W;
+    // 1. this warp's share: its largest maximum, then the weighted sums
+    float mw = -INFINITY;
+    for (int i = warp; i < n; i += kWideWarps) mw = fmaxf(mw, ml[i * mstep]);
+    float a[KC];
+#pragma unroll
+    for (int k = 0; k < KC; ++k) a[k] = 0.f;
+    float lw = 0.f;
+    if (mw != -INFINITY) {
+      for (int i0 = warp; i0 < n; i0 += 4 * kWideWarps) {  // four partials' rows in flight
+        float v[4][KC], wt[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = i0 + u * kWideWarps;
+          const bool ok = i < n;
+          const float m = ok ? ml[i * mstep] : -INFINITY;
+          wt[u] = m == -INFINITY ? 0.f : exp2f(m - mw);
+          lw = fmaf(wt[u], ok ? ml[i * mstep + 1] : 0.f, lw);
+#pragma unroll
+          for (int k = 0; k < KC; ++k) {
+            const int j = lane + 32 * k;
+            v[u][k] = (ok && j < W) ? acc0[i * astep + j] : 0.f;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int k = 0; k < KC; ++k) a[k] = fmaf(wt[u], v[u][k], a[k]);
+      }
+    }
+    __syncthreads();  // the previous pair's reads of the shared arrays are done
+    if (lane == 0) {
+      s_m[warp] = mw;
+      s_l[warp] = lw;
+    }
+#pragma unroll
+    for (int k = 0; k < KC; ++k) s_acc[warp][lane + 32 * k] = a[k];
+    __syncthreads();
+    // 2. the CTA's merge of the warp shares (threads own columns)
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWideWarps; ++w) M = fmaxf(M, s_m[w]);
+    float sw[kWideWarps], L = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWideWarps; ++w) {
+      sw[w] = s_m[w] == -INFINITY ? 0.f : exp2f(s_m[w] - M);
+      L = fmaf(sw[w], s_l[w], L);
+    }
+    const float inv_l = 1.f / L;
+    for (int t = threadIdx.x; t < W; t += blockDim.x) {
+      float acc = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWideWarps; ++w) acc = fmaf(sw[w], s_acc[w][t], acc);
+      if (t < dh) s_os[t] = acc * inv_l; else s_z[t - dh] = acc * inv_l;
+    }
+    __syncthreads();
+    // 3. the lift through (B_h^V)^T and the outputs
+    for (int t = threadIdx.x; t < dh; t += blockDim.x) {
+      float v = s_os[t];
+      const size_t base = (static_cast<size_t>(h) * dh + t) * r;
+      for (int cc = 0; cc < r; ++cc) v = fmaf(load_elem(P.b_v, base + cc, BF16), s_z[cc], v);
+      o[t] = v;
+    }
+    if (threadIdx.x == 0 && P.lse) P.lse[static_cast<size_t>(b) * H + h] = (M + log2f(L)) * kLn2;
+  }
+  if (blockIdx.x == 0 && warp == 0) {
+    // the device status of this call: the bits every scan CTA wrote
+    uint32_t bits = 0u;
+    for (int i = lane; i < P.grid * P.mt; i += 32) bits |= P.cta_status[i];
+    for (int o2 = 16; o2 > 0; o2 >>= 1) bits |= __shfl_xor_sync(0xffffffffu, bits, o2);
+    if (lane == 0) *P.status = bits;
+  }
+}
+
 // ======================================================================= host
 namespace {
 
@@ -775,6 +887,11 @@ using CombineFn = void (*)(const DecodePlan);
 template <bool BF16>
 CombineFn combine_fn(const DecodePlan& P) {
   const int cols = (P.dh + P.r + 31) / 32;
+  if (P.wide_merge) {
+    if (cols <= 3) return lrkv_decode_merge_wide_kernel<BF16, 3>;
+    if (cols <= 6) return lrkv_decode_merge_wide_kernel<BF16, 6>;
+    return lrkv_decode_merge_wide_kernel<BF16, 10>;
+  }
   if (cols <= 3) return lrkv_decode_combine_kernel<BF16, 3>;
   if (cols <= 6) return lrkv_decode_combine_kernel<BF16, 6>;
   return lrkv_decode_combine_kernel<BF16, 10>;
@@ -847,7 +964,7 @@ lrkv_status launch_all(const DecodePlan& P, cudaStream_t stream, cudaEvent_t ev_
                            absorb_smem) != cudaSuccess)
     return LRKV_ERR_CUDA;
   const CombineFn combine = combine_fn<BF16>(P);
-  if (P.combine_smem > 48 * 1024 &&
+  if (!P.wide_merge && P.combine_smem > 48 * 1024 &&
       cudaFuncSetAttribute(combine, cudaFuncAttributeMaxDynamicSharedMemorySize, P.combine_smem) != cudaSuccess)
     return LRKV_ERR_CUDA;
 
@@ -877,8 +994,8 @@ lrkv_status launch_all(const DecodePlan& P, cudaStream_t stream, cudaEvent_t ev_
 
   cudaLaunchConfig_t ccfg = {};
   ccfg.gridDim = dim3(P.combine_ctas);
-  ccfg.blockDim = dim3(32 * kCombineWarps);
-  ccfg.dynamicSmemBytes = P.combine_smem;
+  ccfg.blockDim = dim3(32 * (P.wide_merge ? kWideWarps : kCombineWarps));
+  ccfg.dynamicSmemBytes = P.wide_merge ? 0 : P.combine_smem;
   ccfg.stream = stream;
   ccfg.attrs = attr;
   ccfg.numAttrs = pdl ? 1 : 0;
@@ -985,8 +1102,14 @@ lrkv_status decode_make_plan(const lrkv_dims& d, int num_sms, DecodePlan& P, siz
   // divides P.grid by the row tiles
   if (P.bf16 && env_int("LRKV_DECODE_TILE_SYNC", 0) == 0) stream_plan(P);
   if (!P.stream) P.grid = env_int("LRKV_DECODE_GRID", num_sms);
-  P.combine_ctas = P.stream && !large ? std::max(reserve, 1)
-                                      : static_cast<int>(std::min<long long>(pair_ctas, large ? num_sms : 65535));
+  // a large cache's merge: one CTA per (sequence, head) (grid-stride, at
+  // most 4 per SM), after the scan on all SMs
+  P.wide_merge = (P.stream && large) ? env_int("LRKV_DECODE_WIDE_MERGE", 1) : 0;
+  if (P.wide_merge)
+    P.combine_ctas = static_cast<int>(std::min<long long>(static_cast<long long>(P.B) * H, 4ll * num_sms));
+  else
+    P.combine_ctas = (P.stream && !large) ? std::max(reserve, 1)
+                                          : static_cast<int>(std::min<long long>(pair_ctas, large ? num_sms : 65535));
   P.min_tokens = env_int("LRKV_DECODE_MIN_TOKENS", P.stream ? 8 * P.T : 2 * P.T);
   if (P.stream) {
     // L2 prefetch window: about 48 MB in flight over all CTAs (L2 is 126 MB).
