@@ -881,6 +881,15 @@ int env_int(const char* name, int dflt) {
   return (v && *v) ? std::atoi(v) : dflt;
 }
 
+// The bound of the decode's waits for its copies (SM cycles): the
+// environment variable LRKV_WAIT_LIMIT_CYCLES when it holds a positive
+// number (for tests of the timeout path), else kWaitLimitCycles.
+long long wait_limit_cycles() {
+  const char* v = std::getenv("LRKV_WAIT_LIMIT_CYCLES");
+  const long long x = (v && *v) ? std::atoll(v) : 0;
+  return x > 0 ? x : kWaitLimitCycles;
+}
+
 using SplitFn = void (*)(const DecodePlan, const CUtensorMap, const CUtensorMap);
 using CombineFn = void (*)(const DecodePlan);
 
@@ -1013,6 +1022,7 @@ lrkv_status decode_make_plan(const lrkv_dims& d, int num_sms, DecodePlan& P, siz
   P.scale_log2 = scale * kLog2e;
   P.bf16 = d.dtype == LRKV_BF16;
   P.esz = P.bf16 ? 2 : 4;
+  P.wait_limit = wait_limit_cycles();
   const int H = P.H, dh = P.dh, r = P.r;
   if (r % 4 != 0) return LRKV_ERR_UNSUPPORTED;
   if (H > kThreads) return LRKV_ERR_UNSUPPORTED;

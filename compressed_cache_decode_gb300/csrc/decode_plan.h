@@ -71,6 +71,7 @@ struct DecodePlan {
   int kst;           // 16-wide steps over the latents of 8 heads (r / 2)
   int pfw;           // tiles a CTA keeps prefetched into L2 beyond its ring
   int after_append;  // 1: the launch before writes cache rows: the scan waits for it before its first copy
+  long long wait_limit;  // SM cycles a wait for a copy may take before it gives up (drains keep the full bound)
   int bk_dsplit;     // head-dim parts of the in-kernel q B^K (threads per output group)
   int bk_stages;     // ring stages that first hold the row tile's B^K (0: B^K read from global)
   int bk_warps;      // warps with absorb work (the first ones)

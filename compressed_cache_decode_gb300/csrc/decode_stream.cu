@@ -60,6 +60,7 @@ constexpr int kThreadsS = 32 * kWarps;
 constexpr int kPairs = kWarps / 2;           // a tile is shared by a pair (8 heads each)
 constexpr float kRescaleLog2 = 8.f;          // raise the reference max only past 2^8
 constexpr int kCursorOff = 640;              // shared bytes of the pairs' tile cursors (2 per pair)
+constexpr int kQLastOff = 896;               // [2] last piece whose q went into each p/q buffer
 constexpr int kHeaderBytes = 1024;           // barriers, stage records, step offsets, cursors
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -157,7 +158,9 @@ __device__ __forceinline__ bool stream_issue(const DecodePlan& P, const CUtensor
 // q (bf16) of the row tile's heads of sequence b into p/q buffer `buf`
 // (one thread).
 __device__ __forceinline__ void q_issue(const DecodePlan& P, unsigned char* smem, uint64_t* pbar, int buf, int b,
-                                        int m0) {
+                                        int m0, int piece) {
+  // the last piece whose q went into buffer `buf` (drained before exit)
+  reinterpret_cast<volatile int*>(smem + kQLastOff)[buf] = piece;
   const uint32_t qbytes = static_cast<uint32_t>(min(16, P.H - m0) * P.dh * 2);
   unsigned char* dst = smem + P.off_pq + buf * P.pq_bytes;
   mbar_arrive_expect_tx(&pbar[buf], qbytes);
@@ -288,12 +291,12 @@ __device__ __forceinline__ void prefetch_tmap(const void* p) {
 // before it waits on the stage's barrier, so the parity it waits for always
 // names the barrier's current phase (a waiter two phases ahead would take
 // the completed phase two back for its own).  Bounded like the barrier wait.
-__device__ __forceinline__ bool wait_issued(const int* issued, int want) {
+__device__ __forceinline__ bool wait_issued(const int* issued, int want, long long limit) {
   const volatile int* p = issued;
   if (*p >= want) return true;
   const long long t0 = clock64();
   while (*p < want) {
-    if (clock64() - t0 > kWaitLimitCycles) return false;
+    if (clock64() - t0 > limit) return false;
   }
   return true;
 }
@@ -393,6 +396,8 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     }
     s_timeout = 0;
     s_nopage = 0;
+    reinterpret_cast<int*>(smem + kQLastOff)[0] = -1;
+    reinterpret_cast<int*>(smem + kQLastOff)[1] = -1;
     for (int s = 0; s < P.stages; ++s) {
       mbar_init(&full[s], 1);
       issued[s] = -1;
@@ -464,8 +469,8 @@ __global__ void __launch_bounds__(kThreadsS, 1)
   uint64_t* bkbar = reinterpret_cast<uint64_t*>(smem + 272);
   const int first_burst = P.stages - P.bk_stages;
   if (tid == 0) {
-    q_issue(P, smem, pbar, 0, pc.b, m0);
-    if (two) q_issue(P, smem, pbar, 1, pc1.b, m0);
+    q_issue(P, smem, pbar, 0, pc.b, m0, 0);
+    if (two) q_issue(P, smem, pbar, 1, pc1.b, m0, 1);
     if (P.bk_stages > 0) {
       const uint32_t bytes = static_cast<uint32_t>(min(16, H - m0) * dh * r * 2);
       mbar_arrive_expect_tx(bkbar, bytes);
@@ -518,7 +523,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
   bool ok = true;
   if (MZMAX > 0 && !warm) {
     // p of the first two pieces, from their q rows and B^K
-    ok = mbar_wait_bounded(&pbar[0], 0u) && (!two || mbar_wait_bounded(&pbar[1], 0u));
+    ok = mbar_wait_bounded(&pbar[0], 0u, P.wait_limit) && (!two || mbar_wait_bounded(&pbar[1], 0u, P.wait_limit));
     unsigned char* pq0 = smem + P.off_pq;
     unsigned char* pq1 = pq0 + P.pq_bytes;
     const __nv_bfloat16* qa = reinterpret_cast<const __nv_bfloat16*>(pq0);
@@ -526,7 +531,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     float* pa = reinterpret_cast<float*>(pq0 + 16 * dh * 2);
     float* pb = two ? reinterpret_cast<float*>(pq1 + 16 * dh * 2) : nullptr;
     if (P.bk_stages > 0) {
-      const bool bk_in = mbar_wait_bounded(bkbar, 0u);  // always: the copy must land before exit
+      const bool bk_in = ok && mbar_wait_bounded(bkbar, 0u, P.wait_limit);  // drained before exit in any case
       ok = ok && bk_in;
       absorb_rows_smem(P, bkr, smem + P.off_kv + static_cast<size_t>(first_burst) * P.stage_bytes, qa, qb2, pa,
                        pb);
@@ -577,15 +582,18 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     if (!(split && warm))
       named_sync(1, nset);  // the p rows are written; the previous piece is done with the buffers
     const int buf = kp & 1;
-    if (tid == 0 && kp >= 1) {
+    // (only while this warp has seen every earlier copy into that buffer land:
+    // a second copy must never join a phase that is still pending)
+    if (tid == 0 && kp >= 1 && ok && !*reinterpret_cast<volatile int*>(&s_timeout)) {
       Piece nx = pc;
       if (piece_next(nx, pre, B, g1)) {  // prefetch the next piece's q (pieces 0, 1 came first)
         fence_proxy_async_smem();
-        q_issue(P, smem, pbar, buf ^ 1, nx.b, m0);
+        q_issue(P, smem, pbar, buf ^ 1, nx.b, m0, kp + 1);
       }
     }
+    if (ok && *reinterpret_cast<volatile int*>(&s_timeout)) ok = false;  // another warp gave up: stop waiting
     if (ok) {
-      ok = mbar_wait_bounded(&pbar[buf], static_cast<uint32_t>(kp >> 1) & 1u);
+      ok = mbar_wait_bounded(&pbar[buf], static_cast<uint32_t>(kp >> 1) & 1u, P.wait_limit);
       if (!ok) *reinterpret_cast<volatile int*>(&s_timeout) = 1;
     }
     unsigned char* pqb = smem + P.off_pq + buf * P.pq_bytes;
@@ -663,8 +671,10 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       const int t0 = pc.t_beg + (i - ibase) * kT;
       const int nvalid = dry ? 0 : min(kT, pc.t_end - t0);
       const int lo = max(0, pc.t_lo - t0);  // rows [lo, nvalid) of the tile are this CTA's
+      if (ok && !dry && *reinterpret_cast<volatile int*>(&s_timeout)) ok = false;  // stop waiting
       if (ok && !dry) {
-        ok = wait_issued(&issued[s], i) && mbar_wait_bounded(&full[s], static_cast<uint32_t>(i / P.stages) & 1u);
+        ok = wait_issued(&issued[s], i, P.wait_limit) &&
+             mbar_wait_bounded(&full[s], static_cast<uint32_t>(i / P.stages) & 1u, P.wait_limit);
         if (!ok) *reinterpret_cast<volatile int*>(&s_timeout) = 1;
       }
       if (ok && !*reinterpret_cast<volatile int*>(&s_timeout)) {
@@ -832,7 +842,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
           TileCursor rc = pcur[0];
           if (rc.seek(j, pre, B, g1)) {
             fence_proxy_async_smem();
-            if (ok) {
+            if (ok && !*reinterpret_cast<volatile int*>(&s_timeout)) {
               if (!stream_issue(P, &tm_k, &tm_v, &tm_zk, &tm_zv, smem, full, s, rc.pc.b,
                                 rc.pc.t_beg + (j - rc.ibase) * kT, zseg0))
                 *reinterpret_cast<volatile int*>(&s_nopage) = 1;
@@ -914,9 +924,25 @@ __global__ void __launch_bounds__(kThreadsS, 1)
   }
   if (!ok) *reinterpret_cast<volatile int*>(&s_timeout) = 1;
   named_sync(1, kThreadsS);
-  if (tid == 0)
+  if (tid == 0) {
+    // Before the CTA exits, every copy it issued must have landed: a wait
+    // that gave up skipped its stage, so wait (at the full bound) for the
+    // last tile issued into each stage, the last q copy of each buffer and
+    // the B^K copy.
+    bool drained = true;
+    for (int st = 0; st < P.stages; ++st) {
+      const int j = *reinterpret_cast<volatile int*>(&issued[st]);
+      if (j >= 0) drained = mbar_wait_bounded(&full[st], static_cast<uint32_t>(j / P.stages) & 1u) && drained;
+    }
+    for (int bq = 0; bq < 2; ++bq) {
+      const int k = reinterpret_cast<volatile int*>(smem + kQLastOff)[bq];
+      if (k >= 0) drained = mbar_wait_bounded(&pbar[bq], static_cast<uint32_t>(k >> 1) & 1u) && drained;
+    }
+    if (P.bk_stages > 0) drained = mbar_wait_bounded(bkbar, 0u) && drained;
+    if (!drained) *reinterpret_cast<volatile int*>(&s_timeout) = 1;
     *cta_status = (bad || *reinterpret_cast<volatile int*>(&s_nopage) ? kDevBounds : 0u) |
                   (*reinterpret_cast<volatile int*>(&s_timeout) ? kDevTimeout : 0u);
+  }
 }
 
 // ======================================================================= host

@@ -40,7 +40,12 @@
  *    failure returns LRKV_ERR_CUDA.  Problems only the device can see (a
  *    seq_lens entry outside [0, max_len], a bounded wait that ran out) never
  *    trap: the kernels clamp, finish, and record the status in the workspace,
- *    readable with lrkv_read_device_status().
+ *    readable with lrkv_read_device_status().  A wait of the bf16 decode scan
+ *    for its copies gives up after LRKV_WAIT_LIMIT_CYCLES SM cycles (an
+ *    environment variable read at each call; default 2e9, about 1 s); the
+ *    scan then skips the work that depended on it, still waits at the full
+ *    bound for every copy it issued, and records LRKV_ERR_TIMEOUT.  Set the
+ *    variable only to exercise that path.
  *  * Scale.  dims->scale <= 0 selects 1/sqrt(head_dim), the scale of the
  *    summed score (technical review, §3 "Associative decode").
  */

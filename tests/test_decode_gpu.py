@@ -61,10 +61,22 @@ def test_random_shapes(dtype, shape):
     B, H, dh, r, L, lens = shape
     if dtype == "bf16" and dh % 16:
         pytest.skip("bf16 needs head_dim % 16 == 0")
-    if dtype == "f32" and dh > 64 and H >= 32:
-        pytest.skip("f32 path keeps d_h/lanes columns per lane")
     case = inputs.random_decode_case(seed=B * 1000 + H * 10 + r + L, batch=B, heads=H, head_dim=dh,
                                      rank=r, max_len=L, dtype=dtype, lens=lens)
+    if dtype == "f32" and dh > 64 and H >= 32:
+        # the fp32 tile kernel keeps (d_h + r) / (lanes per head) value columns
+        # per thread: these shapes are refused on the host, nothing enqueued
+        d = _to_dev(case)
+        dims = lrkv.make_dims(B, H, dh, r, L, torch.float32)
+        ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+        out = torch.full((B, H, dh), 7.0, dtype=torch.float32, device="cuda")
+        lse = torch.full((B, H), 7.0, dtype=torch.float32, device="cuda")
+        st = lrkv.lrkv_decode(dims, d["q"], d["k_s"], d["v_s"], d["z_k"], d["z_v"], d["b_k"], d["b_v"],
+                              d["seq_lens"], out, lse, ws, ws.numel())
+        torch.cuda.synchronize()
+        assert st == lrkv.LRKV_ERR_UNSUPPORTED
+        assert bool(torch.all(out == 7.0)) and bool(torch.all(lse == 7.0))
+        return
     out, lse, _ = _run(case)
     ref_o, ref_l = _oracle(case)
     assert_decode_close(out, lse, ref_o, ref_l, dtype, what=f"{dtype}{shape}")
