@@ -92,7 +92,7 @@ __device__ __forceinline__ void issue_tile(const DecodePlan& P, const CUtensorMa
 // p_{b,h,c} = q_{b,h} . B_h^K[:, c] per thread.
 constexpr int kAbsorbSeq = 8;
 constexpr int kCombineCtas = 16;  // SMs the streaming scan leaves to the merge
-constexpr long long kLargeCacheBytes = 512ll << 20;  // see decode_make_plan
+constexpr long long kLargeCacheBytes = 256ll << 20;  // see decode_make_plan
 
 template <bool BF16>
 __global__ void __launch_bounds__(256) lrkv_decode_absorb_kernel(const DecodePlan P) {

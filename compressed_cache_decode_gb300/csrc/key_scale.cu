@@ -6,13 +6,14 @@
 // k = s_j + z_j B_h^T (never the two parts normalised apart) and the scale is
 // 1 / sqrt(mean_d k[d]^2 + eps), in fp32.
 //
-// The rebuild is a contraction per (sequence, head, block of 64 tokens):
-// K = Z_h B_h^T (64 x d_h, inner dimension r) plus the shared rows, on the
+// The rebuild is a contraction per (sequence, head, block of 128 tokens):
+// K = Z_h B_h^T (128 x d_h, inner dimension r) plus the shared rows, on the
 // tensor cores (mma.sync m16n8k16: bf16 operands, exact products, fp32
 // accumulation); the epilogue adds the shared row, squares and sums over d
 // (thread, then quad), and writes 1 / sqrt(ss / d_h + eps).  B_h^K, the
-// block's latent rows and shared rows are staged in shared memory with padded
-// row strides (conflict-free ldmatrix).  Four warps, 16 tokens each.
+// block's latent rows and shared rows are staged in shared memory by 16-byte
+// asynchronous copies (all in flight at once) with padded row strides
+// (conflict-free ldmatrix and epilogue reads).  Eight warps, 16 tokens each.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -26,8 +27,8 @@ namespace lrkv {
 
 namespace {
 
-constexpr int kKsTok = 64;       // tokens per CTA
-constexpr int kKsThreads = 128;  // four warps of 16 tokens
+constexpr int kKsTok = 128;      // tokens per CTA (B_h is staged once for all of them)
+constexpr int kKsThreads = 256;  // eight warps of 16 tokens
 constexpr int kKsCols = 128;     // key columns per accumulator pass
 
 struct KeyScaleParams {
@@ -43,14 +44,30 @@ struct KeyScaleParams {
   float* key_scale;           // [B][H][max_len]
 };
 
+// 16-byte asynchronous copy global -> shared; `valid` false fills zeros (no
+// bytes are read; `src` is still a mapped address).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 }  // namespace
 
+// DHC, RPC: head dim and padded rank as compile-time constants (0: read from
+// the parameters), so that the staging loops' index arithmetic folds.
+template <int DHC, int RPC>
 __global__ void __launch_bounds__(kKsThreads) lrkv_key_scale_kernel(const KeyScaleParams p) {
   extern __shared__ __align__(16) unsigned char ks_raw[];
-  const int dh = p.dh, r = p.r, rp = p.rp, zs = p.zs;
+  const int dh = DHC ? DHC : p.dh, rp = RPC ? RPC : p.rp, zs = rp + 8;
+  const int r = p.r;
   __nv_bfloat16* sB = reinterpret_cast<__nv_bfloat16*>(ks_raw);  // [dh][zs]
-  __nv_bfloat16* sZ = sB + dh * zs;                              // [64][zs]
-  __nv_bfloat16* sS = sZ + kKsTok * zs;                          // [64][dh]
+  __nv_bfloat16* sZ = sB + dh * zs;                              // [kKsTok][zs]
+  __nv_bfloat16* sS = sZ + kKsTok * zs;                          // [kKsTok][dh + 8]
   const int h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, q4 = lane & 3;
   const int t0 = blockIdx.x * kKsTok, start = p.start_pos[b];
@@ -62,18 +79,23 @@ __global__ void __launch_bounds__(kKsThreads) lrkv_key_scale_kernel(const KeySca
     return p.z_k + ((static_cast<size_t>(b) * p.max_len + pos) * p.H + h) * r;
   };
   const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
+  const int ss_stride = dh + 8;  // staged shared rows, padded: the epilogue's quad reads hit distinct banks
   if (p.rvec) {
+    // every row in 16-byte pieces, all copies in flight at once (cp.async,
+    // zero-filled where a row lies outside the block or the cache)
     const int pr = rp / 8;  // 16-byte pieces per padded row
+#pragma unroll 4
     for (int i = tid; i < dh * pr; i += kKsThreads) {
       const int d = i / pr, c8 = i - d * pr;
-      *reinterpret_cast<uint4*>(sB + d * zs + 8 * c8) =
-          8 * c8 < r ? reinterpret_cast<const uint4*>(bh + static_cast<size_t>(d) * r)[c8] : zero4;
+      const bool v = 8 * c8 < r;
+      cp_async16(sB + d * zs + 8 * c8, v ? bh + static_cast<size_t>(d) * r + 8 * c8 : bh, v);
     }
+#pragma unroll 4
     for (int i = tid; i < kKsTok * pr; i += kKsThreads) {
       const int t = i / pr, c8 = i - t * pr;
       const __nv_bfloat16* zr = zrow(t);
-      *reinterpret_cast<uint4*>(sZ + t * zs + 8 * c8) =
-          (zr && 8 * c8 < r) ? reinterpret_cast<const uint4*>(zr)[c8] : zero4;
+      const bool v = zr && 8 * c8 < r;
+      cp_async16(sZ + t * zs + 8 * c8, v ? zr + 8 * c8 : bh, v);
     }
   } else {
     const __nv_bfloat16 zb = __float2bfloat16_rn(0.f);
@@ -88,13 +110,15 @@ __global__ void __launch_bounds__(kKsThreads) lrkv_key_scale_kernel(const KeySca
     }
   }
   const int pieces = dh / 8;
+#pragma unroll 4
   for (int i = tid; i < kKsTok * pieces; i += kKsThreads) {
     const int t = i / pieces, c8 = i - t * pieces, pos = start + t0 + t;
-    uint4 u = zero4;
-    if (t < nt && pos >= 0 && pos < p.max_len)
-      u = reinterpret_cast<const uint4*>(p.k_s + (static_cast<size_t>(b) * p.max_len + pos) * dh)[c8];
-    *reinterpret_cast<uint4*>(sS + t * dh + 8 * c8) = u;
+    const bool v = t < nt && pos >= 0 && pos < p.max_len;
+    cp_async16(sS + t * ss_stride + 8 * c8,
+               v ? p.k_s + (static_cast<size_t>(b) * p.max_len + pos) * dh + 8 * c8 : p.k_s, v);
   }
+  cp_async_wait_all();
+  (void)zero4;
   __syncthreads();
 
   const int trow = 16 * warp;  // this warp's first token
@@ -122,8 +146,8 @@ __global__ void __launch_bounds__(kKsThreads) lrkv_key_scale_kernel(const KeySca
     for (int j = 0; j < kKsCols / 8; ++j) {
       if (j < nn) {
         const int d = dc + 8 * j + 2 * q4;
-        const uint32_t s0 = *reinterpret_cast<const uint32_t*>(sS + (trow + g) * dh + d);
-        const uint32_t s1 = *reinterpret_cast<const uint32_t*>(sS + (trow + g + 8) * dh + d);
+        const uint32_t s0 = *reinterpret_cast<const uint32_t*>(sS + (trow + g) * ss_stride + d);
+        const uint32_t s1 = *reinterpret_cast<const uint32_t*>(sS + (trow + g + 8) * ss_stride + d);
         const float k00 = acc[j][0] + bf_lo(s0), k01 = acc[j][1] + bf_hi(s0);
         const float k10 = acc[j][2] + bf_lo(s1), k11 = acc[j][3] + bf_hi(s1);
         ss0 = fmaf(k00, k00, fmaf(k01, k01, ss0));
@@ -160,11 +184,16 @@ lrkv_status key_scale_launch(const lrkv_dims& dm, float eps, int n_new, const vo
   p.b_k = static_cast<const __nv_bfloat16*>(b_k);
   p.start_pos = start_pos;
   p.key_scale = key_scale;
-  const int smem = ((dm.head_dim + kKsTok) * p.zs + kKsTok * dm.head_dim) * 2;
-  if (ensure_kernel_smem(reinterpret_cast<const void*>(lrkv_key_scale_kernel), smem) != cudaSuccess)
-    return LRKV_ERR_CUDA;
+  const int smem = ((dm.head_dim + kKsTok) * p.zs + kKsTok * (dm.head_dim + 8)) * 2;
+  using Fn = void (*)(const KeyScaleParams);
+  Fn kern = lrkv_key_scale_kernel<0, 0>;
+  if (dm.head_dim == 128 && p.rp == 64) kern = lrkv_key_scale_kernel<128, 64>;
+  else if (dm.head_dim == 128 && p.rp == 48) kern = lrkv_key_scale_kernel<128, 48>;
+  else if (dm.head_dim == 128 && p.rp == 32) kern = lrkv_key_scale_kernel<128, 32>;
+  else if (dm.head_dim == 64 && p.rp == 32) kern = lrkv_key_scale_kernel<64, 32>;
+  if (ensure_kernel_smem(reinterpret_cast<const void*>(kern), smem) != cudaSuccess) return LRKV_ERR_CUDA;
   const dim3 grid((n_new + kKsTok - 1) / kKsTok, dm.heads, dm.batch);
-  lrkv_key_scale_kernel<<<grid, kKsThreads, smem, static_cast<cudaStream_t>(stream)>>>(p);
+  kern<<<grid, kKsThreads, smem, static_cast<cudaStream_t>(stream)>>>(p);
   return cudaGetLastError() == cudaSuccess ? LRKV_OK : LRKV_ERR_CUDA;
 }
 
