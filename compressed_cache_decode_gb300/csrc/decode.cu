@@ -762,15 +762,15 @@ __global__ void __launch_bounds__(32 * kCombineWarps) lrkv_decode_combine_kernel
 }
 
 // ================================================================ wide merge
-// The merge of a large cache's decode: one CTA per (sequence b, head h),
-// grid-stride.  The partials of the sequence's pieces are split over the 8
+// The merge of the bf16 streaming decode: one CTA per (sequence b, head h),
+// grid-stride (on a small cache, on the SMs the scan leaves free).  The partials of the sequence's pieces are split over the 8
 // warps (warp w takes partials w, w + 8, ...); each warp merges its share
 // against its own largest maximum (lanes own columns of [acc_s | acc_z]),
 // the CTA merges the 8 warp results through shared memory with the same
 // log-sum-exp rule, then lifts the private sum: o = acc_s / L +
 // (acc_z / L) (B_h^V)^T and lse = (M + log2 L) ln 2 (Algorithm 2 steps 06-09).
-// Spread over every SM it reads the partials at once instead of one warp per
-// (sequence, head) walking all of them.
+// It reads a pair's partials with eight warps at once instead of one warp
+// walking all of them.
 constexpr int kWideWarps = 8;
 
 template <bool BF16, int KC>  // KC: columns per lane, ceil((dh + r) / 32)
@@ -1114,9 +1114,13 @@ lrkv_status decode_make_plan(const lrkv_dims& d, int num_sms, DecodePlan& P, siz
   if (!P.stream) P.grid = env_int("LRKV_DECODE_GRID", num_sms);
   // a large cache's merge: one CTA per (sequence, head) (grid-stride, at
   // most 4 per SM), after the scan on all SMs
-  P.wide_merge = (P.stream && large) ? env_int("LRKV_DECODE_WIDE_MERGE", 1) : 0;
+  // (A small cache keeps one warp per (sequence, head) on the `reserve` SMs
+  // the scan leaves free: measured on 8 x 4K rows, the wide merge there made
+  // a chain of dependent decode steps 11% slower.)
+  P.wide_merge = P.stream ? env_int("LRKV_DECODE_WIDE_MERGE", large ? 1 : 0) : 0;
   if (P.wide_merge)
-    P.combine_ctas = static_cast<int>(std::min<long long>(static_cast<long long>(P.B) * H, 4ll * num_sms));
+    P.combine_ctas = static_cast<int>(
+        std::min<long long>(static_cast<long long>(P.B) * H, 4ll * (large ? num_sms : std::max(reserve, 1))));
   else
     P.combine_ctas = (P.stream && !large) ? std::max(reserve, 1)
                                           : static_cast<int>(std::min<long long>(pair_ctas, large ? num_sms : 65535));

@@ -15,6 +15,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <cstdint>
 
 #include "host_cache.h"
@@ -197,7 +198,10 @@ lrkv_status step_append_launch(const lrkv_dims& dm, int d_model, const void* x, 
   // one warp per output column, at most one CTA per SM
   const long long N = 2ll * dm.head_dim + 2ll * dm.heads * dm.rank;
   const long long wpc = kStepWarps;
-  const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(num_sms, (N + wpc - 1) / wpc)));
+  const char* cap_env = std::getenv("LRKV_STEP_GRID");  // tuning: at most this many CTAs
+  const long long cap = (cap_env && *cap_env) ? std::max(1, std::atoi(cap_env)) : num_sms;
+  const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(std::min<long long>(num_sms, cap),
+                                                                               (N + wpc - 1) / wpc)));
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;

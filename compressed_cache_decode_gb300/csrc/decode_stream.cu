@@ -136,7 +136,11 @@ __device__ __forceinline__ bool cache_coords(const DecodePlan& P, int b, int t, 
 __device__ __forceinline__ bool stream_issue(const DecodePlan& P, const CUtensorMap* tk, const CUtensorMap* tv,
                                              const CUtensorMap* tzk, const CUtensorMap* tzv,
                                              unsigned char* smem, uint64_t* full, int s, int b_log, int t_log,
-                                             int zseg0) {
+                                             int zseg0, const int* pre) {
+  // In a decode step the launch before writes each sequence's newest row
+  // (row L_b - 1): only a copy of the tile that holds it waits for that
+  // launch; every other tile streams at once.
+  if (P.after_append && t_log + kT >= pre[b_log + 1] - pre[b_log]) pdl_wait();
   int b, t0;  // a 16-token tile never spans two pages (page_size is a multiple of 16)
   const bool in_pool = cache_coords(P, b_log, t_log, b, t0);
   unsigned char* ks = smem + P.off_kv + static_cast<size_t>(s) * P.stage_bytes;
@@ -478,9 +482,6 @@ __global__ void __launch_bounds__(kThreadsS, 1)
                   static_cast<const __nv_bfloat16*>(P.b_k) + static_cast<size_t>(m0) * dh * r, bytes, bkbar);
     }
   }
-  // a decode step's token rows come from the launch before: wait for it
-  // before the first cache copy (the set-up above overlapped it)
-  if (P.after_append) pdl_wait();
   if (lane == 0) {
     TileCursor cur;
     cur.pc = pc;
@@ -488,7 +489,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     cur.ibase = 0;
     for (int j = warp; j < first_burst && cur.seek(j, pre, B, g1); j += kWarps) {
       if (!stream_issue(P, &tm_k, &tm_v, &tm_zk, &tm_zv, smem, full, j, cur.pc.b,
-                        cur.pc.t_beg + (j - cur.ibase) * kT, zseg0))
+                        cur.pc.t_beg + (j - cur.ibase) * kT, zseg0, pre))
         *reinterpret_cast<volatile int*>(&s_nopage) = 1;
       *reinterpret_cast<volatile int*>(&issued[j]) = j;
     }
@@ -551,7 +552,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       cur.ibase = 0;
       for (int j = first_burst + warp; j < P.stages && cur.seek(j, pre, B, g1); j += P.bk_warps) {
         if (!stream_issue(P, &tm_k, &tm_v, &tm_zk, &tm_zv, smem, full, j, cur.pc.b,
-                          cur.pc.t_beg + (j - cur.ibase) * kT, zseg0))
+                          cur.pc.t_beg + (j - cur.ibase) * kT, zseg0, pre))
           *reinterpret_cast<volatile int*>(&s_nopage) = 1;
         *reinterpret_cast<volatile int*>(&issued[j]) = j;
       }
@@ -844,7 +845,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
             fence_proxy_async_smem();
             if (ok && !*reinterpret_cast<volatile int*>(&s_timeout)) {
               if (!stream_issue(P, &tm_k, &tm_v, &tm_zk, &tm_zv, smem, full, s, rc.pc.b,
-                                rc.pc.t_beg + (j - rc.ibase) * kT, zseg0))
+                                rc.pc.t_beg + (j - rc.ibase) * kT, zseg0, pre))
                 *reinterpret_cast<volatile int*>(&s_nopage) = 1;
               *reinterpret_cast<volatile int*>(&issued[s]) = j;
             }
