@@ -35,7 +35,8 @@ Readings where the pages leave a step open:
     and sees keys j <= that position (bottom-right causal alignment; the pages
     only say "causal").
   * an empty history (seq_lens[b] == 0) gives out = 0 and lse = -inf.
-  * no RoPE (notes §2.7; review §8).  Post-projection RMSNorm only in the
+  * no RoPE except in the *_rope functions (notes §2.7; review §8: exact
+    rotation of the rebuilt keys, see the readings there).  Post-projection RMSNorm only in the
     *_normed functions (review §8, "Post-projection normalization has a cache
     cost"): the key k_j = s_j + z_j B_h^T is divided by its joint RMS
     n_{h,j} = sqrt(mean_d k_j[d]^2 + eps) (never the two parts by separate
@@ -292,6 +293,103 @@ def decode_factored(q, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens, scale: Optional[f
             shared = a @ v_s[b, :L]                                # step 07
             private = a @ z_v[b, :L, h, :]
             out[b, h] = shared + private @ b_v[h].T                # steps 08-09
+            lse[b, h] = m + math.log(l)
+    return out, lse
+
+
+# --------------------------------------------------------------------------
+# Full rotary position embedding on the factored cache (review §8, "Full RoPE
+# needs a stronger identity"; notes §2.7).  The latents cannot be rotated in
+# rank space for a generic basis, so the cache keeps unrotated rows and the
+# rotation of key position j is applied to the rebuilt key.
+#
+# Readings (the pages fix none of these): theta_k = base^(-2k/d_h) for
+# k = 0 .. d_h/2 - 1 with base 10000; the pairs are adjacent coordinates
+# (2k, 2k+1) and the rotation of a row at position j multiplies each pair,
+# read as the complex number x_{2k} + i x_{2k+1}, by exp(i j theta_k); cache
+# row j sits at position j + pos_offset; the query arrives already rotated to
+# its own position (the review's q~_i); values are not rotated.
+# --------------------------------------------------------------------------
+
+def rope_frequencies(head_dim: int, base: float = 10000.0) -> np.ndarray:
+    """theta_k = base^(-2k/d_h), k = 0 .. d_h/2 - 1."""
+    k = np.arange(head_dim // 2, dtype=np.float64)
+    return base ** (-2.0 * k / head_dim)
+
+
+def rope_rotate_rows(X, positions, theta) -> np.ndarray:
+    """Row j of X [L, d_h] times D_{positions[j]} (row vectors): pair
+    (2k, 2k+1) turned by the angle positions[j] * theta[k]:
+    x'_{2k} = x_{2k} cos - x_{2k+1} sin, x'_{2k+1} = x_{2k} sin + x_{2k+1} cos."""
+    X = _f64(X)
+    ang = np.asarray(positions, dtype=np.float64)[:, None] * np.asarray(theta, dtype=np.float64)[None, :]
+    c, s = np.cos(ang), np.sin(ang)
+    out = np.empty_like(X)
+    out[:, 0::2] = X[:, 0::2] * c - X[:, 1::2] * s
+    out[:, 1::2] = X[:, 0::2] * s + X[:, 1::2] * c
+    return out
+
+
+def decode_reference_rope(q_rot, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens, base: float = 10000.0,
+                          theta=None, pos_offset: int = 0, scale: Optional[float] = None,
+                          pairs: Optional[Iterable[Tuple[int, int]]] = None):
+    """Decode with full RoPE on the keys, computed by the definition: for
+    each (sequence b, head h) rebuild K_h = S_K + Z_h B_h^T over rows
+    [0, seq_lens[b]), rotate row j by D_{j + pos_offset}, score
+    s_j = scale * q_rot . (K_h[j] D_j), one softmax, o = sum_j a_j V_h[j] with
+    V_h = S_V + Z_v B_V^T unrotated.  q_rot [B, H, d_h] is the query already
+    rotated to its position.  `theta` overrides the frequency schedule."""
+    q, k_s, v_s, z_k, z_v, b_k, b_v = (_f64(a) for a in (q_rot, k_s, v_s, z_k, z_v, b_k, b_v))
+    lens = np.asarray(_f64(seq_lens), dtype=np.int64)
+    B, H, dh = q.shape
+    if scale is None:
+        scale = default_scale(dh)
+    th = rope_frequencies(dh, base) if theta is None else np.asarray(theta, dtype=np.float64)
+    out = np.full((B, H, dh), np.nan)
+    lse = np.full((B, H), np.nan)
+    todo = pairs if pairs is not None else [(b, h) for b in range(B) for h in range(H)]
+    for b, h in todo:
+        L = int(lens[b])
+        if L == 0:
+            out[b, h] = 0.0
+            lse[b, h] = -np.inf
+            continue
+        K = reconstruct_head(k_s[b, :L], z_k[b, :L, h, :], b_k[h])
+        K = rope_rotate_rows(K, np.arange(L) + pos_offset, th)
+        V = reconstruct_head(v_s[b, :L], z_v[b, :L, h, :], b_v[h])
+        s = scale * (K @ q[b, h])
+        out[b, h], lse[b, h] = _softmax_attend(s, V)
+    return out, lse
+
+
+def decode_rope_factored(q_rot, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens, base: float = 10000.0,
+                         theta=None, scale: Optional[float] = None):
+    """The review's exact decode option in its own form, never rebuilding
+    K_h: the query is turned back to each key position, u_j = q~ D_j^T, and
+    the score is u_j . s_j + (u_j B_h) . z_j (the position-specific
+    contraction (q~ D_j^T B_h) z_j^T); one softmax; the values as in
+    decode_factored.  Used only to pin decode_reference_rope."""
+    q, k_s, v_s, z_k, z_v, b_k, b_v = (_f64(a) for a in (q_rot, k_s, v_s, z_k, z_v, b_k, b_v))
+    lens = np.asarray(_f64(seq_lens), dtype=np.int64)
+    B, H, dh = q.shape
+    if scale is None:
+        scale = default_scale(dh)
+    th = rope_frequencies(dh, base) if theta is None else np.asarray(theta, dtype=np.float64)
+    out = np.zeros((B, H, dh))
+    lse = np.full((B, H), -np.inf)
+    for b in range(B):
+        L = int(lens[b])
+        if L == 0:
+            continue
+        for h in range(H):
+            U = rope_rotate_rows(np.tile(q[b, h], (L, 1)), -np.arange(L), th)   # rows q~ D_j^T = q~ D_{-j}
+            score = np.sum(U * k_s[b, :L], axis=1) + np.sum((U @ b_k[h]) * z_k[b, :L, h, :], axis=1)
+            score = score * scale
+            m = np.max(score)
+            w = np.exp(score - m)
+            l = np.sum(w)
+            a = w / l
+            out[b, h] = a @ v_s[b, :L] + (a @ z_v[b, :L, h, :]) @ b_v[h].T
             lse[b, h] = m + math.log(l)
     return out, lse
 
