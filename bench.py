@@ -27,7 +27,8 @@ measurement on the other decode workloads), `e2e` (host copies in and out
 every step, one public-API call per step), `decode_step` (the new token's
 rows from its layer input, then the decode, as dependent steps),
 `decode_normed` (post-projection RMSNorm key scales), `decode_paged` (the
-rows in 256-row pages through a block table) and `prefill` (append GEMM,
+rows in 256-row pages through a block table), `decode_rope` (full RoPE of the
+keys, exact: keys rebuilt tile by tile and rotated) and `prefill` (append GEMM,
 causal prefill and the normalised-key prefill of 2 x 4096 tokens, against the
 bf16 tensor peak).
 """
@@ -731,6 +732,39 @@ def decode_paged_leg(setup, K, W, stream, use_graph, world, dev, base_ms, page=2
             "decode_ms_per_step": base_ms, "gbs": job_gbs(setup.total_bytes, world, p_ms)}
 
 
+def decode_rope_leg(setup, K, W, stream, use_graph, world, dev, base_ms):
+    """Decode with full RoPE of the keys on the same cache (the query taken as
+    already rotated): the keys are rebuilt tile by tile (d_h r multiply-adds
+    per row and head on the tensor cores), turned by the library's table and
+    dotted with the query.  Reported against the plain decode of the cache."""
+    import torch
+    from compressed_cache_decode_gb300 import lrkv
+    w = setup.w
+    table = lrkv.rope_table(w.max_len, w.head_dim, device=dev)
+    ws = torch.empty(lrkv.lrkv_decode_rope_workspace_size(setup.dims), dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+
+    def rstep(i, s):
+        x = setup.reps[i % setup.n_rep]
+        st = lrkv.lrkv_decode_rope(setup.dims, x["q"], x["k_s"], x["v_s"], x["z_k"], x["z_v"], x["b_k"], x["b_v"],
+                                   table, w.max_len, x["seq_lens"], setup.out, setup.lse, ws, ws.numel(), s)
+        if st != lrkv.LRKV_OK:
+            raise lrkv.LRKVError(st, "lrkv_decode_rope")
+
+    t = StepTimer(rstep, K, W, stream, use_graph)
+    t.warm()
+    sp = _spread(t.time(repeats=7))
+    r_ms = max_over_ranks(sp["median"], world, dev)
+    tokens = int(setup.case["seq_lens"].long().sum())
+    table_bytes = w.max_len * w.head_dim * 4
+    rebuild_flop = 2 * tokens * w.heads * w.head_dim * w.rank
+    return {"workload": w.name, "ms_per_step": r_ms, "ms_per_step_spread": sp, "decode_ms_per_step": base_ms,
+            "algorithmic_bytes": setup.total_bytes + table_bytes,
+            "gbs": job_gbs(setup.total_bytes + table_bytes, world, r_ms),
+            "hbm_frac": (setup.total_bytes + table_bytes) / (r_ms * 1e-3) / 1e9 / _peaks()[0],
+            "rebuild_flop": rebuild_flop, "rebuild_tflops": rebuild_flop / (r_ms * 1e-3) / 1e12 * world}
+
+
 def e2e_leg(setup, K, stream, use_graph, world, dev):
     """End to end through the public API: every step copies the new token's
     layer input x, its query q and the lengths from pinned host memory (one
@@ -880,6 +914,7 @@ def main():
     e2e = e2e_leg(head, K, stream, use_graph, world, dev) if not a.no_legs else None
     normed_leg = decode_normed_leg(head, K, W, stream, use_graph, world, dev, ms_step) if not a.no_legs else None
     paged_leg = decode_paged_leg(head, K, W, stream, use_graph, world, dev, ms_step) if not a.no_legs else None
+    rope_leg = decode_rope_leg(head, K, W, stream, use_graph, world, dev, ms_step) if not a.no_legs else None
 
     # ---- the other decode workloads, and the decode step on the 4K one ----
     legs, step_leg = {}, None
@@ -936,6 +971,7 @@ def main():
             "decode_step": step_leg,
             "decode_normed": normed_leg,
             "decode_paged": paged_leg,
+            "decode_rope": rope_leg,
             "prefill": prefill,
         }
         print(json.dumps(res), flush=True)

@@ -1135,22 +1135,44 @@ lrkv_status decode_make_plan(const lrkv_dims& d, int num_sms, DecodePlan& P, siz
     const int pfw = (large || P.mt > 1) ? 0 : static_cast<int>(per_cta / P.stage_bytes);
     P.pfw = env_int("LRKV_DECODE_PREFETCH_TILES", pfw);
   }
-  const int slots = (P.B + P.grid) * P.ngw;
   // per warp: the lift's z row, and the weights and denominators of one sequence's partials
   P.combine_smem = kCombineWarps * (std::max(r, 1) + 2 * P.grid * P.ngw) * 4;
+  *ws_bytes = decode_workspace_bytes(P);
+  return LRKV_OK;
+}
 
+size_t decode_workspace_bytes(const DecodePlan& P) {
   // workspace: status | meta | prefix | p | part_ml | part_acc | CTA status
+  const size_t slots = static_cast<size_t>(P.B + P.grid) * P.ngw;
   size_t w = 256;
   w += static_cast<size_t>(round_up(P.B + 1, 64)) * 4;
-  w += static_cast<size_t>(P.B) * H * std::max(r, 1) * 4;
+  w += static_cast<size_t>(P.B) * P.H * std::max(P.r, 1) * 4;
   w = (w + 255) / 256 * 256;
-  w += static_cast<size_t>(slots) * H * 2 * 4;
+  w += slots * P.H * 2 * 4;
   w = (w + 255) / 256 * 256;
-  w += static_cast<size_t>(slots) * H * (dh + r) * 4;
+  w += slots * P.H * (P.dh + P.r) * 4;
   w = (w + 255) / 256 * 256;
   w += static_cast<size_t>(P.grid) * std::max(P.mt, 1) * 4;
-  *ws_bytes = w;
-  return LRKV_OK;
+  return w;
+}
+
+lrkv_status decode_merge_launch(const DecodePlan& P, void* stream, bool pdl) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const CombineFn combine = P.bf16 ? combine_fn<true>(P) : combine_fn<false>(P);
+  if (ensure_kernel_smem(reinterpret_cast<const void*>(combine), P.wide_merge ? 0 : P.combine_smem, true) !=
+      cudaSuccess)
+    return LRKV_ERR_CUDA;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t ccfg = {};
+  ccfg.gridDim = dim3(P.combine_ctas);
+  ccfg.blockDim = dim3(32 * (P.wide_merge ? kWideWarps : kCombineWarps));
+  ccfg.dynamicSmemBytes = P.wide_merge ? 0 : P.combine_smem;
+  ccfg.stream = s;
+  ccfg.attrs = attr;
+  ccfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&ccfg, combine, P) == cudaSuccess ? LRKV_OK : LRKV_ERR_CUDA;
 }
 
 void decode_bind_workspace(DecodePlan& P, void* ws) {

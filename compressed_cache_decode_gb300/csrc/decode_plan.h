@@ -106,6 +106,10 @@ struct DecodePlan {
   int map_len, map_seqs;
   float* out;
   float* lse;
+  // full-RoPE decode: the cos/sin table [max_pos][dh] (pairs (cos, sin) per
+  // frequency) and its staged tile ([16][cs_row] fp32 per ring stage)
+  const float* rope_cs;
+  int cs_row, cs_bytes, rope_max_pos;
 };
 
 // Fills everything but the operand pointers; returns the workspace size.
@@ -117,6 +121,10 @@ lrkv_status step_append_launch(const lrkv_dims& dm, int d_model, const void* x, 
                                void* k_s, void* v_s, void* z_k, void* z_v, int num_sms, void* stream,
                                const int32_t* block_table = nullptr, int page_size = 0, int num_pages = 0);
 void decode_bind_workspace(DecodePlan& P, void* ws);
+size_t decode_workspace_bytes(const DecodePlan& P);
+// The merge of a streaming decode's partials (wide or narrow, per the plan),
+// launched with programmatic dependent launch when `pdl`.
+lrkv_status decode_merge_launch(const DecodePlan& P, void* stream, bool pdl);
 lrkv_status decode_launch(const DecodePlan& P, void* stream, void* ev_begin = nullptr, void* ev_end = nullptr);
 
 }  // namespace lrkv

@@ -47,6 +47,9 @@ EXPORTED = (
     "lrkv_append_paged",
     "lrkv_decode_step_paged",
     "lrkv_prefill_paged",
+    "lrkv_rope_table",
+    "lrkv_decode_rope_workspace_size",
+    "lrkv_decode_rope",
     "lrkv_read_device_status",
 )
 
@@ -130,6 +133,13 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.lrkv_prefill_paged.restype = ctypes.c_int
     lib.lrkv_prefill_paged.argtypes = [dims_p, ctypes.c_int, vp, ctypes.c_int, ctypes.c_int, i32p, vp, vp, vp, vp,
                                        vp, vp, i32p, vp, vp, vp, sz, vp]
+    lib.lrkv_rope_table.restype = ctypes.c_int
+    lib.lrkv_rope_table.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_float, vp, vp]
+    lib.lrkv_decode_rope_workspace_size.restype = ctypes.c_int
+    lib.lrkv_decode_rope_workspace_size.argtypes = [dims_p, ctypes.POINTER(sz)]
+    lib.lrkv_decode_rope.restype = ctypes.c_int
+    lib.lrkv_decode_rope.argtypes = [dims_p, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int, i32p, vp, vp, vp, sz,
+                                     vp]
     lib.lrkv_read_device_status.restype = ctypes.c_int
     lib.lrkv_read_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
     if path is None:
@@ -518,3 +528,55 @@ def prefill_paged(q, k_s, v_s, z_k, z_v, b_k, b_v, block_table, seq_lens, scale:
     if st != LRKV_OK:
         raise LRKVError(st, "lrkv_prefill_paged")
     return out, lse, ws
+
+
+# ------------------------------------------------------------ full RoPE --
+
+def rope_table(max_pos: int, head_dim: int, base: float = 10000.0, device="cuda", stream=None) -> torch.Tensor:
+    """The rotation table [max_pos, head_dim] fp32 (cos, sin pairs) computed
+    by the library."""
+    t = torch.empty((max_pos, head_dim), dtype=torch.float32, device=device)
+    st = int(load().lrkv_rope_table(int(max_pos), int(head_dim), float(base), _ptr(t), _stream_handle(stream)))
+    if st != LRKV_OK:
+        raise LRKVError(st, "lrkv_rope_table")
+    return t
+
+
+def lrkv_decode_rope_workspace_size(dims: lrkv_dims) -> int:
+    n = ctypes.c_size_t(0)
+    st = load().lrkv_decode_rope_workspace_size(ctypes.byref(dims), ctypes.byref(n))
+    if st != LRKV_OK:
+        raise LRKVError(st, "lrkv_decode_rope_workspace_size")
+    return int(n.value)
+
+
+def lrkv_decode_rope(dims: lrkv_dims, q_rot, k_s, v_s, z_k, z_v, b_k, b_v, cos_sin, max_pos: int, seq_lens, out,
+                     lse, ws, ws_bytes: int, stream=None) -> int:
+    """Direct call of the full-RoPE decode entry point; returns its status."""
+    return int(load().lrkv_decode_rope(ctypes.byref(dims), _ptr(q_rot), _ptr(k_s), _ptr(v_s), _ptr(z_k),
+                                       _ptr(z_v), _ptr(b_k), _ptr(b_v), _ptr(cos_sin), int(max_pos),
+                                       _ptr(seq_lens), _ptr(out), _ptr(lse), _ptr(ws), ws_bytes,
+                                       _stream_handle(stream)))
+
+
+def decode_rope(q_rot, k_s, v_s, z_k, z_v, b_k, b_v, cos_sin, seq_lens, scale: float = 0.0, out=None, lse=None,
+                ws=None, stream=None):
+    """Decode with full RoPE of the keys: q_rot [B, H, d_h] is the query
+    rotated to its position, the cache holds unrotated rows, cos_sin is a
+    table from rope_table().  Returns (out, lse)."""
+    B, H, dh = q_rot.shape
+    dims = make_dims(B, H, dh, z_k.shape[-1], k_s.shape[1], q_rot.dtype, scale)
+    if out is None:
+        out = torch.empty((B, H, dh), dtype=torch.float32, device=q_rot.device)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q_rot.device)
+    if ws is None:
+        ws = torch.empty(lrkv_decode_rope_workspace_size(dims), dtype=torch.uint8, device=q_rot.device)
+    for t in (q_rot, k_s, v_s, z_k, z_v, b_k, b_v, cos_sin, seq_lens):
+        if not t.is_contiguous():
+            raise ValueError("LRKV tensors must be contiguous")
+    st = lrkv_decode_rope(dims, q_rot, k_s, v_s, z_k, z_v, b_k, b_v, cos_sin, cos_sin.shape[0], seq_lens, out, lse,
+                          ws, ws.numel(), stream)
+    if st != LRKV_OK:
+        raise LRKVError(st, "lrkv_decode_rope")
+    return out, lse

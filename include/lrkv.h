@@ -48,6 +48,8 @@
  *    variable only to exercise that path.
  *  * Scale.  dims->scale <= 0 selects 1/sqrt(head_dim), the scale of the
  *    summed score (technical review, §3 "Associative decode").
+ *  * Positions.  Without RoPE the decode and prefill carry no position
+ *    encoding; lrkv_decode_rope applies full RoPE to the keys exactly.
  */
 #ifndef LRKV_H_
 #define LRKV_H_
@@ -378,6 +380,44 @@ lrkv_status lrkv_decode_step_paged(const lrkv_dims* dims, int d_model, const voi
                                    int page_size, int num_pages, const int32_t* block_table, void* k_s, void* v_s,
                                    void* z_k, void* z_v, const void* b_k, const void* b_v, const int32_t* seq_lens,
                                    float* out, float* lse, void* ws, size_t ws_bytes, lrkv_stream_t stream);
+
+/*
+ * Decode with full rotary position embedding (RoPE) of the keys, exactly
+ * ("Low-Rank Key Value Attention | What a shared cache can preserve", §8,
+ * "Full RoPE needs a stronger identity"; "Low-Rank Key Value
+ * Attention：中文研读笔记", §2.7).  A key rotation cannot be moved into the
+ * rank-r latent for a generic basis, so the cache keeps unrotated rows and the
+ * decode rebuilds each key, k_j = s_j + z_j B_h^T, turns it by the rotation of
+ * its position j and takes the dot product with the query, which the caller
+ * passes already rotated to its own position (the review's q~).  Values are
+ * not rotated.  For head h and row j of sequence b:
+ *   score = scale * q~_h . (k_j D_j),  D_j: each pair (2k, 2k+1) turned by the
+ *   angle j theta_k (as the complex number x_2k + i x_2k+1 times
+ *   exp(i j theta_k)), theta_k = base^(-2k / head_dim);
+ * one softmax over the rows [0, seq_lens[b]); o_h as in lrkv_decode.  Row j
+ * of the cache sits at position j.
+ *
+ * lrkv_rope_table writes the rotation table cos_sin [max_pos][head_dim] fp32
+ * (device, caller-allocated): cos_sin[j][2k] = cos(j theta_k),
+ * cos_sin[j][2k+1] = sin(j theta_k), with the angle and both functions in
+ * fp64, rounded once to fp32.  Compute it once per model; base > 1, head_dim
+ * even.
+ *
+ * lrkv_decode_rope takes the arguments of lrkv_decode (q is q~, [B][H][d_h]
+ * in the cache dtype) plus the table and its row count max_pos (at least
+ * dims->max_len, else LRKV_ERR_INVALID_ARG), and a workspace of
+ * lrkv_decode_rope_workspace_size() bytes.  Supported: dtype BF16,
+ * head_dim 64 or 128, rank 16, 32, 48 or 64, heads a multiple of 8, a
+ * contiguous cache; others return LRKV_ERR_UNSUPPORTED.  The rebuild costs
+ * head_dim x rank multiply-adds per (row, head) on the tensor cores beyond
+ * lrkv_decode.
+ */
+lrkv_status lrkv_rope_table(int max_pos, int head_dim, float base, float* cos_sin, lrkv_stream_t stream);
+lrkv_status lrkv_decode_rope_workspace_size(const lrkv_dims* dims, size_t* bytes);
+lrkv_status lrkv_decode_rope(const lrkv_dims* dims, const void* q_rot, const void* k_s, const void* v_s,
+                             const void* z_k, const void* z_v, const void* b_k, const void* b_v,
+                             const float* cos_sin, int max_pos, const int32_t* seq_lens, float* out, float* lse,
+                             void* ws, size_t ws_bytes, lrkv_stream_t stream);
 
 /*
  * Read the device status word that the kernels of the last call(s) using

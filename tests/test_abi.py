@@ -201,3 +201,29 @@ def test_prefill_workspace_size_and_rejection_without_gpu(lib):
     paged = (fake,) * 6 + (fake,)  # k_s .. b_v, seq_lens
     assert lib.lrkv_prefill_paged(ctypes.byref(d), 128, fake, 128, 64, fake, *paged, fake, fake, fake, need - 1,
                                   None) == lrkv.LRKV_ERR_WORKSPACE
+
+
+def test_rope_entries_reject_bad_arguments_without_gpu(lib):
+    """The full-RoPE table and decode check shapes, the table length and the
+    workspace on the host before any launch."""
+    fake = ctypes.c_void_p(4096)
+    assert lib.lrkv_rope_table(0, 128, 10000.0, fake, None) == lrkv.LRKV_ERR_INVALID_ARG
+    assert lib.lrkv_rope_table(16, 127, 10000.0, fake, None) == lrkv.LRKV_ERR_INVALID_ARG   # odd head_dim
+    assert lib.lrkv_rope_table(16, 128, 1.0, fake, None) == lrkv.LRKV_ERR_INVALID_ARG      # base must exceed 1
+    assert lib.lrkv_rope_table(16, 128, 10000.0, None, None) == lrkv.LRKV_ERR_INVALID_ARG
+    n = ctypes.c_size_t(0)
+    for dims, want in [(lrkv.make_dims(2, 16, 64, 28, 64, "bf16"), lrkv.LRKV_ERR_UNSUPPORTED),    # rank % 16
+                       (lrkv.make_dims(2, 12, 64, 32, 64, "bf16"), lrkv.LRKV_ERR_UNSUPPORTED),    # heads % 8
+                       (lrkv.make_dims(2, 16, 96, 32, 64, "bf16"), lrkv.LRKV_ERR_UNSUPPORTED),    # head_dim
+                       (lrkv.make_dims(2, 16, 64, 32, 64, "f32"), lrkv.LRKV_ERR_UNSUPPORTED),
+                       (lrkv.make_dims(0, 16, 64, 32, 64, "bf16"), lrkv.LRKV_ERR_INVALID_ARG)]:
+        assert lib.lrkv_decode_rope_workspace_size(ctypes.byref(dims), ctypes.byref(n)) == want
+    ok = lrkv.make_dims(2, 16, 64, 32, 64, "bf16")
+    args = (fake,) * 8   # q~, the cache, the bases, the table
+    # a table shorter than the cache, a missing pointer, a missing workspace
+    assert lib.lrkv_decode_rope(ctypes.byref(ok), *args, 63, fake, fake, fake, fake, 1 << 20, None) == \
+        lrkv.LRKV_ERR_INVALID_ARG
+    assert lib.lrkv_decode_rope(ctypes.byref(ok), *args[:7], None, 64, fake, fake, fake, fake, 1 << 20, None) == \
+        lrkv.LRKV_ERR_INVALID_ARG
+    assert lib.lrkv_decode_rope(ctypes.byref(ok), *args, 64, fake, fake, fake, None, 1 << 20, None) == \
+        lrkv.LRKV_ERR_WORKSPACE
