@@ -395,6 +395,95 @@ def decode_rope_factored(q_rot, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens, base: fl
 
 
 # --------------------------------------------------------------------------
+# Comparison decodes on the same box (review §4 "Weight count and the two
+# decode regimes", §5 on absorbed MLA and optimized GQA): dense attention over
+# materialised K/V with grouped heads, and MLA with the up-projections
+# absorbed.  Readings: GQA query head h reads KV head h // (H / H_kv); MLA
+# keeps one latent row c_j of width d_c per token for all heads,
+# K_h = C W_uk[h]^T and V_h = C W_uv[h]^T with W_uk[h], W_uv[h] of shape
+# [d_h, d_c]; one scale 1/sqrt(d_h); no position encoding on either (the same
+# positional semantics as the LRKV decode).
+# --------------------------------------------------------------------------
+
+def dense_decode_reference(q, k, v, seq_lens, scale: Optional[float] = None,
+                           pairs: Optional[Iterable[Tuple[int, int]]] = None):
+    """Textbook decode over materialised K/V: q [B, H, d], k and v
+    [B, L, H_kv, d]; query head h attends KV head h // (H / H_kv) over rows
+    [0, seq_lens[b]).  Returns out [B, H, d], lse [B, H] (float64)."""
+    q, k, v = (_f64(a) for a in (q, k, v))
+    lens = np.asarray(_f64(seq_lens), dtype=np.int64)
+    B, H, d = q.shape
+    Hkv = k.shape[2]
+    g = H // Hkv
+    if scale is None:
+        scale = default_scale(d)
+    out = np.full((B, H, d), np.nan)
+    lse = np.full((B, H), np.nan)
+    todo = pairs if pairs is not None else [(b, h) for b in range(B) for h in range(H)]
+    for b, h in todo:
+        L = int(lens[b])
+        if L == 0:
+            out[b, h] = 0.0
+            lse[b, h] = -np.inf
+            continue
+        K, V = k[b, :L, h // g], v[b, :L, h // g]
+        out[b, h], lse[b, h] = _softmax_attend(scale * (K @ q[b, h]), V)
+    return out, lse
+
+
+def mla_decode_reference(q, c, w_uk, w_uv, seq_lens, scale: Optional[float] = None,
+                         pairs: Optional[Iterable[Tuple[int, int]]] = None):
+    """MLA decode by the definition: rebuild every head's keys and values from
+    the shared latent rows, K_h = C W_uk[h]^T, V_h = C W_uv[h]^T (c [B, L, d_c],
+    w_uk, w_uv [H, d_h, d_c]), then textbook softmax attention with q
+    [B, H, d_h].  Returns out [B, H, d_h], lse [B, H]."""
+    q, c, w_uk, w_uv = (_f64(a) for a in (q, c, w_uk, w_uv))
+    lens = np.asarray(_f64(seq_lens), dtype=np.int64)
+    B, H, dh = q.shape
+    if scale is None:
+        scale = default_scale(dh)
+    out = np.full((B, H, dh), np.nan)
+    lse = np.full((B, H), np.nan)
+    todo = pairs if pairs is not None else [(b, h) for b in range(B) for h in range(H)]
+    for b, h in todo:
+        L = int(lens[b])
+        if L == 0:
+            out[b, h] = 0.0
+            lse[b, h] = -np.inf
+            continue
+        K = c[b, :L] @ w_uk[h].T
+        V = c[b, :L] @ w_uv[h].T
+        out[b, h], lse[b, h] = _softmax_attend(scale * (K @ q[b, h]), V)
+    return out, lse
+
+
+def mla_decode_absorbed(q, c, w_uk, w_uv, seq_lens, scale: Optional[float] = None):
+    """The absorbed form (review §5: (q_h A_h) Z^T for the scores, the values
+    likewise): q_c = q_h W_uk[h] (d_c), scores q_c . c_j, o_c = sum_j a_j c_j,
+    o_h = o_c W_uv[h]^T.  Used only to pin mla_decode_reference."""
+    q, c, w_uk, w_uv = (_f64(a) for a in (q, c, w_uk, w_uv))
+    lens = np.asarray(_f64(seq_lens), dtype=np.int64)
+    B, H, dh = q.shape
+    if scale is None:
+        scale = default_scale(dh)
+    out = np.zeros((B, H, dh))
+    lse = np.full((B, H), -np.inf)
+    for b in range(B):
+        L = int(lens[b])
+        if L == 0:
+            continue
+        for h in range(H):
+            qc = q[b, h] @ w_uk[h]
+            s = scale * (c[b, :L] @ qc)
+            m = np.max(s)
+            w = np.exp(s - m)
+            l = np.sum(w)
+            out[b, h] = ((w / l) @ c[b, :L]) @ w_uv[h].T
+            lse[b, h] = m + math.log(l)
+    return out, lse
+
+
+# --------------------------------------------------------------------------
 # Cache and parameter accounting (notes §2.5-2.6; review §4)
 # --------------------------------------------------------------------------
 
