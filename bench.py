@@ -28,7 +28,8 @@ every step, one public-API call per step), `decode_step` (the new token's
 rows from its layer input, then the decode, as dependent steps),
 `decode_normed` (post-projection RMSNorm key scales), `decode_paged` (the
 rows in 256-row pages through a block table), `decode_rope` (full RoPE of the
-keys, exact: keys rebuilt tile by tile and rotated) and `prefill` (append GEMM,
+keys, exact: keys rebuilt tile by tile and rotated), `compare` (dense MHA, GQA
+and absorbed MLA at the headline's batch, length and heads) and `prefill` (append GEMM,
 causal prefill and the normalised-key prefill of 2 x 4096 tokens, against the
 bf16 tensor peak).
 """
@@ -765,6 +766,72 @@ def decode_rope_leg(setup, K, W, stream, use_graph, world, dev, base_ms):
             "rebuild_flop": rebuild_flop, "rebuild_tflops": rebuild_flop / (r_ms * 1e-3) / 1e12 * world}
 
 
+def compare_leg(w, K, W, stream, use_graph, world, dev, lrkv_ms, peak):
+    """The comparison decodes at the headline's batch, length, heads and
+    dtype (review §5: a fair serving comparison runs absorbed MLA and
+    optimized GQA beside the factored kernel): dense MHA and GQA (8 KV heads)
+    over materialised K/V, and absorbed MLA with a 512-wide latent; inputs
+    drawn on the device (timing only; parity is in the tests)."""
+    import torch
+    from compressed_cache_decode_gb300 import lrkv
+    B, L, H, dh = w.batch, w.max_len, w.heads, w.head_dim
+    gen = torch.Generator(device=dev).manual_seed(11)
+    lens = torch.full((B,), L, dtype=torch.int32, device=dev)
+    out = torch.empty((B, H, dh), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+    res = {}
+
+    def timed(fn, alg_bytes):
+        t = StepTimer(fn, K, W, stream, use_graph)
+        t.warm()
+        sp = _spread(t.time(repeats=7))
+        ms = max_over_ranks(sp["median"], world, dev)
+        return {"ms_per_step": ms, "ms_per_step_spread": sp, "algorithmic_bytes": alg_bytes,
+                "gbs": job_gbs(alg_bytes, world, ms), "hbm_frac": alg_bytes / (ms * 1e-3) / 1e9 / peak,
+                "vs_lrkv_time": ms / lrkv_ms}
+
+    q = torch.randn((B, H, dh), generator=gen, device=dev).to(torch.bfloat16)
+    for name, hkv in (("mha", H), ("gqa8", 8)):
+        k = torch.randn((B, L, hkv, dh), generator=gen, device=dev).to(torch.bfloat16)
+        v = torch.randn((B, L, hkv, dh), generator=gen, device=dev).to(torch.bfloat16)
+        _, _, ws = lrkv.dense_decode(q, k, v, lens, out=out, lse=lse)
+        dims = lrkv.lrkv_dense_dims(B, H, hkv, dh, L, 0.0)
+
+        def dstep(i, s, k=k, v=v, ws=ws, dims=dims):
+            st = lrkv.load().lrkv_dense_decode(lrkv.ctypes.byref(dims), lrkv._ptr(q), lrkv._ptr(k), lrkv._ptr(v),
+                                               lrkv._ptr(lens), lrkv._ptr(out), lrkv._ptr(lse), lrkv._ptr(ws),
+                                               ws.numel(), lrkv._stream_handle(s))
+            if st != lrkv.LRKV_OK:
+                raise lrkv.LRKVError(st, "lrkv_dense_decode")
+
+        alg = B * L * 2 * hkv * dh * 2 + q.numel() * 2 + B * H * (dh + 1) * 4
+        res[name] = dict(timed(dstep, alg), kv_heads=hkv, cache_elems_per_token=2 * hkv * dh)
+        del k, v, ws
+        torch.cuda.empty_cache()
+    dc = 512
+    c = torch.randn((B, L, dc), generator=gen, device=dev).to(torch.bfloat16)
+    w_uk = (torch.randn((H, dh, dc), generator=gen, device=dev) / dc ** 0.5).to(torch.bfloat16)
+    w_uv = (torch.randn((H, dh, dc), generator=gen, device=dev) / dc ** 0.5).to(torch.bfloat16)
+    _, _, ws = lrkv.mla_decode(q, c, w_uk, w_uv, lens, out=out, lse=lse)
+    mdims = lrkv.lrkv_mla_dims(B, H, dh, dc, L, 0.0)
+
+    def mstep(i, s):
+        st = lrkv.load().lrkv_mla_decode(lrkv.ctypes.byref(mdims), lrkv._ptr(q), lrkv._ptr(c), lrkv._ptr(w_uk),
+                                         lrkv._ptr(w_uv), lrkv._ptr(lens), lrkv._ptr(out), lrkv._ptr(lse),
+                                         lrkv._ptr(ws), ws.numel(), lrkv._stream_handle(s))
+        if st != lrkv.LRKV_OK:
+            raise lrkv.LRKVError(st, "lrkv_mla_decode")
+
+    alg = B * L * dc * 2 + 2 * H * dh * dc * 2 + q.numel() * 2 + B * H * (dh + 1) * 4
+    res["mla512"] = dict(timed(mstep, alg), latent_dim=dc, cache_elems_per_token=dc,
+                         score_value_flop=4 * B * L * H * dc)
+    del c, w_uk, w_uv, ws
+    torch.cuda.empty_cache()
+    res["lrkv"] = {"ms_per_step": lrkv_ms, "cache_elems_per_token": 2 * (dh + H * w.rank)}
+    res["shape"] = {"batch": B, "seq_len": L, "heads": H, "head_dim": dh, "dtype": "bf16", "position": "none"}
+    return res
+
+
 def e2e_leg(setup, K, stream, use_graph, world, dev):
     """End to end through the public API: every step copies the new token's
     layer input x, its query q and the lengths from pinned host memory (one
@@ -915,6 +982,11 @@ def main():
     normed_leg = decode_normed_leg(head, K, W, stream, use_graph, world, dev, ms_step) if not a.no_legs else None
     paged_leg = decode_paged_leg(head, K, W, stream, use_graph, world, dev, ms_step) if not a.no_legs else None
     rope_leg = decode_rope_leg(head, K, W, stream, use_graph, world, dev, ms_step) if not a.no_legs else None
+    cmp_leg = None
+    if not a.no_legs:
+        del head.reps[1:]
+        torch.cuda.empty_cache()
+        cmp_leg = compare_leg(w, K, W, stream, use_graph, world, dev, ms_step, peak)
 
     # ---- the other decode workloads, and the decode step on the 4K one ----
     legs, step_leg = {}, None
@@ -972,6 +1044,7 @@ def main():
             "decode_normed": normed_leg,
             "decode_paged": paged_leg,
             "decode_rope": rope_leg,
+            "compare": cmp_leg,
             "prefill": prefill,
         }
         print(json.dumps(res), flush=True)

@@ -777,8 +777,8 @@ template <bool BF16, int KC>  // KC: columns per lane, ceil((dh + r) / 32)
 __global__ void __launch_bounds__(32 * kWideWarps) lrkv_decode_merge_wide_kernel(const DecodePlan P) {
   __shared__ float s_m[kWideWarps], s_l[kWideWarps];
   __shared__ float s_acc[kWideWarps][32 * KC];
-  __shared__ float s_z[kMaxRank];
-  __shared__ float s_os[256];  // acc_s / L (head_dim <= 256)
+  __shared__ float s_z[KC * 32];   // acc_z / L (private width <= 32 KC)
+  __shared__ float s_os[KC * 32];  // acc_s / L
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = P.H, dh = P.dh, r = P.r, W = dh + r;
   pdl_trigger();  // the next step's scan may launch (it waits before it writes)
@@ -899,7 +899,8 @@ CombineFn combine_fn(const DecodePlan& P) {
   if (P.wide_merge) {
     if (cols <= 3) return lrkv_decode_merge_wide_kernel<BF16, 3>;
     if (cols <= 6) return lrkv_decode_merge_wide_kernel<BF16, 6>;
-    return lrkv_decode_merge_wide_kernel<BF16, 10>;
+    if (cols <= 10) return lrkv_decode_merge_wide_kernel<BF16, 10>;
+    return lrkv_decode_merge_wide_kernel<BF16, 20>;
   }
   if (cols <= 3) return lrkv_decode_combine_kernel<BF16, 3>;
   if (cols <= 6) return lrkv_decode_combine_kernel<BF16, 6>;

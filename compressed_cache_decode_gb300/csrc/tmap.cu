@@ -45,6 +45,19 @@ bool make_tmap_4d_bf16_strided(CUtensorMap* map, const void* base, const uint64_
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_tmap_4d_bf16_swizzled(CUtensorMap* map, const void* base, const uint64_t dims[4],
+                                const uint64_t strides_bytes[3], const uint32_t box[4]) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t d[4] = {dims[0], dims[1], dims[2], dims[3]};
+  const cuuint64_t st[3] = {strides_bytes[0], strides_bytes[1], strides_bytes[2]};
+  const cuuint32_t bx[4] = {box[0], box[1], box[2], box[3]};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), d, st, bx, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_tmap_2d_f32(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint32_t b0, uint32_t b1) {
   auto fn = encode_fn();
   if (!fn) return false;

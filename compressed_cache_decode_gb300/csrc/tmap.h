@@ -23,6 +23,10 @@ bool make_tmap_3d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t
 bool make_tmap_4d_bf16_strided(CUtensorMap* map, const void* base, const uint64_t dims[4],
                                const uint64_t strides_bytes[3], const uint32_t box[4]);
 
+// As make_tmap_4d_bf16_strided, with the 128-byte swizzle (b0 * 2 <= 128).
+bool make_tmap_4d_bf16_swizzled(CUtensorMap* map, const void* base, const uint64_t dims[4],
+                                const uint64_t strides_bytes[3], const uint32_t box[4]);
+
 // Encode a 2-D tiled tensor map for a row-major [d1][d0] fp32 tensor with box
 // {b0, b1} (b0 may exceed d0: the excess is filled with zeros) and no swizzle.
 bool make_tmap_2d_f32(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint32_t b0, uint32_t b1);

@@ -224,3 +224,29 @@ def random_prefill_case(seed: int, batch: int, q_len: int, heads: int, head_dim:
     dt = torch.float32 if dtype == "f32" else torch.bfloat16
     return dict(q=q.to(dt), k_s=k_s.to(dt), v_s=v_s.to(dt), z_k=z_k.to(dt), z_v=z_v.to(dt),
                 b_k=b_k.to(dt), b_v=b_v.to(dt), seq_lens=torch.tensor(lens, dtype=torch.int32))
+
+
+def random_dense_case(seed: int, batch: int, heads: int, kv_heads: int, head_dim: int, max_len: int, lens,
+                      dtype=torch.bfloat16) -> Dict[str, torch.Tensor]:
+    """Materialised K/V for the comparison decode: q [B, H, d], k, v
+    [B, L, H_kv, d] ~ N(0,1); draw order k, v, q."""
+    gen = torch.Generator().manual_seed(seed)
+    k = _normal(gen, (batch, max_len, kv_heads, head_dim))
+    v = _normal(gen, (batch, max_len, kv_heads, head_dim))
+    q = _normal(gen, (batch, heads, head_dim))
+    return dict(q=q.to(dtype), k=k.to(dtype), v=v.to(dtype), seq_lens=torch.tensor(lens, dtype=torch.int32))
+
+
+def random_mla_case(seed: int, batch: int, heads: int, head_dim: int, latent_dim: int, max_len: int, lens,
+                    dtype=torch.bfloat16) -> Dict[str, torch.Tensor]:
+    """Latent rows and up-projections for the absorbed-MLA comparison
+    decode: c [B, L, d_c] ~ N(0,1), q [B, H, d_h] ~ N(0,1), w_uk, w_uv
+    [H, d_h, d_c] ~ N(0, 1/d_c); draw order c, q, w_uk, w_uv."""
+    gen = torch.Generator().manual_seed(seed)
+    c = _normal(gen, (batch, max_len, latent_dim))
+    q = _normal(gen, (batch, heads, head_dim))
+    wstd = 1.0 / math.sqrt(latent_dim)
+    w_uk = _normal(gen, (heads, head_dim, latent_dim), wstd)
+    w_uv = _normal(gen, (heads, head_dim, latent_dim), wstd)
+    return dict(q=q.to(dtype), c=c.to(dtype), w_uk=w_uk.to(dtype), w_uv=w_uv.to(dtype),
+                seq_lens=torch.tensor(lens, dtype=torch.int32))

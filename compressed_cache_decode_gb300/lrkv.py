@@ -50,6 +50,10 @@ EXPORTED = (
     "lrkv_rope_table",
     "lrkv_decode_rope_workspace_size",
     "lrkv_decode_rope",
+    "lrkv_dense_decode_workspace_size",
+    "lrkv_dense_decode",
+    "lrkv_mla_decode_workspace_size",
+    "lrkv_mla_decode",
     "lrkv_read_device_status",
 )
 
@@ -64,6 +68,16 @@ class lrkv_dims(ctypes.Structure):
         ("dtype", ctypes.c_int),
         ("scale", ctypes.c_float),
     ]
+
+
+class lrkv_dense_dims(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int), ("heads", ctypes.c_int), ("kv_heads", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("max_len", ctypes.c_int), ("scale", ctypes.c_float)]
+
+
+class lrkv_mla_dims(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int), ("heads", ctypes.c_int), ("head_dim", ctypes.c_int),
+                ("latent_dim", ctypes.c_int), ("max_len", ctypes.c_int), ("scale", ctypes.c_float)]
 
 
 class LRKVError(RuntimeError):
@@ -140,6 +154,15 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.lrkv_decode_rope.restype = ctypes.c_int
     lib.lrkv_decode_rope.argtypes = [dims_p, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int, i32p, vp, vp, vp, sz,
                                      vp]
+    ddp, mdp = ctypes.POINTER(lrkv_dense_dims), ctypes.POINTER(lrkv_mla_dims)
+    lib.lrkv_dense_decode_workspace_size.restype = ctypes.c_int
+    lib.lrkv_dense_decode_workspace_size.argtypes = [ddp, ctypes.POINTER(sz)]
+    lib.lrkv_dense_decode.restype = ctypes.c_int
+    lib.lrkv_dense_decode.argtypes = [ddp, vp, vp, vp, i32p, vp, vp, vp, sz, vp]
+    lib.lrkv_mla_decode_workspace_size.restype = ctypes.c_int
+    lib.lrkv_mla_decode_workspace_size.argtypes = [mdp, ctypes.POINTER(sz)]
+    lib.lrkv_mla_decode.restype = ctypes.c_int
+    lib.lrkv_mla_decode.argtypes = [mdp, vp, vp, vp, vp, i32p, vp, vp, vp, sz, vp]
     lib.lrkv_read_device_status.restype = ctypes.c_int
     lib.lrkv_read_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
     if path is None:
@@ -580,3 +603,49 @@ def decode_rope(q_rot, k_s, v_s, z_k, z_v, b_k, b_v, cos_sin, seq_lens, scale: f
     if st != LRKV_OK:
         raise LRKVError(st, "lrkv_decode_rope")
     return out, lse
+
+
+# ------------------------------------------------- comparison decodes --
+
+def dense_decode(q, k, v, seq_lens, scale: float = 0.0, out=None, lse=None, ws=None, stream=None):
+    """Decode over materialised K/V (MHA, GQA, MQA): q [B, H, d], k, v
+    [B, L, H_kv, d] bf16.  Returns (out, lse, ws)."""
+    B, H, d = q.shape
+    dims = lrkv_dense_dims(B, H, k.shape[2], d, k.shape[1], float(scale))
+    if out is None:
+        out = torch.empty((B, H, d), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    if ws is None:
+        n = ctypes.c_size_t(0)
+        st = load().lrkv_dense_decode_workspace_size(ctypes.byref(dims), ctypes.byref(n))
+        if st != LRKV_OK:
+            raise LRKVError(st, "lrkv_dense_decode_workspace_size")
+        ws = torch.empty(int(n.value), dtype=torch.uint8, device=q.device)
+    st = int(load().lrkv_dense_decode(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(seq_lens), _ptr(out),
+                                      _ptr(lse), _ptr(ws), ws.numel(), _stream_handle(stream)))
+    if st != LRKV_OK:
+        raise LRKVError(st, "lrkv_dense_decode")
+    return out, lse, ws
+
+
+def mla_decode(q, c, w_uk, w_uv, seq_lens, scale: float = 0.0, out=None, lse=None, ws=None, stream=None):
+    """Absorbed MLA decode: q [B, H, d_h], c [B, L, d_c], w_uk, w_uv
+    [H, d_h, d_c] bf16.  Returns (out, lse, ws)."""
+    B, H, dh = q.shape
+    dims = lrkv_mla_dims(B, H, dh, c.shape[2], c.shape[1], float(scale))
+    if out is None:
+        out = torch.empty((B, H, dh), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    if ws is None:
+        n = ctypes.c_size_t(0)
+        st = load().lrkv_mla_decode_workspace_size(ctypes.byref(dims), ctypes.byref(n))
+        if st != LRKV_OK:
+            raise LRKVError(st, "lrkv_mla_decode_workspace_size")
+        ws = torch.empty(int(n.value), dtype=torch.uint8, device=q.device)
+    st = int(load().lrkv_mla_decode(ctypes.byref(dims), _ptr(q), _ptr(c), _ptr(w_uk), _ptr(w_uv), _ptr(seq_lens),
+                                    _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream_handle(stream)))
+    if st != LRKV_OK:
+        raise LRKVError(st, "lrkv_mla_decode")
+    return out, lse, ws

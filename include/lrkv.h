@@ -420,6 +420,66 @@ lrkv_status lrkv_decode_rope(const lrkv_dims* dims, const void* q_rot, const voi
                              void* ws, size_t ws_bytes, lrkv_stream_t stream);
 
 /*
+ * Comparison decodes on the same box ("Low-Rank Key Value Attention | What a
+ * shared cache can preserve", §4 "Weight count and the two decode regimes"
+ * and §5: a fair serving comparison runs optimized GQA, dense MHA and
+ * absorbed MLA beside the factored kernel at the same batch, length and
+ * dtype).  They are not part of the LRKV method; they measure the layouts it
+ * replaces.
+ *
+ * lrkv_dense_decode: one decode step over materialised K/V (bf16),
+ *   q [batch][heads][head_dim], k, v [batch][max_len][kv_heads][head_dim];
+ *   query head h attends KV head h / (heads / kv_heads) over rows
+ *   [0, seq_lens[b]) with one softmax (MHA: kv_heads = heads; GQA; MQA:
+ *   kv_heads = 1); out [batch][heads][head_dim] fp32, lse [batch][heads] or
+ *   NULL.  No position encoding.  Supported: head_dim 64 or 128,
+ *   heads / kv_heads in {1, 2, 4, 8}.  Workspace:
+ *   lrkv_dense_decode_workspace_size() bytes; status word and errors as in
+ *   lrkv_decode.
+ */
+typedef struct {
+  int batch;       /* B >= 1                                 */
+  int heads;       /* query heads H >= 1                     */
+  int kv_heads;    /* KV heads, dividing H                   */
+  int head_dim;    /* d                                      */
+  int max_len;     /* rows per sequence in k and v           */
+  float scale;     /* <= 0 selects 1/sqrt(head_dim)          */
+} lrkv_dense_dims;
+
+lrkv_status lrkv_dense_decode_workspace_size(const lrkv_dense_dims* dims, size_t* bytes);
+lrkv_status lrkv_dense_decode(const lrkv_dense_dims* dims, const void* q, const void* k, const void* v,
+                              const int32_t* seq_lens, float* out, float* lse, void* ws, size_t ws_bytes,
+                              lrkv_stream_t stream);
+
+/*
+ * lrkv_mla_decode: absorbed multi-head latent attention over one latent row
+ * per token for all heads (review §5: the head computes (q_h A_h) Z^T instead
+ * of materialising its keys; the values likewise), bf16 storage:
+ *   q [batch][heads][head_dim], c [batch][max_len][latent_dim],
+ *   w_uk, w_uv [heads][head_dim][latent_dim] (K_h = C W_uk[h]^T,
+ *   V_h = C W_uv[h]^T), score q_h . k_h,j * scale (scale <= 0:
+ *   1/sqrt(head_dim)), one softmax, out [batch][heads][head_dim] fp32, lse as
+ *   in lrkv_decode.  Three launches: q_h W_uk[h] (fp32, in the workspace),
+ *   the scan over c (q_c split into two bf16 parts for the tensor cores), and
+ *   the merge, which lifts the latent sum through W_uv[h]^T.  Supported:
+ *   latent_dim 256 or 512, heads 8, 16 or 32, head_dim <= 128; c 16-byte
+ *   aligned.  Workspace: lrkv_mla_decode_workspace_size() bytes.
+ */
+typedef struct {
+  int batch;
+  int heads;
+  int head_dim;    /* d_h of q and of the output                          */
+  int latent_dim;  /* d_c of the cached latent rows                       */
+  int max_len;
+  float scale;     /* <= 0 selects 1/sqrt(head_dim)                       */
+} lrkv_mla_dims;
+
+lrkv_status lrkv_mla_decode_workspace_size(const lrkv_mla_dims* dims, size_t* bytes);
+lrkv_status lrkv_mla_decode(const lrkv_mla_dims* dims, const void* q, const void* c, const void* w_uk,
+                            const void* w_uv, const int32_t* seq_lens, float* out, float* lse, void* ws,
+                            size_t ws_bytes, lrkv_stream_t stream);
+
+/*
  * Read the device status word that the kernels of the last call(s) using
  * `ws` recorded (LRKV_OK, LRKV_ERR_TIMEOUT or LRKV_ERR_DEVICE_BOUNDS).
  * Synchronises `stream`.  Each lrkv_decode/lrkv_prefill call sets the word

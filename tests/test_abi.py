@@ -227,3 +227,27 @@ def test_rope_entries_reject_bad_arguments_without_gpu(lib):
         lrkv.LRKV_ERR_INVALID_ARG
     assert lib.lrkv_decode_rope(ctypes.byref(ok), *args, 64, fake, fake, fake, None, 1 << 20, None) == \
         lrkv.LRKV_ERR_WORKSPACE
+
+
+def test_comparison_entries_reject_bad_arguments_without_gpu(lib):
+    """The dense and MLA comparison decodes check shapes before any launch."""
+    n = ctypes.c_size_t(0)
+    dd = lrkv.lrkv_dense_dims
+    for dims, want in [(dd(2, 32, 2, 128, 64, 0.0), lrkv.LRKV_ERR_UNSUPPORTED),   # group of 16
+                       (dd(2, 8, 8, 96, 64, 0.0), lrkv.LRKV_ERR_UNSUPPORTED),     # head_dim 96
+                       (dd(2, 8, 3, 64, 64, 0.0), lrkv.LRKV_ERR_INVALID_ARG),     # 3 does not divide 8
+                       (dd(0, 8, 8, 64, 64, 0.0), lrkv.LRKV_ERR_INVALID_ARG)]:
+        assert lib.lrkv_dense_decode_workspace_size(ctypes.byref(dims), ctypes.byref(n)) == want
+    md = lrkv.lrkv_mla_dims
+    for dims, want in [(md(2, 32, 128, 384, 64, 0.0), lrkv.LRKV_ERR_UNSUPPORTED),   # latent width
+                       (md(2, 12, 128, 512, 64, 0.0), lrkv.LRKV_ERR_UNSUPPORTED),    # 12 heads
+                       (md(2, 32, 256, 512, 64, 0.0), lrkv.LRKV_ERR_UNSUPPORTED),    # head_dim
+                       (md(2, 32, 128, 512, 0, 0.0), lrkv.LRKV_ERR_INVALID_ARG)]:
+        assert lib.lrkv_mla_decode_workspace_size(ctypes.byref(dims), ctypes.byref(n)) == want
+    fake = ctypes.c_void_p(4096)
+    ok = dd(2, 8, 8, 64, 64, 0.0)
+    assert lib.lrkv_dense_decode(ctypes.byref(ok), fake, fake, fake, fake, fake, None, None, 1 << 20, None) == \
+        lrkv.LRKV_ERR_WORKSPACE
+    okm = md(2, 8, 64, 256, 64, 0.0)
+    assert lib.lrkv_mla_decode(ctypes.byref(okm), fake, ctypes.c_void_p(4096 + 8), fake, fake, fake, fake, None,
+                               fake, 1 << 20, None) == lrkv.LRKV_ERR_INVALID_ARG   # c not 16-byte aligned
