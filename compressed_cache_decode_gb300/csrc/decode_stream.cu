@@ -39,6 +39,7 @@
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <type_traits>
 #include <utility>
 
 #include <cuda.h>
@@ -347,7 +348,9 @@ __device__ __forceinline__ void l2_prefetch_tiles(const DecodePlan& P, const int
 
 }  // namespace
 
-template <int DHT, int MZMAX>
+// EXACT: the launch's latent step count equals MZMAX (its loops need no
+// per-step guard); otherwise at most MZMAX steps, guarded at run time.
+template <int DHT, int MZMAX, bool EXACT>
 __global__ void __launch_bounds__(kThreadsS, 1)
     lrkv_decode_stream_kernel(const __grid_constant__ DecodePlan P, const __grid_constant__ CUtensorMap tm_k,
                               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_zk,
@@ -356,6 +359,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
   constexpr int BS = MZA > 16 ? 2 : 4;       // private-score steps per load batch
   constexpr int BZ = MZA > 16 ? 4 : 8;       // private-value steps per load batch
   constexpr int KB = DHT > 4 ? 4 : DHT;      // head-dim steps per load batch of the shared rows
+  const int kst = EXACT ? MZA : P.kst;       // latent steps per warp (a constant when EXACT)
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ int s_timeout;
   __shared__ int s_nopage;  // a block table entry named no page of the pool
@@ -510,7 +514,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
   // steps kk whose latent column 16 kk + 2 q4 (bit of vmask0), or that
   // column + 8 (vmask1), belongs to this lane's head g within the half
   uint32_t vmask0 = 0u, vmask1 = 0u;
-  for (int kk = 0; kk < P.kst; ++kk) {
+  for (int kk = 0; kk < kst; ++kk) {
     const int j = 16 * kk + 2 * q4;
     vmask0 |= (j / r == g ? 1u : 0u) << kk;
     vmask1 |= ((j + 8) / r == g ? 1u : 0u) << kk;
@@ -557,6 +561,20 @@ __global__ void __launch_bounds__(kThreadsS, 1)
         *reinterpret_cast<volatile int*>(&issued[j]) = j;
       }
     }
+  }
+  // this pair's next tile (tiles pair, pair + 4, ... across the pieces), its
+  // ring stage and that stage's phase parity, advanced without a division
+  int inext = pair, snext = pair % P.stages;
+  uint32_t pnext = static_cast<uint32_t>(pair / P.stages) & 1u;
+  // ldmatrix row addresses within the shared rows' 128-byte-swizzled boxes
+  // for head-dim steps n with n & 3 = m (step n is in box n >> 2): chunk
+  // 2 m + (lane half) of row arow (scores) or trow (transposed values),
+  // XORed with the row's low bits
+  int koff[4], voff[4];
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    koff[m] = arow * 128 + (((2 * m + ahalf) ^ (arow & 7)) << 4);
+    voff[m] = trow * 128 + (((2 * m + tcol) ^ (trow & 7)) << 4);
   }
   int ibase = 0;      // tile index of the piece's first tile
   int kp = warm ? -1 : 0;  // piece counter (p/q buffer kp & 1); -1: the warm-up pass
@@ -666,16 +684,19 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       l2_prefetch_tiles(P, pre, B, g0, g1, P.stages, P.stages + P.pfw);
 
     // ---- this pair's tiles of the piece ----------------------------------------
-    const int first = ibase + ((pair - ibase) % kPairs + kPairs) % kPairs;
-    for (int i = first; i < ibase + pc.ntiles; i += kPairs) {
-      const int s = i % P.stages;
+    // rows of the piece's sequence: a tile reaching past them may hold
+    // unwritten rows (any bits, NaN included)
+    const int seq_rows = pre[pc.b + 1] - pre[pc.b];
+    while (inext < ibase + pc.ntiles) {
+      const int i = inext, s = snext;
+      const uint32_t par = pnext;
       const int t0 = pc.t_beg + (i - ibase) * kT;
       const int nvalid = dry ? 0 : min(kT, pc.t_end - t0);
       const int lo = max(0, pc.t_lo - t0);  // rows [lo, nvalid) of the tile are this CTA's
       if (ok && !dry && *reinterpret_cast<volatile int*>(&s_timeout)) ok = false;  // stop waiting
       if (ok && !dry) {
         ok = wait_issued(&issued[s], i, P.wait_limit) &&
-             mbar_wait_bounded(&full[s], static_cast<uint32_t>(i / P.stages) & 1u, P.wait_limit);
+             mbar_wait_bounded(&full[s], par, P.wait_limit);
         if (!ok) *reinterpret_cast<volatile int*>(&s_timeout) = 1;
       }
       if (ok && !*reinterpret_cast<volatile int*>(&s_timeout)) {
@@ -715,8 +736,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
           uint2 qv[KB];
 #pragma unroll
           for (int u = 0; u < KB; ++u) {
-            const int ch = 2 * (k0 + u) + ahalf;
-            ldsm_x4(a[u][0], a[u][1], a[u][2], a[u][3], ks + (ch >> 3) * (kT * 128) + swz_off(arow, ch & 7, 128));
+            ldsm_x4(a[u][0], a[u][1], a[u][2], a[u][3], ks + ((k0 + u) >> 2) * (kT * 128) + koff[(k0 + u) & 3]);
             qv[u] = qfl[(k0 + u) * 32];
           }
 #pragma unroll
@@ -731,19 +751,20 @@ __global__ void __launch_bounds__(kThreadsS, 1)
           const unsigned char* z0 = zk + arow * zrow + ahalf * 16;
           const int* zoh = zo + 32 * hf;
           const uint2* pt = reinterpret_cast<const uint2*>(pqcur + 16 * dh * 2) + 4 * hf * r + q4;
-          for (int kk = 0; kk < P.kst; kk += BS) {  // batches of BS steps (kst is even)
+#pragma unroll 1
+          for (int kk = 0; kk < kst; kk += BS) {  // batches of BS steps (kst is even)
             uint32_t a[BS][4];
             uint2 f0[BS], f1[BS];
 #pragma unroll
             for (int u = 0; u < BS; ++u)
-              if (u < 2 || kk + u < P.kst) {
+              if (kk + u < kst) {
                 ldsm_x4(a[u][0], a[u][1], a[u][2], a[u][3], z0 + zoh[kk + u]);
                 f0[u] = pt[8 * (kk + u)];
                 f1[u] = pt[8 * (kk + u) + 4];
               }
 #pragma unroll
             for (int u = 0; u < BS; ++u)
-              if (u < 2 || kk + u < P.kst) {
+              if (kk + u < kst) {
                 const bool k0v = (vmask0 >> (kk + u)) & 1u, k1v = (vmask1 >> (kk + u)) & 1u;
                 const uint32_t h0 = k0v ? f0[u].x : 0u, l0 = k0v ? f0[u].y : 0u;
                 const uint32_t h1 = k1v ? f1[u].x : 0u, l1 = k1v ? f1[u].y : 0u;
@@ -797,37 +818,55 @@ __global__ void __launch_bounds__(kThreadsS, 1)
         const uint32_t pb0 = movmatrix_trans(pack_bf16(p0, p1));  // tokens 0-7
         const uint32_t pb1 = movmatrix_trans(pack_bf16(p2, p3));  // tokens 8-15
 
-        // shared values: O_s^T += V_s^T P^T (rows = head dim)
+        // Values.  The A operands of tokens outside [lo, nvalid) meet zero
+        // probabilities; only a tile reaching past the sequence's rows may
+        // hold non-finite bits there (unwritten rows), where 0 x NaN must not
+        // reach the sums: that tile (and the warm-up pass) zeroes those
+        // tokens' operand halves, every other tile runs unmasked.
+        auto values = [&](auto masked) {
+          constexpr bool M = decltype(masked)::value;
+          const uint32_t k0 = M ? keep0 : 0xffffffffu, k1 = M ? keep1 : 0xffffffffu;
+          // shared values: O_s^T += V_s^T P^T (rows = head dim)
 #pragma unroll
-        for (int n0 = 0; n0 < DHT; n0 += KB) {
-          uint32_t a[KB][4];
+          for (int n0 = 0; n0 < DHT; n0 += KB) {
+            uint32_t a[KB][4];
 #pragma unroll
-          for (int u = 0; u < KB; ++u) {
-            const int ch = 2 * (n0 + u) + tcol;
-            ldsm_x4_trans(a[u][0], a[u][1], a[u][2], a[u][3], vs + (ch >> 3) * (kT * 128) + swz_off(trow, ch & 7, 128));
+            for (int u = 0; u < KB; ++u)
+              ldsm_x4_trans(a[u][0], a[u][1], a[u][2], a[u][3], vs + ((n0 + u) >> 2) * (kT * 128) + voff[(n0 + u) & 3]);
+#pragma unroll
+            for (int u = 0; u < KB; ++u) {
+              if (M)
+                mma_bf16_16816(acc_v[n0 + u], a[u][0] & k0, a[u][1] & k0, a[u][2] & k1, a[u][3] & k1, pb0, pb1);
+              else
+                mma_bf16_16816(acc_v[n0 + u], a[u][0], a[u][1], a[u][2], a[u][3], pb0, pb1);
+            }
           }
+          // private values: O_z^T += Z_v^T P^T over this half's latent columns
+          if (MZMAX > 0) {
+            const unsigned char* z0 = zv + trow * zrow + tcol * 16;
+            const int* zoh = zo + 32 * hf;
 #pragma unroll
-          for (int u = 0; u < KB; ++u)
-            mma_bf16_16816(acc_v[n0 + u], a[u][0] & keep0, a[u][1] & keep0, a[u][2] & keep1, a[u][3] & keep1, pb0,
-                           pb1);
-        }
-        // private values: O_z^T += Z_v^T P^T over this half's latent columns
-        if (MZMAX > 0) {
-          const unsigned char* z0 = zv + trow * zrow + tcol * 16;
-          const int* zoh = zo + 32 * hf;
+            for (int n0 = 0; n0 < MZA; n0 += BZ) {  // batches of BZ steps
+              uint32_t a[BZ][4];
 #pragma unroll
-          for (int n0 = 0; n0 < MZA; n0 += BZ) {  // batches of BZ steps
-            uint32_t a[BZ][4];
+              for (int u = 0; u < BZ; ++u)
+                if (n0 + u < kst) ldsm_x4_trans(a[u][0], a[u][1], a[u][2], a[u][3], z0 + zoh[n0 + u]);
 #pragma unroll
-            for (int u = 0; u < BZ; ++u)
-              if (n0 + u < P.kst) ldsm_x4_trans(a[u][0], a[u][1], a[u][2], a[u][3], z0 + zoh[n0 + u]);
-#pragma unroll
-            for (int u = 0; u < BZ; ++u)
-              if (n0 + u < P.kst)
-                mma_bf16_16816(acc_z[n0 + u], a[u][0] & keep0, a[u][1] & keep0, a[u][2] & keep1, a[u][3] & keep1,
-                               pb0, pb1);
+              for (int u = 0; u < BZ; ++u)
+                if (n0 + u < kst) {
+                  if (M)
+                    mma_bf16_16816(acc_z[n0 + u], a[u][0] & k0, a[u][1] & k0, a[u][2] & k1, a[u][3] & k1, pb0,
+                                   pb1);
+                  else
+                    mma_bf16_16816(acc_z[n0 + u], a[u][0], a[u][1], a[u][2], a[u][3], pb0, pb1);
+                }
+            }
           }
-        }
+        };
+        if (dry || t0 + kT > seq_rows)
+          values(std::true_type{});
+        else
+          values(std::false_type{});
       }
       if (dry) break;
       // done with the stage: the second warp of the pair refills it with
@@ -864,6 +903,12 @@ __global__ void __launch_bounds__(kThreadsS, 1)
         }
       }
       __syncwarp();
+      inext += kPairs;
+      snext += kPairs;
+      while (snext >= P.stages) {
+        snext -= P.stages;
+        pnext ^= 1u;
+      }
     }
 
     if (dry) {  // warm-up pass done: the real first piece
@@ -909,7 +954,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
             // row j (this half) holds latent column j - (hl - hb) r of head hl
 #pragma unroll
             for (int n = 0; n < MZA; ++n) {
-              if (n < P.kst) {
+              if (n < kst) {
                 const int ca = 16 * n + g - (hl - hb) * r, cb = ca + 8;
                 if (ca >= 0 && ca < r) o[dh + ca] = acc_z[n][e];
                 if (cb >= 0 && cb < r) o[dh + cb] = acc_z[n][2 + e];
@@ -952,22 +997,20 @@ namespace {
 using StreamFn = void (*)(const DecodePlan, const CUtensorMap, const CUtensorMap, const CUtensorMap,
                           const CUtensorMap);
 
-// The latent steps a warp keeps accumulators for: the smallest instantiated
-// count >= kst (accumulators sized exactly for the common ranks 48 and 56
-// keep the kernel free of register spills).
-int mz_max_of(const DecodePlan& P) {
-  if (P.r == 0) return 0;
-  return P.kst <= 16 ? 16 : P.kst <= 24 ? 24 : P.kst <= 28 ? 28 : 32;
-}
-
+// The latent steps a warp keeps accumulators for: exactly kst for the ranks
+// 28, 32, 48, 56 and 64 (loops without guards, accumulators sized exactly:
+// no register spills), else the smallest of 16 and 32 that holds kst.
 template <int DHT>
 StreamFn pick_mz(const DecodePlan& P) {
-  switch (mz_max_of(P)) {
-    case 0: return lrkv_decode_stream_kernel<DHT, 0>;
-    case 16: return lrkv_decode_stream_kernel<DHT, 16>;
-    case 24: return lrkv_decode_stream_kernel<DHT, 24>;
-    case 28: return lrkv_decode_stream_kernel<DHT, 28>;
-    default: return lrkv_decode_stream_kernel<DHT, 32>;
+  if (P.r == 0) return lrkv_decode_stream_kernel<DHT, 0, false>;
+  switch (P.kst) {
+    case 14: return lrkv_decode_stream_kernel<DHT, 14, true>;
+    case 16: return lrkv_decode_stream_kernel<DHT, 16, true>;
+    case 24: return lrkv_decode_stream_kernel<DHT, 24, true>;
+    case 28: return lrkv_decode_stream_kernel<DHT, 28, true>;
+    case 32: return lrkv_decode_stream_kernel<DHT, 32, true>;
+    default:
+      return P.kst < 16 ? lrkv_decode_stream_kernel<DHT, 16, false> : lrkv_decode_stream_kernel<DHT, 32, false>;
   }
 }
 

@@ -6,8 +6,11 @@ call) the waits give up at once.  The scan must then skip the work that
 depended on them, still wait at the full bound for every copy it issued (so
 no copy lands in shared memory after the block exits), return, and record
 LRKV_ERR_TIMEOUT in the call's status word.  The next call on the same
-workspace with the default bound returns LRKV_OK and matches the oracle.  One
-small case per scan instantiation: a 16-head row tile, and 32 heads (two row
+workspace with the default bound returns LRKV_OK and matches the oracle.  The
+call runs with L2 flushed and caches larger than L2, so that its copies come
+from HBM and the ring streams at the HBM rate: the warps must wait for copies
+in flight (with every row already in L2 a copy may land before anyone waits
+for it, and nothing times out).  A 16-head row tile, and 32 heads (two row
 tiles, B^K staged through the ring)."""
 import numpy as np
 import pytest
@@ -28,7 +31,8 @@ def _lib():
     lrkv.load()
 
 
-@pytest.mark.parametrize("shape", [(2, 16, 64, 28, 300, [300, 77]), (2, 32, 128, 48, 200, [200, 64])])
+@pytest.mark.parametrize("shape", [(4, 16, 64, 28, 32768, [32768, 32768, 9000, 32768]),
+                                   (2, 32, 128, 48, 32768, [32768, 20000])])
 def test_decode_wait_timeout_is_reported_and_the_next_call_recovers(shape, monkeypatch):
     B, H, dh, r, L, lens = shape
     case = inputs.random_decode_case(seed=31 + H, batch=B, heads=H, head_dim=dh, rank=r, max_len=L,
@@ -38,6 +42,8 @@ def test_decode_wait_timeout_is_reported_and_the_next_call_recovers(shape, monke
     ws = lrkv.decode_workspace(dims, "cuda")
     args = (d["q"], d["k_s"], d["v_s"], d["z_k"], d["z_v"], d["b_k"], d["b_v"], d["seq_lens"])
 
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    flush.fill_(1)  # evicts the cache rows the copies to the device left in L2
     monkeypatch.setenv("LRKV_WAIT_LIMIT_CYCLES", "1")
     lrkv.decode(*args, ws=ws)
     torch.cuda.synchronize()
