@@ -360,6 +360,14 @@ __global__ void __launch_bounds__(kThreadsS, 1)
   constexpr int BZ = MZA > 16 ? 4 : 8;       // private-value steps per load batch
   constexpr int KB = DHT > 4 ? 4 : DHT;      // head-dim steps per load batch of the shared rows
   const int kst = EXACT ? MZA : P.kst;       // latent steps per warp (a constant when EXACT)
+  // Private values per head (ranks a multiple of 8, EXACT: r = 2 MZMAX):
+  // accumulator tile s holds latent columns 16 s .. 16 s + 15 of every head
+  // of the half (column h = head hb + h), each head's product masked to its
+  // own column; otherwise one tile per 16-column step of the half's 8 r
+  // latents, of which the diagonal blocks are kept.
+  constexpr bool PH = EXACT && MZMAX > 0 && (2 * MZMAX) % 8 == 0;
+  constexpr int NZH = PH ? (2 * MZMAX + 15) / 16 : 1;  // tiles per head (r / 16, rounded up)
+  constexpr int NZV = PH ? NZH : MZA;                  // private value accumulator tiles
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ int s_timeout;
   __shared__ int s_nopage;  // a block table entry named no page of the pool
@@ -382,6 +390,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
   int* cons = reinterpret_cast<int*>(smem + 192);     // [16] warps done with each stage
   uint64_t* pbar = reinterpret_cast<uint64_t*>(smem + 256);  // [2] p/q buffers
   int* zo = reinterpret_cast<int*>(smem + 320);       // [2][32] latent step offsets
+  int* zhead = reinterpret_cast<int*>(smem + 576);    // [16] shared byte offset of each head's latents
   int* pre = reinterpret_cast<int*>(smem + P.off_prefix);
   uint2* qf = reinterpret_cast<uint2*>(smem + P.off_pf);    // shared-score B fragments (q)
 
@@ -417,6 +426,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     fence_barrier_init();
   }
   if (tid < 64) zo[tid] = P.zo[tid >> 5][tid & 31];
+  if (PH && tid < 16) zhead[tid] = (tid / P.hs) * kT * P.segp * 2 + (tid % P.hs) * r * 2;
   int bad = 0;
   for (int b = tid; b < B; b += blockDim.x) {
     int L = P.seq_lens[b];
@@ -505,7 +515,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
   if (P.bk_stages == 0) bk_load(P, m0, bkr, 0, bkv);
 
   float acc_v[DHT][4] = {};      // O_s^T: rows d = 16 m + g (+8), columns heads 2 q4 + e
-  float acc_z[MZA][4] = {};      // O_z^T: rows latent column j = 16 m + g (+8) of this half
+  float acc_z[NZV][4] = {};      // O_z^T: rows latent column 16 m + g (+8) of this half (PH: of each head)
   float mc[2] = {-INFINITY, -INFINITY}, lc[2] = {0.f, 0.f};  // reference max, denominator
   const int zrow = P.segp * 2;  // bytes per segment row
   const int hb = 8 * hf;        // first head (row-tile local) of this half
@@ -632,7 +642,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
 #pragma unroll
       for (int k = 0; k < 4; ++k) acc_v[n][k] = 0.f;
 #pragma unroll
-    for (int n = 0; n < MZA; ++n)
+    for (int n = 0; n < NZV; ++n)
 #pragma unroll
       for (int k = 0; k < 4; ++k) acc_z[n][k] = 0.f;
     {
@@ -653,7 +663,31 @@ __global__ void __launch_bounds__(kThreadsS, 1)
         qf[e] = v;
       }
     }
-    if (MZMAX > 0) {
+    if (MZMAX > 0 && P.off_gt > 0) {
+      // the per-lane fragment table: entry (h2, g, kk, q4) holds p of head
+      // 8 h2 + g at the half's latent columns j = 16 kk + 2 q4 (+1) and j + 8
+      // (+9) as bf16 hi and lo parts, where the column is that head's (its r
+      // columns start at g r), zero elsewhere and past H
+      const float* prow = reinterpret_cast<const float*>(pqb + 16 * dh * 2);
+      const int ne = 64 * kst;
+      for (int e = tid; e < (tid < nset ? ne : 0); e += nset) {
+        const int q4e = e & 3, kk = (e >> 2) % kst, row = (e >> 2) / kst;  // row = 8 h2 + g
+        const int gg = row & 7;
+        uint32_t w[4];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int j = 16 * kk + 2 * q4e + 8 * half;
+          float2 v = make_float2(0.f, 0.f);
+          if (j / r == gg && row < nh) v = *reinterpret_cast<const float2*>(prow + row * r + j - gg * r);
+          const float h0 = __bfloat162float(__float2bfloat16_rn(v.x));
+          const float h1 = __bfloat162float(__float2bfloat16_rn(v.y));
+          w[2 * half] = pack_bf16(h0, h1);
+          w[2 * half + 1] = pack_bf16(v.x - h0, v.y - h1);
+        }
+        *reinterpret_cast<uint4*>(smem + P.off_gt + row * P.gt_stride + kk * 64 + q4e * 16) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    } else if (MZMAX > 0) {
       // p of the row tile's heads as bf16 high and low parts, head-major in
       // pairs of latent columns: entry e = hl r/2 + c/2 holds
       // {hi(p[c]), hi(p[c+1])}, {lo(p[c]), lo(p[c+1])} (zero past H), written
@@ -750,8 +784,29 @@ __global__ void __launch_bounds__(kThreadsS, 1)
           // (bit kk of vmask0 / vmask1) and zero elsewhere (block diagonal)
           const unsigned char* z0 = zk + arow * zrow + ahalf * 16;
           const int* zoh = zo + 32 * hf;
+          if (P.off_gt > 0) {
+            // this lane's fragments, already zero off its head's columns
+            const uint4* gt = reinterpret_cast<const uint4*>(smem + P.off_gt + (hb + g) * P.gt_stride) + q4;
+#pragma unroll (PH ? MZA : 1)
+            for (int kk = 0; kk < kst; kk += BS) {
+              uint32_t a[BS][4];
+              uint4 f[BS];
+#pragma unroll
+              for (int u = 0; u < BS; ++u)
+                if (kk + u < kst) {
+                  ldsm_x4(a[u][0], a[u][1], a[u][2], a[u][3], z0 + zoh[kk + u]);
+                  f[u] = gt[4 * (kk + u)];
+                }
+#pragma unroll
+              for (int u = 0; u < BS; ++u)
+                if (kk + u < kst) {
+                  mma_bf16_16816((u & 1) ? sb : sa, a[u][0], a[u][1], a[u][2], a[u][3], f[u].x, f[u].z);
+                  mma_bf16_16816((u & 1) ? lb : la, a[u][0], a[u][1], a[u][2], a[u][3], f[u].y, f[u].w);
+                }
+            }
+          } else {
           const uint2* pt = reinterpret_cast<const uint2*>(pqcur + 16 * dh * 2) + 4 * hf * r + q4;
-#pragma unroll 1
+#pragma unroll (PH ? MZA : 1)
           for (int kk = 0; kk < kst; kk += BS) {  // batches of BS steps (kst is even)
             uint32_t a[BS][4];
             uint2 f0[BS], f1[BS];
@@ -771,6 +826,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
                 mma_bf16_16816((u & 1) ? sb : sa, a[u][0], a[u][1], a[u][2], a[u][3], h0, h1);
                 mma_bf16_16816((u & 1) ? lb : la, a[u][0], a[u][1], a[u][2], a[u][3], l0, l1);
               }
+          }
           }
         }
 
@@ -805,7 +861,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
             acc_v[n][0] *= al[0]; acc_v[n][1] *= al[1]; acc_v[n][2] *= al[0]; acc_v[n][3] *= al[1];
           }
 #pragma unroll
-          for (int n = 0; n < MZA; ++n) {
+          for (int n = 0; n < NZV; ++n) {
             acc_z[n][0] *= al[0]; acc_z[n][1] *= al[1]; acc_z[n][2] *= al[0]; acc_z[n][3] *= al[1];
           }
         }
@@ -841,8 +897,28 @@ __global__ void __launch_bounds__(kThreadsS, 1)
                 mma_bf16_16816(acc_v[n0 + u], a[u][0], a[u][1], a[u][2], a[u][3], pb0, pb1);
             }
           }
-          // private values: O_z^T += Z_v^T P^T over this half's latent columns
-          if (MZMAX > 0) {
+          // private values, per head: O_z,h^T += Z_v,h^T P^T with P^T kept in
+          // column h only (this lane's column g)
+          if (PH) {
+            const unsigned char* zvb = zv + trow * zrow + tcol * 16;
+#pragma unroll
+            for (int h = 0; h < 8; ++h) {
+              const bool own = g == h;
+              const uint32_t b0 = own ? pb0 : 0u, b1 = own ? pb1 : 0u;
+              const unsigned char* zb = zvb + zhead[hb + h];
+              uint32_t a[NZH][4];
+#pragma unroll
+              for (int u = 0; u < NZH; ++u) ldsm_x4_trans(a[u][0], a[u][1], a[u][2], a[u][3], zb + 32 * u);
+#pragma unroll
+              for (int u = 0; u < NZH; ++u) {
+                if (M)
+                  mma_bf16_16816(acc_z[u], a[u][0] & k0, a[u][1] & k0, a[u][2] & k1, a[u][3] & k1, b0, b1);
+                else
+                  mma_bf16_16816(acc_z[u], a[u][0], a[u][1], a[u][2], a[u][3], b0, b1);
+              }
+            }
+          } else if (MZMAX > 0) {
+            // private values: O_z^T += Z_v^T P^T over this half's latent columns
             const unsigned char* z0 = zv + trow * zrow + tcol * 16;
             const int* zoh = zo + 32 * hf;
 #pragma unroll
@@ -855,10 +931,10 @@ __global__ void __launch_bounds__(kThreadsS, 1)
               for (int u = 0; u < BZ; ++u)
                 if (n0 + u < kst) {
                   if (M)
-                    mma_bf16_16816(acc_z[n0 + u], a[u][0] & k0, a[u][1] & k0, a[u][2] & k1, a[u][3] & k1, pb0,
-                                   pb1);
+                    mma_bf16_16816(acc_z[(n0 + u) % NZV], a[u][0] & k0, a[u][1] & k0, a[u][2] & k1, a[u][3] & k1,
+                                   pb0, pb1);
                   else
-                    mma_bf16_16816(acc_z[n0 + u], a[u][0], a[u][1], a[u][2], a[u][3], pb0, pb1);
+                    mma_bf16_16816(acc_z[(n0 + u) % NZV], a[u][0], a[u][1], a[u][2], a[u][3], pb0, pb1);
                 }
             }
           }
@@ -950,14 +1026,22 @@ __global__ void __launch_bounds__(kThreadsS, 1)
             o[16 * n + g] = acc_v[n][e];
             o[16 * n + g + 8] = acc_v[n][2 + e];
           }
-          if (MZMAX > 0) {
+          if (PH) {
+            // tile n, row g (+8) holds latent column 16 n + g (+8) of head hl
+#pragma unroll
+            for (int n = 0; n < NZH; ++n) {
+              const int ca = 16 * n + g, cb = ca + 8;
+              if (ca < r) o[dh + ca] = acc_z[n][e];
+              if (cb < r) o[dh + cb] = acc_z[n][2 + e];
+            }
+          } else if (MZMAX > 0) {
             // row j (this half) holds latent column j - (hl - hb) r of head hl
 #pragma unroll
             for (int n = 0; n < MZA; ++n) {
               if (n < kst) {
                 const int ca = 16 * n + g - (hl - hb) * r, cb = ca + 8;
-                if (ca >= 0 && ca < r) o[dh + ca] = acc_z[n][e];
-                if (cb >= 0 && cb < r) o[dh + cb] = acc_z[n][2 + e];
+                if (ca >= 0 && ca < r) o[dh + ca] = acc_z[n % NZV][e];
+                if (cb >= 0 && cb < r) o[dh + cb] = acc_z[n % NZV][2 + e];
               }
             }
           }
@@ -1081,12 +1165,19 @@ static lrkv_status stream_plan_impl(DecodePlan& P) {
   P.stage_bytes = round_up(2 * P.kv_bytes + 2 * P.zt_bytes, 1024);
   const int pf_bytes = 2 * (dh / 16) * 32 * 8;  // q fragments of both halves
 
-  // shared memory: barriers | prefix | p/q buffers | p fragments | ring
+  // the per-lane private-score fragment table: 16 rows (half, head) of kst
+  // steps x 4 x 16 bytes, padded by 64 bytes so that the two heads a
+  // quarter-warp reads sit in different banks
+  P.gt_stride = 64 * (P.kst + 1);
+  int gt_bytes = 0;
+
+  // shared memory: barriers | prefix | p/q buffers | q fragments | p fragment table | ring
   auto layout = [&](int stages) {
     int off = kHeaderBytes;  // barriers, stage records, step offsets, tile cursors
     P.off_prefix = off; off = round_up(off + (P.B + 1) * 4, 128);
     P.off_pq = off; off = round_up(off + 2 * P.pq_bytes, 128);
     P.off_pf = off; off = round_up(off + std::max(pf_bytes, 16), 1024);
+    P.off_gt = gt_bytes > 0 ? off : 0; off = round_up(off + gt_bytes, 1024);
     P.off_kv = off; off += stages * P.stage_bytes;
     return off + 1024;  // alignment slack
   };
@@ -1097,6 +1188,14 @@ static lrkv_status stream_plan_impl(DecodePlan& P) {
   while (stages < std::min(16, cap) && layout(stages + 1) <= budget) ++stages;
   if (stages < 2) return LRKV_ERR_UNSUPPORTED;
   P.stages = stages;
+  // the fragment table when it fits beside the same ring (LRKV_DECODE_GTAB=0:
+  // tuning, the compact p table with per-step selects)
+  {
+    const char* gt_env = std::getenv("LRKV_DECODE_GTAB");
+    const bool want = r > 0 && !((gt_env && *gt_env) && std::atoi(gt_env) == 0);
+    gt_bytes = 16 * P.gt_stride;
+    if (!want || layout(P.stages) > budget) gt_bytes = 0;
+  }
   P.smem_bytes = layout(P.stages);
   // B^K of a row tile staged through the last ring stages when it fits
   // (leaving at least one stage for the first tiles)
