@@ -79,11 +79,6 @@ struct DecodePlan {
   int zo[2][32];     // shared byte offset of 16-column latent step n of head half h2
   int pq_bytes;      // one p/q buffer: q rows [16][dh] bf16 then p rows [16][r] fp32
   int off_pq, off_pf, off_kv;
-  // per-lane private-score fragment table (0: not used, the compact p table
-  // and per-step selects instead): rows (half h2, head g) of gt_stride bytes,
-  // each [kst][4] uint4 {hi, lo of p at half columns j, j + 1, hi, lo at
-  // j + 8, j + 9}, j = 16 kk + 2 q4, zero where the column is not head g's
-  int off_gt, gt_stride;
   // workspace carve-up
   uint32_t* status;
   int* meta;         // [0] = total tokens N, [1] = CTAs used

@@ -360,14 +360,18 @@ __global__ void __launch_bounds__(kThreadsS, 1)
   constexpr int BZ = MZA > 16 ? 4 : 8;       // private-value steps per load batch
   constexpr int KB = DHT > 4 ? 4 : DHT;      // head-dim steps per load batch of the shared rows
   const int kst = EXACT ? MZA : P.kst;       // latent steps per warp (a constant when EXACT)
-  // Private values per head (ranks a multiple of 8, EXACT: r = 2 MZMAX):
-  // accumulator tile s holds latent columns 16 s .. 16 s + 15 of every head
-  // of the half (column h = head hb + h), each head's product masked to its
-  // own column; otherwise one tile per 16-column step of the half's 8 r
-  // latents, of which the diagonal blocks are kept.
-  constexpr bool PH = EXACT && MZMAX > 0 && (2 * MZMAX) % 8 == 0;
-  constexpr int NZH = PH ? (2 * MZMAX + 15) / 16 : 1;  // tiles per head (r / 16, rounded up)
-  constexpr int NZV = PH ? NZH : MZA;                  // private value accumulator tiles
+  // Private values by head group (EXACT: r = 2 MZMAX): a group is GH heads
+  // whose latents start on a 16-byte boundary (one head when r is a multiple
+  // of 8, else two); accumulator tile s holds the group's latent columns
+  // 16 s .. 16 s + 15 (column h = head hb + h), each group's product taking
+  // the probabilities of its own heads' columns only.  Entry (s, row, h) is
+  // latent 16 s + row - (h % GH) r of head h, or no latent (never written).
+  // Otherwise one tile per 16-column step of the half's 8 r latents, of
+  // which the diagonal blocks are kept.
+  constexpr bool PH = EXACT && MZMAX > 0;
+  constexpr int GH = (2 * MZMAX) % 8 == 0 ? 1 : 2;          // heads per value group
+  constexpr int NZH = PH ? (GH * 2 * MZMAX + 15) / 16 : 1;  // tiles per group
+  constexpr int NZV = PH ? NZH : MZA;                       // private value accumulator tiles
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ int s_timeout;
   __shared__ int s_nopage;  // a block table entry named no page of the pool
@@ -663,31 +667,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
         qf[e] = v;
       }
     }
-    if (MZMAX > 0 && P.off_gt > 0) {
-      // the per-lane fragment table: entry (h2, g, kk, q4) holds p of head
-      // 8 h2 + g at the half's latent columns j = 16 kk + 2 q4 (+1) and j + 8
-      // (+9) as bf16 hi and lo parts, where the column is that head's (its r
-      // columns start at g r), zero elsewhere and past H
-      const float* prow = reinterpret_cast<const float*>(pqb + 16 * dh * 2);
-      const int ne = 64 * kst;
-      for (int e = tid; e < (tid < nset ? ne : 0); e += nset) {
-        const int q4e = e & 3, kk = (e >> 2) % kst, row = (e >> 2) / kst;  // row = 8 h2 + g
-        const int gg = row & 7;
-        uint32_t w[4];
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const int j = 16 * kk + 2 * q4e + 8 * half;
-          float2 v = make_float2(0.f, 0.f);
-          if (j / r == gg && row < nh) v = *reinterpret_cast<const float2*>(prow + row * r + j - gg * r);
-          const float h0 = __bfloat162float(__float2bfloat16_rn(v.x));
-          const float h1 = __bfloat162float(__float2bfloat16_rn(v.y));
-          w[2 * half] = pack_bf16(h0, h1);
-          w[2 * half + 1] = pack_bf16(v.x - h0, v.y - h1);
-        }
-        *reinterpret_cast<uint4*>(smem + P.off_gt + row * P.gt_stride + kk * 64 + q4e * 16) =
-            make_uint4(w[0], w[1], w[2], w[3]);
-      }
-    } else if (MZMAX > 0) {
+    if (MZMAX > 0) {
       // p of the row tile's heads as bf16 high and low parts, head-major in
       // pairs of latent columns: entry e = hl r/2 + c/2 holds
       // {hi(p[c]), hi(p[c+1])}, {lo(p[c]), lo(p[c+1])} (zero past H), written
@@ -784,29 +764,10 @@ __global__ void __launch_bounds__(kThreadsS, 1)
           // (bit kk of vmask0 / vmask1) and zero elsewhere (block diagonal)
           const unsigned char* z0 = zk + arow * zrow + ahalf * 16;
           const int* zoh = zo + 32 * hf;
-          if (P.off_gt > 0) {
-            // this lane's fragments, already zero off its head's columns
-            const uint4* gt = reinterpret_cast<const uint4*>(smem + P.off_gt + (hb + g) * P.gt_stride) + q4;
-#pragma unroll (PH ? MZA : 1)
-            for (int kk = 0; kk < kst; kk += BS) {
-              uint32_t a[BS][4];
-              uint4 f[BS];
-#pragma unroll
-              for (int u = 0; u < BS; ++u)
-                if (kk + u < kst) {
-                  ldsm_x4(a[u][0], a[u][1], a[u][2], a[u][3], z0 + zoh[kk + u]);
-                  f[u] = gt[4 * (kk + u)];
-                }
-#pragma unroll
-              for (int u = 0; u < BS; ++u)
-                if (kk + u < kst) {
-                  mma_bf16_16816((u & 1) ? sb : sa, a[u][0], a[u][1], a[u][2], a[u][3], f[u].x, f[u].z);
-                  mma_bf16_16816((u & 1) ? lb : la, a[u][0], a[u][1], a[u][2], a[u][3], f[u].y, f[u].w);
-                }
-            }
-          } else {
           const uint2* pt = reinterpret_cast<const uint2*>(pqcur + 16 * dh * 2) + 4 * hf * r + q4;
-#pragma unroll (PH ? MZA : 1)
+          // (6 batches unrolled with the per-group values: measured faster than none
+          // or all of them, which runs out of registers)
+#pragma unroll (PH ? 6 : 1)
           for (int kk = 0; kk < kst; kk += BS) {  // batches of BS steps (kst is even)
             uint32_t a[BS][4];
             uint2 f0[BS], f1[BS];
@@ -826,7 +787,6 @@ __global__ void __launch_bounds__(kThreadsS, 1)
                 mma_bf16_16816((u & 1) ? sb : sa, a[u][0], a[u][1], a[u][2], a[u][3], h0, h1);
                 mma_bf16_16816((u & 1) ? lb : la, a[u][0], a[u][1], a[u][2], a[u][3], l0, l1);
               }
-          }
           }
         }
 
@@ -897,13 +857,13 @@ __global__ void __launch_bounds__(kThreadsS, 1)
                 mma_bf16_16816(acc_v[n0 + u], a[u][0], a[u][1], a[u][2], a[u][3], pb0, pb1);
             }
           }
-          // private values, per head: O_z,h^T += Z_v,h^T P^T with P^T kept in
-          // column h only (this lane's column g)
+          // private values, per head group: O_z,grp^T += Z_v,grp^T P^T with
+          // P^T kept in the group's columns only (this lane's column g)
           if (PH) {
             const unsigned char* zvb = zv + trow * zrow + tcol * 16;
 #pragma unroll
-            for (int h = 0; h < 8; ++h) {
-              const bool own = g == h;
+            for (int h = 0; h < 8; h += GH) {
+              const bool own = g / GH == h / GH;
               const uint32_t b0 = own ? pb0 : 0u, b1 = own ? pb1 : 0u;
               const unsigned char* zb = zvb + zhead[hb + h];
               uint32_t a[NZH][4];
@@ -1027,12 +987,13 @@ __global__ void __launch_bounds__(kThreadsS, 1)
             o[16 * n + g + 8] = acc_v[n][2 + e];
           }
           if (PH) {
-            // tile n, row g (+8) holds latent column 16 n + g (+8) of head hl
+            // tile n, row g (+8) holds latent 16 n + g (+8) - (hl % GH) r of head hl
+            const int c0 = ((hl - hb) % GH) * r;
 #pragma unroll
             for (int n = 0; n < NZH; ++n) {
-              const int ca = 16 * n + g, cb = ca + 8;
-              if (ca < r) o[dh + ca] = acc_z[n][e];
-              if (cb < r) o[dh + cb] = acc_z[n][2 + e];
+              const int ca = 16 * n + g - c0, cb = ca + 8;
+              if (ca >= 0 && ca < r) o[dh + ca] = acc_z[n][e];
+              if (cb >= 0 && cb < r) o[dh + cb] = acc_z[n][2 + e];
             }
           } else if (MZMAX > 0) {
             // row j (this half) holds latent column j - (hl - hb) r of head hl
@@ -1165,19 +1126,12 @@ static lrkv_status stream_plan_impl(DecodePlan& P) {
   P.stage_bytes = round_up(2 * P.kv_bytes + 2 * P.zt_bytes, 1024);
   const int pf_bytes = 2 * (dh / 16) * 32 * 8;  // q fragments of both halves
 
-  // the per-lane private-score fragment table: 16 rows (half, head) of kst
-  // steps x 4 x 16 bytes, padded by 64 bytes so that the two heads a
-  // quarter-warp reads sit in different banks
-  P.gt_stride = 64 * (P.kst + 1);
-  int gt_bytes = 0;
-
-  // shared memory: barriers | prefix | p/q buffers | q fragments | p fragment table | ring
+  // shared memory: barriers | prefix | p/q buffers | q fragments | ring
   auto layout = [&](int stages) {
     int off = kHeaderBytes;  // barriers, stage records, step offsets, tile cursors
     P.off_prefix = off; off = round_up(off + (P.B + 1) * 4, 128);
     P.off_pq = off; off = round_up(off + 2 * P.pq_bytes, 128);
     P.off_pf = off; off = round_up(off + std::max(pf_bytes, 16), 1024);
-    P.off_gt = gt_bytes > 0 ? off : 0; off = round_up(off + gt_bytes, 1024);
     P.off_kv = off; off += stages * P.stage_bytes;
     return off + 1024;  // alignment slack
   };
@@ -1188,14 +1142,6 @@ static lrkv_status stream_plan_impl(DecodePlan& P) {
   while (stages < std::min(16, cap) && layout(stages + 1) <= budget) ++stages;
   if (stages < 2) return LRKV_ERR_UNSUPPORTED;
   P.stages = stages;
-  // the fragment table when it fits beside the same ring (LRKV_DECODE_GTAB=0:
-  // tuning, the compact p table with per-step selects)
-  {
-    const char* gt_env = std::getenv("LRKV_DECODE_GTAB");
-    const bool want = r > 0 && !((gt_env && *gt_env) && std::atoi(gt_env) == 0);
-    gt_bytes = 16 * P.gt_stride;
-    if (!want || layout(P.stages) > budget) gt_bytes = 0;
-  }
   P.smem_bytes = layout(P.stages);
   // B^K of a row tile staged through the last ring stages when it fits
   // (leaving at least one stage for the first tiles)
