@@ -70,6 +70,7 @@ def _args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-legs", action="store_true", help="headline decode only (no e2e, no other legs)")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the length x concurrency sweep")
     ap.add_argument("--max-len", type=int, default=None,
                     help="rows per sequence of the headline workload (a smaller copy of its recipe)")
     return ap.parse_args()
@@ -510,6 +511,126 @@ class DecodeSetup:
             raise lrkv.LRKVError(st, "lrkv_decode_profiled")
 
 
+def call_latency_us(step, n_rep, stream, n=200, use_graph=True):
+    """Per-call latency: each call's own CUDA-event interval (one decode per
+    graph replay, cycled over the cache replicas so that every call reads a
+    cold cache), after warm replays.  Percentiles in microseconds."""
+    import torch
+    graphs = []
+    if use_graph:
+        try:
+            for i in range(n_rep):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+                    step(i, torch.cuda.current_stream())
+                graphs.append(g)
+            torch.cuda.synchronize()
+        except Exception as e:
+            print(f"latency graph capture failed ({e}); eager calls", file=sys.stderr)
+            graphs = []
+            torch.cuda.synchronize()
+
+    def one(i):
+        if graphs:
+            graphs[i % len(graphs)].replay()
+        else:
+            step(i, stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(20, 2 * n_rep)):
+            one(i)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    with torch.cuda.stream(stream):
+        for i in range(n):
+            evs[i][0].record(stream)
+            one(i)
+            evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    t = sorted(e0.elapsed_time(e1) * 1e3 for e0, e1 in evs)
+
+    def pct(p):
+        return t[min(len(t) - 1, int(round(p / 100.0 * (len(t) - 1))))]
+
+    return {"p50": pct(50), "p90": pct(90), "p99": pct(99), "min": t[0], "max": t[-1], "n": n,
+            "timing": "CUDA events around each call (graph replay of one call, " +
+                      ("graph" if graphs else "eager") + "), calls back to back"}
+
+
+# The length x concurrency grid of the sweep (the headline's head shape): the
+# points the pages' evaluation design asks for on both sides of the
+# bandwidth/compute and latency/throughput transitions, up to 2^20 cached rows.
+SWEEP_BATCH = (1, 4, 16, 64)
+SWEEP_LEN = (1024, 4096, 16384, 65536)
+SWEEP_MAX_ROWS = 1 << 20
+
+
+class SweepSetup:
+    """A decode point of the sweep on device-generated inputs (the headline's
+    recipe: cache entries and q ~ N(0,1), B ~ N(0,1/r)); rotating cache
+    replicas while the cache is small enough to stay in L2."""
+
+    def __init__(self, w, B, L, dev, seed):
+        import dataclasses
+        import torch
+        from compressed_cache_decode_gb300 import lrkv
+        self.w = dataclasses.replace(w, name=f"{w.name}@B{B}xL{L}", batch=B, max_len=L, ragged=None,
+                                     outlier_frac=0.0)
+        H, dh, r = w.heads, w.head_dim, w.rank
+        g = torch.Generator(device=dev).manual_seed(1000 + seed)
+        bf = torch.bfloat16
+
+        def nrm(*shape, std=1.0):
+            return (torch.randn(*shape, generator=g, device=dev) * std).to(bf)
+
+        self.seq_lens = torch.full((B,), L, dtype=torch.int32, device=dev)
+        self.q, self.b_k, self.b_v = nrm(B, H, dh), nrm(H, dh, r, std=r ** -0.5), nrm(H, dh, r, std=r ** -0.5)
+        self.total_bytes, self.split_bytes, cache_alg = decode_bytes(self.w, self.seq_lens.cpu())
+        self.n_rep = 1 if cache_alg >= 4 * L2_BYTES else min(16, max(2, math.ceil(4 * L2_BYTES / cache_alg)))
+        self.caches = [(nrm(B, L, dh), nrm(B, L, dh), nrm(B, L, H, r), nrm(B, L, H, r)) for _ in range(self.n_rep)]
+        self.dims = lrkv.make_dims(B, H, dh, r, L, bf)
+        self.ws = lrkv.decode_workspace(self.dims, dev)
+        self.out = torch.empty((B, H, dh), dtype=torch.float32, device=dev)
+        self.lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+
+    def step(self, i, s):
+        from compressed_cache_decode_gb300 import lrkv
+        k_s, v_s, z_k, z_v = self.caches[i % self.n_rep]
+        st = lrkv.lrkv_decode(self.dims, self.q, k_s, v_s, z_k, z_v, self.b_k, self.b_v, self.seq_lens, self.out,
+                              self.lse, self.ws, self.ws.numel(), s)
+        if st != lrkv.LRKV_OK:
+            raise lrkv.LRKVError(st, "lrkv_decode")
+
+
+def sweep_leg(w, K, W, stream, use_graph, peak, world, dev, seed):
+    """Length x concurrency sweep of the decode (the headline's head shape):
+    per point the step rate, its HBM fraction, tokens/s and the per-call
+    latency quantiles."""
+    import torch
+    points = []
+    for B in SWEEP_BATCH:
+        for L in SWEEP_LEN:
+            if B * L > SWEEP_MAX_ROWS:
+                continue
+            sp = SweepSetup(w, B, L, dev, seed)
+            t = StepTimer(sp.step, K, W, stream, use_graph)
+            t.warm(ms=50)
+            ms = max_over_ranks(_spread(t.time(repeats=5))["median"], world, dev)
+            del t
+            lat = call_latency_us(sp.step, sp.n_rep, stream, n=100, use_graph=use_graph)
+            points.append({"batch": B, "seq_len": L, "ms_per_step": ms,
+                           "gbs": job_gbs(sp.total_bytes, world, ms),
+                           "hbm_frac": sp.total_bytes / (ms * 1e-3) / 1e9 / peak,
+                           "tokens_per_s": B * world / (ms * 1e-3), "bytes_per_step": sp.total_bytes,
+                           "cache_replicas": sp.n_rep,
+                           "latency_us": {k: v for k, v in lat.items() if k != "timing"}})
+            del sp
+            torch.cuda.empty_cache()
+    return {"heads": w.heads, "head_dim": w.head_dim, "rank": w.rank, "data": "synthetic, generated on the device",
+            "timing": f"median of 5 timed regions of {K} steps per point; latency: CUDA events around each of "
+                      "100 back-to-back calls (graph replays)", "points": points}
+
+
 def scan_kernel_name(w):
     return "lrkv_decode_stream_kernel" if w.dtype == "bf16" else "lrkv_decode_split_kernel"
 
@@ -525,7 +646,9 @@ def decode_leg(setup, K, W, stream, use_graph, peak, world, dev, repeats=7, min_
     ms_step = max_over_ranks(sp["median"], world, dev)
     iso, iso_min, iso_max, kind = scan_launch_ms(setup.profiled, min(K, 20), stream, use_graph)
     achieved = setup.split_bytes / (iso * 1e-3) / 1e9
+    lat = call_latency_us(setup.step, setup.n_rep, stream, n=200, use_graph=use_graph)
     return {
+        "latency_us": lat,
         "workload": w.name, "ms_per_step": ms_step, "ms_per_step_spread": sp,
         "gbs": job_gbs(setup.total_bytes, world, ms_step), "hbm_frac": setup.total_bytes / (ms_step * 1e-3) / 1e9 / peak,
         "tokens_per_s": w.batch * world / (ms_step * 1e-3), "bytes_per_step": setup.total_bytes,
@@ -977,6 +1100,7 @@ def main():
     ms_step = max_over_ranks(spread["median"], world, dev)
     iso, iso_min, iso_max, iso_kind = scan_launch_ms(head.profiled, min(K, 20), stream, use_graph)
     del timer
+    latency = call_latency_us(head.step, head.n_rep, stream, n=200, use_graph=use_graph)
 
     e2e = e2e_leg(head, K, stream, use_graph, world, dev) if not a.no_legs else None
     normed_leg = decode_normed_leg(head, K, W, stream, use_graph, world, dev, ms_step) if not a.no_legs else None
@@ -1000,6 +1124,10 @@ def main():
             del s
             torch.cuda.empty_cache()
 
+    sweep = None
+    if not a.no_legs and not a.no_sweep:
+        sweep = sweep_leg(w, K, W, stream, use_graph, peak, world, dev, seed=rank)
+
     prefill = None
     if not a.no_prefill:
         prefill = prefill_leg(dev)
@@ -1014,7 +1142,8 @@ def main():
         traffic = _profile_traffic(w.name, _src_sha())
         res = {
             "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
-            "ms_per_step": ms_step, "ms_per_step_spread": spread, "higher_is_better": True, "scaling": "weak",
+            "ms_per_step": ms_step, "ms_per_step_spread": spread, "latency_us": latency,
+            "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "accumulate": "f32", "data": "synthetic",
             "tokens_per_s": w.batch * world / (ms_step * 1e-3),
             "hbm_frac": gbs / world / peak,
@@ -1045,6 +1174,7 @@ def main():
             "decode_paged": paged_leg,
             "decode_rope": rope_leg,
             "compare": cmp_leg,
+            "sweep": sweep,
             "prefill": prefill,
         }
         print(json.dumps(res), flush=True)

@@ -194,7 +194,9 @@ lrkv_status step_append_launch(const lrkv_dims& dm, int d_model, const void* x, 
   p.z_k = static_cast<__nv_bfloat16*>(z_k); p.z_v = static_cast<__nv_bfloat16*>(z_v);
   const int smem = static_cast<int>((p.bc + (p.wstage ? kStepWarps : 0)) * row_bytes);
   auto kern = M == 8 ? lrkv_append_token_kernel<8> : lrkv_append_token_kernel<16>;
-  if (ensure_kernel_smem(reinterpret_cast<const void*>(kern), smem) != cudaSuccess) return LRKV_ERR_CUDA;
+  // the largest shared-memory carveout, as the scan after it asks for (no
+  // reconfiguration of the SMs between the two launches)
+  if (ensure_kernel_smem(reinterpret_cast<const void*>(kern), smem, true) != cudaSuccess) return LRKV_ERR_CUDA;
   // one warp per output column, at most one CTA per SM
   const long long N = 2ll * dm.head_dim + 2ll * dm.heads * dm.rank;
   const long long wpc = kStepWarps;

@@ -399,6 +399,9 @@ __global__ void __launch_bounds__(kThreadsS, 1)
   uint2* qf = reinterpret_cast<uint2*>(smem + P.off_pf);    // shared-score B fragments (q)
 
   // ---- 1. barriers, sequence starts (clamped lengths) ----------------------
+  // the first lengths are read before anything else (their latency is the
+  // start of the chain to the first tile)
+  const int len0 = tid < B ? P.seq_lens[tid] : 0;
   {
     // one read per 64-byte line of the launch plan, all at once, so that the
     // later dependent reads of its fields hit the constant cache
@@ -428,12 +431,22 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     mbar_init(&pbar[1], 1);
     mbar_init(reinterpret_cast<uint64_t*>(smem + 272), 1);
     fence_barrier_init();
+    // with bk_stages > 0 the row tile's B^K lands in the last bk_stages ring
+    // stages (one bulk copy, issued first: it depends on nothing) and those
+    // stages get their tiles once the first two pieces are absorbed
+    if (P.bk_stages > 0) {
+      const uint32_t bytes = static_cast<uint32_t>(min(16, H - m0) * dh * r * 2);
+      uint64_t* bkb = reinterpret_cast<uint64_t*>(smem + 272);
+      mbar_arrive_expect_tx(bkb, bytes);
+      tma_load_1d(smem + P.off_kv + static_cast<size_t>(P.stages - P.bk_stages) * P.stage_bytes,
+                  static_cast<const __nv_bfloat16*>(P.b_k) + static_cast<size_t>(m0) * dh * r, bytes, bkb);
+    }
   }
   if (tid < 64) zo[tid] = P.zo[tid >> 5][tid & 31];
   if (PH && tid < 16) zhead[tid] = (tid / P.hs) * kT * P.segp * 2 + (tid % P.hs) * r * 2;
   int bad = 0;
   for (int b = tid; b < B; b += blockDim.x) {
-    int L = P.seq_lens[b];
+    int L = b == tid ? len0 : P.seq_lens[b];
     if (L < 0 || L > P.max_len) {
       bad = 1;
       L = min(max(L, 0), P.max_len);
@@ -467,7 +480,11 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       for (int b = tid; b <= B; b += blockDim.x) P.prefix[b] = pre[b];
       if (tid == 0) { P.meta[0] = N; P.meta[1] = G; }
     }
-    if (tid == 0) *cta_status = bad ? kDevBounds : 0u;
+    if (tid == 0) {
+      // the B^K copy must land before the block's shared memory is released
+      const bool drained = P.bk_stages == 0 || mbar_wait_bounded(reinterpret_cast<uint64_t*>(smem + 272), 0u);
+      *cta_status = (bad ? kDevBounds : 0u) | (drained ? 0u : kDevTimeout);
+    }
     return;
   }
   const int c = blockIdx.x;
@@ -485,20 +502,11 @@ __global__ void __launch_bounds__(kThreadsS, 1)
   bool more = piece_first(pc, pre, B, g0, g1, P.block_table != nullptr);
   Piece pc1 = pc;
   const bool two = piece_next(pc1, pre, B, g1);
-  // with bk_stages > 0 the row tile's B^K lands in the last bk_stages ring
-  // stages (one bulk copy, ahead of the tiles) and those stages get their
-  // tiles once the first two pieces are absorbed
-  uint64_t* bkbar = reinterpret_cast<uint64_t*>(smem + 272);
+  uint64_t* bkbar = reinterpret_cast<uint64_t*>(smem + 272);  // the B^K copy (issued at entry)
   const int first_burst = P.stages - P.bk_stages;
   if (tid == 0) {
     q_issue(P, smem, pbar, 0, pc.b, m0, 0);
     if (two) q_issue(P, smem, pbar, 1, pc1.b, m0, 1);
-    if (P.bk_stages > 0) {
-      const uint32_t bytes = static_cast<uint32_t>(min(16, H - m0) * dh * r * 2);
-      mbar_arrive_expect_tx(bkbar, bytes);
-      tma_load_1d(smem + P.off_kv + static_cast<size_t>(first_burst) * P.stage_bytes,
-                  static_cast<const __nv_bfloat16*>(P.b_k) + static_cast<size_t>(m0) * dh * r, bytes, bkbar);
-    }
   }
   if (lane == 0) {
     TileCursor cur;
