@@ -46,9 +46,10 @@ namespace lrkv {
 using namespace dec;
 
 lrkv_status stream_plan(DecodePlan& P);
-lrkv_status stream_prepare(const DecodePlan& P, CUtensorMap* tm_zk, CUtensorMap* tm_zv);
+lrkv_status stream_prepare(const DecodePlan& P, CUtensorMap* tm_zk, CUtensorMap* tm_zv, CUtensorMap* tm_ks);
 lrkv_status stream_launch(const DecodePlan& P, cudaStream_t stream, bool pdl, const CUtensorMap& tm_k,
-                          const CUtensorMap& tm_v, const CUtensorMap& tm_zk, const CUtensorMap& tm_zv);
+                          const CUtensorMap& tm_v, const CUtensorMap& tm_zk, const CUtensorMap& tm_zv,
+                          const CUtensorMap& tm_ks);
 
 namespace {
 
@@ -940,7 +941,8 @@ template <bool BF16>
 // scan kernel alone.
 lrkv_status launch_all(const DecodePlan& P, cudaStream_t stream, cudaEvent_t ev_begin, cudaEvent_t ev_end) {
   const bool pdl = ev_begin == nullptr && ev_end == nullptr;
-  CUtensorMap tm_k, tm_v, tm_zk, tm_zv;
+  CUtensorMap tm_k, tm_v, tm_zk, tm_zv, tm_ks;
+  std::memset(&tm_ks, 0, sizeof(tm_ks));
   std::memset(&tm_k, 0, sizeof(tm_k));
   std::memset(&tm_v, 0, sizeof(tm_v));
   std::memset(&tm_zk, 0, sizeof(tm_zk));
@@ -955,7 +957,7 @@ lrkv_status launch_all(const DecodePlan& P, cudaStream_t stream, cudaEvent_t ev_
   }
   const SplitFn split = P.stream ? nullptr : split_fn(P);
   if (P.stream) {
-    const lrkv_status st = stream_prepare(P, &tm_zk, &tm_zv);
+    const lrkv_status st = stream_prepare(P, &tm_zk, &tm_zv, &tm_ks);
     if (st != LRKV_OK) return st;
   } else if (cudaFuncSetAttribute(split, cudaFuncAttributeMaxDynamicSharedMemorySize, P.smem_bytes) != cudaSuccess) {
     return LRKV_ERR_CUDA;
@@ -988,7 +990,7 @@ lrkv_status launch_all(const DecodePlan& P, cudaStream_t stream, cudaEvent_t ev_
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   if (P.stream) {
-    const lrkv_status st = stream_launch(P, stream, pdl, tm_k, tm_v, tm_zk, tm_zv);
+    const lrkv_status st = stream_launch(P, stream, pdl, tm_k, tm_v, tm_zk, tm_zv, tm_ks);
     if (st != LRKV_OK) return st;
   } else {
     cudaLaunchConfig_t cfg = {};
@@ -1107,7 +1109,11 @@ lrkv_status decode_make_plan(const lrkv_dims& d, int num_sms, DecodePlan& P, siz
   // gets one warp per (sequence, head) on as many SMs as that needs.
   const long long cap_bytes = static_cast<long long>(P.B) * P.max_len * per_token;
   const bool large = P.bf16 && cap_bytes >= kLargeCacheBytes;
-  const int reserve = large ? 0 : static_cast<int>(std::min<long long>(pair_ctas, kCombineCtas));
+  // More (sequence, head) pairs than the narrow merge's warps on its SMs:
+  // the scan takes every SM and the merge runs wide after it (measured on
+  // 16 x 1K rows of 32 heads: the narrow merge took 62 us for 512 pairs).
+  const bool many_pairs = static_cast<long long>(P.B) * H > static_cast<long long>(kCombineWarps) * kCombineCtas;
+  const int reserve = (large || many_pairs) ? 0 : static_cast<int>(std::min<long long>(pair_ctas, kCombineCtas));
   P.grid = env_int("LRKV_DECODE_GRID", std::max(1, num_sms - reserve));
   // the streaming kernel's grid is (range CTAs, row tiles of 16 heads): it
   // divides P.grid by the row tiles
@@ -1118,12 +1124,11 @@ lrkv_status decode_make_plan(const lrkv_dims& d, int num_sms, DecodePlan& P, siz
   // (A small cache keeps one warp per (sequence, head) on the `reserve` SMs
   // the scan leaves free: measured on 8 x 4K rows, the wide merge there made
   // a chain of dependent decode steps 11% slower.)
-  P.wide_merge = P.stream ? env_int("LRKV_DECODE_WIDE_MERGE", large ? 1 : 0) : 0;
+  P.wide_merge = P.stream ? env_int("LRKV_DECODE_WIDE_MERGE", (large || many_pairs) ? 1 : 0) : 0;
   if (P.wide_merge)
-    P.combine_ctas = static_cast<int>(
-        std::min<long long>(static_cast<long long>(P.B) * H, 4ll * (large ? num_sms : std::max(reserve, 1))));
+    P.combine_ctas = static_cast<int>(std::min<long long>(static_cast<long long>(P.B) * H, 4ll * num_sms));
   else
-    P.combine_ctas = (P.stream && !large) ? std::max(reserve, 1)
+    P.combine_ctas = (P.stream && !large && !many_pairs) ? std::max(reserve, 1)
                                           : static_cast<int>(std::min<long long>(pair_ctas, large ? num_sms : 65535));
   P.min_tokens = env_int("LRKV_DECODE_MIN_TOKENS", P.stream ? 8 * P.T : 2 * P.T);
   if (P.stream) {

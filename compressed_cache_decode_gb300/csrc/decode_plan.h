@@ -78,6 +78,11 @@ struct DecodePlan {
   int bk_head_bytes; // shared bytes per head of the staged B^K (padded)
   int zo[2][32];     // shared byte offset of 16-column latent step n of head half h2
   int pq_bytes;      // one p/q buffer: q rows [16][dh] bf16 then p rows [16][r] fp32
+  // key scales of a post-projection RMSNorm decode staged with each tile: a
+  // [16 heads][kKsBoxT tokens] fp32 box at stage offset off_ks (ks_bytes per
+  // stage, 0: no slot) from the row rounded down to a multiple of 4;
+  // ks_tma: 1 when the call stages them (else each lane loads its own)
+  int ks_bytes, off_ks, ks_tma;
   int off_pq, off_pf, off_kv;
   // workspace carve-up
   uint32_t* status;

@@ -63,6 +63,7 @@ constexpr float kRescaleLog2 = 8.f;          // raise the reference max only pas
 constexpr int kCursorOff = 640;              // shared bytes of the pairs' tile cursors (2 per pair)
 constexpr int kQLastOff = 896;               // [2] last piece whose q went into each p/q buffer
 constexpr int kHeaderBytes = 1024;           // barriers, stage records, step offsets, cursors
+constexpr int kKsBoxT = 20;                  // tokens per staged key-scale row (16 from a row 4-aligned below)
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -135,9 +136,9 @@ __device__ __forceinline__ bool cache_coords(const DecodePlan& P, int b, int t, 
 }
 
 __device__ __forceinline__ bool stream_issue(const DecodePlan& P, const CUtensorMap* tk, const CUtensorMap* tv,
-                                             const CUtensorMap* tzk, const CUtensorMap* tzv,
+                                             const CUtensorMap* tzk, const CUtensorMap* tzv, const CUtensorMap* tks,
                                              unsigned char* smem, uint64_t* full, int s, int b_log, int t_log,
-                                             int zseg0, const int* pre) {
+                                             int zseg0, int m0, const int* pre) {
   // In a decode step the launch before writes each sequence's newest row
   // (row L_b - 1): only a copy of the tile that holds it waits for that
   // launch; every other tile streams at once.
@@ -148,7 +149,11 @@ __device__ __forceinline__ bool stream_issue(const DecodePlan& P, const CUtensor
   unsigned char* vs = ks + P.kv_bytes;
   unsigned char* zk = vs + P.kv_bytes;
   unsigned char* zv = zk + P.zt_bytes;
-  mbar_arrive_expect_tx(&full[s], 2u * P.nbox * kT * 128u + 2u * static_cast<uint32_t>(P.zt_bytes));
+  mbar_arrive_expect_tx(&full[s], 2u * P.nbox * kT * 128u + 2u * static_cast<uint32_t>(P.zt_bytes) +
+                                       (P.ks_tma ? static_cast<uint32_t>(P.ks_bytes) : 0u));
+  // the key scales of the tile's 16 logical rows (from the row rounded down
+  // to a multiple of 4, the copy's alignment) and the row tile's 16 heads
+  if (P.ks_tma) tma_load_3d(ks + P.off_ks, tks, t_log & ~3, m0, b_log, &full[s]);
   for (int cb = 0; cb < P.nbox; ++cb) {
     tma_load_3d(ks + cb * kT * 128, tk, cb * 64, t0, b, &full[s]);
     tma_load_3d(vs + cb * kT * 128, tv, cb * 64, t0, b, &full[s]);
@@ -354,7 +359,7 @@ template <int DHT, int MZMAX, bool EXACT>
 __global__ void __launch_bounds__(kThreadsS, 1)
     lrkv_decode_stream_kernel(const __grid_constant__ DecodePlan P, const __grid_constant__ CUtensorMap tm_k,
                               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_zk,
-                              const __grid_constant__ CUtensorMap tm_zv) {
+                              const __grid_constant__ CUtensorMap tm_zv, const __grid_constant__ CUtensorMap tm_ks) {
   constexpr int MZA = MZMAX > 0 ? MZMAX : 1;
   constexpr int BS = MZA > 16 ? 2 : 4;       // private-score steps per load batch
   constexpr int BZ = MZA > 16 ? 4 : 8;       // private-value steps per load batch
@@ -418,6 +423,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       prefetch_tmap(&tm_zk);
       prefetch_tmap(&tm_zv);
     }
+    if (P.ks_tma) prefetch_tmap(&tm_ks);
     s_timeout = 0;
     s_nopage = 0;
     reinterpret_cast<int*>(smem + kQLastOff)[0] = -1;
@@ -514,8 +520,8 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     cur.more = more;
     cur.ibase = 0;
     for (int j = warp; j < first_burst && cur.seek(j, pre, B, g1); j += kWarps) {
-      if (!stream_issue(P, &tm_k, &tm_v, &tm_zk, &tm_zv, smem, full, j, cur.pc.b,
-                        cur.pc.t_beg + (j - cur.ibase) * kT, zseg0, pre))
+      if (!stream_issue(P, &tm_k, &tm_v, &tm_zk, &tm_zv, &tm_ks, smem, full, j, cur.pc.b,
+                        cur.pc.t_beg + (j - cur.ibase) * kT, zseg0, m0, pre))
         *reinterpret_cast<volatile int*>(&s_nopage) = 1;
       *reinterpret_cast<volatile int*>(&issued[j]) = j;
     }
@@ -577,8 +583,8 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       cur.more = more;
       cur.ibase = 0;
       for (int j = first_burst + warp; j < P.stages && cur.seek(j, pre, B, g1); j += P.bk_warps) {
-        if (!stream_issue(P, &tm_k, &tm_v, &tm_zk, &tm_zv, smem, full, j, cur.pc.b,
-                          cur.pc.t_beg + (j - cur.ibase) * kT, zseg0, pre))
+        if (!stream_issue(P, &tm_k, &tm_v, &tm_zk, &tm_zv, &tm_ks, smem, full, j, cur.pc.b,
+                          cur.pc.t_beg + (j - cur.ibase) * kT, zseg0, m0, pre))
           *reinterpret_cast<volatile int*>(&s_nopage) = 1;
         *reinterpret_cast<volatile int*>(&issued[j]) = j;
       }
@@ -736,7 +742,15 @@ __global__ void __launch_bounds__(kThreadsS, 1)
         // (token g / g+8, head hb + 2 q4 + e) multiplies its summed score;
         // loaded now, used after the score MMAs
         float ksc[4] = {1.f, 1.f, 1.f, 1.f};
-        if (P.key_scale) {
+        if (P.ks_tma) {
+          // from the stage: [16 heads][kKsBoxT rows from t0 & ~3] (rows and
+          // heads past the extents read as zeros, their scores are masked)
+          const float* kss = reinterpret_cast<const float*>(ks + P.off_ks) + (hb + 2 * q4) * kKsBoxT + (t0 & 3) + g;
+          ksc[0] = kss[0];
+          ksc[1] = kss[kKsBoxT];
+          ksc[2] = kss[8];
+          ksc[3] = kss[kKsBoxT + 8];
+        } else if (P.key_scale) {
           const int hl = m0 + hb + 2 * q4;
           const float* kp = P.key_scale + (static_cast<size_t>(pc.b) * H + hl) * P.max_len + t0;
           if (g < nvalid) {
@@ -927,8 +941,8 @@ __global__ void __launch_bounds__(kThreadsS, 1)
           if (rc.seek(j, pre, B, g1)) {
             fence_proxy_async_smem();
             if (ok && !*reinterpret_cast<volatile int*>(&s_timeout)) {
-              if (!stream_issue(P, &tm_k, &tm_v, &tm_zk, &tm_zv, smem, full, s, rc.pc.b,
-                                rc.pc.t_beg + (j - rc.ibase) * kT, zseg0, pre))
+              if (!stream_issue(P, &tm_k, &tm_v, &tm_zk, &tm_zv, &tm_ks, smem, full, s, rc.pc.b,
+                                rc.pc.t_beg + (j - rc.ibase) * kT, zseg0, m0, pre))
                 *reinterpret_cast<volatile int*>(&s_nopage) = 1;
               *reinterpret_cast<volatile int*>(&issued[s]) = j;
             }
@@ -1048,7 +1062,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
 namespace {
 
 using StreamFn = void (*)(const DecodePlan, const CUtensorMap, const CUtensorMap, const CUtensorMap,
-                          const CUtensorMap);
+                          const CUtensorMap, const CUtensorMap);
 
 // The latent steps a warp keeps accumulators for: exactly kst for the ranks
 // 28, 32, 48, 56 and 64 (loops without guards, accumulators sized exactly:
@@ -1132,6 +1146,11 @@ static lrkv_status stream_plan_impl(DecodePlan& P) {
   while (r > 0 && 16 * (r / 4) * P.bk_dsplit * 2 <= kThreadsS && P.bk_dsplit * 2 <= dh / 4) P.bk_dsplit *= 2;
   P.bk_warps = r > 0 ? (16 * (r / 4) * P.bk_dsplit + 31) / 32 : 1;
   P.stage_bytes = round_up(2 * P.kv_bytes + 2 * P.zt_bytes, 1024);
+  // the key-scale slot (post-projection RMSNorm decode) when the stages
+  // still fit as many of it (set below)
+  P.off_ks = 2 * P.kv_bytes + 2 * P.zt_bytes;  // 256-byte aligned
+  P.ks_bytes = 0;
+  P.ks_tma = 0;
   const int pf_bytes = 2 * (dh / 16) * 32 * 8;  // q fragments of both halves
 
   // shared memory: barriers | prefix | p/q buffers | q fragments | ring
@@ -1150,6 +1169,14 @@ static lrkv_status stream_plan_impl(DecodePlan& P) {
   while (stages < std::min(16, cap) && layout(stages + 1) <= budget) ++stages;
   if (stages < 2) return LRKV_ERR_UNSUPPORTED;
   P.stages = stages;
+  {
+    const int plain = P.stage_bytes;
+    P.stage_bytes = round_up(P.off_ks + 16 * kKsBoxT * 4, 1024);
+    if (layout(P.stages) <= budget)
+      P.ks_bytes = 16 * kKsBoxT * 4;
+    else
+      P.stage_bytes = plain;
+  }
   P.smem_bytes = layout(P.stages);
   // B^K of a row tile staged through the last ring stages when it fits
   // (leaving at least one stage for the first tiles)
@@ -1165,11 +1192,17 @@ static lrkv_status stream_plan_impl(DecodePlan& P) {
 
 // Host preparation of a streaming launch: the latent tensor maps and the
 // kernel's shared-memory attribute (set once per kernel and size).
-lrkv_status stream_prepare(const DecodePlan& P, CUtensorMap* tm_zk, CUtensorMap* tm_zv) {
+lrkv_status stream_prepare(const DecodePlan& P, CUtensorMap* tm_zk, CUtensorMap* tm_zv, CUtensorMap* tm_ks) {
   const StreamFn kern = stream_fn(P);
   if (!kern) return LRKV_ERR_UNSUPPORTED;
   std::memset(tm_zk, 0, sizeof(*tm_zk));
   std::memset(tm_zv, 0, sizeof(*tm_zv));
+  std::memset(tm_ks, 0, sizeof(*tm_ks));
+  // key scales [B][H][max_len] fp32 in boxes of [16 heads][kKsBoxT rows]
+  if (P.ks_tma &&
+      !make_tmap_3d_f32(tm_ks, P.key_scale, static_cast<uint64_t>(P.max_len), static_cast<uint64_t>(P.H),
+                        static_cast<uint64_t>(P.B), kKsBoxT, 16u))
+    return LRKV_ERR_CUDA;
   if (P.r > 0) {
     // z[b][t][h][c] viewed as [b][segment][t][hs r]: dims (inner first)
     // {hs r, rows, H / hs, sequences}, strides t: H r, segment: hs r, b: rows H r
@@ -1203,7 +1236,8 @@ lrkv_status stream_prepare(const DecodePlan& P, CUtensorMap* tm_zk, CUtensorMap*
 }
 
 lrkv_status stream_launch(const DecodePlan& P, cudaStream_t stream, bool pdl, const CUtensorMap& tm_k,
-                          const CUtensorMap& tm_v, const CUtensorMap& tm_zk, const CUtensorMap& tm_zv) {
+                          const CUtensorMap& tm_v, const CUtensorMap& tm_zk, const CUtensorMap& tm_zv,
+                          const CUtensorMap& tm_ks) {
   const StreamFn kern = stream_fn(P);
   if (!kern) return LRKV_ERR_UNSUPPORTED;
   cudaLaunchAttribute attr[1];
@@ -1216,7 +1250,7 @@ lrkv_status stream_launch(const DecodePlan& P, cudaStream_t stream, bool pdl, co
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, P, tm_k, tm_v, tm_zk, tm_zv) == cudaSuccess ? LRKV_OK : LRKV_ERR_CUDA;
+  return cudaLaunchKernelEx(&cfg, kern, P, tm_k, tm_v, tm_zk, tm_zv, tm_ks) == cudaSuccess ? LRKV_OK : LRKV_ERR_CUDA;
 }
 
 }  // namespace lrkv

@@ -128,6 +128,9 @@ lrkv_status decode_common(const lrkv_dims* dims, const void* q, const void* k_s,
   P.q = q; P.k_s = k_s; P.v_s = v_s; P.z_k = z_k; P.z_v = z_v; P.b_k = b_k; P.b_v = b_v;
   P.seq_lens = seq_lens; P.out = out; P.lse = lse;
   P.key_scale = key_scale;
+  // key scales staged with the tiles: a slot in the ring stages and rows of
+  // a multiple of 16 bytes (the copy's stride rule); else each lane loads its own
+  P.ks_tma = key_scale && P.ks_bytes > 0 && dims->max_len % 4 == 0 && aligned16(key_scale);
   return lrkv::decode_launch(P, stream, ev_begin, ev_end);
 }
 

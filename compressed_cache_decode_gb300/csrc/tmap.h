@@ -31,4 +31,10 @@ bool make_tmap_4d_bf16_swizzled(CUtensorMap* map, const void* base, const uint64
 // {b0, b1} (b0 may exceed d0: the excess is filled with zeros) and no swizzle.
 bool make_tmap_2d_f32(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint32_t b0, uint32_t b1);
 
+// Encode a 3-D tiled tensor map for a row-major [d2][d1][d0] fp32 tensor
+// (d0 * 4 a multiple of 16) with box {b0, b1, 1} and no swizzle; box elements
+// outside the extents are filled with zeros.
+bool make_tmap_3d_f32(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0,
+                      uint32_t b1);
+
 }  // namespace lrkv

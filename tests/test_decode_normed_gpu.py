@@ -52,6 +52,8 @@ def test_key_scales_match_oracle(shape):
     (2, 8, 128, 32, 300, [300, 129]),
     (4, 16, 64, 28, 4096, [4096, 3000, 17, 0]),
     (6, 18, 64, 8, 80, [1, 2, 3, 80, 79, 5]),     # several pieces per CTA, a partial row tile
+    (2, 32, 128, 48, 1024, [1024, 777]),          # two row tiles; scales staged with the tiles
+    (2, 16, 64, 28, 301, [301, 150]),             # max_len not a multiple of 4: per-lane scale loads
 ])
 def test_decode_normed_matches_oracle(shape):
     B, H, dh, r, Lm, lens = shape
