@@ -718,16 +718,31 @@ def prefill_leg(dev, iters=10):
     def kscales():
         lrkv.key_scales(k_s, z_k, d["b_k"], d["start_pos"], T, kscale, eps=1e-6)
 
-    res = {}
+    res, kinds = {}, {}
     for name, fn in (("append", app), ("prefill", pre), ("key_scales", kscales), ("prefill_normed", pre_normed)):
         for _ in range(3):
             fn()
+        torch.cuda.synchronize()
+        # each call captured once and replayed, so that the interval holds the
+        # kernel and not the host's argument marshalling and tensor-map set-up
+        run = fn
+        try:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, capture_error_mode="thread_local"):
+                fn()
+            torch.cuda.synchronize()
+            run = g.replay
+            kinds[name] = "graph"
+        except Exception as e:
+            print(f"prefill leg: graph capture of {name} failed ({e}); eager calls", file=sys.stderr)
+            torch.cuda.synchronize()
+            kinds[name] = "eager"
         ts = []
         for _ in range(iters):
             flush.zero_()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
-            fn()
+            run()
             e1.record()
             torch.cuda.synchronize()
             ts.append(e0.elapsed_time(e1))
@@ -751,7 +766,8 @@ def prefill_leg(dev, iters=10):
             "peak_tflops": peak[0], "peak_kind": peak[1],
             "attention_frac": attn / (ms["prefill"] * 1e-3) / 1e12 / peak[0],
             "append_frac": append / (ms["append"] * 1e-3) / 1e12 / peak[0],
-            "timing": f"CUDA events around each launch, L2 flushed before it, median of {iters}"}
+            "timing": f"CUDA events around each launch (replayed from a CUDA graph: "
+                      f"{', '.join(f'{k} {v}' for k, v in kinds.items())}), L2 flushed before it, median of {iters}"}
 
 
 # -------------------------------------------------------------------- legs

@@ -87,10 +87,6 @@ struct PrefillMaps {
   CUtensorMap bv;   // {r, dh, H}
 };
 
-__device__ __forceinline__ void mbar_arrive_cta(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
 // L2 prefetch of a 5-D tensor box (no destination, no completion)
 __device__ __forceinline__ void tma_prefetch_5d(const void* tmap, int x, int y, int z, int w, int v) {
   asm volatile("cp.async.bulk.prefetch.tensor.5d.L2.global.tile [%0, {%1, %2, %3, %4, %5}];" ::"l"(tmap), "r"(x),

@@ -27,8 +27,11 @@ def _lib():
     (2, 4, 64, 16, 200, [0, 37], 150, 1e-6),
     (1, 8, 128, 64, 130, [0], 130, 1e-3),     # two 64-token blocks + a ragged one
     (3, 16, 64, 28, 96, [5, 90, 0], 20, 0.0),  # rows past max_len skipped
+    (2, 36, 128, 48, 700, [0, 250], 512, 1e-6),  # rank padded to 64 by the copy, a partial head group
 ])
-def test_key_scales_match_oracle(shape):
+@pytest.mark.parametrize("tc", ["1", "0"])  # the tcgen05 form (where it applies) and the mma.sync form
+def test_key_scales_match_oracle(shape, tc, monkeypatch):
+    monkeypatch.setenv("LRKV_KEY_SCALE_TC", tc)
     B, H, dh, r, Lm, start, n_new, eps = shape
     case = inputs.random_decode_case(seed=B * 11 + dh, batch=B, heads=H, head_dim=dh, rank=r, max_len=Lm,
                                      dtype="bf16")
