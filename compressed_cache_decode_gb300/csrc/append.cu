@@ -9,11 +9,14 @@
 // N = 2 d_h + 2 H r, and the epilogue scatters each column range into its
 // cache tensor at row start_pos[b] + t of sequence b.
 //
-// Tile 128 x 256, K step 64 (one 128-byte swizzle atom of bf16).  Warp 0
-// issues TMA loads into a 4-stage ring, warp 1 issues the MMAs (one thread,
-// accumulator in 256 TMEM columns) and frees each stage with tcgen05.commit;
-// then all four warps read the accumulator back (tcgen05.ld), round to bf16
-// and store.
+// Tile 256 x 256, K step 64 (one 128-byte swizzle atom of bf16): two M = 128
+// MMAs per K step share the B tile, into two accumulators of 256 TMEM
+// columns each (all 512), so that a K step moves 64 KB of operands for
+// 256 x 256 outputs (a 128 x 256 tile moved 48 KB for half as many; it ran
+// the tensor pipe 56% busy, its 4-stage ring covering ~1.3 us of load
+// latency).  Warp 0 issues TMA loads into a 3-stage ring, warp 1 issues the
+// MMAs (one thread) and frees each stage with tcgen05.commit; then all four
+// warps read the accumulators back (tcgen05.ld), round to bf16 and store.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -27,8 +30,8 @@ namespace lrkv {
 
 namespace {
 
-constexpr int kBM = 128, kBN = 256, kBK = 64, kStages = 4;
-constexpr int kABytes = kBM * kBK * 2;   // 16 KB
+constexpr int kBM = 256, kBN = 256, kBK = 64, kStages = 3;
+constexpr int kABytes = kBM * kBK * 2;   // 32 KB (two 128-row halves)
 constexpr int kBBytes = kBN * kBK * 2;   // 32 KB
 constexpr int kSub = 64;                 // rows of one weight box
 constexpr uint32_t kStatusBounds = 2u;
@@ -78,7 +81,7 @@ __global__ void __launch_bounds__(128, 1)
     s_fail = 0;
     fence_barrier_init();
   }
-  if (warp == 0) tmem_alloc(&tmem_base, kBN);
+  if (warp == 0) tmem_alloc(&tmem_base, 2 * kBN);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -112,7 +115,7 @@ __global__ void __launch_bounds__(128, 1)
     }
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer ----------------------------------------------------------
-    constexpr uint32_t idesc = idesc_bf16(kBM, kBN, 0, 0);
+    constexpr uint32_t idesc = idesc_bf16(128, kBN, 0, 0);
     bool ok = true;
     for (int kb = 0; kb < kblocks && ok; ++kb) {
       const int s = kb % kStages;
@@ -125,9 +128,12 @@ __global__ void __launch_bounds__(128, 1)
       const uint32_t a0 = smem_u32(a_st + s * kABytes), b0 = smem_u32(b_st + s * kBBytes);
 #pragma unroll
       for (int kk = 0; kk < kBK / 16; ++kk) {
-        const uint64_t ad = smem_desc(a0 + kk * 32, 16, 1024, 2);
         const uint64_t bd = smem_desc(b0 + kk * 32, 16, 1024, 2);
-        tc_mma_ss(tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {  // rows 128 half .. 128 half + 127 into columns 256 half ..
+          const uint64_t ad = smem_desc(a0 + half * (128 * 128) + kk * 32, 16, 1024, 2);
+          tc_mma_ss(tmem + half * kBN, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+        }
       }
       tc_commit(&empty[s]);
     }
@@ -141,7 +147,8 @@ __global__ void __launch_bounds__(128, 1)
   if (!got || s_fail) {
     if (threadIdx.x == 0) atomicOr(p.status, 1u);
   } else {
-    const int m = m0 + warp * 32 + lane;  // this thread's output row
+    for (int half = 0; half < 2; ++half) {
+    const int m = m0 + half * 128 + warp * 32 + lane;  // this thread's output row
     size_t crow = 0;
     bool row_ok = m < p.M;
     if (row_ok) {
@@ -165,7 +172,7 @@ __global__ void __launch_bounds__(128, 1)
     for (int c = 0; c < kBN / 32; ++c) {
       const int n = n0 + c * 32;
       uint32_t v[32];
-      tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c * 32, v);
+      tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + half * kBN + c * 32, v);
       tmem_wait_ld();
       if (!row_ok || n >= p.N) continue;
       int seg = 0;
@@ -186,10 +193,11 @@ __global__ void __launch_bounds__(128, 1)
         dst[q] = w;
       }
     }
+    }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, kBN);
+  if (warp == 0) tmem_dealloc(tmem, 2 * kBN);
 }
 
 }  // namespace lrkv
@@ -247,7 +255,7 @@ static lrkv_status append_impl(const lrkv_dims* dims, int d_model, int n_new, co
 
   lrkv::AppendMaps maps;
   std::memset(&maps, 0, sizeof(maps));
-  if (!make_map_2d(&maps.x, x, d_model, p.M, 64, 128) ||
+  if (!make_map_2d(&maps.x, x, d_model, p.M, 64, lrkv::kBM) ||
       !make_map_2d(&maps.w[0], w_sk, d_model, d.head_dim, 64, 64) ||
       !make_map_2d(&maps.w[1], w_sv, d_model, d.head_dim, 64, 64))
     return LRKV_ERR_CUDA;
