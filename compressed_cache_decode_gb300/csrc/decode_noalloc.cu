@@ -12,8 +12,11 @@
 // The array lives in device memory of every GPU that loads the library and is
 // held until the process exits.  All calls on a device share it and it keeps
 // the previous call's contents; the decode kernels rewrite every byte they
-// read before reading it (the status word is cleared by the first kernel of
-// each call), so nothing has to be zeroed between calls.  Calls whose kernels
+// read before reading it, so nothing has to be zeroed between calls.  That
+// includes the status word at offset 0: on the fp32 path the absorb kernel
+// clears it; on the bf16 streaming path every scan CTA writes its own status
+// word on every launch and the merge kernel folds those words into the status
+// word.  lrkv_read_static_scratch_status reads it back.  Calls whose kernels
 // overlap on the GPU (different streams without ordering) race on the array.
 #include <cuda_runtime.h>
 
@@ -59,4 +62,12 @@ extern "C" lrkv_status lrkv_decode_static_scratch(const lrkv_dims* dims, const v
   if ((st = scratch_address(&ws)) != LRKV_OK) return st;
   return lrkv_decode(dims, q, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens, out, lse, ws,
                      static_cast<size_t>(LRKV_STATIC_SCRATCH_BYTES), stream);
+}
+
+extern "C" lrkv_status lrkv_read_static_scratch_status(lrkv_stream_t stream, lrkv_status* out_status) {
+  if (!out_status) return LRKV_ERR_INVALID_ARG;
+  void* ws = nullptr;
+  const lrkv_status st = scratch_address(&ws);
+  if (st != LRKV_OK) return st;
+  return lrkv_read_device_status(ws, stream, out_status);
 }

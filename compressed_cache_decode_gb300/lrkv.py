@@ -36,6 +36,7 @@ EXPORTED = (
     "lrkv_decode",
     "lrkv_decode_profiled",
     "lrkv_decode_static_scratch",
+    "lrkv_read_static_scratch_status",
     "lrkv_append",
     "lrkv_prefill",
     "lrkv_prefill_workspace_size",
@@ -165,6 +166,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.lrkv_mla_decode.argtypes = [mdp, vp, vp, vp, vp, i32p, vp, vp, vp, sz, vp]
     lib.lrkv_read_device_status.restype = ctypes.c_int
     lib.lrkv_read_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
+    lib.lrkv_read_static_scratch_status.restype = ctypes.c_int
+    lib.lrkv_read_static_scratch_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
     if path is None:
         _lib = lib
     return lib
@@ -238,6 +241,15 @@ def lrkv_decode_static_scratch(dims: lrkv_dims, q, k_s, v_s, z_k, z_v, b_k, b_v,
     return int(load().lrkv_decode_static_scratch(
         ctypes.byref(dims), _ptr(q), _ptr(k_s), _ptr(v_s), _ptr(z_k), _ptr(z_v), _ptr(b_k),
         _ptr(b_v), _ptr(seq_lens), _ptr(out), _ptr(lse), _stream_handle(stream)))
+
+
+def lrkv_read_static_scratch_status(stream=None) -> int:
+    """Status of the last lrkv_decode_static_scratch call on the current device."""
+    out = ctypes.c_int(0)
+    st = load().lrkv_read_static_scratch_status(_stream_handle(stream), ctypes.byref(out))
+    if st != LRKV_OK:
+        raise LRKVError(st, "lrkv_read_static_scratch_status")
+    return int(out.value)
 
 
 def lrkv_read_device_status(ws: torch.Tensor, stream=None) -> int:

@@ -179,12 +179,22 @@ lrkv_status lrkv_decode_profiled(const lrkv_dims* dims, const void* q, const voi
  *  * All calls on a device share the array and it keeps the last call's
  *    contents; nothing in it has to start at zero.  Calls whose kernels
  *    overlap on the GPU (unordered streams) race on it.
- *  * The device status word lives in that array and cannot be read back.
+ *  * The device status word lives at offset 0 of that array;
+ *    lrkv_read_static_scratch_status reads it back (the last call's).
  */
 lrkv_status lrkv_decode_static_scratch(const lrkv_dims* dims, const void* q, const void* k_s,
                                        const void* v_s, const void* z_k, const void* z_v,
                                        const void* b_k, const void* b_v, const int32_t* seq_lens,
                                        float* out, float* lse, lrkv_stream_t stream);
+
+/*
+ * The device status of the last lrkv_decode_static_scratch call on the
+ * current device, as lrkv_read_device_status reports a workspace's: waits
+ * for `stream` to drain, then sets *out_status to LRKV_OK,
+ * LRKV_ERR_DEVICE_BOUNDS or LRKV_ERR_TIMEOUT.  Returns LRKV_ERR_INVALID_ARG
+ * for a null out_status, LRKV_ERR_CUDA when the copy fails.  Allocates nothing.
+ */
+lrkv_status lrkv_read_static_scratch_status(lrkv_stream_t stream, lrkv_status* out_status);
 
 /*
  * Append new tokens to the factored cache ("Low-Rank Key Value Attention |
