@@ -23,6 +23,7 @@
 #include <cstring>
 
 #include "lrkv.h"
+#include "trace.h"
 #include "ptx.cuh"
 #include "tmap.h"
 
@@ -278,6 +279,7 @@ extern "C" lrkv_status lrkv_append(const lrkv_dims* dims, int d_model, int n_new
                                    const void* w_sk, const void* w_sv, const void* u_k, const void* u_v,
                                    const int32_t* start_pos, void* k_s, void* v_s, void* z_k, void* z_v,
                                    void* ws, size_t ws_bytes, lrkv_stream_t stream) {
+  LRKV_TRACE_CALL("lrkv_append");
   return append_impl(dims, d_model, n_new, x, w_sk, w_sv, u_k, u_v, start_pos, nullptr, 0, 0, k_s, v_s, z_k, z_v,
                      ws, ws_bytes, stream);
 }
@@ -287,6 +289,7 @@ extern "C" lrkv_status lrkv_append_paged(const lrkv_dims* dims, int d_model, int
                                          const int32_t* start_pos, int page_size, int num_pages,
                                          const int32_t* block_table, void* k_s, void* v_s, void* z_k, void* z_v,
                                          void* ws, size_t ws_bytes, lrkv_stream_t stream) {
+  LRKV_TRACE_CALL("lrkv_append_paged");
   if (!dims || !block_table) return LRKV_ERR_INVALID_ARG;
   if (page_size < 16 || (page_size & (page_size - 1)) != 0 || num_pages < 1) return LRKV_ERR_INVALID_ARG;
   if (dims->max_len % page_size != 0) return LRKV_ERR_INVALID_ARG;

@@ -23,6 +23,7 @@
 #include <mutex>
 
 #include "lrkv.h"
+#include "trace.h"
 
 namespace {
 
@@ -54,6 +55,7 @@ extern "C" lrkv_status lrkv_decode_static_scratch(const lrkv_dims* dims, const v
                                                   const void* v_s, const void* z_k, const void* z_v,
                                                   const void* b_k, const void* b_v, const int32_t* seq_lens,
                                                   float* out, float* lse, lrkv_stream_t stream) {
+  LRKV_TRACE_CALL("lrkv_decode_static_scratch");
   size_t need = 0;
   lrkv_status st = lrkv_decode_workspace_size(dims, &need);
   if (st != LRKV_OK) return st;

@@ -34,6 +34,7 @@
 #include "decode_plan.h"
 #include "host_cache.h"
 #include "lrkv.h"
+#include "trace.h"
 #include "ptx.cuh"
 #include "tmap.h"
 
@@ -451,6 +452,7 @@ bool a16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 extern "C" {
 
 lrkv_status lrkv_rope_table(int max_pos, int head_dim, float base, float* cos_sin, lrkv_stream_t stream) {
+  LRKV_TRACE_CALL("lrkv_rope_table");
   if (max_pos < 1 || head_dim < 2 || head_dim % 2 != 0 || !(base > 1.f) || !cos_sin) return LRKV_ERR_INVALID_ARG;
   const long long n = static_cast<long long>(max_pos) * (head_dim / 2);
   if (n > (1ll << 40)) return LRKV_ERR_UNSUPPORTED;
@@ -476,6 +478,7 @@ lrkv_status lrkv_decode_rope(const lrkv_dims* dims, const void* q_rot, const voi
                              const void* z_k, const void* z_v, const void* b_k, const void* b_v,
                              const float* cos_sin, int max_pos, const int32_t* seq_lens, float* out, float* lse,
                              void* ws, size_t ws_bytes, lrkv_stream_t stream) {
+  LRKV_TRACE_CALL("lrkv_decode_rope");
   lrkv_status st = lrkv::rope_check(dims);
   if (st != LRKV_OK) return st;
   if (!q_rot || !k_s || !v_s || !z_k || !z_v || !b_k || !b_v || !cos_sin || !seq_lens || !out)

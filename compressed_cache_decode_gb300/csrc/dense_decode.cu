@@ -29,6 +29,7 @@
 #include "decode_plan.h"
 #include "host_cache.h"
 #include "lrkv.h"
+#include "trace.h"
 #include "ptx.cuh"
 #include "tmap.h"
 
@@ -759,6 +760,7 @@ lrkv_status lrkv_dense_decode_workspace_size(const lrkv_dense_dims* dims, size_t
 lrkv_status lrkv_dense_decode(const lrkv_dense_dims* dims, const void* q, const void* k, const void* v,
                               const int32_t* seq_lens, float* out, float* lse, void* ws, size_t ws_bytes,
                               lrkv_stream_t stream) {
+  LRKV_TRACE_CALL("lrkv_dense_decode");
   lrkv_status st = lrkv::dense_check(dims);
   if (st != LRKV_OK) return st;
   if (!q || !k || !v || !seq_lens || !out) return LRKV_ERR_INVALID_ARG;
@@ -816,6 +818,7 @@ lrkv_status lrkv_mla_decode_workspace_size(const lrkv_mla_dims* dims, size_t* by
 lrkv_status lrkv_mla_decode(const lrkv_mla_dims* dims, const void* q, const void* c, const void* w_uk,
                             const void* w_uv, const int32_t* seq_lens, float* out, float* lse, void* ws,
                             size_t ws_bytes, lrkv_stream_t stream) {
+  LRKV_TRACE_CALL("lrkv_mla_decode");
   lrkv_status st = lrkv::mla_check(dims);
   if (st != LRKV_OK) return st;
   if (!q || !c || !w_uk || !w_uv || !seq_lens || !out) return LRKV_ERR_INVALID_ARG;

@@ -5,14 +5,22 @@
 
 #include <cuda_runtime.h>
 
+#include <cstdlib>
 #include <map>
 #include <mutex>
 #include <tuple>
 
 namespace lrkv {
 
-// SM count of the current device (0 on error).
+// SM count the launch plans are made for: LRKV_SM_COUNT when set to a
+// positive number (planning without a device, e.g. to size workspaces ahead
+// of time; any value gives correct results, the grids follow it), else the
+// current device's (0 on error).
 inline int device_sm_count() {
+  if (const char* env = std::getenv("LRKV_SM_COUNT")) {
+    const int n = std::atoi(env);
+    if (n > 0) return n;
+  }
   static std::mutex mu;
   static std::map<int, int> cache;
   int dev = 0;

@@ -5,7 +5,9 @@
 
 #include <cstdint>
 
+#include "host_cache.h"
 #include "lrkv.h"
+#include "trace.h"
 #include "decode_plan.h"
 
 namespace {
@@ -31,10 +33,8 @@ lrkv_status check_decode_dims(const lrkv_dims* d) {
 }
 
 lrkv_status current_sm_count(int* n) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return LRKV_ERR_CUDA;
-  if (cudaDeviceGetAttribute(n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return LRKV_ERR_CUDA;
-  return LRKV_OK;
+  *n = lrkv::device_sm_count();
+  return *n > 0 ? LRKV_OK : LRKV_ERR_CUDA;
 }
 
 }  // namespace
@@ -142,6 +142,7 @@ lrkv_status lrkv_decode(const lrkv_dims* dims, const void* q, const void* k_s, c
                         const void* z_k, const void* z_v, const void* b_k, const void* b_v,
                         const int32_t* seq_lens, float* out, float* lse, void* ws, size_t ws_bytes,
                         lrkv_stream_t stream) {
+  LRKV_TRACE_CALL("lrkv_decode");
   return decode_common(dims, q, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens, out, lse, ws, ws_bytes, stream,
                        nullptr, nullptr);
 }
@@ -151,6 +152,7 @@ lrkv_status lrkv_decode_profiled(const lrkv_dims* dims, const void* q, const voi
                                  const int32_t* seq_lens, float* out, float* lse, void* ws,
                                  size_t ws_bytes, lrkv_stream_t stream, void* ev_split_begin,
                                  void* ev_split_end) {
+  LRKV_TRACE_CALL("lrkv_decode_profiled");
   if (!ev_split_begin || !ev_split_end) return LRKV_ERR_INVALID_ARG;
   return decode_common(dims, q, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens, out, lse, ws, ws_bytes, stream,
                        ev_split_begin, ev_split_end);
@@ -160,6 +162,7 @@ lrkv_status lrkv_decode_paged(const lrkv_dims* dims, int page_size, int num_page
                               const void* q, const void* k_s, const void* v_s, const void* z_k, const void* z_v,
                               const void* b_k, const void* b_v, const int32_t* seq_lens, float* out, float* lse,
                               void* ws, size_t ws_bytes, lrkv_stream_t stream) {
+  LRKV_TRACE_CALL("lrkv_decode_paged");
   const PagedCache pc{block_table, page_size, num_pages};
   const lrkv_status st = check_paging(dims, pc);
   if (st != LRKV_OK) return st;
@@ -170,6 +173,7 @@ lrkv_status lrkv_decode_paged(const lrkv_dims* dims, int page_size, int num_page
 
 lrkv_status lrkv_key_scales(const lrkv_dims* dims, float eps, int n_new, const void* k_s, const void* z_k,
                             const void* b_k, const int32_t* start_pos, float* key_scale, lrkv_stream_t stream) {
+  LRKV_TRACE_CALL("lrkv_key_scales");
   lrkv_status st = check_decode_dims(dims);
   if (st != LRKV_OK) return st;
   if (dims->dtype != LRKV_BF16 || dims->rank < 1 || dims->head_dim > 256) return LRKV_ERR_UNSUPPORTED;
@@ -184,6 +188,7 @@ lrkv_status lrkv_decode_normed(const lrkv_dims* dims, const void* q, const void*
                                const void* z_k, const void* z_v, const void* b_k, const void* b_v,
                                const float* key_scale, const int32_t* seq_lens, float* out, float* lse, void* ws,
                                size_t ws_bytes, lrkv_stream_t stream) {
+  LRKV_TRACE_CALL("lrkv_decode_normed");
   if (!key_scale || !dims) return LRKV_ERR_INVALID_ARG;
   if (dims->dtype != LRKV_BF16 || dims->rank < 1) return LRKV_ERR_UNSUPPORTED;
   return decode_common(dims, q, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens, out, lse, ws, ws_bytes, stream, nullptr,
@@ -240,6 +245,7 @@ lrkv_status lrkv_decode_step(const lrkv_dims* dims, int d_model, const void* x, 
                              void* v_s, void* z_k, void* z_v, const void* b_k, const void* b_v,
                              const int32_t* seq_lens, float* out, float* lse, void* ws, size_t ws_bytes,
                              lrkv_stream_t stream) {
+  LRKV_TRACE_CALL("lrkv_decode_step");
   return decode_step_common(dims, d_model, x, w_sk, w_sv, u_k, u_v, q, k_s, v_s, z_k, z_v, b_k, b_v, seq_lens,
                             out, lse, ws, ws_bytes, stream, nullptr);
 }
@@ -249,6 +255,7 @@ lrkv_status lrkv_decode_step_paged(const lrkv_dims* dims, int d_model, const voi
                                    int page_size, int num_pages, const int32_t* block_table, void* k_s, void* v_s,
                                    void* z_k, void* z_v, const void* b_k, const void* b_v, const int32_t* seq_lens,
                                    float* out, float* lse, void* ws, size_t ws_bytes, lrkv_stream_t stream) {
+  LRKV_TRACE_CALL("lrkv_decode_step_paged");
   const PagedCache pc{block_table, page_size, num_pages};
   const lrkv_status st = check_paging(dims, pc);
   if (st != LRKV_OK) return st;

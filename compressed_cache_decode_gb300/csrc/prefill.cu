@@ -36,6 +36,7 @@
 
 #include "host_cache.h"
 #include "lrkv.h"
+#include "trace.h"
 #include "ptx.cuh"
 #include "tmap.h"
 
@@ -786,6 +787,7 @@ extern "C" lrkv_status lrkv_prefill(const lrkv_dims* dims, int q_len, const void
                                     const void* v_s, const void* z_k, const void* z_v, const void* b_k,
                                     const void* b_v, const int32_t* seq_lens, float* out, float* lse, void* ws,
                                     size_t ws_bytes, lrkv_stream_t stream) {
+  LRKV_TRACE_CALL("lrkv_prefill");
   return prefill_impl(dims, q_len, q, k_s, v_s, z_k, z_v, b_k, b_v, nullptr, seq_lens, out, lse, ws, ws_bytes,
                       stream);
 }
@@ -795,6 +797,7 @@ extern "C" lrkv_status lrkv_prefill_normed(const lrkv_dims* dims, int q_len, con
                                            const void* b_v, const float* key_scale, const int32_t* seq_lens,
                                            float* out, float* lse, void* ws, size_t ws_bytes,
                                            lrkv_stream_t stream) {
+  LRKV_TRACE_CALL("lrkv_prefill_normed");
   if (!key_scale) return LRKV_ERR_INVALID_ARG;
   return prefill_impl(dims, q_len, q, k_s, v_s, z_k, z_v, b_k, b_v, key_scale, seq_lens, out, lse, ws, ws_bytes,
                       stream);
@@ -805,6 +808,7 @@ extern "C" lrkv_status lrkv_prefill_paged(const lrkv_dims* dims, int q_len, cons
                                           const void* v_s, const void* z_k, const void* z_v, const void* b_k,
                                           const void* b_v, const int32_t* seq_lens, float* out, float* lse,
                                           void* ws, size_t ws_bytes, lrkv_stream_t stream) {
+  LRKV_TRACE_CALL("lrkv_prefill_paged");
   if (!dims || !block_table) return LRKV_ERR_INVALID_ARG;
   if (page_size < 128 || (page_size & (page_size - 1)) != 0 || num_pages < 1) return LRKV_ERR_INVALID_ARG;
   if (dims->max_len % page_size != 0) return LRKV_ERR_INVALID_ARG;

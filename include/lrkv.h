@@ -46,6 +46,10 @@
  *    scan then skips the work that depended on it, still waits at the full
  *    bound for every copy it issued, and records LRKV_ERR_TIMEOUT.  Set the
  *    variable only to exercise that path.
+ *  * Planning.  Launch grids and workspace sizes follow the current device's
+ *    SM count, or LRKV_SM_COUNT when that environment variable holds a
+ *    positive number (read at each call: workspace sizes without a device;
+ *    results are the same for any value).
  *  * Scale.  dims->scale <= 0 selects 1/sqrt(head_dim), the scale of the
  *    summed score (technical review, §3 "Associative decode").
  *  * Positions.  Without RoPE the decode and prefill carry no position
