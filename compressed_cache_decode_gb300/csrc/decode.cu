@@ -764,20 +764,20 @@ __global__ void __launch_bounds__(32 * kCombineWarps) lrkv_decode_combine_kernel
 
 // ================================================================ wide merge
 // The merge of the bf16 streaming decode: one CTA per (sequence b, head h),
-// grid-stride (on a small cache, on the SMs the scan leaves free).  The partials of the sequence's pieces are split over the 8
-// warps (warp w takes partials w, w + 8, ...); each warp merges its share
-// against its own largest maximum (lanes own columns of [acc_s | acc_z]),
-// the CTA merges the 8 warp results through shared memory with the same
-// log-sum-exp rule, then lifts the private sum: o = acc_s / L +
-// (acc_z / L) (B_h^V)^T and lse = (M + log2 L) ln 2 (Algorithm 2 steps 06-09).
-// It reads a pair's partials with eight warps at once instead of one warp
-// walking all of them.
-constexpr int kWideWarps = 8;
+// grid-stride.  The partials of the sequence's pieces are split over the NW
+// warps (warp w takes partials w, w + NW, ...); each warp merges its share in
+// one pass against a running maximum, a batch of partials in flight at a time
+// (lanes own columns of [acc_s | acc_z]); the CTA merges the warp results
+// through shared memory with the same log-sum-exp rule, then lifts the
+// private sum: o = acc_s / L + (acc_z / L) (B_h^V)^T (each output column's
+// B^V row read with 8-byte loads all in flight) and lse = (M + log2 L) ln 2
+// (Algorithm 2 steps 06-09).
+constexpr int kWideWarps = 8;  // warps per (sequence, head); 16 for at most 64 pairs
 
-template <bool BF16, int KC>  // KC: columns per lane, ceil((dh + r) / 32)
-__global__ void __launch_bounds__(32 * kWideWarps) lrkv_decode_merge_wide_kernel(const DecodePlan P) {
-  __shared__ float s_m[kWideWarps], s_l[kWideWarps];
-  __shared__ float s_acc[kWideWarps][32 * KC];
+template <bool BF16, int KC, int NW>  // KC: columns per lane, ceil((dh + r) / 32); NW: warps
+__global__ void __launch_bounds__(32 * NW) lrkv_decode_merge_wide_kernel(const DecodePlan P) {
+  __shared__ float s_m[NW], s_l[NW];
+  __shared__ float s_acc[NW][32 * KC];
   __shared__ float s_z[KC * 32];   // acc_z / L (private width <= 32 KC)
   __shared__ float s_os[KC * 32];  // acc_s / L
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -801,33 +801,44 @@ __global__ void __launch_bounds__(32 * kWideWarps) lrkv_decode_merge_wide_kernel
     const size_t s0 = static_cast<size_t>(b + c0) * P.ngw;
     const float* ml = P.part_ml + (s0 * H + h) * 2;
     const float* acc0 = P.part_acc + (s0 * H + h) * W;
-    // 1. this warp's share: its largest maximum, then the weighted sums
-    float mw = -INFINITY;
-    for (int i = warp; i < n; i += kWideWarps) mw = fmaxf(mw, ml[i * mstep]);
+    // 1. this warp's share in one pass, eight partials' (m, l) and rows in
+    //    flight at a time (fewer for wide rows), against a running maximum (raised per batch: the
+    //    sums so far are rescaled, the same for every lane)
+    float mw = -INFINITY, lw = 0.f;
     float a[KC];
 #pragma unroll
     for (int k = 0; k < KC; ++k) a[k] = 0.f;
-    float lw = 0.f;
-    if (mw != -INFINITY) {
-      for (int i0 = warp; i0 < n; i0 += 4 * kWideWarps) {  // four partials' rows in flight
-        float v[4][KC], wt[4];
+    constexpr int kBatch = KC <= 3 ? 8 : KC <= 6 ? 6 : KC <= 10 ? 4 : 2;  // registers: kBatch x KC row values
+    for (int i0 = warp; i0 < n; i0 += kBatch * NW) {
+      float v[kBatch][KC], mv[kBatch], lv[kBatch];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int i = i0 + u * kWideWarps;
-          const bool ok = i < n;
-          const float m = ok ? ml[i * mstep] : -INFINITY;
-          wt[u] = m == -INFINITY ? 0.f : exp2f(m - mw);
-          lw = fmaf(wt[u], ok ? ml[i * mstep + 1] : 0.f, lw);
+      for (int u = 0; u < kBatch; ++u) {
+        const int i = i0 + u * NW;
+        const bool ok = i < n;
+        mv[u] = ok ? ml[i * mstep] : -INFINITY;
+        lv[u] = ok ? ml[i * mstep + 1] : 0.f;
 #pragma unroll
-          for (int k = 0; k < KC; ++k) {
-            const int j = lane + 32 * k;
-            v[u][k] = (ok && j < W) ? acc0[i * astep + j] : 0.f;
-          }
+        for (int k = 0; k < KC; ++k) {
+          const int j = lane + 32 * k;
+          v[u][k] = (ok && j < W) ? acc0[i * astep + j] : 0.f;
         }
+      }
+      float bm = mv[0];
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
+      for (int u = 1; u < kBatch; ++u) bm = fmaxf(bm, mv[u]);
+      if (bm > mw) {
+        const float sc = mw == -INFINITY ? 0.f : exp2f(mw - bm);
+        lw *= sc;
 #pragma unroll
-          for (int k = 0; k < KC; ++k) a[k] = fmaf(wt[u], v[u][k], a[k]);
+        for (int k = 0; k < KC; ++k) a[k] *= sc;
+        mw = bm;
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const float wt = mv[u] == -INFINITY ? 0.f : exp2f(mv[u] - mw);
+        lw = fmaf(wt, lv[u], lw);
+#pragma unroll
+        for (int k = 0; k < KC; ++k) a[k] = fmaf(wt, v[u][k], a[k]);
       }
     }
     __syncthreads();  // the previous pair's reads of the shared arrays are done
@@ -841,10 +852,10 @@ __global__ void __launch_bounds__(32 * kWideWarps) lrkv_decode_merge_wide_kernel
     // 2. the CTA's merge of the warp shares (threads own columns)
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kWideWarps; ++w) M = fmaxf(M, s_m[w]);
-    float sw[kWideWarps], L = 0.f;
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, s_m[w]);
+    float sw[NW], L = 0.f;
 #pragma unroll
-    for (int w = 0; w < kWideWarps; ++w) {
+    for (int w = 0; w < NW; ++w) {
       sw[w] = s_m[w] == -INFINITY ? 0.f : exp2f(s_m[w] - M);
       L = fmaf(sw[w], s_l[w], L);
     }
@@ -852,15 +863,33 @@ __global__ void __launch_bounds__(32 * kWideWarps) lrkv_decode_merge_wide_kernel
     for (int t = threadIdx.x; t < W; t += blockDim.x) {
       float acc = 0.f;
 #pragma unroll
-      for (int w = 0; w < kWideWarps; ++w) acc = fmaf(sw[w], s_acc[w][t], acc);
+      for (int w = 0; w < NW; ++w) acc = fmaf(sw[w], s_acc[w][t], acc);
       if (t < dh) s_os[t] = acc * inv_l; else s_z[t - dh] = acc * inv_l;
     }
     __syncthreads();
-    // 3. the lift through (B_h^V)^T and the outputs
+    // 3. the lift through (B_h^V)^T and the outputs: a thread's B^V row read
+    //    with 8-byte loads, all in flight at once, where r and the base allow
+    const bool vec = BF16 && r % 4 == 0 && r <= 64 && (reinterpret_cast<uintptr_t>(P.b_v) & 7u) == 0;
     for (int t = threadIdx.x; t < dh; t += blockDim.x) {
       float v = s_os[t];
       const size_t base = (static_cast<size_t>(h) * dh + t) * r;
-      for (int cc = 0; cc < r; ++cc) v = fmaf(load_elem(P.b_v, base + cc, BF16), s_z[cc], v);
+      if (vec) {
+        const uint2* row = reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(P.b_v) + base);
+        uint2 w[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) w[q] = 4 * q < r ? row[q] : make_uint2(0u, 0u);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          if (4 * q < r) {
+            v = fmaf(bf_lo(w[q].x), s_z[4 * q], v);
+            v = fmaf(bf_hi(w[q].x), s_z[4 * q + 1], v);
+            v = fmaf(bf_lo(w[q].y), s_z[4 * q + 2], v);
+            v = fmaf(bf_hi(w[q].y), s_z[4 * q + 3], v);
+          }
+        }
+      } else {
+        for (int cc = 0; cc < r; ++cc) v = fmaf(load_elem(P.b_v, base + cc, BF16), s_z[cc], v);
+      }
       o[t] = v;
     }
     if (threadIdx.x == 0 && P.lse) P.lse[static_cast<size_t>(b) * H + h] = (M + log2f(L)) * kLn2;
@@ -898,10 +927,16 @@ template <bool BF16>
 CombineFn combine_fn(const DecodePlan& P) {
   const int cols = (P.dh + P.r + 31) / 32;
   if (P.wide_merge) {
-    if (cols <= 3) return lrkv_decode_merge_wide_kernel<BF16, 3>;
-    if (cols <= 6) return lrkv_decode_merge_wide_kernel<BF16, 6>;
-    if (cols <= 10) return lrkv_decode_merge_wide_kernel<BF16, 10>;
-    return lrkv_decode_merge_wide_kernel<BF16, 20>;
+    if (P.wide_warps == 16) {
+      if (cols <= 3) return lrkv_decode_merge_wide_kernel<BF16, 3, 16>;
+      if (cols <= 6) return lrkv_decode_merge_wide_kernel<BF16, 6, 16>;
+      if (cols <= 10) return lrkv_decode_merge_wide_kernel<BF16, 10, 16>;
+      return lrkv_decode_merge_wide_kernel<BF16, 20, 16>;
+    }
+    if (cols <= 3) return lrkv_decode_merge_wide_kernel<BF16, 3, kWideWarps>;
+    if (cols <= 6) return lrkv_decode_merge_wide_kernel<BF16, 6, kWideWarps>;
+    if (cols <= 10) return lrkv_decode_merge_wide_kernel<BF16, 10, kWideWarps>;
+    return lrkv_decode_merge_wide_kernel<BF16, 20, kWideWarps>;
   }
   if (cols <= 3) return lrkv_decode_combine_kernel<BF16, 3>;
   if (cols <= 6) return lrkv_decode_combine_kernel<BF16, 6>;
@@ -1006,7 +1041,7 @@ lrkv_status launch_all(const DecodePlan& P, cudaStream_t stream, cudaEvent_t ev_
 
   cudaLaunchConfig_t ccfg = {};
   ccfg.gridDim = dim3(P.combine_ctas);
-  ccfg.blockDim = dim3(32 * (P.wide_merge ? kWideWarps : kCombineWarps));
+  ccfg.blockDim = dim3(32 * (P.wide_merge ? (P.wide_warps == 16 ? 16 : kWideWarps) : kCombineWarps));
   ccfg.dynamicSmemBytes = P.wide_merge ? 0 : P.combine_smem;
   ccfg.stream = stream;
   ccfg.attrs = attr;
@@ -1125,6 +1160,10 @@ lrkv_status decode_make_plan(const lrkv_dims& d, int num_sms, DecodePlan& P, siz
   // the scan leaves free: measured on 8 x 4K rows, the wide merge there made
   // a chain of dependent decode steps 11% slower.)
   P.wide_merge = P.stream ? env_int("LRKV_DECODE_WIDE_MERGE", (large || many_pairs) ? 1 : 0) : 0;
+  // with at most 64 (sequence, head) pairs each pair's merge gets 16 warps
+  // (one 64K-row sequence of 32 heads, 304 partials a pair: 14.8 -> 14.2 us;
+  // four sequences, 128 pairs of 76: 8.4 us with 8 warps, 9.1 with 16)
+  P.wide_warps = static_cast<long long>(P.B) * H <= 64 ? 16 : kWideWarps;
   if (P.wide_merge)
     P.combine_ctas = static_cast<int>(std::min<long long>(static_cast<long long>(P.B) * H, 4ll * num_sms));
   else
@@ -1173,7 +1212,7 @@ lrkv_status decode_merge_launch(const DecodePlan& P, void* stream, bool pdl) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t ccfg = {};
   ccfg.gridDim = dim3(P.combine_ctas);
-  ccfg.blockDim = dim3(32 * (P.wide_merge ? kWideWarps : kCombineWarps));
+  ccfg.blockDim = dim3(32 * (P.wide_merge ? (P.wide_warps == 16 ? 16 : kWideWarps) : kCombineWarps));
   ccfg.dynamicSmemBytes = P.wide_merge ? 0 : P.combine_smem;
   ccfg.stream = s;
   ccfg.attrs = attr;

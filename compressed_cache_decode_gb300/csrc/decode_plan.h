@@ -53,6 +53,7 @@ struct DecodePlan {
   int combine_smem;
   int combine_ctas;  // grid of the combine kernel (one warp per (sequence, head), grid-stride)
   int wide_merge;    // 1: the merge runs as one CTA per (sequence, head) (large caches)
+  int wide_warps;    // warps of each wide-merge CTA (8 or 16; other values: 8)
   // bf16 streaming kernel: grid (range CTAs, row tiles of 16 heads); the 8
   // warps of a CTA form 4 pairs, pair p takes every 4th 16-token tile of the
   // CTA's range (tile i in stage i % stages) and each warp of the pair 8 of

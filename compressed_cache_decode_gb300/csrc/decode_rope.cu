@@ -437,6 +437,7 @@ lrkv_status rope_make_plan(const lrkv_dims& d, int num_sms, DecodePlan& P, size_
   P.smem_bytes = P.off_kv + P.stages * P.stage_bytes + 1024;
   P.min_tokens = 8 * kRT;
   P.wide_merge = 1;
+  P.wide_warps = 8;
   P.combine_ctas = static_cast<int>(std::min<long long>(static_cast<long long>(P.B) * P.H, 4ll * num_sms));
   P.combine_smem = 0;
   *ws_bytes = decode_workspace_bytes(P);

@@ -682,6 +682,7 @@ lrkv_status dense_make_plan(const lrkv_dense_dims& d, int num_sms, DecodePlan& P
   P.smem_bytes = P.off_kv + P.stages * P.stage_bytes + 1024;
   P.min_tokens = 8 * kDT;
   P.wide_merge = 1;
+  P.wide_warps = 8;
   P.combine_ctas = static_cast<int>(std::min<long long>(static_cast<long long>(P.B) * P.H, 4ll * num_sms));
   *ws_bytes = decode_workspace_bytes(P);
   return LRKV_OK;
@@ -736,6 +737,7 @@ lrkv_status mla_make_plan(const lrkv_mla_dims& d, int num_sms, DecodePlan& P, si
   P.smem_bytes = P.off_kv + P.stages * P.stage_bytes + 1024;
   P.min_tokens = 8 * kDT;
   P.wide_merge = 1;
+  P.wide_warps = 8;
   P.combine_ctas = static_cast<int>(std::min<long long>(static_cast<long long>(P.B) * P.H, 4ll * num_sms));
   *ws_bytes = decode_workspace_bytes(P);
   return LRKV_OK;
