@@ -1134,32 +1134,30 @@ lrkv_status decode_make_plan(const lrkv_dims& d, int num_sms, DecodePlan& P, siz
   P.ngw = 1;
   // bf16 shapes the streaming kernel covers use it; the rest (and fp32) run
   // the tile-synchronous kernel planned above
-  // the combine kernel: one warp per (sequence, head), at most kCombineCtas
-  // CTAs; the streaming scan leaves it that many SMs, so that consecutive
-  // steps' scans and merges overlap
+  // CTAs of the narrow combine: one warp per (sequence, head)
   const long long pair_ctas = (static_cast<long long>(P.B) * H + kCombineWarps - 1) / kCombineWarps;
-  // A large cache (at least kLargeCacheBytes of rows at capacity) keeps every
-  // SM on the scan: a step is long, so the scan's streaming matters more
-  // than overlapping the merge with the next step's scan; the merge then
-  // gets one warp per (sequence, head) on as many SMs as that needs.
+  // A large cache: at least kLargeCacheBytes of rows at capacity (no L2
+  // prefetch window below).
   const long long cap_bytes = static_cast<long long>(P.B) * P.max_len * per_token;
   const bool large = P.bf16 && cap_bytes >= kLargeCacheBytes;
-  // More (sequence, head) pairs than the narrow merge's warps on its SMs:
-  // the scan takes every SM and the merge runs wide after it (measured on
-  // 16 x 1K rows of 32 heads: the narrow merge took 62 us for 512 pairs).
+  // The bf16 scan's merge runs wide: one CTA per (sequence, head), 8 or 16
+  // warps splitting its partials, after the scan, which takes every SM.
+  // Tuning: LRKV_DECODE_WIDE_MERGE=0 keeps a small cache's merge narrow (one
+  // warp per pair on SMs the scan leaves free, beside the next call's scan):
+  // faster for independent back-to-back calls (8 x 4K rows: 21.0 against
+  // 24.7 us a call), slower wherever a call waits for the one before it
+  // (latency p50 38.8 against 32.7 us; dependent decode steps 35.6 against
+  // 30.4 us), and far slower with many pairs (16 x 1K rows of 32 heads: 62 us
+  // for its 512 pairs).
   const bool many_pairs = static_cast<long long>(P.B) * H > static_cast<long long>(kCombineWarps) * kCombineCtas;
-  const int reserve = (large || many_pairs) ? 0 : static_cast<int>(std::min<long long>(pair_ctas, kCombineCtas));
+  const bool narrow = P.bf16 && !large && !many_pairs && env_int("LRKV_DECODE_WIDE_MERGE", 1) == 0;
+  const int reserve = narrow ? static_cast<int>(std::min<long long>(pair_ctas, kCombineCtas)) : 0;
   P.grid = env_int("LRKV_DECODE_GRID", std::max(1, num_sms - reserve));
   // the streaming kernel's grid is (range CTAs, row tiles of 16 heads): it
   // divides P.grid by the row tiles
   if (P.bf16 && env_int("LRKV_DECODE_TILE_SYNC", 0) == 0) stream_plan(P);
   if (!P.stream) P.grid = env_int("LRKV_DECODE_GRID", num_sms);
-  // a large cache's merge: one CTA per (sequence, head) (grid-stride, at
-  // most 4 per SM), after the scan on all SMs
-  // (A small cache keeps one warp per (sequence, head) on the `reserve` SMs
-  // the scan leaves free: measured on 8 x 4K rows, the wide merge there made
-  // a chain of dependent decode steps 11% slower.)
-  P.wide_merge = P.stream ? env_int("LRKV_DECODE_WIDE_MERGE", (large || many_pairs) ? 1 : 0) : 0;
+  P.wide_merge = (P.stream && !narrow) ? 1 : 0;
   // with at most 64 (sequence, head) pairs each pair's merge gets 16 warps
   // (one 64K-row sequence of 32 heads, 304 partials a pair: 14.8 -> 14.2 us;
   // four sequences, 128 pairs of 76: 8.4 us with 8 warps, 9.1 with 16)
@@ -1167,8 +1165,8 @@ lrkv_status decode_make_plan(const lrkv_dims& d, int num_sms, DecodePlan& P, siz
   if (P.wide_merge)
     P.combine_ctas = static_cast<int>(std::min<long long>(static_cast<long long>(P.B) * H, 4ll * num_sms));
   else
-    P.combine_ctas = (P.stream && !large && !many_pairs) ? std::max(reserve, 1)
-                                          : static_cast<int>(std::min<long long>(pair_ctas, large ? num_sms : 65535));
+    P.combine_ctas = P.stream ? std::max(reserve, 1)
+                              : static_cast<int>(std::min<long long>(pair_ctas, large ? num_sms : 65535));
   P.min_tokens = env_int("LRKV_DECODE_MIN_TOKENS", P.stream ? 8 * P.T : 2 * P.T);
   if (P.stream) {
     // L2 prefetch window: about 48 MB in flight over all CTAs (L2 is 126 MB).

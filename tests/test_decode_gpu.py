@@ -85,6 +85,25 @@ def test_random_shapes(dtype, shape):
             assert np.all(out[b] == 0.0)
 
 
+@pytest.mark.parametrize("shape", [
+    (2, 16, 64, 28, 300, [300, 129]),
+    (4, 32, 128, 48, 97, [97, 0, 33, 64]),
+    (8, 16, 64, 28, 4096, [4096, 4000, 1, 2048, 3333, 17, 4096, 640]),
+])
+def test_narrow_merge_tuning(monkeypatch, shape):
+    """LRKV_DECODE_WIDE_MERGE=0: a small cache's merge runs one warp per pair on
+    SMs the scan leaves free; same results as the default wide merge."""
+    B, H, dh, r, L, lens = shape
+    case = inputs.random_decode_case(seed=B * 7 + L, batch=B, heads=H, head_dim=dh, rank=r, max_len=L,
+                                     dtype="bf16", lens=lens)
+    wide_o, wide_l, _ = _run(case)
+    monkeypatch.setenv("LRKV_DECODE_WIDE_MERGE", "0")
+    out, lse, _ = _run(case)
+    ref_o, ref_l = _oracle(case)
+    assert_decode_close(out, lse, ref_o, ref_l, "bf16", what=f"narrow{shape}")
+    assert_decode_close(wide_o, wide_l, ref_o, ref_l, "bf16", what=f"wide{shape}")
+
+
 def test_explicit_scale():
     case = inputs.random_decode_case(seed=3, batch=2, heads=16, head_dim=64, rank=28, max_len=100,
                                      dtype="bf16", lens=[100, 40])
