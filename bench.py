@@ -419,11 +419,18 @@ class StepTimer:
         return out
 
 
+LAUNCH_REPLAYS = 10  # replays whose launches are read by scan_launch_ms
+
+
 def scan_launch_ms(profiled, n, stream, use_graph=True):
-    """Median duration of one isolated scan launch: `profiled(i, ev0, ev1, s)`
+    """Mean duration of one isolated scan launch: `profiled(i, ev0, ev1, s)`
     enqueues a decode with CUDA events right around its scan kernel; the n
     calls are replayed from a graph (so the interval holds the kernel, not the
-    host's launch latency), warm, and the last replay's launches are read."""
+    host's launch latency), warm, then LAUNCH_REPLAYS more replays are read
+    one by one (n x LAUNCH_REPLAYS launches).  The mean, not the median: event
+    intervals on these GPUs come in steps of ~2 us, so a median of a ~25 us
+    launch jumps by a whole step while the mean of a few hundred samples
+    does not.  Returns (mean, median, min, max, kind)."""
     import torch
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
     with torch.cuda.stream(stream):
@@ -444,8 +451,7 @@ def scan_launch_ms(profiled, n, stream, use_graph=True):
             print(f"profiled graph capture failed ({e}); eager timing", file=sys.stderr)
             g = None
             torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    while True:
+    def replay():
         with torch.cuda.stream(stream):
             if g is not None:
                 g.replay()
@@ -453,10 +459,17 @@ def scan_launch_ms(profiled, n, stream, use_graph=True):
                 for i in range(n):
                     profiled(i, evs[i][0], evs[i][1], stream)
         torch.cuda.synchronize()
+
+    t0 = time.perf_counter()
+    while True:
+        replay()
         if (time.perf_counter() - t0) * 1e3 >= 50.0:
             break
-    ms = [e0.elapsed_time(e1) for e0, e1 in evs]
-    return statistics.median(ms), min(ms), max(ms), kind
+    ms = []
+    for _ in range(LAUNCH_REPLAYS):
+        replay()
+        ms += [e0.elapsed_time(e1) for e0, e1 in evs]
+    return statistics.fmean(ms), statistics.median(ms), min(ms), max(ms), kind
 
 
 class DecodeSetup:
@@ -644,7 +657,7 @@ def decode_leg(setup, K, W, stream, use_graph, peak, world, dev, repeats=7, min_
     ms = timer.time(repeats=repeats, min_ms=min_ms)
     sp = _spread(ms)
     ms_step = max_over_ranks(sp["median"], world, dev)
-    iso, iso_min, iso_max, kind = scan_launch_ms(setup.profiled, min(K, 20), stream, use_graph)
+    iso, iso_med, iso_min, iso_max, kind = scan_launch_ms(setup.profiled, min(K, 20), stream, use_graph)
     achieved = setup.split_bytes / (iso * 1e-3) / 1e9
     lat = call_latency_us(setup.step, setup.n_rep, stream, n=200, use_graph=use_graph)
     return {
@@ -656,9 +669,10 @@ def decode_leg(setup, K, W, stream, use_graph, peak, world, dev, repeats=7, min_
         "graph": timer.graph is not None,
         "roofline": {"bound": "hbm", "kernel": scan_kernel_name(w), "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "algorithmic_bytes_per_launch": setup.split_bytes,
-                     "launch_ms": iso, "launch_ms_min": iso_min, "launch_ms_max": iso_max,
+                     "launch_ms": iso, "launch_ms_median": iso_med, "launch_ms_min": iso_min,
+                     "launch_ms_max": iso_max,
                      "launch_timing": f"CUDA events right around each isolated scan launch on the launching "
-                                      f"stream ({kind} launches), median of {min(K, 20)}"},
+                                      f"stream ({kind} launches), mean of {min(K, 20) * LAUNCH_REPLAYS}"},
     }, timer
 
 
@@ -1114,7 +1128,7 @@ def main():
         dist.barrier()
     spread = _spread(ms_list)
     ms_step = max_over_ranks(spread["median"], world, dev)
-    iso, iso_min, iso_max, iso_kind = scan_launch_ms(head.profiled, min(K, 20), stream, use_graph)
+    iso, iso_med, iso_min, iso_max, iso_kind = scan_launch_ms(head.profiled, min(K, 20), stream, use_graph)
     del timer
     latency = call_latency_us(head.step, head.n_rep, stream, n=200, use_graph=use_graph)
 
@@ -1174,9 +1188,9 @@ def main():
                          "peak": peak, "peak_kind": f"{peak_kind} HBM copy", "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "algorithmic_bytes_per_launch": head.split_bytes, "launch_ms": iso,
-                         "launch_ms_min": iso_min, "launch_ms_max": iso_max,
+                         "launch_ms_median": iso_med, "launch_ms_min": iso_min, "launch_ms_max": iso_max,
                          "launch_timing": f"CUDA events right around each isolated scan launch on the launching "
-                                          f"stream ({iso_kind} launches), median of {min(K, 20)}",
+                                          f"stream ({iso_kind} launches), mean of {min(K, 20) * LAUNCH_REPLAYS}",
                          "step_rate_gbs": head.split_bytes / (ms_step * 1e-3) / 1e9,
                          "step_rate_frac": head.split_bytes / (ms_step * 1e-3) / 1e9 / peak},
             "cpu_baseline": cpu,

@@ -1136,8 +1136,8 @@ lrkv_status decode_make_plan(const lrkv_dims& d, int num_sms, DecodePlan& P, siz
   // the tile-synchronous kernel planned above
   // CTAs of the narrow combine: one warp per (sequence, head)
   const long long pair_ctas = (static_cast<long long>(P.B) * H + kCombineWarps - 1) / kCombineWarps;
-  // A large cache: at least kLargeCacheBytes of rows at capacity (no L2
-  // prefetch window below).
+  // A large cache: at least kLargeCacheBytes of rows at capacity (its merge
+  // is never the narrow one).
   const long long cap_bytes = static_cast<long long>(P.B) * P.max_len * per_token;
   const bool large = P.bf16 && cap_bytes >= kLargeCacheBytes;
   // The bf16 scan's merge runs wide: one CTA per (sequence, head), 8 or 16
@@ -1169,13 +1169,16 @@ lrkv_status decode_make_plan(const lrkv_dims& d, int num_sms, DecodePlan& P, siz
                               : static_cast<int>(std::min<long long>(pair_ctas, large ? num_sms : 65535));
   P.min_tokens = env_int("LRKV_DECODE_MIN_TOKENS", P.stream ? 8 * P.T : 2 * P.T);
   if (P.stream) {
-    // L2 prefetch window: about 48 MB in flight over all CTAs (L2 is 126 MB).
-    // Only for a small cache read by one row tile: with several row tiles
-    // every CTA of a range would prefetch the same rows, and on a large
-    // cache the ring alone keeps HBM busier (measured: 0.51 -> 0.69 of the
-    // HBM peak on 4 x 64K rows of 32 heads without it).
-    const long long per_cta = (48ll << 20) / std::max(1, P.grid * P.mt);
-    const int pfw = (large || P.mt > 1) ? 0 : static_cast<int>(per_cta / P.stage_bytes);
+    // L2 prefetch window beyond the ring (tiles per CTA): none.  Tuning:
+    // LRKV_DECODE_PREFETCH_TILES=n prefetches each CTA's n tiles after the
+    // first burst into L2, issued right behind the burst.  Measured slower
+    // everywhere with the current scan: on 4 x 64K rows of 32 heads it cost
+    // 0.69 -> 0.51 of the HBM peak (two row tiles prefetched the same rows;
+    // the ring alone keeps HBM busier); on 8 x 4K rows of 16 heads the
+    // isolated launch took 26.6 us with 9 or 16 tiles against 24.6 us
+    // without (the prefetch's bulk copies queue beside the ring's in the TMA
+    // unit, and the issuing lane spends ~6K cycles on them).
+    const int pfw = 0;
     P.pfw = env_int("LRKV_DECODE_PREFETCH_TILES", pfw);
   }
   // per warp: the lift's z row, and the weights and denominators of one sequence's partials

@@ -215,6 +215,18 @@ __device__ __forceinline__ void bk_load(const DecodePlan& P, int m0, const BkRol
     v[u] = (R.on && d0 + u < R.nd) ? *reinterpret_cast<const uint2*>(base + (d0 + u) * step) : make_uint2(0u, 0u);
 }
 
+// p[hl][4 cg .. 4 cg + 3] into the private-score table: entry hl r/2 + c/2
+// holds {hi(p[c]), hi(p[c+1])}, {lo(p[c]), lo(p[c+1])} (bf16 high parts and
+// the bf16 of what they leave), the same 8 bytes per column pair as the fp32
+// row would take: one 16-byte store of two entries.
+__device__ __forceinline__ void store_p_entries(float* prow, const float (&a)[4]) {
+  float h[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) h[u] = __bfloat162float(__float2bfloat16_rn(a[u]));
+  *reinterpret_cast<uint4*>(prow) = make_uint4(pack_bf16(h[0], h[1]), pack_bf16(a[0] - h[0], a[1] - h[1]),
+                                               pack_bf16(h[2], h[3]), pack_bf16(a[2] - h[2], a[3] - h[3]));
+}
+
 // The same from a shared-memory copy of the row tile's B^K: head hl's
 // [dh][r] bf16 block at hl * bk_head_bytes, head-dim rows d = i bk_dsplit + dp.
 __device__ __forceinline__ void absorb_rows_smem(const DecodePlan& P, const BkRole& R,
@@ -245,17 +257,15 @@ __device__ __forceinline__ void absorb_rows_smem(const DecodePlan& P, const BkRo
       aa[u] += __shfl_xor_sync(0xffffffffu, aa[u], o);
       ab[u] += __shfl_xor_sync(0xffffffffu, ab[u], o);
     }
-  if (R.on && R.dp == 0) {
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      pa[R.hl * P.r + 4 * R.cg + u] = aa[u];
-      if (pb) pb[R.hl * P.r + 4 * R.cg + u] = ab[u];
-    }
+  // heads past H get zero entries
+  if (R.hl < 16 && R.dp == 0) {
+    store_p_entries(pa + R.hl * P.r + 4 * R.cg, aa);
+    if (pb) store_p_entries(pb + R.hl * P.r + 4 * R.cg, ab);
   }
 }
 
 // p rows of up to two sequences (q rows qa, qb: [16][dh] bf16; p rows pa, pb:
-// [16][r] fp32); v holds the first chunk of B^K already.
+// [16][r] private-score table entries); v holds the first chunk of B^K already.
 __device__ __forceinline__ void absorb_rows(const DecodePlan& P, int m0, const BkRole& R, uint2 (&v)[kBkChunk],
                                             const __nv_bfloat16* qa, const __nv_bfloat16* qb, float* pa, float* pb) {
   float aa[4] = {0.f, 0.f, 0.f, 0.f}, ab[4] = {0.f, 0.f, 0.f, 0.f};
@@ -284,12 +294,10 @@ __device__ __forceinline__ void absorb_rows(const DecodePlan& P, int m0, const B
       aa[u] += __shfl_xor_sync(0xffffffffu, aa[u], o);
       ab[u] += __shfl_xor_sync(0xffffffffu, ab[u], o);
     }
-  if (R.on && R.dp == 0) {
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      pa[R.hl * P.r + 4 * R.cg + u] = aa[u];
-      if (pb) pb[R.hl * P.r + 4 * R.cg + u] = ab[u];
-    }
+  // heads past H get zero entries
+  if (R.hl < 16 && R.dp == 0) {
+    store_p_entries(pa + R.hl * P.r + 4 * R.cg, aa);
+    if (pb) store_p_entries(pb + R.hl * P.r + 4 * R.cg, ab);
   }
 }
 
@@ -407,6 +415,11 @@ __global__ void __launch_bounds__(kThreadsS, 1)
   // the first lengths are read before anything else (their latency is the
   // start of the chain to the first tile)
   const int len0 = tid < B ? P.seq_lens[tid] : 0;
+  // without the shared-memory B^K: this thread's B^K columns (one chunk) are
+  // loaded now, their latency hidden behind the set-up below
+  const BkRole bkr = bk_role(P, m0, tid);
+  uint2 bkv[kBkChunk];
+  if (P.bk_stages == 0) bk_load(P, m0, bkr, 0, bkv);
   {
     // one read per 64-byte line of the launch plan, all at once, so that the
     // later dependent reads of its fields hit the constant cache
@@ -416,37 +429,44 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       if (v == 0x7f7f7f7f && tid == 0) s_timeout = v;  // never true: keeps the read
     }
   }
+  // barriers and records set up by several threads at once (one thread
+  // doing all of it delayed the whole block by ~1.3K cycles)
   if (tid == 0) {
+    // with bk_stages > 0 the row tile's B^K lands in the last bk_stages ring
+    // stages (one bulk copy, issued first: it depends on nothing) and those
+    // stages get their tiles once the first two pieces are absorbed
+    uint64_t* bkb = reinterpret_cast<uint64_t*>(smem + 272);
+    mbar_init(bkb, 1);
+    fence_barrier_init();
+    if (P.bk_stages > 0) {
+      const uint32_t bytes = static_cast<uint32_t>(min(16, H - m0) * dh * r * 2);
+      mbar_arrive_expect_tx(bkb, bytes);
+      tma_load_1d(smem + P.off_kv + static_cast<size_t>(P.stages - P.bk_stages) * P.stage_bytes,
+                  static_cast<const __nv_bfloat16*>(P.b_k) + static_cast<size_t>(m0) * dh * r, bytes, bkb);
+    }
+  } else if (tid == 1) {
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
+  } else if (tid == 2) {
     if (r > 0) {
       prefetch_tmap(&tm_zk);
       prefetch_tmap(&tm_zv);
     }
     if (P.ks_tma) prefetch_tmap(&tm_ks);
+  } else if (tid == 3) {
     s_timeout = 0;
     s_nopage = 0;
     reinterpret_cast<int*>(smem + kQLastOff)[0] = -1;
     reinterpret_cast<int*>(smem + kQLastOff)[1] = -1;
-    for (int s = 0; s < P.stages; ++s) {
-      mbar_init(&full[s], 1);
-      issued[s] = -1;
-      cons[s] = 0;
-    }
     mbar_init(&pbar[0], 1);
     mbar_init(&pbar[1], 1);
-    mbar_init(reinterpret_cast<uint64_t*>(smem + 272), 1);
     fence_barrier_init();
-    // with bk_stages > 0 the row tile's B^K lands in the last bk_stages ring
-    // stages (one bulk copy, issued first: it depends on nothing) and those
-    // stages get their tiles once the first two pieces are absorbed
-    if (P.bk_stages > 0) {
-      const uint32_t bytes = static_cast<uint32_t>(min(16, H - m0) * dh * r * 2);
-      uint64_t* bkb = reinterpret_cast<uint64_t*>(smem + 272);
-      mbar_arrive_expect_tx(bkb, bytes);
-      tma_load_1d(smem + P.off_kv + static_cast<size_t>(P.stages - P.bk_stages) * P.stage_bytes,
-                  static_cast<const __nv_bfloat16*>(P.b_k) + static_cast<size_t>(m0) * dh * r, bytes, bkb);
-    }
+  } else if (tid >= 96 && tid < 96 + P.stages) {
+    const int s = tid - 96;
+    mbar_init(&full[s], 1);
+    issued[s] = -1;
+    cons[s] = 0;
+    fence_barrier_init();
   }
   if (tid < 64) zo[tid] = P.zo[tid >> 5][tid & 31];
   if (PH && tid < 16) zhead[tid] = (tid / P.hs) * kT * P.segp * 2 + (tid % P.hs) * r * 2;
@@ -510,28 +530,37 @@ __global__ void __launch_bounds__(kThreadsS, 1)
   const bool two = piece_next(pc1, pre, B, g1);
   uint64_t* bkbar = reinterpret_cast<uint64_t*>(smem + 272);  // the B^K copy (issued at entry)
   const int first_burst = P.stages - P.bk_stages;
-  if (tid == 0) {
-    q_issue(P, smem, pbar, 0, pc.b, m0, 0);
-    if (two) q_issue(P, smem, pbar, 1, pc1.b, m0, 1);
+  // The last warp, when it has no absorb role (warm: see below), issues the
+  // q copies and the first burst of tiles, one tile per lane, so that the
+  // absorbing warps wait only for q (a tile's four copies take a lane ~1.5K
+  // cycles to issue), and after its warm-up pass the tiles of the stages
+  // that held B^K; otherwise lane 0 of warp w issues tiles w, w + 8, ... and
+  // thread 0 the q copies, and the absorbing warps the later stages' tiles.
+  const bool warm = warp == kWarps - 1 && warp >= P.bk_warps;
+  const bool lone = P.bk_warps < kWarps;  // there is such a warp
+  const bool issuer = !lone || warm;
+  if (issuer && (lone ? lane >= 30 : tid < 2)) {
+    const int qi = lone ? 31 - lane : tid;
+    if (qi == 0) q_issue(P, smem, pbar, 0, pc.b, m0, 0);
+    else if (two) q_issue(P, smem, pbar, 1, pc1.b, m0, 1);
   }
-  if (lane == 0) {
+  if (issuer && (lone ? lane < first_burst : lane == 0)) {
     TileCursor cur;
     cur.pc = pc;
     cur.more = more;
     cur.ibase = 0;
-    for (int j = warp; j < first_burst && cur.seek(j, pre, B, g1); j += kWarps) {
+    for (int j = lone ? lane : warp; j < first_burst && cur.seek(j, pre, B, g1); j += lone ? 32 : kWarps) {
       if (!stream_issue(P, &tm_k, &tm_v, &tm_zk, &tm_zv, &tm_ks, smem, full, j, cur.pc.b,
                         cur.pc.t_beg + (j - cur.ibase) * kT, zseg0, m0, pre))
         *reinterpret_cast<volatile int*>(&s_nopage) = 1;
       *reinterpret_cast<volatile int*>(&issued[j]) = j;
     }
+    // the tiles after the first burst start streaming into L2 at once, behind
+    // the burst's copies in the TMA unit's queue (which it serves in order):
+    // they land while the block absorbs and builds its tables
+    if ((lone ? lane == 0 : warp == kWarps - 1) && P.pfw > 0)
+      l2_prefetch_tiles(P, pre, B, g0, g1, first_burst, P.stages + P.pfw);
   }
-  // without the shared-memory B^K: its first chunk in registers (after the
-  // copies were issued: the loads hold the issuing warps until they drain)
-  const BkRole bkr = bk_role(P, m0, tid);
-  uint2 bkv[kBkChunk];
-  if (P.bk_stages == 0) bk_load(P, m0, bkr, 0, bkv);
-
   float acc_v[DHT][4] = {};      // O_s^T: rows d = 16 m + g (+8), columns heads 2 q4 + e
   float acc_z[NZV][4] = {};      // O_z^T: rows latent column 16 m + g (+8) of this half (PH: of each head)
   float mc[2] = {-INFINITY, -INFINITY}, lc[2] = {0.f, 0.f};  // reference max, denominator
@@ -541,18 +570,26 @@ __global__ void __launch_bounds__(kThreadsS, 1)
   const unsigned char* pqcur = smem + P.off_pq;  // the current piece's q / p buffer
   // steps kk whose latent column 16 kk + 2 q4 (bit of vmask0), or that
   // column + 8 (vmask1), belongs to this lane's head g within the half
+  // (head g's columns are g r .. g r + r - 1; unrolled and without a
+  // division: this runs once per launch, on the way to the first tile)
   uint32_t vmask0 = 0u, vmask1 = 0u;
-  for (int kk = 0; kk < kst; ++kk) {
-    const int j = 16 * kk + 2 * q4;
-    vmask0 |= (j / r == g ? 1u : 0u) << kk;
-    vmask1 |= ((j + 8) / r == g ? 1u : 0u) << kk;
+  {
+    const int rr = (EXACT && MZMAX > 0) ? 2 * MZMAX : r;
+    const int lo = g * rr, hi = lo + rr;
+#pragma unroll
+    for (int kk = 0; kk < MZA; ++kk) {
+      if (kk < kst) {
+        const int j = 16 * kk + 2 * q4;
+        vmask0 |= (j >= lo && j < hi ? 1u : 0u) << kk;
+        vmask1 |= (j + 8 >= lo && j + 8 < hi ? 1u : 0u) << kk;
+      }
+    }
   }
 
   // The last warp, when it has no absorb role, first runs one tile of the
   // scan's code on no tokens (nvalid 0: every score is masked, no value row
   // kept, no stage consumed) while the other warps absorb, so that the tile
   // code is in the SM's instruction cache when the first tiles arrive.
-  const bool warm = warp == kWarps - 1 && warp >= P.bk_warps;
   bool ok = true;
   if (MZMAX > 0 && !warm) {
     // p of the first two pieces, from their q rows and B^K
@@ -573,7 +610,12 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     }
     if (!ok) *reinterpret_cast<volatile int*>(&s_timeout) = 1;
   }
-  if (P.bk_stages > 0 && warp < P.bk_warps) {
+  if (P.bk_stages > 0 && warp < P.bk_warps && lone) {
+    // B^K is consumed (by the warps that absorb): the warm-up warp gives the
+    // last stages their tiles
+    fence_proxy_async_smem();
+    named_arrive(2, 32 * (P.bk_warps + 1));
+  } else if (P.bk_stages > 0 && warp < P.bk_warps) {
     // B^K is consumed (by the warps that absorb): the last stages get their tiles
     fence_proxy_async_smem();
     named_sync(2, 32 * P.bk_warps);
@@ -681,20 +723,6 @@ __global__ void __launch_bounds__(kThreadsS, 1)
         qf[e] = v;
       }
     }
-    if (MZMAX > 0) {
-      // p of the row tile's heads as bf16 high and low parts, head-major in
-      // pairs of latent columns: entry e = hl r/2 + c/2 holds
-      // {hi(p[c]), hi(p[c+1])}, {lo(p[c]), lo(p[c+1])} (zero past H), written
-      // over the fp32 p rows in place (the same 8 bytes per entry)
-      float2* pr = reinterpret_cast<float2*>(pqb + 16 * dh * 2);
-      const int np = 16 * (r / 2);
-      for (int e = tid; e < (tid < nset ? np : 0); e += nset) {
-        const float2 v = e / (r / 2) < nh ? pr[e] : make_float2(0.f, 0.f);
-        const float h0 = __bfloat162float(__float2bfloat16_rn(v.x));
-        const float h1 = __bfloat162float(__float2bfloat16_rn(v.y));
-        reinterpret_cast<uint2*>(pr)[e] = make_uint2(pack_bf16(h0, h1), pack_bf16(v.x - h0, v.y - h1));
-      }
-    }
     if (!split) {
       named_sync(1, kThreadsS);  // fragments ready
     } else if (!warm) {
@@ -704,12 +732,6 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       named_sync(3, kThreadsS);  // fragments ready (the warm-up warp)
     }
     }
-
-    // the ring's later tiles start streaming into L2 (issued by the last warp,
-    // whose pair has the fewest tiles, once the ring's own copies are queued:
-    // the TMA unit serves its queue in order)
-    if (kp == 0 && tid == kThreadsS - 32)
-      l2_prefetch_tiles(P, pre, B, g0, g1, P.stages, P.stages + P.pfw);
 
     // ---- this pair's tiles of the piece ----------------------------------------
     // rows of the piece's sequence: a tile reaching past them may hold
@@ -970,6 +992,24 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     }
 
     if (dry) {  // warm-up pass done: the real first piece
+      if (P.bk_stages > 0) {
+        // the stages that held B^K get their tiles once the absorbing warps
+        // are done with it (one tile per lane)
+        named_sync(2, 32 * (P.bk_warps + 1));
+        if (lane < P.bk_stages && ok && !*reinterpret_cast<volatile int*>(&s_timeout)) {
+          TileCursor cur;
+          cur.pc = pc;
+          cur.more = true;
+          cur.ibase = 0;
+          const int j = first_burst + lane;
+          if (cur.seek(j, pre, B, g1)) {
+            if (!stream_issue(P, &tm_k, &tm_v, &tm_zk, &tm_zv, &tm_ks, smem, full, j, cur.pc.b,
+                              cur.pc.t_beg + (j - cur.ibase) * kT, zseg0, m0, pre))
+              *reinterpret_cast<volatile int*>(&s_nopage) = 1;
+            *reinterpret_cast<volatile int*>(&issued[j]) = j;
+          }
+        }
+      }
       kp = 0;
       continue;
     }
@@ -1179,12 +1219,20 @@ static lrkv_status stream_plan_impl(DecodePlan& P) {
   }
   P.smem_bytes = layout(P.stages);
   // B^K of a row tile staged through the last ring stages when it fits
-  // (leaving at least one stage for the first tiles)
+  // (leaving at least one stage for the first tiles), those stages getting
+  // their tiles after the absorb; otherwise each absorb thread loads its
+  // columns at entry.  Tuning: LRKV_DECODE_BK_REGS=1 takes the register
+  // path whenever a thread's columns are one chunk (d_h / bk_dsplit <=
+  // kBkChunk rows); measured slower on 8 x 4K rows of 16 heads, rank 28:
+  // the absorb from registers took ~5.5K cycles against ~2.4K from shared
+  // memory.
   {
     P.bk_head_bytes = dh * r * 2;
     const long long bk_bytes = 16ll * P.bk_head_bytes;
     const int nbk = r > 0 ? static_cast<int>((bk_bytes + P.stage_bytes - 1) / P.stage_bytes) : 0;
-    P.bk_stages = (r > 0 && nbk < stages) ? nbk : 0;
+    const char* regs_env = std::getenv("LRKV_DECODE_BK_REGS");
+    const bool one_chunk = dh / P.bk_dsplit <= kBkChunk && regs_env && regs_env[0] == '1';
+    P.bk_stages = (r > 0 && nbk < stages && !one_chunk) ? nbk : 0;
   }
   P.pfw = 0;  // L2 prefetch window beyond the ring (tiles); set with the grid
   return stream_fn(P) ? LRKV_OK : LRKV_ERR_UNSUPPORTED;
