@@ -1170,14 +1170,14 @@ lrkv_status decode_make_plan(const lrkv_dims& d, int num_sms, DecodePlan& P, siz
   P.min_tokens = env_int("LRKV_DECODE_MIN_TOKENS", P.stream ? 8 * P.T : 2 * P.T);
   if (P.stream) {
     // L2 prefetch window beyond the ring (tiles per CTA): none.  Tuning:
-    // LRKV_DECODE_PREFETCH_TILES=n prefetches each CTA's n tiles after the
-    // first burst into L2, issued right behind the burst.  Measured slower
-    // everywhere with the current scan: on 4 x 64K rows of 32 heads it cost
-    // 0.69 -> 0.51 of the HBM peak (two row tiles prefetched the same rows;
-    // the ring alone keeps HBM busier); on 8 x 4K rows of 16 heads the
-    // isolated launch took 26.6 us with 9 or 16 tiles against 24.6 us
-    // without (the prefetch's bulk copies queue beside the ring's in the TMA
-    // unit, and the issuing lane spends ~6K cycles on them).
+    // LRKV_DECODE_PREFETCH_TILES=n has thread 0 prefetch each CTA's n tiles
+    // after the ring into L2 once it has absorbed.  Measured slower
+    // everywhere: on 4 x 64K rows of 32 heads 0.69 -> 0.51 of the HBM peak
+    // (two row tiles prefetched the same rows; the ring alone keeps HBM
+    // busier); on 8 x 4K rows of 16 heads 25.4 us a launch without, 26.6
+    // with 9 tiles, 27.3 with 4: the prefetch traffic delays the block's
+    // instruction fetches, which miss to HBM once the caches are cold (the
+    // loop's first code then arrives ~8K cycles later than without).
     const int pfw = 0;
     P.pfw = env_int("LRKV_DECODE_PREFETCH_TILES", pfw);
   }

@@ -555,11 +555,6 @@ __global__ void __launch_bounds__(kThreadsS, 1)
         *reinterpret_cast<volatile int*>(&s_nopage) = 1;
       *reinterpret_cast<volatile int*>(&issued[j]) = j;
     }
-    // the tiles after the first burst start streaming into L2 at once, behind
-    // the burst's copies in the TMA unit's queue (which it serves in order):
-    // they land while the block absorbs and builds its tables
-    if ((lone ? lane == 0 : warp == kWarps - 1) && P.pfw > 0)
-      l2_prefetch_tiles(P, pre, B, g0, g1, first_burst, P.stages + P.pfw);
   }
   float acc_v[DHT][4] = {};      // O_s^T: rows d = 16 m + g (+8), columns heads 2 q4 + e
   float acc_z[NZV][4] = {};      // O_z^T: rows latent column 16 m + g (+8) of this half (PH: of each head)
@@ -632,6 +627,11 @@ __global__ void __launch_bounds__(kThreadsS, 1)
       }
     }
   }
+  // with an L2 prefetch window (a tuning option, off by default): the tiles
+  // after the ring's start streaming into L2, issued by thread 0 once it has
+  // absorbed and released B^K (the ring's copies are queued by then, and the
+  // warm-up warp, which issues them, is not held up)
+  if (tid == 0 && P.pfw > 0) l2_prefetch_tiles(P, pre, B, g0, g1, P.stages, P.stages + P.pfw);
   // this pair's next tile (tiles pair, pair + 4, ... across the pieces), its
   // ring stage and that stage's phase parity, advanced without a division
   int inext = pair, snext = pair % P.stages;
