@@ -28,8 +28,8 @@
 //       O_z^T += Z_v^T P^T      (private values: the half's latent rows; only
 //                                the entries on a head's own rows are kept).
 // At the end of each (sequence, range) piece every pair writes its state
-// (m, l, O_s, O_z of its heads) as one partial; the combine kernel merges
-// the pairs' and the pieces' partials.  The first launch phase (lengths,
+// (m, l, O_s, O_z of its heads) as one partial; the merge kernel (decode.cu)
+// merges the pairs' and the pieces' partials.  The first launch phase (lengths,
 // first copies, absorb of p, set-up) runs code the SM has not fetched yet;
 // the last warp runs the tile code once on no tokens meanwhile, so that the
 // tiles find it in the instruction cache.
