@@ -415,8 +415,8 @@ __global__ void __launch_bounds__(kThreadsS, 1)
   // the first lengths are read before anything else (their latency is the
   // start of the chain to the first tile)
   const int len0 = tid < B ? P.seq_lens[tid] : 0;
-  // without the shared-memory B^K: this thread's B^K columns (one chunk) are
-  // loaded now, their latency hidden behind the set-up below
+  // without the shared-memory B^K: the first chunk of this thread's B^K
+  // columns is loaded now, its latency hidden behind the set-up below
   const BkRole bkr = bk_role(P, m0, tid);
   uint2 bkv[kBkChunk];
   if (P.bk_stages == 0) bk_load(P, m0, bkr, 0, bkv);
