@@ -4,7 +4,8 @@ Builds the library's sources with the host compiler's sanitizers (device code
 as PTX only: nothing is launched) and links them with `host_checks.cpp`,
 which exercises status strings, cache accounting, the launch planning behind
 every workspace-size query over a grid of shapes (LRKV_SM_COUNT stands in
-for a device) and the argument checks of every compute entry point.  Any
+for a device; the default plans and the planner's tuning branches) and the
+argument checks of every compute entry point.  Any
 sanitizer report or failed expectation fails the test.  Runs on the CPU machine.
 """
 import concurrent.futures as cf
@@ -52,11 +53,15 @@ def test_host_side_under_asan_and_ubsan(tmp_path):
     exe = str(tmp_path / "host_checks")
     res = subprocess.run([nvcc, *PTX_ONLY, *SAN, "-o", exe, drv_obj, *objs], capture_output=True, text=True)
     assert res.returncode == 0, res.stderr[-2000:]
-    env = dict(os.environ, LRKV_SM_COUNT="152",
-               ASAN_OPTIONS="detect_leaks=0:protect_shadow_gap=0:abort_on_error=0",
-               UBSAN_OPTIONS="print_stacktrace=1:halt_on_error=1")
-    run = subprocess.run([exe], capture_output=True, text=True, env=env, timeout=300)
-    report = run.stdout + run.stderr
-    assert run.returncode == 0, report[-4000:]
-    assert "runtime error" not in report and "AddressSanitizer" not in report, report[-4000:]
-    assert "host checks ok" in run.stdout
+    base = dict(os.environ, LRKV_SM_COUNT="152",
+                ASAN_OPTIONS="detect_leaks=0:protect_shadow_gap=0:abort_on_error=0",
+                UBSAN_OPTIONS="print_stacktrace=1:halt_on_error=1")
+    # the default plans, then the planner's tuning branches (the narrow merge,
+    # B^K in registers, an L2 window) and another SM count
+    for extra in ({}, {"LRKV_DECODE_WIDE_MERGE": "0", "LRKV_DECODE_BK_REGS": "1", "LRKV_DECODE_PREFETCH_TILES": "4"},
+                  {"LRKV_SM_COUNT": "148"}):
+        run = subprocess.run([exe], capture_output=True, text=True, env=dict(base, **extra), timeout=300)
+        report = run.stdout + run.stderr
+        assert run.returncode == 0, f"{extra}: " + report[-4000:]
+        assert "runtime error" not in report and "AddressSanitizer" not in report, f"{extra}: " + report[-4000:]
+        assert "host checks ok" in run.stdout, extra
